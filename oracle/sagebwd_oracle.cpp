@@ -1,0 +1,647 @@
+// SageBwd CPU oracle.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check
+// and the bench's CPU baseline call this; the product path never does.
+// It shares no code with the CUDA library.
+//
+// What it computes (sources):
+//  * "SageBwd: A Trainable Low-bit Attention", Abstract: a trainable INT8
+//    attention whose forward and backward quantize six of the seven attention
+//    matmuls; K-smoothing (subtracting the mean of K over tokens) is kept;
+//    the score gradient dS is the main error source.
+//  * "SageAttention3: Microscaling FP4 Attention for Inference and An
+//    Exploration of 8-Bit Training" (summary page), Approach and the
+//    "Measured effects" row "Keep dO V^T in FP16": the product dO.V^T is the
+//    one matmul left in 16/64-bit floating point.
+//  * FlashAttention / FlashAttention-2 (listed under "Builds on" of the SageBwd
+//    page): the forward keeps the log-sum-exp of each query row, and the
+//    backward uses D_i = rowsum(dO_i * O_i) and dS = P * (dP - D).
+//
+// The pages fix no block size, scale rule or rounding mode.  The readings
+// implemented here (one per function below) are:
+//  * every quantized operand of Q, K, V, dO is cut into blocks of 128 tokens
+//    (all d channels), one scale per block: a = max|x|, s = a/127,
+//    code = clamp(rint(x * (127/a)), -127, 127); a zero block gives code 0 and
+//    s = 0; the scale arithmetic is IEEE FP32;
+//  * K is smoothed by its FP32 channel mean over all N tokens (sum taken in
+//    FP64, divided by N in FP64, rounded once to FP32), K' = K - mean in FP32;
+//  * forward P~: per query row and 128-key tile, code = rint(127*2^(t - tmax))
+//    with tmax the row maximum inside the tile (so the tile's scale is
+//    2^(tmax - m)/127 relative to the running maximum m); the softmax
+//    denominator is summed from the unquantized P~;
+//  * backward P (for dV = P^T dO): per key and 128-query tile, scale
+//    max_i P / 127;  backward dS: one scale per 128 x 128 tile, max|dS|/127,
+//    one code matrix shared by dK = dS^T Q and dQ = dS K;
+//  * dP = dO V^T uses the BF16 inputs, accumulated here in FP64;
+//  * no correction term for the gradient through the K mean (each row of dS
+//    sums to zero, so the mean's gradient vanishes).
+//
+// Every floating-point quantity that decides an integer code is rounded to
+// FP32 exactly where the GPU path computes it in FP32 (Mode::F below); every
+// other sum and product is FP64.  With exact_codes = 1 the quantizers keep
+// their scales but skip rint and clamp and no FP32 rounding happens: the whole
+// pipeline must then reproduce exact FP64 attention, which is what pins its
+// structure (scales, masks, tile bookkeeping) in the tests.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+extern "C" {
+typedef struct {
+  int32_t B, Hq, Hkv, N, d;
+  int32_t causal;       // 1: key k is visible to query i iff k <= i (top-left aligned, N_q == N_k)
+  int32_t smooth_k;     // 1: subtract the per-channel mean of K before quantizing it
+  int32_t exact_codes;  // 1: quantizers keep their scales but neither round nor clamp; no FP32 rounding
+  int32_t threads;      // <= 0: OpenMP default
+  uint32_t exact_mask;  // error attribution: bit set = that quantizer keeps its scale but skips rint/clamp
+                        // (bit 0 Q, 1 K, 2 V, 3 dO, 4 P~ forward, 5 P^T backward, 6 dS); FP32 rounding stays
+  double softmax_scale;  // <= 0: 1/sqrt(d)
+} oracle_problem;
+}
+
+namespace {
+
+constexpr int BLK = 128;  // tokens per quantization block and per tile
+constexpr double kLog2e = 1.4426950408889634073599246810019;
+constexpr double kLn2 = 0.69314718055994530941723212145818;
+const double kInf = std::numeric_limits<double>::infinity();
+
+inline double bf16_to_double(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+// Which quantizer a code belongs to (bit index of exact_mask).
+enum Quantizer { QZ_Q = 0, QZ_K = 1, QZ_V = 2, QZ_DO = 3, QZ_PF = 4, QZ_PB = 5, QZ_DS = 6 };
+
+// Arithmetic of the quantized algorithm.  F() is an FP32 rounding point (the
+// GPU computes that value in FP32); Q() turns a scaled value into its integer
+// code: round to nearest, ties to even (C nearbyint in the default mode), then
+// clamp to [-127, 127].  Codes are stored as doubles: every integer product
+// sum here stays far below 2^53, so it is exact.
+struct Mode {
+  bool fp32;       // false only in the exact_codes pin mode
+  uint32_t exact;  // bit set: that quantizer does not round
+  double F(double x) const { return fp32 ? (double)(float)x : x; }
+  double Q(int which, double x) const {
+    if (exact & (1u << which)) return x;
+    const double r = std::nearbyint(x);
+    return std::min(127.0, std::max(-127.0, r));
+  }
+};
+inline Mode mode_of(const oracle_problem* p) {
+  return p->exact_codes ? Mode{false, 0x7Fu} : Mode{true, p->exact_mask};
+}
+
+inline int nblocks(int N) { return (N + BLK - 1) / BLK; }
+inline double scale_of(const oracle_problem* p) {
+  return p->softmax_scale > 0 ? p->softmax_scale : 1.0 / std::sqrt((double)p->d);
+}
+inline void set_threads(const oracle_problem* p) {
+#ifdef _OPENMP
+  if (p->threads > 0) omp_set_num_threads(p->threads);
+#else
+  (void)p;
+#endif
+}
+
+// One quantized tensor [BH][N][d]: codes, one scale per (bh, 128-token block), optional channel mean.
+struct QTensor {
+  int BH = 0, N = 0, d = 0;
+  std::vector<double> codes;
+  std::vector<double> scale;  // [BH][nblocks]
+  std::vector<double> mean;   // [BH][d] (K only)
+  double c(int bh, int n, int ch) const { return codes[((size_t)bh * N + n) * d + ch]; }
+  double s(int bh, int blk) const { return scale[(size_t)bh * nblocks(N) + blk]; }
+};
+
+// Per-block absmax quantizer (the build's reading: 128 tokens x d channels,
+// symmetric, scale a/127, round to nearest even, clamp to +-127).
+void quant_block(const Mode& M, int which, const double* x, int count, double* codes, double* scale) {
+  double a = 0;
+  for (int e = 0; e < count; ++e) a = std::max(a, std::fabs(x[e]));
+  if (a == 0) {
+    for (int e = 0; e < count; ++e) codes[e] = 0;
+    *scale = 0;
+    return;
+  }
+  const double inv = M.F(127.0 / a);
+  *scale = M.F(a / 127.0);
+  for (int e = 0; e < count; ++e) codes[e] = M.Q(which, M.F(x[e] * inv));
+}
+
+// Quantize a BF16 tensor [BH][N][d]; with smooth, first subtract the channel
+// mean over all N tokens ("SageBwd: A Trainable Low-bit Attention", Abstract:
+// K-smoothing).
+void quantize_tensor(const Mode& M, int which, const uint16_t* x, int BH, int N, int d, bool smooth, QTensor& out) {
+  out.BH = BH;
+  out.N = N;
+  out.d = d;
+  const int nb = nblocks(N);
+  out.codes.assign((size_t)BH * N * d, 0);
+  out.scale.assign((size_t)BH * nb, 0.0);
+  out.mean.assign(smooth ? (size_t)BH * d : 0, 0.0);
+#pragma omp parallel for schedule(dynamic)
+  for (int bh = 0; bh < BH; ++bh) {
+    const uint16_t* xb = x + (size_t)bh * N * d;
+    std::vector<double> mu(d, 0.0);
+    if (smooth) {
+      for (int ch = 0; ch < d; ++ch) {
+        double sum = 0;
+        for (int n = 0; n < N; ++n) sum += bf16_to_double(xb[(size_t)n * d + ch]);
+        mu[ch] = M.F(sum / (double)N);
+        out.mean[(size_t)bh * d + ch] = mu[ch];
+      }
+    }
+    std::vector<double> vals((size_t)BLK * d);
+    for (int blk = 0; blk < nb; ++blk) {
+      const int n0 = blk * BLK, rows = std::min(BLK, N - n0);
+      for (int r = 0; r < rows; ++r)
+        for (int ch = 0; ch < d; ++ch) {
+          const double v = bf16_to_double(xb[(size_t)(n0 + r) * d + ch]);
+          vals[(size_t)r * d + ch] = smooth ? M.F(v - mu[ch]) : v;
+        }
+      quant_block(M, which, vals.data(), rows * d, &out.codes[((size_t)bh * N + n0) * d], &out.scale[(size_t)bh * nb + blk]);
+    }
+  }
+}
+
+inline bool visible(const oracle_problem* p, int i, int k) { return k < p->N && (!p->causal || k <= i); }
+
+// Base-2 logits of one query row against one 128-key tile:
+// t_k = S_int * (sQ sK) * (scale log2 e) with S_int = Q^_i . K^_k, the row's
+// FP32 logit of S = Q K^T; -inf where the key is masked.  Returns the tile's
+// row maximum (-inf when every key of the tile is masked).
+double fwd_tile_logits(const Mode& M, const oracle_problem* p, const QTensor& qq, const QTensor& kq, int b, int h,
+                       int i, int jb, double c0, double* t /* indexed by key */) {
+  const int N = p->N, d = p->d, G = p->Hq / p->Hkv, hk = h / G;
+  const int bhq = b * p->Hq + h, bhk = b * p->Hkv + hk, ib = i / BLK;
+  const double qks = M.F(M.F(qq.s(bhq, ib) * kq.s(bhk, jb)) * c0);
+  double tmax = -kInf;
+  for (int k = jb * BLK; k < std::min(N, (jb + 1) * BLK); ++k) {
+    if (!visible(p, i, k)) {
+      t[k] = -kInf;
+      continue;
+    }
+    double s = 0;
+    for (int ch = 0; ch < d; ++ch) s += qq.c(bhq, i, ch) * kq.c(bhk, k, ch);
+    t[k] = M.F(s * qks);
+    tmax = std::max(tmax, t[k]);
+  }
+  return tmax;
+}
+
+// Code of P~ for one key: rint(127 * 2^(t - tmax)), tmax the row maximum of its tile.
+inline double fwd_p_code(const Mode& M, double t, double tmax) {
+  return M.Q(QZ_PF, M.F(127.0 * M.F(std::exp2(M.F(t - tmax)))));
+}
+
+// Forward of the quantized algorithm for query row i of head h, written as the
+// definition rather than as the online recurrence: the per-tile quantization
+// of P~ depends only on the tile's own row maximum, so the result equals what
+// an online-softmax kernel computes for any order of the key tiles.
+//   O_i = sum_j 2^(tmax_j - m)/127 * sV_j * sum_{k in j} code(P~)_k V^_k  /  l
+//   l   = sum_k 2^(t_k - m)   (unquantized P~),   m = max_j tmax_j
+//   LSE = (m + log2 l) ln 2
+void fwd_row(const Mode& M, const oracle_problem* p, const QTensor& qq, const QTensor& kq, const QTensor& vq, int b,
+             int h, int i, double c0, double* o_row, double* lse_out, std::vector<double>& t, std::vector<double>& acc) {
+  const int N = p->N, d = p->d, G = p->Hq / p->Hkv, hk = h / G, nb = nblocks(N);
+  const int bhk = b * p->Hkv + hk;
+  const int jb_end = p->causal ? i / BLK : nb - 1;
+  std::vector<double> tmax(jb_end + 1, -kInf);
+  for (int jb = 0; jb <= jb_end; ++jb) tmax[jb] = fwd_tile_logits(M, p, qq, kq, b, h, i, jb, c0, t.data());
+  double m = -kInf;
+  for (int jb = 0; jb <= jb_end; ++jb) m = std::max(m, tmax[jb]);
+  double l = 0;
+  for (int k = 0; k < std::min(N, (jb_end + 1) * BLK); ++k)
+    if (t[k] != -kInf) l += std::exp2(t[k] - m);
+  std::fill(acc.begin(), acc.end(), 0.0);
+  for (int jb = 0; jb <= jb_end; ++jb) {
+    if (tmax[jb] == -kInf) continue;
+    const double w = std::exp2(tmax[jb] - m) / 127.0 * vq.s(bhk, jb);
+    for (int ch = 0; ch < d; ++ch) {
+      double s = 0;
+      for (int k = jb * BLK; k < std::min(N, (jb + 1) * BLK); ++k) {
+        if (t[k] == -kInf) continue;
+        s += fwd_p_code(M, t[k], tmax[jb]) * vq.c(bhk, k, ch);
+      }
+      acc[ch] += w * s;
+    }
+  }
+  for (int ch = 0; ch < d; ++ch) o_row[ch] = acc[ch] / l;
+  *lse_out = (m + std::log2(l)) * kLn2;
+}
+
+void fwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o, double* lse,
+              const uint8_t* qsel) {
+  const Mode M = mode_of(p);
+  QTensor qq, kq, vq;
+  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq);
+  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq);
+  quantize_tensor(M, QZ_V, v, p->B * p->Hkv, p->N, p->d, false, vq);
+  const double c0 = M.F(scale_of(p) * kLog2e);
+  const int N = p->N, d = p->d, nb = nblocks(N);
+  const long rows = (long)p->B * p->Hq * N;
+#pragma omp parallel
+  {
+    std::vector<double> t(N), acc(d);
+#pragma omp for schedule(dynamic, 16)
+    for (long r = 0; r < rows; ++r) {
+      const int i = (int)(r % N);
+      const int bh = (int)(r / N);
+      if (qsel && !qsel[(size_t)bh * nb + i / BLK]) continue;
+      fwd_row(M, p, qq, kq, vq, bh / p->Hq, bh % p->Hq, i, c0, o + (size_t)r * d, lse + r, t, acc);
+    }
+  }
+}
+
+// One 128 x 128 backward tile (query block ib, key block jb, query head h):
+// everything that the three quantized backward products of the tile consume.
+struct BwdTile {
+  int i0 = 0, k0 = 0, ni = 0, nk = 0;
+  std::vector<double> pt;   // code(P^T)[k][i]
+  std::vector<double> spc;  // scale of row k of P^T
+  std::vector<double> ds;   // code(dS)[i][k]
+  double sds = 0;                       // scale of the dS tile
+};
+
+void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const QTensor& kq, const uint16_t* v,
+              const uint16_t* dO, const double* o, const double* lse, int b, int h, int ib, int jb, double c0,
+              double l2e, BwdTile& T) {
+  const int N = p->N, d = p->d, G = p->Hq / p->Hkv, hk = h / G;
+  const int bhq = b * p->Hq + h, bhk = b * p->Hkv + hk;
+  T.i0 = ib * BLK;
+  T.k0 = jb * BLK;
+  T.ni = std::min(BLK, N - T.i0);
+  T.nk = std::min(BLK, N - T.k0);
+  std::vector<double> P((size_t)BLK * BLK, 0.0), dS((size_t)BLK * BLK, 0.0);
+  const double qks = M.F(M.F(qq.s(bhq, ib) * kq.s(bhk, jb)) * c0);
+  for (int a = 0; a < T.ni; ++a) {
+    const int i = T.i0 + a;
+    const size_t qrow = ((size_t)bhq * N + i) * d;
+    double D = 0;  // D_i = rowsum(dO_i * O_i)
+    for (int ch = 0; ch < d; ++ch) D += bf16_to_double(dO[qrow + ch]) * o[qrow + ch];
+    const double L = M.F(M.F(lse[(size_t)bhq * N + i]) * l2e);  // LSE in base 2
+    for (int c = 0; c < T.nk; ++c) {
+      const int kk = T.k0 + c;
+      if (!visible(p, i, kk)) continue;
+      double s = 0;
+      for (int ch = 0; ch < d; ++ch) s += qq.c(bhq, i, ch) * kq.c(bhk, kk, ch);
+      const double tt = M.F(s * qks);
+      const double pp = M.F(std::exp2(M.F(tt - L)));  // normalized probability
+      // dP = dO V^T: the product kept in high precision (BF16 inputs, FP64 sum here).
+      double dp = 0;
+      const size_t vrow = ((size_t)bhk * N + kk) * d;
+      for (int ch = 0; ch < d; ++ch) dp += bf16_to_double(dO[qrow + ch]) * bf16_to_double(v[vrow + ch]);
+      P[(size_t)a * BLK + c] = pp;
+      dS[(size_t)a * BLK + c] = M.F(pp * (dp - D));
+    }
+  }
+  // P^T quantized per key row over the tile's queries.
+  T.pt.assign((size_t)BLK * BLK, 0);
+  T.spc.assign(BLK, 0.0);
+  for (int c = 0; c < T.nk; ++c) {
+    double cmax = 0;
+    for (int a = 0; a < T.ni; ++a) cmax = std::max(cmax, P[(size_t)a * BLK + c]);
+    if (cmax == 0) continue;
+    const double inv = M.F(127.0 / cmax);
+    T.spc[c] = M.F(cmax / 127.0);
+    for (int a = 0; a < T.ni; ++a) T.pt[(size_t)c * BLK + a] = M.Q(QZ_PB, M.F(P[(size_t)a * BLK + c] * inv));
+  }
+  // dS quantized with one scale for the whole tile.
+  T.ds.assign((size_t)BLK * BLK, 0);
+  double amax = 0;
+  for (int a = 0; a < T.ni; ++a)
+    for (int c = 0; c < T.nk; ++c) amax = std::max(amax, std::fabs(dS[(size_t)a * BLK + c]));
+  T.sds = 0;
+  if (amax > 0) {
+    const double inv = M.F(127.0 / amax);
+    T.sds = M.F(amax / 127.0);
+    for (int a = 0; a < T.ni; ++a)
+      for (int c = 0; c < T.nk; ++c) T.ds[(size_t)a * BLK + c] = M.Q(QZ_DS, M.F(dS[(size_t)a * BLK + c] * inv));
+  }
+}
+
+void bwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v, const double* o,
+              const uint16_t* dO, const double* lse, double* dq, double* dk, double* dv, const uint8_t* qsel,
+              const uint8_t* ksel) {
+  const Mode M = mode_of(p);
+  QTensor qq, kq, dq8;
+  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq);
+  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq);
+  quantize_tensor(M, QZ_DO, dO, p->B * p->Hq, p->N, p->d, false, dq8);
+  const double sc = scale_of(p);
+  const double c0 = M.F(sc * kLog2e);
+  const double l2e = M.F(kLog2e);
+  const int N = p->N, d = p->d, nb = nblocks(N), G = p->Hq / p->Hkv;
+  // dK, dV: one task per (b, kv head, key block), summed over the G query heads.
+  const long ktasks = (long)p->B * p->Hkv * nb;
+#pragma omp parallel
+  {
+    BwdTile T;
+    std::vector<double> accv((size_t)BLK * d), acck((size_t)BLK * d);
+#pragma omp for schedule(dynamic)
+    for (long task = 0; task < ktasks; ++task) {
+      if (ksel && !ksel[task]) continue;
+      const int jb = (int)(task % nb), bhk = (int)(task / nb), b = bhk / p->Hkv, hk = bhk % p->Hkv;
+      std::fill(accv.begin(), accv.end(), 0.0);
+      std::fill(acck.begin(), acck.end(), 0.0);
+      for (int h = hk * G; h < (hk + 1) * G; ++h) {
+        const int bhq = b * p->Hq + h;
+        for (int ib = p->causal ? jb : 0; ib < nb; ++ib) {
+          bwd_tile(M, p, qq, kq, v, dO, o, lse, b, h, ib, jb, c0, l2e, T);
+          for (int c = 0; c < T.nk; ++c)
+            for (int ch = 0; ch < d; ++ch) {
+              double sv = 0, sk = 0;
+              for (int a = 0; a < T.ni; ++a) {
+                sv += T.pt[(size_t)c * BLK + a] * dq8.c(bhq, T.i0 + a, ch);  // P^T dO
+                sk += T.ds[(size_t)a * BLK + c] * qq.c(bhq, T.i0 + a, ch);   // dS^T Q
+              }
+              accv[(size_t)c * d + ch] += T.spc[c] * dq8.s(bhq, ib) * sv;
+              acck[(size_t)c * d + ch] += sc * T.sds * qq.s(bhq, ib) * sk;
+            }
+        }
+      }
+      for (int c = 0; c < std::min(BLK, N - jb * BLK); ++c)
+        for (int ch = 0; ch < d; ++ch) {
+          const size_t idx = ((size_t)bhk * N + jb * BLK + c) * d + ch;
+          dv[idx] = accv[(size_t)c * d + ch];
+          dk[idx] = acck[(size_t)c * d + ch];
+        }
+    }
+  }
+  // dQ: one task per (b, query head, query block).
+  const long qtasks = (long)p->B * p->Hq * nb;
+#pragma omp parallel
+  {
+    BwdTile T;
+    std::vector<double> accq((size_t)BLK * d);
+#pragma omp for schedule(dynamic)
+    for (long task = 0; task < qtasks; ++task) {
+      if (qsel && !qsel[task]) continue;
+      const int ib = (int)(task % nb), bhq = (int)(task / nb), b = bhq / p->Hq, h = bhq % p->Hq;
+      const int bhk = b * p->Hkv + h / G;
+      std::fill(accq.begin(), accq.end(), 0.0);
+      for (int jb = 0; jb <= (p->causal ? ib : nb - 1); ++jb) {
+        bwd_tile(M, p, qq, kq, v, dO, o, lse, b, h, ib, jb, c0, l2e, T);
+        for (int a = 0; a < T.ni; ++a)
+          for (int ch = 0; ch < d; ++ch) {
+            double s = 0;
+            for (int c = 0; c < T.nk; ++c) s += T.ds[(size_t)a * BLK + c] * kq.c(bhk, T.k0 + c, ch);  // dS K
+            accq[(size_t)a * d + ch] += sc * T.sds * kq.s(bhk, jb) * s;
+          }
+      }
+      for (int a = 0; a < std::min(BLK, N - ib * BLK); ++a)
+        for (int ch = 0; ch < d; ++ch) dq[((size_t)bhq * N + ib * BLK + a) * d + ch] = accq[(size_t)a * d + ch];
+    }
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_check_problem(const oracle_problem* p) {
+  if (!p || p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->N < 1 || p->d < 1) return 1;
+  if (p->Hq % p->Hkv != 0) return 1;
+  return 0;
+}
+
+// Quantize one BF16 tensor [BH][N][d]: integer codes (int8), FP32 block scales
+// [BH][ceil(N/128)], and (smooth only) the FP32 channel means [BH][d].
+int oracle_quantize(const oracle_problem* p, const uint16_t* x, int BH, int smooth, int8_t* codes, float* scales,
+                    float* mean) {
+  if (oracle_check_problem(p)) return 1;
+  set_threads(p);
+  QTensor qt;
+  quantize_tensor(Mode{true, 0}, QZ_Q, x, BH, p->N, p->d, smooth != 0, qt);
+  for (size_t e = 0; e < qt.codes.size(); ++e) codes[e] = (int8_t)qt.codes[e];
+  for (size_t e = 0; e < qt.scale.size(); ++e) scales[e] = (float)qt.scale[e];
+  if (smooth && mean)
+    for (size_t e = 0; e < qt.mean.size(); ++e) mean[e] = (float)qt.mean[e];
+  return 0;
+}
+
+// Same, without rounding: codes are x/s as FP64 (exact_codes pipeline), for pins.
+int oracle_quantize_exact(const oracle_problem* p, const uint16_t* x, int BH, int smooth, double* codes,
+                          double* scales, double* mean) {
+  if (oracle_check_problem(p)) return 1;
+  set_threads(p);
+  QTensor qt;
+  quantize_tensor(Mode{false, 0x7Fu}, QZ_Q, x, BH, p->N, p->d, smooth != 0, qt);
+  std::copy(qt.codes.begin(), qt.codes.end(), codes);
+  std::copy(qt.scale.begin(), qt.scale.end(), scales);
+  if (smooth && mean) std::copy(qt.mean.begin(), qt.mean.end(), mean);
+  return 0;
+}
+
+// Quantized forward.  o: FP64 [B][Hq][N][d]; lse: FP64 [B][Hq][N] (natural log).
+// qsel (optional): [B*Hq][ceil(N/128)] flags; unselected query blocks are not written.
+int oracle_fwd(const oracle_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o,
+               double* lse, const uint8_t* qsel) {
+  if (oracle_check_problem(p)) return 1;
+  set_threads(p);
+  fwd_impl(p, q, k, v, o, lse, qsel);
+  return 0;
+}
+
+// Quantized backward.  o: the forward output as FP64 values (the caller passes
+// the forward's result, rounded to BF16 when it mirrors the library's call);
+// lse: the forward's LSE.  qsel selects the dQ query blocks [B*Hq][nb], ksel
+// the dK/dV key blocks [B*Hkv][nb]; NULL selects all.
+int oracle_bwd(const oracle_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v, const double* o,
+               const uint16_t* dO, const double* lse, double* dq, double* dk, double* dv, const uint8_t* qsel,
+               const uint8_t* ksel) {
+  if (oracle_check_problem(p)) return 1;
+  set_threads(p);
+  bwd_impl(p, q, k, v, o, dO, lse, dq, dk, dv, qsel, ksel);
+  return 0;
+}
+
+// Exact FP64 softmax attention (the full-precision reference for the cosine
+// similarity criteria): S = scale * Q K^T, P = softmax(S), O = P V.
+int oracle_exact_fwd(const oracle_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o,
+                     double* lse, const uint8_t* qsel) {
+  if (oracle_check_problem(p)) return 1;
+  set_threads(p);
+  const int N = p->N, d = p->d, G = p->Hq / p->Hkv, nb = nblocks(N);
+  const double sc = scale_of(p);
+  const long rows = (long)p->B * p->Hq * N;
+#pragma omp parallel
+  {
+    std::vector<double> s(N);
+#pragma omp for schedule(dynamic, 16)
+    for (long r = 0; r < rows; ++r) {
+      const int i = (int)(r % N), bhq = (int)(r / N), b = bhq / p->Hq, h = bhq % p->Hq;
+      if (qsel && !qsel[(size_t)bhq * nb + i / BLK]) continue;
+      const int bhk = b * p->Hkv + h / G;
+      double m = -kInf;
+      for (int kk = 0; kk < N; ++kk) {
+        if (!visible(p, i, kk)) continue;
+        double acc = 0;
+        for (int ch = 0; ch < d; ++ch)
+          acc += bf16_to_double(q[(size_t)r * d + ch]) * bf16_to_double(k[((size_t)bhk * N + kk) * d + ch]);
+        s[kk] = sc * acc;
+        m = std::max(m, s[kk]);
+      }
+      double l = 0;
+      for (int kk = 0; kk < N; ++kk) {
+        s[kk] = visible(p, i, kk) ? std::exp(s[kk] - m) : 0.0;  // unnormalized probability
+        l += s[kk];
+      }
+      for (int ch = 0; ch < d; ++ch) {
+        double acc = 0;
+        for (int kk = 0; kk < N; ++kk) acc += s[kk] * bf16_to_double(v[((size_t)bhk * N + kk) * d + ch]);
+        o[(size_t)r * d + ch] = acc / l;
+      }
+      lse[r] = m + std::log(l);
+    }
+  }
+  return 0;
+}
+
+// Exact FP64 attention backward given the exact forward's O and LSE:
+// P = exp(S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
+// dS = P * (dP - D), dQ = scale * dS K, dK = scale * dS^T Q (GQA: summed over
+// the query heads that share a kv head).
+int oracle_exact_bwd(const oracle_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const double* o, const uint16_t* dO, const double* lse, double* dq, double* dk, double* dv,
+                     const uint8_t* qsel, const uint8_t* ksel) {
+  if (oracle_check_problem(p)) return 1;
+  set_threads(p);
+  const int N = p->N, d = p->d, G = p->Hq / p->Hkv, nb = nblocks(N);
+  const double sc = scale_of(p);
+  // D_i = rowsum(dO_i * O_i) for every query row.
+  std::vector<double> Dv((size_t)p->B * p->Hq * N);
+#pragma omp parallel for schedule(static)
+  for (long r = 0; r < (long)Dv.size(); ++r) {
+    double D = 0;
+    for (int ch = 0; ch < d; ++ch) D += bf16_to_double(dO[(size_t)r * d + ch]) * o[(size_t)r * d + ch];
+    Dv[r] = D;
+  }
+  auto Dval = [&](int bhq, int i) { return Dv[(size_t)bhq * N + i]; };
+  auto P_dS = [&](int bhq, int bhk, int i, int kk, double D, double* Pout) {
+    double s = 0, dp = 0;
+    for (int ch = 0; ch < d; ++ch) {
+      s += bf16_to_double(q[((size_t)bhq * N + i) * d + ch]) * bf16_to_double(k[((size_t)bhk * N + kk) * d + ch]);
+      dp += bf16_to_double(dO[((size_t)bhq * N + i) * d + ch]) * bf16_to_double(v[((size_t)bhk * N + kk) * d + ch]);
+    }
+    const double P = std::exp(sc * s - lse[(size_t)bhq * N + i]);
+    *Pout = P;
+    return P * (dp - D);
+  };
+  const long krows = (long)p->B * p->Hkv * N;
+#pragma omp parallel
+  {
+    std::vector<double> av(d), ak(d);
+#pragma omp for schedule(dynamic, 16)
+    for (long r = 0; r < krows; ++r) {
+      const int kk = (int)(r % N), bhk = (int)(r / N), b = bhk / p->Hkv, hk = bhk % p->Hkv;
+      if (ksel && !ksel[(size_t)bhk * nb + kk / BLK]) continue;
+      std::fill(av.begin(), av.end(), 0.0);
+      std::fill(ak.begin(), ak.end(), 0.0);
+      for (int h = hk * G; h < (hk + 1) * G; ++h) {
+        const int bhq = b * p->Hq + h;
+        for (int i = 0; i < N; ++i) {
+          if (!visible(p, i, kk)) continue;
+          double P;
+          const double dS = P_dS(bhq, bhk, i, kk, Dval(bhq, i), &P);
+          for (int ch = 0; ch < d; ++ch) {
+            av[ch] += P * bf16_to_double(dO[((size_t)bhq * N + i) * d + ch]);
+            ak[ch] += sc * dS * bf16_to_double(q[((size_t)bhq * N + i) * d + ch]);
+          }
+        }
+      }
+      for (int ch = 0; ch < d; ++ch) {
+        dv[(size_t)r * d + ch] = av[ch];
+        dk[(size_t)r * d + ch] = ak[ch];
+      }
+    }
+  }
+  const long qrows = (long)p->B * p->Hq * N;
+#pragma omp parallel
+  {
+    std::vector<double> aq(d);
+#pragma omp for schedule(dynamic, 16)
+    for (long r = 0; r < qrows; ++r) {
+      const int i = (int)(r % N), bhq = (int)(r / N), b = bhq / p->Hq, h = bhq % p->Hq;
+      if (qsel && !qsel[(size_t)bhq * nb + i / BLK]) continue;
+      const int bhk = b * p->Hkv + h / G;
+      const double D = Dval(bhq, i);
+      std::fill(aq.begin(), aq.end(), 0.0);
+      for (int kk = 0; kk < N; ++kk) {
+        if (!visible(p, i, kk)) continue;
+        double P;
+        const double dS = P_dS(bhq, bhk, i, kk, D, &P);
+        for (int ch = 0; ch < d; ++ch) aq[ch] += sc * dS * bf16_to_double(k[((size_t)bhk * N + kk) * d + ch]);
+      }
+      for (int ch = 0; ch < d; ++ch) dq[(size_t)r * d + ch] = aq[ch];
+    }
+  }
+  return 0;
+}
+
+// Codes of P~ of one forward tile (query block ib, key block jb, head h):
+// codes [128][128] (row = query ib*128+a, col = key jb*128+c; 0 where masked
+// or outside N) and the tile's row maxima tmax [128] (base-2 logits; -inf
+// where the row sees no key or lies outside N).
+int oracle_fwd_tile(const oracle_problem* p, const uint16_t* q, const uint16_t* k, int b, int h, int ib, int jb,
+                    int32_t* codes, double* tmax) {
+  if (oracle_check_problem(p) || p->exact_codes) return 1;
+  set_threads(p);
+  const Mode M = mode_of(p);
+  QTensor qq, kq;
+  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq);
+  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq);
+  const double c0 = M.F(scale_of(p) * kLog2e);
+  std::vector<double> t(p->N);
+  for (int a = 0; a < BLK; ++a) {
+    const int i = ib * BLK + a;
+    tmax[a] = -kInf;
+    for (int c = 0; c < BLK; ++c) codes[a * BLK + c] = 0;
+    if (i >= p->N) continue;
+    tmax[a] = fwd_tile_logits(M, p, qq, kq, b, h, i, jb, c0, t.data());
+    for (int c = 0; c < BLK; ++c) {
+      const int kk = jb * BLK + c;
+      if (kk < p->N && t[kk] != -kInf) codes[a * BLK + c] = (int32_t)fwd_p_code(M, t[kk], tmax[a]);
+    }
+  }
+  return 0;
+}
+
+// Everything the quantized backward of one tile consumes: pt [128][128] codes
+// of P^T (row = key), spc [128] their per-key scales, ds [128][128] codes of dS
+// (row = query), *sds the tile's dS scale.  o, lse: the forward's outputs.
+int oracle_bwd_tile(const oracle_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v, const double* o,
+                    const uint16_t* dO, const double* lse, int b, int h, int ib, int jb, int32_t* pt, double* spc,
+                    int32_t* ds, double* sds) {
+  if (oracle_check_problem(p) || p->exact_codes) return 1;
+  set_threads(p);
+  const Mode M = mode_of(p);
+  QTensor qq, kq;
+  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq);
+  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq);
+  BwdTile T;
+  bwd_tile(M, p, qq, kq, v, dO, o, lse, b, h, ib, jb, M.F(scale_of(p) * kLog2e), M.F(kLog2e), T);
+  for (size_t e = 0; e < T.pt.size(); ++e) pt[e] = (int32_t)T.pt[e];
+  std::copy(T.spc.begin(), T.spc.end(), spc);
+  for (size_t e = 0; e < T.ds.size(); ++e) ds[e] = (int32_t)T.ds[e];
+  *sds = T.sds;
+  return 0;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+}  // extern "C"

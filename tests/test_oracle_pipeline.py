@@ -1,0 +1,175 @@
+"""Pins of the oracle's quantized SageBwd forward and backward (CPU only).
+
+* With every quantizer kept at its scale but not rounded (exact_codes), the
+  pipeline must reproduce exact FP64 attention: this pins the scales, masks,
+  GQA mapping, ragged tiles and the no-correction reading of the K-mean
+  gradient.
+* Q = 0 gives uniform attention, a closed form also under quantization.
+* Tile code properties (every quantized row/tile reaches 127).
+* GQA equals MHA with repeated K/V heads.
+* Accuracy against exact attention on the synthetic workloads, the direction
+  of the K-smoothing ablation ("SageAttention3 ... 8-Bit Training" summary,
+  Measured effects: K smoothing helps), and dS as the dominant error source
+  ("SageBwd: A Trainable Low-bit Attention", Abstract, finding (ii)).
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_trainable_attention_gb300 import workloads as W
+
+
+def cos(a, b):
+    a = np.nan_to_num(np.asarray(a, np.float64)).ravel()
+    b = np.nan_to_num(np.asarray(b, np.float64)).ravel()
+    return float(a @ b / np.linalg.norm(a) / np.linalg.norm(b))
+
+
+PIN_CASES = [
+    W.small("gqa_causal_ragged", 1, 4, 2, 300, 32, True, 21, k_offset_sd=2.0),
+    W.small("gqa_noncausal_ragged", 2, 2, 1, 129, 64, False, 22, qk_norm=True, k_offset_sd=3.0),
+    W.small("mha_one_tile", 1, 2, 2, 100, 16, True, 23),
+]
+
+
+@pytest.mark.parametrize("smooth", [True, False])
+@pytest.mark.parametrize("w", PIN_CASES, ids=lambda w: w.name)
+def test_unrounded_pipeline_is_exact_attention(oracle_mod, w, smooth):
+    x = W.make_inputs(w)
+    pe = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_k=smooth, exact_codes=True)
+    r = oracle_mod.pipeline(pe, x["q"], x["k"], x["v"], x["do"])
+    ref = oracle_mod.pipeline(pe, x["q"], x["k"], x["v"], x["do"], exact=True)
+    for key in ("o", "dq", "dk", "dv"):
+        np.testing.assert_allclose(r[key], ref[key], rtol=0, atol=1e-10 * np.abs(ref[key]).max(), err_msg=key)
+    # K-smoothing shifts the log-sum-exp of row i by -scale * Q_i . mean(K): the
+    # library's LSE is that of the smoothed scores.
+    lse_ref = ref["lse"]
+    if smooth:
+        qd = x["q"].double().numpy()
+        kd = x["k"].double().numpy()
+        mu = kd.mean(axis=2).repeat(w.G, axis=1)  # [B, Hq, d]
+        lse_ref = lse_ref - (qd * mu[:, :, None, :]).sum(-1) / np.sqrt(w.d)
+    np.testing.assert_allclose(r["lse"], lse_ref, rtol=0, atol=1e-10 * max(1, np.abs(lse_ref).max()))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_query_closed_form(oracle_mod, causal):
+    """Q = 0: every visible key gets the same probability, so O_i is the mean of
+    the dequantized V rows it sees, and (non-causal) dV_k = mean_i deq(dO_i)."""
+    w = W.small("zq", 1, 2, 1, 260, 32, causal, 31)
+    x = W.make_inputs(w)
+    x["q"] = torch.zeros_like(x["q"])
+    p = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+    r = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"])
+    vc, vs, _ = oracle_mod.quantize(p, x["v"], w.B * w.Hkv, False)
+    vdeq = vc.astype(np.float64) * np.repeat(vs.astype(np.float64), 128, axis=1)[:, :w.N, None]
+    if causal:
+        ref = np.cumsum(vdeq[0], axis=0) / np.arange(1, w.N + 1)[:, None]
+    else:
+        ref = np.broadcast_to(vdeq[0].mean(axis=0), (w.N, w.d))
+    for h in range(w.Hq):
+        np.testing.assert_allclose(r["o"][0, h], ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+    if not causal:
+        dc, dsc, _ = oracle_mod.quantize(p, x["do"], w.B * w.Hq, False)
+        ddeq = dc.astype(np.float64) * np.repeat(dsc.astype(np.float64), 128, axis=1)[:, :w.N, None]
+        ref_dv = ddeq.mean(axis=1).sum(axis=0)  # summed over the 2 query heads of the kv head
+        for k in (0, 100, 259):
+            np.testing.assert_allclose(r["dv"][0, 0, k], ref_dv, rtol=2e-6, atol=1e-6 * np.abs(ref_dv).max())
+
+
+def test_tile_code_properties(oracle_mod):
+    w = W.small("tiles", 1, 2, 1, 300, 32, True, 41, qk_norm=True, k_offset_sd=2.0)
+    x = W.make_inputs(w)
+    p = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+    r = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"])
+    o_in = oracle_mod.bf16_round(r["o"])
+    for (ib, jb) in [(0, 0), (1, 0), (2, 2), (2, 1)]:
+        codes, tmax = oracle_mod.fwd_tile(p, x["q"], x["k"], 0, 1, ib, jb)
+        rows = min(128, w.N - ib * 128)
+        assert codes.min() >= 0 and codes.max() <= 127
+        for a in range(rows):
+            i = ib * 128 + a
+            visible = [k for k in range(jb * 128, min(w.N, jb * 128 + 128)) if k <= i]
+            if visible:
+                assert codes[a].max() == 127 and np.isfinite(tmax[a])
+                masked = [c for c in range(128) if jb * 128 + c > i or jb * 128 + c >= w.N]
+                assert np.all(codes[a, masked] == 0)
+            else:
+                assert np.all(codes[a] == 0) and tmax[a] == -np.inf
+        pt, spc, ds, sds = oracle_mod.bwd_tile(p, x["q"], x["k"], x["v"], o_in, x["do"], r["lse"], 0, 1, ib, jb)
+        assert pt.min() >= 0 and pt.max() <= 127 and np.abs(ds).max() <= 127
+        for c in range(min(128, w.N - jb * 128)):
+            if spc[c] > 0:
+                assert pt[c].max() == 127
+        assert sds > 0 and np.abs(ds).max() == 127
+
+
+def test_gqa_equals_repeated_heads(oracle_mod):
+    """Query head h reads kv head h // G: GQA gives the MHA result on K/V
+    repeated per query head, and dK/dV are the sums over each group."""
+    w = W.small("gqa", 1, 6, 2, 200, 16, True, 51, k_offset_sd=2.0)
+    x = W.make_inputs(w)
+    p = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+    g = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"])
+    xm = dict(x)
+    xm["k"] = x["k"].repeat_interleave(w.G, dim=1).contiguous()
+    xm["v"] = x["v"].repeat_interleave(w.G, dim=1).contiguous()
+    pm = oracle_mod.problem(w.B, w.Hq, w.Hq, w.N, w.d, w.causal)
+    m = oracle_mod.pipeline(pm, xm["q"], xm["k"], xm["v"], xm["do"])
+    np.testing.assert_array_equal(g["o"], m["o"])
+    np.testing.assert_array_equal(g["dq"], m["dq"])
+    for key in ("dk", "dv"):
+        summed = m[key].reshape(w.B, w.Hkv, w.G, w.N, w.d).sum(axis=2)
+        np.testing.assert_allclose(g[key], summed, rtol=0, atol=1e-12 * np.abs(summed).max())
+
+
+ACC_CASES = [
+    W.WORKLOADS["tiny"],
+    W.WORKLOADS["pretrain"].with_(B=1, Hq=2, Hkv=2, N=384),
+    W.WORKLOADS["llama1b"].with_(Hq=8, Hkv=2, N=384),
+    W.WORKLOADS["videodit"].with_(B=1, Hq=2, Hkv=2, N=300),
+]
+
+
+@pytest.mark.parametrize("w", ACC_CASES, ids=lambda w: w.name)
+def test_accuracy_against_exact_attention(oracle_mod, w):
+    """Cosine similarity to exact attention: >= 0.995 for O, >= 0.99 for the gradients."""
+    x = W.make_inputs(w)
+    p = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+    r = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"])
+    ref = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"], exact=True)
+    assert cos(r["o"], ref["o"]) >= 0.995
+    for key in ("dq", "dk", "dv"):
+        assert cos(r[key], ref[key]) >= 0.99, key
+
+
+def test_k_smoothing_helps(oracle_mod):
+    w = W.WORKLOADS["videodit"].with_(B=1, Hq=2, Hkv=2, N=300)
+    x = W.make_inputs(w)
+    out = {}
+    for smooth in (True, False):
+        p = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_k=smooth)
+        out[smooth] = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"])
+    ref = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"], exact=True)
+    assert cos(out[True]["dq"], ref["dq"]) > cos(out[False]["dq"], ref["dq"])
+    assert cos(out[True]["o"], ref["o"]) > cos(out[False]["o"], ref["o"])
+
+
+def test_ds_is_the_dominant_error(oracle_mod):
+    """Leaving only dS unrounded removes most of the dQ/dK error; leaving any
+    other single quantizer unrounded removes little of it."""
+    w = W.WORKLOADS["llama1b"].with_(Hq=8, Hkv=2, N=384)
+    x = W.make_inputs(w)
+    p0 = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+    ref = oracle_mod.pipeline(p0, x["q"], x["k"], x["v"], x["do"], exact=True)
+    base = oracle_mod.pipeline(p0, x["q"], x["k"], x["v"], x["do"])
+    err = {k: 1 - cos(base[k], ref[k]) for k in ("dq", "dk")}
+    for bit in range(7):
+        p = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, exact_mask=1 << bit)
+        r = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"])
+        for k in ("dq", "dk"):
+            e = 1 - cos(r[k], ref[k])
+            if bit == 6:  # dS
+                assert e < 0.3 * err[k], (bit, k)
+            else:
+                assert e > 0.6 * err[k], (bit, k)
