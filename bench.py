@@ -1,0 +1,363 @@
+"""Benchmark of the SageBwd hot path: INT8 attention forward + backward.
+
+One step = the whole path on one batch of synthetic input already resident
+in HBM: K mean + Q/K/V quantization, the fused forward, the backward
+preprocess (D, dO quantization), the fused backward and the dQ conversion.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints ONE JSON line.  Throughput is TOPS with the FlashAttention FLOP
+convention (forward 4 B Hq N^2 d, backward 2.5x forward, causal halves both).
+Under torchrun (N > 1) every rank runs its own batch (independent problems,
+weak scaling, no collective on the data path); rank 0 prints the line with
+the maximum time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import bit_trainable_attention_gb300 as sb  # noqa: E402
+from bit_trainable_attention_gb300 import workloads as W  # noqa: E402
+
+METRIC = "SageBwd fwd+bwd TOPS at seq 8K/16K (1 GB300); % of INT8 tensor peak; cos-sim"
+L2_FLUSH_BYTES = 256 << 20
+# tcgen05 kind::f16 is the instruction the six INT8-semantics products run on (integer-valued BF16
+# operands); legacy mma.sync s8 and torch._int_mm measured on this GPU for the "% of INT8 peak" line.
+INT8_MMA_SYNC_TOPS = 150.5
+INT8_TORCH_INT_MM_TOPS = 78.3
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_burst": float(d["bf16_tflops"]), "bf16_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- the library arm
+class Step:
+    """Buffers and the stage-by-stage calls of one forward + backward step."""
+
+    def __init__(self, w: W.Workload, dev):
+        self.w = w
+        x = W.make_inputs(w)
+        self.host = x
+        self.x = {k: v.to(dev) for k, v in x.items()}
+        self.prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+        p = self.prob
+        self.o = torch.empty_like(self.x["q"])
+        self.lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+        self.saved = sb.empty_bytes(sb.sagebwd_saved_bytes(p), dev)
+        self.ws0 = sb.empty_bytes(sb.sagebwd_workspace_bytes(p, 0), dev)
+        self.ws1 = sb.empty_bytes(sb.sagebwd_workspace_bytes(p, 1), dev)
+        self.dq = torch.empty_like(self.x["q"])
+        self.dk = torch.empty_like(self.x["k"])
+        self.dv = torch.empty_like(self.x["v"])
+
+    def run(self, ev=None):
+        """The five stages; ev (optional) = 6 events recorded between them."""
+        p, x = self.prob, self.x
+        s = torch.cuda.current_stream()
+        rec = (lambda i: ev[i].record(s)) if ev is not None else (lambda i: None)
+        rec(0)
+        sb.sagebwd_fwd_quantize(p, x["q"], x["k"], x["v"], self.saved, self.ws0, s)
+        rec(1)
+        sb.sagebwd_fwd_attention(p, self.saved, self.o, self.lse, self.ws0, s)
+        rec(2)
+        sb.sagebwd_bwd_prepare(p, self.o, x["do"], self.ws1, s)
+        rec(3)
+        sb.sagebwd_bwd_attention(p, x["v"], x["do"], self.lse, self.saved, self.dk, self.dv, self.ws1, s)
+        rec(4)
+        sb.sagebwd_bwd_finish(p, self.dq, self.ws1, s)
+        rec(5)
+
+    # kernels of ours per step: [K mean partial + final] + quantize + fwd + prep + bwd + dq convert
+    def launches(self):
+        return (2 if self.prob.smooth_k else 0) + 5
+
+
+def cossim_vs_torch(step: Step):
+    """Cosine similarity of O, dQ, dK, dV against PyTorch FP32 attention (not timed)."""
+    w, x = step.w, step.x
+    q = x["q"].float().requires_grad_(True)
+    k = x["k"].float().requires_grad_(True)
+    v = x["v"].float().requires_grad_(True)
+    kk = k.repeat_interleave(w.G, dim=1)
+    vv = v.repeat_interleave(w.G, dim=1)
+    o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=w.causal)
+    o.backward(x["do"].float())
+    out = {}
+    for name, a, b in (("o", step.o, o), ("dq", step.dq, q.grad), ("dk", step.dk, k.grad), ("dv", step.dv, v.grad)):
+        out[name] = round(float(torch.nn.functional.cosine_similarity(a.float().reshape(-1), b.reshape(-1), dim=0)), 6)
+    return out
+
+
+def time_device(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_barrier):
+    for _ in range(warmup):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    dist_barrier()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()  # L2 flush between timed steps, outside the events
+        step.run(evs[i])
+    torch.cuda.synchronize()
+    dist_barrier()
+    stage = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)] for j in range(5)]
+    total = [evs[i][0].elapsed_time(evs[i][5]) for i in range(steps)]
+    return total, stage
+
+
+def time_e2e(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_barrier):
+    """Public API (sagebwd_fwd + sagebwd_bwd) with pinned host inputs and outputs: H2D of Q, K, V, dO and
+    D2H of O, dQ, dK, dV inside the timed region."""
+    p, x = step.prob, step.x
+    hin = {k: v.pin_memory() for k, v in step.host.items()}
+    hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+            for k, v in (("o", step.o), ("dq", step.dq), ("dk", step.dk), ("dv", step.dv))}
+    s = torch.cuda.current_stream()
+
+    def one():
+        for k in ("q", "k", "v", "do"):
+            x[k].copy_(hin[k], non_blocking=True)
+        sb.sagebwd_fwd(p, x["q"], x["k"], x["v"], step.o, step.lse, step.saved, step.ws0, s)
+        sb.sagebwd_bwd(p, x["q"], x["k"], x["v"], step.o, x["do"], step.lse, step.saved, step.dq, step.dk, step.dv,
+                       step.ws1, s)
+        for k, t in (("o", step.o), ("dq", step.dq), ("dk", step.dk), ("dv", step.dv)):
+            hout[k].copy_(t, non_blocking=True)
+
+    for _ in range(warmup):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    dist_barrier()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(s)
+        one()
+        ev[i][1].record(s)
+    torch.cuda.synchronize()
+    dist_barrier()
+    ms = [e[0].elapsed_time(e[1]) for e in ev]
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------------------- the oracle (CPU) arm
+def oracle_sample_run(w: W.Workload, n_tokens: int):
+    """Time the oracle on the first n_tokens tokens of the workload's own inputs (all heads, full
+    forward + backward of that prefix).  Returns (seconds, algorithmic ops of the sample)."""
+    import oracle  # the CPU baseline leg is the one place bench.py runs the oracle
+    x = W.make_inputs(w)
+    sub = {k: v[:, :, :n_tokens].contiguous() for k, v in x.items()}
+    ws = w.with_(N=n_tokens)
+    op = oracle.problem(ws.B, ws.Hq, ws.Hkv, ws.N, ws.d, ws.causal)
+    t0 = time.perf_counter()
+    oracle.pipeline(op, sub["q"], sub["k"], sub["v"], sub["do"])
+    dt = time.perf_counter() - t0
+    return dt, ws.flops_fwd() + ws.flops_bwd(), oracle.max_threads()
+
+
+def pick_sample_tokens(w: W.Workload, budget_s: float):
+    """Largest multiple of 128 tokens whose oracle run should take about budget_s seconds (quadratic cost)."""
+    n = min(256, w.N)
+    dt, _, _ = oracle_sample_run(w, n)
+    target = int(n * (budget_s / max(dt, 1e-3)) ** 0.5)
+    return max(128, min(w.N, target // 128 * 128))
+
+
+def cpu_baseline(w: W.Workload, budget_s: float):
+    n = pick_sample_tokens(w, budget_s)
+    dt, ops, cores = oracle_sample_run(w, n)
+    return {"value": round(ops / dt / 1e12, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {w.N} tokens of the same inputs, all {w.B}x{w.Hq} heads, full forward + "
+                      f"backward of that prefix ({ops:.3e} ops in {dt:.2f} s)"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    n = pick_sample_tokens(w, args.reference_step_s)
+    for _ in range(args.warmup):
+        oracle_sample_run(w, n)
+    times, ops, cores = [], 0.0, 1
+    for _ in range(args.steps):
+        dt, ops, cores = oracle_sample_run(w, n)
+        times.append(dt)
+    mean = sum(times) / len(times)
+    value = ops / mean / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (codes decided in f32)", "data": "synthetic",
+        "config": {"workload": describe(w), "sample": f"first {n} tokens"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of {w.N} tokens of the same inputs, all heads, full forward + backward"},
+        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def describe(w: W.Workload) -> str:
+    return (f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.N} d={w.d} {'causal' if w.causal else 'non-causal'}")
+
+
+# ---------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen15b", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="library", choices=["library", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="oracle CPU-baseline sample size (seconds)")
+    ap.add_argument("--reference-step-s", type=float, default=8.0, help="oracle seconds per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = W.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # the CPU baseline first (before any GPU work), rank 0 at N = 1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_budget_s)
+
+    sb.load_library()
+    step = Step(w, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sampler = ClockSampler(local)
+    total, stage = time_device(step, args.steps, args.warmup, flush, barrier)
+    clocks = sampler.stop()
+    e2e_ms, h2d, d2h = time_e2e(step, max(3, args.steps // 5), max(3, args.warmup), flush, barrier)
+    code0, _ = sb.sagebwd_check_status(step.ws0)
+    code1, _ = sb.sagebwd_check_status(step.ws1)
+
+    ms = sum(total) / len(total)
+    e2e = sum(e2e_ms) / len(e2e_ms)
+    if dist is not None:
+        t = torch.tensor([ms, e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e = float(t[0]), float(t[1])
+    ops = w.flops_fwd() + w.flops_bwd()
+    value = world * ops / (ms * 1e-3) / 1e12
+    stage_ms = [sum(s) / len(s) for s in stage]
+    peaks = load_peaks()
+    bwd_ms = stage_ms[3]
+    achieved = w.flops_bwd() / (bwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 (integer-valued bf16 on tcgen05, fp32 accumulate) + bf16 dP",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "l2": "flushed between timed steps (256 MB write)",
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+        "breakdown_ms": {"quantize": round(stage_ms[0], 4), "fwd": round(stage_ms[1], 4),
+                         "bwd_prepare": round(stage_ms[2], 4), "bwd": round(stage_ms[3], 4),
+                         "dq_convert": round(stage_ms[4], 4)},
+        "tops": {"fwd_incl_quantize": round(w.flops_fwd() / ((stage_ms[0] + stage_ms[1]) * 1e-3) / 1e12, 2),
+                 "bwd_incl_prepare": round(w.flops_bwd() / (sum(stage_ms[2:]) * 1e-3) / 1e12, 2)},
+        "roofline": {"kernel": "sagebwd bwd_kernel", "bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_sustained"], 4), "traffic": None,
+                     "peak_kind": f"bf16 dense, sustained ({peaks['source']})"},
+        "int8_peak_frac": {"vs_mma_sync_s8": round(value / world / INT8_MMA_SYNC_TOPS, 3),
+                           "vs_torch_int_mm": round(value / world / INT8_TORCH_INT_MM_TOPS, 3),
+                           "vs_bf16_dense_burst": round(value / world / peaks["bf16_burst"], 4)},
+        "e2e": {"value": round(world * ops / (e2e * 1e-3) / 1e12, 3), "unit": "TOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},
+        "gpu_launches": step.launches() * args.steps,
+        "clocks": clocks,
+        "status": [code0, code1],
+    }
+    if rank == 0:
+        line["cossim_vs_torch_fp32"] = cossim_vs_torch(step)
+        line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

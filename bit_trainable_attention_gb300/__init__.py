@@ -1,0 +1,266 @@
+"""SageBwd trainable INT8 attention for GB300 (sm_103a).
+
+Python binding of the C ABI declared in ``include/sagebwd.h``: every function
+named ``sagebwd_*`` here marshals torch tensors (device memory and the current
+stream) into the C call of the same name; all computation happens in the
+library's CUDA kernels.  ``SageBwdAttention`` / ``attention`` wrap the forward
+and backward calls as a ``torch.autograd.Function``.
+
+There is no fallback: if ``libsagebwd.so`` cannot be built or loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "Problem", "SageBwdError", "load_library", "sagebwd_saved_bytes", "sagebwd_workspace_bytes",
+    "sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd", "sagebwd_fwd_quantize", "sagebwd_fwd_attention",
+    "sagebwd_bwd_prepare", "sagebwd_bwd_attention", "sagebwd_bwd_finish", "sagebwd_check_status",
+    "sagebwd_status_string", "sagebwd_version", "attention", "SageBwdAttention",
+    "SAGEBWD_Q", "SAGEBWD_K", "SAGEBWD_V", "SAGEBWD_DO", "FLAG_DROP_ONE_LOAD",
+]
+
+SAGEBWD_Q, SAGEBWD_K, SAGEBWD_V, SAGEBWD_DO = 0, 1, 2, 3
+FLAG_DROP_ONE_LOAD = 0x1
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA", 5: "TIMEOUT"}
+
+EXPORTED_SYMBOLS = (
+    "sagebwd_saved_bytes", "sagebwd_workspace_bytes", "sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd",
+    "sagebwd_fwd_quantize", "sagebwd_fwd_attention", "sagebwd_bwd_prepare", "sagebwd_bwd_attention",
+    "sagebwd_bwd_finish", "sagebwd_check_status", "sagebwd_status_string", "sagebwd_version",
+)
+
+
+class SageBwdError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({_status_text(code)})")
+
+
+class Problem(ctypes.Structure):
+    """Mirror of ``sagebwd_problem``."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("N", ctypes.c_int32),
+        ("d", ctypes.c_int32), ("causal", ctypes.c_int32), ("smooth_k", ctypes.c_int32),
+        ("flags", ctypes.c_uint32), ("softmax_scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_uint32),
+    ]
+
+    @classmethod
+    def make(cls, B, Hq, Hkv, N, d, causal, smooth_k=True, flags=0, softmax_scale=0.0, wait_timeout_ms=0):
+        return cls(B, Hq, Hkv, N, d, int(bool(causal)), int(bool(smooth_k)), flags, softmax_scale, wait_timeout_ms)
+
+    @classmethod
+    def from_tensors(cls, q, k, causal, **kw):
+        B, Hq, N, d = q.shape
+        return cls.make(B, Hq, k.shape[1], N, d, causal, **kw)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library():
+    """Build (if needed) and load libsagebwd.so; raises if that is impossible."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            P = ctypes.POINTER(Problem)
+            vp, st = ctypes.c_void_p, ctypes.c_int
+            lib.sagebwd_saved_bytes.argtypes = [P]
+            lib.sagebwd_saved_bytes.restype = ctypes.c_size_t
+            lib.sagebwd_workspace_bytes.argtypes = [P, ctypes.c_int]
+            lib.sagebwd_workspace_bytes.restype = ctypes.c_size_t
+            lib.sagebwd_quantize.argtypes = [P, ctypes.c_int, vp, vp, vp, vp, vp, vp]
+            lib.sagebwd_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.sagebwd_bwd.argtypes = [P] + [vp] * 12
+            lib.sagebwd_fwd_quantize.argtypes = [P, vp, vp, vp, vp, vp, vp]
+            lib.sagebwd_fwd_attention.argtypes = [P, vp, vp, vp, vp, vp]
+            lib.sagebwd_bwd_prepare.argtypes = [P, vp, vp, vp, vp]
+            lib.sagebwd_bwd_attention.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.sagebwd_bwd_finish.argtypes = [P, vp, vp, vp]
+            lib.sagebwd_check_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+            lib.sagebwd_status_string.argtypes = [ctypes.c_int]
+            lib.sagebwd_status_string.restype = ctypes.c_char_p
+            lib.sagebwd_version.restype = ctypes.c_int32
+            for name in ("sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd", "sagebwd_fwd_quantize",
+                         "sagebwd_fwd_attention", "sagebwd_bwd_prepare", "sagebwd_bwd_attention",
+                         "sagebwd_bwd_finish", "sagebwd_check_status"):
+                getattr(lib, name).restype = st
+            _lib = lib
+    return _lib
+
+
+def _status_text(code: int) -> str:
+    try:
+        return load_library().sagebwd_status_string(code).decode()
+    except Exception:  # noqa: BLE001 - only used to decorate an error message
+        return "?"
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SageBwdError(code, where)
+
+
+def sagebwd_saved_bytes(prob: Problem) -> int:
+    return int(load_library().sagebwd_saved_bytes(ctypes.byref(prob)))
+
+
+def sagebwd_workspace_bytes(prob: Problem, pass_: int) -> int:
+    return int(load_library().sagebwd_workspace_bytes(ctypes.byref(prob), pass_))
+
+
+def sagebwd_quantize(prob, which, x, x_q, scales, k_mean, ws, stream=None):
+    _check(load_library().sagebwd_quantize(ctypes.byref(prob), which, _ptr(x), _ptr(x_q), _ptr(scales),
+                                           _ptr(k_mean), _ptr(ws), _stream(stream)), "sagebwd_quantize")
+
+
+def sagebwd_fwd(prob, q, k, v, o, lse, saved, ws, stream=None):
+    _check(load_library().sagebwd_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                      _ptr(saved), _ptr(ws), _stream(stream)), "sagebwd_fwd")
+
+
+def sagebwd_bwd(prob, q, k, v, o, dO, lse, saved, dq, dk, dv, ws, stream=None):
+    _check(load_library().sagebwd_bwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                      _ptr(saved), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), _stream(stream)),
+           "sagebwd_bwd")
+
+
+def sagebwd_fwd_quantize(prob, q, k, v, saved, ws, stream=None):
+    _check(load_library().sagebwd_fwd_quantize(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(saved), _ptr(ws),
+                                               _stream(stream)), "sagebwd_fwd_quantize")
+
+
+def sagebwd_fwd_attention(prob, saved, o, lse, ws, stream=None):
+    _check(load_library().sagebwd_fwd_attention(ctypes.byref(prob), _ptr(saved), _ptr(o), _ptr(lse), _ptr(ws),
+                                                _stream(stream)), "sagebwd_fwd_attention")
+
+
+def sagebwd_bwd_prepare(prob, o, dO, ws, stream=None):
+    _check(load_library().sagebwd_bwd_prepare(ctypes.byref(prob), _ptr(o), _ptr(dO), _ptr(ws), _stream(stream)),
+           "sagebwd_bwd_prepare")
+
+
+def sagebwd_bwd_attention(prob, v, dO, lse, saved, dk, dv, ws, stream=None):
+    _check(load_library().sagebwd_bwd_attention(ctypes.byref(prob), _ptr(v), _ptr(dO), _ptr(lse), _ptr(saved),
+                                                _ptr(dk), _ptr(dv), _ptr(ws), _stream(stream)),
+           "sagebwd_bwd_attention")
+
+
+def sagebwd_bwd_finish(prob, dq, ws, stream=None):
+    _check(load_library().sagebwd_bwd_finish(ctypes.byref(prob), _ptr(dq), _ptr(ws), _stream(stream)),
+           "sagebwd_bwd_finish")
+
+
+def sagebwd_check_status(ws, stream=None):
+    """Synchronize the stream; return (status code, raw status word)."""
+    word = ctypes.c_int32(0)
+    code = load_library().sagebwd_check_status(_ptr(ws), _stream(stream), ctypes.byref(word))
+    return int(code), int(word.value)
+
+
+def sagebwd_status_string(code: int) -> str:
+    return load_library().sagebwd_status_string(code).decode()
+
+
+def sagebwd_version() -> int:
+    return int(load_library().sagebwd_version())
+
+
+# ---------------------------------------------------------------------------- buffers and autograd
+
+
+def empty_bytes(nbytes: int, device) -> torch.Tensor:
+    """A device byte buffer (torch allocations are 256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def quantized_views(prob: Problem, saved: torch.Tensor) -> dict:
+    """Views of the `saved` buffer of sagebwd_fwd (layout of the library: 256-byte aligned sections
+    q^, k^, v^ (BF16), sQ, sK, sV (FP32 block scales), mean of K (FP32))."""
+    def al(x):
+        return (x + 255) // 256 * 256
+    B, Hq, Hkv, N, d = prob.B, prob.Hq, prob.Hkv, prob.N, prob.d
+    nb = (N + 127) // 128
+    sizes = [("q", B * Hq * N * d * 2), ("k", B * Hkv * N * d * 2), ("v", B * Hkv * N * d * 2),
+             ("sq", B * Hq * nb * 4), ("sk", B * Hkv * nb * 4), ("sv", B * Hkv * nb * 4), ("mu", B * Hkv * d * 4)]
+    out, off = {}, 0
+    for name, n in sizes:
+        out[name] = saved[off:off + n]
+        off += al(n)
+    out["q"] = out["q"].view(torch.bfloat16).view(B, Hq, N, d)
+    out["k"] = out["k"].view(torch.bfloat16).view(B, Hkv, N, d)
+    out["v"] = out["v"].view(torch.bfloat16).view(B, Hkv, N, d)
+    out["sq"] = out["sq"].view(torch.float32).view(B * Hq, nb)
+    out["sk"] = out["sk"].view(torch.float32).view(B * Hkv, nb)
+    out["sv"] = out["sv"].view(torch.float32).view(B * Hkv, nb)
+    out["mu"] = out["mu"].view(torch.float32).view(B * Hkv, d)
+    return out
+
+
+def _check_inputs(q, k, v):
+    for t in (q, k, v):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4):
+            raise ValueError("q, k, v must be contiguous 4-D bfloat16 CUDA tensors [B, H, N, d]")
+
+
+class SageBwdAttention(torch.autograd.Function):
+    """softmax(scale Q K^T) V with SageBwd's INT8 forward and backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal=False, softmax_scale=0.0, smooth_k=True):
+        _check_inputs(q, k, v)
+        prob = Problem.from_tensors(q, k, causal, smooth_k=smooth_k, softmax_scale=softmax_scale)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+        saved = empty_bytes(sagebwd_saved_bytes(prob), q.device)
+        ws = empty_bytes(sagebwd_workspace_bytes(prob, 0), q.device)
+        sagebwd_fwd(prob, q, k, v, o, lse, saved, ws)
+        ctx.prob = prob
+        ctx.save_for_backward(q, k, v, o, lse, saved)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, saved = ctx.saved_tensors
+        prob = ctx.prob
+        do = do.contiguous()
+        dq = torch.empty_like(q)
+        dk = torch.empty_like(k)
+        dv = torch.empty_like(v)
+        ws = empty_bytes(sagebwd_workspace_bytes(prob, 1), q.device)
+        sagebwd_bwd(prob, q, k, v, o, do, lse, saved, dq, dk, dv, ws)
+        return dq, dk, dv, None, None, None
+
+
+def attention(q, k, v, causal=False, softmax_scale=0.0, smooth_k=True):
+    """SageBwd attention on BF16 [B, H, N, d] CUDA tensors (GQA when k/v have fewer heads)."""
+    return SageBwdAttention.apply(q, k, v, causal, softmax_scale, smooth_k)

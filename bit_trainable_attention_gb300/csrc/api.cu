@@ -1,0 +1,378 @@
+// C ABI of libsagebwd: argument checks, buffer layouts, TMA tensor maps and
+// the launch sequence of each entry point.  All device memory belongs to the
+// caller; nothing here allocates, frees or synchronizes (except
+// sagebwd_check_status).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "sagebwd_internal.h"
+
+using namespace sagebwd;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool problem_ok(const sagebwd_problem* p) {
+  return p && p->B >= 1 && p->Hq >= 1 && p->Hkv >= 1 && p->N >= 1 && p->d >= 1 && p->Hq % p->Hkv == 0;
+}
+
+sagebwd_status check_problem(const sagebwd_problem* p) {
+  if (!problem_ok(p)) return SAGEBWD_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return SAGEBWD_ERR_UNSUPPORTED;
+  // int32 element indices inside the kernels, and grid limits
+  const double elems = (double)p->B * p->Hq * p->N * p->d;
+  if (elems >= 2147483648.0) return SAGEBWD_ERR_UNSUPPORTED;
+  if ((double)nblocks(p->N) * p->B * p->Hq >= 2147483647.0) return SAGEBWD_ERR_UNSUPPORTED;
+  return SAGEBWD_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+struct SavedLayout {
+  size_t q, k, v, sq, sk, sv, mu, total;
+};
+SavedLayout saved_layout(const sagebwd_problem* p) {
+  const size_t nb = (size_t)nblocks(p->N);
+  const size_t qe = (size_t)p->B * p->Hq * p->N * p->d, ke = (size_t)p->B * p->Hkv * p->N * p->d;
+  SavedLayout L;
+  size_t off = 0;
+  L.q = off; off += align_up(qe * 2);
+  L.k = off; off += align_up(ke * 2);
+  L.v = off; off += align_up(ke * 2);
+  L.sq = off; off += align_up((size_t)p->B * p->Hq * nb * 4);
+  L.sk = off; off += align_up((size_t)p->B * p->Hkv * nb * 4);
+  L.sv = off; off += align_up((size_t)p->B * p->Hkv * nb * 4);
+  L.mu = off; off += align_up((size_t)p->B * p->Hkv * p->d * 4);
+  L.total = off;
+  return L;
+}
+
+// Workspace: [status word | pass scratch].
+struct WsLayout {
+  size_t status, kpart, D, dOq, sdo, dqacc, total;
+};
+WsLayout ws_layout(const sagebwd_problem* p, int pass) {
+  const size_t nb = (size_t)nblocks(p->N);
+  WsLayout L{};
+  size_t off = 0;
+  L.status = off; off += kAlign;
+  if (pass == 0) {
+    L.kpart = off; off += align_up((size_t)p->B * p->Hkv * nb * p->d * 8);
+  } else {
+    const size_t qe = (size_t)p->B * p->Hq * p->N * p->d;
+    L.D = off; off += align_up((size_t)p->B * p->Hq * p->N * 4);
+    L.dOq = off; off += align_up(qe * 2);
+    L.sdo = off; off += align_up((size_t)p->B * p->Hq * nb * 4);
+    L.dqacc = off; off += align_up(qe * 4);
+  }
+  L.total = off;
+  return L;
+}
+
+template <class T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+}
+template <class T>
+const T* at(const void* base, size_t off) {
+  return reinterpret_cast<const T*>(static_cast<const uint8_t*>(base) + off);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a BF16 [BH][N][d] tensor: box = 64 channels x 128 tokens x 1
+// head, 128-byte swizzle; tokens past N read as zero.
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+float softmax_scale_of(const sagebwd_problem* p) {
+  return p->softmax_scale > 0.f ? p->softmax_scale : (float)(1.0 / std::sqrt((double)p->d));
+}
+float c0_of(const sagebwd_problem* p) {
+  // scale * log2(e), formed in FP64 and rounded once
+  return (float)((double)softmax_scale_of(p) * 1.4426950408889634073599246810019);
+}
+uint64_t timeout_of(const sagebwd_problem* p) {
+  return p->wait_timeout_ms ? (uint64_t)p->wait_timeout_ms * 1000000ull : kDefaultTimeoutNs;
+}
+
+sagebwd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SAGEBWD_OK : SAGEBWD_ERR_CUDA; }
+
+#define SB_CHECK(expr)                          \
+  do {                                          \
+    const sagebwd_status st_ = (expr);          \
+    if (st_ != SAGEBWD_OK) return st_;          \
+  } while (0)
+
+sagebwd_status need(bool ok, sagebwd_status err) { return ok ? SAGEBWD_OK : err; }
+
+sagebwd_status check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs) {
+    if (p == nullptr) return SAGEBWD_ERR_INVALID_ARG;
+    if (!aligned16(p)) return SAGEBWD_ERR_MISALIGNED;
+  }
+  return SAGEBWD_OK;
+}
+
+sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const void* k, const void* v, void* saved,
+                                 void* ws, cudaStream_t st) {
+  const SavedLayout S = saved_layout(p);
+  const WsLayout W = ws_layout(p, 0);
+  int* status = at<int>(ws, W.status);
+  const int nb = nblocks(p->N);
+  const float* mean = nullptr;
+  if (p->smooth_k) {
+    SB_CHECK(cuda_status(launch_kmean(static_cast<const __nv_bfloat16*>(k), at<double>(ws, W.kpart),
+                                      at<float>(saved, S.mu), p->B * p->Hkv, p->N, p->d, status, 1, st)));
+    mean = at<float>(saved, S.mu);
+  }
+  QuantParams qp{};
+  qp.job[0] = {static_cast<const __nv_bfloat16*>(q), at<__nv_bfloat16>(saved, S.q), at<float>(saved, S.sq), nullptr,
+               p->B * p->Hq};
+  qp.job[1] = {static_cast<const __nv_bfloat16*>(k), at<__nv_bfloat16>(saved, S.k), at<float>(saved, S.sk), mean,
+               p->B * p->Hkv};
+  qp.job[2] = {static_cast<const __nv_bfloat16*>(v), at<__nv_bfloat16>(saved, S.v), at<float>(saved, S.sv), nullptr,
+               p->B * p->Hkv};
+  qp.njobs = 3;
+  qp.block_start[0] = 0;
+  for (int j = 0; j < 3; ++j) qp.block_start[j + 1] = qp.block_start[j] + qp.job[j].BH * nb;
+  qp.N = p->N;
+  qp.d = p->d;
+  qp.nb = nb;
+  qp.status = status;
+  qp.clear_status = p->smooth_k ? 0 : 1;
+  return cuda_status(launch_quantize(qp, st));
+}
+
+sagebwd_status fwd_attention_impl(const sagebwd_problem* p, const void* saved, void* o, float* lse, void* ws,
+                                  cudaStream_t st) {
+  const SavedLayout S = saved_layout(p);
+  const WsLayout W = ws_layout(p, 0);
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, at<uint8_t>(saved, S.q), p->B * p->Hq, p->N, p->d) ||
+      !make_map(&tk, at<uint8_t>(saved, S.k), p->B * p->Hkv, p->N, p->d) ||
+      !make_map(&tv, at<uint8_t>(saved, S.v), p->B * p->Hkv, p->N, p->d))
+    return SAGEBWD_ERR_CUDA;
+  FwdParams fp{};
+  fp.B = p->B;
+  fp.Hq = p->Hq;
+  fp.Hkv = p->Hkv;
+  fp.N = p->N;
+  fp.nb = nblocks(p->N);
+  fp.G = p->Hq / p->Hkv;
+  fp.c0 = c0_of(p);
+  fp.sq = at<float>(saved, S.sq);
+  fp.sk = at<float>(saved, S.sk);
+  fp.sv = at<float>(saved, S.sv);
+  fp.o = static_cast<__nv_bfloat16*>(o);
+  fp.lse = lse;
+  fp.status = at<int>(ws, W.status);
+  fp.timeout_ns = timeout_of(p);
+  fp.flags = p->flags;
+  return cuda_status(launch_fwd(tq, tk, tv, fp, p->d, p->causal, st));
+}
+
+sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const void* dO, void* ws, cudaStream_t st) {
+  const WsLayout W = ws_layout(p, 1);
+  PrepParams pp{};
+  pp.o = static_cast<const __nv_bfloat16*>(o);
+  pp.dO = static_cast<const __nv_bfloat16*>(dO);
+  pp.D = at<float>(ws, W.D);
+  pp.dOq = at<__nv_bfloat16>(ws, W.dOq);
+  pp.sdo = at<float>(ws, W.sdo);
+  pp.dq_acc = at<float>(ws, W.dqacc);
+  pp.BH = p->B * p->Hq;
+  pp.N = p->N;
+  pp.d = p->d;
+  pp.nb = nblocks(p->N);
+  pp.status = at<int>(ws, W.status);
+  return cuda_status(launch_bwd_prep(pp, st));
+}
+
+sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const void* dO, const float* lse,
+                                  const void* saved, void* dk, void* dv, void* ws, cudaStream_t st) {
+  const SavedLayout S = saved_layout(p);
+  const WsLayout W = ws_layout(p, 1);
+  CUtensorMap tq, tk, tv, tdo, tdoq;
+  if (!make_map(&tq, at<uint8_t>(saved, S.q), p->B * p->Hq, p->N, p->d) ||
+      !make_map(&tk, at<uint8_t>(saved, S.k), p->B * p->Hkv, p->N, p->d) ||
+      !make_map(&tv, v, p->B * p->Hkv, p->N, p->d) || !make_map(&tdo, dO, p->B * p->Hq, p->N, p->d) ||
+      !make_map(&tdoq, at<uint8_t>(ws, W.dOq), p->B * p->Hq, p->N, p->d))
+    return SAGEBWD_ERR_CUDA;
+  BwdParams bp{};
+  bp.B = p->B;
+  bp.Hq = p->Hq;
+  bp.Hkv = p->Hkv;
+  bp.N = p->N;
+  bp.nb = nblocks(p->N);
+  bp.G = p->Hq / p->Hkv;
+  bp.c0 = c0_of(p);
+  bp.sc = softmax_scale_of(p);
+  bp.sq = at<float>(saved, S.sq);
+  bp.sk = at<float>(saved, S.sk);
+  bp.sdo = at<float>(ws, W.sdo);
+  bp.lse = lse;
+  bp.D = at<float>(ws, W.D);
+  bp.dq_acc = at<float>(ws, W.dqacc);
+  bp.dk = static_cast<__nv_bfloat16*>(dk);
+  bp.dv = static_cast<__nv_bfloat16*>(dv);
+  bp.status = at<int>(ws, W.status);
+  bp.timeout_ns = timeout_of(p);
+  bp.flags = p->flags;
+  return cuda_status(launch_bwd(tq, tk, tv, tdo, tdoq, bp, p->d, p->causal, st));
+}
+
+sagebwd_status bwd_finish_impl(const sagebwd_problem* p, void* dq, void* ws, cudaStream_t st) {
+  const WsLayout W = ws_layout(p, 1);
+  const size_t n = (size_t)p->B * p->Hq * p->N * p->d;
+  return cuda_status(launch_dq_convert(at<float>(ws, W.dqacc), static_cast<__nv_bfloat16*>(dq), n, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sagebwd_saved_bytes(const sagebwd_problem* prob) {
+  if (check_problem(prob) != SAGEBWD_OK) return 0;
+  return saved_layout(prob).total;
+}
+
+size_t sagebwd_workspace_bytes(const sagebwd_problem* prob, int pass) {
+  if (check_problem(prob) != SAGEBWD_OK || (pass != 0 && pass != 1)) return 0;
+  return ws_layout(prob, pass).total;
+}
+
+sagebwd_status sagebwd_quantize(const sagebwd_problem* prob, int which, const void* x, void* x_q, float* scales,
+                                float* k_mean, void* ws, void* stream) {
+  SB_CHECK(check_problem(prob));
+  SB_CHECK(need(which >= SAGEBWD_Q && which <= SAGEBWD_DO, SAGEBWD_ERR_INVALID_ARG));
+  const bool smooth = which == SAGEBWD_K && prob->smooth_k;
+  SB_CHECK(check_ptrs({x, x_q, scales, ws}));
+  if (smooth) SB_CHECK(check_ptrs({k_mean}));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WsLayout W = ws_layout(prob, 0);
+  int* status = at<int>(ws, W.status);
+  const int heads = (which == SAGEBWD_K || which == SAGEBWD_V) ? prob->Hkv : prob->Hq;
+  const int BH = prob->B * heads, nb = nblocks(prob->N);
+  if (smooth)
+    SB_CHECK(cuda_status(launch_kmean(static_cast<const __nv_bfloat16*>(x), at<double>(ws, W.kpart), k_mean, BH,
+                                      prob->N, prob->d, status, 1, st)));
+  QuantParams qp{};
+  qp.job[0] = {static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(x_q), scales,
+               smooth ? k_mean : nullptr, BH};
+  qp.njobs = 1;
+  qp.block_start[0] = 0;
+  qp.block_start[1] = BH * nb;
+  qp.N = prob->N;
+  qp.d = prob->d;
+  qp.nb = nb;
+  qp.status = status;
+  qp.clear_status = smooth ? 0 : 1;
+  return cuda_status(launch_quantize(qp, st));
+}
+
+sagebwd_status sagebwd_fwd_quantize(const sagebwd_problem* prob, const void* q, const void* k, const void* v,
+                                    void* saved, void* ws, void* stream) {
+  SB_CHECK(check_problem(prob));
+  SB_CHECK(check_ptrs({q, k, v, saved, ws}));
+  return fwd_quantize_impl(prob, q, k, v, saved, ws, static_cast<cudaStream_t>(stream));
+}
+
+sagebwd_status sagebwd_fwd_attention(const sagebwd_problem* prob, const void* saved, void* o, float* lse, void* ws,
+                                     void* stream) {
+  SB_CHECK(check_problem(prob));
+  SB_CHECK(check_ptrs({saved, o, lse, ws}));
+  return fwd_attention_impl(prob, saved, o, lse, ws, static_cast<cudaStream_t>(stream));
+}
+
+sagebwd_status sagebwd_fwd(const sagebwd_problem* prob, const void* q, const void* k, const void* v, void* o,
+                           float* lse, void* saved, void* ws, void* stream) {
+  SB_CHECK(check_problem(prob));
+  SB_CHECK(check_ptrs({q, k, v, o, lse, saved, ws}));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SB_CHECK(fwd_quantize_impl(prob, q, k, v, saved, ws, st));
+  return fwd_attention_impl(prob, saved, o, lse, ws, st);
+}
+
+sagebwd_status sagebwd_bwd_prepare(const sagebwd_problem* prob, const void* o, const void* dO, void* ws,
+                                   void* stream) {
+  SB_CHECK(check_problem(prob));
+  SB_CHECK(check_ptrs({o, dO, ws}));
+  return bwd_prepare_impl(prob, o, dO, ws, static_cast<cudaStream_t>(stream));
+}
+
+sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v, const void* dO, const float* lse,
+                                     const void* saved, void* dk, void* dv, void* ws, void* stream) {
+  SB_CHECK(check_problem(prob));
+  SB_CHECK(check_ptrs({v, dO, lse, saved, dk, dv, ws}));
+  return bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, static_cast<cudaStream_t>(stream));
+}
+
+sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* ws, void* stream) {
+  SB_CHECK(check_problem(prob));
+  SB_CHECK(check_ptrs({dq, ws}));
+  return bwd_finish_impl(prob, dq, ws, static_cast<cudaStream_t>(stream));
+}
+
+sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, const void* saved, void* dq, void* dk, void* dv, void* ws,
+                           void* stream) {
+  SB_CHECK(check_problem(prob));
+  SB_CHECK(check_ptrs({q, k, v, o, dO, lse, saved, dq, dk, dv, ws}));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SB_CHECK(bwd_prepare_impl(prob, o, dO, ws, st));
+  SB_CHECK(bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, st));
+  return bwd_finish_impl(prob, dq, ws, st);
+}
+
+sagebwd_status sagebwd_check_status(const void* ws, void* stream, int32_t* detail) {
+  if (ws == nullptr) return SAGEBWD_ERR_INVALID_ARG;
+  int32_t word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SAGEBWD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SAGEBWD_ERR_CUDA;
+  if (detail) *detail = word;
+  return (word & 0xFF) == 0 ? SAGEBWD_OK : static_cast<sagebwd_status>(word & 0xFF);
+}
+
+const char* sagebwd_status_string(sagebwd_status s) {
+  switch (s) {
+    case SAGEBWD_OK: return "ok";
+    case SAGEBWD_ERR_INVALID_ARG: return "invalid argument";
+    case SAGEBWD_ERR_UNSUPPORTED: return "unsupported problem (head dim must be 64 or 128; sizes within int32)";
+    case SAGEBWD_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case SAGEBWD_ERR_CUDA: return "CUDA runtime error";
+    case SAGEBWD_ERR_TIMEOUT: return "a kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+int32_t sagebwd_version(void) { return 100; }
+
+}  // extern "C"

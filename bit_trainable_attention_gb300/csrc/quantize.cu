@@ -1,0 +1,239 @@
+// HBM-bound kernels of the SageBwd path: the K channel mean, the per-block
+// absmax INT8 quantizer (Q, K, V and dO), the backward preprocess
+// (D = rowsum(dO * O) with the dO quantization) and the FP32 -> BF16 dQ
+// conversion.  Loads and stores are 16-byte vectors along d; one CTA owns one
+// 128-token block of one head, so the block's absmax never leaves the CTA.
+//
+// Quantizer ("SageBwd: A Trainable Low-bit Attention", Abstract: INT8
+// attention with K-smoothing; the block size and scale rule are this
+// library's reading): a = max|x| over a 128 x d block, inv = 127/a and
+// s = a/127 in IEEE FP32, code = clamp(rint(x * inv), -127, 127); a block
+// whose max is below 2^-120 (zero, or so small that 127/a would overflow)
+// gives codes 0 and s = 0.  K first subtracts its channel mean over all
+// N tokens, summed in FP64 in a fixed order (deterministic) and rounded once
+// to FP32.
+#include "sagebwd_internal.h"
+
+namespace sagebwd {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f[2 * e] = __uint_as_float(w[e] << 16);
+    f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+}
+
+// codes are integers in [-127, 127]: the BF16 conversion is exact
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float quant_code(float x, float inv) {
+  float c = rintf(__fmul_rn(x, inv));
+  return fminf(127.f, fmaxf(-127.f, c));
+}
+
+// Block-wide max of non-negative values; every thread gets the result.
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // red may still be read from a previous use
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float m = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, red[w]);
+  return m;
+}
+
+// Quantize the 128 x D block (bh, blk) of one tensor.  V8 = D / 8 16-byte vectors per row.
+template <int D>
+__device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xq,
+                               float* __restrict__ scale, const float* __restrict__ mean, int bh, int blk, int N,
+                               int nb, float* red) {
+  constexpr int V8 = D / 8;
+  constexpr int PER = kBlk * V8 / kThreads;  // 16-byte vectors per thread
+  const int row0 = blk * kBlk;
+  const size_t base = ((size_t)bh * N + row0) * D;
+  float v[PER][8];
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int idx = threadIdx.x + e * kThreads;
+    const int r = idx / V8, c8 = idx % V8;
+    if (row0 + r < N) {
+      const uint4 u = *reinterpret_cast<const uint4*>(x + base + (size_t)r * D + c8 * 8);
+      unpack8(u, v[e]);
+      if (mean != nullptr) {
+        const float* mu = mean + (size_t)bh * D + c8 * 8;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[e][k] = __fsub_rn(v[e][k], mu[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[e][k]));
+    }
+  }
+  const float a = block_max(amax, red);
+  const bool live = a >= kMinGroupMax;
+  const float inv = live ? __fdiv_rn(127.f, a) : 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int idx = threadIdx.x + e * kThreads;
+    const int r = idx / V8, c8 = idx % V8;
+    if (row0 + r < N) {
+      uint4 out;
+      out.x = pack2(quant_code(v[e][0], inv), quant_code(v[e][1], inv));
+      out.y = pack2(quant_code(v[e][2], inv), quant_code(v[e][3], inv));
+      out.z = pack2(quant_code(v[e][4], inv), quant_code(v[e][5], inv));
+      out.w = pack2(quant_code(v[e][6], inv), quant_code(v[e][7], inv));
+      *reinterpret_cast<uint4*>(xq + base + (size_t)r * D + c8 * 8) = out;
+    }
+  }
+  if (threadIdx.x == 0) scale[(size_t)bh * nb + blk] = live ? __fdiv_rn(a, 127.f) : 0.f;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantParams p) {
+  __shared__ float red[kThreads / 32];
+  if (p.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = 0;
+  int j = 0;
+  while (j + 1 < p.njobs && (int)blockIdx.x >= p.block_start[j + 1]) ++j;
+  const int local = blockIdx.x - p.block_start[j];
+  const QuantJob& job = p.job[j];
+  quantize_block<D>(job.x, job.xq, job.scale, job.mean, local / p.nb, local % p.nb, p.N, p.nb, red);
+}
+
+// Channel sums of K over one 128-token block, in FP64 (exact for BF16 inputs of
+// ordinary range), reduced across threads in a fixed order.
+template <int D>
+__global__ void __launch_bounds__(kThreads) kmean_partial_kernel(const __nv_bfloat16* __restrict__ k,
+                                                                 double* __restrict__ part, int N, int nb,
+                                                                 int* status, int clear_status) {
+  constexpr int V8 = D / 8, RL = kThreads / V8;  // row lanes
+  __shared__ double red[RL][D];
+  if (clear_status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
+  const int bh = blockIdx.y, blk = blockIdx.x;
+  const int c8 = threadIdx.x % V8, rl = threadIdx.x / V8;
+  double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int r = blk * kBlk + rl; r < min(N, blk * kBlk + kBlk); r += RL) {
+    const uint4 u = *reinterpret_cast<const uint4*>(k + ((size_t)bh * N + r) * D + c8 * 8);
+    float f[8];
+    unpack8(u, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += (double)f[e];
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[rl][c8 * 8 + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    double s = 0;
+    for (int q = 0; q < RL; ++q) s += red[q][threadIdx.x];
+    part[((size_t)bh * nb + blk) * D + threadIdx.x] = s;
+  }
+}
+
+__global__ void kmean_final_kernel(const double* __restrict__ part, float* __restrict__ mean, int N, int nb, int d) {
+  const int bh = blockIdx.x, c = threadIdx.x;
+  if (c >= d) return;
+  double s = 0;
+  for (int b = 0; b < nb; ++b) s += part[((size_t)bh * nb + b) * d + c];
+  mean[(size_t)bh * d + c] = (float)(s / (double)N);
+}
+
+// Backward preprocess for one 128-query block: D_i = sum_c dO[i,c] O[i,c]
+// (FP32), the dO block quantization, and zeroing the block's rows of the FP32
+// dQ accumulator.
+template <int D>
+__global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const PrepParams p) {
+  __shared__ float red[kThreads / 32];
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = 0;
+  constexpr int V8 = D / 8;
+  constexpr int PER = kBlk * V8 / kThreads;
+  const int bh = blockIdx.y, blk = blockIdx.x;
+  const int row0 = blk * kBlk;
+  const size_t base = ((size_t)bh * p.N + row0) * D;
+  // D = rowsum(dO * O): V8 consecutive threads share a row (V8 divides 32).
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int idx = threadIdx.x + e * kThreads;
+    const int r = idx / V8, c8 = idx % V8;
+    float s = 0.f;
+    if (row0 + r < p.N) {
+      float a[8], b[8];
+      unpack8(*reinterpret_cast<const uint4*>(p.dO + base + (size_t)r * D + c8 * 8), a);
+      unpack8(*reinterpret_cast<const uint4*>(p.o + base + (size_t)r * D + c8 * 8), b);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s = fmaf(a[k], b[k], s);
+      float4* z = reinterpret_cast<float4*>(p.dq_acc + base + (size_t)r * D + c8 * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int o = V8 / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (c8 == 0 && row0 + r < p.N) p.D[(size_t)bh * p.N + row0 + r] = s;
+  }
+  quantize_block<D>(p.dO, p.dOq, p.sdo, nullptr, bh, blk, p.N, p.nb, red);
+}
+
+__global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ out, size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = acc[i];
+    out[i] = make_uint2(pack2(v.x, v.y), pack2(v.z, v.w));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s) {
+  const int blocks = p.block_start[p.njobs];
+  if (blocks == 0) return cudaSuccess;
+  if (p.d == 64)
+    quantize_kernel<64><<<blocks, kThreads, 0, s>>>(p);
+  else
+    quantize_kernel<128><<<blocks, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kmean(const __nv_bfloat16* k, double* part, float* mean, int BH, int N, int d, int* status,
+                         int clear_status, cudaStream_t s) {
+  const int nb = nblocks(N);
+  dim3 grid(nb, BH);
+  if (d == 64)
+    kmean_partial_kernel<64><<<grid, kThreads, 0, s>>>(k, part, N, nb, status, clear_status);
+  else
+    kmean_partial_kernel<128><<<grid, kThreads, 0, s>>>(k, part, N, nb, status, clear_status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kmean_final_kernel<<<BH, d, 0, s>>>(part, mean, N, nb, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const PrepParams& p, cudaStream_t s) {
+  dim3 grid(p.nb, p.BH);
+  if (p.d == 64)
+    bwd_prep_kernel<64><<<grid, kThreads, 0, s>>>(p);
+  else
+    bwd_prep_kernel<128><<<grid, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const float* acc, __nv_bfloat16* dq, size_t n, cudaStream_t s) {
+  const size_t n4 = n / 4;  // d is a multiple of 8
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t want = (n4 + 255) / 256;
+  const int blocks = (int)(want < (size_t)sms * 8 ? want : (size_t)sms * 8);
+  dq_convert_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(reinterpret_cast<const float4*>(acc),
+                                                           reinterpret_cast<uint2*>(dq), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace sagebwd

@@ -1,0 +1,97 @@
+// Host/device declarations shared by the translation units of libsagebwd.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/sagebwd.h"
+
+namespace sagebwd {
+
+constexpr int kBlk = 128;                            // tokens per quantization block and per tile
+constexpr float kLog2e = 1.4426950408889634f;        // log2(e)
+constexpr float kLn2 = 0.69314718055994531f;         // ln(2)
+constexpr float kLog2_127 = 6.9886846867721655f;     // log2(127)
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// A quantization group (block, P^T row, dS tile) whose largest magnitude is
+// below 2^-120 quantizes to zero codes with scale 0, so that 127/max never
+// overflows FP32.
+constexpr float kMinGroupMax = 7.52316384526264e-37f;  // 2^-120
+
+// Status word codes written by kernels (low byte = sagebwd_status, bits 8..15 = wait site).
+__host__ __device__ constexpr int status_timeout(int site) { return (int)SAGEBWD_ERR_TIMEOUT | (site << 8); }
+
+inline int nblocks(int N) { return (N + kBlk - 1) / kBlk; }
+
+// ------------------------------------------------------------------ quantize
+struct QuantJob {
+  const __nv_bfloat16* x;  // [BH][N][d]
+  __nv_bfloat16* xq;       // [BH][N][d] integer-valued codes
+  float* scale;            // [BH][nb]
+  const float* mean;       // [BH][d] or nullptr
+  int BH;
+};
+struct QuantParams {
+  QuantJob job[3];
+  int njobs;
+  int block_start[4];  // prefix sums of BH * nb over the jobs
+  int N, d, nb;
+  int* status;         // cleared by block 0 when clear_status
+  int clear_status;
+};
+cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s);
+cudaError_t launch_kmean(const __nv_bfloat16* k, double* part, float* mean, int BH, int N, int d, int* status,
+                         int clear_status, cudaStream_t s);
+
+// ------------------------------------------------------------------ backward helpers
+struct PrepParams {
+  const __nv_bfloat16* o;   // [BHq][N][d]
+  const __nv_bfloat16* dO;  // [BHq][N][d]
+  float* D;                 // [BHq][N]
+  __nv_bfloat16* dOq;       // [BHq][N][d]
+  float* sdo;               // [BHq][nb]
+  float* dq_acc;            // [BHq][N][d], zeroed
+  int BH, N, d, nb;
+  int* status;
+};
+cudaError_t launch_bwd_prep(const PrepParams& p, cudaStream_t s);
+cudaError_t launch_dq_convert(const float* acc, __nv_bfloat16* dq, size_t n, cudaStream_t s);
+
+// ------------------------------------------------------------------ attention kernels
+struct FwdParams {
+  int B, Hq, Hkv, N, nb, G;
+  float c0;  // softmax_scale * log2(e), FP32
+  const float* sq;
+  const float* sk;
+  const float* sv;
+  __nv_bfloat16* o;
+  float* lse;
+  int* status;
+  uint64_t timeout_ns;
+  uint32_t flags;
+};
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                       int d, int causal, cudaStream_t s);
+
+struct BwdParams {
+  int B, Hq, Hkv, N, nb, G;
+  float c0;        // softmax_scale * log2(e)
+  float sc;        // softmax_scale
+  const float* sq;  // [BHq][nb]
+  const float* sk;  // [BHk][nb]
+  const float* sdo; // [BHq][nb]
+  const float* lse; // [BHq][N]
+  const float* D;   // [BHq][N]
+  float* dq_acc;    // [BHq][N][d]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* status;
+  uint64_t timeout_ns;
+  uint32_t flags;
+};
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const CUtensorMap& tdoq, const BwdParams& p, int d, int causal, cudaStream_t s);
+
+}  // namespace sagebwd

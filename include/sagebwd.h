@@ -1,0 +1,156 @@
+/*
+ * sagebwd.h -- C ABI of the GB300 (sm_103a) SageBwd attention library.
+ *
+ * SageBwd is the trainable INT8 attention of "SageBwd: A Trainable Low-bit
+ * Attention" (Abstract): its forward and backward quantize six of the seven
+ * attention matmuls to INT8 -- forward S = Q K^T and O = P V, backward S
+ * recompute, dV = P^T dO, dQ = dS K and dK = dS^T Q -- and keep only
+ * dP = dO V^T in 16-bit floating point ("SageAttention3: Microscaling FP4
+ * Attention for Inference and An Exploration of 8-Bit Training", summary
+ * page, Approach, and the "Measured effects" row "Keep dO V^T in FP16").
+ * K is smoothed by subtracting its per-channel mean over tokens (SageBwd
+ * Abstract, finding (iv)); QK-norm, where used, is applied by the caller.
+ *
+ * Quantization granularity (the pages leave it open; this library's choice):
+ *   Q, K, V, dO : one FP32 scale per 128-token block of a head (all d
+ *                 channels): a = max|x|, scale = a/127,
+ *                 code = clamp(rint(x * 127/a), -127, 127), half to even;
+ *   forward P~  : per query row and 128-key tile, code = rint(127*2^(t-tmax));
+ *   backward P  : per key and 128-query tile, scale = max P / 127;
+ *   backward dS : one scale per 128 x 128 tile, scale = max|dS| / 127.
+ * The INT8 codes are held as integer-valued BF16 and multiplied on the
+ * tensor cores with FP32 accumulation, which is exact for these tiles
+ * (|sum| <= 128 * 127^2 < 2^24).
+ *
+ * Conventions for every entry point:
+ *   - Tensors are row-major contiguous. Q, dO, O, dQ: BF16 [B][Hq][N][d];
+ *     K, V, dK, dV: BF16 [B][Hkv][N][d]; LSE: FP32 [B][Hq][N].
+ *     Query head h reads kv head h / (Hq / Hkv) (grouped-query attention).
+ *   - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned.
+ *     The library allocates, frees and synchronizes nothing (except
+ *     sagebwd_check_status, which synchronizes the given stream), keeps no
+ *     global state, and launches only on the given stream.
+ *   - Supported: d in {64, 128}; Hq % Hkv == 0; N >= 1; B, Hq, Hkv >= 1.
+ *   - Errors are returned before any launch for bad arguments; a launch
+ *     failure returns SAGEBWD_ERR_CUDA.  Kernels bound every wait; a wait
+ *     that runs out records SAGEBWD_ERR_TIMEOUT in the status word kept in
+ *     the workspace, read with sagebwd_check_status.  No C++ exception
+ *     crosses this interface.
+ */
+#ifndef SAGEBWD_H_
+#define SAGEBWD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SAGEBWD_OK = 0,
+  SAGEBWD_ERR_INVALID_ARG = 1, /* null pointer, bad sizes, Hq % Hkv != 0 */
+  SAGEBWD_ERR_UNSUPPORTED = 2, /* head dim other than 64 / 128, or a size beyond the int32 index range */
+  SAGEBWD_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned */
+  SAGEBWD_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  SAGEBWD_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out (device status word) */
+} sagebwd_status;
+
+/* Which operand sagebwd_quantize handles. */
+enum { SAGEBWD_Q = 0, SAGEBWD_K = 1, SAGEBWD_V = 2, SAGEBWD_DO = 3 };
+
+/* sagebwd_problem.flags */
+#define SAGEBWD_FLAG_DROP_ONE_LOAD 0x1u /* fault injection: the forward kernel skips one K-tile load, so its
+                                           bounded wait runs out and the call reports SAGEBWD_ERR_TIMEOUT */
+
+typedef struct {
+  int32_t B, Hq, Hkv, N, d;
+  int32_t causal;       /* 1: key k visible to query i iff k <= i (top-left aligned); 0: all keys */
+  int32_t smooth_k;     /* 1: subtract the per-channel mean of K over tokens before quantizing (the method) */
+  uint32_t flags;       /* SAGEBWD_FLAG_* (0 in normal use) */
+  float softmax_scale;  /* <= 0 selects 1/sqrt(d) */
+  uint32_t wait_timeout_ms; /* bound of every in-kernel wait; 0 selects 2000 ms */
+} sagebwd_problem;
+
+/* Bytes of the `saved` buffer that sagebwd_fwd fills and sagebwd_bwd reads:
+ * the quantized Q, K, V (integer-valued BF16, same shapes as the inputs),
+ * their FP32 block scales and the FP32 mean of K.  Returns 0 for an invalid
+ * problem. */
+size_t sagebwd_saved_bytes(const sagebwd_problem* prob);
+
+/* Bytes of workspace for pass 0 (forward, sagebwd_fwd / sagebwd_quantize) or
+ * pass 1 (backward, sagebwd_bwd).  The workspace holds the status word first,
+ * then scratch (K-mean partial sums; D = rowsum(dO*O), the quantized dO and
+ * its scales, the FP32 dQ accumulator).  Contents need no initialisation and
+ * are not meaningful between calls, except the status word. */
+size_t sagebwd_workspace_bytes(const sagebwd_problem* prob, int pass);
+
+/* Quantize one operand ("SageBwd", Abstract: INT8 quantization; K-smoothing).
+ *   which  : SAGEBWD_Q / _K / _V / _DO; x has that operand's shape.
+ *   x_q    : BF16 output, same shape, integer values in [-127, 127].
+ *   scales : FP32 [B*H][ceil(N/128)] block scales.
+ *   k_mean : FP32 [B*Hkv][d] channel means when which == SAGEBWD_K and
+ *            smooth_k == 1 (then required), else ignored (may be NULL).
+ *   ws     : forward workspace (sagebwd_workspace_bytes(prob, 0)).       */
+sagebwd_status sagebwd_quantize(const sagebwd_problem* prob, int which, const void* x, void* x_q, float* scales,
+                                float* k_mean, void* ws, void* stream);
+
+/* Forward: quantize Q, K (smoothed), V into `saved`, then the fused
+ * attention forward with online softmax ("SageBwd", Abstract; FlashAttention
+ * lineage listed under "Builds on").
+ *   o   : BF16 [B][Hq][N][d] output.
+ *   lse : FP32 [B][Hq][N], natural-log log-sum-exp of each row of the scores
+ *         the kernel softmaxes, scale * Q (K - mean_K)^T (with smooth_k = 1 this
+ *         differs from the LSE of scale * Q K^T by -scale * Q_i . mean_K).
+ *   saved : sagebwd_saved_bytes(prob) bytes, read back by sagebwd_bwd.
+ *   ws  : sagebwd_workspace_bytes(prob, 0) bytes.                          */
+sagebwd_status sagebwd_fwd(const sagebwd_problem* prob, const void* q, const void* k, const void* v, void* o,
+                           float* lse, void* saved, void* ws, void* stream);
+
+/* Backward: D = rowsum(dO * O) and the quantized dO, then the fused backward
+ * (S recompute, dV = P^T dO, dP = dO V^T in BF16, dS = P (dP - D),
+ * dK = dS^T Q, dQ = dS K) and the FP32 -> BF16 conversion of dQ.
+ *   q, k, v, o, dO : the forward's inputs and output and the gradient of o.
+ *   lse, saved     : exactly as produced by sagebwd_fwd for these inputs.
+ *   dq : BF16 [B][Hq][N][d]; dk, dv : BF16 [B][Hkv][N][d] (summed over the
+ *        query heads of each kv head).
+ *   ws : sagebwd_workspace_bytes(prob, 1) bytes.                            */
+sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, const void* saved, void* dq, void* dk, void* dv, void* ws,
+                           void* stream);
+
+/* The same two passes split into the library's kernel stages, for callers
+ * that schedule or time them separately.  Calling the stages in this order,
+ * on one stream, is exactly sagebwd_fwd / sagebwd_bwd.
+ *   sagebwd_fwd_quantize  : K mean and the Q, K, V quantization into `saved`.
+ *   sagebwd_fwd_attention : the fused forward kernel on `saved` -> o, lse.
+ *   sagebwd_bwd_prepare   : D = rowsum(dO * O), quantized dO, zeroed dQ
+ *                           accumulator (all in the backward workspace).
+ *   sagebwd_bwd_attention : the fused backward kernel -> dk, dv and the FP32
+ *                           dQ accumulator in the workspace.
+ *   sagebwd_bwd_finish    : dQ accumulator -> BF16 dq.                       */
+sagebwd_status sagebwd_fwd_quantize(const sagebwd_problem* prob, const void* q, const void* k, const void* v,
+                                    void* saved, void* ws, void* stream);
+sagebwd_status sagebwd_fwd_attention(const sagebwd_problem* prob, const void* saved, void* o, float* lse, void* ws,
+                                     void* stream);
+sagebwd_status sagebwd_bwd_prepare(const sagebwd_problem* prob, const void* o, const void* dO, void* ws,
+                                   void* stream);
+sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v, const void* dO, const float* lse,
+                                     const void* saved, void* dk, void* dv, void* ws, void* stream);
+sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* ws, void* stream);
+
+/* Synchronize `stream` and return the status word in `ws` (SAGEBWD_OK or
+ * SAGEBWD_ERR_TIMEOUT); *detail (optional) receives the raw word, whose bits
+ * 8..15 name the wait that ran out. */
+sagebwd_status sagebwd_check_status(const void* ws, void* stream, int32_t* detail);
+
+const char* sagebwd_status_string(sagebwd_status s);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int32_t sagebwd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGEBWD_H_ */

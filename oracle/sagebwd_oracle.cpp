@@ -19,8 +19,9 @@
 // implemented here (one per function below) are:
 //  * every quantized operand of Q, K, V, dO is cut into blocks of 128 tokens
 //    (all d channels), one scale per block: a = max|x|, s = a/127,
-//    code = clamp(rint(x * (127/a)), -127, 127); a zero block gives code 0 and
-//    s = 0; the scale arithmetic is IEEE FP32;
+//    code = clamp(rint(x * (127/a)), -127, 127); a block whose max is below
+//    2^-120 (zero, or so small that 127/a would overflow FP32) gives codes 0
+//    and s = 0; the scale arithmetic is IEEE FP32;
 //  * K is smoothed by its FP32 channel mean over all N tokens (sum taken in
 //    FP64, divided by N in FP64, rounded once to FP32), K' = K - mean in FP32;
 //  * forward P~: per query row and 128-key tile, code = rint(127*2^(t - tmax))
@@ -66,6 +67,9 @@ typedef struct {
 namespace {
 
 constexpr int BLK = 128;  // tokens per quantization block and per tile
+// A quantization group (block, P^T row, dS tile) whose largest magnitude is
+// below this quantizes to all-zero codes with scale 0: 127/a stays finite in FP32.
+const double kMinGroupMax = std::ldexp(1.0, -120);
 constexpr double kLog2e = 1.4426950408889634073599246810019;
 constexpr double kLn2 = 0.69314718055994530941723212145818;
 const double kInf = std::numeric_limits<double>::infinity();
@@ -126,7 +130,7 @@ struct QTensor {
 void quant_block(const Mode& M, int which, const double* x, int count, double* codes, double* scale) {
   double a = 0;
   for (int e = 0; e < count; ++e) a = std::max(a, std::fabs(x[e]));
-  if (a == 0) {
+  if (a < kMinGroupMax) {
     for (int e = 0; e < count; ++e) codes[e] = 0;
     *scale = 0;
     return;
@@ -309,7 +313,7 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
   for (int c = 0; c < T.nk; ++c) {
     double cmax = 0;
     for (int a = 0; a < T.ni; ++a) cmax = std::max(cmax, P[(size_t)a * BLK + c]);
-    if (cmax == 0) continue;
+    if (cmax < kMinGroupMax) continue;
     const double inv = M.F(127.0 / cmax);
     T.spc[c] = M.F(cmax / 127.0);
     for (int a = 0; a < T.ni; ++a) T.pt[(size_t)c * BLK + a] = M.Q(QZ_PB, M.F(P[(size_t)a * BLK + c] * inv));
@@ -320,7 +324,7 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
   for (int a = 0; a < T.ni; ++a)
     for (int c = 0; c < T.nk; ++c) amax = std::max(amax, std::fabs(dS[(size_t)a * BLK + c]));
   T.sds = 0;
-  if (amax > 0) {
+  if (amax >= kMinGroupMax) {
     const double inv = M.F(127.0 / amax);
     T.sds = M.F(amax / 127.0);
     for (int a = 0; a < T.ni; ++a)

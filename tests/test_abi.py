@@ -1,0 +1,83 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function include/sagebwd.h declares, and rejects bad arguments before
+any launch (those paths make no CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_trainable_attention_gb300 as sb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "sagebwd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(sagebwd_[a-z_0-9]+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return sb.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd", "sagebwd_check_status"):
+        assert required in names
+    assert set(names) == set(sb.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_sizes_and_strings(lib):
+    p = sb.Problem.make(1, 4, 2, 300, 64, True)
+    nb = 3
+    saved = sb.sagebwd_saved_bytes(p)
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    expect = al(1 * 4 * 300 * 64 * 2) + 2 * al(1 * 2 * 300 * 64 * 2) + al(4 * nb * 4) + 2 * al(2 * nb * 4) + \
+        al(2 * 64 * 4)
+    assert saved == expect
+    assert sb.sagebwd_workspace_bytes(p, 0) >= 256 + 2 * nb * 64 * 8
+    assert sb.sagebwd_workspace_bytes(p, 1) >= 256 + 4 * 300 * 64 * (4 + 2)
+    assert sb.sagebwd_workspace_bytes(p, 2) == 0
+    assert sb.sagebwd_status_string(0) == "ok"
+    assert "timed out" in sb.sagebwd_status_string(5)
+    assert sb.sagebwd_version() >= 100
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), 2),                    # unsupported head dim
+    (dict(Hq=3, Hkv=2), 1),             # Hq % Hkv != 0
+    (dict(N=0), 1),
+    (dict(B=0), 1),
+    (dict(N=1 << 30), 2),               # beyond int32 element indices
+])
+def test_bad_problems_rejected_before_launch(lib, kw, code):
+    args = dict(B=1, Hq=4, Hkv=2, N=256, d=64, causal=True)
+    args.update(kw)
+    p = sb.Problem.make(**args)
+    assert sb.sagebwd_saved_bytes(p) == 0
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    rc = lib.sagebwd_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, fake, fake, None)
+    assert rc == code
+
+
+def test_bad_pointers_rejected_before_launch(lib):
+    p = sb.Problem.make(1, 4, 2, 256, 64, True)
+    good = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.sagebwd_fwd(ctypes.byref(p), None, good, good, good, good, good, good, None) == 1
+    assert lib.sagebwd_fwd(ctypes.byref(p), good, odd, good, good, good, good, good, None) == 3
+    assert lib.sagebwd_bwd(ctypes.byref(p), *([good] * 5), odd, *([good] * 6)) == 3
+    assert lib.sagebwd_quantize(ctypes.byref(p), 7, good, good, good, None, good, None) == 1
+    # K with smoothing needs the mean output
+    assert lib.sagebwd_quantize(ctypes.byref(p), 1, good, good, good, None, good, None) == 1
+    assert lib.sagebwd_check_status(None, None, None) == 1

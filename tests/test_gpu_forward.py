@@ -1,0 +1,105 @@
+"""GPU parity of the quantize stage and the fused forward against the oracle.
+
+The INT8 codes, block scales and K means the library writes must equal the
+oracle's bit for bit; O and LSE must meet the normwise tolerance of
+tests/_parity.py.  Small shapes cover several tiles, ragged tails, GQA,
+causal masks, N = 1 and both head dims; the five named workloads are checked
+at full size on sampled query blocks.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_trainable_attention_gb300 as sb
+from bit_trainable_attention_gb300 import workloads as W
+from _parity import (LSE_TOL, assert_parity, block_selection, cos, device_inputs, gpu_forward, oracle_problem,
+                     to_np)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    W.WORKLOADS["tiny"],
+    W.small("gqa_causal_300_d64", 1, 4, 2, 300, 64, True, 101, qk_norm=True, k_offset_sd=2.0),
+    W.small("gqa_noncausal_257_d128", 2, 3, 1, 257, 128, False, 102, k_offset_sd=3.0),
+    W.small("outlier_causal_384_d128", 1, 2, 2, 384, 128, True, 103, outlier_frac=0.01),
+    W.small("n1_d64", 1, 2, 1, 1, 64, True, 104),
+    W.small("n129_d128_noncausal", 1, 2, 2, 129, 128, False, 105, qk_norm=True),
+    W.small("n127_d64_causal", 2, 2, 2, 127, 64, True, 106),
+]
+
+
+def check_quantized(oracle_mod, w, x, fwd, smooth_k=True):
+    op = oracle_problem(oracle_mod, w, smooth_k)
+    views = sb.quantized_views(fwd["prob"], fwd["saved"])
+    for name, key, BH, smooth in (("q", "q", w.B * w.Hq, False), ("k", "k", w.B * w.Hkv, smooth_k),
+                                  ("v", "v", w.B * w.Hkv, False)):
+        codes, scales, mean = oracle_mod.quantize(op, x[key], BH, smooth)
+        gcodes = views[name].float().cpu().numpy().reshape(codes.shape)
+        np.testing.assert_array_equal(gcodes, codes.astype(np.float32), err_msg=f"{name} codes")
+        gs = views["s" + name].cpu().numpy()
+        np.testing.assert_array_equal(gs.view(np.uint32), scales.view(np.uint32), err_msg=f"{name} scales")
+        if smooth:
+            gm = views["mu"].cpu().numpy()
+            np.testing.assert_array_equal(gm.view(np.uint32), mean.view(np.uint32), err_msg="k mean")
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_forward_small(oracle_mod, w):
+    x, xd = device_inputs(w)
+    fwd = gpu_forward(w, xd)
+    assert fwd["status"] == 0
+    check_quantized(oracle_mod, w, x, fwd)
+    op = oracle_problem(oracle_mod, w)
+    o_ref, lse_ref = oracle_mod.fwd(op, x["q"], x["k"], x["v"])
+    assert_parity(to_np(fwd["o"]), o_ref, "O")
+    np.testing.assert_allclose(to_np(fwd["lse"]), lse_ref, rtol=0, atol=LSE_TOL)
+    ex_o, _ = oracle_mod.fwd(op, x["q"], x["k"], x["v"], exact=True)
+    if w.outlier_frac == 0:
+        assert cos(to_np(fwd["o"]), ex_o) >= 0.995
+
+
+def test_forward_without_smoothing(oracle_mod):
+    w = W.small("nosmooth", 1, 2, 1, 200, 64, True, 111, k_offset_sd=2.0)
+    x, xd = device_inputs(w)
+    fwd = gpu_forward(w, xd, smooth_k=False)
+    check_quantized(oracle_mod, w, x, fwd, smooth_k=False)
+    op = oracle_problem(oracle_mod, w, smooth_k=False)
+    o_ref, lse_ref = oracle_mod.fwd(op, x["q"], x["k"], x["v"])
+    assert_parity(to_np(fwd["o"]), o_ref, "O")
+    np.testing.assert_allclose(to_np(fwd["lse"]), lse_ref, rtol=0, atol=LSE_TOL)
+
+
+def test_forward_repeatable(oracle_mod):
+    """Two calls on the same inputs give identical bits (no atomics in the forward)."""
+    w = W.small("rep", 1, 4, 2, 520, 64, True, 112, qk_norm=True)
+    _, xd = device_inputs(w)
+    a = gpu_forward(w, xd)
+    b = gpu_forward(w, xd)
+    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
+    va, vb = sb.quantized_views(a["prob"], a["saved"]), sb.quantized_views(b["prob"], b["saved"])
+    for key in va:  # the sections of the saved buffer (its alignment padding is never written)
+        assert torch.equal(va[key], vb[key]), key
+
+
+@pytest.mark.parametrize("name", ["pretrain", "llama1b", "qwen15b", "videodit"])
+def test_forward_full_size_sampled(oracle_mod, name):
+    """Full-size workload in the bench's launch configuration; quantized
+    operands compared in full, O/LSE on sampled query blocks (first, middle,
+    last) of two heads."""
+    w = W.WORKLOADS[name]
+    x, xd = device_inputs(w)
+    fwd = gpu_forward(w, xd)
+    assert fwd["status"] == 0
+    check_quantized(oracle_mod, w, x, fwd)
+    nb = (w.N + 127) // 128
+    heads = [0, w.Hq - 1]
+    sel = block_selection(w, heads, [0, nb // 2, -1])
+    op = oracle_problem(oracle_mod, w)
+    o_ref, lse_ref = oracle_mod.fwd(op, x["q"], x["k"], x["v"], qsel=sel)
+    o = to_np(fwd["o"])
+    lse = to_np(fwd["lse"])
+    m = np.isfinite(lse_ref)
+    assert m.sum() > 0
+    assert_parity(o[m], o_ref[m], "O")
+    np.testing.assert_allclose(lse[m], lse_ref[m], rtol=0, atol=LSE_TOL)
+    assert np.all(np.isfinite(o))
