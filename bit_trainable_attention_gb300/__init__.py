@@ -24,18 +24,20 @@ __all__ = [
     "Problem", "SageBwdError", "load_library", "sagebwd_saved_bytes", "sagebwd_workspace_bytes",
     "sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd", "sagebwd_fwd_quantize", "sagebwd_fwd_attention",
     "sagebwd_bwd_prepare", "sagebwd_bwd_attention", "sagebwd_bwd_finish", "sagebwd_check_status",
-    "sagebwd_status_string", "sagebwd_version", "attention", "SageBwdAttention",
+    "sagebwd_status_string", "sagebwd_version", "sagebwd_quantize_k_noalloc", "attention", "SageBwdAttention",
     "SAGEBWD_Q", "SAGEBWD_K", "SAGEBWD_V", "SAGEBWD_DO", "FLAG_DROP_ONE_LOAD",
 ]
 
 SAGEBWD_Q, SAGEBWD_K, SAGEBWD_V, SAGEBWD_DO = 0, 1, 2, 3
 FLAG_DROP_ONE_LOAD = 0x1
-STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA", 5: "TIMEOUT"}
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA", 5: "TIMEOUT",
+                6: "SCRATCH_LIMIT"}
 
 EXPORTED_SYMBOLS = (
     "sagebwd_saved_bytes", "sagebwd_workspace_bytes", "sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd",
     "sagebwd_fwd_quantize", "sagebwd_fwd_attention", "sagebwd_bwd_prepare", "sagebwd_bwd_attention",
     "sagebwd_bwd_finish", "sagebwd_check_status", "sagebwd_status_string", "sagebwd_version",
+    "sagebwd_quantize_k_noalloc",
 )
 
 
@@ -91,12 +93,13 @@ def load_library():
             lib.sagebwd_bwd_attention.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.sagebwd_bwd_finish.argtypes = [P, vp, vp, vp]
             lib.sagebwd_check_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+            lib.sagebwd_quantize_k_noalloc.argtypes = [P, vp, vp, vp, vp, vp]
             lib.sagebwd_status_string.argtypes = [ctypes.c_int]
             lib.sagebwd_status_string.restype = ctypes.c_char_p
             lib.sagebwd_version.restype = ctypes.c_int32
             for name in ("sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd", "sagebwd_fwd_quantize",
                          "sagebwd_fwd_attention", "sagebwd_bwd_prepare", "sagebwd_bwd_attention",
-                         "sagebwd_bwd_finish", "sagebwd_check_status"):
+                         "sagebwd_bwd_finish", "sagebwd_check_status", "sagebwd_quantize_k_noalloc"):
                 getattr(lib, name).restype = st
             _lib = lib
     return _lib
@@ -178,6 +181,15 @@ def sagebwd_bwd_attention(prob, v, dO, lse, saved, dk, dv, ws, stream=None):
 def sagebwd_bwd_finish(prob, dq, ws, stream=None):
     _check(load_library().sagebwd_bwd_finish(ctypes.byref(prob), _ptr(dq), _ptr(ws), _stream(stream)),
            "sagebwd_bwd_finish")
+
+
+def sagebwd_quantize_k_noalloc(prob, k, k_q, scales, k_mean, stream=None):
+    """K quantization without a workspace, for callers that cannot allocate device memory: the
+    K-mean scratch is a fixed 8 MiB array inside the library (limit B*Hkv*ceil(N/128)*d <= 2^20).
+    Calls that overlap on the GPU share that array and race; the first call on a device should
+    come before any stream capture."""
+    _check(load_library().sagebwd_quantize_k_noalloc(ctypes.byref(prob), _ptr(k), _ptr(k_q), _ptr(scales),
+                                                     _ptr(k_mean), _stream(stream)), "sagebwd_quantize_k_noalloc")
 
 
 def sagebwd_check_status(ws, stream=None):

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(OUT_DIR, "libsagebwd.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-UNITS = ["api", "quantize", "fwd", "bwd"]
+UNITS = ["api", "quantize", "fwd", "bwd", "noalloc"]
 
 
 def _nvcc() -> str:

@@ -369,6 +369,7 @@ const char* sagebwd_status_string(sagebwd_status s) {
     case SAGEBWD_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case SAGEBWD_ERR_CUDA: return "CUDA runtime error";
     case SAGEBWD_ERR_TIMEOUT: return "a kernel wait timed out";
+    case SAGEBWD_ERR_SCRATCH_LIMIT: return "problem too large for the fixed scratch of sagebwd_quantize_k_noalloc";
   }
   return "unknown status";
 }

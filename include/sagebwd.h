@@ -53,7 +53,8 @@ typedef enum {
   SAGEBWD_ERR_UNSUPPORTED = 2, /* head dim other than 64 / 128, or a size beyond the int32 index range */
   SAGEBWD_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned */
   SAGEBWD_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
-  SAGEBWD_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out (device status word) */
+  SAGEBWD_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (device status word) */
+  SAGEBWD_ERR_SCRATCH_LIMIT = 6 /* the problem needs more than the fixed scratch of sagebwd_quantize_k_noalloc */
 } sagebwd_status;
 
 /* Which operand sagebwd_quantize handles. */
@@ -138,6 +139,29 @@ sagebwd_status sagebwd_bwd_prepare(const sagebwd_problem* prob, const void* o, c
 sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v, const void* dO, const float* lse,
                                      const void* saved, void* dk, void* dv, void* ws, void* stream);
 sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* ws, void* stream);
+
+/* K quantization (K-smoothing mean + per-block codes), like
+ * sagebwd_quantize(prob, SAGEBWD_K, ...), for callers that cannot allocate
+ * device memory -- an operator hook handed only its input and output tensors,
+ * code that runs where cudaMalloc is not allowed or would synchronize the
+ * device, a process whose memory belongs to a pool it cannot draw from at that
+ * point.  It takes no workspace: the FP64 channel sums of the K-mean pass go to
+ * a fixed 8 MiB array compiled into the library, which every GPU that loads
+ * the library keeps until the process exits.  (The SageBwd pages have no
+ * counterpart of this entry point.)
+ *   - Limit: B * Hkv * ceil(N/128) * d <= 1048576 (e.g. B=2, Hkv=30, N=17776,
+ *     d=64 needs 533760); larger problems return SAGEBWD_ERR_SCRATCH_LIMIT
+ *     before any launch.  With smooth_k == 0 no scratch is used.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.  It allocates nothing at any time.
+ *   - All calls share the one array: calls that can overlap on the GPU (other
+ *     streams, other host threads) race and must be serialized by the caller.
+ *     Every partial sum is written before it is read, so the array needs no
+ *     clearing between calls.
+ *   k, k_q, scales, k_mean: as for sagebwd_quantize with which == SAGEBWD_K. */
+sagebwd_status sagebwd_quantize_k_noalloc(const sagebwd_problem* prob, const void* k, void* k_q, float* scales,
+                                          float* k_mean, void* stream);
 
 /* Synchronize `stream` and return the status word in `ws` (SAGEBWD_OK or
  * SAGEBWD_ERR_TIMEOUT); *detail (optional) receives the raw word, whose bits
