@@ -145,9 +145,12 @@ def cossim_vs_torch(step: Step):
     vv = v.repeat_interleave(w.G, dim=1)
     o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=w.causal)
     o.backward(x["do"].float())
+    ref = {"o": o.detach(), "dq": q.grad, "dk": k.grad, "dv": v.grad}
+    got = {"o": step.o, "dq": step.dq, "dk": step.dk, "dv": step.dv}
     out = {}
-    for name, a, b in (("o", step.o, o), ("dq", step.dq, q.grad), ("dk", step.dk, k.grad), ("dv", step.dv, v.grad)):
-        out[name] = round(float(torch.nn.functional.cosine_similarity(a.float().reshape(-1), b.reshape(-1), dim=0)), 6)
+    for name in ("o", "dq", "dk", "dv"):
+        a, b = got[name].float().reshape(-1), ref[name].reshape(-1)
+        out[name] = round(float(torch.nn.functional.cosine_similarity(a, b, dim=0)), 6)
     return out
 
 
@@ -278,6 +281,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="oracle CPU-baseline sample size (seconds)")
     ap.add_argument("--reference-step-s", type=float, default=8.0, help="oracle seconds per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end pass (profiling runs)")
+    ap.add_argument("--no-cossim", action="store_true", help="skip the cosine-similarity reference (profiling runs)")
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
 
@@ -310,7 +315,10 @@ def main():
     sampler = ClockSampler(local)
     total, stage = time_device(step, args.steps, args.warmup, flush, barrier)
     clocks = sampler.stop()
-    e2e_ms, h2d, d2h = time_e2e(step, max(3, args.steps // 5), max(3, args.warmup), flush, barrier)
+    if args.no_e2e:
+        e2e_ms, h2d, d2h = [float("nan")], 0, 0
+    else:
+        e2e_ms, h2d, d2h = time_e2e(step, max(3, args.steps // 5), max(3, args.warmup), flush, barrier)
     code0, _ = sb.sagebwd_check_status(step.ws0)
     code1, _ = sb.sagebwd_check_status(step.ws1)
 
@@ -352,7 +360,7 @@ def main():
         "status": [code0, code1],
     }
     if rank == 0:
-        line["cossim_vs_torch_fp32"] = cossim_vs_torch(step)
+        line["cossim_vs_torch_fp32"] = None if args.no_cossim else cossim_vs_torch(step)
         line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -8,11 +8,15 @@
 // heads of that kv head and their 128-query blocks i, so dK_j and dV_j are
 // summed in registers and written once; dQ is accumulated across CTAs with
 // FP32 reductions into the workspace.  Warp roles:
-//   warps 0-3 / 4-7  compute warpgroups 0 / 1: thread (w, r) owns key row r
-//                    (TMEM lane r), query columns [64w, 64w+64) of the tile and
-//                    output columns [w d/2, (w+1) d/2) of dK, dV, dQ
-//   warp 8           TMA producer (K^_j, V_j once; Q^_i, dO_i, dO^_i per tile)
-//   warp 9           TMEM allocation and the MMA-issuing thread
+//   warps 0-15       four compute warpgroups: thread (w, r) owns key row r
+//                    (TMEM lane r), query columns [32w, 32w+32) of the tile and
+//                    output columns [w d/4, (w+1) d/4) of dK, dV, dQ
+//   warp 16          TMA producer (K^_j, V_j once; Q^_i, dO_i, dO^_i per tile)
+//   warp 17          TMEM allocation and the MMA-issuing thread
+//   warps 18-19      idle (they complete the fifth warpgroup, which gives its
+//                    registers to the compute warpgroups: 640 threads launch
+//                    with 96 registers each; the producer warpgroup drops to
+//                    kRegsLow, the compute warpgroups rise to kRegsHigh)
 // Per tile (TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+d),
 // dK [256+d,256+2d), dQ [0,d) reusing S^T once it is consumed):
 //   MMA   S^T = K^_j Q^_i^T (integer-valued BF16, exact)  dP^T = V_j dO_i^T (BF16)
@@ -40,26 +44,33 @@ struct BwdCfg {
   static constexpr int OFF_DOQ = OFF_DO + NS * TILE;
   static constexpr int OFF_PT = OFF_DOQ + NS * TILE;
   static constexpr int OFF_DST = OFF_PT + PTILE;
-  static constexpr int OFF_VEC = OFF_DST + PTILE;  // L2[128], Dv[128], pm[2][128], am[8]
-  static constexpr int OFF_BAR = OFF_VEC + (128 + 128 + 256 + 8) * 4;
+  static constexpr int OFF_VEC = OFF_DST + PTILE;  // L2[128], Dv[128], pmax bits[128], am[16]
+  static constexpr int OFF_BAR = OFF_VEC + (128 + 128 + 128 + 16) * 4;
   static constexpr int NBAR = 1 + 6 * NS + 4 + 2 + 1;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
   // The tiles need a 1024-byte aligned base; the D = 128 layout leaves no room for padding.
   static constexpr int SMEM = BYTES + 1024 <= 232448 ? BYTES + 1024 : BYTES;
   static constexpr int C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D, C_DQ = 0;
+  static_assert(BYTES <= 232448, "shared memory beyond the per-CTA limit");
 };
+
+constexpr int kNWG = 4;                      // compute warpgroups
+constexpr int kCompute = kNWG * 128;          // compute threads
+constexpr int kThreads = kCompute + 128;      // + the producer / MMA warpgroup
+constexpr int kQC = 128 / kNWG;               // query columns per compute thread
+constexpr uint32_t kRegsLaunch = 96, kRegsLow = 32, kRegsHigh = 112;
+static_assert(128 * kRegsLow + kCompute * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
 
 enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty, bSiteDOQFull, bSiteDOQEmpty,
                bSiteSDP, bSiteDSReady, bSiteAcc, bSiteTmemFree, bSiteAlign, bSiteC1, bSiteC2 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmDOQ, const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int NS = C::NS;
-  constexpr int HALF = D / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   if (C::SMEM == C::BYTES && smem != smem_raw) {
@@ -69,8 +80,8 @@ __global__ void __launch_bounds__(320, 1)
   }
   float* L2v = reinterpret_cast<float*>(smem + C::OFF_VEC);
   float* Dv = L2v + 128;
-  float* pm = Dv + 128;   // [2][128]
-  float* am = pm + 256;   // [8]
+  int* pmx = reinterpret_cast<int*>(Dv + 128);  // [128] row maxima of P (P >= 0: float bits order as ints)
+  float* am = reinterpret_cast<float*>(pmx + 128);  // [16] per-warp maxima of |dS|
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* bar_kv = bars;
   uint64_t* bar_q_full = bar_kv + 1;
@@ -111,16 +122,16 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar_doq_empty + s, 1);
     }
     mbar_init(bar_sdp, 1);
-    mbar_init(bar_ds_ready, 256);
+    mbar_init(bar_ds_ready, kCompute);
     mbar_init(bar_acc, 1);
-    mbar_init(bar_tmem_free, 256);
-    mbar_init(bar_c1, 256);
-    mbar_init(bar_c2, 256);
+    mbar_init(bar_tmem_free, kCompute);
+    mbar_init(bar_c1, kCompute);
+    mbar_init(bar_c2, kCompute);
     mbar_init(bar_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 17) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -129,10 +140,10 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
-
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  if (warp >= 16) {
+    setmaxnreg_dec<kRegsLow>();
+    if (warp == 16 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
       int q_iss[NS], do_iss[NS], doq_iss[NS];
       for (int s = 0; s < NS; ++s) q_iss[s] = do_iss[s] = doq_iss[s] = 0;
       mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
@@ -167,10 +178,8 @@ __global__ void __launch_bounds__(320, 1)
         if (do_iss[s]) drain(bar_do_full + s, (do_iss[s] - 1) & 1, p.timeout_ns);
         if (doq_iss[s]) drain(bar_doq_full + s, (doq_iss[s] - 1) & 1, p.timeout_ns);
       }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 17 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       const uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       const uint32_t idKM = idesc_bf16_f32(128, D, false, true);     // dK, dV: A K-major, B MN-major
       const uint32_t idQM = idesc_bf16_f32(128, D, true, true);      // dQ: A MN-major, B MN-major
@@ -225,17 +234,19 @@ __global__ void __launch_bounds__(320, 1)
       drain(bar_final, 0, p.timeout_ns);
     }
   } else {
+    setmaxnreg_inc<kRegsHigh>();
     // ------------------------------------------------------------ compute warpgroups
-    const int w = warp >> 2;           // 0 / 1
+    constexpr int DC = D / kNWG;       // output columns per thread
+    const int w = warp >> 2;           // compute warpgroup 0..kNWG-1
     const int r = tid & 127;           // key row == TMEM lane
-    const int ct = tid;                // 0..255 among the compute threads
+    const int ct = tid;                // index among the compute threads
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int kglob = k0 + r;
     const bool key_ok = kglob < p.N;
     const float sKv = p.sk[(size_t)bhk * p.nb + j];
-    float dv_run[HALF], dk_run[HALF];
+    float dv_run[DC], dk_run[DC];
 #pragma unroll
-    for (int c = 0; c < HALF; ++c) dv_run[c] = dk_run[c] = 0.f;
+    for (int c = 0; c < DC; ++c) dv_run[c] = dk_run[c] = 0.f;
 
     for (int it = 0; it < T; ++it) {
       const int bhq = b * p.Hq + hk * p.G + it / nq;
@@ -247,8 +258,10 @@ __global__ void __launch_bounds__(320, 1)
         const bool in = i0 + q < p.N;
         if (ct < 128)
           L2v[q] = in ? __fmul_rn(p.lse[(size_t)bhq * p.N + i0 + q], kLog2e) : INFINITY;
-        else
+        else if (ct < 256)
           Dv[q] = in ? p.D[(size_t)bhq * p.N + i0 + q] : 0.f;
+        else if (ct < 384)
+          pmx[q] = 0;
       }
       // (an mbarrier rather than bar.sync, so that this wait is bounded too)
       mbar_arrive(bar_c1);
@@ -260,36 +273,36 @@ __global__ void __launch_bounds__(320, 1)
       // pass 1
       float pmax = 0.f, amax = 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        const int col = 64 * w + c0;  // query column within the tile
-        uint32_t sv[16], dpv[16], pw[16], dsw[16];
-        tmem_ld16(tmem + lane_base + C::C_S + col, sv);
-        tmem_ld16(tmem + lane_base + C::C_DP + col, dpv);
+      for (int c0 = 0; c0 < kQC; c0 += 8) {
+        const int col = kQC * w + c0;  // query column within the tile
+        uint32_t sv[8], dpv[8];        // S -> P and dP -> dS, converted in place
+        tmem_ld8(tmem + lane_base + C::C_S + col, sv);
+        tmem_ld8(tmem + lane_base + C::C_DP + col, dpv);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 8; ++e) {
           float pr = ex2_approx(fmaf(__uint_as_float(sv[e]), qks, -L2v[col + e]));
           if (!key_ok || (diag && col + e < r)) pr = 0.f;
           const float ds = pr * (__uint_as_float(dpv[e]) - Dv[col + e]);
           pmax = fmaxf(pmax, pr);
           amax = fmaxf(amax, fabsf(ds));
-          pw[e] = __float_as_uint(pr);
-          dsw[e] = __float_as_uint(ds);
+          sv[e] = __float_as_uint(pr);
+          dpv[e] = __float_as_uint(ds);
         }
-        tmem_st16(tmem + lane_base + C::C_S + col, pw);
-        tmem_st16(tmem + lane_base + C::C_DP + col, dsw);
+        tmem_st8(tmem + lane_base + C::C_S + col, sv);
+        tmem_st8(tmem + lane_base + C::C_DP + col, dpv);
       }
       tmem_st_wait();
-      pm[w * 128 + r] = pmax;
+      atomicMax(pmx + r, __float_as_int(pmax));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (lane == 0) am[warp] = amax;
       mbar_arrive(bar_c2);
       if (!waitw(wc, bar_c2, it & 1, bSiteC2)) break;
-      const float cmax = fmaxf(pm[r], pm[128 + r]);
+      const float cmax = __int_as_float(pmx[r]);
       float a = am[0];
 #pragma unroll
-      for (int q = 1; q < 8; ++q) a = fmaxf(a, am[q]);
+      for (int q = 1; q < kCompute / 32; ++q) a = fmaxf(a, am[q]);
       const bool p_live = cmax >= kMinGroupMax, d_live = a >= kMinGroupMax;
       const float invP = p_live ? __fdiv_rn(127.f, cmax) : 0.f;
       const float sPc = p_live ? __fdiv_rn(cmax, 127.f) : 0.f;
@@ -298,24 +311,22 @@ __global__ void __launch_bounds__(320, 1)
       // pass 2: codes into the swizzled A tiles (row = key r, 16-byte chunk = 8 queries)
       const uint32_t pt_base = smem_u32(smem + C::OFF_PT), ds_base = smem_u32(smem + C::OFF_DST);
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        const int col = 64 * w + c0;
-        uint32_t pv[16], dsv[16], pk[8], dk8[8];
-        tmem_ld16(tmem + lane_base + C::C_S + col, pv);
-        tmem_ld16(tmem + lane_base + C::C_DP + col, dsv);
+      for (int c0 = 0; c0 < kQC; c0 += 8) {
+        const int col = kQC * w + c0;
+        uint32_t pv[8], dsv[8];
+        tmem_ld8(tmem + lane_base + C::C_S + col, pv);
+        tmem_ld8(tmem + lane_base + C::C_DP + col, dsv);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          pk[e >> 1] = pack_bf16x2(rint_f32(__fmul_rn(__uint_as_float(pv[e]), invP)),
+        for (int e = 0; e < 8; e += 2) {
+          pv[e >> 1] = pack_bf16x2(rint_f32(__fmul_rn(__uint_as_float(pv[e]), invP)),
                                    rint_f32(__fmul_rn(__uint_as_float(pv[e + 1]), invP)));
-          dk8[e >> 1] = pack_bf16x2(rint_f32(__fmul_rn(__uint_as_float(dsv[e]), invA)),
+          dsv[e >> 1] = pack_bf16x2(rint_f32(__fmul_rn(__uint_as_float(dsv[e]), invA)),
                                     rint_f32(__fmul_rn(__uint_as_float(dsv[e + 1]), invA)));
         }
-        const int ch = col >> 3;
-        st_shared_v4(pt_base + sw128_offset(r, ch), pk[0], pk[1], pk[2], pk[3]);
-        st_shared_v4(pt_base + sw128_offset(r, ch + 1), pk[4], pk[5], pk[6], pk[7]);
-        st_shared_v4(ds_base + sw128_offset(r, ch), dk8[0], dk8[1], dk8[2], dk8[3]);
-        st_shared_v4(ds_base + sw128_offset(r, ch + 1), dk8[4], dk8[5], dk8[6], dk8[7]);
+        const uint32_t off = sw128_offset(r, col >> 3);
+        st_shared_v4(pt_base + off, pv[0], pv[1], pv[2], pv[3]);
+        st_shared_v4(ds_base + off, dsv[0], dsv[1], dsv[2], dsv[3]);
       }
       tc_fence_before();
       fence_proxy_async_smem();
@@ -327,23 +338,23 @@ __global__ void __launch_bounds__(320, 1)
       const float fk = __fmul_rn(__fmul_rn(p.sc, sDS), p.sq[(size_t)bhq * p.nb + ib]);
       const float fq = __fmul_rn(__fmul_rn(p.sc, sDS), sKv);
       const int qrow = i0 + r;  // dQ tile: lane r is query row i0 + r
-      float* dq_dst = p.dq_acc + ((size_t)bhq * p.N + qrow) * D + w * HALF;
+      float* dq_dst = p.dq_acc + ((size_t)bhq * p.N + qrow) * D + w * DC;
 #pragma unroll
-      for (int c0 = 0; c0 < HALF; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + C::C_DV + w * HALF + c0, v);
+      for (int c0 = 0; c0 < DC; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_base + C::C_DV + w * DC + c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) dv_run[c0 + e] = fmaf(fv, __uint_as_float(v[e]), dv_run[c0 + e]);
-        tmem_ld32(tmem + lane_base + C::C_DK + w * HALF + c0, v);
+        for (int e = 0; e < 16; ++e) dv_run[c0 + e] = fmaf(fv, __uint_as_float(v[e]), dv_run[c0 + e]);
+        tmem_ld16(tmem + lane_base + C::C_DK + w * DC + c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) dk_run[c0 + e] = fmaf(fk, __uint_as_float(v[e]), dk_run[c0 + e]);
-        tmem_ld32(tmem + lane_base + C::C_DQ + w * HALF + c0, v);
+        for (int e = 0; e < 16; ++e) dk_run[c0 + e] = fmaf(fk, __uint_as_float(v[e]), dk_run[c0 + e]);
+        tmem_ld16(tmem + lane_base + C::C_DQ + w * DC + c0, v);
         tmem_ld_wait();
         if (qrow < p.N) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
+          for (int e = 0; e < 16; e += 4)
             red_add_v4_f32(dq_dst + c0 + e, fq * __uint_as_float(v[e]), fq * __uint_as_float(v[e + 1]),
                            fq * __uint_as_float(v[e + 2]), fq * __uint_as_float(v[e + 3]));
         }
@@ -352,10 +363,10 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(bar_tmem_free);
     }
     if (!*abort_flag && key_ok) {
-      uint4* dkd = reinterpret_cast<uint4*>(p.dk + ((size_t)bhk * p.N + kglob) * D + w * HALF);
-      uint4* dvd = reinterpret_cast<uint4*>(p.dv + ((size_t)bhk * p.N + kglob) * D + w * HALF);
+      uint4* dkd = reinterpret_cast<uint4*>(p.dk + ((size_t)bhk * p.N + kglob) * D + w * DC);
+      uint4* dvd = reinterpret_cast<uint4*>(p.dv + ((size_t)bhk * p.N + kglob) * D + w * DC);
 #pragma unroll
-      for (int c = 0; c < HALF; c += 8) {
+      for (int c = 0; c < DC; c += 8) {
         dkd[c / 8] = make_uint4(pack_bf16x2(dk_run[c], dk_run[c + 1]), pack_bf16x2(dk_run[c + 2], dk_run[c + 3]),
                                 pack_bf16x2(dk_run[c + 4], dk_run[c + 5]), pack_bf16x2(dk_run[c + 6], dk_run[c + 7]));
         dvd[c / 8] = make_uint4(pack_bf16x2(dv_run[c], dv_run[c + 1]), pack_bf16x2(dv_run[c + 2], dv_run[c + 3]),
@@ -365,7 +376,7 @@ __global__ void __launch_bounds__(320, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 17) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -379,7 +390,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = p.nb * p.B * p.Hkv;
-  kern<<<grid, 320, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, p);
+  kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, p);
   return cudaGetLastError();
 }
 
