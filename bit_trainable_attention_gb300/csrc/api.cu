@@ -110,6 +110,20 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over an FP32 [BH][N][d] tensor for reduce-adds: box = 32 channels x
+// 128 tokens x 1 head, 128-byte swizzle; rows past N are not written.
+bool make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 float softmax_scale_of(const sagebwd_problem* p) {
   return p->softmax_scale > 0.f ? p->softmax_scale : (float)(1.0 / std::sqrt((double)p->d));
 }
@@ -218,11 +232,12 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
                                   const void* saved, void* dk, void* dv, void* ws, cudaStream_t st) {
   const SavedLayout S = saved_layout(p);
   const WsLayout W = ws_layout(p, 1);
-  CUtensorMap tq, tk, tv, tdo, tdoq;
+  CUtensorMap tq, tk, tv, tdo, tdoq, tdq;
   if (!make_map(&tq, at<uint8_t>(saved, S.q), p->B * p->Hq, p->N, p->d) ||
       !make_map(&tk, at<uint8_t>(saved, S.k), p->B * p->Hkv, p->N, p->d) ||
       !make_map(&tv, v, p->B * p->Hkv, p->N, p->d) || !make_map(&tdo, dO, p->B * p->Hq, p->N, p->d) ||
-      !make_map(&tdoq, at<uint8_t>(ws, W.dOq), p->B * p->Hq, p->N, p->d))
+      !make_map(&tdoq, at<uint8_t>(ws, W.dOq), p->B * p->Hq, p->N, p->d) ||
+      !make_map_f32(&tdq, at<uint8_t>(ws, W.dqacc), p->B * p->Hq, p->N, p->d))
     return SAGEBWD_ERR_CUDA;
   BwdParams bp{};
   bp.B = p->B;
@@ -244,7 +259,7 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
   bp.status = at<int>(ws, W.status);
   bp.timeout_ns = timeout_of(p);
   bp.flags = p->flags;
-  return cuda_status(launch_bwd(tq, tk, tv, tdo, tdoq, bp, p->d, p->causal, st));
+  return cuda_status(launch_bwd(tq, tk, tv, tdo, tdoq, tdq, bp, p->d, p->causal, st));
 }
 
 sagebwd_status bwd_finish_impl(const sagebwd_problem* p, void* dq, void* ws, cudaStream_t st) {

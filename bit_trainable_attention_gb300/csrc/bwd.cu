@@ -6,31 +6,41 @@
 //
 // One CTA owns one 128-key block j of one kv head and loops over the G query
 // heads of that kv head and their 128-query blocks i, so dK_j and dV_j are
-// summed in registers and written once; dQ is accumulated across CTAs with
-// FP32 reductions into the workspace.  Warp roles:
-//   warps 0-15       four compute warpgroups: thread (w, r) owns key row r
-//                    (TMEM lane r), query columns [32w, 32w+32) of the tile and
-//                    output columns [w d/4, (w+1) d/4) of dK, dV, dQ
-//   warp 16          TMA producer (K^_j, V_j once; Q^_i, dO_i, dO^_i per tile)
-//   warp 17          TMEM allocation and the MMA-issuing thread
-//   warps 18-19      idle (they complete the fifth warpgroup, which gives its
-//                    registers to the compute warpgroups: 640 threads launch
-//                    with 96 registers each; the producer warpgroup drops to
-//                    kRegsLow, the compute warpgroups rise to kRegsHigh)
-// Per tile (TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+d),
-// dK [256+d,256+2d), dQ [0,d) reusing S^T once it is consumed):
-//   MMA   S^T = K^_j Q^_i^T (integer-valued BF16, exact)  dP^T = V_j dO_i^T (BF16)
-//   pass 1  P = 2^(S sQ sK scale log2e - LSE_i log2e), dS = P (dP - D_i); both
+// summed in registers and written once; dQ is accumulated across CTAs by
+// TMA bulk reduce-adds into an FP32 workspace.  Warp roles:
+//   warps 0-15   four compute warpgroups: thread (w, r) owns key row r
+//                (TMEM lane r), query columns [32w, 32w+32) of the tile and
+//                output columns [w d/4, (w+1) d/4) of dK, dV, dQ
+//   warp 16      TMA producer (K^_j, V_j once; dO_i, Q^_i, dO^_i per tile)
+//   warp 17      TMEM allocation and the MMA-issuing thread
+//   warp 18      dQ reducer: bulk reduce-add of each staged dQ tile
+//   warp 19      idle (completes the fifth warpgroup: 640 threads launch with
+//                96 registers each; that warpgroup drops to kRegsLow and the
+//                compute warpgroups rise to kRegsHigh)
+// TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d),
+// dQ [0,d) (reusing S^T once P is consumed).
+// Per tile i (MMAs in issue order; the compute passes between them):
+//   pass 1  P = 2^(S sQ sK scale log2e - LSE_i log2e), dS = P (dP - D_i), both
 //           written back to TMEM in place; row max of P, tile max of |dS|
-//   pass 2  code(P^T) per key row (scale max P / 127), code(dS) per tile
-//           (scale max|dS| / 127) into swizzled shared-memory A operands
-//   MMA   dK = dS^T Q^_i, dQ = dS K^_j, dV = P^T dO^_i (all exact integer products)
-//   pass 3  dequantize: dV += sP sdO [.], dK += scale sdS sQ [.],
-//           dQ_acc += scale sdS sK [.] (FP32 reduction to global)
+//   pass 2a code(P^T) per key row (scale max P / 127) -> shared A tile
+//     MMA  dV = P^T dO^_i
+//   pass 2b code(dS) per tile (scale max|dS| / 127) -> shared A tile
+//     MMA  dK = dS^T Q^_i, dQ = dS K^_j
+//     MMA  next tile's dP^T = V_j dO_i+1^T (BF16), then S^T = K^_j Q^_i+1^T once
+//          the dQ tile has been read (they overlap pass 3)
+//   pass 3  dequantize: dQ tile * scale sdS sK -> FP32 staging tile (reduced
+//           into global by the reducer warp); dV += sP sdO [.], dK += scale sdS sQ [.]
 #include "kernel_common.cuh"
 
 namespace sagebwd {
 namespace {
+
+constexpr int kNWG = 4;                      // compute warpgroups
+constexpr int kCompute = kNWG * 128;          // compute threads
+constexpr int kThreads = kCompute + 128;      // + the producer / MMA / reducer warpgroup
+constexpr int kQC = 128 / kNWG;               // query columns per compute thread
+constexpr uint32_t kRegsLaunch = 96, kRegsLow = 64, kRegsHigh = 104;
+static_assert(128 * kRegsLow + kCompute * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
 
 template <int D>
 struct BwdCfg {
@@ -42,33 +52,29 @@ struct BwdCfg {
   static constexpr int OFF_Q = OFF_V + TILE;
   static constexpr int OFF_DO = OFF_Q + NS * TILE;
   static constexpr int OFF_DOQ = OFF_DO + NS * TILE;
-  static constexpr int OFF_PT = OFF_DOQ + NS * TILE;
+  static constexpr int OFF_PT = OFF_DOQ + NS * TILE;  // P^T codes; with dS^T: the dQ staging tile
   static constexpr int OFF_DST = OFF_PT + PTILE;
   static constexpr int OFF_VEC = OFF_DST + PTILE;  // L2[128], Dv[128], pmax bits[128], am[16]
   static constexpr int OFF_BAR = OFF_VEC + (128 + 128 + 128 + 16) * 4;
-  static constexpr int NBAR = 1 + 6 * NS + 4 + 2 + 1;
+  static constexpr int NBAR = 1 + 6 * NS + 10 + 1;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
-  // The tiles need a 1024-byte aligned base; the D = 128 layout leaves no room for padding.
+  // The tiles need a 1024-byte aligned base; the d = 128 layout leaves no room for padding.
   static constexpr int SMEM = BYTES + 1024 <= 232448 ? BYTES + 1024 : BYTES;
   static constexpr int C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D, C_DQ = 0;
   static_assert(BYTES <= 232448, "shared memory beyond the per-CTA limit");
+  static_assert(128 * D * 4 <= 2 * PTILE, "the FP32 dQ staging tile must fit in the two code tiles");
 };
 
-constexpr int kNWG = 4;                      // compute warpgroups
-constexpr int kCompute = kNWG * 128;          // compute threads
-constexpr int kThreads = kCompute + 128;      // + the producer / MMA warpgroup
-constexpr int kQC = 128 / kNWG;               // query columns per compute thread
-constexpr uint32_t kRegsLaunch = 96, kRegsLow = 32, kRegsHigh = 112;
-static_assert(128 * kRegsLow + kCompute * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
-
 enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty, bSiteDOQFull, bSiteDOQEmpty,
-               bSiteSDP, bSiteDSReady, bSiteAcc, bSiteTmemFree, bSiteAlign, bSiteC1, bSiteC2 };
+               bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAcc, bSiteDQRead, bSiteTmemFree, bSiteDQStaged,
+               bSiteStagingFree, bSiteC1, bSiteC2, bSiteAlign };
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-               const __grid_constant__ CUtensorMap tmDOQ, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tmDOQ, const __grid_constant__ CUtensorMap tmDQ,
+               const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -80,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   float* L2v = reinterpret_cast<float*>(smem + C::OFF_VEC);
   float* Dv = L2v + 128;
-  int* pmx = reinterpret_cast<int*>(Dv + 128);  // [128] row maxima of P (P >= 0: float bits order as ints)
+  int* pmx = reinterpret_cast<int*>(Dv + 128);      // [128] row maxima of P (P >= 0: float bits order as ints)
   float* am = reinterpret_cast<float*>(pmx + 128);  // [16] per-warp maxima of |dS|
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* bar_kv = bars;
@@ -90,12 +96,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_do_empty = bar_do_full + NS;
   uint64_t* bar_doq_full = bar_do_empty + NS;
   uint64_t* bar_doq_empty = bar_doq_full + NS;
-  uint64_t* bar_sdp = bar_doq_empty + NS;
-  uint64_t* bar_ds_ready = bar_sdp + 1;
-  uint64_t* bar_acc = bar_ds_ready + 1;
-  uint64_t* bar_tmem_free = bar_acc + 1;
-  uint64_t* bar_c1 = bar_tmem_free + 1;  // compute threads: LSE / D of the tile stored
-  uint64_t* bar_c2 = bar_c1 + 1;         // compute threads: row and tile maxima stored
+  uint64_t* bar_sdp = bar_doq_empty + NS;          // S^T and dP^T of the tile are in TMEM
+  uint64_t* bar_pt_ready = bar_sdp + 1;            // P^T codes written (compute)
+  uint64_t* bar_ds_ready = bar_pt_ready + 1;       // dS codes written, P / dS reads done (compute)
+  uint64_t* bar_acc = bar_ds_ready + 1;            // dV, dK, dQ tiles in TMEM
+  uint64_t* bar_dq_read = bar_acc + 1;             // dQ tile read out of TMEM (compute)
+  uint64_t* bar_tmem_free = bar_dq_read + 1;       // dV, dK tiles read out of TMEM (compute)
+  uint64_t* bar_dq_staged = bar_tmem_free + 1;     // FP32 dQ tile written to the staging tile (compute)
+  uint64_t* bar_staging_free = bar_dq_staged + 1;  // staging tile read by the reduce (reducer)
+  uint64_t* bar_c1 = bar_staging_free + 1;         // compute threads: LSE / D of the tile stored
+  uint64_t* bar_c2 = bar_c1 + 1;                   // compute threads: row and tile maxima stored
   uint64_t* bar_final = bar_c2 + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_final + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -122,9 +132,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_doq_empty + s, 1);
     }
     mbar_init(bar_sdp, 1);
+    mbar_init(bar_pt_ready, kCompute);
     mbar_init(bar_ds_ready, kCompute);
     mbar_init(bar_acc, 1);
+    mbar_init(bar_dq_read, kCompute);
     mbar_init(bar_tmem_free, kCompute);
+    mbar_init(bar_dq_staged, kCompute);
+    mbar_init(bar_staging_free, 1);
     mbar_init(bar_c1, kCompute);
     mbar_init(bar_c2, kCompute);
     mbar_init(bar_final, 1);
@@ -140,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
   if (warp >= 16) {
     setmaxnreg_dec<kRegsLow>();
     if (warp == 16 && lane == 0) {
@@ -185,33 +200,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idQM = idesc_bf16_f32(128, D, true, true);      // dQ: A MN-major, B MN-major
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       const uint32_t sPT = smem_u32(smem + C::OFF_PT), sDST = smem_u32(smem + C::OFF_DST);
-      bool ok = wait1(wc, bar_kv, 0, bSiteKV);
-      for (int it = 0; ok && it < T; ++it) {
-        const int s = it % NS;
-        const uint32_t ph = (it / NS) & 1;
-        const uint32_t sQ = smem_u32(smem + C::OFF_Q + s * C::TILE);
+      auto issue_dp = [&](int s) {
         const uint32_t sDO = smem_u32(smem + C::OFF_DO + s * C::TILE);
-        const uint32_t sDOQ = smem_u32(smem + C::OFF_DOQ + s * C::TILE);
-        if (!wait1(wc, bar_q_full + s, ph, bSiteQFull)) break;
-        if (!wait1(wc, bar_do_full + s, ph, bSiteDOFull)) break;
-        if (it >= 1 && !wait1(wc, bar_tmem_free, (it - 1) & 1, bSiteTmemFree)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + C::C_S, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idSS, kk > 0);
-        }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           umma_ss(tmem + C::C_DP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idSS, kk > 0);
         }
-        umma_commit(bar_sdp);
         umma_commit(bar_do_empty + s);
-        if (!wait1(wc, bar_ds_ready, it & 1, bSiteDSReady)) break;
-        if (!wait1(wc, bar_doq_full + s, ph, bSiteDOQFull)) break;
+      };
+      auto issue_s = [&](int s) {
+        const uint32_t sQ = smem_u32(smem + C::OFF_Q + s * C::TILE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_ss(tmem + C::C_S, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idSS, kk > 0);
+        }
+        umma_commit(bar_sdp);  // also covers the dP^T issued before it
+      };
+      bool ok = wait1(wc, bar_kv, 0, bSiteKV) && wait1(wc, bar_do_full, 0, bSiteDOFull) &&
+                wait1(wc, bar_q_full, 0, bSiteQFull);
+      if (ok) {
         tc_fence_after();
+        issue_dp(0);
+        issue_s(0);
+      }
+      for (int it = 0; ok && it < T; ++it) {
+        const int s = it % NS;
+        const uint32_t ph = (it / NS) & 1;
+        // dV = P^T dO^  (A: P^T tile [key][query], K-major; B: dO^ [query][d], MN-major)
+        if (!wait1(wc, bar_pt_ready, it & 1, bSitePTReady)) break;
+        if (!wait1(wc, bar_doq_full + s, ph, bSiteDOQFull)) break;
+        if (it >= 1 && !wait1(wc, bar_tmem_free, (it - 1) & 1, bSiteTmemFree)) break;
+        tc_fence_after();
+        const uint32_t sDOQ = smem_u32(smem + C::OFF_DOQ + s * C::TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + C::C_DV, sdesc_sw128(sPT + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                  sdesc_sw128(sDOQ + kk * 2048, 16384, 1024), idKM, kk > 0);
+        umma_commit(bar_doq_empty + s);
         // dK = dS^T Q^  (A: dS^T tile [key][query], K-major; B: Q^ [query][d], MN-major)
+        if (!wait1(wc, bar_ds_ready, it & 1, bSiteDSReady)) break;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(smem + C::OFF_Q + s * C::TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + C::C_DK, sdesc_sw128(sDST + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
@@ -222,16 +253,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + C::C_DQ, sdesc_sw128(sDST + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024),
                   idQM, kk > 0);
-        // dV = P^T dO^  (A: P^T tile [key][query], K-major; B: dO^ [query][d], MN-major)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + C::C_DV, sdesc_sw128(sPT + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                  sdesc_sw128(sDOQ + kk * 2048, 16384, 1024), idKM, kk > 0);
-        umma_commit(bar_doq_empty + s);
         umma_commit(bar_acc);
+        // the next tile's dP^T now (its columns are free), its S^T once the dQ tile is read
+        if (it + 1 < T) {
+          const int s2 = (it + 1) % NS;
+          const uint32_t ph2 = ((it + 1) / NS) & 1;
+          if (!wait1(wc, bar_do_full + s2, ph2, bSiteDOFull)) break;
+          tc_fence_after();
+          issue_dp(s2);
+          if (!wait1(wc, bar_q_full + s2, ph2, bSiteQFull)) break;
+          if (!wait1(wc, bar_dq_read, it & 1, bSiteDQRead)) break;
+          tc_fence_after();
+          issue_s(s2);
+        }
       }
+      // Every MMA issued above must complete before TMEM is released.
       umma_commit(bar_final);
       drain(bar_final, 0, p.timeout_ns);
+    } else if (warp == 18 && lane == 0) {
+      // ---------------------------------------------------------- dQ reducer
+      const uint8_t* staging = smem + C::OFF_PT;
+      for (int it = 0; it < T; ++it) {
+        if (!wait1(wc, bar_dq_staged, it & 1, bSiteDQStaged)) break;
+        const int bhq = b * p.Hq + hk * p.G + it / nq;
+        const int i0 = (ib0 + it % nq) * kBlk;
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx) tma_reduce_add_3d(&tmDQ, staging + bx * 16384, bx * 32, i0, bhq);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(bar_staging_free);
+      }
+      bulk_wait_group0();
     }
   } else {
     setmaxnreg_inc<kRegsHigh>();
@@ -244,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kglob = k0 + r;
     const bool key_ok = kglob < p.N;
     const float sKv = p.sk[(size_t)bhk * p.nb + j];
+    const uint32_t pt_base = smem_u32(smem + C::OFF_PT), ds_base = smem_u32(smem + C::OFF_DST);
     float dv_run[DC], dk_run[DC];
 #pragma unroll
     for (int c = 0; c < DC; ++c) dv_run[c] = dk_run[c] = 0.f;
@@ -252,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bhq = b * p.Hq + hk * p.G + it / nq;
       const int ib = ib0 + it % nq;
       const int i0 = ib * kBlk;
-      // LSE (base 2) and D of the tile's queries; +inf / 0 past N
+      // LSE (base 2) and D of the tile's queries (+inf / 0 past N); reset the row maxima
       {
         const int q = ct & 127;
         const bool in = i0 + q < p.N;
@@ -263,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else if (ct < 384)
           pmx[q] = 0;
       }
-      // (an mbarrier rather than bar.sync, so that this wait is bounded too)
+      // (mbarriers rather than bar.sync, so that these waits are bounded too)
       mbar_arrive(bar_c1);
       if (!waitw(wc, bar_c1, it & 1, bSiteC1)) break;
       const float qks = __fmul_rn(__fmul_rn(p.sq[(size_t)bhq * p.nb + ib], sKv), p.c0);
@@ -278,12 +331,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sv[8], dpv[8];        // S -> P and dP -> dS, converted in place
         tmem_ld8(tmem + lane_base + C::C_S + col, sv);
         tmem_ld8(tmem + lane_base + C::C_DP + col, dpv);
+        const float4 la = *reinterpret_cast<const float4*>(L2v + col);
+        const float4 lb = *reinterpret_cast<const float4*>(L2v + col + 4);
+        const float4 da = *reinterpret_cast<const float4*>(Dv + col);
+        const float4 db = *reinterpret_cast<const float4*>(Dv + col + 4);
+        const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+        const float dvv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          float pr = ex2_approx(fmaf(__uint_as_float(sv[e]), qks, -L2v[col + e]));
+          float pr = ex2_approx(fmaf(__uint_as_float(sv[e]), qks, -lv[e]));
           if (!key_ok || (diag && col + e < r)) pr = 0.f;
-          const float ds = pr * (__uint_as_float(dpv[e]) - Dv[col + e]);
+          const float ds = pr * (__uint_as_float(dpv[e]) - dvv[e]);
           pmax = fmaxf(pmax, pr);
           amax = fmaxf(amax, fabsf(ds));
           sv[e] = __float_as_uint(pr);
@@ -308,37 +367,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sPc = p_live ? __fdiv_rn(cmax, 127.f) : 0.f;
       const float invA = d_live ? __fdiv_rn(127.f, a) : 0.f;
       const float sDS = d_live ? __fdiv_rn(a, 127.f) : 0.f;
-      // pass 2: codes into the swizzled A tiles (row = key r, 16-byte chunk = 8 queries)
-      const uint32_t pt_base = smem_u32(smem + C::OFF_PT), ds_base = smem_u32(smem + C::OFF_DST);
+      // the code tiles double as the dQ staging tile: wait until the last reduce has read it
+      if (it >= 1 && !waitw(wc, bar_staging_free, (it - 1) & 1, bSiteStagingFree)) break;
+      // pass 2a: codes of P^T into the swizzled A tile (row = key r, 16-byte chunk = 8 queries)
 #pragma unroll
       for (int c0 = 0; c0 < kQC; c0 += 8) {
         const int col = kQC * w + c0;
-        uint32_t pv[8], dsv[8];
+        uint32_t pv[8];
         tmem_ld8(tmem + lane_base + C::C_S + col, pv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 8; e += 2)
+          pv[e >> 1] = pack_bf16x2(rint_f32(__fmul_rn(__uint_as_float(pv[e]), invP)),
+                                   rint_f32(__fmul_rn(__uint_as_float(pv[e + 1]), invP)));
+        st_shared_v4(pt_base + sw128_offset(r, col >> 3), pv[0], pv[1], pv[2], pv[3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar_pt_ready);
+      // pass 2b: codes of dS (one scale per tile)
+#pragma unroll
+      for (int c0 = 0; c0 < kQC; c0 += 8) {
+        const int col = kQC * w + c0;
+        uint32_t dsv[8];
         tmem_ld8(tmem + lane_base + C::C_DP + col, dsv);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          pv[e >> 1] = pack_bf16x2(rint_f32(__fmul_rn(__uint_as_float(pv[e]), invP)),
-                                   rint_f32(__fmul_rn(__uint_as_float(pv[e + 1]), invP)));
+        for (int e = 0; e < 8; e += 2)
           dsv[e >> 1] = pack_bf16x2(rint_f32(__fmul_rn(__uint_as_float(dsv[e]), invA)),
                                     rint_f32(__fmul_rn(__uint_as_float(dsv[e + 1]), invA)));
-        }
-        const uint32_t off = sw128_offset(r, col >> 3);
-        st_shared_v4(pt_base + off, pv[0], pv[1], pv[2], pv[3]);
-        st_shared_v4(ds_base + off, dsv[0], dsv[1], dsv[2], dsv[3]);
+        st_shared_v4(ds_base + sw128_offset(r, col >> 3), dsv[0], dsv[1], dsv[2], dsv[3]);
       }
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar_ds_ready);
       if (!waitw(wc, bar_acc, it & 1, bSiteAcc)) break;
       tc_fence_after();
-      // pass 3: dequantize the three integer tiles
+      // pass 3a: dQ tile (lane r = query row i0 + r) -> scaled FP32 staging tile, D/32 boxes of
+      // [128 rows][32 floats] with the 128-byte swizzle, reduced into global by the reducer warp
+      const float fq = __fmul_rn(__fmul_rn(p.sc, sDS), sKv);
+#pragma unroll
+      for (int c0 = 0; c0 < DC; c0 += 8) {
+        uint32_t v[8];
+        tmem_ld8(tmem + lane_base + C::C_DQ + w * DC + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int col = w * DC + c0 + 4 * h;
+          const uint32_t off = (uint32_t)((col >> 5) * 16384 + r * 128 + ((((col & 31) >> 2) ^ (r & 7)) << 4));
+          st_shared_v4(pt_base + off, __float_as_uint(fq * __uint_as_float(v[4 * h])),
+                       __float_as_uint(fq * __uint_as_float(v[4 * h + 1])),
+                       __float_as_uint(fq * __uint_as_float(v[4 * h + 2])),
+                       __float_as_uint(fq * __uint_as_float(v[4 * h + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_dq_read);
+      fence_proxy_async_smem();
+      mbar_arrive(bar_dq_staged);
+      // pass 3b: dV and dK tiles into the running sums
       const float fv = __fmul_rn(sPc, p.sdo[(size_t)bhq * p.nb + ib]);
       const float fk = __fmul_rn(__fmul_rn(p.sc, sDS), p.sq[(size_t)bhq * p.nb + ib]);
-      const float fq = __fmul_rn(__fmul_rn(p.sc, sDS), sKv);
-      const int qrow = i0 + r;  // dQ tile: lane r is query row i0 + r
-      float* dq_dst = p.dq_acc + ((size_t)bhq * p.N + qrow) * D + w * DC;
 #pragma unroll
       for (int c0 = 0; c0 < DC; c0 += 16) {
         uint32_t v[16];
@@ -350,14 +438,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) dk_run[c0 + e] = fmaf(fk, __uint_as_float(v[e]), dk_run[c0 + e]);
-        tmem_ld16(tmem + lane_base + C::C_DQ + w * DC + c0, v);
-        tmem_ld_wait();
-        if (qrow < p.N) {
-#pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            red_add_v4_f32(dq_dst + c0 + e, fq * __uint_as_float(v[e]), fq * __uint_as_float(v[e + 1]),
-                           fq * __uint_as_float(v[e + 2]), fq * __uint_as_float(v[e + 3]));
-        }
       }
       tc_fence_before();
       mbar_arrive(bar_tmem_free);
@@ -384,25 +464,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                         const CUtensorMap& tdoq, const BwdParams& p, cudaStream_t s) {
+                         const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s) {
   using C = BwdCfg<D>;
   auto kern = bwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = p.nb * p.B * p.Hkv;
-  kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, p);
+  kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tdoq, const BwdParams& p, int d, int causal, cudaStream_t s) {
+                       const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, int d, int causal,
+                       cudaStream_t s) {
   if (d == 64)
-    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdoq, p, s)
-                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdoq, p, s);
-  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdoq, p, s)
-                : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdoq, p, s);
+    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdoq, tdq, p, s)
+                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdoq, tdq, p, s);
+  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdoq, tdq, p, s)
+                : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdoq, tdq, p, s);
 }
 
 }  // namespace sagebwd

@@ -92,6 +92,7 @@ struct BwdParams {
   uint32_t flags;
 };
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tdoq, const BwdParams& p, int d, int causal, cudaStream_t s);
+                       const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, int d, int causal,
+                       cudaStream_t s);
 
 }  // namespace sagebwd
