@@ -56,7 +56,7 @@ struct BwdCfg {
   static constexpr int OFF_DST = OFF_PT + PTILE;
   static constexpr int OFF_VEC = OFF_DST + PTILE;  // L2[128], Dv[128], pmax bits[128], am[16]
   static constexpr int OFF_BAR = OFF_VEC + (128 + 128 + 128 + 16) * 4;
-  static constexpr int NBAR = 1 + 6 * NS + 10 + 1;
+  static constexpr int NBAR = 1 + 6 * NS + 12 + 1;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
   // The tiles need a 1024-byte aligned base; the d = 128 layout leaves no room for padding.
   static constexpr int SMEM = BYTES + 1024 <= 232448 ? BYTES + 1024 : BYTES;
@@ -66,8 +66,8 @@ struct BwdCfg {
 };
 
 enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty, bSiteDOQFull, bSiteDOQEmpty,
-               bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAcc, bSiteDQRead, bSiteTmemFree, bSiteDQStaged,
-               bSiteStagingFree, bSiteC1, bSiteC2, bSiteAlign };
+               bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAccV, bSiteAccQ, bSiteDQRead, bSiteTmemFree, bSiteDQStaged,
+               bSiteStagingFree, bSiteStagingFree2, bSiteC1, bSiteC2, bSiteAlign };
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -99,12 +99,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_sdp = bar_doq_empty + NS;          // S^T and dP^T of the tile are in TMEM
   uint64_t* bar_pt_ready = bar_sdp + 1;            // P^T codes written (compute)
   uint64_t* bar_ds_ready = bar_pt_ready + 1;       // dS codes written, P / dS reads done (compute)
-  uint64_t* bar_acc = bar_ds_ready + 1;            // dV, dK, dQ tiles in TMEM
-  uint64_t* bar_dq_read = bar_acc + 1;             // dQ tile read out of TMEM (compute)
+  uint64_t* bar_acc_v = bar_ds_ready + 1;          // dV tile in TMEM
+  uint64_t* bar_acc_q = bar_acc_v + 1;             // dK and dQ tiles in TMEM
+  uint64_t* bar_dq_read = bar_acc_q + 1;           // dQ tile read out of TMEM (compute)
   uint64_t* bar_tmem_free = bar_dq_read + 1;       // dV, dK tiles read out of TMEM (compute)
   uint64_t* bar_dq_staged = bar_tmem_free + 1;     // FP32 dQ tile written to the staging tile (compute)
-  uint64_t* bar_staging_free = bar_dq_staged + 1;  // staging tile read by the reduce (reducer)
-  uint64_t* bar_c1 = bar_staging_free + 1;         // compute threads: LSE / D of the tile stored
+  uint64_t* bar_staging_free = bar_dq_staged + 1;  // staging half in the P^T tile read by the reduce (reducer)
+  uint64_t* bar_staging_free2 = bar_staging_free + 1;  // staging half in the dS^T tile read (reducer)
+  uint64_t* bar_c1 = bar_staging_free2 + 1;        // compute threads: LSE / D of the tile stored
   uint64_t* bar_c2 = bar_c1 + 1;                   // compute threads: row and tile maxima stored
   uint64_t* bar_final = bar_c2 + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_final + 1);
@@ -134,11 +136,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_sdp, 1);
     mbar_init(bar_pt_ready, kCompute);
     mbar_init(bar_ds_ready, kCompute);
-    mbar_init(bar_acc, 1);
+    mbar_init(bar_acc_v, 1);
+    mbar_init(bar_acc_q, 1);
     mbar_init(bar_dq_read, kCompute);
     mbar_init(bar_tmem_free, kCompute);
     mbar_init(bar_dq_staged, kCompute);
     mbar_init(bar_staging_free, 1);
+    mbar_init(bar_staging_free2, 1);
     mbar_init(bar_c1, kCompute);
     mbar_init(bar_c2, kCompute);
     mbar_init(bar_final, 1);
@@ -198,24 +202,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       const uint32_t idKM = idesc_bf16_f32(128, D, false, true);     // dK, dV: A K-major, B MN-major
       const uint32_t idQM = idesc_bf16_f32(128, D, true, true);      // dQ: A MN-major, B MN-major
-      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      const uint32_t sPT = smem_u32(smem + C::OFF_PT), sDST = smem_u32(smem + C::OFF_DST);
+      // Descriptor low words are built once per buffer; the chained MMAs add the per-K-step
+      // offsets (no carry: shared addresses stay below 2^18).
+      const uint32_t dK_k = sdesc_sw128_lo(smem_u32(smem + C::OFF_K), 16);
+      const uint32_t dK_mn = sdesc_sw128_lo(smem_u32(smem + C::OFF_K), 16384);
+      const uint32_t dV_k = sdesc_sw128_lo(smem_u32(smem + C::OFF_V), 16);
+      const uint32_t dPT_k = sdesc_sw128_lo(smem_u32(smem + C::OFF_PT), 16);
+      const uint32_t dDS_k = sdesc_sw128_lo(smem_u32(smem + C::OFF_DST), 16);
+      const uint32_t dDS_mn = sdesc_sw128_lo(smem_u32(smem + C::OFF_DST), 16384);
+      auto dQ_k = [&](int st) { return sdesc_sw128_lo(smem_u32(smem + C::OFF_Q + st * C::TILE), 16); };
+      auto dQ_mn = [&](int st) { return sdesc_sw128_lo(smem_u32(smem + C::OFF_Q + st * C::TILE), 16384); };
+      auto dDO_k = [&](int st) { return sdesc_sw128_lo(smem_u32(smem + C::OFF_DO + st * C::TILE), 16); };
+      auto dDOQ_mn = [&](int st) { return sdesc_sw128_lo(smem_u32(smem + C::OFF_DOQ + st * C::TILE), 16384); };
+      auto chain_kk = [&](uint32_t d_col, uint32_t a_lo, uint32_t b_lo, uint32_t idesc) {
+        if constexpr (D == 128)
+          umma_chain8_kk(tmem + d_col, sdesc_from_lo(a_lo), sdesc_from_lo(b_lo), idesc);
+        else
+          umma_chain4_kk(tmem + d_col, sdesc_from_lo(a_lo), sdesc_from_lo(b_lo), idesc);
+      };
       auto issue_dp = [&](int s) {
-        const uint32_t sDO = smem_u32(smem + C::OFF_DO + s * C::TILE);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + C::C_DP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idSS, kk > 0);
-        }
+        chain_kk(C::C_DP, dV_k, dDO_k(s), idSS);
         umma_commit(bar_do_empty + s);
       };
       auto issue_s = [&](int s) {
-        const uint32_t sQ = smem_u32(smem + C::OFF_Q + s * C::TILE);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + C::C_S, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idSS, kk > 0);
-        }
+        chain_kk(C::C_S, dK_k, dQ_k(s), idSS);
         umma_commit(bar_sdp);  // also covers the dP^T issued before it
       };
       bool ok = wait1(wc, bar_kv, 0, bSiteKV) && wait1(wc, bar_do_full, 0, bSiteDOFull) &&
@@ -233,27 +243,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait1(wc, bar_doq_full + s, ph, bSiteDOQFull)) break;
         if (it >= 1 && !wait1(wc, bar_tmem_free, (it - 1) & 1, bSiteTmemFree)) break;
         tc_fence_after();
-        const uint32_t sDOQ = smem_u32(smem + C::OFF_DOQ + s * C::TILE);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + C::C_DV, sdesc_sw128(sPT + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                  sdesc_sw128(sDOQ + kk * 2048, 16384, 1024), idKM, kk > 0);
+        umma_chain8_km(tmem + C::C_DV, sdesc_from_lo(dPT_k), sdesc_from_lo(dDOQ_mn(s)), idKM);
         umma_commit(bar_doq_empty + s);
+        umma_commit(bar_acc_v);
         // dK = dS^T Q^  (A: dS^T tile [key][query], K-major; B: Q^ [query][d], MN-major)
         if (!wait1(wc, bar_ds_ready, it & 1, bSiteDSReady)) break;
         tc_fence_after();
-        const uint32_t sQ = smem_u32(smem + C::OFF_Q + s * C::TILE);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + C::C_DK, sdesc_sw128(sDST + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                  sdesc_sw128(sQ + kk * 2048, 16384, 1024), idKM, kk > 0);
+        umma_chain8_km(tmem + C::C_DK, sdesc_from_lo(dDS_k), sdesc_from_lo(dQ_mn(s)), idKM);
         umma_commit(bar_q_empty + s);
         // dQ = dS K^  (A: the same dS^T tile read MN-major as [query][key]; B: K^ [key][d], MN-major)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + C::C_DQ, sdesc_sw128(sDST + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024),
-                  idQM, kk > 0);
-        umma_commit(bar_acc);
+        umma_chain8_mm(tmem + C::C_DQ, sdesc_from_lo(dDS_mn), sdesc_from_lo(dK_mn), idQM);
+        umma_commit(bar_acc_q);
         // the next tile's dP^T now (its columns are free), its S^T once the dQ tile is read
         if (it + 1 < T) {
           const int s2 = (it + 1) % NS;
@@ -272,16 +272,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain(bar_final, 0, p.timeout_ns);
     } else if (warp == 18 && lane == 0) {
       // ---------------------------------------------------------- dQ reducer
+      // The FP32 dQ tile is staged as D/32 boxes of [128 rows][32 floats]: the first half of
+      // the boxes in the P^T code tile, the second half in the dS^T code tile.  Each half is
+      // its own bulk group, so the P^T tile is released as soon as its half has been read.
       const uint8_t* staging = smem + C::OFF_PT;
+      const uint8_t* staging2 = smem + C::OFF_DST;
       for (int it = 0; it < T; ++it) {
         if (!wait1(wc, bar_dq_staged, it & 1, bSiteDQStaged)) break;
         const int bhq = b * p.Hq + hk * p.G + it / nq;
         const int i0 = (ib0 + it % nq) * kBlk;
 #pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx) tma_reduce_add_3d(&tmDQ, staging + bx * 16384, bx * 32, i0, bhq);
+        for (int bx = 0; bx < D / 64; ++bx) tma_reduce_add_3d(&tmDQ, staging + bx * 16384, bx * 32, i0, bhq);
         bulk_commit_group();
-        bulk_wait_group_read0();
+#pragma unroll
+        for (int bx = D / 64; bx < D / 32; ++bx)
+          tma_reduce_add_3d(&tmDQ, staging2 + (bx - D / 64) * 16384, bx * 32, i0, bhq);
+        bulk_commit_group();
+        bulk_wait_group_read<1>();
         mbar_arrive(bar_staging_free);
+        bulk_wait_group_read<0>();
+        mbar_arrive(bar_staging_free2);
       }
       bulk_wait_group0();
     }
@@ -301,52 +311,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int c = 0; c < DC; ++c) dv_run[c] = dk_run[c] = 0.f;
 
+    // Per-tile LSE (base 2) / D values and block scales, loaded one tile ahead so
+    // that their global-memory latency hides behind the current tile.
+    const int q_own = ct & 127;
+    auto tile_vec = [&](int t) -> float {
+      const int bq = b * p.Hq + hk * p.G + t / nq;
+      const int row = (ib0 + t % nq) * kBlk + q_own;
+      const bool in = row < p.N;
+      if (ct < 128) return in ? __fmul_rn(p.lse[(size_t)bq * p.N + row], kLog2e) : INFINITY;
+      if (ct < 256) return in ? p.D[(size_t)bq * p.N + row] : 0.f;
+      return 0.f;
+    };
+    auto tile_sq = [&](int t) { return p.sq[(size_t)(b * p.Hq + hk * p.G + t / nq) * p.nb + ib0 + t % nq]; };
+    auto tile_sdo = [&](int t) { return p.sdo[(size_t)(b * p.Hq + hk * p.G + t / nq) * p.nb + ib0 + t % nq]; };
+    float pf_vec = tile_vec(0), pf_sq = tile_sq(0), pf_sdo = tile_sdo(0);
+
     for (int it = 0; it < T; ++it) {
       const int bhq = b * p.Hq + hk * p.G + it / nq;
       const int ib = ib0 + it % nq;
       const int i0 = ib * kBlk;
+      (void)i0;
       // LSE (base 2) and D of the tile's queries (+inf / 0 past N); reset the row maxima
-      {
-        const int q = ct & 127;
-        const bool in = i0 + q < p.N;
-        if (ct < 128)
-          L2v[q] = in ? __fmul_rn(p.lse[(size_t)bhq * p.N + i0 + q], kLog2e) : INFINITY;
-        else if (ct < 256)
-          Dv[q] = in ? p.D[(size_t)bhq * p.N + i0 + q] : 0.f;
-        else if (ct < 384)
-          pmx[q] = 0;
+      if (ct < 128)
+        L2v[q_own] = pf_vec;
+      else if (ct < 256)
+        Dv[q_own] = pf_vec;
+      else if (ct < 384)
+        pmx[q_own] = 0;
+      const float sQt = pf_sq, sdOt = pf_sdo;
+      if (it + 1 < T) {
+        pf_vec = tile_vec(it + 1);
+        pf_sq = tile_sq(it + 1);
+        pf_sdo = tile_sdo(it + 1);
       }
       // (mbarriers rather than bar.sync, so that these waits are bounded too)
       mbar_arrive(bar_c1);
       if (!waitw(wc, bar_c1, it & 1, bSiteC1)) break;
-      const float qks = __fmul_rn(__fmul_rn(p.sq[(size_t)bhq * p.nb + ib], sKv), p.c0);
+      const float qks = __fmul_rn(__fmul_rn(sQt, sKv), p.c0);
       const bool diag = CAUSAL && ib == j;
       if (!waitw(wc, bar_sdp, it & 1, bSiteSDP)) break;
       tc_fence_after();
       // pass 1
       float pmax = 0.f, amax = 0.f;
+      const bool masked = diag || (k0 + kBlk > p.N);
 #pragma unroll
       for (int c0 = 0; c0 < kQC; c0 += 8) {
         const int col = kQC * w + c0;  // query column within the tile
         uint32_t sv[8], dpv[8];        // S -> P and dP -> dS, converted in place
         tmem_ld8(tmem + lane_base + C::C_S + col, sv);
         tmem_ld8(tmem + lane_base + C::C_DP + col, dpv);
-        const float4 la = *reinterpret_cast<const float4*>(L2v + col);
-        const float4 lb = *reinterpret_cast<const float4*>(L2v + col + 4);
-        const float4 da = *reinterpret_cast<const float4*>(Dv + col);
-        const float4 db = *reinterpret_cast<const float4*>(Dv + col + 4);
-        const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-        const float dvv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float pr = ex2_approx(fmaf(__uint_as_float(sv[e]), qks, -lv[e]));
-          if (!key_ok || (diag && col + e < r)) pr = 0.f;
-          const float ds = pr * (__uint_as_float(dpv[e]) - dvv[e]);
-          pmax = fmaxf(pmax, pr);
-          amax = fmaxf(amax, fabsf(ds));
-          sv[e] = __float_as_uint(pr);
-          dpv[e] = __float_as_uint(ds);
+        for (int e4 = 0; e4 < 8; e4 += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(L2v + col + e4);
+          const float4 d4 = *reinterpret_cast<const float4*>(Dv + col + e4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e1 = 0; e1 < 4; ++e1) {
+            const int e = e4 + e1;
+            float pr = ex2_approx(fmaf(__uint_as_float(sv[e]), qks, -lv[e1]));
+            if (masked) pr = (!key_ok || (diag && col + e < r)) ? 0.f : pr;
+            const float ds = pr * (__uint_as_float(dpv[e]) - dvv[e1]);
+            pmax = fmaxf(pmax, pr);
+            amax = fmaxf(amax, fabsf(ds));
+            sv[e] = __float_as_uint(pr);
+            dpv[e] = __float_as_uint(ds);
+          }
         }
         tmem_st8(tmem + lane_base + C::C_S + col, sv);
         tmem_st8(tmem + lane_base + C::C_DP + col, dpv);
@@ -363,70 +394,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q = 1; q < kCompute / 32; ++q) a = fmaxf(a, am[q]);
       const bool p_live = cmax >= kMinGroupMax, d_live = a >= kMinGroupMax;
-      const float invP = p_live ? __fdiv_rn(127.f, cmax) : 0.f;
-      const float sPc = p_live ? __fdiv_rn(cmax, 127.f) : 0.f;
-      const float invA = d_live ? __fdiv_rn(127.f, a) : 0.f;
-      const float sDS = d_live ? __fdiv_rn(a, 127.f) : 0.f;
-      // the code tiles double as the dQ staging tile: wait until the last reduce has read it
+      // hardware reciprocal (<= 2 ulp) rather than IEEE division: these scales only
+      // decide codes of this tile and dequantize it; a code at a rounding tie may differ
+      const float invP = p_live ? __fdividef(127.f, cmax) : 0.f;
+      const float sPc = p_live ? cmax * (1.f / 127.f) : 0.f;
+      const float invA = d_live ? __fdividef(127.f, a) : 0.f;
+      const float sDS = d_live ? a * (1.f / 127.f) : 0.f;
+      // the code tiles double as the dQ staging tile: wait until the last reduce has read its half
       if (it >= 1 && !waitw(wc, bar_staging_free, (it - 1) & 1, bSiteStagingFree)) break;
       // pass 2a: codes of P^T into the swizzled A tile (row = key r, 16-byte chunk = 8 queries)
+      {
 #pragma unroll
-      for (int c0 = 0; c0 < kQC; c0 += 8) {
-        const int col = kQC * w + c0;
-        uint32_t pv[8];
-        tmem_ld8(tmem + lane_base + C::C_S + col, pv);
-        tmem_ld_wait();
+        for (int h = 0; h < kQC; h += 16) {
+          uint32_t pv[16];
+          tmem_ld16(tmem + lane_base + C::C_S + kQC * w + h, pv);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 8; e += 2)
-          pv[e >> 1] = pack_bf16x2(rint_f32(__fmul_rn(__uint_as_float(pv[e]), invP)),
-                                   rint_f32(__fmul_rn(__uint_as_float(pv[e + 1]), invP)));
-        st_shared_v4(pt_base + sw128_offset(r, col >> 3), pv[0], pv[1], pv[2], pv[3]);
+          for (int e = 0; e < 16; e += 2)
+            pv[e >> 1] = pack_int_bf16x2(rint_small(__fmul_rn(__uint_as_float(pv[e]), invP)),
+                                         rint_small(__fmul_rn(__uint_as_float(pv[e + 1]), invP)));
+          st_shared_v4(pt_base + sw128_offset(r, ((kQC * w + h) >> 3)), pv[0], pv[1], pv[2], pv[3]);
+          st_shared_v4(pt_base + sw128_offset(r, ((kQC * w + h) >> 3) + 1), pv[4], pv[5], pv[6], pv[7]);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(bar_pt_ready);
       // pass 2b: codes of dS (one scale per tile)
+      if (it >= 1 && !waitw(wc, bar_staging_free2, (it - 1) & 1, bSiteStagingFree2)) break;
+      {
 #pragma unroll
-      for (int c0 = 0; c0 < kQC; c0 += 8) {
-        const int col = kQC * w + c0;
-        uint32_t dsv[8];
-        tmem_ld8(tmem + lane_base + C::C_DP + col, dsv);
-        tmem_ld_wait();
+        for (int h = 0; h < kQC; h += 16) {
+          uint32_t dsv[16];
+          tmem_ld16(tmem + lane_base + C::C_DP + kQC * w + h, dsv);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 8; e += 2)
-          dsv[e >> 1] = pack_bf16x2(rint_f32(__fmul_rn(__uint_as_float(dsv[e]), invA)),
-                                    rint_f32(__fmul_rn(__uint_as_float(dsv[e + 1]), invA)));
-        st_shared_v4(ds_base + sw128_offset(r, col >> 3), dsv[0], dsv[1], dsv[2], dsv[3]);
+          for (int e = 0; e < 16; e += 2)
+            dsv[e >> 1] = pack_int_bf16x2(rint_small(__fmul_rn(__uint_as_float(dsv[e]), invA)),
+                                          rint_small(__fmul_rn(__uint_as_float(dsv[e + 1]), invA)));
+          st_shared_v4(ds_base + sw128_offset(r, ((kQC * w + h) >> 3)), dsv[0], dsv[1], dsv[2], dsv[3]);
+          st_shared_v4(ds_base + sw128_offset(r, ((kQC * w + h) >> 3) + 1), dsv[4], dsv[5], dsv[6], dsv[7]);
+        }
       }
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar_ds_ready);
-      if (!waitw(wc, bar_acc, it & 1, bSiteAcc)) break;
-      tc_fence_after();
-      // pass 3a: dQ tile (lane r = query row i0 + r) -> scaled FP32 staging tile, D/32 boxes of
-      // [128 rows][32 floats] with the 128-byte swizzle, reduced into global by the reducer warp
+      // pass 3: dV first (its MMA finishes first), then dQ (frees the S^T columns for
+      // the next tile), then dK
+      const float fv = __fmul_rn(sPc, sdOt);
+      const float fk = __fmul_rn(__fmul_rn(p.sc, sDS), sQt);
       const float fq = __fmul_rn(__fmul_rn(p.sc, sDS), sKv);
-#pragma unroll
-      for (int c0 = 0; c0 < DC; c0 += 8) {
-        uint32_t v[8];
-        tmem_ld8(tmem + lane_base + C::C_DQ + w * DC + c0, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int col = w * DC + c0 + 4 * h;
-          const uint32_t off = (uint32_t)((col >> 5) * 16384 + r * 128 + ((((col & 31) >> 2) ^ (r & 7)) << 4));
-          st_shared_v4(pt_base + off, __float_as_uint(fq * __uint_as_float(v[4 * h])),
-                       __float_as_uint(fq * __uint_as_float(v[4 * h + 1])),
-                       __float_as_uint(fq * __uint_as_float(v[4 * h + 2])),
-                       __float_as_uint(fq * __uint_as_float(v[4 * h + 3])));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(bar_dq_read);
-      fence_proxy_async_smem();
-      mbar_arrive(bar_dq_staged);
-      // pass 3b: dV and dK tiles into the running sums
-      const float fv = __fmul_rn(sPc, p.sdo[(size_t)bhq * p.nb + ib]);
-      const float fk = __fmul_rn(__fmul_rn(p.sc, sDS), p.sq[(size_t)bhq * p.nb + ib]);
+      if (!waitw(wc, bar_acc_v, it & 1, bSiteAccV)) break;
+      tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < DC; c0 += 16) {
         uint32_t v[16];
@@ -434,6 +452,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) dv_run[c0 + e] = fmaf(fv, __uint_as_float(v[e]), dv_run[c0 + e]);
+      }
+      if (!waitw(wc, bar_acc_q, it & 1, bSiteAccQ)) break;
+      tc_fence_after();
+      // dQ tile (lane r = query row i0 + r) -> scaled FP32 staging tile, D/32 boxes of
+      // [128 rows][32 floats] with the 128-byte swizzle, reduced into global by the reducer warp
+#pragma unroll
+      for (int c0 = 0; c0 < DC; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_base + C::C_DQ + w * DC + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c4 = 0; c4 < 16; c4 += 4) {
+          const int col = w * DC + c0 + c4;
+          const int box = col >> 5;  // boxes [0, D/64) in the P^T tile, the rest in the dS^T tile
+          const uint32_t box_base = box < D / 64 ? pt_base + box * 16384 : ds_base + (box - D / 64) * 16384;
+          const uint32_t off = (uint32_t)(r * 128 + ((((col & 31) >> 2) ^ (r & 7)) << 4));
+          st_shared_v4(box_base + off, __float_as_uint(fq * __uint_as_float(v[c4])),
+                       __float_as_uint(fq * __uint_as_float(v[c4 + 1])), __float_as_uint(fq * __uint_as_float(v[c4 + 2])),
+                       __float_as_uint(fq * __uint_as_float(v[c4 + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_dq_read);
+      fence_proxy_async_smem();
+      mbar_arrive(bar_dq_staged);
+#pragma unroll
+      for (int c0 = 0; c0 < DC; c0 += 16) {
+        uint32_t v[16];
         tmem_ld16(tmem + lane_base + C::C_DK + w * DC + c0, v);
         tmem_ld_wait();
 #pragma unroll

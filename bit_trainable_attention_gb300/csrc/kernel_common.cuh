@@ -63,6 +63,19 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity, uint64_t l
   }
 }
 
+// Round to the nearest integer, ties to even, for |x| < 2^22, on the FMA pipe
+// (the classic magic-number method): adding 1.5 * 2^23 leaves no fraction bits,
+// so the IEEE round-to-nearest-even of the addition is the rounding of x, and
+// subtracting the constant again is exact.  Same result as rint(x) there.
+__device__ __forceinline__ float rint_small(float x) {
+  return __fsub_rn(__fadd_rn(x, 12582912.0f), 12582912.0f);
+}
+// Two integer-valued floats with |v| <= 256 are exact in BF16, whose bits are
+// the upper half of the FP32 bits: pack (lo, hi) into bf16x2 with one byte permute.
+__device__ __forceinline__ uint32_t pack_int_bf16x2(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }

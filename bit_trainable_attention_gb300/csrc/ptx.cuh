@@ -107,9 +107,10 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every committed bulk group of this thread has finished READING its shared-memory source.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// Wait until at most N committed bulk groups of this thread are still READING their shared-memory sources.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 // Wait until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -147,6 +148,98 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// ---------------------------------------------------------------- chained MMAs
+// One K loop of tcgen05.mma kind::f16 in a single asm block (the first MMA
+// overwrites D, the rest accumulate), so the issuing thread spends about three
+// instructions per MMA.  The descriptors advance in 16-byte units of the start
+// address: a K-major 128-byte-swizzled operand by 32 bytes per K step of 16
+// (and to the next 16 KB sub-tile every four steps), an MN-major one by 16
+// rows of 128 bytes.
+// 8 K steps, A and B K-major.
+__device__ __forceinline__ void umma_chain8_kk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p0, 0, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+      "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 1024;\n\tadd.s64 rb, %2, 1024;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 1026;\n\tadd.s64 rb, %2, 1026;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 1028;\n\tadd.s64 rb, %2, 1028;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 1030;\n\tadd.s64 rb, %2, 1030;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "}\n" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc)
+      : "memory");
+}
+// 4 K steps, A and B K-major.
+__device__ __forceinline__ void umma_chain4_kk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p0, 0, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+      "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "}\n" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc)
+      : "memory");
+}
+// 8 K steps, A K-major, B MN-major.
+__device__ __forceinline__ void umma_chain8_km(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p0, 0, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+      "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 128;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 256;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 384;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 1024;\n\tadd.s64 rb, %2, 512;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 1026;\n\tadd.s64 rb, %2, 640;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 1028;\n\tadd.s64 rb, %2, 768;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 1030;\n\tadd.s64 rb, %2, 896;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "}\n" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc)
+      : "memory");
+}
+// 8 K steps, A and B MN-major.
+__device__ __forceinline__ void umma_chain8_mm(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p0, 0, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+      "add.s64 ra, %1, 128;\n\tadd.s64 rb, %2, 128;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 256;\n\tadd.s64 rb, %2, 256;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 384;\n\tadd.s64 rb, %2, 384;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 512;\n\tadd.s64 rb, %2, 512;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 640;\n\tadd.s64 rb, %2, 640;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 768;\n\tadd.s64 rb, %2, 768;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "add.s64 ra, %1, 896;\n\tadd.s64 rb, %2, 896;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p1;\n\t"
+      "}\n" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -174,6 +267,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   d |= (uint64_t)1u << 46;
   d |= (uint64_t)2u << 61;
   return d;
+}
+
+// Low 32 bits of a 128-byte-swizzle descriptor (start address and leading byte
+// offset); the high half is the same for every descriptor with a 1024-byte
+// stride offset, see sdesc_sw128_hi.
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi() { return (1024u >> 4) | (1u << 14) | (2u << 29); }
+__device__ __forceinline__ uint64_t sdesc_from_lo(uint32_t lo) {
+  return ((uint64_t)sdesc_sw128_hi() << 32) | lo;
 }
 
 // ---------------------------------------------------------------- TMEM ld / st
