@@ -2,53 +2,63 @@
 // Attention", Abstract: INT8 S = Q K^T and O = P V; FlashAttention-style
 // online softmax with the LSE kept for the backward).
 //
-// One CTA computes one 128-row query tile of one head.  Warp roles:
-//   warps 0-3  softmax / correction: thread r owns query row r (TMEM lane r)
-//   warp 4     TMA producer: Q^ once, then K^_j and V^_j through a ring of stages
-//   warp 5     TMEM allocation and the single MMA-issuing thread
-// Per key tile j the MMA thread issues S_j = Q^ K^_j^T (integer-valued BF16,
-// FP32 accumulation, exact) into one of two TMEM S buffers, then the
-// previous tile's O_j-1 = P^_j-1 V^_j-1 into one of two TMEM O buffers, so the
-// softmax of tile j overlaps the tensor-core work of tiles j and j-1.
+// One CTA computes two 128-row query tiles (t = 0, 1) of one head, so that the
+// softmax of one tile overlaps the tensor-core work of the other.  Warp roles:
+//   warps 0-3 / 4-7  softmax warpgroup of tile 0 / 1: thread r owns query row r
+//                    (TMEM lane r) and keeps that row of the running output in
+//                    FP32 registers
+//   warp 8           TMA producer: both Q^ tiles once, K^_j and V^_j through rings
+//   warp 9           TMEM allocation and the single MMA-issuing thread
+//   warps 10-11      idle (complete the third warpgroup, which gives its
+//                    registers to the softmax warpgroups: 384 threads launch with
+//                    168 registers each; 128 * kRegsLow + 256 * kRegsHigh <= 384 * 168)
+// TMEM: tile t owns S_t [256t, 256t+128) and O_t [256t+128, 256t+128+d).  The
+// quantized P~ codes are written over S_t (packed BF16, columns [256t, 256t+64))
+// and feed O_t = P^_t V^_j as the A operand straight from TMEM.
+// MMA order per key tile j: S_0(j), S_1(j), then P^_0 V^_j, P^_1 V^_j; S_t(j+1)
+// waits until P^_t V^_j has consumed the codes that share its columns.
 //
-// Softmax of tile j (FP32, base-2 logits t = S_int * sQ sK scale log2e):
+// Softmax of tile j for one row (FP32, base-2 logits t = S_int * sQ sK scale log2e):
 //   tmax  = max_k t_k over the visible keys of the row in the tile
-//   code  = rint(2^(t - tmax + log2 127)) in [0, 127]   (P~ quantized per row
-//           and tile; written as the A operand of the P V product)
+//   code  = rint(2^(t - tmax + log2 127)) in [0, 127]   (P~ quantized per row and tile)
 //   m'    = max(m, tmax),  alpha = 2^(m - m'),  r = 2^(tmax - m')
-//   l     = l alpha + (r/127) sum_k 2^(t - tmax + log2 127)  (unquantized P~)
-//   O    <- O alpha + (r/127) sV_j [P^ V^]_j   (dequantization per tile;
-//           applied one tile late, when the P V product has landed)
+//   l     = l alpha + (r/127) sum_k 2^(t - tmax + log2 127)   (unquantized P~)
+//   O    <- O alpha + (r/127) sV_j [P^ V^]_j   (dequantization per tile, applied one
+//           tile late, once the P V product has landed)
 // Epilogue: O / l as BF16, LSE = (m + log2 l) ln 2.
 #include "kernel_common.cuh"
 
 namespace sagebwd {
 namespace {
 
+constexpr int kFThreads = 384;
+constexpr uint32_t kFRegsLaunch = 168, kFRegsLow = 40, kFRegsHigh = 232;
+static_assert(128 * kFRegsLow + 256 * kFRegsHigh <= kFThreads * kFRegsLaunch, "register split exceeds the launch");
+
 template <int D>
 struct FwdCfg {
-  static constexpr int NS = D == 128 ? 2 : 3;  // K / V stages
-  static constexpr int NP = D == 128 ? 1 : 2;  // P^ buffers
-  static constexpr int TILE = 128 * D * 2;     // one Q^/K^/V^ tile (bytes)
-  static constexpr int PTILE = 128 * 128 * 2;  // one P^ tile
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int NS = 2;             // K / V stages
+  static constexpr int TILE = 128 * D * 2;  // one Q^ / K^ / V^ tile (bytes)
+  static constexpr int OFF_Q = 0;           // two Q^ tiles
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_P = OFF_V + NS * TILE;
-  static constexpr int OFF_BAR = OFF_P + NP * PTILE;
-  static constexpr int NBAR = 1 + 4 * NS + 2 + 2 + 2 * NP + 2 + 2 + 1;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  static constexpr int NBAR = 1 + 4 * NS + 2 * 4 + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+  static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
+  __host__ __device__ static constexpr int col_s(int t) { return 256 * t; }
+  __host__ __device__ static constexpr int col_o(int t) { return 256 * t + 128; }
 };
 
-enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteSFull, kSiteSEmpty,
-               kSitePFull, kSitePEmpty, kSiteOFull, kSiteOEmpty };
+enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteSFull, kSitePFull, kSitePVDone,
+               kSiteOEmpty };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kFThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
-  constexpr int NS = C::NS, NP = C::NP;
+  constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -57,25 +67,29 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* bar_k_empty = bar_k_full + NS;
   uint64_t* bar_v_full = bar_k_empty + NS;
   uint64_t* bar_v_empty = bar_v_full + NS;
-  uint64_t* bar_s_full = bar_v_empty + NS;
-  uint64_t* bar_s_empty = bar_s_full + 2;
-  uint64_t* bar_p_full = bar_s_empty + 2;
-  uint64_t* bar_p_empty = bar_p_full + NP;
-  uint64_t* bar_o_full = bar_p_empty + NP;
-  uint64_t* bar_o_empty = bar_o_full + 2;
+  uint64_t* bar_s_full = bar_v_empty + NS;  // [2] S_t in TMEM
+  uint64_t* bar_p_full = bar_s_full + 2;    // [2] codes of P~_t in TMEM (softmax)
+  uint64_t* bar_pv_done = bar_p_full + 2;   // [2] P^_t V^ in TMEM (and the codes consumed)
+  uint64_t* bar_o_empty = bar_pv_done + 2;  // [2] O_t folded into registers (softmax)
   uint64_t* bar_final = bar_o_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_final + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BH = p.B * p.Hq;
+  const int npairs = (p.nb + 1) / 2;
   const int L = blockIdx.x;
-  const int qb = CAUSAL ? (p.nb - 1 - L / BH) : (L / BH);  // causal: longest rows first
+  const int pr = CAUSAL ? (npairs - 1 - L / BH) : (L / BH);  // causal: longest rows first
   const int bhq = L % BH;
   const int b = bhq / p.Hq, h = bhq % p.Hq;
   const int bhk = b * p.Hkv + h / p.G;
-  const int q0 = qb * kBlk;
-  const int nkb = CAUSAL ? qb + 1 : p.nb;
+  int nkb[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qb = 2 * pr + t;
+    nkb[t] = qb >= p.nb ? 0 : (CAUSAL ? qb + 1 : p.nb);
+  }
+  const int nkb_max = nkb[0] > nkb[1] ? nkb[0] : nkb[1];
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
@@ -85,21 +99,17 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(bar_v_full + s, 1);
       mbar_init(bar_v_empty + s, 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_s_full + s, 1);
-      mbar_init(bar_s_empty + s, 128);
-      mbar_init(bar_o_full + s, 1);
-      mbar_init(bar_o_empty + s, 128);
-    }
-    for (int s = 0; s < NP; ++s) {
-      mbar_init(bar_p_full + s, 128);
-      mbar_init(bar_p_empty + s, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s_full + t, 1);
+      mbar_init(bar_p_full + t, 128);
+      mbar_init(bar_pv_done + t, 1);
+      mbar_init(bar_o_empty + t, 128);
     }
     mbar_init(bar_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -109,14 +119,19 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  if (warp >= 8) {
+    setmaxnreg_dec<kFRegsLow>();
+    if (warp == 8 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
       int k_issued[NS], v_issued[NS];
       for (int s = 0; s < NS; ++s) k_issued[s] = v_issued[s] = 0;
-      mbar_arrive_expect_tx(bar_q, C::TILE);
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(smem + C::OFF_Q + c * 16384, &tmQ, bar_q, c * 64, q0, bhq);
-      for (int j = 0; j < nkb; ++j) {
+      const int nq = (nkb[0] > 0) + (nkb[1] > 0);
+      mbar_arrive_expect_tx(bar_q, nq * C::TILE);
+      for (int t = 0; t < 2; ++t)
+        if (nkb[t] > 0)
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::OFF_Q + t * C::TILE + c * 16384, &tmQ, bar_q, c * 64, (2 * pr + t) * kBlk, bhq);
+      for (int j = 0; j < nkb_max; ++j) {
         const int s = j % NS, n = j / NS;
         if (j >= NS && !wait1(wc, bar_k_empty + s, (n - 1) & 1, kSiteKEmpty)) break;
         if (!((p.flags & SAGEBWD_FLAG_DROP_ONE_LOAD) && j == 1)) {  // fault injection skips one load
@@ -137,57 +152,73 @@ __global__ void __launch_bounds__(192, 1)
         if (k_issued[s]) drain(bar_k_full + s, (k_issued[s] - 1) & 1, p.timeout_ns);
         if (v_issued[s]) drain(bar_v_full + s, (v_issued[s] - 1) & 1, p.timeout_ns);
       }
-    }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 9 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       const uint32_t idO = idesc_bf16_f32(128, D, false, true);
       bool ok = wait1(wc, bar_q, 0, kSiteQ);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-      for (int j = 0; ok && j <= nkb; ++j) {
-        if (j < nkb) {
-          const int s = j % NS, sb = j & 1;
-          if (!wait1(wc, bar_k_full + s, (j / NS) & 1, kSiteKFull)) break;
-          if (j >= 2 && !wait1(wc, bar_s_empty + sb, ((j >> 1) - 1) & 1, kSiteSEmpty)) break;
-          tc_fence_after();
-          const uint32_t sK = smem_u32(smem + C::OFF_K + s * C::TILE);
+      for (int j = 0; ok && j < nkb_max; ++j) {
+        const int s = j % NS;
+        if (!wait1(wc, bar_k_full + s, (j / NS) & 1, kSiteKFull)) break;
+        const uint32_t kdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_K + s * C::TILE), 16);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_ss(tmem + sb * 128, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), idS, kk > 0);
+        for (int t = 0; t < 2; ++t) {
+          if (j >= nkb[t]) continue;
+          // S_t(j) overwrites the columns that held P^_t(j-1): wait until P^_t(j-1) V^ is done
+          if (j >= 1 && !wait1(wc, bar_pv_done + t, (j - 1) & 1, kSitePVDone)) {
+            ok = false;
+            break;
           }
-          umma_commit(bar_s_full + sb);
-          umma_commit(bar_k_empty + s);
-        }
-        if (j >= 1) {
-          const int jj = j - 1, s = jj % NS, ob = jj & 1, pb = jj % NP;
-          if (!wait1(wc, bar_p_full + pb, (jj / NP) & 1, kSitePFull)) break;
-          if (!wait1(wc, bar_v_full + s, (jj / NS) & 1, kSiteVFull)) break;
-          if (jj >= 2 && !wait1(wc, bar_o_empty + ob, ((jj >> 1) - 1) & 1, kSiteOEmpty)) break;
           tc_fence_after();
-          const uint32_t sP = smem_u32(smem + C::OFF_P + pb * C::PTILE);
-          const uint32_t sV = smem_u32(smem + C::OFF_V + s * C::TILE);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            umma_ss(tmem + 256 + ob * D, sdesc_sw128(sP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                    sdesc_sw128(sV + kk * 2048, 16384, 1024), idO, kk > 0);
-          }
-          umma_commit(bar_o_full + ob);
-          umma_commit(bar_v_empty + s);
-          umma_commit(bar_p_empty + pb);
+          const uint32_t qdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_Q + t * C::TILE), 16);
+          if constexpr (D == 128)
+            umma_chain8_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
+          else
+            umma_chain4_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
+          umma_commit(bar_s_full + t);
         }
+        if (!ok) break;
+        umma_commit(bar_k_empty + s);
+        if (!wait1(wc, bar_v_full + s, (j / NS) & 1, kSiteVFull)) break;
+        const uint32_t vdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_V + s * C::TILE), 16384);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j >= nkb[t]) continue;
+          if (!wait1(wc, bar_p_full + t, j & 1, kSitePFull)) {
+            ok = false;
+            break;
+          }
+          if (j >= 1 && !wait1(wc, bar_o_empty + t, (j - 1) & 1, kSiteOEmpty)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // O_t = P^_t V^_j: A = the codes in TMEM (K = 128 keys = 64 packed columns, 8 per
+          // K step), B = V^_j [key][d] read MN-major
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_from_lo(vdesc + kk * 128), idO, kk > 0);
+          umma_commit(bar_pv_done + t);
+        }
+        if (!ok) break;
+        umma_commit(bar_v_empty + s);
       }
       // Every MMA issued above must complete before TMEM is released.
       umma_commit(bar_final);
       drain(bar_final, 0, p.timeout_ns);
     }
   } else {
+    setmaxnreg_inc<kFRegsHigh>();
     // ------------------------------------------------------------ softmax / correction
-    const int r = tid;  // query row within the tile == TMEM lane
-    const int i = q0 + r;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const float sQv = p.sq[(size_t)bhq * p.nb + qb];
+    const int t = warp >> 2;  // query tile of this warpgroup
+    const int r = tid & 127;  // query row within the tile == TMEM lane
+    const int qb = 2 * pr + t;
+    const int i = qb * kBlk + r;
+    const int nk = nkb[t];
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + C::col_s(t);
+    const uint32_t o_addr = tmem + lane_base + C::col_o(t);
+    const float sQv = nk > 0 ? p.sq[(size_t)bhq * p.nb + qb] : 0.f;
     float m = -INFINITY, l = 0.f;
     float o_acc[D];
 #pragma unroll
@@ -195,27 +226,25 @@ __global__ void __launch_bounds__(192, 1)
     float pend_alpha = 0.f, pend_w = 0.f;
     bool ok = true;
 
-    // Fold tile t's P V product into the running output.
-    auto fold = [&](int t, float a, float w) -> bool {
-      const int ob = t & 1;
-      if (!waitw(wc, bar_o_full + ob, (t >> 1) & 1, kSiteOFull)) return false;
+    // Fold tile jj's P V product into the running output.
+    auto fold = [&](int jj, float a, float w) -> bool {
+      if (!waitw(wc, bar_pv_done + t, jj & 1, kSitePVDone)) return false;
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + 256 + ob * D + c0, v);
+        tmem_ld32(o_addr + c0, v);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 32; ++e) o_acc[c0 + e] = fmaf(w, __uint_as_float(v[e]), o_acc[c0 + e] * a);
       }
       tc_fence_before();
-      mbar_arrive(bar_o_empty + ob);
+      mbar_arrive(bar_o_empty + t);
       return true;
     };
 
-    for (int j = 0; j < nkb; ++j) {
-      const int sb = j & 1;
-      if (!waitw(wc, bar_s_full + sb, (j >> 1) & 1, kSiteSFull)) {
+    for (int j = 0; j < nk; ++j) {
+      if (!waitw(wc, bar_s_full + t, j & 1, kSiteSFull)) {
         ok = false;
         break;
       }
@@ -226,7 +255,6 @@ __global__ void __launch_bounds__(192, 1)
       const int k0 = j * kBlk;
       const bool need_mask = (CAUSAL && j == qb) || (k0 + kBlk > p.N);
       const int kvis = need_mask ? (min(p.N, CAUSAL ? i + 1 : p.N) - k0) : kBlk;  // visible keys of this row
-      const uint32_t s_addr = tmem + lane_base + sb * 128;
       // pass 1: row maximum of S_int over the visible keys
       float smax = -INFINITY;
 #pragma unroll
@@ -245,13 +273,8 @@ __global__ void __launch_bounds__(192, 1)
       const float alpha = ex2_approx(m - m_new);
       const float rj = ex2_approx(tmax - m_new);
       const float bias = kLog2_127 - tmax;
-      const int pb = j % NP;
-      if (j >= NP && !waitw(wc, bar_p_empty + pb, ((j / NP) - 1) & 1, kSitePEmpty)) {
-        ok = false;
-        break;
-      }
-      // pass 2: codes of P~ into the swizzled A tile, and the unquantized row sum
-      const uint32_t p_base = smem_u32(smem + C::OFF_P + pb * C::PTILE);
+      // pass 2: codes of P~ written over the S columns already read (chunk c of 32 keys
+      // -> 16 packed columns starting at 16c), and the unquantized row sum
       float usum = 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -268,17 +291,13 @@ __global__ void __launch_bounds__(192, 1)
             if (c0 + e + 1 >= kvis) u1 = 0.f;
           }
           usum += u0 + u1;
-          pk[e >> 1] = pack_bf16x2(rint_f32(u0), rint_f32(u1));
+          pk[e >> 1] = pack_int_bf16x2(rint_small(u0), rint_small(u1));
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_shared_v4(p_base + sw128_offset(r, (c0 >> 3) + q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                       pk[4 * q + 3]);
+        tmem_st16(s_addr + (c0 >> 1), pk);
       }
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_s_empty + sb);
-      fence_proxy_async_smem();
-      mbar_arrive(bar_p_full + pb);
+      mbar_arrive(bar_p_full + t);
       const float w_l = rj * (1.f / 127.f);
       l = fmaf(w_l, usum, l * alpha);
       m = m_new;
@@ -289,8 +308,8 @@ __global__ void __launch_bounds__(192, 1)
       pend_alpha = alpha;
       pend_w = w_l * sVv;
     }
-    if (ok) ok = fold(nkb - 1, pend_alpha, pend_w);
-    if (ok && !*abort_flag && i < p.N) {
+    if (ok && nk > 0) ok = fold(nk - 1, pend_alpha, pend_w);
+    if (ok && nk > 0 && !*abort_flag && i < p.N) {
       const float inv_l = 1.f / l;
       uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bhq * p.N + i) * D);
 #pragma unroll
@@ -307,7 +326,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -320,8 +339,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = fwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const int grid = p.nb * p.B * p.Hq;
-  kern<<<grid, 192, C::SMEM, s>>>(tq, tk, tv, p);
+  const int grid = (p.nb + 1) / 2 * p.B * p.Hq;
+  kern<<<grid, kFThreads, C::SMEM, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
