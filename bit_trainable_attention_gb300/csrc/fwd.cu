@@ -15,17 +15,20 @@
 // TMEM: tile t owns S_t [256t, 256t+128) and O_t [256t+128, 256t+128+d).  The
 // quantized P~ codes are written over S_t (packed BF16, columns [256t, 256t+64))
 // and feed O_t = P^_t V^_j as the A operand straight from TMEM.
-// MMA order per key tile j: S_0(j), S_1(j), then P^_0 V^_j, P^_1 V^_j; S_t(j+1)
-// waits until P^_t V^_j has consumed the codes that share its columns.
+// MMA order: S_0(0), S_1(0), then per key tile j: P^_0 V^_j, S_0(j+1), P^_1 V^_j,
+// S_1(j+1).  S_t(j+1) waits until P^_t V^_j has consumed the codes that share its
+// columns; the softmax of one tile runs while the tensor core serves the other.
 //
 // Softmax of tile j for one row (FP32, base-2 logits t = S_int * sQ sK scale log2e):
 //   tmax  = max_k t_k over the visible keys of the row in the tile
 //   code  = rint(2^(t - tmax + log2 127)) in [0, 127]   (P~ quantized per row and tile)
-//   m'    = max(m, tmax),  alpha = 2^(m - m'),  r = 2^(tmax - m')
-//   l     = l alpha + (r/127) sum_k 2^(t - tmax + log2 127)   (unquantized P~)
-//   O    <- O alpha + (r/127) sV_j [P^ V^]_j   (dequantization per tile, applied one
+//   The output and row sum are kept relative to a reference m_ref (raised to tmax,
+//   with a rescale by a = 2^(m_ref - tmax), only when tmax > m_ref + 8), r = 2^(tmax - m_ref):
+//   l     = l a + (r/127) sum_k 2^(t - tmax + log2 127)   (unquantized P~)
+//   O    <- O a + (r/127) sV_j [P^ V^]_j   (dequantization per tile, applied one
 //           tile late, once the P V product has landed)
-// Epilogue: O / l as BF16, LSE = (m + log2 l) ln 2.
+// Epilogue: O / l as BF16, LSE = (m_ref + log2 l) ln 2.  The quotient does not depend
+// on the reference, so this is the online softmax of the definition.
 #include "kernel_common.cuh"
 
 namespace sagebwd {
@@ -156,52 +159,65 @@ __global__ void __launch_bounds__(kFThreads, 1)
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       const uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      bool ok = wait1(wc, bar_q, 0, kSiteQ);
+      // S_t = Q^_t K^_j^T into TMEM columns [col_s(t), col_s(t) + 128)
+      auto issue_s = [&](int t, uint32_t kdesc) {
+        const uint32_t qdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_Q + t * C::TILE), 16);
+        if constexpr (D == 128)
+          umma_chain8_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
+        else
+          umma_chain4_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
+        umma_commit(bar_s_full + t);
+      };
+      bool ok = wait1(wc, bar_q, 0, kSiteQ) && wait1(wc, bar_k_full, 0, kSiteKFull);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t kdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_K), 16);
+        for (int t = 0; t < 2; ++t)
+          if (nkb[t] > 0) issue_s(t, kdesc);
+        umma_commit(bar_k_empty);
+      }
+      // Per key tile j: P^_0 V^_j, S_0(j+1), P^_1 V^_j, S_1(j+1), so that the tensor
+      // core works on one tile while the softmax warpgroup of the other runs.
       for (int j = 0; ok && j < nkb_max; ++j) {
-        const int s = j % NS;
-        if (!wait1(wc, bar_k_full + s, (j / NS) & 1, kSiteKFull)) break;
-        const uint32_t kdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_K + s * C::TILE), 16);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (j >= nkb[t]) continue;
-          // S_t(j) overwrites the columns that held P^_t(j-1): wait until P^_t(j-1) V^ is done
-          if (j >= 1 && !wait1(wc, bar_pv_done + t, (j - 1) & 1, kSitePVDone)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t qdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_Q + t * C::TILE), 16);
-          if constexpr (D == 128)
-            umma_chain8_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
-          else
-            umma_chain4_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
-          umma_commit(bar_s_full + t);
-        }
-        if (!ok) break;
-        umma_commit(bar_k_empty + s);
+        const int s = j % NS, s1 = (j + 1) % NS;
         if (!wait1(wc, bar_v_full + s, (j / NS) & 1, kSiteVFull)) break;
         const uint32_t vdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_V + s * C::TILE), 16384);
+        const uint32_t kdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_K + s1 * C::TILE), 16);
+        bool k_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (j >= nkb[t]) continue;
-          if (!wait1(wc, bar_p_full + t, j & 1, kSitePFull)) {
-            ok = false;
-            break;
-          }
-          if (j >= 1 && !wait1(wc, bar_o_empty + t, (j - 1) & 1, kSiteOEmpty)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // O_t = P^_t V^_j: A = the codes in TMEM (K = 128 keys = 64 packed columns, 8 per
-          // K step), B = V^_j [key][d] read MN-major
+          if (j < nkb[t]) {
+            if (!wait1(wc, bar_p_full + t, j & 1, kSitePFull) ||
+                (j >= 1 && !wait1(wc, bar_o_empty + t, (j - 1) & 1, kSiteOEmpty))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // O_t = P^_t V^_j: A = the codes in TMEM (128 keys = 64 packed columns, 8 per
+            // K step), B = V^_j [key][d] read MN-major
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_from_lo(vdesc + kk * 128), idO, kk > 0);
-          umma_commit(bar_pv_done + t);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_from_lo(vdesc + kk * 128), idO, kk > 0);
+            umma_commit(bar_pv_done + t);
+          }
+          if (j + 1 < nkb[t]) {
+            if (!k_ready && !wait1(wc, bar_k_full + s1, ((j + 1) / NS) & 1, kSiteKFull)) {
+              ok = false;
+              break;
+            }
+            k_ready = true;
+            // S_t(j+1) overwrites the code columns: P^_t V^_j must have read them
+            if (!wait1(wc, bar_pv_done + t, j & 1, kSitePVDone)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, kdesc);
+          }
         }
         if (!ok) break;
         umma_commit(bar_v_empty + s);
+        if (k_ready) umma_commit(bar_k_empty + s1);
       }
       // Every MMA issued above must complete before TMEM is released.
       umma_commit(bar_final);
@@ -219,24 +235,34 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t s_addr = tmem + lane_base + C::col_s(t);
     const uint32_t o_addr = tmem + lane_base + C::col_o(t);
     const float sQv = nk > 0 ? p.sq[(size_t)bhq * p.nb + qb] : 0.f;
-    float m = -INFINITY, l = 0.f;
-    float o_acc[D];
+    // The running output and sum are kept relative to a reference maximum m_ref that
+    // only moves when a tile's maximum exceeds it by more than 2^8; the result is the
+    // same ratio, and the rescale of the output is skipped on most tiles.
+    float m_ref = -INFINITY, l = 0.f;
+    uint64_t o_acc[D / 2];
 #pragma unroll
-    for (int c = 0; c < D; ++c) o_acc[c] = 0.f;
-    float pend_alpha = 0.f, pend_w = 0.f;
+    for (int c = 0; c < D / 2; ++c) o_acc[c] = 0ull;
+    float pend_a = 1.f, pend_w = 0.f;
     bool ok = true;
 
-    // Fold tile jj's P V product into the running output.
+    // Fold tile jj's P V product into the running output: o = o * a + w * [P^ V^]_jj.
     auto fold = [&](int jj, float a, float w) -> bool {
       if (!waitw(wc, bar_pv_done + t, jj & 1, kSitePVDone)) return false;
       tc_fence_after();
+      if (__any_sync(0xffffffffu, a != 1.f)) {
+        const uint64_t a2 = pack_f32x2(a, a);
+#pragma unroll
+        for (int c = 0; c < D / 2; ++c) fmul2_acc(o_acc[c], a2);
+      }
+      const uint64_t w2 = pack_f32x2(w, w);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(o_addr + c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o_acc[c0 + e] = fmaf(w, __uint_as_float(v[e]), o_acc[c0 + e] * a);
+        for (int e = 0; e < 32; e += 2)
+          ffma2_acc(o_acc[(c0 + e) >> 1], w2, v[e], v[e + 1]);
       }
       tc_fence_before();
       mbar_arrive(bar_o_empty + t);
@@ -244,6 +270,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
     };
 
     for (int j = 0; j < nk; ++j) {
+      // the previous tile's product lands while S_t(j) is computed
+      if (j >= 1 && !fold(j - 1, pend_a, pend_w)) {
+        ok = false;
+        break;
+      }
       if (!waitw(wc, bar_s_full + t, j & 1, kSiteSFull)) {
         ok = false;
         break;
@@ -257,25 +288,40 @@ __global__ void __launch_bounds__(kFThreads, 1)
       const int kvis = need_mask ? (min(p.N, CAUSAL ? i + 1 : p.N) - k0) : kBlk;  // visible keys of this row
       // pass 1: row maximum of S_int over the visible keys
       float smax = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(s_addr + c0, v);
-        tmem_ld_wait();
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(s_addr + c0, v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float sv = __uint_as_float(v[e]);
-          smax = fmaxf(smax, (need_mask && c0 + e >= kvis) ? -INFINITY : sv);
+          for (int e = 0; e < 32; e += 2)
+            smax = fmax3(smax, c0 + e < kvis ? __uint_as_float(v[e]) : -INFINITY,
+                         c0 + e + 1 < kvis ? __uint_as_float(v[e + 1]) : -INFINITY);
+        }
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(s_addr + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) smax = fmax3(smax, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
         }
       }
       const float tmax = __fmul_rn(smax, qks);
-      const float m_new = fmaxf(m, tmax);
-      const float alpha = ex2_approx(m - m_new);
-      const float rj = ex2_approx(tmax - m_new);
+      float a = 1.f;
+      if (tmax > m_ref + 8.f) {
+        a = ex2_approx(m_ref - tmax);
+        m_ref = tmax;
+      }
+      const float rj = ex2_approx(tmax - m_ref);
       const float bias = kLog2_127 - tmax;
       // pass 2: codes of P~ written over the S columns already read (chunk c of 32 keys
       // -> 16 packed columns starting at 16c), and the unquantized row sum
-      float usum = 0.f;
+      const float2 qks2 = make_float2(qks, qks), bias2 = make_float2(bias, bias);
+      const float2 mg = make_float2(12582912.0f, 12582912.0f), nmg = make_float2(-12582912.0f, -12582912.0f);
+      float2 usum = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t v[32];
@@ -284,14 +330,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float u0 = ex2_approx(fmaf(__uint_as_float(v[e]), qks, bias));
-          float u1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), qks, bias));
+          const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), qks2, bias2);
+          float2 u = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (need_mask) {
-            if (c0 + e >= kvis) u0 = 0.f;
-            if (c0 + e + 1 >= kvis) u1 = 0.f;
+            if (c0 + e >= kvis) u.x = 0.f;
+            if (c0 + e + 1 >= kvis) u.y = 0.f;
           }
-          usum += u0 + u1;
-          pk[e >> 1] = pack_int_bf16x2(rint_small(u0), rint_small(u1));
+          usum = fadd2(usum, u);
+          // round to the nearest integer (ties to even) with the 1.5 * 2^23 constant
+          const float2 cd = fadd2(fadd2(u, mg), nmg);
+          pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
         }
         tmem_st16(s_addr + (c0 >> 1), pk);
       }
@@ -299,29 +347,24 @@ __global__ void __launch_bounds__(kFThreads, 1)
       tc_fence_before();
       mbar_arrive(bar_p_full + t);
       const float w_l = rj * (1.f / 127.f);
-      l = fmaf(w_l, usum, l * alpha);
-      m = m_new;
-      if (j >= 1 && !fold(j - 1, pend_alpha, pend_w)) {
-        ok = false;
-        break;
-      }
-      pend_alpha = alpha;
+      l = fmaf(w_l, usum.x + usum.y, l * a);
+      pend_a = a;
       pend_w = w_l * sVv;
     }
-    if (ok && nk > 0) ok = fold(nk - 1, pend_alpha, pend_w);
+    if (ok && nk > 0) ok = fold(nk - 1, pend_a, pend_w);
     if (ok && nk > 0 && !*abort_flag && i < p.N) {
       const float inv_l = 1.f / l;
       uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bhq * p.N + i) * D);
 #pragma unroll
-      for (int c = 0; c < D; c += 8) {
+      for (int c = 0; c < D / 2; c += 4) {
         uint4 u;
-        u.x = pack_bf16x2(o_acc[c] * inv_l, o_acc[c + 1] * inv_l);
-        u.y = pack_bf16x2(o_acc[c + 2] * inv_l, o_acc[c + 3] * inv_l);
-        u.z = pack_bf16x2(o_acc[c + 4] * inv_l, o_acc[c + 5] * inv_l);
-        u.w = pack_bf16x2(o_acc[c + 6] * inv_l, o_acc[c + 7] * inv_l);
-        dst[c / 8] = u;
+        u.x = pack_bf16x2(lo_f32(o_acc[c]) * inv_l, hi_f32(o_acc[c]) * inv_l);
+        u.y = pack_bf16x2(lo_f32(o_acc[c + 1]) * inv_l, hi_f32(o_acc[c + 1]) * inv_l);
+        u.z = pack_bf16x2(lo_f32(o_acc[c + 2]) * inv_l, hi_f32(o_acc[c + 2]) * inv_l);
+        u.w = pack_bf16x2(lo_f32(o_acc[c + 3]) * inv_l, hi_f32(o_acc[c + 3]) * inv_l);
+        dst[c / 4] = u;
       }
-      p.lse[(size_t)bhq * p.N + i] = (m + log2f(l)) * kLn2;
+      p.lse[(size_t)bhq * p.N + i] = (m_ref + log2f(l)) * kLn2;
     }
   }
   tc_fence_before();

@@ -336,6 +336,49 @@ __device__ __forceinline__ float rint_f32(float x) {
   asm("cvt.rni.f32.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Packed FP32 on sm_100-class parts: one instruction performs two IEEE
+// round-to-nearest operations on a register pair, so the elementwise softmax
+// work costs half the issue slots.  Each lane's result equals the scalar op's.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// A register pair holding two FP32 lanes (lo, hi), for accumulators that stay packed.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo_f32(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x)); }
+__device__ __forceinline__ float hi_f32(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x >> 32)); }
+// acc = w2 * (v0, v1) + acc, lane by lane
+__device__ __forceinline__ void ffma2_acc(uint64_t& acc, uint64_t w2, uint32_t v0, uint32_t v1) {
+  asm("{\n\t.reg .b64 rv;\n\tmov.b64 rv, {%2, %3};\n\tfma.rn.f32x2 %0, %1, rv, %0;\n\t}"
+      : "+l"(acc)
+      : "l"(w2), "r"(v0), "r"(v1));
+}
+// acc = acc * a2, lane by lane
+__device__ __forceinline__ void fmul2_acc(uint64_t& acc, uint64_t a2) {
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(a2));
+}
+// Three-input maximum (one instruction on sm_100-class parts).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 // Pack two floats into bf16x2 (lo = a, hi = b), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   uint32_t r;
