@@ -307,19 +307,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool key_ok = kglob < p.N;
     const float sKv = p.sk[(size_t)bhk * p.nb + j];
     const uint32_t pt_base = smem_u32(smem + C::OFF_PT), ds_base = smem_u32(smem + C::OFF_DST);
-    float dv_run[DC], dk_run[DC];
+    uint64_t dv_run[DC / 2], dk_run[DC / 2];  // packed FP32 pairs (columns c, c + 1)
 #pragma unroll
-    for (int c = 0; c < DC; ++c) dv_run[c] = dk_run[c] = 0.f;
+    for (int c = 0; c < DC / 2; ++c) dv_run[c] = dk_run[c] = 0ull;
 
-    // Per-tile LSE (base 2) / D values and block scales, loaded one tile ahead so
-    // that their global-memory latency hides behind the current tile.
+    // Per-tile LSE (base 2) / D values (stored negated: they enter as addends) and
+    // block scales, loaded one tile ahead so that their global-memory latency hides
+    // behind the current tile.
     const int q_own = ct & 127;
     auto tile_vec = [&](int t) -> float {
       const int bq = b * p.Hq + hk * p.G + t / nq;
       const int row = (ib0 + t % nq) * kBlk + q_own;
       const bool in = row < p.N;
-      if (ct < 128) return in ? __fmul_rn(p.lse[(size_t)bq * p.N + row], kLog2e) : INFINITY;
-      if (ct < 256) return in ? p.D[(size_t)bq * p.N + row] : 0.f;
+      if (ct < 128) return in ? -__fmul_rn(p.lse[(size_t)bq * p.N + row], kLog2e) : -INFINITY;
+      if (ct < 256) return in ? -p.D[(size_t)bq * p.N + row] : 0.f;
       return 0.f;
     };
     auto tile_sq = [&](int t) { return p.sq[(size_t)(b * p.Hq + hk * p.G + t / nq) * p.nb + ib0 + t % nq]; };
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ib = ib0 + it % nq;
       const int i0 = ib * kBlk;
       (void)i0;
-      // LSE (base 2) and D of the tile's queries (+inf / 0 past N); reset the row maxima
+      // -LSE (base 2) and -D of the tile's queries (-inf / 0 past N); reset the row maxima
       if (ct < 128)
         L2v[q_own] = pf_vec;
       else if (ct < 256)
@@ -353,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // pass 1
       float pmax = 0.f, amax = 0.f;
+      const float2 qks2 = make_float2(qks, qks);
       const bool masked = diag || (k0 + kBlk > p.N);
 #pragma unroll
       for (int c0 = 0; c0 < kQC; c0 += 8) {
@@ -363,20 +365,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int e4 = 0; e4 < 8; e4 += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(L2v + col + e4);
-          const float4 d4 = *reinterpret_cast<const float4*>(Dv + col + e4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+          const float4 l4 = *reinterpret_cast<const float4*>(L2v + col + e4);  // -LSE log2 e
+          const float4 d4 = *reinterpret_cast<const float4*>(Dv + col + e4);   // -D
 #pragma unroll
-          for (int e1 = 0; e1 < 4; ++e1) {
-            const int e = e4 + e1;
-            float pr = ex2_approx(fmaf(__uint_as_float(sv[e]), qks, -lv[e1]));
-            if (masked) pr = (!key_ok || (diag && col + e < r)) ? 0.f : pr;
-            const float ds = pr * (__uint_as_float(dpv[e]) - dvv[e1]);
-            pmax = fmaxf(pmax, pr);
-            amax = fmaxf(amax, fabsf(ds));
-            sv[e] = __float_as_uint(pr);
-            dpv[e] = __float_as_uint(ds);
+          for (int e2 = 0; e2 < 4; e2 += 2) {
+            const int e = e4 + e2;
+            const float2 nl = e2 == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+            const float2 nd = e2 == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+            const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), qks2, nl);
+            float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            if (masked) {
+              if (!key_ok || (diag && col + e < r)) pr.x = 0.f;
+              if (!key_ok || (diag && col + e + 1 < r)) pr.y = 0.f;
+            }
+            const float2 ds =
+                fmul2(pr, fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), nd));
+            pmax = fmax3(pmax, pr.x, pr.y);
+            amax = fmax3(amax, fabsf(ds.x), fabsf(ds.y));
+            sv[e] = __float_as_uint(pr.x);
+            sv[e + 1] = __float_as_uint(pr.y);
+            dpv[e] = __float_as_uint(ds.x);
+            dpv[e + 1] = __float_as_uint(ds.y);
           }
         }
         tmem_st8(tmem + lane_base + C::C_S + col, sv);
@@ -400,6 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sPc = p_live ? cmax * (1.f / 127.f) : 0.f;
       const float invA = d_live ? __fdividef(127.f, a) : 0.f;
       const float sDS = d_live ? a * (1.f / 127.f) : 0.f;
+      const float2 invP2 = make_float2(invP, invP), invA2 = make_float2(invA, invA);
+      // codes = rint(x) by adding and removing 1.5 * 2^23 (exact for |x| < 2^22)
+      const float2 kMagic2 = make_float2(12582912.0f, 12582912.0f), kNegMagic2 = make_float2(-12582912.0f, -12582912.0f);
       // the code tiles double as the dQ staging tile: wait until the last reduce has read its half
       if (it >= 1 && !waitw(wc, bar_staging_free, (it - 1) & 1, bSiteStagingFree)) break;
       // pass 2a: codes of P^T into the swizzled A tile (row = key r, 16-byte chunk = 8 queries)
@@ -410,9 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld16(tmem + lane_base + C::C_S + kQC * w + h, pv);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; e += 2)
-            pv[e >> 1] = pack_int_bf16x2(rint_small(__fmul_rn(__uint_as_float(pv[e]), invP)),
-                                         rint_small(__fmul_rn(__uint_as_float(pv[e + 1]), invP)));
+          for (int e = 0; e < 16; e += 2) {
+            const float2 cd = fadd2(
+                fadd2(fmul2(make_float2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), invP2), kMagic2), kNegMagic2);
+            pv[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+          }
           st_shared_v4(pt_base + sw128_offset(r, ((kQC * w + h) >> 3)), pv[0], pv[1], pv[2], pv[3]);
           st_shared_v4(pt_base + sw128_offset(r, ((kQC * w + h) >> 3) + 1), pv[4], pv[5], pv[6], pv[7]);
         }
@@ -428,9 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld16(tmem + lane_base + C::C_DP + kQC * w + h, dsv);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; e += 2)
-            dsv[e >> 1] = pack_int_bf16x2(rint_small(__fmul_rn(__uint_as_float(dsv[e]), invA)),
-                                          rint_small(__fmul_rn(__uint_as_float(dsv[e + 1]), invA)));
+          for (int e = 0; e < 16; e += 2) {
+            const float2 cd = fadd2(
+                fadd2(fmul2(make_float2(__uint_as_float(dsv[e]), __uint_as_float(dsv[e + 1])), invA2), kMagic2),
+                kNegMagic2);
+            dsv[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+          }
           st_shared_v4(ds_base + sw128_offset(r, ((kQC * w + h) >> 3)), dsv[0], dsv[1], dsv[2], dsv[3]);
           st_shared_v4(ds_base + sw128_offset(r, ((kQC * w + h) >> 3) + 1), dsv[4], dsv[5], dsv[6], dsv[7]);
         }
@@ -443,6 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float fv = __fmul_rn(sPc, sdOt);
       const float fk = __fmul_rn(__fmul_rn(p.sc, sDS), sQt);
       const float fq = __fmul_rn(__fmul_rn(p.sc, sDS), sKv);
+      const uint64_t fv2 = pack_f32x2(fv, fv), fk2 = pack_f32x2(fk, fk);
+      const float2 fq2 = make_float2(fq, fq);
       if (!waitw(wc, bar_acc_v, it & 1, bSiteAccV)) break;
       tc_fence_after();
 #pragma unroll
@@ -451,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tmem + lane_base + C::C_DV + w * DC + c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) dv_run[c0 + e] = fmaf(fv, __uint_as_float(v[e]), dv_run[c0 + e]);
+        for (int e = 0; e < 16; e += 2) ffma2_acc(dv_run[(c0 + e) >> 1], fv2, v[e], v[e + 1]);
       }
       if (!waitw(wc, bar_acc_q, it & 1, bSiteAccQ)) break;
       tc_fence_after();
@@ -468,9 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int box = col >> 5;  // boxes [0, D/64) in the P^T tile, the rest in the dS^T tile
           const uint32_t box_base = box < D / 64 ? pt_base + box * 16384 : ds_base + (box - D / 64) * 16384;
           const uint32_t off = (uint32_t)(r * 128 + ((((col & 31) >> 2) ^ (r & 7)) << 4));
-          st_shared_v4(box_base + off, __float_as_uint(fq * __uint_as_float(v[c4])),
-                       __float_as_uint(fq * __uint_as_float(v[c4 + 1])), __float_as_uint(fq * __uint_as_float(v[c4 + 2])),
-                       __float_as_uint(fq * __uint_as_float(v[c4 + 3])));
+          const float2 q01 = fmul2(fq2, make_float2(__uint_as_float(v[c4]), __uint_as_float(v[c4 + 1])));
+          const float2 q23 = fmul2(fq2, make_float2(__uint_as_float(v[c4 + 2]), __uint_as_float(v[c4 + 3])));
+          st_shared_v4(box_base + off, __float_as_uint(q01.x), __float_as_uint(q01.y), __float_as_uint(q23.x),
+                       __float_as_uint(q23.y));
         }
       }
       tc_fence_before();
@@ -483,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tmem + lane_base + C::C_DK + w * DC + c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) dk_run[c0 + e] = fmaf(fk, __uint_as_float(v[e]), dk_run[c0 + e]);
+        for (int e = 0; e < 16; e += 2) ffma2_acc(dk_run[(c0 + e) >> 1], fk2, v[e], v[e + 1]);
       }
       tc_fence_before();
       mbar_arrive(bar_tmem_free);
@@ -493,10 +513,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4* dvd = reinterpret_cast<uint4*>(p.dv + ((size_t)bhk * p.N + kglob) * D + w * DC);
 #pragma unroll
       for (int c = 0; c < DC; c += 8) {
-        dkd[c / 8] = make_uint4(pack_bf16x2(dk_run[c], dk_run[c + 1]), pack_bf16x2(dk_run[c + 2], dk_run[c + 3]),
-                                pack_bf16x2(dk_run[c + 4], dk_run[c + 5]), pack_bf16x2(dk_run[c + 6], dk_run[c + 7]));
-        dvd[c / 8] = make_uint4(pack_bf16x2(dv_run[c], dv_run[c + 1]), pack_bf16x2(dv_run[c + 2], dv_run[c + 3]),
-                                pack_bf16x2(dv_run[c + 4], dv_run[c + 5]), pack_bf16x2(dv_run[c + 6], dv_run[c + 7]));
+        const int h = c >> 1;
+        dkd[c / 8] = make_uint4(pack_bf16x2(lo_f32(dk_run[h]), hi_f32(dk_run[h])),
+                                pack_bf16x2(lo_f32(dk_run[h + 1]), hi_f32(dk_run[h + 1])),
+                                pack_bf16x2(lo_f32(dk_run[h + 2]), hi_f32(dk_run[h + 2])),
+                                pack_bf16x2(lo_f32(dk_run[h + 3]), hi_f32(dk_run[h + 3])));
+        dvd[c / 8] = make_uint4(pack_bf16x2(lo_f32(dv_run[h]), hi_f32(dv_run[h])),
+                                pack_bf16x2(lo_f32(dv_run[h + 1]), hi_f32(dv_run[h + 1])),
+                                pack_bf16x2(lo_f32(dv_run[h + 2]), hi_f32(dv_run[h + 2])),
+                                pack_bf16x2(lo_f32(dv_run[h + 3]), hi_f32(dv_run[h + 3])));
       }
     }
   }
