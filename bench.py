@@ -125,9 +125,9 @@ class Step:
         rec(2)
         sb.sagebwd_bwd_prepare(p, self.o, x["do"], self.ws1, s)
         rec(3)
-        sb.sagebwd_bwd_attention(p, x["v"], x["do"], self.lse, self.saved, self.dk, self.dv, self.ws1, s)
+        sb.sagebwd_bwd_attention(p, x["v"], x["do"], self.lse, self.saved, self.ws1, s)
         rec(4)
-        sb.sagebwd_bwd_finish(p, self.dq, self.ws1, s)
+        sb.sagebwd_bwd_finish(p, self.dq, self.dk, self.dv, self.ws1, s)
         rec(5)
 
     # kernels of ours per step: [K mean partial + final] + quantize + fwd + prep + bwd + dq convert
@@ -343,7 +343,7 @@ def main():
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
         "breakdown_ms": {"quantize": round(stage_ms[0], 4), "fwd": round(stage_ms[1], 4),
                          "bwd_prepare": round(stage_ms[2], 4), "bwd": round(stage_ms[3], 4),
-                         "dq_convert": round(stage_ms[4], 4)},
+                         "grad_convert": round(stage_ms[4], 4)},
         "tops": {"fwd_incl_quantize": round(w.flops_fwd() / ((stage_ms[0] + stage_ms[1]) * 1e-3) / 1e12, 2),
                  "bwd_incl_prepare": round(w.flops_bwd() / (sum(stage_ms[2:]) * 1e-3) / 1e12, 2)},
         "roofline": {"kernel": "sagebwd bwd_kernel", "bound": "tensor", "achieved": round(achieved, 2),

@@ -53,7 +53,7 @@ SavedLayout saved_layout(const sagebwd_problem* p) {
 
 // Workspace: [status word | pass scratch].
 struct WsLayout {
-  size_t status, kpart, D, dOq, sdo, dqacc, total;
+  size_t status, kpart, D, dOq, sdo, dqacc, dkacc, dvacc, total;
 };
 WsLayout ws_layout(const sagebwd_problem* p, int pass) {
   const size_t nb = (size_t)nblocks(p->N);
@@ -68,6 +68,9 @@ WsLayout ws_layout(const sagebwd_problem* p, int pass) {
     L.dOq = off; off += align_up(qe * 2);
     L.sdo = off; off += align_up((size_t)p->B * p->Hq * nb * 4);
     L.dqacc = off; off += align_up(qe * 4);
+    const size_t ke = (size_t)p->B * p->Hkv * p->N * p->d;
+    L.dkacc = off; off += align_up(ke * 4);
+    L.dvacc = off; off += align_up(ke * 4);
   }
   L.total = off;
   return L;
@@ -220,7 +223,10 @@ sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const v
   pp.dOq = at<__nv_bfloat16>(ws, W.dOq);
   pp.sdo = at<float>(ws, W.sdo);
   pp.dq_acc = at<float>(ws, W.dqacc);
+  pp.dk_acc = at<float>(ws, W.dkacc);
+  pp.dv_acc = at<float>(ws, W.dvacc);
   pp.BH = p->B * p->Hq;
+  pp.BHk = p->B * p->Hkv;
   pp.N = p->N;
   pp.d = p->d;
   pp.nb = nblocks(p->N);
@@ -228,8 +234,36 @@ sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const v
   return cuda_status(launch_bwd_prep(pp, st));
 }
 
+// Query heads per backward CTA for this shape on the current device, memoised
+// (the list schedule behind it costs more host time than a launch).
+int heads_per_cta(const sagebwd_problem* p) {
+  struct Key {
+    int B, Hkv, G, nb, causal, sms;
+    bool operator==(const Key& o) const {
+      return B == o.B && Hkv == o.Hkv && G == o.G && nb == o.nb && causal == o.causal && sms == o.sms;
+    }
+  };
+  static std::mutex mu;
+  static Key keys[16];
+  static int vals[16];
+  static int used = 0, next = 0;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const Key k{p->B, p->Hkv, p->Hq / p->Hkv, nblocks(p->N), p->causal ? 1 : 0, sms};
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (keys[i] == k) return vals[i];
+  const int hs = bwd_heads_per_cta(k.B, k.Hkv, k.G, k.nb, k.causal, k.sms);
+  keys[next] = k;
+  vals[next] = hs;
+  next = (next + 1) % 16;
+  if (used < 16) ++used;
+  return hs;
+}
+
 sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const void* dO, const float* lse,
-                                  const void* saved, void* dk, void* dv, void* ws, cudaStream_t st) {
+                                  const void* saved, void* ws, cudaStream_t st) {
   const SavedLayout S = saved_layout(p);
   const WsLayout W = ws_layout(p, 1);
   CUtensorMap tq, tk, tv, tdo, tdoq, tdq;
@@ -253,19 +287,23 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
   bp.sdo = at<float>(ws, W.sdo);
   bp.lse = lse;
   bp.D = at<float>(ws, W.D);
+  bp.HS = heads_per_cta(p);
   bp.dq_acc = at<float>(ws, W.dqacc);
-  bp.dk = static_cast<__nv_bfloat16*>(dk);
-  bp.dv = static_cast<__nv_bfloat16*>(dv);
+  bp.dk_acc = at<float>(ws, W.dkacc);
+  bp.dv_acc = at<float>(ws, W.dvacc);
   bp.status = at<int>(ws, W.status);
   bp.timeout_ns = timeout_of(p);
   bp.flags = p->flags;
   return cuda_status(launch_bwd(tq, tk, tv, tdo, tdoq, tdq, bp, p->d, p->causal, st));
 }
 
-sagebwd_status bwd_finish_impl(const sagebwd_problem* p, void* dq, void* ws, cudaStream_t st) {
+sagebwd_status bwd_finish_impl(const sagebwd_problem* p, void* dq, void* dk, void* dv, void* ws, cudaStream_t st) {
   const WsLayout W = ws_layout(p, 1);
-  const size_t n = (size_t)p->B * p->Hq * p->N * p->d;
-  return cuda_status(launch_dq_convert(at<float>(ws, W.dqacc), static_cast<__nv_bfloat16*>(dq), n, st));
+  const size_t nq = (size_t)p->B * p->Hq * p->N * p->d, nk = (size_t)p->B * p->Hkv * p->N * p->d;
+  const ConvertJob jobs[3] = {{at<float>(ws, W.dqacc), static_cast<__nv_bfloat16*>(dq), nq},
+                              {at<float>(ws, W.dkacc), static_cast<__nv_bfloat16*>(dk), nk},
+                              {at<float>(ws, W.dvacc), static_cast<__nv_bfloat16*>(dv), nk}};
+  return cuda_status(launch_grad_convert(jobs, 3, st));
 }
 
 }  // namespace
@@ -342,16 +380,16 @@ sagebwd_status sagebwd_bwd_prepare(const sagebwd_problem* prob, const void* o, c
 }
 
 sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v, const void* dO, const float* lse,
-                                     const void* saved, void* dk, void* dv, void* ws, void* stream) {
+                                     const void* saved, void* ws, void* stream) {
   SB_CHECK(check_problem(prob));
-  SB_CHECK(check_ptrs({v, dO, lse, saved, dk, dv, ws}));
-  return bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, static_cast<cudaStream_t>(stream));
+  SB_CHECK(check_ptrs({v, dO, lse, saved, ws}));
+  return bwd_attention_impl(prob, v, dO, lse, saved, ws, static_cast<cudaStream_t>(stream));
 }
 
-sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* ws, void* stream) {
+sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* dk, void* dv, void* ws, void* stream) {
   SB_CHECK(check_problem(prob));
-  SB_CHECK(check_ptrs({dq, ws}));
-  return bwd_finish_impl(prob, dq, ws, static_cast<cudaStream_t>(stream));
+  SB_CHECK(check_ptrs({dq, dk, dv, ws}));
+  return bwd_finish_impl(prob, dq, dk, dv, ws, static_cast<cudaStream_t>(stream));
 }
 
 sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const void* k, const void* v, const void* o,
@@ -361,8 +399,8 @@ sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const voi
   SB_CHECK(check_ptrs({q, k, v, o, dO, lse, saved, dq, dk, dv, ws}));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   SB_CHECK(bwd_prepare_impl(prob, o, dO, ws, st));
-  SB_CHECK(bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, st));
-  return bwd_finish_impl(prob, dq, ws, st);
+  SB_CHECK(bwd_attention_impl(prob, v, dO, lse, saved, ws, st));
+  return bwd_finish_impl(prob, dq, dk, dv, ws, st);
 }
 
 sagebwd_status sagebwd_check_status(const void* ws, void* stream, int32_t* detail) {

@@ -4,10 +4,13 @@
 // kept in 16-bit floating point; FlashAttention-2 backward structure with
 // D = rowsum(dO * O) and dS = P (dP - D)).
 //
-// One CTA owns one 128-key block j of one kv head and loops over the G query
-// heads of that kv head and their 128-query blocks i, so dK_j and dV_j are
-// summed in registers and written once; dQ is accumulated across CTAs by
-// TMA bulk reduce-adds into an FP32 workspace.  Warp roles:
+// One CTA owns one 128-key block j of one kv head and loops over HS of the G
+// query heads of that kv head and their 128-query blocks i.  dK_j and dV_j are
+// summed in registers over those tiles and added once into FP32 accumulators;
+// dQ is accumulated across CTAs by TMA bulk reduce-adds into an FP32 workspace.
+// CTAs are numbered longest first (causal: small j has the most query blocks),
+// and HS is chosen on the host so that this list balances over the SMs.
+// Warp roles:
 //   warps 0-15   four compute warpgroups: thread (w, r) owns key row r
 //                (TMEM lane r), query columns [32w, 32w+32) of the tile and
 //                output columns [w d/4, (w+1) d/4) of dK, dV, dQ
@@ -30,6 +33,10 @@
 //          the dQ tile has been read (they overlap pass 3)
 //   pass 3  dequantize: dQ tile * scale sdS sK -> FP32 staging tile (reduced
 //           into global by the reducer warp); dV += sP sdO [.], dK += scale sdS sQ [.]
+#include <functional>
+#include <queue>
+#include <vector>
+
 #include "kernel_common.cuh"
 
 namespace sagebwd {
@@ -114,14 +121,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BHk = p.B * p.Hkv;
+  const int NG = p.G / p.HS;  // head groups per kv head
   const int L = blockIdx.x;
-  const int j = L / BHk;  // causal: small j has the most query blocks, scheduled first
-  const int bhk = L % BHk;
+  const int j = L / (BHk * NG);  // causal: small j has the most query blocks, scheduled first
+  const int bhk = (L / NG) % BHk;
   const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
+  const int hq0 = hk * p.G + (L % NG) * p.HS;  // first query head of this CTA
   const int k0 = j * kBlk;
   const int ib0 = CAUSAL ? j : 0;
   const int nq = p.nb - ib0;
-  const int T = p.G * nq;
+  const int T = p.HS * nq;
 
   if (tid == 0) {
     mbar_init(bar_kv, 1);
@@ -172,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int it = 0; it < T; ++it) {
         const int s = it % NS, n = it / NS;
-        const int bhq = b * p.Hq + hk * p.G + it / nq;
+        const int bhq = b * p.Hq + hq0 + it / nq;
         const int i0 = (ib0 + it % nq) * kBlk;
         // dO is released first (after dP), then Q^ (after dK), then dO^ (after dV)
         if (it >= NS && !wait1(wc, bar_do_empty + s, (n - 1) & 1, bSiteDOEmpty)) break;
@@ -279,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* staging2 = smem + C::OFF_DST;
       for (int it = 0; it < T; ++it) {
         if (!wait1(wc, bar_dq_staged, it & 1, bSiteDQStaged)) break;
-        const int bhq = b * p.Hq + hk * p.G + it / nq;
+        const int bhq = b * p.Hq + hq0 + it / nq;
         const int i0 = (ib0 + it % nq) * kBlk;
 #pragma unroll
         for (int bx = 0; bx < D / 64; ++bx) tma_reduce_add_3d(&tmDQ, staging + bx * 16384, bx * 32, i0, bhq);
@@ -316,22 +325,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // behind the current tile.
     const int q_own = ct & 127;
     auto tile_vec = [&](int t) -> float {
-      const int bq = b * p.Hq + hk * p.G + t / nq;
+      const int bq = b * p.Hq + hq0 + t / nq;
       const int row = (ib0 + t % nq) * kBlk + q_own;
       const bool in = row < p.N;
       if (ct < 128) return in ? -__fmul_rn(p.lse[(size_t)bq * p.N + row], kLog2e) : -INFINITY;
       if (ct < 256) return in ? -p.D[(size_t)bq * p.N + row] : 0.f;
       return 0.f;
     };
-    auto tile_sq = [&](int t) { return p.sq[(size_t)(b * p.Hq + hk * p.G + t / nq) * p.nb + ib0 + t % nq]; };
-    auto tile_sdo = [&](int t) { return p.sdo[(size_t)(b * p.Hq + hk * p.G + t / nq) * p.nb + ib0 + t % nq]; };
+    auto tile_sq = [&](int t) { return p.sq[(size_t)(b * p.Hq + hq0 + t / nq) * p.nb + ib0 + t % nq]; };
+    auto tile_sdo = [&](int t) { return p.sdo[(size_t)(b * p.Hq + hq0 + t / nq) * p.nb + ib0 + t % nq]; };
     float pf_vec = tile_vec(0), pf_sq = tile_sq(0), pf_sdo = tile_sdo(0);
 
     for (int it = 0; it < T; ++it) {
-      const int bhq = b * p.Hq + hk * p.G + it / nq;
       const int ib = ib0 + it % nq;
-      const int i0 = ib * kBlk;
-      (void)i0;
       // -LSE (base 2) and -D of the tile's queries (-inf / 0 past N); reset the row maxima
       if (ct < 128)
         L2v[q_own] = pf_vec;
@@ -509,19 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar_tmem_free);
     }
     if (!*abort_flag && key_ok) {
-      uint4* dkd = reinterpret_cast<uint4*>(p.dk + ((size_t)bhk * p.N + kglob) * D + w * DC);
-      uint4* dvd = reinterpret_cast<uint4*>(p.dv + ((size_t)bhk * p.N + kglob) * D + w * DC);
+      // this CTA's share of dK_j, dV_j (row kglob, columns [w DC, (w+1) DC)) into the FP32 sums
+      float* dka = p.dk_acc + ((size_t)bhk * p.N + kglob) * D + w * DC;
+      float* dva = p.dv_acc + ((size_t)bhk * p.N + kglob) * D + w * DC;
 #pragma unroll
-      for (int c = 0; c < DC; c += 8) {
+      for (int c = 0; c < DC; c += 4) {
         const int h = c >> 1;
-        dkd[c / 8] = make_uint4(pack_bf16x2(lo_f32(dk_run[h]), hi_f32(dk_run[h])),
-                                pack_bf16x2(lo_f32(dk_run[h + 1]), hi_f32(dk_run[h + 1])),
-                                pack_bf16x2(lo_f32(dk_run[h + 2]), hi_f32(dk_run[h + 2])),
-                                pack_bf16x2(lo_f32(dk_run[h + 3]), hi_f32(dk_run[h + 3])));
-        dvd[c / 8] = make_uint4(pack_bf16x2(lo_f32(dv_run[h]), hi_f32(dv_run[h])),
-                                pack_bf16x2(lo_f32(dv_run[h + 1]), hi_f32(dv_run[h + 1])),
-                                pack_bf16x2(lo_f32(dv_run[h + 2]), hi_f32(dv_run[h + 2])),
-                                pack_bf16x2(lo_f32(dv_run[h + 3]), hi_f32(dv_run[h + 3])));
+        red_add_v4_f32(dka + c, lo_f32(dk_run[h]), hi_f32(dk_run[h]), lo_f32(dk_run[h + 1]), hi_f32(dk_run[h + 1]));
+        red_add_v4_f32(dva + c, lo_f32(dv_run[h]), hi_f32(dv_run[h]), lo_f32(dv_run[h + 1]), hi_f32(dv_run[h + 1]));
       }
     }
   }
@@ -540,7 +541,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = bwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const int grid = p.nb * p.B * p.Hkv;
+  const int grid = p.nb * p.B * p.Hkv * (p.G / p.HS);
   kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, p);
   return cudaGetLastError();
 }
@@ -555,6 +556,36 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                   : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdoq, tdq, p, s);
   return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdoq, tdq, p, s)
                 : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdoq, tdq, p, s);
+}
+
+// Longest-processing-time list schedule of the backward CTAs (one per key block,
+// kv head and group of HS query heads, in launch order) on `sms` SMs, for each
+// divisor HS of G; a CTA costs its tiles plus one tile of setup and drain.
+int bwd_heads_per_cta(int B, int Hkv, int G, int nb, int causal, int sms) {
+  if (sms < 1) sms = 1;
+  int best_hs = G;
+  double best = -1.0;
+  for (int hs = G; hs >= 1; --hs) {
+    if (G % hs) continue;
+    const long long per_j = (long long)B * Hkv * (G / hs);
+    std::priority_queue<double, std::vector<double>, std::greater<double>> load;
+    for (int m = 0; m < sms; ++m) load.push(0.0);
+    double makespan = 0.0;
+    for (int j = 0; j < nb; ++j) {
+      const double cost = (double)hs * (causal ? nb - j : nb) + 1.0;
+      for (long long c = 0; c < per_j; ++c) {
+        const double t = load.top() + cost;
+        load.pop();
+        load.push(t);
+        if (t > makespan) makespan = t;
+      }
+    }
+    if (best < 0.0 || makespan < best * 0.995) {  // a smaller HS must win by more than noise
+      best = makespan;
+      best_hs = hs;
+    }
+  }
+  return best_hs;
 }
 
 }  // namespace sagebwd

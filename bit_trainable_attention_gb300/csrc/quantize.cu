@@ -174,6 +174,11 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const PrepParams p) 
       float4* z = reinterpret_cast<float4*>(p.dq_acc + base + (size_t)r * D + c8 * 8);
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (bh < p.BHk) {  // the kv heads' dK / dV accumulators (BHk <= BH)
+        float4* zk = reinterpret_cast<float4*>(p.dk_acc + base + (size_t)r * D + c8 * 8);
+        float4* zv = reinterpret_cast<float4*>(p.dv_acc + base + (size_t)r * D + c8 * 8);
+        zk[0] = zk[1] = zv[0] = zv[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
     for (int o = V8 / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -182,10 +187,19 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const PrepParams p) 
   quantize_block<D>(p.dO, p.dOq, p.sdo, nullptr, bh, blk, p.N, p.nb, red);
 }
 
-__global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ out, size_t n4) {
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = acc[i];
-    out[i] = make_uint2(pack2(v.x, v.y), pack2(v.z, v.w));
+struct ConvertJobs {
+  ConvertJob job[3];
+  int njobs;
+};
+__global__ void grad_convert_kernel(const ConvertJobs J) {
+  for (int k = 0; k < J.njobs; ++k) {
+    const float4* acc = reinterpret_cast<const float4*>(J.job[k].acc);
+    uint2* out = reinterpret_cast<uint2*>(J.job[k].out);
+    const size_t n4 = J.job[k].n / 4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+      const float4 v = acc[i];
+      out[i] = make_uint2(pack2(v.x, v.y), pack2(v.z, v.w));
+    }
   }
 }
 
@@ -224,15 +238,21 @@ cudaError_t launch_bwd_prep(const PrepParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_convert(const float* acc, __nv_bfloat16* dq, size_t n, cudaStream_t s) {
-  const size_t n4 = n / 4;  // d is a multiple of 8
+cudaError_t launch_grad_convert(const ConvertJob* jobs, int njobs, cudaStream_t s) {
+  ConvertJobs J{};
+  size_t n4 = 0;
+  for (int k = 0; k < njobs && k < 3; ++k) {
+    J.job[k] = jobs[k];
+    n4 = J.job[k].n / 4 > n4 ? J.job[k].n / 4 : n4;
+  }
+  J.njobs = njobs < 3 ? njobs : 3;
+  if (n4 == 0) return cudaSuccess;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const size_t want = (n4 + 255) / 256;
   const int blocks = (int)(want < (size_t)sms * 8 ? want : (size_t)sms * 8);
-  dq_convert_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(reinterpret_cast<const float4*>(acc),
-                                                           reinterpret_cast<uint2*>(dq), n4);
+  grad_convert_kernel<<<blocks, 256, 0, s>>>(J);
   return cudaGetLastError();
 }
 

@@ -53,11 +53,19 @@ struct PrepParams {
   __nv_bfloat16* dOq;       // [BHq][N][d]
   float* sdo;               // [BHq][nb]
   float* dq_acc;            // [BHq][N][d], zeroed
-  int BH, N, d, nb;
+  float* dk_acc;            // [BHk][N][d], zeroed
+  float* dv_acc;            // [BHk][N][d], zeroed
+  int BH, BHk, N, d, nb;
   int* status;
 };
 cudaError_t launch_bwd_prep(const PrepParams& p, cudaStream_t s);
-cudaError_t launch_dq_convert(const float* acc, __nv_bfloat16* dq, size_t n, cudaStream_t s);
+// FP32 gradient accumulators -> BF16 outputs, up to three arrays in one launch.
+struct ConvertJob {
+  const float* acc;
+  __nv_bfloat16* out;
+  size_t n;  // elements, a multiple of 4
+};
+cudaError_t launch_grad_convert(const ConvertJob* jobs, int njobs, cudaStream_t s);
 
 // ------------------------------------------------------------------ attention kernels
 struct FwdParams {
@@ -84,9 +92,10 @@ struct BwdParams {
   const float* sdo; // [BHq][nb]
   const float* lse; // [BHq][N]
   const float* D;   // [BHq][N]
+  int HS;           // query heads per CTA (a divisor of G)
   float* dq_acc;    // [BHq][N][d]
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  float* dk_acc;    // [BHk][N][d]
+  float* dv_acc;    // [BHk][N][d]
   int* status;
   uint64_t timeout_ns;
   uint32_t flags;
@@ -94,5 +103,8 @@ struct BwdParams {
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, int d, int causal,
                        cudaStream_t s);
+// Query heads per backward CTA: the divisor of G whose CTAs, dispatched longest
+// first onto `sms` multiprocessors, finish soonest (ties: more heads per CTA).
+int bwd_heads_per_cta(int B, int Hkv, int G, int nb, int causal, int sms);
 
 }  // namespace sagebwd

@@ -82,7 +82,7 @@ size_t sagebwd_saved_bytes(const sagebwd_problem* prob);
 /* Bytes of workspace for pass 0 (forward, sagebwd_fwd / sagebwd_quantize) or
  * pass 1 (backward, sagebwd_bwd).  The workspace holds the status word first,
  * then scratch (K-mean partial sums; D = rowsum(dO*O), the quantized dO and
- * its scales, the FP32 dQ accumulator).  Contents need no initialisation and
+ * its scales, the FP32 dQ, dK and dV accumulators).  Contents need no initialisation and
  * are not meaningful between calls, except the status word. */
 size_t sagebwd_workspace_bytes(const sagebwd_problem* prob, int pass);
 
@@ -125,11 +125,11 @@ sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const voi
  * on one stream, is exactly sagebwd_fwd / sagebwd_bwd.
  *   sagebwd_fwd_quantize  : K mean and the Q, K, V quantization into `saved`.
  *   sagebwd_fwd_attention : the fused forward kernel on `saved` -> o, lse.
- *   sagebwd_bwd_prepare   : D = rowsum(dO * O), quantized dO, zeroed dQ
- *                           accumulator (all in the backward workspace).
- *   sagebwd_bwd_attention : the fused backward kernel -> dk, dv and the FP32
- *                           dQ accumulator in the workspace.
- *   sagebwd_bwd_finish    : dQ accumulator -> BF16 dq.                       */
+ *   sagebwd_bwd_prepare   : D = rowsum(dO * O), quantized dO, zeroed dQ, dK
+ *                           and dV accumulators (all in the backward workspace).
+ *   sagebwd_bwd_attention : the fused backward kernel -> the FP32 dQ, dK, dV
+ *                           accumulators in the workspace.
+ *   sagebwd_bwd_finish    : the accumulators -> BF16 dq, dk, dv.             */
 sagebwd_status sagebwd_fwd_quantize(const sagebwd_problem* prob, const void* q, const void* k, const void* v,
                                     void* saved, void* ws, void* stream);
 sagebwd_status sagebwd_fwd_attention(const sagebwd_problem* prob, const void* saved, void* o, float* lse, void* ws,
@@ -137,8 +137,8 @@ sagebwd_status sagebwd_fwd_attention(const sagebwd_problem* prob, const void* sa
 sagebwd_status sagebwd_bwd_prepare(const sagebwd_problem* prob, const void* o, const void* dO, void* ws,
                                    void* stream);
 sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v, const void* dO, const float* lse,
-                                     const void* saved, void* dk, void* dv, void* ws, void* stream);
-sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* ws, void* stream);
+                                     const void* saved, void* ws, void* stream);
+sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* dk, void* dv, void* ws, void* stream);
 
 /* K quantization (K-smoothing mean + per-block codes), like
  * sagebwd_quantize(prob, SAGEBWD_K, ...), for callers that cannot allocate
