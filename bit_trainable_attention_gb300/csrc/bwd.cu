@@ -5,34 +5,40 @@
 // D = rowsum(dO * O) and dS = P (dP - D)).
 //
 // One CTA owns one 128-key block j of one kv head and loops over HS of the G
-// query heads of that kv head and their 128-query blocks i.  dK_j and dV_j are
-// summed in registers over those tiles and added once into FP32 accumulators;
-// dQ is accumulated across CTAs by TMA bulk reduce-adds into an FP32 workspace.
-// CTAs are numbered longest first (causal: small j has the most query blocks),
-// and HS is chosen on the host so that this list balances over the SMs.
-// Warp roles:
-//   warps 0-15   four compute warpgroups: thread (w, r) owns key row r
-//                (TMEM lane r), query columns [32w, 32w+32) of the tile and
-//                output columns [w d/4, (w+1) d/4) of dK, dV, dQ
-//   warp 16      TMA producer (K^_j, V_j once; dO_i, Q^_i, dO^_i per tile)
-//   warp 17      TMEM allocation and the MMA-issuing thread
-//   warp 18      dQ reducer: bulk reduce-add of each staged dQ tile
-//   warp 19      idle (completes the fifth warpgroup: 640 threads launch with
-//                96 registers each; that warpgroup drops to kRegsLow and the
-//                compute warpgroups rise to kRegsHigh)
-// TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d),
-// dQ [0,d) (reusing S^T once P is consumed).
-// Per tile i (MMAs in issue order; the compute passes between them):
-//   pass 1  P = 2^(S sQ sK scale log2e - LSE_i log2e), dS = P (dP - D_i), both
-//           written back to TMEM in place; row max of P, tile max of |dS|
-//   pass 2a code(P^T) per key row (scale max P / 127) -> shared A tile
-//     MMA  dV = P^T dO^_i
-//   pass 2b code(dS) per tile (scale max|dS| / 127) -> shared A tile
-//     MMA  dK = dS^T Q^_i, dQ = dS K^_j
-//     MMA  next tile's dP^T = V_j dO_i+1^T (BF16), then S^T = K^_j Q^_i+1^T once
-//          the dQ tile has been read (they overlap pass 3)
-//   pass 3  dequantize: dQ tile * scale sdS sK -> FP32 staging tile (reduced
-//           into global by the reducer warp); dV += sP sdO [.], dK += scale sdS sQ [.]
+// query heads of that kv head and their 128-query blocks i (the tiles).  dK_j
+// and dV_j are summed in registers over those tiles and added once into FP32
+// accumulators; dQ is accumulated across CTAs by TMA bulk reduce-adds into an
+// FP32 workspace.  CTAs are numbered longest first (causal: small j has the
+// most query blocks), and HS is chosen on the host so that this list balances
+// over the SMs.
+//
+// Warp roles (640 threads; the work of one tile flows S -> A while the tensor
+// core already computes the next tile's S^T and dP^T):
+//   warps 0-7   softmax warpgroups S (two): thread (s, r) owns key row r (TMEM
+//               lane r) and queries [64s, 64s+64) of the tile: P, dS, the codes
+//               of P^T (row scale: the two halves of a row exchange their maxima
+//               through shared memory) written to TMEM as the A operand of dV,
+//               and the codes of dS (tile scale) written to shared memory
+//   warps 8-15  accumulator warpgroups A (two): thread (a, r) owns output
+//               columns [a d/2, (a+1) d/2) of row r of dV and dK (FP32 sums in
+//               registers) and of the dQ tile it scales into the staging tile
+//   warp 16     TMA producer; warp 17 TMEM allocation and the MMA-issuing thread;
+//   warp 18     dQ reducer (bulk reduce-add of each staged half); warp 19 idle
+// Registers: 640 threads launch with 96 each; the last warpgroup drops to 32 and
+// the others rise (d = 128: S 64, A 160; 128 * 32 + 256 * 64 + 256 * 160 = 640 * 96).
+// TMEM columns: S^T / P [0,128), dP^T / dS [128,256), dV [256,256+d), dK
+// [256+d,256+2d).  d = 128: dQ reuses the dV columns once they are read and the
+// P^T codes sit in the first 64 dK columns until dV has read them; d = 64: dQ
+// [384,448), P^T codes [448,512).
+// MMA order per tile i (each waits for what it overwrites or reads):
+//   S^T(i+1) = K^_j Q^_i+1^T                 once the P of tile i has been coded
+//   dP^T(i+1) = V_j dO_i+1^T (BF16)          once the dS of tile i has been coded
+//   dV(i) = P^T codes (TMEM) x dO^_i
+//   dK(i) = dS^T Q^_i, dQ(i) = dS K^_j       from the shared dS code tile
+// so the softmax warpgroups wait for the next tile only while dP^T(i+1) runs.
+// Shared memory at d = 128 has room for one dO, dO^ stage and two Q^ stages, so
+// the FP32 dQ staging tile borrows the dO^ tile (after dV(i)) and the dS code
+// tile (after dK(i), dQ(i)); d = 64 double-buffers everything and has its own.
 #include <functional>
 #include <queue>
 #include <vector>
@@ -42,42 +48,50 @@
 namespace sagebwd {
 namespace {
 
-constexpr int kNWG = 4;                      // compute warpgroups
-constexpr int kCompute = kNWG * 128;          // compute threads
-constexpr int kThreads = kCompute + 128;      // + the producer / MMA / reducer warpgroup
-constexpr int kQC = 128 / kNWG;               // query columns per compute thread
-constexpr uint32_t kRegsLaunch = 96, kRegsLow = 64, kRegsHigh = 104;
-static_assert(128 * kRegsLow + kCompute * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
+constexpr int kBThreads = 640;
+constexpr uint32_t kBRegsLaunch = 96, kBRegsCtl = 32;
 
 template <int D>
 struct BwdCfg {
-  static constexpr int NS = D == 128 ? 1 : 2;  // stages of the per-tile operands
+  static constexpr bool ALIAS = D == 128;     // staging tile borrowed from dO^ and the dS codes
+  static constexpr int NS = D == 128 ? 1 : 2;  // dO, dO^ stages (Q^ always has two)
   static constexpr int TILE = 128 * D * 2;
-  static constexpr int PTILE = 128 * 128 * 2;
+  static constexpr int CTILE = 128 * 128 * 2;  // dS code tile
+  static constexpr uint32_t REG_S = D == 128 ? 64 : 96, REG_A = D == 128 ? 160 : 112;
+  static_assert(128 * kBRegsCtl + 256 * REG_S + 256 * REG_A <= kBThreads * kBRegsLaunch,
+                "register split exceeds the launch");
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_Q = OFF_V + TILE;
-  static constexpr int OFF_DO = OFF_Q + NS * TILE;
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;
   static constexpr int OFF_DOQ = OFF_DO + NS * TILE;
-  static constexpr int OFF_PT = OFF_DOQ + NS * TILE;  // P^T codes; with dS^T: the dQ staging tile
-  static constexpr int OFF_DST = OFF_PT + PTILE;
-  static constexpr int OFF_VEC = OFF_DST + PTILE;  // L2[128], Dv[128], pmax bits[128], am[16]
-  static constexpr int OFF_BAR = OFF_VEC + (128 + 128 + 128 + 16) * 4;
-  static constexpr int NBAR = 1 + 6 * NS + 12 + 1;
+  static constexpr int OFF_DST = OFF_DOQ + NS * TILE;
+  static constexpr int OFF_STG = OFF_DST + CTILE;  // own staging tile (d = 64 only)
+  static constexpr int OFF_VEC = OFF_STG + (ALIAS ? 0 : 128 * D * 4);
+  // -LSE log2 e [128], -D [128], P^T scale x sdO per row [2][128], dS scale [2], |dS| maxima [8],
+  // row maxima of P exchanged between the two softmax warpgroups [128]
+  static constexpr int VEC_FLOATS = 128 + 128 + 256 + 2 + 8 + 128;
+  static constexpr int OFF_BAR = OFF_VEC + ((VEC_FLOATS * 4 + 15) / 16) * 16;
+  static constexpr int NBAR = 1 + 4 + 4 * NS + 18;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
   // The tiles need a 1024-byte aligned base; the d = 128 layout leaves no room for padding.
   static constexpr int SMEM = BYTES + 1024 <= 232448 ? BYTES + 1024 : BYTES;
-  static constexpr int C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D, C_DQ = 0;
+  static constexpr int C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D, C_DQ = ALIAS ? C_DV : 256 + 2 * D,
+                       C_PC = ALIAS ? C_DK : 448;  // P^T codes (64 packed columns)
   static_assert(BYTES <= 232448, "shared memory beyond the per-CTA limit");
-  static_assert(128 * D * 4 <= 2 * PTILE, "the FP32 dQ staging tile must fit in the two code tiles");
+  static_assert(ALIAS ? (128 * D * 4 == NS * TILE + CTILE) : true, "the staging halves must fill dO^ and dS codes");
+  // FP32 dQ staging: D/32 boxes of [128 rows][32 floats] (16 KB, 128-byte swizzle)
+  __host__ __device__ static constexpr int stg_box(int b) {
+    return ALIAS ? (b < D / 64 ? OFF_DOQ + b * 16384 : OFF_DST + (b - D / 64) * 16384) : OFF_STG + b * 16384;
+  }
 };
 
 enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty, bSiteDOQFull, bSiteDOQEmpty,
-               bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAccV, bSiteAccQ, bSiteDQRead, bSiteTmemFree, bSiteDQStaged,
-               bSiteStagingFree, bSiteStagingFree2, bSiteC1, bSiteC2, bSiteAlign };
+               bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAccV, bSiteAccQ, bSiteAccK, bSiteTmemFreeV, bSiteDVQFree,
+               bSiteTmemFreeK, bSiteStaged, bSiteStgFree, bSiteC1, bSiteC2, bSiteC3, bSiteAlign };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmDOQ, const __grid_constant__ CUtensorMap tmDQ,
@@ -91,31 +105,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicCAS(p.status, 0, status_timeout(bSiteAlign));
     return;
   }
-  float* L2v = reinterpret_cast<float*>(smem + C::OFF_VEC);
-  float* Dv = L2v + 128;
-  int* pmx = reinterpret_cast<int*>(Dv + 128);      // [128] row maxima of P (P >= 0: float bits order as ints)
-  float* am = reinterpret_cast<float*>(pmx + 128);  // [16] per-warp maxima of |dS|
+  float* L2v = reinterpret_cast<float*>(smem + C::OFF_VEC);  // -LSE_q log2 e of the tile's queries
+  float* Dv = L2v + 128;                                      // -D_q
+  float* fv_ring = Dv + 128;                                  // [2][128] sP_row * sdO per tile parity
+  float* sds_ring = fv_ring + 256;                            // [2] dS scale per tile parity
+  float* am = sds_ring + 2;                                   // [8] per-warp maxima of |dS|
+  float* pm = am + 8;                                         // [128] row maxima of P (exchange)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* bar_kv = bars;
-  uint64_t* bar_q_full = bar_kv + 1;
-  uint64_t* bar_q_empty = bar_q_full + NS;
-  uint64_t* bar_do_full = bar_q_empty + NS;
-  uint64_t* bar_do_empty = bar_do_full + NS;
-  uint64_t* bar_doq_full = bar_do_empty + NS;
-  uint64_t* bar_doq_empty = bar_doq_full + NS;
-  uint64_t* bar_sdp = bar_doq_empty + NS;          // S^T and dP^T of the tile are in TMEM
-  uint64_t* bar_pt_ready = bar_sdp + 1;            // P^T codes written (compute)
-  uint64_t* bar_ds_ready = bar_pt_ready + 1;       // dS codes written, P / dS reads done (compute)
-  uint64_t* bar_acc_v = bar_ds_ready + 1;          // dV tile in TMEM
-  uint64_t* bar_acc_q = bar_acc_v + 1;             // dK and dQ tiles in TMEM
-  uint64_t* bar_dq_read = bar_acc_q + 1;           // dQ tile read out of TMEM (compute)
-  uint64_t* bar_tmem_free = bar_dq_read + 1;       // dV, dK tiles read out of TMEM (compute)
-  uint64_t* bar_dq_staged = bar_tmem_free + 1;     // FP32 dQ tile written to the staging tile (compute)
-  uint64_t* bar_staging_free = bar_dq_staged + 1;  // staging half in the P^T tile read by the reduce (reducer)
-  uint64_t* bar_staging_free2 = bar_staging_free + 1;  // staging half in the dS^T tile read (reducer)
-  uint64_t* bar_c1 = bar_staging_free2 + 1;        // compute threads: LSE / D of the tile stored
-  uint64_t* bar_c2 = bar_c1 + 1;                   // compute threads: row and tile maxima stored
-  uint64_t* bar_final = bar_c2 + 1;
+  uint64_t* bar_q_full = bar_kv + 1;              // [2]
+  uint64_t* bar_q_empty = bar_q_full + 2;         // [2]
+  uint64_t* bar_do_full = bar_q_empty + 2;        // [NS]
+  uint64_t* bar_do_empty = bar_do_full + NS;      // [NS]
+  uint64_t* bar_doq_full = bar_do_empty + NS;     // [NS]
+  uint64_t* bar_doq_empty = bar_doq_full + NS;    // [NS] (own staging only)
+  uint64_t* bar_sdp = bar_doq_empty + NS;         // S^T and dP^T of the tile in TMEM
+  uint64_t* bar_pt_ready = bar_sdp + 1;           // P^T codes in TMEM, tile scales stored (S)
+  uint64_t* bar_ds_ready = bar_pt_ready + 1;      // dS codes in shared memory, dS read (S)
+  uint64_t* bar_acc_v = bar_ds_ready + 1;         // dV tile in TMEM
+  uint64_t* bar_acc_q = bar_acc_v + 1;            // dQ tile in TMEM
+  uint64_t* bar_acc_k = bar_acc_q + 1;            // dK tile in TMEM (dS codes no longer read)
+  uint64_t* bar_tmem_free_v = bar_acc_k + 1;      // dV tile read (A; gates the aliased dQ)
+  uint64_t* bar_dvq_free = bar_tmem_free_v + 1;   // dV and dQ tiles read (A)
+  uint64_t* bar_tmem_free_k = bar_dvq_free + 1;   // dK tile read (A)
+  uint64_t* bar_staged = bar_tmem_free_k + 1;     // [2] staging half h written (A warpgroup h)
+  uint64_t* bar_stg_free = bar_staged + 2;        // [2] staging half h read by the reduce (reducer)
+  uint64_t* bar_c1 = bar_stg_free + 2;            // S: the tile's -LSE / -D vectors stored
+  uint64_t* bar_c2 = bar_c1 + 1;                  // S: |dS| maxima and half-row maxima of P stored
+  uint64_t* bar_c3 = bar_c2 + 1;                  // S: row maxima of P combined
+  uint64_t* bar_final = bar_c3 + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_final + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -131,29 +149,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ib0 = CAUSAL ? j : 0;
   const int nq = p.nb - ib0;
   const int T = p.HS * nq;
+  auto tile_bhq = [&](int t) { return b * p.Hq + hq0 + t / nq; };
+  auto tile_ib = [&](int t) { return ib0 + t % nq; };
 
   if (tid == 0) {
     mbar_init(bar_kv, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar_q_full + s, 1);
       mbar_init(bar_q_empty + s, 1);
+      mbar_init(bar_staged + s, 128);
+      mbar_init(bar_stg_free + s, 1);
+    }
+    for (int s = 0; s < NS; ++s) {
       mbar_init(bar_do_full + s, 1);
       mbar_init(bar_do_empty + s, 1);
       mbar_init(bar_doq_full + s, 1);
       mbar_init(bar_doq_empty + s, 1);
     }
     mbar_init(bar_sdp, 1);
-    mbar_init(bar_pt_ready, kCompute);
-    mbar_init(bar_ds_ready, kCompute);
+    mbar_init(bar_pt_ready, 256);
+    mbar_init(bar_ds_ready, 256);
     mbar_init(bar_acc_v, 1);
     mbar_init(bar_acc_q, 1);
-    mbar_init(bar_dq_read, kCompute);
-    mbar_init(bar_tmem_free, kCompute);
-    mbar_init(bar_dq_staged, kCompute);
-    mbar_init(bar_staging_free, 1);
-    mbar_init(bar_staging_free2, 1);
-    mbar_init(bar_c1, kCompute);
-    mbar_init(bar_c2, kCompute);
+    mbar_init(bar_acc_k, 1);
+    mbar_init(bar_tmem_free_v, 256);
+    mbar_init(bar_dvq_free, 256);
+    mbar_init(bar_tmem_free_k, 256);
+    mbar_init(bar_c1, 256);
+    mbar_init(bar_c2, 256);
+    mbar_init(bar_c3, 128);
     mbar_init(bar_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -169,54 +193,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
   if (warp >= 16) {
-    setmaxnreg_dec<kRegsLow>();
+    setmaxnreg_to<kBRegsCtl, kBRegsLaunch>();
     if (warp == 16 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
-      int q_iss[NS], do_iss[NS], doq_iss[NS];
-      for (int s = 0; s < NS; ++s) q_iss[s] = do_iss[s] = doq_iss[s] = 0;
+      int q_iss[2] = {0, 0}, do_iss[NS], doq_iss[NS];
+      for (int s = 0; s < NS; ++s) do_iss[s] = doq_iss[s] = 0;
       mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
       for (int c = 0; c < D / 64; ++c) {
         tma_load_3d(smem + C::OFF_K + c * 16384, &tmK, bar_kv, c * 64, k0, bhk);
         tma_load_3d(smem + C::OFF_V + c * 16384, &tmV, bar_kv, c * 64, k0, bhk);
       }
-      for (int it = 0; it < T; ++it) {
-        const int s = it % NS, n = it / NS;
-        const int bhq = b * p.Hq + hq0 + it / nq;
-        const int i0 = (ib0 + it % nq) * kBlk;
-        // dO is released first (after dP), then Q^ (after dK), then dO^ (after dV)
-        if (it >= NS && !wait1(wc, bar_do_empty + s, (n - 1) & 1, bSiteDOEmpty)) break;
-        mbar_arrive_expect_tx(bar_do_full + s, C::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_DO + s * C::TILE + c * 16384, &tmDO, bar_do_full + s, c * 64, i0, bhq);
-        do_iss[s] = n + 1;
-        if (it >= NS && !wait1(wc, bar_q_empty + s, (n - 1) & 1, bSiteQEmpty)) break;
-        mbar_arrive_expect_tx(bar_q_full + s, C::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * 16384, &tmQ, bar_q_full + s, c * 64, i0, bhq);
-        q_iss[s] = n + 1;
-        if (it >= NS && !wait1(wc, bar_doq_empty + s, (n - 1) & 1, bSiteDOQEmpty)) break;
+      // dO and Q^ of tile it, then dO^ of tile it-1: the dO^ slot frees late on d = 128
+      // (it holds the previous tile's dQ staging half 0), and the next tile's Q^ and dO
+      // must not queue behind it
+      auto load_doq = [&](int t) -> bool {
+        const int s = t % NS, n = t / NS;
+        if (C::ALIAS) {
+          if (t >= 1 && !wait1(wc, bar_stg_free, (t - 1) & 1, bSiteStgFree)) return false;
+        } else {
+          if (t >= NS && !wait1(wc, bar_doq_empty + s, (n - 1) & 1, bSiteDOQEmpty)) return false;
+        }
         mbar_arrive_expect_tx(bar_doq_full + s, C::TILE);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_DOQ + s * C::TILE + c * 16384, &tmDOQ, bar_doq_full + s, c * 64, i0, bhq);
+          tma_load_3d(smem + C::OFF_DOQ + s * C::TILE + c * 16384, &tmDOQ, bar_doq_full + s, c * 64,
+                      tile_ib(t) * kBlk, tile_bhq(t));
         doq_iss[s] = n + 1;
+        return true;
+      };
+      for (int it = 0; it <= T; ++it) {
+        if (it < T) {
+          const int s = it % NS, n = it / NS, sq = it & 1, nq2 = it >> 1;
+          const int bhq = tile_bhq(it), i0 = tile_ib(it) * kBlk;
+          if (it >= NS && !wait1(wc, bar_do_empty + s, (n - 1) & 1, bSiteDOEmpty)) break;
+          mbar_arrive_expect_tx(bar_do_full + s, C::TILE);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::OFF_DO + s * C::TILE + c * 16384, &tmDO, bar_do_full + s, c * 64, i0, bhq);
+          do_iss[s] = n + 1;
+          if (it >= 2 && !wait1(wc, bar_q_empty + sq, (nq2 - 1) & 1, bSiteQEmpty)) break;
+          mbar_arrive_expect_tx(bar_q_full + sq, C::TILE);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::OFF_Q + sq * C::TILE + c * 16384, &tmQ, bar_q_full + sq, c * 64, i0, bhq);
+          q_iss[sq] = nq2 + 1;
+        }
+        if (it >= 1 && !load_doq(it - 1)) break;
       }
+      // Copies still in flight must land before the CTA's shared memory is released.
       drain(bar_kv, 0, p.timeout_ns);
-      for (int s = 0; s < NS; ++s) {
+      for (int s = 0; s < 2; ++s)
         if (q_iss[s]) drain(bar_q_full + s, (q_iss[s] - 1) & 1, p.timeout_ns);
+      for (int s = 0; s < NS; ++s) {
         if (do_iss[s]) drain(bar_do_full + s, (do_iss[s] - 1) & 1, p.timeout_ns);
         if (doq_iss[s]) drain(bar_doq_full + s, (doq_iss[s] - 1) & 1, p.timeout_ns);
       }
     } else if (warp == 17 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-      const uint32_t idKM = idesc_bf16_f32(128, D, false, true);     // dK, dV: A K-major, B MN-major
+      const uint32_t idKM = idesc_bf16_f32(128, D, false, true);     // dK (SS), dV (TS): B MN-major
       const uint32_t idQM = idesc_bf16_f32(128, D, true, true);      // dQ: A MN-major, B MN-major
-      // Descriptor low words are built once per buffer; the chained MMAs add the per-K-step
-      // offsets (no carry: shared addresses stay below 2^18).
+      // Descriptor low words (the chained MMAs add the per-K-step offsets; no carry:
+      // shared addresses stay below 2^18).
       const uint32_t dK_k = sdesc_sw128_lo(smem_u32(smem + C::OFF_K), 16);
       const uint32_t dK_mn = sdesc_sw128_lo(smem_u32(smem + C::OFF_K), 16384);
       const uint32_t dV_k = sdesc_sw128_lo(smem_u32(smem + C::OFF_V), 16);
-      const uint32_t dPT_k = sdesc_sw128_lo(smem_u32(smem + C::OFF_PT), 16);
       const uint32_t dDS_k = sdesc_sw128_lo(smem_u32(smem + C::OFF_DST), 16);
       const uint32_t dDS_mn = sdesc_sw128_lo(smem_u32(smem + C::OFF_DST), 16384);
       auto dQ_k = [&](int st) { return sdesc_sw128_lo(smem_u32(smem + C::OFF_Q + st * C::TILE), 16); };
@@ -229,297 +267,360 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           umma_chain4_kk(tmem + d_col, sdesc_from_lo(a_lo), sdesc_from_lo(b_lo), idesc);
       };
-      auto issue_dp = [&](int s) {
-        chain_kk(C::C_DP, dV_k, dDO_k(s), idSS);
-        umma_commit(bar_do_empty + s);
-      };
-      auto issue_s = [&](int s) {
-        chain_kk(C::C_S, dK_k, dQ_k(s), idSS);
-        umma_commit(bar_sdp);  // also covers the dP^T issued before it
-      };
-      bool ok = wait1(wc, bar_kv, 0, bSiteKV) && wait1(wc, bar_do_full, 0, bSiteDOFull) &&
-                wait1(wc, bar_q_full, 0, bSiteQFull);
+      bool ok = wait1(wc, bar_kv, 0, bSiteKV) && wait1(wc, bar_q_full, 0, bSiteQFull) &&
+                wait1(wc, bar_do_full, 0, bSiteDOFull);
       if (ok) {
         tc_fence_after();
-        issue_dp(0);
-        issue_s(0);
+        chain_kk(C::C_S, dK_k, dQ_k(0), idSS);
+        chain_kk(C::C_DP, dV_k, dDO_k(0), idSS);
+        umma_commit(bar_sdp);
+        umma_commit(bar_do_empty);
       }
       for (int it = 0; ok && it < T; ++it) {
         const int s = it % NS;
         const uint32_t ph = (it / NS) & 1;
-        // dV = P^T dO^  (A: P^T tile [key][query], K-major; B: dO^ [query][d], MN-major)
+        const bool next = it + 1 < T;
+        // S^T of the next tile once the P of this tile has been read into codes
         if (!wait1(wc, bar_pt_ready, it & 1, bSitePTReady)) break;
-        if (!wait1(wc, bar_doq_full + s, ph, bSiteDOQFull)) break;
-        if (it >= 1 && !wait1(wc, bar_tmem_free, (it - 1) & 1, bSiteTmemFree)) break;
-        tc_fence_after();
-        umma_chain8_km(tmem + C::C_DV, sdesc_from_lo(dPT_k), sdesc_from_lo(dDOQ_mn(s)), idKM);
-        umma_commit(bar_doq_empty + s);
-        umma_commit(bar_acc_v);
-        // dK = dS^T Q^  (A: dS^T tile [key][query], K-major; B: Q^ [query][d], MN-major)
+        if (next) {
+          const int sq = (it + 1) & 1;
+          if (!wait1(wc, bar_q_full + sq, ((it + 1) >> 1) & 1, bSiteQFull)) break;
+          tc_fence_after();
+          chain_kk(C::C_S, dK_k, dQ_k(sq), idSS);
+        }
+        // dP^T of the next tile once dS is coded (its columns are free)
         if (!wait1(wc, bar_ds_ready, it & 1, bSiteDSReady)) break;
+        if (next) {
+          const int s2 = (it + 1) % NS;
+          if (!wait1(wc, bar_do_full + s2, ((it + 1) / NS) & 1, bSiteDOFull)) break;
+          tc_fence_after();
+          chain_kk(C::C_DP, dV_k, dDO_k(s2), idSS);
+          umma_commit(bar_sdp);  // covers S^T(i+1) issued above
+          umma_commit(bar_do_empty + s2);
+        }
+        // dV = P^T dO^: A = the P^T codes in TMEM (row = key, 128 queries = 64 packed
+        // columns, 8 per K step), B = dO^ [query][d] read MN-major
+        if (!wait1(wc, bar_doq_full + s, ph, bSiteDOQFull)) break;
+        if (it >= 1 && !wait1(wc, bar_dvq_free, (it - 1) & 1, bSiteDVQFree)) break;
         tc_fence_after();
-        umma_chain8_km(tmem + C::C_DK, sdesc_from_lo(dDS_k), sdesc_from_lo(dQ_mn(s)), idKM);
-        umma_commit(bar_q_empty + s);
-        // dQ = dS K^  (A: the same dS^T tile read MN-major as [query][key]; B: K^ [key][d], MN-major)
+        {
+          const uint32_t bdesc = dDOQ_mn(s);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + C::C_DV, tmem + C::C_PC + kk * 8, sdesc_from_lo(bdesc + kk * 128), idKM, kk > 0);
+        }
+        umma_commit(bar_acc_v);
+        if (!C::ALIAS) umma_commit(bar_doq_empty + s);
+        // dK = dS^T Q^  (A: dS^T codes [key][query], K-major; B: Q^ [query][d], MN-major);
+        // on d = 128 it overwrites the P^T codes, so dV must have read them
+        if (C::ALIAS && !wait1(wc, bar_acc_v, it & 1, bSiteAccV)) break;
+        if (it >= 1 && !wait1(wc, bar_tmem_free_k, (it - 1) & 1, bSiteTmemFreeK)) break;
+        tc_fence_after();
+        umma_chain8_km(tmem + C::C_DK, sdesc_from_lo(dDS_k), sdesc_from_lo(dQ_mn(it & 1)), idKM);
+        umma_commit(bar_acc_k);
+        umma_commit(bar_q_empty + (it & 1));
+        // dQ = dS K^  (A: the dS^T code tile read MN-major as [query][key]; B: K^ [key][d], MN-major)
+        if (C::ALIAS && !wait1(wc, bar_tmem_free_v, it & 1, bSiteTmemFreeV)) break;
+        tc_fence_after();
         umma_chain8_mm(tmem + C::C_DQ, sdesc_from_lo(dDS_mn), sdesc_from_lo(dK_mn), idQM);
         umma_commit(bar_acc_q);
-        // the next tile's dP^T now (its columns are free), its S^T once the dQ tile is read
-        if (it + 1 < T) {
-          const int s2 = (it + 1) % NS;
-          const uint32_t ph2 = ((it + 1) / NS) & 1;
-          if (!wait1(wc, bar_do_full + s2, ph2, bSiteDOFull)) break;
-          tc_fence_after();
-          issue_dp(s2);
-          if (!wait1(wc, bar_q_full + s2, ph2, bSiteQFull)) break;
-          if (!wait1(wc, bar_dq_read, it & 1, bSiteDQRead)) break;
-          tc_fence_after();
-          issue_s(s2);
-        }
       }
       // Every MMA issued above must complete before TMEM is released.
       umma_commit(bar_final);
       drain(bar_final, 0, p.timeout_ns);
     } else if (warp == 18 && lane == 0) {
       // ---------------------------------------------------------- dQ reducer
-      // The FP32 dQ tile is staged as D/32 boxes of [128 rows][32 floats]: the first half of
-      // the boxes in the P^T code tile, the second half in the dS^T code tile.  Each half is
-      // its own bulk group, so the P^T tile is released as soon as its half has been read.
-      const uint8_t* staging = smem + C::OFF_PT;
-      const uint8_t* staging2 = smem + C::OFF_DST;
+      // Half h of the FP32 dQ tile (columns [h d/2, (h+1) d/2)) is staged by accumulator
+      // warpgroup h.  Half 1 goes first: on d = 128 it occupies the dS code tile that the
+      // softmax warpgroups need next; both reduces run at once and each half is released
+      // as soon as its own read has finished.
       for (int it = 0; it < T; ++it) {
-        if (!wait1(wc, bar_dq_staged, it & 1, bSiteDQStaged)) break;
-        const int bhq = b * p.Hq + hq0 + it / nq;
-        const int i0 = (ib0 + it % nq) * kBlk;
+        const int bhq = tile_bhq(it), i0 = tile_ib(it) * kBlk;
+        if (!wait1(wc, bar_staged + 1, it & 1, bSiteStaged)) break;
 #pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx) tma_reduce_add_3d(&tmDQ, staging + bx * 16384, bx * 32, i0, bhq);
+        for (int bx = D / 64; bx < D / 32; ++bx) tma_reduce_add_3d(&tmDQ, smem + C::stg_box(bx), bx * 32, i0, bhq);
         bulk_commit_group();
+        if (!wait1(wc, bar_staged, it & 1, bSiteStaged)) break;
 #pragma unroll
-        for (int bx = D / 64; bx < D / 32; ++bx)
-          tma_reduce_add_3d(&tmDQ, staging2 + (bx - D / 64) * 16384, bx * 32, i0, bhq);
+        for (int bx = 0; bx < D / 64; ++bx) tma_reduce_add_3d(&tmDQ, smem + C::stg_box(bx), bx * 32, i0, bhq);
         bulk_commit_group();
         bulk_wait_group_read<1>();
-        mbar_arrive(bar_staging_free);
+        mbar_arrive(bar_stg_free + 1);
         bulk_wait_group_read<0>();
-        mbar_arrive(bar_staging_free2);
+        mbar_arrive(bar_stg_free);
       }
       bulk_wait_group0();
     }
-  } else {
-    setmaxnreg_inc<kRegsHigh>();
-    // ------------------------------------------------------------ compute warpgroups
-    constexpr int DC = D / kNWG;       // output columns per thread
-    const int w = warp >> 2;           // compute warpgroup 0..kNWG-1
+  } else if (warp < 8) {
+    setmaxnreg_to<C::REG_S, kBRegsLaunch>();
+    // ------------------------------------------------------------ softmax warpgroups
+    const int ws = warp >> 2;          // query half [64 ws, 64 ws + 64)
     const int r = tid & 127;           // key row == TMEM lane
-    const int ct = tid;                // index among the compute threads
+    const int qc0 = 64 * ws;           // first query column of this thread
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int kglob = k0 + r;
-    const bool key_ok = kglob < p.N;
+    const uint32_t s_addr = tmem + lane_base + C::C_S + qc0, dp_addr = tmem + lane_base + C::C_DP + qc0;
+    const uint32_t pc_addr = tmem + lane_base + C::C_PC + qc0 / 2;
+    const bool key_ok = k0 + r < p.N;
     const float sKv = p.sk[(size_t)bhk * p.nb + j];
-    const uint32_t pt_base = smem_u32(smem + C::OFF_PT), ds_base = smem_u32(smem + C::OFF_DST);
-    uint64_t dv_run[DC / 2], dk_run[DC / 2];  // packed FP32 pairs (columns c, c + 1)
-#pragma unroll
-    for (int c = 0; c < DC / 2; ++c) dv_run[c] = dk_run[c] = 0ull;
-
-    // Per-tile LSE (base 2) / D values (stored negated: they enter as addends) and
-    // block scales, loaded one tile ahead so that their global-memory latency hides
-    // behind the current tile.
-    const int q_own = ct & 127;
+    const uint32_t ds_base = smem_u32(smem + C::OFF_DST);
+    const uint32_t l2v_s = smem_u32(L2v), dv_s = smem_u32(Dv);
+    // Per tile: half 0 stores -LSE (base 2) of query r, half 1 stores -D (-inf / 0
+    // past N); loaded one tile ahead so that their latency hides behind the current tile.
     auto tile_vec = [&](int t) -> float {
-      const int bq = b * p.Hq + hq0 + t / nq;
-      const int row = (ib0 + t % nq) * kBlk + q_own;
-      const bool in = row < p.N;
-      if (ct < 128) return in ? -__fmul_rn(p.lse[(size_t)bq * p.N + row], kLog2e) : -INFINITY;
-      if (ct < 256) return in ? -p.D[(size_t)bq * p.N + row] : 0.f;
-      return 0.f;
+      const int row = tile_ib(t) * kBlk + r;
+      if (row >= p.N) return ws == 0 ? -INFINITY : 0.f;
+      const size_t idx = (size_t)tile_bhq(t) * p.N + row;
+      return ws == 0 ? -__fmul_rn(p.lse[idx], kLog2e) : -p.D[idx];
     };
-    auto tile_sq = [&](int t) { return p.sq[(size_t)(b * p.Hq + hq0 + t / nq) * p.nb + ib0 + t % nq]; };
-    auto tile_sdo = [&](int t) { return p.sdo[(size_t)(b * p.Hq + hq0 + t / nq) * p.nb + ib0 + t % nq]; };
+    auto tile_sq = [&](int t) { return p.sq[(size_t)tile_bhq(t) * p.nb + tile_ib(t)]; };
+    auto tile_sdo = [&](int t) { return p.sdo[(size_t)tile_bhq(t) * p.nb + tile_ib(t)]; };
     float pf_vec = tile_vec(0), pf_sq = tile_sq(0), pf_sdo = tile_sdo(0);
+    const float2 kMagic2 = make_float2(12582912.0f, 12582912.0f), kNegMagic2 = make_float2(-12582912.0f, -12582912.0f);
 
     for (int it = 0; it < T; ++it) {
-      const int ib = ib0 + it % nq;
-      // -LSE (base 2) and -D of the tile's queries (-inf / 0 past N); reset the row maxima
-      if (ct < 128)
-        L2v[q_own] = pf_vec;
-      else if (ct < 256)
-        Dv[q_own] = pf_vec;
-      else if (ct < 384)
-        pmx[q_own] = 0;
+      const int ib = tile_ib(it);
+      // the vectors of the previous tile were last read before its c2
+      (ws == 0 ? L2v : Dv)[r] = pf_vec;
       const float sQt = pf_sq, sdOt = pf_sdo;
       if (it + 1 < T) {
         pf_vec = tile_vec(it + 1);
         pf_sq = tile_sq(it + 1);
         pf_sdo = tile_sdo(it + 1);
       }
-      // (mbarriers rather than bar.sync, so that these waits are bounded too)
       mbar_arrive(bar_c1);
       if (!waitw(wc, bar_c1, it & 1, bSiteC1)) break;
       const float qks = __fmul_rn(__fmul_rn(sQt, sKv), p.c0);
+      const float2 qks2 = make_float2(qks, qks);
       const bool diag = CAUSAL && ib == j;
+      const bool masked = diag || (k0 + kBlk > p.N);
       if (!waitw(wc, bar_sdp, it & 1, bSiteSDP)) break;
       tc_fence_after();
-      // pass 1
+      // pass 1: P = 2^(S sQ sK scale log2e - LSE log2e), dS = P (dP - D), written back in
+      // place; the next chunk's TMEM loads are in flight while a chunk is computed
       float pmax = 0.f, amax = 0.f;
-      const float2 qks2 = make_float2(qks, qks);
-      const bool masked = diag || (k0 + kBlk > p.N);
+      {
+        uint32_t sv[2][8], dpv[2][8];
+        tmem_ld8(s_addr, sv[0]);
+        tmem_ld8(dp_addr, dpv[0]);
 #pragma unroll
-      for (int c0 = 0; c0 < kQC; c0 += 8) {
-        const int col = kQC * w + c0;  // query column within the tile
-        uint32_t sv[8], dpv[8];        // S -> P and dP -> dS, converted in place
-        tmem_ld8(tmem + lane_base + C::C_S + col, sv);
-        tmem_ld8(tmem + lane_base + C::C_DP + col, dpv);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e4 = 0; e4 < 8; e4 += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(L2v + col + e4);  // -LSE log2 e
-          const float4 d4 = *reinterpret_cast<const float4*>(Dv + col + e4);   // -D
-#pragma unroll
-          for (int e2 = 0; e2 < 4; e2 += 2) {
-            const int e = e4 + e2;
-            const float2 nl = e2 == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
-            const float2 nd = e2 == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
-            const float2 x = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), qks2, nl);
-            float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            if (masked) {
-              if (!key_ok || (diag && col + e < r)) pr.x = 0.f;
-              if (!key_ok || (diag && col + e + 1 < r)) pr.y = 0.f;
-            }
-            const float2 ds =
-                fmul2(pr, fadd2(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), nd));
-            pmax = fmax3(pmax, pr.x, pr.y);
-            amax = fmax3(amax, fabsf(ds.x), fabsf(ds.y));
-            sv[e] = __float_as_uint(pr.x);
-            sv[e + 1] = __float_as_uint(pr.y);
-            dpv[e] = __float_as_uint(ds.x);
-            dpv[e + 1] = __float_as_uint(ds.y);
+        for (int c = 0; c < 8; ++c) {
+          const int cur = c & 1;
+          tmem_ld_wait_regs(sv[cur]);
+          tmem_ld_wait_regs(dpv[cur]);
+          if (c + 1 < 8) {
+            tmem_ld8(s_addr + (c + 1) * 8, sv[cur ^ 1]);
+            tmem_ld8(dp_addr + (c + 1) * 8, dpv[cur ^ 1]);
           }
+#pragma unroll
+          for (int e4 = 0; e4 < 8; e4 += 4) {
+            const int q = qc0 + c * 8 + e4;  // query column within the tile
+            const float4 l4 = ld_shared_v4_f32(l2v_s + q * 4);
+            const float4 d4 = ld_shared_v4_f32(dv_s + q * 4);
+#pragma unroll
+            for (int e2 = 0; e2 < 4; e2 += 2) {
+              const int e = e4 + e2;
+              const float2 nl = e2 == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+              const float2 nd = e2 == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+              const float2 x =
+                  ffma2(make_float2(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])), qks2, nl);
+              float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              if (masked) {
+                if (!key_ok || (diag && q + e2 < r)) pr.x = 0.f;
+                if (!key_ok || (diag && q + e2 + 1 < r)) pr.y = 0.f;
+              }
+              const float2 ds = fmul2(
+                  pr, fadd2(make_float2(__uint_as_float(dpv[cur][e]), __uint_as_float(dpv[cur][e + 1])), nd));
+              pmax = fmax3(pmax, pr.x, pr.y);
+              amax = fmax3(amax, fabsf(ds.x), fabsf(ds.y));
+              sv[cur][e] = __float_as_uint(pr.x);
+              sv[cur][e + 1] = __float_as_uint(pr.y);
+              dpv[cur][e] = __float_as_uint(ds.x);
+              dpv[cur][e + 1] = __float_as_uint(ds.y);
+            }
+          }
+          tmem_st8(s_addr + c * 8, sv[cur]);
+          tmem_st8(dp_addr + c * 8, dpv[cur]);
         }
-        tmem_st8(tmem + lane_base + C::C_S + col, sv);
-        tmem_st8(tmem + lane_base + C::C_DP + col, dpv);
       }
       tmem_st_wait();
-      atomicMax(pmx + r, __float_as_int(pmax));
+      // tile maximum of |dS| over the 8 softmax warps; row maximum of P over the two halves:
+      // half 0 publishes its maximum, half 1 combines and publishes the row's
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (lane == 0) am[warp] = amax;
+      if (ws == 0) pm[r] = pmax;
       mbar_arrive(bar_c2);
       if (!waitw(wc, bar_c2, it & 1, bSiteC2)) break;
-      const float cmax = __int_as_float(pmx[r]);
+      if (ws == 1) {
+        pmax = fmaxf(pmax, pm[r]);
+        pm[r] = pmax;
+        mbar_arrive(bar_c3);
+      } else {
+        if (!waitw(wc, bar_c3, it & 1, bSiteC3)) break;
+        pmax = pm[r];
+      }
       float a = am[0];
 #pragma unroll
-      for (int q = 1; q < kCompute / 32; ++q) a = fmaxf(a, am[q]);
-      const bool p_live = cmax >= kMinGroupMax, d_live = a >= kMinGroupMax;
+      for (int q = 1; q < 8; ++q) a = fmaxf(a, am[q]);
+      const bool p_live = pmax >= kMinGroupMax, d_live = a >= kMinGroupMax;
       // hardware reciprocal (<= 2 ulp) rather than IEEE division: these scales only
       // decide codes of this tile and dequantize it; a code at a rounding tie may differ
-      const float invP = p_live ? __fdividef(127.f, cmax) : 0.f;
-      const float sPc = p_live ? cmax * (1.f / 127.f) : 0.f;
+      const float invP = p_live ? __fdividef(127.f, pmax) : 0.f;
+      const float sPc = p_live ? pmax * (1.f / 127.f) : 0.f;
       const float invA = d_live ? __fdividef(127.f, a) : 0.f;
       const float sDS = d_live ? a * (1.f / 127.f) : 0.f;
-      const float2 invP2 = make_float2(invP, invP), invA2 = make_float2(invA, invA);
-      // codes = rint(x) by adding and removing 1.5 * 2^23 (exact for |x| < 2^22)
-      const float2 kMagic2 = make_float2(12582912.0f, 12582912.0f), kNegMagic2 = make_float2(-12582912.0f, -12582912.0f);
-      // the code tiles double as the dQ staging tile: wait until the last reduce has read its half
-      if (it >= 1 && !waitw(wc, bar_staging_free, (it - 1) & 1, bSiteStagingFree)) break;
-      // pass 2a: codes of P^T into the swizzled A tile (row = key r, 16-byte chunk = 8 queries)
+      if (ws == 0) fv_ring[(it & 1) * 128 + r] = __fmul_rn(sPc, sdOt);
+      if (tid == 0) sds_ring[it & 1] = sDS;
+      // pass 2a: codes of P^T (row scale), 32 queries -> 16 packed columns, over the previous
+      // tile's codes: dV(i-1) must have read them (d = 64), and on d = 128, where they share
+      // the dK columns, dK(i-1) must have been read too (which implies the former)
+      if (it >= 1 && !(C::ALIAS ? waitw(wc, bar_tmem_free_k, (it - 1) & 1, bSiteTmemFreeK)
+                                : waitw(wc, bar_acc_v, (it - 1) & 1, bSiteAccV)))
+        break;
+      tc_fence_after();
       {
+        const float2 invP2 = make_float2(invP, invP);
 #pragma unroll
-        for (int h = 0; h < kQC; h += 16) {
-          uint32_t pv[16];
-          tmem_ld16(tmem + lane_base + C::C_S + kQC * w + h, pv);
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(s_addr + c0, v);
           tmem_ld_wait();
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
+          for (int e = 0; e < 32; e += 2) {
             const float2 cd = fadd2(
-                fadd2(fmul2(make_float2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), invP2), kMagic2), kNegMagic2);
-            pv[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+                fadd2(fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invP2), kMagic2),
+                kNegMagic2);
+            pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
           }
-          st_shared_v4(pt_base + sw128_offset(r, ((kQC * w + h) >> 3)), pv[0], pv[1], pv[2], pv[3]);
-          st_shared_v4(pt_base + sw128_offset(r, ((kQC * w + h) >> 3) + 1), pv[4], pv[5], pv[6], pv[7]);
+          tmem_st16(pc_addr + (c0 >> 1), pk);
         }
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
       mbar_arrive(bar_pt_ready);
-      // pass 2b: codes of dS (one scale per tile)
-      if (it >= 1 && !waitw(wc, bar_staging_free2, (it - 1) & 1, bSiteStagingFree2)) break;
+      // pass 2b: codes of dS (tile scale) into the shared A tile [key r][query], 16-byte
+      // chunk = 8 queries, 128-byte swizzle, over the previous tile's codes: dK(i-1) and
+      // dQ(i-1) must have read them (d = 64), and on d = 128 the tile is then the previous
+      // tile's dQ staging half 1 until the reducer has read it (which implies the former)
+      if (it >= 1 && !(C::ALIAS ? waitw(wc, bar_stg_free + 1, (it - 1) & 1, bSiteStgFree)
+                                : waitw(wc, bar_acc_q, (it - 1) & 1, bSiteAccQ)))
+        break;
       {
+        const float2 invA2 = make_float2(invA, invA);
 #pragma unroll
-        for (int h = 0; h < kQC; h += 16) {
-          uint32_t dsv[16];
-          tmem_ld16(tmem + lane_base + C::C_DP + kQC * w + h, dsv);
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(dp_addr + c0, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
+          for (int e = 0; e < 32; e += 2) {
             const float2 cd = fadd2(
-                fadd2(fmul2(make_float2(__uint_as_float(dsv[e]), __uint_as_float(dsv[e + 1])), invA2), kMagic2),
+                fadd2(fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invA2), kMagic2),
                 kNegMagic2);
-            dsv[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+            v[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
           }
-          st_shared_v4(ds_base + sw128_offset(r, ((kQC * w + h) >> 3)), dsv[0], dsv[1], dsv[2], dsv[3]);
-          st_shared_v4(ds_base + sw128_offset(r, ((kQC * w + h) >> 3) + 1), dsv[4], dsv[5], dsv[6], dsv[7]);
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+            st_shared_v4(ds_base + sw128_offset(r, ((qc0 + c0) >> 3) + h), v[4 * h], v[4 * h + 1], v[4 * h + 2],
+                         v[4 * h + 3]);
         }
       }
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar_ds_ready);
-      // pass 3: dV first (its MMA finishes first), then dQ (frees the S^T columns for
-      // the next tile), then dK
-      const float fv = __fmul_rn(sPc, sdOt);
+    }
+  } else {
+    setmaxnreg_to<C::REG_A, kBRegsLaunch>();
+    // ------------------------------------------------------------ accumulator warpgroups
+    constexpr int DH = D / 2;           // output columns per thread
+    const int wa = (warp - 8) >> 2;     // accumulator warpgroup 0 / 1
+    const int r = tid & 127;            // key row == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int kglob = k0 + r;
+    const float sKv = p.sk[(size_t)bhk * p.nb + j];
+    uint64_t dv_run[DH / 2], dk_run[DH / 2];  // packed FP32 pairs (columns c, c + 1)
+#pragma unroll
+    for (int c = 0; c < DH / 2; ++c) dv_run[c] = dk_run[c] = 0ull;
+    float sq_next = p.sq[(size_t)tile_bhq(0) * p.nb + tile_ib(0)];
+
+    for (int it = 0; it < T; ++it) {
+      const float sQt = sq_next;
+      if (it + 1 < T) sq_next = p.sq[(size_t)tile_bhq(it + 1) * p.nb + tile_ib(it + 1)];
+      if (!waitw(wc, bar_acc_v, it & 1, bSiteAccV)) break;
+      // the tile's scales were stored before the P^T codes were released
+      if (!waitw(wc, bar_pt_ready, it & 1, bSitePTReady)) break;
+      tc_fence_after();
+      const float fv = fv_ring[(it & 1) * 128 + r];
+      const float sDS = sds_ring[it & 1];
       const float fk = __fmul_rn(__fmul_rn(p.sc, sDS), sQt);
       const float fq = __fmul_rn(__fmul_rn(p.sc, sDS), sKv);
-      const uint64_t fv2 = pack_f32x2(fv, fv), fk2 = pack_f32x2(fk, fk);
-      const float2 fq2 = make_float2(fq, fq);
-      if (!waitw(wc, bar_acc_v, it & 1, bSiteAccV)) break;
-      tc_fence_after();
+      {
+        const uint64_t fv2 = pack_f32x2(fv, fv);
 #pragma unroll
-      for (int c0 = 0; c0 < DC; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_base + C::C_DV + w * DC + c0, v);
-        tmem_ld_wait();
+        for (int c0 = 0; c0 < DH; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + C::C_DV + wa * DH + c0, v);
+          tmem_ld_wait_regs(v);
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) ffma2_acc(dv_run[(c0 + e) >> 1], fv2, v[e], v[e + 1]);
+          for (int e = 0; e < 16; e += 2) ffma2_acc(dv_run[(c0 + e) >> 1], fv2, v[e], v[e + 1]);
+        }
       }
-      if (!waitw(wc, bar_acc_q, it & 1, bSiteAccQ)) break;
+      if (C::ALIAS) {
+        tc_fence_before();
+        mbar_arrive(bar_tmem_free_v);
+      }
+      if (!waitw(wc, bar_acc_k, it & 1, bSiteAccK)) break;
       tc_fence_after();
-      // dQ tile (lane r = query row i0 + r) -> scaled FP32 staging tile, D/32 boxes of
-      // [128 rows][32 floats] with the 128-byte swizzle, reduced into global by the reducer warp
+      {
+        const uint64_t fk2 = pack_f32x2(fk, fk);
 #pragma unroll
-      for (int c0 = 0; c0 < DC; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_base + C::C_DQ + w * DC + c0, v);
-        tmem_ld_wait();
+        for (int c0 = 0; c0 < DH; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + C::C_DK + wa * DH + c0, v);
+          tmem_ld_wait_regs(v);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; c4 += 4) {
-          const int col = w * DC + c0 + c4;
-          const int box = col >> 5;  // boxes [0, D/64) in the P^T tile, the rest in the dS^T tile
-          const uint32_t box_base = box < D / 64 ? pt_base + box * 16384 : ds_base + (box - D / 64) * 16384;
-          const uint32_t off = (uint32_t)(r * 128 + ((((col & 31) >> 2) ^ (r & 7)) << 4));
-          const float2 q01 = fmul2(fq2, make_float2(__uint_as_float(v[c4]), __uint_as_float(v[c4 + 1])));
-          const float2 q23 = fmul2(fq2, make_float2(__uint_as_float(v[c4 + 2]), __uint_as_float(v[c4 + 3])));
-          st_shared_v4(box_base + off, __float_as_uint(q01.x), __float_as_uint(q01.y), __float_as_uint(q23.x),
-                       __float_as_uint(q23.y));
+          for (int e = 0; e < 16; e += 2) ffma2_acc(dk_run[(c0 + e) >> 1], fk2, v[e], v[e + 1]);
         }
       }
       tc_fence_before();
-      mbar_arrive(bar_dq_read);
-      fence_proxy_async_smem();
-      mbar_arrive(bar_dq_staged);
+      mbar_arrive(bar_tmem_free_k);
+      // dQ tile (lane r = query row i0 + r) -> scaled FP32 staging half wa: boxes of
+      // [128 rows][32 floats] with the 128-byte swizzle, reduced into global by the reducer
+      // (on d = 128 half 0 overwrites dO^ and half 1 the dS codes: dV, dK, dQ are done)
+      if (!waitw(wc, bar_acc_q, it & 1, bSiteAccQ)) break;
+      if (!C::ALIAS && it >= 1 && !waitw(wc, bar_stg_free + wa, (it - 1) & 1, bSiteStgFree)) break;
+      tc_fence_after();
+      {
+        const float2 fq2 = make_float2(fq, fq);
 #pragma unroll
-      for (int c0 = 0; c0 < DC; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_base + C::C_DK + w * DC + c0, v);
-        tmem_ld_wait();
+        for (int c0 = 0; c0 < DH; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + C::C_DQ + wa * DH + c0, v);
+          tmem_ld_wait_regs(v);
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) ffma2_acc(dk_run[(c0 + e) >> 1], fk2, v[e], v[e + 1]);
+          for (int c4 = 0; c4 < 16; c4 += 4) {
+            const int col = wa * DH + c0 + c4;
+            const uint32_t box_base = smem_u32(smem + C::stg_box(col >> 5));
+            const uint32_t off = (uint32_t)(r * 128 + ((((col & 31) >> 2) ^ (r & 7)) << 4));
+            const float2 q01 = fmul2(fq2, make_float2(__uint_as_float(v[c4]), __uint_as_float(v[c4 + 1])));
+            const float2 q23 = fmul2(fq2, make_float2(__uint_as_float(v[c4 + 2]), __uint_as_float(v[c4 + 3])));
+            st_shared_v4(box_base + off, __float_as_uint(q01.x), __float_as_uint(q01.y), __float_as_uint(q23.x),
+                         __float_as_uint(q23.y));
+          }
+        }
       }
+      fence_proxy_async_smem();
+      mbar_arrive(bar_staged + wa);
       tc_fence_before();
-      mbar_arrive(bar_tmem_free);
+      mbar_arrive(bar_dvq_free);
     }
-    if (!*abort_flag && key_ok) {
-      // this CTA's share of dK_j, dV_j (row kglob, columns [w DC, (w+1) DC)) into the FP32 sums
-      float* dka = p.dk_acc + ((size_t)bhk * p.N + kglob) * D + w * DC;
-      float* dva = p.dv_acc + ((size_t)bhk * p.N + kglob) * D + w * DC;
+    if (!*abort_flag && kglob < p.N) {
+      // this CTA's share of dK_j, dV_j (row kglob, columns [wa d/2, (wa+1) d/2)) into the FP32 sums
+      float* dka = p.dk_acc + ((size_t)bhk * p.N + kglob) * D + wa * DH;
+      float* dva = p.dv_acc + ((size_t)bhk * p.N + kglob) * D + wa * DH;
 #pragma unroll
-      for (int c = 0; c < DC; c += 4) {
+      for (int c = 0; c < DH; c += 4) {
         const int h = c >> 1;
         red_add_v4_f32(dka + c, lo_f32(dk_run[h]), hi_f32(dk_run[h]), lo_f32(dk_run[h + 1]), hi_f32(dk_run[h + 1]));
         red_add_v4_f32(dva + c, lo_f32(dv_run[h]), hi_f32(dv_run[h]), lo_f32(dv_run[h + 1]), hi_f32(dv_run[h + 1]));
@@ -542,7 +643,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = p.nb * p.B * p.Hkv * (p.G / p.HS);
-  kern<<<grid, kThreads, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, p);
+  kern<<<grid, kBThreads, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, p);
   return cudaGetLastError();
 }
 
