@@ -22,8 +22,9 @@
 //   warps 8-15  accumulator warpgroups A (two): thread (a, r) owns output
 //               columns [a d/2, (a+1) d/2) of row r of dV and dK (FP32 sums in
 //               registers) and of the dQ tile it scales into the staging tile
-//   warp 16     TMA producer; warp 17 TMEM allocation and the MMA-issuing thread;
-//   warp 18     dQ reducer (bulk reduce-add of each staged half); warp 19 idle
+//   warp 16     TMA producer of K^, V, dO; warp 19 TMA producer of Q^, dO^;
+//   warp 17     TMEM allocation and the MMA-issuing thread;
+//   warp 18     dQ reducer (bulk reduce-add of each staged half)
 // Registers: 640 threads launch with 96 each; the last warpgroup drops to 32 and
 // the others rise (d = 128: S 64, A 160; 128 * 32 + 256 * 64 + 256 * 160 = 640 * 96).
 // TMEM columns: S^T / P [0,128), dP^T / dS [128,256), dV [256,256+d), dK
@@ -32,13 +33,14 @@
 // [384,448), P^T codes [448,512).
 // MMA order per tile i (each waits for what it overwrites or reads):
 //   S^T(i+1) = K^_j Q^_i+1^T                 once the P of tile i has been coded
+//   dV(i) = P^T codes (TMEM) x dO^_i         while the dS of tile i is coded
 //   dP^T(i+1) = V_j dO_i+1^T (BF16)          once the dS of tile i has been coded
-//   dV(i) = P^T codes (TMEM) x dO^_i
 //   dK(i) = dS^T Q^_i, dQ(i) = dS K^_j       from the shared dS code tile
 // so the softmax warpgroups wait for the next tile only while dP^T(i+1) runs.
 // Shared memory at d = 128 has room for one dO, dO^ stage and two Q^ stages, so
-// the FP32 dQ staging tile borrows the dO^ tile (after dV(i)) and the dS code
-// tile (after dK(i), dQ(i)); d = 64 double-buffers everything and has its own.
+// the FP32 dQ staging tile of tile i borrows the dO tile (dO_i+1 has been read by
+// dP^T(i+1) by then) and the dS code tile (after dK(i), dQ(i)); d = 64
+// double-buffers everything and has its own.
 #include <functional>
 #include <queue>
 #include <vector>
@@ -53,7 +55,7 @@ constexpr uint32_t kBRegsLaunch = 96, kBRegsCtl = 32;
 
 template <int D>
 struct BwdCfg {
-  static constexpr bool ALIAS = D == 128;     // staging tile borrowed from dO^ and the dS codes
+  static constexpr bool ALIAS = D == 128;     // staging tile borrowed from dO and the dS codes
   static constexpr int NS = D == 128 ? 1 : 2;  // dO, dO^ stages (Q^ always has two)
   static constexpr int TILE = 128 * D * 2;
   static constexpr int CTILE = 128 * 128 * 2;  // dS code tile
@@ -79,10 +81,10 @@ struct BwdCfg {
   static constexpr int C_S = 0, C_DP = 128, C_DV = 256, C_DK = 256 + D, C_DQ = ALIAS ? C_DV : 256 + 2 * D,
                        C_PC = ALIAS ? C_DK : 448;  // P^T codes (64 packed columns)
   static_assert(BYTES <= 232448, "shared memory beyond the per-CTA limit");
-  static_assert(ALIAS ? (128 * D * 4 == NS * TILE + CTILE) : true, "the staging halves must fill dO^ and dS codes");
+  static_assert(ALIAS ? (128 * D * 4 == NS * TILE + CTILE) : true, "the staging halves must fill dO and dS codes");
   // FP32 dQ staging: D/32 boxes of [128 rows][32 floats] (16 KB, 128-byte swizzle)
   __host__ __device__ static constexpr int stg_box(int b) {
-    return ALIAS ? (b < D / 64 ? OFF_DOQ + b * 16384 : OFF_DST + (b - D / 64) * 16384) : OFF_STG + b * 16384;
+    return ALIAS ? (b < D / 64 ? OFF_DO + b * 16384 : OFF_DST + (b - D / 64) * 16384) : OFF_STG + b * 16384;
   }
 };
 
@@ -195,56 +197,56 @@ __global__ void __launch_bounds__(kBThreads, 1)
   if (warp >= 16) {
     setmaxnreg_to<kBRegsCtl, kBRegsLaunch>();
     if (warp == 16 && lane == 0) {
-      // ---------------------------------------------------------- TMA producer
-      int q_iss[2] = {0, 0}, do_iss[NS], doq_iss[NS];
-      for (int s = 0; s < NS; ++s) do_iss[s] = doq_iss[s] = 0;
+      // ---------------------------------------------------------- TMA producer: K^, V, dO
+      // (the dO slot is released late on d = 128, where it holds tile it-2's dQ staging
+      // half 0; Q^ and dO^ have their own producer so that they never queue behind it)
+      int do_iss[NS];
+      for (int s = 0; s < NS; ++s) do_iss[s] = 0;
       mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
       for (int c = 0; c < D / 64; ++c) {
         tma_load_3d(smem + C::OFF_K + c * 16384, &tmK, bar_kv, c * 64, k0, bhk);
         tma_load_3d(smem + C::OFF_V + c * 16384, &tmV, bar_kv, c * 64, k0, bhk);
       }
-      // dO and Q^ of tile it, then dO^ of tile it-1: the dO^ slot frees late on d = 128
-      // (it holds the previous tile's dQ staging half 0), and the next tile's Q^ and dO
-      // must not queue behind it
-      auto load_doq = [&](int t) -> bool {
-        const int s = t % NS, n = t / NS;
+      for (int it = 0; it < T; ++it) {
+        const int s = it % NS, n = it / NS;
         if (C::ALIAS) {
-          if (t >= 1 && !wait1(wc, bar_stg_free, (t - 1) & 1, bSiteStgFree)) return false;
+          if (it == 1 && !wait1(wc, bar_do_empty, 0, bSiteDOEmpty)) break;
+          if (it >= 2 && !wait1(wc, bar_stg_free, (it - 2) & 1, bSiteStgFree)) break;
         } else {
-          if (t >= NS && !wait1(wc, bar_doq_empty + s, (n - 1) & 1, bSiteDOQEmpty)) return false;
-        }
-        mbar_arrive_expect_tx(bar_doq_full + s, C::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_DOQ + s * C::TILE + c * 16384, &tmDOQ, bar_doq_full + s, c * 64,
-                      tile_ib(t) * kBlk, tile_bhq(t));
-        doq_iss[s] = n + 1;
-        return true;
-      };
-      for (int it = 0; it <= T; ++it) {
-        if (it < T) {
-          const int s = it % NS, n = it / NS, sq = it & 1, nq2 = it >> 1;
-          const int bhq = tile_bhq(it), i0 = tile_ib(it) * kBlk;
           if (it >= NS && !wait1(wc, bar_do_empty + s, (n - 1) & 1, bSiteDOEmpty)) break;
-          mbar_arrive_expect_tx(bar_do_full + s, C::TILE);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + C::OFF_DO + s * C::TILE + c * 16384, &tmDO, bar_do_full + s, c * 64, i0, bhq);
-          do_iss[s] = n + 1;
-          if (it >= 2 && !wait1(wc, bar_q_empty + sq, (nq2 - 1) & 1, bSiteQEmpty)) break;
-          mbar_arrive_expect_tx(bar_q_full + sq, C::TILE);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + C::OFF_Q + sq * C::TILE + c * 16384, &tmQ, bar_q_full + sq, c * 64, i0, bhq);
-          q_iss[sq] = nq2 + 1;
         }
-        if (it >= 1 && !load_doq(it - 1)) break;
+        mbar_arrive_expect_tx(bar_do_full + s, C::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::OFF_DO + s * C::TILE + c * 16384, &tmDO, bar_do_full + s, c * 64,
+                      tile_ib(it) * kBlk, tile_bhq(it));
+        do_iss[s] = n + 1;
       }
       // Copies still in flight must land before the CTA's shared memory is released.
       drain(bar_kv, 0, p.timeout_ns);
+      for (int s = 0; s < NS; ++s)
+        if (do_iss[s]) drain(bar_do_full + s, (do_iss[s] - 1) & 1, p.timeout_ns);
+    } else if (warp == 19 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer: Q^, dO^
+      int q_iss[2] = {0, 0}, doq_iss[NS];
+      for (int s = 0; s < NS; ++s) doq_iss[s] = 0;
+      for (int it = 0; it < T; ++it) {
+        const int s = it % NS, n = it / NS, sq = it & 1, nq2 = it >> 1;
+        const int bhq = tile_bhq(it), i0 = tile_ib(it) * kBlk;
+        if (it >= 2 && !wait1(wc, bar_q_empty + sq, (nq2 - 1) & 1, bSiteQEmpty)) break;
+        mbar_arrive_expect_tx(bar_q_full + sq, C::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::OFF_Q + sq * C::TILE + c * 16384, &tmQ, bar_q_full + sq, c * 64, i0, bhq);
+        q_iss[sq] = nq2 + 1;
+        if (it >= NS && !wait1(wc, bar_doq_empty + s, (n - 1) & 1, bSiteDOQEmpty)) break;
+        mbar_arrive_expect_tx(bar_doq_full + s, C::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::OFF_DOQ + s * C::TILE + c * 16384, &tmDOQ, bar_doq_full + s, c * 64, i0, bhq);
+        doq_iss[s] = n + 1;
+      }
       for (int s = 0; s < 2; ++s)
         if (q_iss[s]) drain(bar_q_full + s, (q_iss[s] - 1) & 1, p.timeout_ns);
-      for (int s = 0; s < NS; ++s) {
-        if (do_iss[s]) drain(bar_do_full + s, (do_iss[s] - 1) & 1, p.timeout_ns);
+      for (int s = 0; s < NS; ++s)
         if (doq_iss[s]) drain(bar_doq_full + s, (doq_iss[s] - 1) & 1, p.timeout_ns);
-      }
     } else if (warp == 17 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
@@ -288,18 +290,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
           tc_fence_after();
           chain_kk(C::C_S, dK_k, dQ_k(sq), idSS);
         }
-        // dP^T of the next tile once dS is coded (its columns are free)
-        if (!wait1(wc, bar_ds_ready, it & 1, bSiteDSReady)) break;
-        if (next) {
-          const int s2 = (it + 1) % NS;
-          if (!wait1(wc, bar_do_full + s2, ((it + 1) / NS) & 1, bSiteDOFull)) break;
-          tc_fence_after();
-          chain_kk(C::C_DP, dV_k, dDO_k(s2), idSS);
-          umma_commit(bar_sdp);  // covers S^T(i+1) issued above
-          umma_commit(bar_do_empty + s2);
-        }
         // dV = P^T dO^: A = the P^T codes in TMEM (row = key, 128 queries = 64 packed
-        // columns, 8 per K step), B = dO^ [query][d] read MN-major
+        // columns, 8 per K step), B = dO^ [query][d] read MN-major; it runs while the
+        // softmax warpgroups code dS
         if (!wait1(wc, bar_doq_full + s, ph, bSiteDOQFull)) break;
         if (it >= 1 && !wait1(wc, bar_dvq_free, (it - 1) & 1, bSiteDVQFree)) break;
         tc_fence_after();
@@ -310,7 +303,17 @@ __global__ void __launch_bounds__(kBThreads, 1)
             umma_ts(tmem + C::C_DV, tmem + C::C_PC + kk * 8, sdesc_from_lo(bdesc + kk * 128), idKM, kk > 0);
         }
         umma_commit(bar_acc_v);
-        if (!C::ALIAS) umma_commit(bar_doq_empty + s);
+        umma_commit(bar_doq_empty + s);
+        // dP^T of the next tile once dS is coded (its columns are free)
+        if (!wait1(wc, bar_ds_ready, it & 1, bSiteDSReady)) break;
+        if (next) {
+          const int s2 = (it + 1) % NS;
+          if (!wait1(wc, bar_do_full + s2, ((it + 1) / NS) & 1, bSiteDOFull)) break;
+          tc_fence_after();
+          chain_kk(C::C_DP, dV_k, dDO_k(s2), idSS);
+          umma_commit(bar_sdp);  // covers S^T(i+1) issued above
+          if (!C::ALIAS) umma_commit(bar_do_empty + s2);
+        }
         // dK = dS^T Q^  (A: dS^T codes [key][query], K-major; B: Q^ [query][d], MN-major);
         // on d = 128 it overwrites the P^T codes, so dV must have read them
         if (C::ALIAS && !wait1(wc, bar_acc_v, it & 1, bSiteAccV)) break;
@@ -587,7 +590,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
       mbar_arrive(bar_tmem_free_k);
       // dQ tile (lane r = query row i0 + r) -> scaled FP32 staging half wa: boxes of
       // [128 rows][32 floats] with the 128-byte swizzle, reduced into global by the reducer
-      // (on d = 128 half 0 overwrites dO^ and half 1 the dS codes: dV, dK, dQ are done)
+      // (on d = 128 half 0 overwrites dO_i+1, which dP^T(i+1) has read, and half 1 the dS
+      // codes, which dK(i) and dQ(i) have read)
       if (!waitw(wc, bar_acc_q, it & 1, bSiteAccQ)) break;
       if (!C::ALIAS && it >= 1 && !waitw(wc, bar_stg_free + wa, (it - 1) & 1, bSiteStgFree)) break;
       tc_fence_after();
