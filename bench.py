@@ -15,6 +15,7 @@ the maximum time over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -36,6 +37,27 @@ L2_FLUSH_BYTES = 256 << 20
 # operands); legacy mma.sync s8 and torch._int_mm measured on this GPU for the "% of INT8 peak" line.
 INT8_MMA_SYNC_TOPS = 150.5
 INT8_TORCH_INT_MM_TOPS = 78.3
+
+
+# DRAM bytes (read + write) of one bwd_kernel launch on the qwen15b workload, from
+# the one-pass ncu capture summarised in profiles/bwd_kernel_qwen15b_ncu.md.  The
+# figure belongs to the kernel sources it was taken from: once any of them changes
+# the line reports null until the capture is repeated.
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1.33e9 + 517.12e6,
+               "sources_sha256": "86b2fbb1418765703ecb71377f317d4d35e9381067a73f58d0a18fd0c83da044"}
+BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
+               "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
+               "include/sagebwd.h"]
+
+
+def bwd_traffic(w):
+    import hashlib
+    h = hashlib.sha256()
+    for f in BWD_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    ok = h.hexdigest() == BWD_TRAFFIC["sources_sha256"] and w.name == BWD_TRAFFIC["workload"]
+    return BWD_TRAFFIC["bytes"] if ok else None
 
 
 def load_peaks():
@@ -283,8 +305,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end pass (profiling runs)")
     ap.add_argument("--no-cossim", action="store_true", help="skip the cosine-similarity reference (profiling runs)")
+    ap.add_argument("--seq", type=int, default=0,
+                    help="profiling only: override the workload's sequence length (the line then names it)")
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
+    if args.seq > 0:
+        w = dataclasses.replace(w, N=args.seq)
 
     if args.impl == "reference":
         run_reference(args, w)
@@ -316,14 +342,14 @@ def main():
     total, stage = time_device(step, args.steps, args.warmup, flush, barrier)
     clocks = sampler.stop()
     if args.no_e2e:
-        e2e_ms, h2d, d2h = [float("nan")], 0, 0
+        e2e_ms, h2d, d2h = None, 0, 0
     else:
         e2e_ms, h2d, d2h = time_e2e(step, max(3, args.steps // 5), max(3, args.warmup), flush, barrier)
     code0, _ = sb.sagebwd_check_status(step.ws0)
     code1, _ = sb.sagebwd_check_status(step.ws1)
 
     ms = sum(total) / len(total)
-    e2e = sum(e2e_ms) / len(e2e_ms)
+    e2e = sum(e2e_ms) / len(e2e_ms) if e2e_ms else 0.0
     if dist is not None:
         t = torch.tensor([ms, e2e], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -348,13 +374,15 @@ def main():
                  "bwd_incl_prepare": round(w.flops_bwd() / (sum(stage_ms[2:]) * 1e-3) / 1e12, 2)},
         "roofline": {"kernel": "sagebwd bwd_kernel", "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": round(achieved / peaks["bf16_sustained"], 4), "traffic": None,
+                     "frac": round(achieved / peaks["bf16_sustained"], 4), "traffic": bwd_traffic(w),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "peak_kind": f"bf16 dense, sustained ({peaks['source']})"},
         "int8_peak_frac": {"vs_mma_sync_s8": round(value / world / INT8_MMA_SYNC_TOPS, 3),
                            "vs_torch_int_mm": round(value / world / INT8_TORCH_INT_MM_TOPS, 3),
                            "vs_bf16_dense_burst": round(value / world / peaks["bf16_burst"], 4)},
-        "e2e": {"value": round(world * ops / (e2e * 1e-3) / 1e12, 3), "unit": "TOPS", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},
+        "e2e": None if e2e_ms is None else {
+            "value": round(world * ops / (e2e * 1e-3) / 1e12, 3), "unit": "TOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},
         "gpu_launches": step.launches() * args.steps,
         "clocks": clocks,
         "status": [code0, code1],
