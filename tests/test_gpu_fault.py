@@ -1,0 +1,51 @@
+"""Failure detection on the GPU without a GPU fault.
+
+The problem flag SAGEBWD_FLAG_DROP_ONE_LOAD makes the forward kernel's producer
+skip the TMA load of one K tile.  Nothing then completes that tile's mbarrier:
+the waits behind it run out after the problem's short wait_timeout_ms, record
+SAGEBWD_ERR_TIMEOUT with the site of the first wait that gave up, raise the
+CTA's abort flag so every other role leaves its loop, drain the copies and MMAs
+already issued and free TMEM.  The call must come back with that status, the
+CUDA context must stay usable, and the next ordinary call must be correct.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import bit_trainable_attention_gb300 as sb
+from bit_trainable_attention_gb300 import workloads as W
+from _parity import LSE_TOL, assert_parity, device_inputs, gpu_backward, gpu_forward, oracle_problem, to_np
+
+pytestmark = pytest.mark.gpu
+
+SAGEBWD_ERR_TIMEOUT = 5
+SAGEBWD_FLAG_DROP_ONE_LOAD = 0x1
+FWD_SITES = range(1, 10)  # the forward kernel's wait sites (Q .. O empty)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
+def test_dropped_load_times_out_and_the_context_survives(oracle_mod, causal):
+    # 512 tokens: 4 key tiles, so every CTA with a second key tile waits for the dropped one
+    w = W.small(f"fault_{int(causal)}", 1, 2, 2, 512, 64, causal, 301)
+    x, xd = device_inputs(w)
+    t0 = time.time()
+    bad = gpu_forward(w, xd, flags=SAGEBWD_FLAG_DROP_ONE_LOAD, timeout_ms=100)
+    elapsed = time.time() - t0
+    assert bad["status"] == SAGEBWD_ERR_TIMEOUT, sb.sagebwd_status_string(bad["status"])
+    assert bad["word"] & 0xFF == SAGEBWD_ERR_TIMEOUT
+    assert (bad["word"] >> 8) in FWD_SITES, hex(bad["word"])
+    assert elapsed < 30.0  # bounded: the waits gave up instead of hanging
+    assert sb.sagebwd_status_string(bad["status"]).strip()
+
+    # the context is still usable: an ordinary forward and backward on the same inputs
+    torch.cuda.synchronize()
+    good = gpu_forward(w, xd)
+    assert good["status"] == 0
+    op = oracle_problem(oracle_mod, w)
+    o_ref, lse_ref = oracle_mod.fwd(op, x["q"], x["k"], x["v"])
+    assert_parity(to_np(good["o"]), o_ref, "O")
+    np.testing.assert_allclose(to_np(good["lse"]), lse_ref, rtol=0, atol=LSE_TOL)
+    bwd = gpu_backward(w, xd, good)
+    assert bwd["status"] == 0
