@@ -157,6 +157,38 @@ class Step:
         return (2 if self.prob.smooth_k else 0) + 5
 
 
+def time_torch_sdpa(step: Step, steps: int, warmup: int, flush: torch.Tensor):
+    """PyTorch's BF16 scaled_dot_product_attention forward + backward on the same inputs (the
+    backend torch picks on this GPU), timed like the library's step: context for the INT8 path,
+    which here runs on the BF16 tensor-core instructions (no INT8 tcgen05 form on sm_103a)."""
+    w, x = step.w, step.x
+    q = x["q"].detach().clone().requires_grad_(True)
+    k = x["k"].detach().clone().requires_grad_(True)
+    v = x["v"].detach().clone().requires_grad_(True)
+    do = x["do"]
+    gqa = w.Hq != w.Hkv
+
+    def one():
+        o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=w.causal, enable_gqa=gqa)
+        o.backward(do)
+        q.grad = k.grad = v.grad = None
+
+    for _ in range(warmup):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record()
+        one()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    return {"ms_per_step": round(ms, 4), "tflops": round((w.flops_fwd() + w.flops_bwd()) / (ms * 1e-3) / 1e12, 2),
+            "dtype": "bf16", "note": "torch.nn.functional.scaled_dot_product_attention fwd+bwd, same shapes"}
+
+
 def cossim_vs_torch(step: Step):
     """Cosine similarity of O, dQ, dK, dV against PyTorch FP32 attention (not timed)."""
     w, x = step.w, step.x
@@ -305,6 +337,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end pass (profiling runs)")
     ap.add_argument("--no-cossim", action="store_true", help="skip the cosine-similarity reference (profiling runs)")
+    ap.add_argument("--compare-sdpa", action="store_true",
+                    help="also time PyTorch's BF16 SDPA forward + backward on the same inputs (context)")
     ap.add_argument("--seq", type=int, default=0,
                     help="profiling only: override the workload's sequence length (the line then names it)")
     args = ap.parse_args()
@@ -389,6 +423,8 @@ def main():
     }
     if rank == 0:
         line["cossim_vs_torch_fp32"] = None if args.no_cossim else cossim_vs_torch(step)
+        if args.compare_sdpa:
+            line["torch_sdpa_bf16"] = time_torch_sdpa(step, max(5, args.steps // 2), args.warmup, flush)
         line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if dist is not None:
