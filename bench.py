@@ -228,21 +228,35 @@ def time_device(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_b
 
 def time_e2e(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_barrier):
     """Public API (sagebwd_fwd + sagebwd_bwd) with pinned host inputs and outputs: H2D of Q, K, V, dO and
-    D2H of O, dQ, dK, dV inside the timed region."""
+    D2H of O, dQ, dK, dV inside the timed region.  As a training step would, the copies that the
+    compute does not wait for run on a second stream: dO travels while the forward runs, O comes back
+    while the backward runs."""
     p, x = step.prob, step.x
     hin = {k: v.pin_memory() for k, v in step.host.items()}
     hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
             for k, v in (("o", step.o), ("dq", step.dq), ("dk", step.dk), ("dv", step.dv))}
     s = torch.cuda.current_stream()
+    c = torch.cuda.Stream()
+    ev_do, ev_fwd = torch.cuda.Event(), torch.cuda.Event()
 
     def one():
-        for k in ("q", "k", "v", "do"):
+        c.wait_stream(s)  # the previous step has finished with every buffer the copies touch
+        for k in ("q", "k", "v"):
             x[k].copy_(hin[k], non_blocking=True)
+        with torch.cuda.stream(c):
+            x["do"].copy_(hin["do"], non_blocking=True)
+            ev_do.record(c)
         sb.sagebwd_fwd(p, x["q"], x["k"], x["v"], step.o, step.lse, step.saved, step.ws0, s)
+        ev_fwd.record(s)
+        with torch.cuda.stream(c):
+            c.wait_event(ev_fwd)
+            hout["o"].copy_(step.o, non_blocking=True)
+        s.wait_event(ev_do)
         sb.sagebwd_bwd(p, x["q"], x["k"], x["v"], step.o, x["do"], step.lse, step.saved, step.dq, step.dk, step.dv,
                        step.ws1, s)
-        for k, t in (("o", step.o), ("dq", step.dq), ("dk", step.dk), ("dv", step.dv)):
+        for k, t in (("dq", step.dq), ("dk", step.dk), ("dv", step.dv)):
             hout[k].copy_(t, non_blocking=True)
+        s.wait_stream(c)
 
     for _ in range(warmup):
         flush.zero_()
