@@ -12,8 +12,6 @@ call raises.
 from __future__ import annotations
 
 import ctypes
-import math
-import os
 import threading
 
 import torch
