@@ -30,7 +30,7 @@ class OracleProblem(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
         ("N", ctypes.c_int32), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
-        ("smooth_k", ctypes.c_int32), ("exact_codes", ctypes.c_int32),
+        ("smooth_k", ctypes.c_int32), ("balance_qk", ctypes.c_int32), ("exact_codes", ctypes.c_int32),
         ("threads", ctypes.c_int32), ("exact_mask", ctypes.c_uint32),
         ("softmax_scale", ctypes.c_double),
     ]
@@ -61,6 +61,7 @@ def _load():
             getattr(lib, name).argtypes = [P, vp, vp, vp, vp, vp, vp]
         for name in ("oracle_bwd", "oracle_exact_bwd"):
             getattr(lib, name).argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.oracle_quantize_qk.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_fwd_tile.argtypes = [P, vp, vp] + [ctypes.c_int] * 4 + [vp, vp]
         lib.oracle_bwd_tile.argtypes = [P, vp, vp, vp, vp, vp, vp] + [ctypes.c_int] * 4 + [vp, vp, vp, vp]
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -86,9 +87,10 @@ def _bf16_bits(x) -> np.ndarray:
     return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
 
 
-def problem(B, Hq, Hkv, N, d, causal, smooth_k=True, exact_codes=False, softmax_scale=0.0, threads=0, exact_mask=0):
-    return OracleProblem(B, Hq, Hkv, N, d, int(causal), int(smooth_k), int(exact_codes), int(threads), int(exact_mask),
-                         float(softmax_scale))
+def problem(B, Hq, Hkv, N, d, causal, smooth_k=True, exact_codes=False, softmax_scale=0.0, threads=0, exact_mask=0,
+            balance_qk=False):
+    return OracleProblem(B, Hq, Hkv, N, d, int(causal), int(smooth_k), int(balance_qk), int(exact_codes),
+                         int(threads), int(exact_mask), float(softmax_scale))
 
 
 def nblocks(N: int) -> int:
@@ -117,6 +119,23 @@ def quantize_exact(p: OracleProblem, x, BH: int, smooth: bool):
                                        _ptr(mean))
     assert rc == 0
     return codes.reshape(BH, p.N, p.d), scales.reshape(BH, -1), (mean.reshape(BH, p.d) if smooth else None)
+
+
+def quantize_qk(p: OracleProblem, q, k):
+    """Q and K as the forward quantizes them (K-smoothing and channel balancing as p selects).
+
+    Returns dict: q / k int8 codes [B*H, N, d], sq / sk FP32 block scales [B*H, nb], mu FP32 K channel
+    means [B*Hkv, d] (zeros without smoothing), e int32 balancing exponents [B*Hkv, d] (zeros unless
+    balance_qk)."""
+    q, k = _bf16_bits(q), _bf16_bits(k)
+    BHq, BHk, nb = p.B * p.Hq, p.B * p.Hkv, nblocks(p.N)
+    out = {"q": np.zeros((BHq, p.N, p.d), np.int8), "sq": np.zeros((BHq, nb), np.float32),
+           "k": np.zeros((BHk, p.N, p.d), np.int8), "sk": np.zeros((BHk, nb), np.float32),
+           "mu": np.zeros((BHk, p.d), np.float32), "e": np.zeros((BHk, p.d), np.int32)}
+    rc = _load().oracle_quantize_qk(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(out["q"]), _ptr(out["sq"]),
+                                    _ptr(out["k"]), _ptr(out["sk"]), _ptr(out["mu"]), _ptr(out["e"]))
+    assert rc == 0
+    return out
 
 
 def _sel(sel, n):

@@ -33,7 +33,13 @@
 //    one code matrix shared by dK = dS^T Q and dQ = dS K;
 //  * dP = dO V^T uses the BF16 inputs, accumulated here in FP64;
 //  * no correction term for the gradient through the K mean (each row of dS
-//    sums to zero, so the mean's gradient vanishes).
+//    sums to zero, so the mean's gradient vanishes);
+//  * optional channel balancing (balance_qk, off by default; the library's
+//    own addition, after SmoothQuant, listed under "Builds on" of the SageBwd
+//    page): per (batch, kv head, channel) an exponent e moves magnitude
+//    between Q and K before their block quantizers -- Q's channel times 2^-e,
+//    K's (smoothed) channel times 2^e -- which leaves Q K^T unchanged exactly;
+//    dQ is multiplied by 2^-e and dK by 2^e at the end.  See balance_exponents.
 //
 // Every floating-point quantity that decides an integer code is rounded to
 // FP32 exactly where the GPU path computes it in FP32 (Mode::F below); every
@@ -56,6 +62,7 @@ typedef struct {
   int32_t B, Hq, Hkv, N, d;
   int32_t causal;       // 1: key k is visible to query i iff k <= i (top-left aligned, N_q == N_k)
   int32_t smooth_k;     // 1: subtract the per-channel mean of K before quantizing it
+  int32_t balance_qk;   // 1: power-of-two channel balancing of Q and K before quantizing them
   int32_t exact_codes;  // 1: quantizers keep their scales but neither round nor clamp; no FP32 rounding
   int32_t threads;      // <= 0: OpenMP default
   uint32_t exact_mask;  // error attribution: bit set = that quantizer keeps its scale but skips rint/clamp
@@ -140,10 +147,24 @@ void quant_block(const Mode& M, int which, const double* x, int count, double* c
   for (int e = 0; e < count; ++e) codes[e] = M.Q(which, M.F(x[e] * inv));
 }
 
+// FP32 channel means of one head's tokens [N][d] ("SageBwd: A Trainable
+// Low-bit Attention", Abstract: K-smoothing): FP64 sum, FP64 divide, one
+// FP32 rounding.
+void channel_mean(const Mode& M, const uint16_t* xb, int N, int d, double* mu) {
+  for (int ch = 0; ch < d; ++ch) {
+    double sum = 0;
+    for (int n = 0; n < N; ++n) sum += bf16_to_double(xb[(size_t)n * d + ch]);
+    mu[ch] = M.F(sum / (double)N);
+  }
+}
+
 // Quantize a BF16 tensor [BH][N][d]; with smooth, first subtract the channel
-// mean over all N tokens ("SageBwd: A Trainable Low-bit Attention", Abstract:
-// K-smoothing).
-void quantize_tensor(const Mode& M, int which, const uint16_t* x, int BH, int N, int d, bool smooth, QTensor& out) {
+// mean over all N tokens (K-smoothing).  With fac, every value (after the
+// smoothing) is then multiplied by its channel's factor
+// (*fac)[(bh / fac_group) * d + ch], rounded to FP32, before the block
+// quantizer sees it (channel balancing).
+void quantize_tensor(const Mode& M, int which, const uint16_t* x, int BH, int N, int d, bool smooth, QTensor& out,
+                     const std::vector<double>* fac = nullptr, int fac_group = 1) {
   out.BH = BH;
   out.N = N;
   out.d = d;
@@ -156,24 +177,87 @@ void quantize_tensor(const Mode& M, int which, const uint16_t* x, int BH, int N,
     const uint16_t* xb = x + (size_t)bh * N * d;
     std::vector<double> mu(d, 0.0);
     if (smooth) {
-      for (int ch = 0; ch < d; ++ch) {
-        double sum = 0;
-        for (int n = 0; n < N; ++n) sum += bf16_to_double(xb[(size_t)n * d + ch]);
-        mu[ch] = M.F(sum / (double)N);
-        out.mean[(size_t)bh * d + ch] = mu[ch];
-      }
+      channel_mean(M, xb, N, d, mu.data());
+      std::copy(mu.begin(), mu.end(), out.mean.begin() + (size_t)bh * d);
     }
+    const double* f = fac ? fac->data() + (size_t)(bh / fac_group) * d : nullptr;
     std::vector<double> vals((size_t)BLK * d);
     for (int blk = 0; blk < nb; ++blk) {
       const int n0 = blk * BLK, rows = std::min(BLK, N - n0);
       for (int r = 0; r < rows; ++r)
         for (int ch = 0; ch < d; ++ch) {
           const double v = bf16_to_double(xb[(size_t)(n0 + r) * d + ch]);
-          vals[(size_t)r * d + ch] = smooth ? M.F(v - mu[ch]) : v;
+          double val = smooth ? M.F(v - mu[ch]) : v;
+          if (f) val = M.F(val * f[ch]);
+          vals[(size_t)r * d + ch] = val;
         }
       quant_block(M, which, vals.data(), rows * d, &out.codes[((size_t)bh * N + n0) * d], &out.scale[(size_t)bh * nb + blk]);
     }
   }
+}
+
+// floor(a / 2) for any sign of a.
+inline int floor_half(int a) { return a >= 0 ? a / 2 : -((1 - a) / 2); }
+
+// Channel balancing exponents, one per (batch, kv head, channel) [B*Hkv][d]
+// (the library's reading, after SmoothQuant's migration of magnitude from
+// activations to weights): with
+//   aQ = max |Q| of the channel over the G query heads of the kv head and
+//        all N tokens,
+//   aK = max |K'| of the channel over all N tokens, K' the K the quantizer
+//        sees (K minus its FP32 channel mean, rounded to FP32, when smoothing),
+// the exponent is e = floor((E(aQ) - E(aK)) / 2), E(a) = floor(log2 a) (the
+// binary exponent), and 0 when aQ or aK is zero.  Scaling Q by 2^-e and K' by
+// 2^e leaves both channel maxima within a factor 4 of sqrt(aQ * aK).
+std::vector<int> balance_exponents(const Mode& M, const oracle_problem* p, const uint16_t* q, const uint16_t* k) {
+  const int N = p->N, d = p->d, G = p->Hq / p->Hkv, BHk = p->B * p->Hkv;
+  std::vector<int> e((size_t)BHk * d, 0);
+#pragma omp parallel for schedule(dynamic)
+  for (int bhk = 0; bhk < BHk; ++bhk) {
+    const uint16_t* kb = k + (size_t)bhk * N * d;
+    std::vector<double> mu(d, 0.0);
+    if (p->smooth_k) channel_mean(M, kb, N, d, mu.data());
+    const int b = bhk / p->Hkv, hk = bhk % p->Hkv;
+    for (int ch = 0; ch < d; ++ch) {
+      double ak = 0, aq = 0;
+      for (int n = 0; n < N; ++n) {
+        const double v = bf16_to_double(kb[(size_t)n * d + ch]);
+        ak = std::max(ak, std::fabs(p->smooth_k ? M.F(v - mu[ch]) : v));
+      }
+      for (int h = hk * G; h < (hk + 1) * G; ++h) {
+        const uint16_t* qb = q + ((size_t)b * p->Hq + h) * N * d;
+        for (int n = 0; n < N; ++n) aq = std::max(aq, std::fabs(bf16_to_double(qb[(size_t)n * d + ch])));
+      }
+      if (aq > 0 && ak > 0) {
+        int eq = 0, ek = 0;
+        std::frexp(aq, &eq);  // a = m 2^E with m in [0.5, 1): floor(log2 a) = E - 1 on both sides
+        std::frexp(ak, &ek);
+        e[(size_t)bhk * d + ch] = floor_half(eq - ek);
+      }
+    }
+  }
+  return e;
+}
+
+// Q and K as the attention consumes them: Q plain, K smoothed (smooth_k), both
+// channel-balanced (balance_qk).  fq / fk (optional) receive the per
+// (b, kv head, channel) factors 2^-e and 2^e (all 1 without balancing).
+void quantize_qk(const Mode& M, const oracle_problem* p, const uint16_t* q, const uint16_t* k, QTensor& qq,
+                 QTensor& kq, std::vector<int>* exps = nullptr, std::vector<double>* fq = nullptr,
+                 std::vector<double>* fk = nullptr) {
+  const size_t nf = (size_t)p->B * p->Hkv * p->d;
+  std::vector<int> e = p->balance_qk ? balance_exponents(M, p, q, k) : std::vector<int>(nf, 0);
+  std::vector<double> f_q(nf), f_k(nf);
+  for (size_t i = 0; i < nf; ++i) {
+    f_q[i] = std::ldexp(1.0, -e[i]);
+    f_k[i] = std::ldexp(1.0, e[i]);
+  }
+  const int G = p->Hq / p->Hkv;
+  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq, p->balance_qk ? &f_q : nullptr, G);
+  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq, p->balance_qk ? &f_k : nullptr, 1);
+  if (exps) *exps = std::move(e);
+  if (fq) *fq = std::move(f_q);
+  if (fk) *fk = std::move(f_k);
 }
 
 inline bool visible(const oracle_problem* p, int i, int k) { return k < p->N && (!p->causal || k <= i); }
@@ -246,8 +330,7 @@ void fwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, con
               const uint8_t* qsel) {
   const Mode M = mode_of(p);
   QTensor qq, kq, vq;
-  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq);
-  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq);
+  quantize_qk(M, p, q, k, qq, kq);
   quantize_tensor(M, QZ_V, v, p->B * p->Hkv, p->N, p->d, false, vq);
   const double c0 = M.F(scale_of(p) * kLog2e);
   const int N = p->N, d = p->d, nb = nblocks(N);
@@ -337,8 +420,8 @@ void bwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, con
               const uint8_t* ksel) {
   const Mode M = mode_of(p);
   QTensor qq, kq, dq8;
-  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq);
-  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq);
+  std::vector<double> fq, fk;  // channel balancing factors, undone on dQ and dK at the end
+  quantize_qk(M, p, q, k, qq, kq, nullptr, &fq, &fk);
   quantize_tensor(M, QZ_DO, dO, p->B * p->Hq, p->N, p->d, false, dq8);
   const double sc = scale_of(p);
   const double c0 = M.F(sc * kLog2e);
@@ -376,7 +459,7 @@ void bwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, con
         for (int ch = 0; ch < d; ++ch) {
           const size_t idx = ((size_t)bhk * N + jb * BLK + c) * d + ch;
           dv[idx] = accv[(size_t)c * d + ch];
-          dk[idx] = acck[(size_t)c * d + ch];
+          dk[idx] = acck[(size_t)c * d + ch] * fk[(size_t)bhk * d + ch];  // dK = dS^T (Q 2^-e) 2^e
         }
     }
   }
@@ -402,7 +485,8 @@ void bwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, con
           }
       }
       for (int a = 0; a < std::min(BLK, N - ib * BLK); ++a)
-        for (int ch = 0; ch < d; ++ch) dq[((size_t)bhq * N + ib * BLK + a) * d + ch] = accq[(size_t)a * d + ch];
+        for (int ch = 0; ch < d; ++ch)  // dQ = dS (K' 2^e) 2^-e
+          dq[((size_t)bhq * N + ib * BLK + a) * d + ch] = accq[(size_t)a * d + ch] * fq[(size_t)bhk * d + ch];
     }
   }
 }
@@ -442,6 +526,28 @@ int oracle_quantize_exact(const oracle_problem* p, const uint16_t* x, int BH, in
   std::copy(qt.codes.begin(), qt.codes.end(), codes);
   std::copy(qt.scale.begin(), qt.scale.end(), scales);
   if (smooth && mean) std::copy(qt.mean.begin(), qt.mean.end(), mean);
+  return 0;
+}
+
+// Q and K as the forward quantizes them (K-smoothing and channel balancing as
+// the problem selects): int8 codes, FP32 block scales, the FP32 K channel
+// means [B*Hkv][d] (smooth_k) and the balancing exponents [B*Hkv][d] (all 0
+// unless balance_qk).  mean and exps may be NULL.
+int oracle_quantize_qk(const oracle_problem* p, const uint16_t* q, const uint16_t* k, int8_t* qc, float* qs,
+                       int8_t* kc, float* ks, float* mean, int32_t* exps) {
+  if (oracle_check_problem(p)) return 1;
+  set_threads(p);
+  QTensor qq, kq;
+  std::vector<int> e;
+  quantize_qk(Mode{true, 0}, p, q, k, qq, kq, &e);
+  for (size_t i = 0; i < qq.codes.size(); ++i) qc[i] = (int8_t)qq.codes[i];
+  for (size_t i = 0; i < qq.scale.size(); ++i) qs[i] = (float)qq.scale[i];
+  for (size_t i = 0; i < kq.codes.size(); ++i) kc[i] = (int8_t)kq.codes[i];
+  for (size_t i = 0; i < kq.scale.size(); ++i) ks[i] = (float)kq.scale[i];
+  if (mean && p->smooth_k)
+    for (size_t i = 0; i < kq.mean.size(); ++i) mean[i] = (float)kq.mean[i];
+  if (exps)
+    for (size_t i = 0; i < e.size(); ++i) exps[i] = e[i];
   return 0;
 }
 
@@ -601,8 +707,7 @@ int oracle_fwd_tile(const oracle_problem* p, const uint16_t* q, const uint16_t* 
   set_threads(p);
   const Mode M = mode_of(p);
   QTensor qq, kq;
-  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq);
-  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq);
+  quantize_qk(M, p, q, k, qq, kq);
   const double c0 = M.F(scale_of(p) * kLog2e);
   std::vector<double> t(p->N);
   for (int a = 0; a < BLK; ++a) {
@@ -629,8 +734,7 @@ int oracle_bwd_tile(const oracle_problem* p, const uint16_t* q, const uint16_t* 
   set_threads(p);
   const Mode M = mode_of(p);
   QTensor qq, kq;
-  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq);
-  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq);
+  quantize_qk(M, p, q, k, qq, kq);
   BwdTile T;
   bwd_tile(M, p, qq, kq, v, dO, o, lse, b, h, ib, jb, M.F(scale_of(p) * kLog2e), M.F(kLog2e), T);
   for (size_t e = 0; e < T.pt.size(); ++e) pt[e] = (int32_t)T.pt[e];
