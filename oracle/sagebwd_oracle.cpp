@@ -207,8 +207,9 @@ inline int floor_half(int a) { return a >= 0 ? a / 2 : -((1 - a) / 2); }
 //   aK = max |K'| of the channel over all N tokens, K' the K the quantizer
 //        sees (K minus its FP32 channel mean, rounded to FP32, when smoothing),
 // the exponent is e = floor((E(aQ) - E(aK)) / 2), E(a) = floor(log2 a) (the
-// binary exponent), and 0 when aQ or aK is zero.  Scaling Q by 2^-e and K' by
-// 2^e leaves both channel maxima within a factor 4 of sqrt(aQ * aK).
+// binary exponent), clamped to [-126, 126] so that 2^e and 2^-e are normal
+// FP32 numbers, and 0 when aQ or aK is zero.  Scaling Q by 2^-e and K' by 2^e
+// leaves both channel maxima within a factor 4 of sqrt(aQ * aK).
 std::vector<int> balance_exponents(const Mode& M, const oracle_problem* p, const uint16_t* q, const uint16_t* k) {
   const int N = p->N, d = p->d, G = p->Hq / p->Hkv, BHk = p->B * p->Hkv;
   std::vector<int> e((size_t)BHk * d, 0);
@@ -232,7 +233,7 @@ std::vector<int> balance_exponents(const Mode& M, const oracle_problem* p, const
         int eq = 0, ek = 0;
         std::frexp(aq, &eq);  // a = m 2^E with m in [0.5, 1): floor(log2 a) = E - 1 on both sides
         std::frexp(ak, &ek);
-        e[(size_t)bhk * d + ch] = floor_half(eq - ek);
+        e[(size_t)bhk * d + ch] = std::min(126, std::max(-126, floor_half(eq - ek)));
       }
     }
   }

@@ -35,8 +35,8 @@ def bf16(a):
 
 
 def test_exponents_closed_form(oracle_mod):
-    """Two query heads share one kv head; N = 3 tokens, d = 8 channels."""
-    d, N = 8, 3
+    """Two query heads share one kv head; N = 3 tokens, d = 16 channels."""
+    d, N = 16, 3
     q = np.zeros((1, 2, N, d), np.float32)
     k = np.zeros((1, 1, N, d), np.float32)
     # channel: (Q values head 0, Q values head 1, K values) -> expected e
@@ -49,12 +49,17 @@ def test_exponents_closed_form(oracle_mod):
         ([3.0, 0.0, 0.0], [0.0, 0.0, 0.0], [1.0, 0.0, 0.0], 0),  # E(3)=1, E(1)=0: floor(0.5)
         ([1.0, 0.0, 0.0], [0.0, -40.0, 0.0], [1.0, 0.0, 0.0], 2),  # max over heads: E(40)=5
         ([1.0, 0.0, 0.0], [0.0, 0.0, 0.0], [2.0 ** -10, 0.0, 0.0], 5),  # diff 10
+        ([2.0 ** 127 * 1.5, 0.0, 0.0], [0.0, 0.0, 0.0], [2.0 ** -133, 0.0, 0.0], 126),  # 130, clamped
+        ([2.0 ** -133, 0.0, 0.0], [0.0, 0.0, 0.0], [2.0 ** 127, 0.0, 0.0], -126),  # -130, clamped
+        ([2.0 ** -130 * 3, 0.0, 0.0], [0.0, 0.0, 0.0], [1.0, 0.0, 0.0], -65),  # subnormal: E = -129
+        ([1.0, -1.0, 0.0], [0.0, 0.0, 0.0], [-(2.0 ** 20) * 1.75, 0.0, 0.0], -10),  # K's max is negative
     ]
     for ch, (q0, q1, kk, _) in enumerate(cases):
         q[0, 0, :, ch], q[0, 1, :, ch], k[0, 0, :, ch] = q0, q1, kk
     p = oracle_mod.problem(1, 2, 1, N, d, False, smooth_k=False, balance_qk=True)
     r = oracle_mod.quantize_qk(p, bf16(q), bf16(k))
-    np.testing.assert_array_equal(r["e"][0], [c[3] for c in cases])
+    expect = [c[3] for c in cases] + [0] * (d - len(cases))  # unused channels are all zero
+    np.testing.assert_array_equal(r["e"][0], expect)
     p0 = oracle_mod.problem(1, 2, 1, N, d, False, smooth_k=False, balance_qk=False)
     assert not oracle_mod.quantize_qk(p0, bf16(q), bf16(k))["e"].any()
 
