@@ -119,12 +119,12 @@ class ClockSampler:
 class Step:
     """Buffers and the stage-by-stage calls of one forward + backward step."""
 
-    def __init__(self, w: W.Workload, dev):
+    def __init__(self, w: W.Workload, dev, balance_qk=False, inputs=None):
         self.w = w
-        x = W.make_inputs(w)
+        x = W.make_inputs(w) if inputs is None else inputs
         self.host = x
         self.x = {k: v.to(dev) for k, v in x.items()}
-        self.prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+        self.prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, balance_qk=balance_qk)
         p = self.prob
         self.o = torch.empty_like(self.x["q"])
         self.lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
@@ -149,12 +149,13 @@ class Step:
         rec(3)
         sb.sagebwd_bwd_attention(p, x["v"], x["do"], self.lse, self.saved, self.ws1, s)
         rec(4)
-        sb.sagebwd_bwd_finish(p, self.dq, self.dk, self.dv, self.ws1, s)
+        sb.sagebwd_bwd_finish(p, self.saved, self.dq, self.dk, self.dv, self.ws1, s)
         rec(5)
 
-    # kernels of ours per step: [K mean partial + final] + quantize + fwd + prep + bwd + dq convert
+    # kernels of ours per step: [K mean or Q/K statistics: partial + final] + quantize + fwd + prep + bwd
+    # + gradient convert
     def launches(self):
-        return (2 if self.prob.smooth_k else 0) + 5
+        return (2 if (self.prob.smooth_k or self.prob.balance_qk) else 0) + 5
 
 
 def time_torch_sdpa(step: Step, steps: int, warmup: int, flush: torch.Tensor):
@@ -224,6 +225,17 @@ def time_device(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_b
     stage = [[evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)] for j in range(5)]
     total = [evs[i][0].elapsed_time(evs[i][5]) for i in range(steps)]
     return total, stage
+
+
+def other_balance_setting(step: Step, args, dev, flush):
+    """The same workload with the Q/K channel balancing switched the other way: a shorter timing
+    (reported, not the headline) and its cosine similarities."""
+    other = Step(step.w, dev, balance_qk=not step.prob.balance_qk, inputs=step.host)
+    total, stage = time_device(other, max(5, args.steps // 5), 3, flush, lambda: None)
+    out = {"balance_qk": bool(other.prob.balance_qk), "ms_per_step": round(sum(total) / len(total), 4),
+           "quantize_ms": round(sum(stage[0]) / len(stage[0]), 4), "cossim_vs_torch_fp32": cossim_vs_torch(other)}
+    del other
+    return out
 
 
 def time_e2e(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_barrier):
@@ -353,6 +365,8 @@ def main():
     ap.add_argument("--no-cossim", action="store_true", help="skip the cosine-similarity reference (profiling runs)")
     ap.add_argument("--compare-sdpa", action="store_true",
                     help="also time PyTorch's BF16 SDPA forward + backward on the same inputs (context)")
+    ap.add_argument("--balance-qk", action="store_true",
+                    help="time the library's optional Q/K channel balancing (the other setting is reported beside)")
     ap.add_argument("--seq", type=int, default=0,
                     help="profiling only: override the workload's sequence length (the line then names it)")
     args = ap.parse_args()
@@ -384,7 +398,7 @@ def main():
         cpu = cpu_baseline(w, args.cpu_budget_s)
 
     sb.load_library()
-    step = Step(w, dev)
+    step = Step(w, dev, balance_qk=args.balance_qk)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(local)
     total, stage = time_device(step, args.steps, args.warmup, flush, barrier)
@@ -431,12 +445,15 @@ def main():
         "e2e": None if e2e_ms is None else {
             "value": round(world * ops / (e2e * 1e-3) / 1e12, 3), "unit": "TOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},
+        "balance_qk": bool(args.balance_qk),
         "gpu_launches": step.launches() * args.steps,
         "clocks": clocks,
         "status": [code0, code1],
     }
     if rank == 0:
         line["cossim_vs_torch_fp32"] = None if args.no_cossim else cossim_vs_torch(step)
+        if not args.no_cossim:
+            line["other_balance_setting"] = other_balance_setting(step, args, dev, flush)
         if args.compare_sdpa:
             line["torch_sdpa_bf16"] = time_torch_sdpa(step, max(5, args.steps // 2), args.warmup, flush)
         line["cpu_baseline"] = cpu

@@ -50,12 +50,14 @@ class Problem(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("N", ctypes.c_int32),
         ("d", ctypes.c_int32), ("causal", ctypes.c_int32), ("smooth_k", ctypes.c_int32),
-        ("flags", ctypes.c_uint32), ("softmax_scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_uint32),
+        ("balance_qk", ctypes.c_int32), ("flags", ctypes.c_uint32), ("softmax_scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_uint32),
     ]
 
     @classmethod
-    def make(cls, B, Hq, Hkv, N, d, causal, smooth_k=True, flags=0, softmax_scale=0.0, wait_timeout_ms=0):
-        return cls(B, Hq, Hkv, N, d, int(bool(causal)), int(bool(smooth_k)), flags, softmax_scale, wait_timeout_ms)
+    def make(cls, B, Hq, Hkv, N, d, causal, smooth_k=True, flags=0, softmax_scale=0.0, wait_timeout_ms=0,
+             balance_qk=False):
+        return cls(B, Hq, Hkv, N, d, int(bool(causal)), int(bool(smooth_k)), int(bool(balance_qk)), flags,
+                   softmax_scale, wait_timeout_ms)
 
     @classmethod
     def from_tensors(cls, q, k, causal, **kw):
@@ -89,7 +91,7 @@ def load_library():
             lib.sagebwd_fwd_attention.argtypes = [P, vp, vp, vp, vp, vp]
             lib.sagebwd_bwd_prepare.argtypes = [P, vp, vp, vp, vp]
             lib.sagebwd_bwd_attention.argtypes = [P, vp, vp, vp, vp, vp, vp]
-            lib.sagebwd_bwd_finish.argtypes = [P, vp, vp, vp, vp, vp]
+            lib.sagebwd_bwd_finish.argtypes = [P, vp, vp, vp, vp, vp, vp]
             lib.sagebwd_check_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
             lib.sagebwd_quantize_k_noalloc.argtypes = [P, vp, vp, vp, vp, vp]
             lib.sagebwd_status_string.argtypes = [ctypes.c_int]
@@ -176,9 +178,9 @@ def sagebwd_bwd_attention(prob, v, dO, lse, saved, ws, stream=None):
            "sagebwd_bwd_attention")
 
 
-def sagebwd_bwd_finish(prob, dq, dk, dv, ws, stream=None):
-    _check(load_library().sagebwd_bwd_finish(ctypes.byref(prob), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
-                                             _stream(stream)),
+def sagebwd_bwd_finish(prob, saved, dq, dk, dv, ws, stream=None):
+    _check(load_library().sagebwd_bwd_finish(ctypes.byref(prob), _ptr(saved), _ptr(dq), _ptr(dk), _ptr(dv),
+                                             _ptr(ws), _stream(stream)),
            "sagebwd_bwd_finish")
 
 
@@ -216,13 +218,14 @@ def empty_bytes(nbytes: int, device) -> torch.Tensor:
 
 def quantized_views(prob: Problem, saved: torch.Tensor) -> dict:
     """Views of the `saved` buffer of sagebwd_fwd (layout of the library: 256-byte aligned sections
-    q^, k^, v^ (BF16), sQ, sK, sV (FP32 block scales), mean of K (FP32))."""
+    q^, k^, v^ (BF16), sQ, sK, sV (FP32 block scales), mean of K (FP32), channel balancing exponents (int32))."""
     def al(x):
         return (x + 255) // 256 * 256
     B, Hq, Hkv, N, d = prob.B, prob.Hq, prob.Hkv, prob.N, prob.d
     nb = (N + 127) // 128
     sizes = [("q", B * Hq * N * d * 2), ("k", B * Hkv * N * d * 2), ("v", B * Hkv * N * d * 2),
-             ("sq", B * Hq * nb * 4), ("sk", B * Hkv * nb * 4), ("sv", B * Hkv * nb * 4), ("mu", B * Hkv * d * 4)]
+             ("sq", B * Hq * nb * 4), ("sk", B * Hkv * nb * 4), ("sv", B * Hkv * nb * 4), ("mu", B * Hkv * d * 4),
+             ("e", B * Hkv * d * 4)]
     out, off = {}, 0
     for name, n in sizes:
         out[name] = saved[off:off + n]
@@ -234,6 +237,7 @@ def quantized_views(prob: Problem, saved: torch.Tensor) -> dict:
     out["sk"] = out["sk"].view(torch.float32).view(B * Hkv, nb)
     out["sv"] = out["sv"].view(torch.float32).view(B * Hkv, nb)
     out["mu"] = out["mu"].view(torch.float32).view(B * Hkv, d)
+    out["e"] = out["e"].view(torch.int32).view(B * Hkv, d)
     return out
 
 
@@ -247,9 +251,10 @@ class SageBwdAttention(torch.autograd.Function):
     """softmax(scale Q K^T) V with SageBwd's INT8 forward and backward."""
 
     @staticmethod
-    def forward(ctx, q, k, v, causal=False, softmax_scale=0.0, smooth_k=True):
+    def forward(ctx, q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False):
         _check_inputs(q, k, v)
-        prob = Problem.from_tensors(q, k, causal, smooth_k=smooth_k, softmax_scale=softmax_scale)
+        prob = Problem.from_tensors(q, k, causal, smooth_k=smooth_k, softmax_scale=softmax_scale,
+                                    balance_qk=balance_qk)
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
         saved = empty_bytes(sagebwd_saved_bytes(prob), q.device)
@@ -269,9 +274,12 @@ class SageBwdAttention(torch.autograd.Function):
         dv = torch.empty_like(v)
         ws = empty_bytes(sagebwd_workspace_bytes(prob, 1), q.device)
         sagebwd_bwd(prob, q, k, v, o, do, lse, saved, dq, dk, dv, ws)
-        return dq, dk, dv, None, None, None
+        return dq, dk, dv, None, None, None, None
 
 
-def attention(q, k, v, causal=False, softmax_scale=0.0, smooth_k=True):
-    """SageBwd attention on BF16 [B, H, N, d] CUDA tensors (GQA when k/v have fewer heads)."""
-    return SageBwdAttention.apply(q, k, v, causal, softmax_scale, smooth_k)
+def attention(q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False):
+    """SageBwd attention on BF16 [B, H, N, d] CUDA tensors (GQA when k/v have fewer heads).
+
+    balance_qk turns on the library's power-of-two Q/K channel balancing before quantization
+    (for inputs with channel outliers; Q K^T is unchanged exactly)."""
+    return SageBwdAttention.apply(q, k, v, causal, softmax_scale, smooth_k, balance_qk)

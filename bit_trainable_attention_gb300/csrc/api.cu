@@ -33,7 +33,7 @@ sagebwd_status check_problem(const sagebwd_problem* p) {
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 struct SavedLayout {
-  size_t q, k, v, sq, sk, sv, mu, total;
+  size_t q, k, v, sq, sk, sv, mu, be, total;
 };
 SavedLayout saved_layout(const sagebwd_problem* p) {
   const size_t nb = (size_t)nblocks(p->N);
@@ -47,13 +47,14 @@ SavedLayout saved_layout(const sagebwd_problem* p) {
   L.sk = off; off += align_up((size_t)p->B * p->Hkv * nb * 4);
   L.sv = off; off += align_up((size_t)p->B * p->Hkv * nb * 4);
   L.mu = off; off += align_up((size_t)p->B * p->Hkv * p->d * 4);
+  L.be = off; off += align_up((size_t)p->B * p->Hkv * p->d * 4);
   L.total = off;
   return L;
 }
 
 // Workspace: [status word | pass scratch].
 struct WsLayout {
-  size_t status, kpart, D, dOq, sdo, dqacc, dkacc, dvacc, total;
+  size_t status, kpart, kmax, kmin, qmax, D, dOq, sdo, dqacc, dkacc, dvacc, total;
 };
 WsLayout ws_layout(const sagebwd_problem* p, int pass) {
   const size_t nb = (size_t)nblocks(p->N);
@@ -62,6 +63,11 @@ WsLayout ws_layout(const sagebwd_problem* p, int pass) {
   L.status = off; off += kAlign;
   if (pass == 0) {
     L.kpart = off; off += align_up((size_t)p->B * p->Hkv * nb * p->d * 8);
+    if (p->balance_qk) {
+      L.kmax = off; off += align_up((size_t)p->B * p->Hkv * nb * p->d * 4);
+      L.kmin = off; off += align_up((size_t)p->B * p->Hkv * nb * p->d * 4);
+      L.qmax = off; off += align_up((size_t)p->B * p->Hq * nb * p->d * 4);
+    }
   } else {
     const size_t qe = (size_t)p->B * p->Hq * p->N * p->d;
     L.D = off; off += align_up((size_t)p->B * p->Hq * p->N * 4);
@@ -162,19 +168,40 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
   const WsLayout W = ws_layout(p, 0);
   int* status = at<int>(ws, W.status);
   const int nb = nblocks(p->N);
-  const float* mean = nullptr;
-  if (p->smooth_k) {
+  const float* mean = p->smooth_k ? at<float>(saved, S.mu) : nullptr;
+  const int* bexp = nullptr;
+  if (p->balance_qk) {
+    StatsParams sp{};
+    sp.q = static_cast<const __nv_bfloat16*>(q);
+    sp.k = static_cast<const __nv_bfloat16*>(k);
+    sp.ksum = at<double>(ws, W.kpart);
+    sp.kmax = at<float>(ws, W.kmax);
+    sp.kmin = at<float>(ws, W.kmin);
+    sp.qmax = at<float>(ws, W.qmax);
+    sp.mean = at<float>(saved, S.mu);
+    sp.bexp = at<int>(saved, S.be);
+    sp.BHq = p->B * p->Hq;
+    sp.BHk = p->B * p->Hkv;
+    sp.G = p->Hq / p->Hkv;
+    sp.N = p->N;
+    sp.d = p->d;
+    sp.nb = nb;
+    sp.smooth = p->smooth_k ? 1 : 0;
+    sp.status = status;
+    SB_CHECK(cuda_status(launch_qk_stats(sp, st)));
+    bexp = at<int>(saved, S.be);
+  } else if (p->smooth_k) {
     SB_CHECK(cuda_status(launch_kmean(static_cast<const __nv_bfloat16*>(k), at<double>(ws, W.kpart),
                                       at<float>(saved, S.mu), p->B * p->Hkv, p->N, p->d, status, 1, st)));
-    mean = at<float>(saved, S.mu);
   }
+  const int G = p->Hq / p->Hkv;
   QuantParams qp{};
   qp.job[0] = {static_cast<const __nv_bfloat16*>(q), at<__nv_bfloat16>(saved, S.q), at<float>(saved, S.sq), nullptr,
-               p->B * p->Hq};
+               p->B * p->Hq, bexp, G, -1};
   qp.job[1] = {static_cast<const __nv_bfloat16*>(k), at<__nv_bfloat16>(saved, S.k), at<float>(saved, S.sk), mean,
-               p->B * p->Hkv};
+               p->B * p->Hkv, bexp, 1, 1};
   qp.job[2] = {static_cast<const __nv_bfloat16*>(v), at<__nv_bfloat16>(saved, S.v), at<float>(saved, S.sv), nullptr,
-               p->B * p->Hkv};
+               p->B * p->Hkv, nullptr, 1, 1};
   qp.njobs = 3;
   qp.block_start[0] = 0;
   for (int j = 0; j < 3; ++j) qp.block_start[j + 1] = qp.block_start[j] + qp.job[j].BH * nb;
@@ -182,7 +209,7 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
   qp.d = p->d;
   qp.nb = nb;
   qp.status = status;
-  qp.clear_status = p->smooth_k ? 0 : 1;
+  qp.clear_status = (p->smooth_k || p->balance_qk) ? 0 : 1;
   return cuda_status(launch_quantize(qp, st));
 }
 
@@ -297,12 +324,16 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
   return cuda_status(launch_bwd(tq, tk, tv, tdo, tdoq, tdq, bp, p->d, p->causal, st));
 }
 
-sagebwd_status bwd_finish_impl(const sagebwd_problem* p, void* dq, void* dk, void* dv, void* ws, cudaStream_t st) {
+sagebwd_status bwd_finish_impl(const sagebwd_problem* p, const void* saved, void* dq, void* dk, void* dv, void* ws,
+                               cudaStream_t st) {
   const WsLayout W = ws_layout(p, 1);
   const size_t nq = (size_t)p->B * p->Hq * p->N * p->d, nk = (size_t)p->B * p->Hkv * p->N * p->d;
-  const ConvertJob jobs[3] = {{at<float>(ws, W.dqacc), static_cast<__nv_bfloat16*>(dq), nq},
-                              {at<float>(ws, W.dkacc), static_cast<__nv_bfloat16*>(dk), nk},
-                              {at<float>(ws, W.dvacc), static_cast<__nv_bfloat16*>(dv), nk}};
+  // with channel balancing: dQ = dS (K 2^e) 2^-e and dK = dS^T (Q 2^-e) 2^e
+  const int* bexp = p->balance_qk ? at<int>(saved, saved_layout(p).be) : nullptr;
+  const ConvertJob jobs[3] = {
+      {at<float>(ws, W.dqacc), static_cast<__nv_bfloat16*>(dq), nq, bexp, -1, p->Hq / p->Hkv, p->N, p->d},
+      {at<float>(ws, W.dkacc), static_cast<__nv_bfloat16*>(dk), nk, bexp, 1, 1, p->N, p->d},
+      {at<float>(ws, W.dvacc), static_cast<__nv_bfloat16*>(dv), nk, nullptr, 1, 1, p->N, p->d}};
   return cuda_status(launch_grad_convert(jobs, 3, st));
 }
 
@@ -324,6 +355,8 @@ sagebwd_status sagebwd_quantize(const sagebwd_problem* prob, int which, const vo
                                 float* k_mean, void* ws, void* stream) {
   SB_CHECK(check_problem(prob));
   SB_CHECK(need(which >= SAGEBWD_Q && which <= SAGEBWD_DO, SAGEBWD_ERR_INVALID_ARG));
+  // balanced Q and K codes depend on both tensors: only sagebwd_fwd_quantize makes them
+  SB_CHECK(need(!(prob->balance_qk && (which == SAGEBWD_Q || which == SAGEBWD_K)), SAGEBWD_ERR_UNSUPPORTED));
   const bool smooth = which == SAGEBWD_K && prob->smooth_k;
   SB_CHECK(check_ptrs({x, x_q, scales, ws}));
   if (smooth) SB_CHECK(check_ptrs({k_mean}));
@@ -386,10 +419,11 @@ sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v,
   return bwd_attention_impl(prob, v, dO, lse, saved, ws, static_cast<cudaStream_t>(stream));
 }
 
-sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* dk, void* dv, void* ws, void* stream) {
+sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, const void* saved, void* dq, void* dk, void* dv,
+                                  void* ws, void* stream) {
   SB_CHECK(check_problem(prob));
-  SB_CHECK(check_ptrs({dq, dk, dv, ws}));
-  return bwd_finish_impl(prob, dq, dk, dv, ws, static_cast<cudaStream_t>(stream));
+  SB_CHECK(check_ptrs({saved, dq, dk, dv, ws}));
+  return bwd_finish_impl(prob, saved, dq, dk, dv, ws, static_cast<cudaStream_t>(stream));
 }
 
 sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const void* k, const void* v, const void* o,
@@ -400,7 +434,7 @@ sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const voi
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   SB_CHECK(bwd_prepare_impl(prob, o, dO, ws, st));
   SB_CHECK(bwd_attention_impl(prob, v, dO, lse, saved, ws, st));
-  return bwd_finish_impl(prob, dq, dk, dv, ws, st);
+  return bwd_finish_impl(prob, saved, dq, dk, dv, ws, st);
 }
 
 sagebwd_status sagebwd_check_status(const void* ws, void* stream, int32_t* detail) {

@@ -45,6 +45,7 @@ extern "C" sagebwd_status sagebwd_quantize_k_noalloc(const sagebwd_problem* prob
   if (prob == nullptr || prob->B < 1 || prob->Hq < 1 || prob->Hkv < 1 || prob->N < 1 || prob->Hq % prob->Hkv != 0)
     return SAGEBWD_ERR_INVALID_ARG;
   if (prob->d != 64 && prob->d != 128) return SAGEBWD_ERR_UNSUPPORTED;
+  if (prob->balance_qk) return SAGEBWD_ERR_UNSUPPORTED;  // balanced K codes depend on Q
   if ((double)prob->B * prob->Hkv * prob->N * prob->d >= 2147483648.0) return SAGEBWD_ERR_UNSUPPORTED;
   const bool smooth = prob->smooth_k != 0;
   for (const void* ptr : {k, (const void*)k_q, (const void*)scales}) {

@@ -12,6 +12,13 @@
 // gives codes 0 and s = 0.  K first subtracts its channel mean over all
 // N tokens, summed in FP64 in a fixed order (deterministic) and rounded once
 // to FP32.
+//
+// Optional channel balancing (the library's addition, after SmoothQuant,
+// listed under "Builds on" of the SageBwd page): per (batch, kv head, channel)
+// e = clamp(floor((E(aQ) - E(aK)) / 2), -126, 126), E the binary exponent of
+// the channel's max |Q| over the kv head's query heads and of its max
+// |K - mean|; Q's channel is multiplied by 2^-e and K's by 2^e (one exact FP32
+// multiply, after the smoothing) before the block quantizer.
 #include "sagebwd_internal.h"
 
 namespace sagebwd {
@@ -53,11 +60,23 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return m;
 }
 
+// 2^e as an FP32 number, for -126 <= e <= 127 (built from the IEEE 754 fields).
+__device__ __forceinline__ float exp2_int(int e) { return __int_as_float((127 + e) << 23); }
+
+// floor(log2 a) for a finite a > 0, read off the IEEE 754 fields (subnormals:
+// the position of the leading mantissa bit).
+__device__ __forceinline__ int binary_exponent(float a) {
+  const uint32_t u = __float_as_uint(a);
+  const int biased = (int)((u >> 23) & 0xFFu);
+  return biased ? biased - 127 : (31 - __clz((int)u)) - 149;
+}
+
 // Quantize the 128 x D block (bh, blk) of one tensor.  V8 = D / 8 16-byte vectors per row.
+// fac (optional): the channel balancing factors of this head's channels, in shared memory.
 template <int D>
 __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xq,
                                float* __restrict__ scale, const float* __restrict__ mean, int bh, int blk, int N,
-                               int nb, float* red) {
+                               int nb, float* red, const float* fac = nullptr) {
   constexpr int V8 = D / 8;
   constexpr int PER = kBlk * V8 / kThreads;  // 16-byte vectors per thread
   const int row0 = blk * kBlk;
@@ -75,6 +94,10 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
         const float* mu = mean + (size_t)bh * D + c8 * 8;
 #pragma unroll
         for (int k = 0; k < 8; ++k) v[e][k] = __fsub_rn(v[e][k], mu[k]);
+      }
+      if (fac != nullptr) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[e][k] = __fmul_rn(v[e][k], fac[c8 * 8 + k]);
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[e][k]));
@@ -102,12 +125,133 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
 template <int D>
 __global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantParams p) {
   __shared__ float red[kThreads / 32];
+  __shared__ float fac[D];
   if (p.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = 0;
   int j = 0;
   while (j + 1 < p.njobs && (int)blockIdx.x >= p.block_start[j + 1]) ++j;
   const int local = blockIdx.x - p.block_start[j];
   const QuantJob& job = p.job[j];
-  quantize_block<D>(job.x, job.xq, job.scale, job.mean, local / p.nb, local % p.nb, p.N, p.nb, red);
+  const int bh = local / p.nb;
+  if (job.bexp != nullptr) {
+    if (threadIdx.x < D) fac[threadIdx.x] = exp2_int(job.bexp_sign * job.bexp[(bh / job.bexp_group) * D + threadIdx.x]);
+    __syncthreads();  // quantize_block reads fac only after this
+  }
+  quantize_block<D>(job.x, job.xq, job.scale, job.mean, bh, local % p.nb, p.N, p.nb, red,
+                    job.bexp != nullptr ? fac : nullptr);
+}
+
+// Channel statistics of one 128-token block of one head.  Blocks with
+// blockIdx.y < BHk read K: FP64 channel sums (exact for BF16 inputs of
+// ordinary range) and channel max / min; the others read Q: channel max |Q|.
+template <int D>
+__global__ void __launch_bounds__(kThreads) qk_stats_partial_kernel(const StatsParams p) {
+  constexpr int V8 = D / 8, RL = kThreads / V8;  // row lanes
+  __shared__ double sred[RL][D];
+  __shared__ float xred[RL][D];
+  __shared__ float nred[RL][D];
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = 0;
+  const bool is_k = (int)blockIdx.y < p.BHk;
+  const int bh = is_k ? blockIdx.y : blockIdx.y - p.BHk, blk = blockIdx.x;
+  const __nv_bfloat16* x = is_k ? p.k : p.q;
+  const int c8 = threadIdx.x % V8, rl = threadIdx.x / V8;
+  double sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float mx[8], mn[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mx[e] = -INFINITY;
+    mn[e] = INFINITY;
+  }
+  for (int r = blk * kBlk + rl; r < min(p.N, blk * kBlk + kBlk); r += RL) {
+    float f[8];
+    unpack8(*reinterpret_cast<const uint4*>(x + ((size_t)bh * p.N + r) * D + c8 * 8), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (is_k) {
+        sum[e] += (double)f[e];
+        mx[e] = fmaxf(mx[e], f[e]);
+        mn[e] = fminf(mn[e], f[e]);
+      } else {
+        mx[e] = fmaxf(mx[e], fabsf(f[e]));
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sred[rl][c8 * 8 + e] = sum[e];
+    xred[rl][c8 * 8 + e] = mx[e];
+    nred[rl][c8 * 8 + e] = mn[e];
+  }
+  __syncthreads();
+  if (threadIdx.x < D) {
+    const int c = threadIdx.x;
+    double s = 0;
+    float a = -INFINITY, b = INFINITY;
+    for (int q = 0; q < RL; ++q) {
+      s += sred[q][c];
+      a = fmaxf(a, xred[q][c]);
+      b = fminf(b, nred[q][c]);
+    }
+    const size_t o = ((size_t)bh * p.nb + blk) * D + c;
+    if (is_k) {
+      p.ksum[o] = s;
+      p.kmax[o] = a;
+      p.kmin[o] = b;
+    } else {
+      p.qmax[o] = a;
+    }
+  }
+}
+
+// Per (b, kv head): the K channel means and the balancing exponents.  A CTA
+// takes 32 channels; its 8 warps reduce interleaved slices of the per-block
+// partials, then warp 0 combines the slices in a fixed order.  The K side of
+// the rule is max_n |fl(K_n - mean)|, which equals
+// max(fl(Kmax - mean), fl(mean - Kmin)) because rounding is monotonic and
+// symmetric.
+constexpr int kFinalSlices = 32;
+__global__ void __launch_bounds__(kFinalSlices * 32) qk_stats_final_kernel(const StatsParams p) {
+  __shared__ double ssum[kFinalSlices][32];
+  __shared__ float smax[kFinalSlices][32], smin[kFinalSlices][32], sq[kFinalSlices][32];
+  const int bhk = blockIdx.x, lane = threadIdx.x & 31, sl = threadIdx.x >> 5;
+  const int c = blockIdx.y * 32 + lane;
+  double s = 0;
+  float kx = -INFINITY, kn = INFINITY, aq = 0.f;
+#pragma unroll 4
+  for (int b = sl; b < p.nb; b += kFinalSlices) {
+    const size_t o = ((size_t)bhk * p.nb + b) * p.d + c;
+    s += p.ksum[o];
+    kx = fmaxf(kx, p.kmax[o]);
+    kn = fminf(kn, p.kmin[o]);
+  }
+  const int nq = p.G * p.nb;  // the kv head's query heads are consecutive: row (bhk * G + g) * nb + b
+#pragma unroll 4
+  for (int m = sl; m < nq; m += kFinalSlices) aq = fmaxf(aq, p.qmax[((size_t)bhk * nq + m) * p.d + c]);
+  ssum[sl][lane] = s;
+  smax[sl][lane] = kx;
+  smin[sl][lane] = kn;
+  sq[sl][lane] = aq;
+  __syncthreads();
+  if (sl != 0) return;
+  for (int q = 1; q < kFinalSlices; ++q) {
+    s += ssum[q][lane];
+    kx = fmaxf(kx, smax[q][lane]);
+    kn = fminf(kn, smin[q][lane]);
+    aq = fmaxf(aq, sq[q][lane]);
+  }
+  float ak;
+  if (p.smooth) {
+    const float mu = (float)(s / (double)p.N);
+    p.mean[(size_t)bhk * p.d + c] = mu;
+    ak = fmaxf(__fsub_rn(kx, mu), __fsub_rn(mu, kn));
+  } else {
+    ak = fmaxf(kx, -kn);
+  }
+  int e = 0;
+  if (aq > 0.f && ak > 0.f) {
+    e = (binary_exponent(aq) - binary_exponent(ak)) >> 1;  // arithmetic shift: floor of the half
+    e = min(126, max(-126, e));
+  }
+  p.bexp[(size_t)bhk * p.d + c] = e;
 }
 
 // Channel sums of K over one 128-token block, in FP64 (exact for BF16 inputs of
@@ -139,11 +283,22 @@ __global__ void __launch_bounds__(kThreads) kmean_partial_kernel(const __nv_bflo
   }
 }
 
-__global__ void kmean_final_kernel(const double* __restrict__ part, float* __restrict__ mean, int N, int nb, int d) {
-  const int bh = blockIdx.x, c = threadIdx.x;
-  if (c >= d) return;
+// Per head: the FP32 channel means from the per-block FP64 sums.  A CTA takes 32
+// channels; its warps sum interleaved slices of the blocks, warp 0 combines
+// the slices in a fixed order.
+__global__ void __launch_bounds__(kFinalSlices * 32) kmean_final_kernel(const double* __restrict__ part,
+                                                                        float* __restrict__ mean, int N, int nb,
+                                                                        int d) {
+  __shared__ double ssum[kFinalSlices][32];
+  const int bh = blockIdx.x, lane = threadIdx.x & 31, sl = threadIdx.x >> 5;
+  const int c = blockIdx.y * 32 + lane;
   double s = 0;
-  for (int b = 0; b < nb; ++b) s += part[((size_t)bh * nb + b) * d + c];
+#pragma unroll 4
+  for (int b = sl; b < nb; b += kFinalSlices) s += part[((size_t)bh * nb + b) * d + c];
+  ssum[sl][lane] = s;
+  __syncthreads();
+  if (sl != 0) return;
+  for (int q = 1; q < kFinalSlices; ++q) s += ssum[q][lane];
   mean[(size_t)bh * d + c] = (float)(s / (double)N);
 }
 
@@ -193,11 +348,22 @@ struct ConvertJobs {
 };
 __global__ void grad_convert_kernel(const ConvertJobs J) {
   for (int k = 0; k < J.njobs; ++k) {
-    const float4* acc = reinterpret_cast<const float4*>(J.job[k].acc);
-    uint2* out = reinterpret_cast<uint2*>(J.job[k].out);
-    const size_t n4 = J.job[k].n / 4;
+    const ConvertJob& job = J.job[k];
+    const float4* acc = reinterpret_cast<const float4*>(job.acc);
+    uint2* out = reinterpret_cast<uint2*>(job.out);
+    const size_t n4 = job.n / 4;
+    const size_t row_elems = (size_t)job.N * job.d;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-      const float4 v = acc[i];
+      float4 v = acc[i];
+      if (job.bexp != nullptr) {  // undo the channel balancing: exact power-of-two factors
+        const size_t e0 = 4 * i;
+        const int c = (int)(e0 % job.d);
+        const int* ex = job.bexp + (e0 / row_elems / job.group) * job.d + c;
+        v.x = __fmul_rn(v.x, exp2_int(job.sign * ex[0]));
+        v.y = __fmul_rn(v.y, exp2_int(job.sign * ex[1]));
+        v.z = __fmul_rn(v.z, exp2_int(job.sign * ex[2]));
+        v.w = __fmul_rn(v.w, exp2_int(job.sign * ex[3]));
+      }
       out[i] = make_uint2(pack2(v.x, v.y), pack2(v.z, v.w));
     }
   }
@@ -225,7 +391,19 @@ cudaError_t launch_kmean(const __nv_bfloat16* k, double* part, float* mean, int 
     kmean_partial_kernel<128><<<grid, kThreads, 0, s>>>(k, part, N, nb, status, clear_status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kmean_final_kernel<<<BH, d, 0, s>>>(part, mean, N, nb, d);
+  kmean_final_kernel<<<dim3(BH, d / 32), kFinalSlices * 32, 0, s>>>(part, mean, N, nb, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qk_stats(const StatsParams& p, cudaStream_t s) {
+  dim3 grid(p.nb, p.BHk + p.BHq);
+  if (p.d == 64)
+    qk_stats_partial_kernel<64><<<grid, kThreads, 0, s>>>(p);
+  else
+    qk_stats_partial_kernel<128><<<grid, kThreads, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  qk_stats_final_kernel<<<dim3(p.BHk, p.d / 32), kFinalSlices * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -32,6 +32,9 @@ struct QuantJob {
   float* scale;            // [BH][nb]
   const float* mean;       // [BH][d] or nullptr
   int BH;
+  const int* bexp;         // [B*Hkv][d] channel balancing exponents, or nullptr
+  int bexp_group;          // heads per exponent row: Hq/Hkv for Q, 1 for K
+  int bexp_sign;           // -1: x times 2^-e (Q); +1: x times 2^e (K)
 };
 struct QuantParams {
   QuantJob job[3];
@@ -44,6 +47,21 @@ struct QuantParams {
 cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s);
 cudaError_t launch_kmean(const __nv_bfloat16* k, double* part, float* mean, int BH, int N, int d, int* status,
                          int clear_status, cudaStream_t s);
+// Channel statistics of Q and K for the channel balancing: per (b, kv head,
+// channel) the K mean (smooth) and the balancing exponent.
+struct StatsParams {
+  const __nv_bfloat16* q;  // [B*Hq][N][d]
+  const __nv_bfloat16* k;  // [B*Hkv][N][d]
+  double* ksum;            // [B*Hkv][nb][d] partial sums (scratch)
+  float* kmax;             // [B*Hkv][nb][d] partial maxima (scratch)
+  float* kmin;             // [B*Hkv][nb][d] partial minima (scratch)
+  float* qmax;             // [B*Hq][nb][d] partial max |Q| (scratch)
+  float* mean;             // [B*Hkv][d] K channel means (written when smooth)
+  int* bexp;               // [B*Hkv][d] balancing exponents
+  int BHq, BHk, G, N, d, nb, smooth;
+  int* status;             // cleared by the first block
+};
+cudaError_t launch_qk_stats(const StatsParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ backward helpers
 struct PrepParams {
@@ -63,7 +81,11 @@ cudaError_t launch_bwd_prep(const PrepParams& p, cudaStream_t s);
 struct ConvertJob {
   const float* acc;
   __nv_bfloat16* out;
-  size_t n;  // elements, a multiple of 4
+  size_t n;          // elements, a multiple of 4
+  const int* bexp;   // nullptr, or [B*Hkv][d] balancing exponents: out = acc * 2^(sign * e)
+  int sign;          // -1 for dQ, +1 for dK
+  int group;         // heads per exponent row (Hq/Hkv for dQ, 1 for dK)
+  int N, d;
 };
 cudaError_t launch_grad_convert(const ConvertJob* jobs, int njobs, cudaStream_t s);
 

@@ -18,6 +18,16 @@
  *   forward P~  : per query row and 128-key tile, code = rint(127*2^(t-tmax));
  *   backward P  : per key and 128-query tile, scale = max P / 127;
  *   backward dS : one scale per 128 x 128 tile, scale = max|dS| / 127.
+ * Optional channel balancing (balance_qk = 1; off by default, this library's
+ * addition after SmoothQuant, listed under "Builds on" of the SageBwd page):
+ * per (batch, kv head, channel) an exponent
+ *   e = clamp(floor((E(aQ) - E(aK)) / 2), -126, 126)   (0 if aQ or aK is 0),
+ * with aQ the channel's max |Q| over the kv head's query heads and all
+ * tokens, aK its max |K - mean_K| (|K| without smoothing), E(a) = floor(log2 a);
+ * Q's channel is multiplied by 2^-e and K's (after smoothing) by 2^e before
+ * the block quantizers, which leaves Q K^T unchanged exactly and evens out
+ * channel outliers between the two operands; dQ is multiplied by 2^-e and
+ * dK by 2^e when they are converted to BF16.
  * The INT8 codes are held as integer-valued BF16 and multiplied on the
  * tensor cores with FP32 accumulation, which is exact for these tiles
  * (|sum| <= 128 * 127^2 < 2^24).
@@ -68,6 +78,7 @@ typedef struct {
   int32_t B, Hq, Hkv, N, d;
   int32_t causal;       /* 1: key k visible to query i iff k <= i (top-left aligned); 0: all keys */
   int32_t smooth_k;     /* 1: subtract the per-channel mean of K over tokens before quantizing (the method) */
+  int32_t balance_qk;   /* 1: power-of-two Q/K channel balancing before quantizing (see above); 0 in the method */
   uint32_t flags;       /* SAGEBWD_FLAG_* (0 in normal use) */
   float softmax_scale;  /* <= 0 selects 1/sqrt(d) */
   uint32_t wait_timeout_ms; /* bound of every in-kernel wait; 0 selects 2000 ms */
@@ -75,19 +86,23 @@ typedef struct {
 
 /* Bytes of the `saved` buffer that sagebwd_fwd fills and sagebwd_bwd reads:
  * the quantized Q, K, V (integer-valued BF16, same shapes as the inputs),
- * their FP32 block scales and the FP32 mean of K.  Returns 0 for an invalid
- * problem. */
+ * their FP32 block scales, the FP32 mean of K [B*Hkv][d] and the int32
+ * balancing exponents [B*Hkv][d] (written only with balance_qk), each section
+ * starting on a 256-byte boundary.  Returns 0 for an invalid problem. */
 size_t sagebwd_saved_bytes(const sagebwd_problem* prob);
 
 /* Bytes of workspace for pass 0 (forward, sagebwd_fwd / sagebwd_quantize) or
  * pass 1 (backward, sagebwd_bwd).  The workspace holds the status word first,
- * then scratch (K-mean partial sums; D = rowsum(dO*O), the quantized dO and
- * its scales, the FP32 dQ, dK and dV accumulators).  Contents need no initialisation and
- * are not meaningful between calls, except the status word. */
+ * then scratch (K-mean partial sums, and with balance_qk the per-block channel
+ * maxima of Q and K; D = rowsum(dO*O), the quantized dO and its scales, the
+ * FP32 dQ, dK and dV accumulators).  Contents need no initialisation and are
+ * not meaningful between calls, except the status word. */
 size_t sagebwd_workspace_bytes(const sagebwd_problem* prob, int pass);
 
 /* Quantize one operand ("SageBwd", Abstract: INT8 quantization; K-smoothing).
- *   which  : SAGEBWD_Q / _K / _V / _DO; x has that operand's shape.
+ *   which  : SAGEBWD_Q / _K / _V / _DO; x has that operand's shape.  With
+ *            balance_qk the codes of Q and K depend on both tensors: Q and K
+ *            then return SAGEBWD_ERR_UNSUPPORTED (use sagebwd_fwd_quantize).
  *   x_q    : BF16 output, same shape, integer values in [-127, 127].
  *   scales : FP32 [B*H][ceil(N/128)] block scales.
  *   k_mean : FP32 [B*Hkv][d] channel means when which == SAGEBWD_K and
@@ -96,7 +111,7 @@ size_t sagebwd_workspace_bytes(const sagebwd_problem* prob, int pass);
 sagebwd_status sagebwd_quantize(const sagebwd_problem* prob, int which, const void* x, void* x_q, float* scales,
                                 float* k_mean, void* ws, void* stream);
 
-/* Forward: quantize Q, K (smoothed), V into `saved`, then the fused
+/* Forward: quantize Q, K (smoothed, balanced as selected), V into `saved`, then the fused
  * attention forward with online softmax ("SageBwd", Abstract; FlashAttention
  * lineage listed under "Builds on").
  *   o   : BF16 [B][Hq][N][d] output.
@@ -123,13 +138,15 @@ sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const voi
 /* The same two passes split into the library's kernel stages, for callers
  * that schedule or time them separately.  Calling the stages in this order,
  * on one stream, is exactly sagebwd_fwd / sagebwd_bwd.
- *   sagebwd_fwd_quantize  : K mean and the Q, K, V quantization into `saved`.
+ *   sagebwd_fwd_quantize  : K mean (and the balancing exponents) and the
+ *                           Q, K, V quantization into `saved`.
  *   sagebwd_fwd_attention : the fused forward kernel on `saved` -> o, lse.
  *   sagebwd_bwd_prepare   : D = rowsum(dO * O), quantized dO, zeroed dQ, dK
  *                           and dV accumulators (all in the backward workspace).
  *   sagebwd_bwd_attention : the fused backward kernel -> the FP32 dQ, dK, dV
  *                           accumulators in the workspace.
- *   sagebwd_bwd_finish    : the accumulators -> BF16 dq, dk, dv.             */
+ *   sagebwd_bwd_finish    : the accumulators -> BF16 dq, dk, dv (times 2^-e
+ *                           and 2^e with balance_qk; `saved` holds e).     */
 sagebwd_status sagebwd_fwd_quantize(const sagebwd_problem* prob, const void* q, const void* k, const void* v,
                                     void* saved, void* ws, void* stream);
 sagebwd_status sagebwd_fwd_attention(const sagebwd_problem* prob, const void* saved, void* o, float* lse, void* ws,
@@ -138,7 +155,8 @@ sagebwd_status sagebwd_bwd_prepare(const sagebwd_problem* prob, const void* o, c
                                    void* stream);
 sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v, const void* dO, const float* lse,
                                      const void* saved, void* ws, void* stream);
-sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* dk, void* dv, void* ws, void* stream);
+sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, const void* saved, void* dq, void* dk, void* dv,
+                                  void* ws, void* stream);
 
 /* K quantization (K-smoothing mean + per-block codes), like
  * sagebwd_quantize(prob, SAGEBWD_K, ...), for callers that cannot allocate
@@ -149,6 +167,8 @@ sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, void* dq, void* d
  * a fixed 8 MiB array compiled into the library, which every GPU that loads
  * the library keeps until the process exits.  (The SageBwd pages have no
  * counterpart of this entry point.)
+ *   - balance_qk must be 0 (K's codes would depend on Q): else
+ *     SAGEBWD_ERR_UNSUPPORTED.
  *   - Limit: B * Hkv * ceil(N/128) * d <= 1048576 (e.g. B=2, Hkv=30, N=17776,
  *     d=64 needs 533760); larger problems return SAGEBWD_ERR_SCRATCH_LIMIT
  *     before any launch.  With smooth_k == 0 no scratch is used.

@@ -43,7 +43,7 @@ def test_sizes_and_strings(lib):
     saved = sb.sagebwd_saved_bytes(p)
     al = lambda x: (x + 255) // 256 * 256  # noqa: E731
     expect = al(1 * 4 * 300 * 64 * 2) + 2 * al(1 * 2 * 300 * 64 * 2) + al(4 * nb * 4) + 2 * al(2 * nb * 4) + \
-        al(2 * 64 * 4)
+        2 * al(2 * 64 * 4)  # ... K mean, balancing exponents
     assert saved == expect
     assert sb.sagebwd_workspace_bytes(p, 0) >= 256 + 2 * nb * 64 * 8
     assert sb.sagebwd_workspace_bytes(p, 1) >= 256 + 4 * 300 * 64 * (4 + 2)
@@ -81,3 +81,23 @@ def test_bad_pointers_rejected_before_launch(lib):
     # K with smoothing needs the mean output
     assert lib.sagebwd_quantize(ctypes.byref(p), 1, good, good, good, None, good, None) == 1
     assert lib.sagebwd_check_status(None, None, None) == 1
+
+
+def test_balancing_sizes_and_rejections(lib):
+    """With balance_qk the forward workspace adds the per-block channel maxima of K (max, min) and Q;
+    the single-operand quantizers refuse Q and K (their codes would depend on both tensors)."""
+    p0 = sb.Problem.make(1, 4, 2, 300, 64, True)
+    p1 = sb.Problem.make(1, 4, 2, 300, 64, True, balance_qk=True)
+    nb = 3
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert sb.sagebwd_saved_bytes(p1) == sb.sagebwd_saved_bytes(p0)
+    extra = 2 * al(2 * nb * 64 * 4) + al(4 * nb * 64 * 4)
+    assert sb.sagebwd_workspace_bytes(p1, 0) == sb.sagebwd_workspace_bytes(p0, 0) + extra
+    assert sb.sagebwd_workspace_bytes(p1, 1) == sb.sagebwd_workspace_bytes(p0, 1)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the calls return before any launch
+    for which in (sb.SAGEBWD_Q, sb.SAGEBWD_K):
+        assert lib.sagebwd_quantize(ctypes.byref(p1), which, fake, fake, fake, fake, fake, None) == 2
+    assert lib.sagebwd_quantize_k_noalloc(ctypes.byref(p1), fake, fake, fake, fake, None) == 2
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.sagebwd_bwd_finish(ctypes.byref(p1), odd, fake, fake, fake, fake, None) == 3
+    assert lib.sagebwd_bwd_finish(ctypes.byref(p1), None, fake, fake, fake, fake, None) == 1

@@ -69,15 +69,18 @@ def test_forward_without_smoothing(oracle_mod):
     np.testing.assert_allclose(to_np(fwd["lse"]), lse_ref, rtol=0, atol=LSE_TOL)
 
 
-def test_forward_repeatable(oracle_mod):
+@pytest.mark.parametrize("balance", [False, True], ids=["plain", "balanced"])
+def test_forward_repeatable(oracle_mod, balance):
     """Two calls on the same inputs give identical bits (no atomics in the forward)."""
-    w = W.small("rep", 1, 4, 2, 520, 64, True, 112, qk_norm=True)
+    w = W.small("rep", 1, 4, 2, 520, 64, True, 112, qk_norm=True, outlier_frac=0.02 if balance else 0.0)
     _, xd = device_inputs(w)
-    a = gpu_forward(w, xd)
-    b = gpu_forward(w, xd)
+    a = gpu_forward(w, xd, balance_qk=balance)
+    b = gpu_forward(w, xd, balance_qk=balance)
     assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
     va, vb = sb.quantized_views(a["prob"], a["saved"]), sb.quantized_views(b["prob"], b["saved"])
     for key in va:  # the sections of the saved buffer (its alignment padding is never written)
+        if key == "e" and not a["prob"].balance_qk:
+            continue  # the balancing exponents are written only with balance_qk
         assert torch.equal(va[key], vb[key]), key
 
 
