@@ -140,39 +140,83 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantParams p)
                     job.bexp != nullptr ? fac : nullptr);
 }
 
+// Exact channel sums of one thread's rows (u: RPL 16-byte vectors of 8 BF16
+// channels; rows past N were loaded as zeros).  FP32 additions are checked
+// with Knuth's error-free TwoSum (s = a + b, err = (a - (s - (s - a))) +
+// (b - (s - a))); when none of them rounded, the FP32 sums are exact and only
+// they are widened to FP64 -- FP64 is slow on this GPU.  A thread whose values
+// span too wide a range for that re-sums its rows in FP64.  The result is the
+// exact sum either way (for BF16 inputs of ordinary range, where the FP64
+// additions that follow are exact too).
+template <int RPL>
+__device__ __forceinline__ void exact_row_sums(const uint4 (&u)[RPL], double (&acc)[8]) {
+  float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  bool exact = true;
+#pragma unroll
+  for (int i = 0; i < RPL; ++i) {
+    float f[8];
+    unpack8(u[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float t = __fadd_rn(sum[e], f[e]);
+      const float bv = __fsub_rn(t, sum[e]);
+      const float err = __fadd_rn(__fsub_rn(sum[e], __fsub_rn(t, bv)), __fsub_rn(f[e], bv));
+      exact = exact && (err == 0.f);
+      sum[e] = t;
+    }
+  }
+  if (exact) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = (double)sum[e];
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0;
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+      float f[8];
+      unpack8(u[i], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += (double)f[e];
+    }
+  }
+}
+
 // Channel statistics of one 128-token block of one head.  Blocks with
 // blockIdx.y < BHk read K: FP64 channel sums (exact for BF16 inputs of
-// ordinary range) and channel max / min; the others read Q: channel max |Q|.
+// ordinary range) and channel max / min; the others read Q: channel max |Q|,
+// in FP32 only.  Every thread loads its RPL rows up front (16-byte vectors,
+// rows past N skipped), then the row lanes are combined in shared memory.
 template <int D>
-__global__ void __launch_bounds__(kThreads) qk_stats_partial_kernel(const StatsParams p) {
-  constexpr int V8 = D / 8, RL = kThreads / V8;  // row lanes
-  __shared__ double sred[RL][D];
-  __shared__ float xred[RL][D];
-  __shared__ float nred[RL][D];
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = 0;
-  const bool is_k = (int)blockIdx.y < p.BHk;
-  const int bh = is_k ? blockIdx.y : blockIdx.y - p.BHk, blk = blockIdx.x;
-  const __nv_bfloat16* x = is_k ? p.k : p.q;
+__device__ __forceinline__ void k_stats_block(const StatsParams& p, int bh, int blk, uint8_t* smem) {
+  constexpr int V8 = D / 8, RL = kThreads / V8, RPL = kBlk / RL;  // row lanes, rows per lane
+  double(*sred)[D] = reinterpret_cast<double(*)[D]>(smem);
+  float(*xred)[D] = reinterpret_cast<float(*)[D]>(smem + sizeof(double) * RL * D);
+  float(*nred)[D] = reinterpret_cast<float(*)[D]>(smem + (sizeof(double) + sizeof(float)) * RL * D);
   const int c8 = threadIdx.x % V8, rl = threadIdx.x / V8;
-  double sum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  uint4 u[RPL];
+#pragma unroll
+  for (int i = 0; i < RPL; ++i) {
+    const int r = blk * kBlk + rl + i * RL;
+    u[i] = r < p.N ? *reinterpret_cast<const uint4*>(p.k + ((size_t)bh * p.N + r) * D + c8 * 8)
+                   : make_uint4(0u, 0u, 0u, 0u);
+  }
+  double sum[8];
+  exact_row_sums<RPL>(u, sum);
   float mx[8], mn[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     mx[e] = -INFINITY;
     mn[e] = INFINITY;
   }
-  for (int r = blk * kBlk + rl; r < min(p.N, blk * kBlk + kBlk); r += RL) {
+#pragma unroll
+  for (int i = 0; i < RPL; ++i) {
+    if (blk * kBlk + rl + i * RL >= p.N) continue;
     float f[8];
-    unpack8(*reinterpret_cast<const uint4*>(x + ((size_t)bh * p.N + r) * D + c8 * 8), f);
+    unpack8(u[i], f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      if (is_k) {
-        sum[e] += (double)f[e];
-        mx[e] = fmaxf(mx[e], f[e]);
-        mn[e] = fminf(mn[e], f[e]);
-      } else {
-        mx[e] = fmaxf(mx[e], fabsf(f[e]));
-      }
+      mx[e] = fmaxf(mx[e], f[e]);
+      mn[e] = fminf(mn[e], f[e]);
     }
   }
 #pragma unroll
@@ -186,20 +230,59 @@ __global__ void __launch_bounds__(kThreads) qk_stats_partial_kernel(const StatsP
     const int c = threadIdx.x;
     double s = 0;
     float a = -INFINITY, b = INFINITY;
+#pragma unroll
     for (int q = 0; q < RL; ++q) {
       s += sred[q][c];
       a = fmaxf(a, xred[q][c]);
       b = fminf(b, nred[q][c]);
     }
     const size_t o = ((size_t)bh * p.nb + blk) * D + c;
-    if (is_k) {
-      p.ksum[o] = s;
-      p.kmax[o] = a;
-      p.kmin[o] = b;
-    } else {
-      p.qmax[o] = a;
-    }
+    p.ksum[o] = s;
+    p.kmax[o] = a;
+    p.kmin[o] = b;
   }
+}
+
+template <int D>
+__device__ __forceinline__ void q_absmax_block(const StatsParams& p, int bh, int blk, uint8_t* smem) {
+  constexpr int V8 = D / 8, RL = kThreads / V8, RPL = kBlk / RL;
+  float(*xred)[D] = reinterpret_cast<float(*)[D]>(smem);
+  const int c8 = threadIdx.x % V8, rl = threadIdx.x / V8;
+  uint4 u[RPL];
+#pragma unroll
+  for (int i = 0; i < RPL; ++i) {
+    const int r = blk * kBlk + rl + i * RL;
+    u[i] = r < p.N ? *reinterpret_cast<const uint4*>(p.q + ((size_t)bh * p.N + r) * D + c8 * 8)
+                   : make_uint4(0u, 0u, 0u, 0u);  // |0| never raises a maximum
+  }
+  float mx[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < RPL; ++i) {
+    float f[8];
+    unpack8(u[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], fabsf(f[e]));
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) xred[rl][c8 * 8 + e] = mx[e];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float a = 0.f;
+#pragma unroll
+    for (int q = 0; q < RL; ++q) a = fmaxf(a, xred[q][threadIdx.x]);
+    p.qmax[((size_t)bh * p.nb + blk) * D + threadIdx.x] = a;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) qk_stats_partial_kernel(const StatsParams p) {
+  constexpr int RL = kThreads / (D / 8);
+  __shared__ __align__(16) uint8_t smem[(sizeof(double) + 2 * sizeof(float)) * RL * D];
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.status = 0;
+  if ((int)blockIdx.y < p.BHk)
+    k_stats_block<D>(p, blockIdx.y, blockIdx.x, smem);
+  else
+    q_absmax_block<D>(p, blockIdx.y - p.BHk, blockIdx.x, smem);
 }
 
 // Per (b, kv head): the K channel means and the balancing exponents.  A CTA
@@ -264,20 +347,23 @@ __global__ void __launch_bounds__(kThreads) kmean_partial_kernel(const __nv_bflo
   __shared__ double red[RL][D];
   if (clear_status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0;
   const int bh = blockIdx.y, blk = blockIdx.x;
+  constexpr int RPL = kBlk / RL;  // rows per lane, all loaded up front
   const int c8 = threadIdx.x % V8, rl = threadIdx.x / V8;
-  double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int r = blk * kBlk + rl; r < min(N, blk * kBlk + kBlk); r += RL) {
-    const uint4 u = *reinterpret_cast<const uint4*>(k + ((size_t)bh * N + r) * D + c8 * 8);
-    float f[8];
-    unpack8(u, f);
+  uint4 u[RPL];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += (double)f[e];
+  for (int i = 0; i < RPL; ++i) {
+    const int r = blk * kBlk + rl + i * RL;
+    u[i] = r < N ? *reinterpret_cast<const uint4*>(k + ((size_t)bh * N + r) * D + c8 * 8)
+                 : make_uint4(0u, 0u, 0u, 0u);  // adds 0
   }
+  double acc[8];
+  exact_row_sums<RPL>(u, acc);
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[rl][c8 * 8 + e] = acc[e];
   __syncthreads();
   if (threadIdx.x < D) {
     double s = 0;
+#pragma unroll
     for (int q = 0; q < RL; ++q) s += red[q][threadIdx.x];
     part[((size_t)bh * nb + blk) * D + threadIdx.x] = s;
   }

@@ -106,3 +106,27 @@ def test_forward_full_size_sampled(oracle_mod, name):
     assert_parity(o[m], o_ref[m], "O")
     np.testing.assert_allclose(lse[m], lse_ref[m], rtol=0, atol=LSE_TOL)
     assert np.all(np.isfinite(o))
+
+
+@pytest.mark.parametrize("balance", [False, True], ids=["kmean", "stats"])
+def test_k_mean_over_a_wide_value_range(oracle_mod, balance):
+    """K values whose magnitudes span 2^-12 .. 2^13 within a channel: FP32 partial sums
+    would round, so the library's exactness check must fall back to FP64; the mean (and the
+    codes) still equal the oracle's bit for bit.  Covers both K-mean kernels (the plain one
+    and the balancing statistics)."""
+    w = W.small("wide", 1, 2, 2, 300, 64, False, 113)
+    x = W.make_inputs(w)
+    g = torch.Generator().manual_seed(7)
+    mag = torch.exp2(torch.randint(-12, 13, x["k"].shape, generator=g).float())  # FP64 sums stay exact
+    x["k"] = (x["k"].float().sign() * mag * (1 + torch.rand(x["k"].shape, generator=g))).to(torch.bfloat16)
+    xd = {k: v.cuda() for k, v in x.items()}
+    fwd = gpu_forward(w, xd, balance_qk=balance)
+    assert fwd["status"] == 0
+    op = oracle_problem(oracle_mod, w, balance_qk=balance)
+    ref = oracle_mod.quantize_qk(op, x["q"], x["k"])
+    views = sb.quantized_views(fwd["prob"], fwd["saved"])
+    np.testing.assert_array_equal(views["mu"].cpu().numpy().view(np.uint32), ref["mu"].view(np.uint32))
+    np.testing.assert_array_equal(views["k"].float().cpu().numpy().reshape(ref["k"].shape),
+                                  ref["k"].astype(np.float32))
+    if balance:
+        np.testing.assert_array_equal(views["e"].cpu().numpy(), ref["e"])
