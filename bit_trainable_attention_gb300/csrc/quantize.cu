@@ -71,36 +71,54 @@ __device__ __forceinline__ int binary_exponent(float a) {
   return biased ? biased - 127 : (31 - __clz((int)u)) - 149;
 }
 
-// Quantize the 128 x D block (bh, blk) of one tensor.  V8 = D / 8 16-byte vectors per row.
+// Quantize the 128 x D block (bh, blk) of one tensor.  V8 = D / 8 16-byte vectors per row;
+// a thread keeps one 8-channel group (kThreads is a multiple of V8) over PER rows, holds
+// the raw vectors in registers and unpacks them twice (absmax pass, code pass), which keeps
+// the register count low enough for several CTAs per SM.
 // fac (optional): the channel balancing factors of this head's channels, in shared memory.
 template <int D>
 __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xq,
                                float* __restrict__ scale, const float* __restrict__ mean, int bh, int blk, int N,
                                int nb, float* red, const float* fac = nullptr) {
-  constexpr int V8 = D / 8;
-  constexpr int PER = kBlk * V8 / kThreads;  // 16-byte vectors per thread
+  constexpr int V8 = D / 8, RL = kThreads / V8;
+  constexpr int PER = kBlk / RL;  // rows (16-byte vectors) per thread
+  static_assert(kThreads % V8 == 0 && kBlk % RL == 0, "thread layout");
   const int row0 = blk * kBlk;
   const size_t base = ((size_t)bh * N + row0) * D;
-  float v[PER][8];
+  const int c8 = threadIdx.x % V8, rl = threadIdx.x / V8;
+  float mu[8], fc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    mu[k] = mean != nullptr ? mean[(size_t)bh * D + c8 * 8 + k] : 0.f;
+    fc[k] = fac != nullptr ? fac[c8 * 8 + k] : 1.f;
+  }
+  // K - mean, then times the balancing factor (each an FP32 rounding), as configured
+  auto load = [&](const uint4& u, float (&v)[8]) {
+    unpack8(u, v);
+    if (mean != nullptr) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = __fsub_rn(v[k], mu[k]);
+    }
+    if (fac != nullptr) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = __fmul_rn(v[k], fc[k]);
+    }
+  };
+  uint4 raw[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int r = rl + e * RL;
+    raw[e] = row0 + r < N ? *reinterpret_cast<const uint4*>(x + base + (size_t)r * D + c8 * 8)
+                          : make_uint4(0u, 0u, 0u, 0u);
+  }
   float amax = 0.f;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
-    const int idx = threadIdx.x + e * kThreads;
-    const int r = idx / V8, c8 = idx % V8;
-    if (row0 + r < N) {
-      const uint4 u = *reinterpret_cast<const uint4*>(x + base + (size_t)r * D + c8 * 8);
-      unpack8(u, v[e]);
-      if (mean != nullptr) {
-        const float* mu = mean + (size_t)bh * D + c8 * 8;
+    if (row0 + rl + e * RL < N) {
+      float v[8];
+      load(raw[e], v);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[e][k] = __fsub_rn(v[e][k], mu[k]);
-      }
-      if (fac != nullptr) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[e][k] = __fmul_rn(v[e][k], fac[c8 * 8 + k]);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[e][k]));
+      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
     }
   }
   const float a = block_max(amax, red);
@@ -108,14 +126,15 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
   const float inv = live ? __fdiv_rn(127.f, a) : 0.f;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
-    const int idx = threadIdx.x + e * kThreads;
-    const int r = idx / V8, c8 = idx % V8;
+    const int r = rl + e * RL;
     if (row0 + r < N) {
+      float v[8];
+      load(raw[e], v);
       uint4 out;
-      out.x = pack2(quant_code(v[e][0], inv), quant_code(v[e][1], inv));
-      out.y = pack2(quant_code(v[e][2], inv), quant_code(v[e][3], inv));
-      out.z = pack2(quant_code(v[e][4], inv), quant_code(v[e][5], inv));
-      out.w = pack2(quant_code(v[e][6], inv), quant_code(v[e][7], inv));
+      out.x = pack2(quant_code(v[0], inv), quant_code(v[1], inv));
+      out.y = pack2(quant_code(v[2], inv), quant_code(v[3], inv));
+      out.z = pack2(quant_code(v[4], inv), quant_code(v[5], inv));
+      out.w = pack2(quant_code(v[6], inv), quant_code(v[7], inv));
       *reinterpret_cast<uint4*>(xq + base + (size_t)r * D + c8 * 8) = out;
     }
   }
@@ -123,7 +142,7 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kThreads, 4) quantize_kernel(const QuantParams p) {
   __shared__ float red[kThreads / 32];
   __shared__ float fac[D];
   if (p.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = 0;
@@ -439,18 +458,30 @@ __global__ void grad_convert_kernel(const ConvertJobs J) {
     uint2* out = reinterpret_cast<uint2*>(job.out);
     const size_t n4 = job.n / 4;
     const size_t row_elems = (size_t)job.N * job.d;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-      float4 v = acc[i];
-      if (job.bexp != nullptr) {  // undo the channel balancing: exact power-of-two factors
-        const size_t e0 = 4 * i;
-        const int c = (int)(e0 % job.d);
-        const int* ex = job.bexp + (e0 / row_elems / job.group) * job.d + c;
-        v.x = __fmul_rn(v.x, exp2_int(job.sign * ex[0]));
-        v.y = __fmul_rn(v.y, exp2_int(job.sign * ex[1]));
-        v.z = __fmul_rn(v.z, exp2_int(job.sign * ex[2]));
-        v.w = __fmul_rn(v.w, exp2_int(job.sign * ex[3]));
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    constexpr int U = 4;  // vectors in flight per thread
+    for (size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n4; i0 += U * stride) {
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const size_t i = i0 + u * stride;
+        if (i < n4) v[u] = acc[i];
       }
-      out[i] = make_uint2(pack2(v.x, v.y), pack2(v.z, v.w));
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const size_t i = i0 + u * stride;
+        if (i >= n4) continue;
+        if (job.bexp != nullptr) {  // undo the channel balancing: exact power-of-two factors
+          const size_t e0 = 4 * i;
+          const int c = (int)(e0 % job.d);
+          const int* ex = job.bexp + (e0 / row_elems / job.group) * job.d + c;
+          v[u].x = __fmul_rn(v[u].x, exp2_int(job.sign * ex[0]));
+          v[u].y = __fmul_rn(v[u].y, exp2_int(job.sign * ex[1]));
+          v[u].z = __fmul_rn(v[u].z, exp2_int(job.sign * ex[2]));
+          v[u].w = __fmul_rn(v[u].w, exp2_int(job.sign * ex[3]));
+        }
+        out[i] = make_uint2(pack2(v[u].x, v[u].y), pack2(v[u].z, v[u].w));
+      }
     }
   }
 }
