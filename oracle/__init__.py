@@ -31,7 +31,7 @@ class OracleProblem(ctypes.Structure):
         ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
         ("N", ctypes.c_int32), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
         ("smooth_k", ctypes.c_int32), ("balance_qk", ctypes.c_int32), ("exact_codes", ctypes.c_int32),
-        ("threads", ctypes.c_int32), ("exact_mask", ctypes.c_uint32),
+        ("threads", ctypes.c_int32), ("exact_mask", ctypes.c_uint32), ("int8_dp", ctypes.c_int32),
         ("softmax_scale", ctypes.c_double),
     ]
 
@@ -88,9 +88,9 @@ def _bf16_bits(x) -> np.ndarray:
 
 
 def problem(B, Hq, Hkv, N, d, causal, smooth_k=True, exact_codes=False, softmax_scale=0.0, threads=0, exact_mask=0,
-            balance_qk=False):
+            balance_qk=False, int8_dp=False):
     return OracleProblem(B, Hq, Hkv, N, d, int(causal), int(smooth_k), int(balance_qk), int(exact_codes),
-                         int(threads), int(exact_mask), float(softmax_scale))
+                         int(threads), int(exact_mask), int(int8_dp), float(softmax_scale))
 
 
 def nblocks(N: int) -> int:

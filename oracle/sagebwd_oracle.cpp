@@ -34,6 +34,8 @@
 //  * dP = dO V^T uses the BF16 inputs, accumulated here in FP64;
 //  * no correction term for the gradient through the K mean (each row of dS
 //    sums to zero, so the mean's gradient vanishes);
+//  * ablation int8_dp (off by default): dP = dO V^T from the INT8 codes of dO
+//    and V, the variant the pages' ablation rejects;
 //  * optional channel balancing (balance_qk, off by default; the library's
 //    own addition, after SmoothQuant, listed under "Builds on" of the SageBwd
 //    page): per (batch, kv head, channel) an exponent e moves magnitude
@@ -67,6 +69,7 @@ typedef struct {
   int32_t threads;      // <= 0: OpenMP default
   uint32_t exact_mask;  // error attribution: bit set = that quantizer keeps its scale but skips rint/clamp
                         // (bit 0 Q, 1 K, 2 V, 3 dO, 4 P~ forward, 5 P^T backward, 6 dS); FP32 rounding stays
+  int32_t int8_dp;      // ablation: dP = dO V^T from the INT8 codes of dO and V instead of BF16 operands
   double softmax_scale;  // <= 0: 1/sqrt(d)
 } oracle_problem;
 }
@@ -361,7 +364,7 @@ struct BwdTile {
 
 void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const QTensor& kq, const uint16_t* v,
               const uint16_t* dO, const double* o, const double* lse, int b, int h, int ib, int jb, double c0,
-              double l2e, BwdTile& T) {
+              double l2e, BwdTile& T, const QTensor* doq = nullptr, const QTensor* vq = nullptr) {
   const int N = p->N, d = p->d, G = p->Hq / p->Hkv, hk = h / G;
   const int bhq = b * p->Hq + h, bhk = b * p->Hkv + hk;
   T.i0 = ib * BLK;
@@ -383,10 +386,17 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
       for (int ch = 0; ch < d; ++ch) s += qq.c(bhq, i, ch) * kq.c(bhk, kk, ch);
       const double tt = M.F(s * qks);
       const double pp = M.F(std::exp2(M.F(tt - L)));  // normalized probability
-      // dP = dO V^T: the product kept in high precision (BF16 inputs, FP64 sum here).
+      // dP = dO V^T: the product kept in high precision (BF16 inputs, FP64 sum here);
+      // the int8_dp ablation takes it from the dO and V codes instead (the pages' ablation
+      // "Keep dO V^T in FP16 instead of quantizing it to INT8", run the other way round).
       double dp = 0;
-      const size_t vrow = ((size_t)bhk * N + kk) * d;
-      for (int ch = 0; ch < d; ++ch) dp += bf16_to_double(dO[qrow + ch]) * bf16_to_double(v[vrow + ch]);
+      if (doq && vq) {
+        for (int ch = 0; ch < d; ++ch) dp += doq->c(bhq, i, ch) * vq->c(bhk, kk, ch);
+        dp *= doq->s(bhq, ib) * vq->s(bhk, jb);
+      } else {
+        const size_t vrow = ((size_t)bhk * N + kk) * d;
+        for (int ch = 0; ch < d; ++ch) dp += bf16_to_double(dO[qrow + ch]) * bf16_to_double(v[vrow + ch]);
+      }
       P[(size_t)a * BLK + c] = pp;
       dS[(size_t)a * BLK + c] = M.F(pp * (dp - D));
     }
@@ -420,10 +430,13 @@ void bwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, con
               const uint16_t* dO, const double* lse, double* dq, double* dk, double* dv, const uint8_t* qsel,
               const uint8_t* ksel) {
   const Mode M = mode_of(p);
-  QTensor qq, kq, dq8;
+  QTensor qq, kq, dq8, vq;
   std::vector<double> fq, fk;  // channel balancing factors, undone on dQ and dK at the end
   quantize_qk(M, p, q, k, qq, kq, nullptr, &fq, &fk);
   quantize_tensor(M, QZ_DO, dO, p->B * p->Hq, p->N, p->d, false, dq8);
+  if (p->int8_dp) quantize_tensor(M, QZ_V, v, p->B * p->Hkv, p->N, p->d, false, vq);
+  const QTensor* dp_do = p->int8_dp ? &dq8 : nullptr;
+  const QTensor* dp_v = p->int8_dp ? &vq : nullptr;
   const double sc = scale_of(p);
   const double c0 = M.F(sc * kLog2e);
   const double l2e = M.F(kLog2e);
@@ -443,7 +456,7 @@ void bwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, con
       for (int h = hk * G; h < (hk + 1) * G; ++h) {
         const int bhq = b * p->Hq + h;
         for (int ib = p->causal ? jb : 0; ib < nb; ++ib) {
-          bwd_tile(M, p, qq, kq, v, dO, o, lse, b, h, ib, jb, c0, l2e, T);
+          bwd_tile(M, p, qq, kq, v, dO, o, lse, b, h, ib, jb, c0, l2e, T, dp_do, dp_v);
           for (int c = 0; c < T.nk; ++c)
             for (int ch = 0; ch < d; ++ch) {
               double sv = 0, sk = 0;
@@ -477,7 +490,7 @@ void bwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, con
       const int bhk = b * p->Hkv + h / G;
       std::fill(accq.begin(), accq.end(), 0.0);
       for (int jb = 0; jb <= (p->causal ? ib : nb - 1); ++jb) {
-        bwd_tile(M, p, qq, kq, v, dO, o, lse, b, h, ib, jb, c0, l2e, T);
+        bwd_tile(M, p, qq, kq, v, dO, o, lse, b, h, ib, jb, c0, l2e, T, dp_do, dp_v);
         for (int a = 0; a < T.ni; ++a)
           for (int ch = 0; ch < d; ++ch) {
             double s = 0;
