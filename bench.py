@@ -290,6 +290,89 @@ def time_e2e(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_barr
     return ms, h2d, d2h
 
 
+# ---------------------------------------------------------------------------- layer-stack timing
+LLAMA_1B = {"layers": 16, "hidden": 2048, "inter": 8192, "hq": 32, "hkv": 8, "d": 64}
+
+
+def _rms(x, eps=1e-6):
+    return x * torch.rsqrt(x.float().pow(2).mean(-1, keepdim=True) + eps).to(x.dtype)
+
+
+class _LlamaShapedStack:
+    """Random-weight decoder layers of Llama-3.2-1B's shapes (RMSNorm, fused QKV projection,
+    QK-norm, grouped-query attention, output projection, SwiGLU MLP, residuals; no RoPE), BF16.
+    Only timing: the weights are random, so nothing here is a trained model."""
+
+    def __init__(self, cfg, dev, seed=0):
+        g = torch.Generator(device="cpu").manual_seed(seed)
+        h, f, hq, hkv, d = cfg["hidden"], cfg["inter"], cfg["hq"], cfg["hkv"], cfg["d"]
+        self.cfg = cfg
+
+        def w(i, o):
+            return (torch.randn(o, i, generator=g) * i ** -0.5).to(torch.bfloat16).to(dev).requires_grad_(True)
+        self.layers = [{"qkv": w(h, (hq + 2 * hkv) * d), "o": w(hq * d, h), "up": w(h, f), "gate": w(h, f),
+                        "down": w(f, h)} for _ in range(cfg["layers"])]
+
+    def params(self):
+        return [t for layer in self.layers for t in layer.values()]
+
+    def forward(self, x, attn):
+        c = self.cfg
+        B, N, _ = x.shape
+        for L in self.layers:
+            qkv = torch.nn.functional.linear(_rms(x), L["qkv"])
+            q, k, v = qkv.split([c["hq"] * c["d"], c["hkv"] * c["d"], c["hkv"] * c["d"]], dim=-1)
+            q = _rms(q.view(B, N, c["hq"], c["d"])).transpose(1, 2).contiguous()  # QK-norm over d
+            k = _rms(k.view(B, N, c["hkv"], c["d"])).transpose(1, 2).contiguous()
+            v = v.view(B, N, c["hkv"], c["d"]).transpose(1, 2).contiguous()
+            o = attn(q, k, v).transpose(1, 2).reshape(B, N, c["hq"] * c["d"])
+            x = x + torch.nn.functional.linear(o, L["o"])
+            hmid = _rms(x)
+            mlp = torch.nn.functional.silu(torch.nn.functional.linear(hmid, L["gate"])) * \
+                torch.nn.functional.linear(hmid, L["up"])
+            x = x + torch.nn.functional.linear(mlp, L["down"])
+        return x
+
+
+def time_layer_stack(n_tokens: int, steps: int, warmup: int, dev):
+    """Forward + backward of a Llama-1B-shaped layer stack (random weights, batch 1) with the
+    attention from this library against PyTorch's BF16 SDPA; everything else identical (cuBLAS
+    GEMMs through torch).  The pages' end-to-end claim is about this kind of step (Llama 1B at
+    8K/16K tokens per step, 2.1 s -> 1.9 s per iteration on an RTX4090)."""
+    cfg = LLAMA_1B
+    stack = _LlamaShapedStack(cfg, dev)
+    g = torch.Generator(device="cpu").manual_seed(1)
+    x0 = torch.randn(1, n_tokens, cfg["hidden"], generator=g).to(torch.bfloat16).to(dev)
+    gy = torch.randn(1, n_tokens, cfg["hidden"], generator=g).to(torch.bfloat16).to(dev)
+    attns = {
+        "sagebwd": lambda q, k, v: sb.attention(q, k, v, causal=True),
+        "torch_sdpa_bf16": lambda q, k, v: torch.nn.functional.scaled_dot_product_attention(
+            q, k, v, is_causal=True, enable_gqa=True),
+    }
+    out = {}
+    for name, attn in attns.items():
+        def one():
+            x = x0.detach().requires_grad_(True)
+            stack.forward(x, attn).backward(gy)
+            for t in stack.params():
+                t.grad = None
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record()
+            one()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        out[name + "_ms"] = round(statistics.median(e[0].elapsed_time(e[1]) for e in ev), 3)
+    out["speedup"] = round(out["torch_sdpa_bf16_ms"] / out["sagebwd_ms"], 4)
+    out["workload"] = (f"Llama-3.2-1B-shaped stack: {cfg['layers']} layers, hidden {cfg['hidden']}, "
+                       f"{cfg['hq']}/{cfg['hkv']} heads, d {cfg['d']}, SwiGLU {cfg['inter']}, QK-norm, no RoPE, "
+                       f"batch 1, {n_tokens} tokens, causal, BF16, random weights; forward + backward, no optimizer")
+    return out
+
+
 # ---------------------------------------------------------------------------- the oracle (CPU) arm
 def oracle_sample_run(w: W.Workload, n_tokens: int):
     """Time the oracle on the first n_tokens tokens of the workload's own inputs (all heads, full
@@ -367,6 +450,9 @@ def main():
                     help="also time PyTorch's BF16 SDPA forward + backward on the same inputs (context)")
     ap.add_argument("--balance-qk", action="store_true",
                     help="time the library's optional Q/K channel balancing (the other setting is reported beside)")
+    ap.add_argument("--layer-step", type=int, default=0, metavar="TOKENS",
+                    help="also time a Llama-1B-shaped 16-layer stack forward + backward at TOKENS tokens with this "
+                         "library's attention and with torch SDPA (context; not the headline)")
     ap.add_argument("--seq", type=int, default=0,
                     help="profiling only: override the workload's sequence length (the line then names it)")
     args = ap.parse_args()
@@ -456,6 +542,8 @@ def main():
             line["other_balance_setting"] = other_balance_setting(step, args, dev, flush)
         if args.compare_sdpa:
             line["torch_sdpa_bf16"] = time_torch_sdpa(step, max(5, args.steps // 2), args.warmup, flush)
+        if args.layer_step > 0:
+            line["layer_step"] = time_layer_stack(args.layer_step, max(3, args.steps // 5), 2, dev)
         line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if dist is not None:
