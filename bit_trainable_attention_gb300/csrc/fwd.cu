@@ -35,8 +35,16 @@ namespace sagebwd {
 namespace {
 
 constexpr int kFThreads = 384;
-constexpr uint32_t kFRegsLaunch = 168, kFRegsLow = 40, kFRegsHigh = 232;
-static_assert(128 * kFRegsLow + 256 * kFRegsHigh <= kFThreads * kFRegsLaunch, "register split exceeds the launch");
+constexpr uint32_t kFRegsLaunch = 168;
+// registers per thread after setmaxnreg: control warps (producer, MMA) and softmax
+// warpgroups.  Measured: 40 / 232 made the control warps spill (forward 0.846 ms on the
+// long-context workload), 56 / 224 does not (0.825 ms); on d = 64, 88 / 208 (0.478 ms
+// against 0.496 ms at 40 / 232 on the 8K-token GQA workload).
+template <int D>
+struct FwdRegs {
+  static constexpr uint32_t LOW = D == 128 ? 56 : 88, HIGH = D == 128 ? 224 : 208;
+  static_assert(128 * LOW + 256 * HIGH <= kFThreads * kFRegsLaunch, "register split exceeds the launch");
+};
 
 template <int D>
 struct FwdCfg {
@@ -123,7 +131,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
   if (warp >= 8) {
-    setmaxnreg_dec<kFRegsLow>();
+    setmaxnreg_dec<FwdRegs<D>::LOW>();
     if (warp == 8 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       int k_issued[NS], v_issued[NS];
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       drain(bar_final, 0, p.timeout_ns);
     }
   } else {
-    setmaxnreg_inc<kFRegsHigh>();
+    setmaxnreg_inc<FwdRegs<D>::HIGH>();
     // ------------------------------------------------------------ softmax / correction
     const int t = warp >> 2;  // query tile of this warpgroup
     const int r = tid & 127;  // query row within the tile == TMEM lane
