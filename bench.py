@@ -43,8 +43,8 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # the one-pass ncu capture summarised in profiles/bwd_kernel_qwen15b_ncu.md.  The
 # figure belongs to the kernel sources it was taken from: once any of them changes
 # the line reports null until the capture is repeated.
-BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1.33e9 + 517.12e6,
-               "sources_sha256": "86b2fbb1418765703ecb71377f317d4d35e9381067a73f58d0a18fd0c83da044"}
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1328772096 + 516808448,
+               "sources_sha256": "aaee5a9a3b1d3c23415565f3e9c99c137c97a0a68bc4f88e6190eac52fb0ce35"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
