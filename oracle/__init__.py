@@ -32,6 +32,7 @@ class OracleProblem(ctypes.Structure):
         ("N", ctypes.c_int32), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
         ("smooth_k", ctypes.c_int32), ("balance_qk", ctypes.c_int32), ("exact_codes", ctypes.c_int32),
         ("threads", ctypes.c_int32), ("exact_mask", ctypes.c_uint32), ("int8_dp", ctypes.c_int32),
+        ("ds_subexp", ctypes.c_int32),
         ("softmax_scale", ctypes.c_double),
     ]
 
@@ -88,9 +89,9 @@ def _bf16_bits(x) -> np.ndarray:
 
 
 def problem(B, Hq, Hkv, N, d, causal, smooth_k=True, exact_codes=False, softmax_scale=0.0, threads=0, exact_mask=0,
-            balance_qk=False, int8_dp=False):
+            balance_qk=False, int8_dp=False, ds_subexp=False):
     return OracleProblem(B, Hq, Hkv, N, d, int(causal), int(smooth_k), int(balance_qk), int(exact_codes),
-                         int(threads), int(exact_mask), int(int8_dp), float(softmax_scale))
+                         int(threads), int(exact_mask), int(int8_dp), int(ds_subexp), float(softmax_scale))
 
 
 def nblocks(N: int) -> int:
@@ -250,7 +251,7 @@ def bwd_tile(p: OracleProblem, q, k, v, o, dO, lse, b: int, h: int, ib: int, jb:
     lse = np.ascontiguousarray(lse, dtype=np.float64)
     pt = np.zeros((BLK, BLK), np.int32)
     spc = np.zeros(BLK, np.float64)
-    ds = np.zeros((BLK, BLK), np.int32)
+    ds = np.zeros((BLK, BLK), np.float64)  # integer codes; with ds_subexp code * 2^-k
     sds = np.zeros(1, np.float64)
     rc = _load().oracle_bwd_tile(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), b, h, ib,
                                  jb, _ptr(pt), _ptr(spc), _ptr(ds), _ptr(sds))

@@ -36,6 +36,10 @@
 //    sums to zero, so the mean's gradient vanishes);
 //  * ablation int8_dp (off by default): dP = dO V^T from the INT8 codes of dO
 //    and V, the variant the pages' ablation rejects;
+//  * optional dS sub-scales (ds_subexp, off by default; the library's own
+//    finer dS granularity): a power-of-two refinement per key and 32-query
+//    group inside each tile, baked into the BF16 operand values (see
+//    ds_subexp_of);
 //  * optional channel balancing (balance_qk, off by default; the library's
 //    own addition, after SmoothQuant, listed under "Builds on" of the SageBwd
 //    page): per (batch, kv head, channel) an exponent e moves magnitude
@@ -70,6 +74,7 @@ typedef struct {
   uint32_t exact_mask;  // error attribution: bit set = that quantizer keeps its scale but skips rint/clamp
                         // (bit 0 Q, 1 K, 2 V, 3 dO, 4 P~ forward, 5 P^T backward, 6 dS); FP32 rounding stays
   int32_t int8_dp;      // ablation: dP = dO V^T from the INT8 codes of dO and V instead of BF16 operands
+  int32_t ds_subexp;    // 1: dS codes carry a power-of-two sub-scale per (key, 32-query group) of a tile
   double softmax_scale;  // <= 0: 1/sqrt(d)
 } oracle_problem;
 }
@@ -362,6 +367,26 @@ struct BwdTile {
   double sds = 0;                       // scale of the dS tile
 };
 
+// dS sub-scales (the library's reading, ds_subexp): the tile's codes keep the
+// one FP32 scale max|dS| / 127, and each key's codes within a group of
+// kSubGroup consecutive queries of the tile are refined by 2^k, k = the
+// largest integer <= log2(tile max / group max), at most kSubMax, 0 when the
+// group max is below 2^-100: code = rint(dS * inv * 2^k), value = code * 2^-k
+// (exact in BF16: a 7-bit integer times a power of two).  Both products that
+// read dS (dK = dS^T Q, dQ = dS K) use these values, so the sub-scale needs no
+// dequantization step of its own.
+constexpr int kSubGroup = 32, kSubMax = 8;
+int ds_subexp_of(const std::vector<double>& dS, int ni, int a0, int c, double amax) {
+  double g = 0;
+  for (int a = a0; a < std::min(ni, a0 + kSubGroup); ++a) g = std::max(g, std::fabs(dS[(size_t)a * BLK + c]));
+  if (g < std::ldexp(1.0, -100)) return 0;
+  // floor(log2(amax / g)) from the binary exponents and fractions (exact)
+  int ea = 0, eg = 0;
+  const double fa = std::frexp(amax, &ea), fg = std::frexp(g, &eg);
+  const int k = ea - eg - (fa < fg ? 1 : 0);
+  return std::min(kSubMax, std::max(0, k));
+}
+
 void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const QTensor& kq, const uint16_t* v,
               const uint16_t* dO, const double* o, const double* lse, int b, int h, int ib, int jb, double c0,
               double l2e, BwdTile& T, const QTensor* doq = nullptr, const QTensor* vq = nullptr) {
@@ -412,7 +437,8 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
     T.spc[c] = M.F(cmax / 127.0);
     for (int a = 0; a < T.ni; ++a) T.pt[(size_t)c * BLK + a] = M.Q(QZ_PB, M.F(P[(size_t)a * BLK + c] * inv));
   }
-  // dS quantized with one scale for the whole tile.
+  // dS quantized with one scale for the whole tile (and, with ds_subexp, a
+  // power-of-two sub-scale per key and group of 32 queries).
   T.ds.assign((size_t)BLK * BLK, 0);
   double amax = 0;
   for (int a = 0; a < T.ni; ++a)
@@ -422,7 +448,16 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
     const double inv = M.F(127.0 / amax);
     T.sds = M.F(amax / 127.0);
     for (int a = 0; a < T.ni; ++a)
-      for (int c = 0; c < T.nk; ++c) T.ds[(size_t)a * BLK + c] = M.Q(QZ_DS, M.F(dS[(size_t)a * BLK + c] * inv));
+      for (int c = 0; c < T.nk; ++c) {
+        const double x = M.F(dS[(size_t)a * BLK + c] * inv);
+        if (!p->ds_subexp) {
+          T.ds[(size_t)a * BLK + c] = M.Q(QZ_DS, x);
+        } else {
+          const int k = ds_subexp_of(dS, T.ni, a / kSubGroup * kSubGroup, c, amax);
+          const double f = std::ldexp(1.0, k);
+          T.ds[(size_t)a * BLK + c] = M.Q(QZ_DS, x * f) / f;  // a code times 2^-k
+        }
+      }
   }
 }
 
@@ -739,11 +774,12 @@ int oracle_fwd_tile(const oracle_problem* p, const uint16_t* q, const uint16_t* 
 }
 
 // Everything the quantized backward of one tile consumes: pt [128][128] codes
-// of P^T (row = key), spc [128] their per-key scales, ds [128][128] codes of dS
-// (row = query), *sds the tile's dS scale.  o, lse: the forward's outputs.
+// of P^T (row = key), spc [128] their per-key scales, ds [128][128] the dS
+// operand values (row = query): integer codes, or code * 2^-k with ds_subexp,
+// *sds the tile's dS scale.  o, lse: the forward's outputs.
 int oracle_bwd_tile(const oracle_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v, const double* o,
                     const uint16_t* dO, const double* lse, int b, int h, int ib, int jb, int32_t* pt, double* spc,
-                    int32_t* ds, double* sds) {
+                    double* ds, double* sds) {
   if (oracle_check_problem(p) || p->exact_codes) return 1;
   set_threads(p);
   const Mode M = mode_of(p);
@@ -753,7 +789,7 @@ int oracle_bwd_tile(const oracle_problem* p, const uint16_t* q, const uint16_t* 
   bwd_tile(M, p, qq, kq, v, dO, o, lse, b, h, ib, jb, M.F(scale_of(p) * kLog2e), M.F(kLog2e), T);
   for (size_t e = 0; e < T.pt.size(); ++e) pt[e] = (int32_t)T.pt[e];
   std::copy(T.spc.begin(), T.spc.end(), spc);
-  for (size_t e = 0; e < T.ds.size(); ++e) ds[e] = (int32_t)T.ds[e];
+  std::copy(T.ds.begin(), T.ds.end(), ds);  // integer codes; with ds_subexp code * 2^-k
   *sds = T.sds;
   return 0;
 }

@@ -1,0 +1,99 @@
+"""Pins of the oracle's optional dS sub-scales (ds_subexp; CPU only).
+
+The dS codes of a 128 x 128 backward tile share one FP32 scale max|dS| / 127
+(the library's default reading).  With ds_subexp each key's codes within a
+group of 32 consecutive queries of the tile are refined by a power of two
+2^k, k = floor(log2(tile max / group max)) clamped to [0, 8]: the operand value
+is code * 2^-k, exact in BF16, so dK = dS^T Q and dQ = dS K consume it with no
+separate dequantization.  "SageBwd: A Trainable Low-bit Attention" (Abstract,
+finding (ii)) names dS as the main source of quantization error; this is the
+library's finer granularity for it.
+
+* tile properties: every group's values are integers times 2^-k with the
+  largest integer in [64, 127] (or k = 8), the group holding the tile
+  maximum has k = 0 and code 127, the tile scale is unchanged, and each value
+  lies within one code step of the per-tile code;
+* the unrounded pipeline with sub-scales is exact attention;
+* dQ and dK get at least 2.5 times closer to exact attention (1 - CosSim) on
+  the synthetic workloads, while O and dV, which do not read dS, are unchanged.
+"""
+import numpy as np
+import pytest
+
+from bit_trainable_attention_gb300 import workloads as W
+
+GROUP, KMAX = 32, 8
+
+
+def cos(a, b):
+    a = np.nan_to_num(np.asarray(a, np.float64)).ravel()
+    b = np.nan_to_num(np.asarray(b, np.float64)).ravel()
+    return float(a @ b / np.linalg.norm(a) / np.linalg.norm(b))
+
+
+def group_exponent(vals):
+    """The k in [0, 8] for which every value times 2^k is an integer and the largest
+    magnitude is in [64, 127] (or k = 8 with magnitudes <= 127); None if there is none."""
+    for k in range(KMAX + 1):
+        c = vals * 2.0 ** k
+        if not np.all(c == np.round(c)):
+            continue
+        m = np.abs(c).max()
+        if 64 <= m <= 127 or (k == KMAX and m <= 127):
+            return k
+    return None
+
+
+def test_tile_properties(oracle_mod):
+    w = W.WORKLOADS["llama1b"].with_(Hq=2, Hkv=1, N=300)
+    x = W.make_inputs(w)
+    p0 = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+    ps = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, ds_subexp=True)
+    r = oracle_mod.pipeline(p0, x["q"], x["k"], x["v"], x["do"])
+    o_in = oracle_mod.bf16_round(r["o"])
+    seen_k = set()
+    for ib, jb in ((0, 0), (1, 0), (2, 1), (2, 2)):
+        pt0, _, ds0, sds0 = oracle_mod.bwd_tile(p0, x["q"], x["k"], x["v"], o_in, x["do"], r["lse"], 0, 1, ib, jb)
+        pts, _, dss, sdss = oracle_mod.bwd_tile(ps, x["q"], x["k"], x["v"], o_in, x["do"], r["lse"], 0, 1, ib, jb)
+        assert sdss == sds0 and np.array_equal(pts, pt0)  # the tile scale and the P^T codes are untouched
+        assert np.abs(dss).max() == 127  # the group holding the tile maximum: k = 0, code 127
+        assert np.all(np.abs(dss - ds0) <= 1.0)  # within one code step of the per-tile code
+        for key in range(128):
+            for g0 in range(0, 128, GROUP):
+                vals = dss[g0:g0 + GROUP, key]
+                if not np.any(vals):
+                    continue
+                k = group_exponent(vals)
+                assert k is not None, (ib, jb, key, g0, vals)
+                seen_k.add(k)
+    assert len(seen_k) >= 3  # the refinement is exercised, not only k = 0
+
+
+@pytest.mark.parametrize("w", [W.small("gqa_causal_ragged", 1, 4, 2, 300, 32, True, 21, k_offset_sd=2.0),
+                               W.small("mha_noncausal", 1, 2, 2, 200, 64, False, 22, qk_norm=True)],
+                         ids=lambda w: w.name)
+def test_unrounded_pipeline_with_subscales_is_exact_attention(oracle_mod, w):
+    x = W.make_inputs(w)
+    pe = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, exact_codes=True, ds_subexp=True)
+    r = oracle_mod.pipeline(pe, x["q"], x["k"], x["v"], x["do"])
+    ref = oracle_mod.pipeline(pe, x["q"], x["k"], x["v"], x["do"], exact=True)
+    for key in ("o", "dq", "dk", "dv"):
+        np.testing.assert_allclose(r[key], ref[key], rtol=0, atol=1e-10 * np.abs(ref[key]).max(), err_msg=key)
+
+
+@pytest.mark.parametrize("w", [W.WORKLOADS["llama1b"].with_(Hq=8, Hkv=2, N=384),
+                               W.WORKLOADS["pretrain"].with_(B=1, Hq=4, Hkv=4, N=512),
+                               W.WORKLOADS["videodit"].with_(B=1, Hq=2, Hkv=2, N=300)],
+                         ids=lambda w: w.name)
+def test_subscales_cut_the_ds_error(oracle_mod, w):
+    x = W.make_inputs(w)
+    p0 = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+    ps = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, ds_subexp=True)
+    ex = oracle_mod.pipeline(p0, x["q"], x["k"], x["v"], x["do"], exact=True)
+    r0 = oracle_mod.pipeline(p0, x["q"], x["k"], x["v"], x["do"])
+    rs = oracle_mod.pipeline(ps, x["q"], x["k"], x["v"], x["do"])
+    for key in ("dq", "dk"):
+        e0, es = 1 - cos(r0[key], ex[key]), 1 - cos(rs[key], ex[key])
+        assert es * 2.5 < e0, (key, e0, es)
+    for key in ("o", "lse", "dv"):
+        np.testing.assert_array_equal(rs[key], r0[key], err_msg=key)
