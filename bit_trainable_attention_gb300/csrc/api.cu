@@ -321,7 +321,7 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
   bp.status = at<int>(ws, W.status);
   bp.timeout_ns = timeout_of(p);
   bp.flags = p->flags;
-  return cuda_status(launch_bwd(tq, tk, tv, tdo, tdoq, tdq, bp, p->d, p->causal, st));
+  return cuda_status(launch_bwd(tq, tk, tv, tdo, tdoq, tdq, bp, p->d, p->causal, p->ds_subexp ? 1 : 0, st));
 }
 
 sagebwd_status bwd_finish_impl(const sagebwd_problem* p, const void* saved, void* dq, void* dk, void* dv, void* ws,

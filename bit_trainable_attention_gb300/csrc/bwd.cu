@@ -52,6 +52,7 @@ namespace {
 
 constexpr int kBThreads = 640;
 constexpr uint32_t kBRegsLaunch = 96;
+constexpr int kDSubMax = 8;  // largest dS sub-scale exponent
 
 template <int D>
 struct BwdCfg {
@@ -95,7 +96,7 @@ enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty,
                bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAccV, bSiteAccQ, bSiteAccK, bSiteTmemFreeV, bSiteDVQFree,
                bSiteTmemFreeK, bSiteStaged, bSiteStgFree, bSiteC1, bSiteC2, bSiteC3, bSiteAlign };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DSX>
 __global__ void __launch_bounds__(kBThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -403,7 +404,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
       tc_fence_after();
       // pass 1: P = 2^(S sQ sK scale log2e - LSE log2e), dS = P (dP - D), written back in
       // place; the next chunk's TMEM loads are in flight while a chunk is computed
-      float pmax = 0.f, amax = 0.f;
+      // amax: |dS| maximum of this thread's first 32 queries, amax_hi: of its last 32 (the
+      // two sub-scale groups; without sub-scales one maximum covers all 64)
+      float pmax = 0.f, amax = 0.f, amax_hi = 0.f;
       {
         uint32_t sv[2][8], dpv[2][8];
         tmem_ld8(s_addr, sv[0]);
@@ -437,7 +440,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
               const float2 ds = fmul2(
                   pr, fadd2(make_float2(__uint_as_float(dpv[cur][e]), __uint_as_float(dpv[cur][e + 1])), nd));
               pmax = fmax3(pmax, pr.x, pr.y);
-              amax = fmax3(amax, fabsf(ds.x), fabsf(ds.y));
+              if (DSX && c >= 4)
+                amax_hi = fmax3(amax_hi, fabsf(ds.x), fabsf(ds.y));
+              else
+                amax = fmax3(amax, fabsf(ds.x), fabsf(ds.y));
               sv[cur][e] = __float_as_uint(pr.x);
               sv[cur][e + 1] = __float_as_uint(pr.y);
               dpv[cur][e] = __float_as_uint(ds.x);
@@ -451,6 +457,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
       tmem_st_wait();
       // tile maximum of |dS| over the 8 softmax warps; row maximum of P over the two halves:
       // half 0 publishes its maximum, half 1 combines and publishes the row's
+      const float amax_lo = amax;
+      if (DSX) amax = fmaxf(amax, amax_hi);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (lane == 0) am[warp] = amax;
@@ -475,6 +483,22 @@ __global__ void __launch_bounds__(kBThreads, 1)
       const float sPc = p_live ? pmax * (1.f / 127.f) : 0.f;
       const float invA = d_live ? __fdividef(127.f, a) : 0.f;
       const float sDS = d_live ? a * (1.f / 127.f) : 0.f;
+      // dS sub-scales: group g of this thread's key gets k = floor(log2(a / max_g)) in
+      // [0, 8] (0 below 2^-100), from the binary exponents and fractions; its operand values
+      // are rint(dS * invA * 2^k) * 2^-k (a code times 2^-k, exact in BF16).  Adding and
+      // subtracting 1.5 * 2^(23-k), whose unit in the last place is 2^-k, rounds to that
+      // grid directly (ties to even), so the sub-scale costs no instruction per element.
+      float magic_lo = 12582912.0f, magic_hi = 12582912.0f;
+      if (DSX) {
+        auto subexp = [&](float g) -> int {
+          if (!(g >= 0x1p-100f)) return 0;
+          const uint32_t ua = __float_as_uint(a), ug = __float_as_uint(g);
+          const int k = (int)(ua >> 23) - (int)(ug >> 23) - ((ua & 0x7FFFFFu) < (ug & 0x7FFFFFu) ? 1 : 0);
+          return min(k, kDSubMax);
+        };
+        magic_lo = __int_as_float(((127 + 23 - subexp(amax_lo)) << 23) | 0x400000);
+        magic_hi = __int_as_float(((127 + 23 - subexp(amax_hi)) << 23) | 0x400000);
+      }
       if (ws == 0) fv_ring[(it & 1) * 128 + r] = __fmul_rn(sPc, sdOt);
       if (tid == 0) sds_ring[it & 1] = sDS;
       // pass 2a: codes of P^T (row scale), 32 queries -> 16 packed columns, over the previous
@@ -513,17 +537,19 @@ __global__ void __launch_bounds__(kBThreads, 1)
                                 : waitw(wc, bar_acc_q, (it - 1) & 1, bSiteAccQ)))
         break;
       {
-        const float2 invA2 = make_float2(invA, invA);
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
+          const float2 invA2 = make_float2(invA, invA);
+          const float mg = c0 == 0 ? magic_lo : magic_hi;
+          const float2 magic2 = make_float2(mg, mg), neg_magic2 = make_float2(-mg, -mg);
           uint32_t v[32];
           tmem_ld32(dp_addr + c0, v);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float2 cd = fadd2(
-                fadd2(fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invA2), kMagic2),
-                kNegMagic2);
+                fadd2(fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invA2), magic2),
+                neg_magic2);
             v[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
           }
 #pragma unroll
@@ -642,11 +668,11 @@ __global__ void __launch_bounds__(kBThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DSX>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                          const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s) {
   using C = BwdCfg<D>;
-  auto kern = bwd_kernel<D, CAUSAL>;
+  auto kern = bwd_kernel<D, CAUSAL, DSX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = p.nb * p.B * p.Hkv * (p.G / p.HS);
@@ -658,12 +684,17 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, int d, int causal,
-                       cudaStream_t s) {
-  if (d == 64)
-    return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdoq, tdq, p, s)
-                  : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdoq, tdq, p, s);
-  return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdoq, tdq, p, s)
-                : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdoq, tdq, p, s);
+                       int ds_subexp, cudaStream_t s) {
+#define SAGEBWD_BWD_CASE(D_, C_)                                                                  \
+  if (d == D_ && (causal != 0) == C_)                                                             \
+    return ds_subexp ? launch_bwd_t<D_, C_, true>(tq, tk, tv, tdo, tdoq, tdq, p, s)              \
+                     : launch_bwd_t<D_, C_, false>(tq, tk, tv, tdo, tdoq, tdq, p, s);
+  SAGEBWD_BWD_CASE(64, true)
+  SAGEBWD_BWD_CASE(64, false)
+  SAGEBWD_BWD_CASE(128, true)
+  SAGEBWD_BWD_CASE(128, false)
+#undef SAGEBWD_BWD_CASE
+  return cudaErrorInvalidValue;
 }
 
 // Longest-processing-time list schedule of the backward CTAs (one per key block,

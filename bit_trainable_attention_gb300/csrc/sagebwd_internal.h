@@ -124,6 +124,7 @@ struct BwdParams {
 };
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, int d, int causal,
+                       int ds_subexp,
                        cudaStream_t s);
 // Query heads per backward CTA: the divisor of G whose CTAs, dispatched longest
 // first onto `sms` multiprocessors, finish soonest (ties: more heads per CTA).

@@ -28,6 +28,13 @@
  * the block quantizers, which leaves Q K^T unchanged exactly and evens out
  * channel outliers between the two operands; dQ is multiplied by 2^-e and
  * dK by 2^e when they are converted to BF16.
+ * Optional dS sub-scales (ds_subexp = 1; off by default, this library's finer
+ * dS granularity): the tile keeps its scale max|dS| / 127, and each key's codes
+ * within a group of 32 queries of the tile are refined by 2^k,
+ * k = clamp(floor(log2(tile max / group max)), 0, 8) (0 if the group max is
+ * below 2^-100): code = rint(dS * 127/max * 2^k), operand value code * 2^-k,
+ * exact in BF16, read as is by dK = dS^T Q and dQ = dS K (their FP32 sums are
+ * then no longer exact integers, but rounding there is at the 2^-24 level).
  * The INT8 codes are held as integer-valued BF16 and multiplied on the
  * tensor cores with FP32 accumulation, which is exact for these tiles
  * (|sum| <= 128 * 127^2 < 2^24).
@@ -79,6 +86,7 @@ typedef struct {
   int32_t causal;       /* 1: key k visible to query i iff k <= i (top-left aligned); 0: all keys */
   int32_t smooth_k;     /* 1: subtract the per-channel mean of K over tokens before quantizing (the method) */
   int32_t balance_qk;   /* 1: power-of-two Q/K channel balancing before quantizing (see above); 0 in the method */
+  int32_t ds_subexp;    /* 1: dS sub-scales per key and 32-query group (see above); 0: one dS scale per tile */
   uint32_t flags;       /* SAGEBWD_FLAG_* (0 in normal use) */
   float softmax_scale;  /* <= 0 selects 1/sqrt(d) */
   uint32_t wait_timeout_ms; /* bound of every in-kernel wait; 0 selects 2000 ms */
