@@ -32,7 +32,7 @@ class OracleProblem(ctypes.Structure):
         ("N", ctypes.c_int32), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
         ("smooth_k", ctypes.c_int32), ("balance_qk", ctypes.c_int32), ("exact_codes", ctypes.c_int32),
         ("threads", ctypes.c_int32), ("exact_mask", ctypes.c_uint32), ("int8_dp", ctypes.c_int32),
-        ("ds_subexp", ctypes.c_int32),
+        ("ds_subexp", ctypes.c_int32), ("qk_subexp", ctypes.c_int32),
         ("softmax_scale", ctypes.c_double),
     ]
 
@@ -89,9 +89,10 @@ def _bf16_bits(x) -> np.ndarray:
 
 
 def problem(B, Hq, Hkv, N, d, causal, smooth_k=True, exact_codes=False, softmax_scale=0.0, threads=0, exact_mask=0,
-            balance_qk=False, int8_dp=False, ds_subexp=False):
+            balance_qk=False, int8_dp=False, ds_subexp=False, qk_subexp=False):
     return OracleProblem(B, Hq, Hkv, N, d, int(causal), int(smooth_k), int(balance_qk), int(exact_codes),
-                         int(threads), int(exact_mask), int(int8_dp), int(ds_subexp), float(softmax_scale))
+                         int(threads), int(exact_mask), int(int8_dp), int(ds_subexp), int(qk_subexp),
+                         float(softmax_scale))
 
 
 def nblocks(N: int) -> int:
@@ -125,13 +126,13 @@ def quantize_exact(p: OracleProblem, x, BH: int, smooth: bool):
 def quantize_qk(p: OracleProblem, q, k):
     """Q and K as the forward quantizes them (K-smoothing and channel balancing as p selects).
 
-    Returns dict: q / k int8 codes [B*H, N, d], sq / sk FP32 block scales [B*H, nb], mu FP32 K channel
+    Returns dict: q / k operand values as float32 [B*H, N, d] (integer codes; code * 2^-k with qk_subexp), sq / sk FP32 block scales [B*H, nb], mu FP32 K channel
     means [B*Hkv, d] (zeros without smoothing), e int32 balancing exponents [B*Hkv, d] (zeros unless
     balance_qk)."""
     q, k = _bf16_bits(q), _bf16_bits(k)
     BHq, BHk, nb = p.B * p.Hq, p.B * p.Hkv, nblocks(p.N)
-    out = {"q": np.zeros((BHq, p.N, p.d), np.int8), "sq": np.zeros((BHq, nb), np.float32),
-           "k": np.zeros((BHk, p.N, p.d), np.int8), "sk": np.zeros((BHk, nb), np.float32),
+    out = {"q": np.zeros((BHq, p.N, p.d), np.float32), "sq": np.zeros((BHq, nb), np.float32),
+           "k": np.zeros((BHk, p.N, p.d), np.float32), "sk": np.zeros((BHk, nb), np.float32),
            "mu": np.zeros((BHk, p.d), np.float32), "e": np.zeros((BHk, p.d), np.int32)}
     rc = _load().oracle_quantize_qk(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(out["q"]), _ptr(out["sq"]),
                                     _ptr(out["k"]), _ptr(out["sk"]), _ptr(out["mu"]), _ptr(out["e"]))

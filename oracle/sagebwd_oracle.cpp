@@ -36,6 +36,9 @@
 //    sums to zero, so the mean's gradient vanishes);
 //  * ablation int8_dp (off by default): dP = dO V^T from the INT8 codes of dO
 //    and V, the variant the pages' ablation rejects;
+//  * optional Q/K sub-scales (qk_subexp, off by default; the library's own
+//    finer Q/K granularity): a power-of-two refinement per 8-channel group of
+//    each 128-token block (see quant_block);
 //  * optional dS sub-scales (ds_subexp, off by default; the library's own
 //    finer dS granularity): a power-of-two refinement per key and 32-query
 //    group inside each tile, baked into the BF16 operand values (see
@@ -75,6 +78,7 @@ typedef struct {
                         // (bit 0 Q, 1 K, 2 V, 3 dO, 4 P~ forward, 5 P^T backward, 6 dS); FP32 rounding stays
   int32_t int8_dp;      // ablation: dP = dO V^T from the INT8 codes of dO and V instead of BF16 operands
   int32_t ds_subexp;    // 1: dS codes carry a power-of-two sub-scale per (key, 32-query group) of a tile
+  int32_t qk_subexp;    // 1: Q and K codes carry a power-of-two sub-scale per (block, 8-channel group)
   double softmax_scale;  // <= 0: 1/sqrt(d)
 } oracle_problem;
 }
@@ -140,9 +144,28 @@ struct QTensor {
   double s(int bh, int blk) const { return scale[(size_t)bh * nblocks(N) + blk]; }
 };
 
+// Power-of-two sub-scale exponent of a group inside a quantization group
+// (the library's reading for the optional sub-scales): the largest integer k
+// <= log2(amax / gmax), clamped to [0, kSubMax], and 0 when gmax is below
+// 2^-100; from the binary exponents and fractions, so exact.
+constexpr int kSubMax = 8;
+int subexp_of(double amax, double gmax) {
+  if (gmax < std::ldexp(1.0, -100)) return 0;
+  int ea = 0, eg = 0;
+  const double fa = std::frexp(amax, &ea), fg = std::frexp(gmax, &eg);
+  const int k = ea - eg - (fa < fg ? 1 : 0);
+  return std::min(kSubMax, std::max(0, k));
+}
+
 // Per-block absmax quantizer (the build's reading: 128 tokens x d channels,
-// symmetric, scale a/127, round to nearest even, clamp to +-127).
-void quant_block(const Mode& M, int which, const double* x, int count, double* codes, double* scale) {
+// symmetric, scale a/127, round to nearest even, clamp to +-127).  With
+// subexp (Q and K under qk_subexp) each group of 8 channels of the block
+// (all its rows) is refined by 2^k, k = subexp_of(block max, group max): the
+// value is code * 2^-k with code = rint(x * inv * 2^k), exact in BF16, and
+// the block scale a/127 dequantizes it as before.
+constexpr int kChanGroup = 8;
+void quant_block(const Mode& M, int which, const double* x, int count, double* codes, double* scale, int d = 0,
+                 bool subexp = false) {
   double a = 0;
   for (int e = 0; e < count; ++e) a = std::max(a, std::fabs(x[e]));
   if (a < kMinGroupMax) {
@@ -152,7 +175,22 @@ void quant_block(const Mode& M, int which, const double* x, int count, double* c
   }
   const double inv = M.F(127.0 / a);
   *scale = M.F(a / 127.0);
-  for (int e = 0; e < count; ++e) codes[e] = M.Q(which, M.F(x[e] * inv));
+  if (!subexp) {
+    for (int e = 0; e < count; ++e) codes[e] = M.Q(which, M.F(x[e] * inv));
+    return;
+  }
+  const int rows = count / d;
+  for (int c0 = 0; c0 < d; c0 += kChanGroup) {
+    double g = 0;
+    for (int r = 0; r < rows; ++r)
+      for (int c = c0; c < c0 + kChanGroup; ++c) g = std::max(g, std::fabs(x[(size_t)r * d + c]));
+    const double f = std::ldexp(1.0, subexp_of(a, g));
+    for (int r = 0; r < rows; ++r)
+      for (int c = c0; c < c0 + kChanGroup; ++c) {
+        const size_t e = (size_t)r * d + c;
+        codes[e] = M.Q(which, M.F(x[e] * inv) * f) / f;
+      }
+  }
 }
 
 // FP32 channel means of one head's tokens [N][d] ("SageBwd: A Trainable
@@ -172,7 +210,7 @@ void channel_mean(const Mode& M, const uint16_t* xb, int N, int d, double* mu) {
 // (*fac)[(bh / fac_group) * d + ch], rounded to FP32, before the block
 // quantizer sees it (channel balancing).
 void quantize_tensor(const Mode& M, int which, const uint16_t* x, int BH, int N, int d, bool smooth, QTensor& out,
-                     const std::vector<double>* fac = nullptr, int fac_group = 1) {
+                     const std::vector<double>* fac = nullptr, int fac_group = 1, bool subexp = false) {
   out.BH = BH;
   out.N = N;
   out.d = d;
@@ -199,7 +237,8 @@ void quantize_tensor(const Mode& M, int which, const uint16_t* x, int BH, int N,
           if (f) val = M.F(val * f[ch]);
           vals[(size_t)r * d + ch] = val;
         }
-      quant_block(M, which, vals.data(), rows * d, &out.codes[((size_t)bh * N + n0) * d], &out.scale[(size_t)bh * nb + blk]);
+      quant_block(M, which, vals.data(), rows * d, &out.codes[((size_t)bh * N + n0) * d], &out.scale[(size_t)bh * nb + blk],
+                  d, subexp);
     }
   }
 }
@@ -262,8 +301,10 @@ void quantize_qk(const Mode& M, const oracle_problem* p, const uint16_t* q, cons
     f_k[i] = std::ldexp(1.0, e[i]);
   }
   const int G = p->Hq / p->Hkv;
-  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq, p->balance_qk ? &f_q : nullptr, G);
-  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq, p->balance_qk ? &f_k : nullptr, 1);
+  quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq, p->balance_qk ? &f_q : nullptr, G,
+                  p->qk_subexp != 0);
+  quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq, p->balance_qk ? &f_k : nullptr, 1,
+                  p->qk_subexp != 0);
   if (exps) *exps = std::move(e);
   if (fq) *fq = std::move(f_q);
   if (fk) *fk = std::move(f_k);
@@ -375,16 +416,11 @@ struct BwdTile {
 // (exact in BF16: a 7-bit integer times a power of two).  Both products that
 // read dS (dK = dS^T Q, dQ = dS K) use these values, so the sub-scale needs no
 // dequantization step of its own.
-constexpr int kSubGroup = 32, kSubMax = 8;
+constexpr int kSubGroup = 32;
 int ds_subexp_of(const std::vector<double>& dS, int ni, int a0, int c, double amax) {
   double g = 0;
   for (int a = a0; a < std::min(ni, a0 + kSubGroup); ++a) g = std::max(g, std::fabs(dS[(size_t)a * BLK + c]));
-  if (g < std::ldexp(1.0, -100)) return 0;
-  // floor(log2(amax / g)) from the binary exponents and fractions (exact)
-  int ea = 0, eg = 0;
-  const double fa = std::frexp(amax, &ea), fg = std::frexp(g, &eg);
-  const int k = ea - eg - (fa < fg ? 1 : 0);
-  return std::min(kSubMax, std::max(0, k));
+  return subexp_of(amax, g);
 }
 
 void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const QTensor& kq, const uint16_t* v,
@@ -578,20 +614,21 @@ int oracle_quantize_exact(const oracle_problem* p, const uint16_t* x, int BH, in
   return 0;
 }
 
-// Q and K as the forward quantizes them (K-smoothing and channel balancing as
-// the problem selects): int8 codes, FP32 block scales, the FP32 K channel
+// Q and K as the forward quantizes them (K-smoothing, channel balancing and
+// sub-scales as the problem selects): the operand values (integer codes, or
+// code * 2^-k with qk_subexp) as FP32, FP32 block scales, the FP32 K channel
 // means [B*Hkv][d] (smooth_k) and the balancing exponents [B*Hkv][d] (all 0
 // unless balance_qk).  mean and exps may be NULL.
-int oracle_quantize_qk(const oracle_problem* p, const uint16_t* q, const uint16_t* k, int8_t* qc, float* qs,
-                       int8_t* kc, float* ks, float* mean, int32_t* exps) {
+int oracle_quantize_qk(const oracle_problem* p, const uint16_t* q, const uint16_t* k, float* qc, float* qs,
+                       float* kc, float* ks, float* mean, int32_t* exps) {
   if (oracle_check_problem(p)) return 1;
   set_threads(p);
   QTensor qq, kq;
   std::vector<int> e;
   quantize_qk(Mode{true, 0}, p, q, k, qq, kq, &e);
-  for (size_t i = 0; i < qq.codes.size(); ++i) qc[i] = (int8_t)qq.codes[i];
+  for (size_t i = 0; i < qq.codes.size(); ++i) qc[i] = (float)qq.codes[i];
   for (size_t i = 0; i < qq.scale.size(); ++i) qs[i] = (float)qq.scale[i];
-  for (size_t i = 0; i < kq.codes.size(); ++i) kc[i] = (int8_t)kq.codes[i];
+  for (size_t i = 0; i < kq.codes.size(); ++i) kc[i] = (float)kq.codes[i];
   for (size_t i = 0; i < kq.scale.size(); ++i) ks[i] = (float)kq.scale[i];
   if (mean && p->smooth_k)
     for (size_t i = 0; i < kq.mean.size(); ++i) mean[i] = (float)kq.mean[i];

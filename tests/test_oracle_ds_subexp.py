@@ -1,4 +1,4 @@
-"""Pins of the oracle's optional dS sub-scales (ds_subexp; CPU only).
+"""Pins of the oracle's optional power-of-two sub-scales (ds_subexp, qk_subexp; CPU only).
 
 The dS codes of a 128 x 128 backward tile share one FP32 scale max|dS| / 127
 (the library's default reading).  With ds_subexp each key's codes within a
@@ -97,3 +97,69 @@ def test_subscales_cut_the_ds_error(oracle_mod, w):
         assert es * 2.5 < e0, (key, e0, es)
     for key in ("o", "lse", "dv"):
         np.testing.assert_array_equal(rs[key], r0[key], err_msg=key)
+
+
+# ---------------------------------------------------------------------------- Q/K sub-scales (qk_subexp)
+# Each 8-channel group of a 128-token block of Q and of K is refined by 2^k,
+# k = floor(log2(block max / group max)) clamped to [0, 8]; the block scale stays.
+
+CHAN = 8
+
+
+def test_qk_block_properties(oracle_mod):
+    w = W.small("qk_outliers", 1, 4, 2, 300, 64, True, 61, outlier_frac=0.03, k_offset_sd=2.0)
+    x = W.make_inputs(w)
+    p0 = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+    ps = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, qk_subexp=True)
+    r0, rs = oracle_mod.quantize_qk(p0, x["q"], x["k"]), oracle_mod.quantize_qk(ps, x["q"], x["k"])
+    seen_k = set()
+    for t in ("q", "k"):
+        np.testing.assert_array_equal(rs["s" + t], r0["s" + t])  # block scales untouched
+        vals, plain = rs[t].astype(np.float64), r0[t].astype(np.float64)
+        assert np.all(np.abs(vals - plain) <= 1.0)  # within one code step of the per-block code
+        for bh in range(vals.shape[0]):
+            for b0 in range(0, w.N, 128):
+                blk = vals[bh, b0:b0 + 128]
+                if not np.any(blk):
+                    continue
+                assert np.abs(blk).max() == 127  # the group holding the block maximum: k = 0
+                for c0 in range(0, w.d, CHAN):
+                    g = blk[:, c0:c0 + CHAN]
+                    if np.any(g):
+                        k = group_exponent(g.ravel())
+                        assert k is not None, (t, bh, b0, c0)
+                        seen_k.add(k)
+    assert len(seen_k) >= 3 and max(seen_k) >= 3  # outlier channels leave the others refined
+
+
+@pytest.mark.parametrize("kw", [dict(qk_subexp=True), dict(qk_subexp=True, ds_subexp=True, balance_qk=True)],
+                         ids=["qk", "qk_ds_balance"])
+def test_unrounded_pipeline_with_qk_subscales_is_exact_attention(oracle_mod, kw):
+    w = W.small("qk_exact", 1, 4, 2, 300, 32, True, 62, outlier_frac=0.05, k_offset_sd=2.0)
+    x = W.make_inputs(w)
+    pe = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, exact_codes=True, **kw)
+    r = oracle_mod.pipeline(pe, x["q"], x["k"], x["v"], x["do"])
+    ref = oracle_mod.pipeline(pe, x["q"], x["k"], x["v"], x["do"], exact=True)
+    for key in ("o", "dq", "dk", "dv"):
+        np.testing.assert_allclose(r[key], ref[key], rtol=0, atol=1e-10 * np.abs(ref[key]).max(), err_msg=key)
+
+
+def test_refinements_meet_the_criteria_on_channel_outliers(oracle_mod):
+    """The long-context workload's recipe (1% of Q and K channels x20, GQA 6:1, d = 128) at 1024
+    tokens: Q/K sub-scales alone lift every CosSim; with channel balancing and dS sub-scales all
+    four meet the criteria (O >= 0.995, gradients >= 0.99)."""
+    w = W.WORKLOADS["qwen15b"].with_(N=1024)
+    x = W.make_inputs(w)
+    p0 = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+    ex = oracle_mod.pipeline(p0, x["q"], x["k"], x["v"], x["do"], exact=True)
+    res = {}
+    for name, kw in (("plain", {}), ("qk", dict(qk_subexp=True)),
+                     ("all", dict(qk_subexp=True, ds_subexp=True, balance_qk=True))):
+        p = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, **kw)
+        r = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"])
+        res[name] = {k: cos(r[k], ex[k]) for k in ("o", "dq", "dk", "dv")}
+    for k in res["plain"]:
+        assert res["qk"][k] > res["plain"][k], (k, res)
+    assert res["all"]["o"] >= 0.995, res
+    for k in ("dq", "dk", "dv"):
+        assert res["all"][k] >= 0.99, (k, res)
