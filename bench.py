@@ -119,13 +119,13 @@ class ClockSampler:
 class Step:
     """Buffers and the stage-by-stage calls of one forward + backward step."""
 
-    def __init__(self, w: W.Workload, dev, balance_qk=False, ds_subexp=False, inputs=None):
+    def __init__(self, w: W.Workload, dev, balance_qk=False, ds_subexp=False, qk_subexp=False, inputs=None):
         self.w = w
         x = W.make_inputs(w) if inputs is None else inputs
         self.host = x
         self.x = {k: v.to(dev) for k, v in x.items()}
         self.prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, balance_qk=balance_qk,
-                                    ds_subexp=ds_subexp)
+                                    ds_subexp=ds_subexp, qk_subexp=qk_subexp)
         p = self.prob
         self.o = torch.empty_like(self.x["q"])
         self.lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
@@ -228,16 +228,23 @@ def time_device(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_b
     return total, stage
 
 
+OPTIONS = ("balance_qk", "qk_subexp", "ds_subexp")
+
+
 def other_settings(step: Step, args, dev, flush):
     """The same workload with the library's optional quantizer refinements (Q/K channel balancing,
-    dS sub-scales) in the other combinations: shorter timings (reported, not the headline) and
-    their cosine similarities."""
+    Q/K sub-scales, dS sub-scales) in other combinations -- none, each alone, all -- skipping the
+    timed one: shorter timings (reported, not the headline) and their cosine similarities."""
+    mine = tuple(bool(getattr(step.prob, o)) for o in OPTIONS)
+    combos = [(False,) * 3] + [tuple(i == j for j in range(3)) for i in range(3)] + [(True,) * 3]
     out = []
-    b0, d0 = bool(step.prob.balance_qk), bool(step.prob.ds_subexp)
-    for bal, dsx in ((not b0, d0), (b0, not d0), (not b0, not d0)):
-        other = Step(step.w, dev, balance_qk=bal, ds_subexp=dsx, inputs=step.host)
+    for combo in combos:
+        if combo == mine:
+            continue
+        kw = dict(zip(OPTIONS, combo))
+        other = Step(step.w, dev, inputs=step.host, **kw)
         total, stage = time_device(other, max(5, args.steps // 5), 3, flush, lambda: None)
-        out.append({"balance_qk": bal, "ds_subexp": dsx, "ms_per_step": round(sum(total) / len(total), 4),
+        out.append({**kw, "ms_per_step": round(sum(total) / len(total), 4),
                     "quantize_ms": round(sum(stage[0]) / len(stage[0]), 4),
                     "bwd_ms": round(sum(stage[3]) / len(stage[3]), 4), "cossim_vs_torch_fp32": cossim_vs_torch(other)})
         del other
@@ -458,6 +465,8 @@ def main():
                     help="time the library's optional Q/K channel balancing (the other settings are reported beside)")
     ap.add_argument("--ds-subexp", action="store_true",
                     help="time the library's optional dS sub-scales (the other settings are reported beside)")
+    ap.add_argument("--qk-subexp", action="store_true",
+                    help="time the library's optional Q/K sub-scales (the other settings are reported beside)")
     ap.add_argument("--layer-step", type=int, default=0, metavar="TOKENS",
                     help="also time a Llama-1B-shaped 16-layer stack forward + backward at TOKENS tokens with this "
                          "library's attention and with torch SDPA (context; not the headline)")
@@ -492,7 +501,7 @@ def main():
         cpu = cpu_baseline(w, args.cpu_budget_s)
 
     sb.load_library()
-    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp)
+    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp, qk_subexp=args.qk_subexp)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(local)
     total, stage = time_device(step, args.steps, args.warmup, flush, barrier)
@@ -539,7 +548,7 @@ def main():
         "e2e": None if e2e_ms is None else {
             "value": round(world * ops / (e2e * 1e-3) / 1e12, 3), "unit": "TOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},
-        "balance_qk": bool(args.balance_qk), "ds_subexp": bool(args.ds_subexp),
+        "balance_qk": bool(args.balance_qk), "qk_subexp": bool(args.qk_subexp), "ds_subexp": bool(args.ds_subexp),
         "gpu_launches": step.launches() * args.steps,
         "clocks": clocks,
         "status": [code0, code1],

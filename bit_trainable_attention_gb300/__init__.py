@@ -50,14 +50,15 @@ class Problem(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("N", ctypes.c_int32),
         ("d", ctypes.c_int32), ("causal", ctypes.c_int32), ("smooth_k", ctypes.c_int32),
-        ("balance_qk", ctypes.c_int32), ("ds_subexp", ctypes.c_int32), ("flags", ctypes.c_uint32), ("softmax_scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_uint32),
+        ("balance_qk", ctypes.c_int32), ("ds_subexp", ctypes.c_int32),
+        ("qk_subexp", ctypes.c_int32), ("flags", ctypes.c_uint32), ("softmax_scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_uint32),
     ]
 
     @classmethod
     def make(cls, B, Hq, Hkv, N, d, causal, smooth_k=True, flags=0, softmax_scale=0.0, wait_timeout_ms=0,
-             balance_qk=False, ds_subexp=False):
+             balance_qk=False, ds_subexp=False, qk_subexp=False):
         return cls(B, Hq, Hkv, N, d, int(bool(causal)), int(bool(smooth_k)), int(bool(balance_qk)),
-                   int(bool(ds_subexp)), flags, softmax_scale, wait_timeout_ms)
+                   int(bool(ds_subexp)), int(bool(qk_subexp)), flags, softmax_scale, wait_timeout_ms)
 
     @classmethod
     def from_tensors(cls, q, k, causal, **kw):
@@ -251,10 +252,11 @@ class SageBwdAttention(torch.autograd.Function):
     """softmax(scale Q K^T) V with SageBwd's INT8 forward and backward."""
 
     @staticmethod
-    def forward(ctx, q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False):
+    def forward(ctx, q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False,
+                qk_subexp=False):
         _check_inputs(q, k, v)
         prob = Problem.from_tensors(q, k, causal, smooth_k=smooth_k, softmax_scale=softmax_scale,
-                                    balance_qk=balance_qk, ds_subexp=ds_subexp)
+                                    balance_qk=balance_qk, ds_subexp=ds_subexp, qk_subexp=qk_subexp)
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
         saved = empty_bytes(sagebwd_saved_bytes(prob), q.device)
@@ -274,13 +276,15 @@ class SageBwdAttention(torch.autograd.Function):
         dv = torch.empty_like(v)
         ws = empty_bytes(sagebwd_workspace_bytes(prob, 1), q.device)
         sagebwd_bwd(prob, q, k, v, o, do, lse, saved, dq, dk, dv, ws)
-        return dq, dk, dv, None, None, None, None, None
+        return dq, dk, dv, None, None, None, None, None, None
 
 
-def attention(q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False):
+def attention(q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False,
+              qk_subexp=False):
     """SageBwd attention on BF16 [B, H, N, d] CUDA tensors (GQA when k/v have fewer heads).
 
     balance_qk turns on the library's power-of-two Q/K channel balancing before quantization
     (for inputs with channel outliers; Q K^T is unchanged exactly); ds_subexp refines the dS codes
-    with power-of-two sub-scales per key and 32-query group (dQ, dK several times closer to exact)."""
-    return SageBwdAttention.apply(q, k, v, causal, softmax_scale, smooth_k, balance_qk, ds_subexp)
+    with power-of-two sub-scales per key and 32-query group (dQ, dK several times closer to exact);
+    qk_subexp refines Q and K with power-of-two sub-scales per 8-channel group of each block."""
+    return SageBwdAttention.apply(q, k, v, causal, softmax_scale, smooth_k, balance_qk, ds_subexp, qk_subexp)

@@ -197,9 +197,9 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
   const int G = p->Hq / p->Hkv;
   QuantParams qp{};
   qp.job[0] = {static_cast<const __nv_bfloat16*>(q), at<__nv_bfloat16>(saved, S.q), at<float>(saved, S.sq), nullptr,
-               p->B * p->Hq, bexp, G, -1};
+               p->B * p->Hq, bexp, G, -1, p->qk_subexp ? 1 : 0};
   qp.job[1] = {static_cast<const __nv_bfloat16*>(k), at<__nv_bfloat16>(saved, S.k), at<float>(saved, S.sk), mean,
-               p->B * p->Hkv, bexp, 1, 1};
+               p->B * p->Hkv, bexp, 1, 1, p->qk_subexp ? 1 : 0};
   qp.job[2] = {static_cast<const __nv_bfloat16*>(v), at<__nv_bfloat16>(saved, S.v), at<float>(saved, S.sv), nullptr,
                p->B * p->Hkv, nullptr, 1, 1};
   qp.njobs = 3;
@@ -370,7 +370,8 @@ sagebwd_status sagebwd_quantize(const sagebwd_problem* prob, int which, const vo
                                       prob->N, prob->d, status, 1, st)));
   QuantParams qp{};
   qp.job[0] = {static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(x_q), scales,
-               smooth ? k_mean : nullptr, BH};
+               smooth ? k_mean : nullptr, BH, nullptr, 1, 1,
+               (prob->qk_subexp && (which == SAGEBWD_Q || which == SAGEBWD_K)) ? 1 : 0};
   qp.njobs = 1;
   qp.block_start[0] = 0;
   qp.block_start[1] = BH * nb;

@@ -76,10 +76,12 @@ __device__ __forceinline__ int binary_exponent(float a) {
 // the raw vectors in registers and unpacks them twice (absmax pass, code pass), which keeps
 // the register count low enough for several CTAs per SM.
 // fac (optional): the channel balancing factors of this head's channels, in shared memory.
+// gred (non-null: Q/K sub-scales): shared scratch [kThreads / 32][D / 8] for the maxima of the
+// 8-channel groups; each group's codes are then refined by 2^k (see below).
 template <int D>
 __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xq,
                                float* __restrict__ scale, const float* __restrict__ mean, int bh, int blk, int N,
-                               int nb, float* red, const float* fac = nullptr) {
+                               int nb, float* red, const float* fac = nullptr, float* gred = nullptr) {
   constexpr int V8 = D / 8, RL = kThreads / V8;
   constexpr int PER = kBlk / RL;  // rows (16-byte vectors) per thread
   static_assert(kThreads % V8 == 0 && kBlk % RL == 0, "thread layout");
@@ -121,21 +123,55 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
       for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
     }
   }
+  float gmax = amax;  // this thread's part of its 8-channel group's maximum
   const float a = block_max(amax, red);
   const bool live = a >= kMinGroupMax;
   const float inv = live ? __fdiv_rn(127.f, a) : 0.f;
+  if (gred != nullptr) {
+    // Q/K sub-scales: the group's maximum over the block's rows (the lanes that share c8,
+    // then the warps), k = floor(log2(a / group max)) in [0, 8] (0 below 2^-100); the
+    // codes are rint(x * inv * 2^k) and the stored values code * 2^-k, rounded onto that
+    // grid directly by adding and subtracting 1.5 * 2^(23-k) (ties to even)
 #pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const int r = rl + e * RL;
-    if (row0 + r < N) {
-      float v[8];
-      load(raw[e], v);
-      uint4 out;
-      out.x = pack2(quant_code(v[0], inv), quant_code(v[1], inv));
-      out.y = pack2(quant_code(v[2], inv), quant_code(v[3], inv));
-      out.z = pack2(quant_code(v[4], inv), quant_code(v[5], inv));
-      out.w = pack2(quant_code(v[6], inv), quant_code(v[7], inv));
-      *reinterpret_cast<uint4*>(xq + base + (size_t)r * D + c8 * 8) = out;
+    for (int o = V8; o < 32; o <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane < V8) gred[warp * V8 + lane] = gmax;
+    __syncthreads();
+    float g = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) g = fmaxf(g, gred[w * V8 + c8]);
+    int k = 0;
+    if (live && g >= 0x1p-100f) {
+      const uint32_t ua = __float_as_uint(a), ug = __float_as_uint(g);
+      k = min(8, (int)(ua >> 23) - (int)(ug >> 23) - ((ua & 0x7FFFFFu) < (ug & 0x7FFFFFu) ? 1 : 0));
+    }
+    const float mg = __int_as_float(((127 + 23 - k) << 23) | 0x400000);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int r = rl + e * RL;
+      if (row0 + r < N) {
+        float v[8];
+        load(raw[e], v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = __fsub_rn(__fadd_rn(__fmul_rn(v[q], inv), mg), mg);
+        const uint4 out = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+        *reinterpret_cast<uint4*>(xq + base + (size_t)r * D + c8 * 8) = out;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int r = rl + e * RL;
+      if (row0 + r < N) {
+        float v[8];
+        load(raw[e], v);
+        uint4 out;
+        out.x = pack2(quant_code(v[0], inv), quant_code(v[1], inv));
+        out.y = pack2(quant_code(v[2], inv), quant_code(v[3], inv));
+        out.z = pack2(quant_code(v[4], inv), quant_code(v[5], inv));
+        out.w = pack2(quant_code(v[6], inv), quant_code(v[7], inv));
+        *reinterpret_cast<uint4*>(xq + base + (size_t)r * D + c8 * 8) = out;
+      }
     }
   }
   if (threadIdx.x == 0) scale[(size_t)bh * nb + blk] = live ? __fdiv_rn(a, 127.f) : 0.f;
@@ -145,6 +181,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 4) quantize_kernel(const QuantParams p) {
   __shared__ float red[kThreads / 32];
   __shared__ float fac[D];
+  __shared__ float gred[kThreads / 32 * (D / 8)];
   if (p.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = 0;
   int j = 0;
   while (j + 1 < p.njobs && (int)blockIdx.x >= p.block_start[j + 1]) ++j;
@@ -156,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 4) quantize_kernel(const QuantParams
     __syncthreads();  // quantize_block reads fac only after this
   }
   quantize_block<D>(job.x, job.xq, job.scale, job.mean, bh, local % p.nb, p.N, p.nb, red,
-                    job.bexp != nullptr ? fac : nullptr);
+                    job.bexp != nullptr ? fac : nullptr, job.subexp ? gred : nullptr);
 }
 
 // Exact channel sums of one thread's rows (u: RPL 16-byte vectors of 8 BF16

@@ -35,6 +35,7 @@ struct QuantJob {
   const int* bexp;         // [B*Hkv][d] channel balancing exponents, or nullptr
   int bexp_group;          // heads per exponent row: Hq/Hkv for Q, 1 for K
   int bexp_sign;           // -1: x times 2^-e (Q); +1: x times 2^e (K)
+  int subexp;              // 1: power-of-two sub-scales per 8-channel group of each block (Q/K option)
 };
 struct QuantParams {
   QuantJob job[3];

@@ -28,6 +28,13 @@
  * the block quantizers, which leaves Q K^T unchanged exactly and evens out
  * channel outliers between the two operands; dQ is multiplied by 2^-e and
  * dK by 2^e when they are converted to BF16.
+ * Optional Q/K sub-scales (qk_subexp = 1; off by default, this library's finer
+ * Q/K granularity): each 8-channel group of a 128-token block of Q and of K
+ * keeps the block scale and is refined by 2^k, k = clamp(floor(log2(block max
+ * / group max)), 0, 8) (0 if the group max is below 2^-100): stored value
+ * rint(x * 127/max * 2^k) * 2^-k, exact in BF16 (x_q of sagebwd_quantize then
+ * holds such values for Q and K).  Channel outliers then cost precision only
+ * in their own group.
  * Optional dS sub-scales (ds_subexp = 1; off by default, this library's finer
  * dS granularity): the tile keeps its scale max|dS| / 127, and each key's codes
  * within a group of 32 queries of the tile are refined by 2^k,
@@ -87,6 +94,7 @@ typedef struct {
   int32_t smooth_k;     /* 1: subtract the per-channel mean of K over tokens before quantizing (the method) */
   int32_t balance_qk;   /* 1: power-of-two Q/K channel balancing before quantizing (see above); 0 in the method */
   int32_t ds_subexp;    /* 1: dS sub-scales per key and 32-query group (see above); 0: one dS scale per tile */
+  int32_t qk_subexp;    /* 1: Q/K sub-scales per 8-channel group of each block (see above); 0: block scale only */
   uint32_t flags;       /* SAGEBWD_FLAG_* (0 in normal use) */
   float softmax_scale;  /* <= 0 selects 1/sqrt(d) */
   uint32_t wait_timeout_ms; /* bound of every in-kernel wait; 0 selects 2000 ms */
@@ -111,7 +119,8 @@ size_t sagebwd_workspace_bytes(const sagebwd_problem* prob, int pass);
  *   which  : SAGEBWD_Q / _K / _V / _DO; x has that operand's shape.  With
  *            balance_qk the codes of Q and K depend on both tensors: Q and K
  *            then return SAGEBWD_ERR_UNSUPPORTED (use sagebwd_fwd_quantize).
- *   x_q    : BF16 output, same shape, integer values in [-127, 127].
+ *   x_q    : BF16 output, same shape, integer values in [-127, 127] (for Q and K
+ *            with qk_subexp: such integers times 2^-k, k in [0, 8]).
  *   scales : FP32 [B*H][ceil(N/128)] block scales.
  *   k_mean : FP32 [B*Hkv][d] channel means when which == SAGEBWD_K and
  *            smooth_k == 1 (then required), else ignored (may be NULL).
