@@ -43,8 +43,8 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # the one-pass ncu capture summarised in profiles/bwd_kernel_qwen15b_ncu.md.  The
 # figure belongs to the kernel sources it was taken from: once any of them changes
 # the line reports null until the capture is repeated.
-BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1328772096 + 516808448,
-               "sources_sha256": "aaee5a9a3b1d3c23415565f3e9c99c137c97a0a68bc4f88e6190eac52fb0ce35"}
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1330226176 + 518849024,
+               "sources_sha256": "219354adc431c23d1d24dc51081aa6058d161807bd5eb9fc1b3071e338d315d9"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
@@ -252,52 +252,82 @@ def other_settings(step: Step, args, dev, flush):
 
 
 def time_e2e(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_barrier):
-    """Public API (sagebwd_fwd + sagebwd_bwd) with pinned host inputs and outputs: H2D of Q, K, V, dO and
-    D2H of O, dQ, dK, dV inside the timed region.  As a training step would, the copies that the
-    compute does not wait for run on a second stream: dO travels while the forward runs, O comes back
-    while the backward runs."""
-    p, x = step.prob, step.x
+    """Public API (sagebwd_fwd + sagebwd_bwd) with pinned host inputs and outputs: every step uploads
+    its Q, K, V, dO and downloads its O, dQ, dK, dV.  As a training loop that prefetches its next batch
+    would, the device buffers are double-buffered and the copies run on two more streams (uploads,
+    downloads; the link is full duplex): step i+1's inputs go up and step i-1's results come down
+    while step i computes.  Step i is timed from the end
+    of the L2 flush that precedes it to the end of its compute (the last step also waits for its own
+    results to arrive on the host), so every copy is inside some step's interval or hidden behind its
+    compute; the copy stream starts a step's copies only after that step's interval has begun."""
+    p = step.prob
     hin = {k: v.pin_memory() for k, v in step.host.items()}
-    hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-            for k, v in (("o", step.o), ("dq", step.dq), ("dk", step.dk), ("dv", step.dv))}
+    sets = []
+    for _ in range(2):
+        sets.append({"in": {k: torch.empty_like(step.x[k]) for k in ("q", "k", "v", "do")},
+                     "o": torch.empty_like(step.o), "lse": torch.empty_like(step.lse), "dq": torch.empty_like(step.dq),
+                     "dk": torch.empty_like(step.dk), "dv": torch.empty_like(step.dv)})
+    hout = {k: torch.empty(step.__dict__[k].shape, dtype=step.__dict__[k].dtype, pin_memory=True)
+            for k in ("o", "dq", "dk", "dv")}
     s = torch.cuda.current_stream()
-    c = torch.cuda.Stream()
-    ev_do, ev_fwd = torch.cuda.Event(), torch.cuda.Event()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def one():
-        c.wait_stream(s)  # the previous step has finished with every buffer the copies touch
-        for k in ("q", "k", "v"):
-            x[k].copy_(hin[k], non_blocking=True)
-        with torch.cuda.stream(c):
-            x["do"].copy_(hin["do"], non_blocking=True)
-            ev_do.record(c)
-        sb.sagebwd_fwd(p, x["q"], x["k"], x["v"], step.o, step.lse, step.saved, step.ws0, s)
-        ev_fwd.record(s)
-        with torch.cuda.stream(c):
-            c.wait_event(ev_fwd)
-            hout["o"].copy_(step.o, non_blocking=True)
-        s.wait_event(ev_do)
-        sb.sagebwd_bwd(p, x["q"], x["k"], x["v"], step.o, x["do"], step.lse, step.saved, step.dq, step.dk, step.dv,
-                       step.ws1, s)
-        for k, t in (("dq", step.dq), ("dk", step.dk), ("dv", step.dv)):
-            hout[k].copy_(t, non_blocking=True)
-        s.wait_stream(c)
+    def run(n, timed):
+        ev_start = [torch.cuda.Event(enable_timing=timed) for _ in range(n)]
+        ev_end = [torch.cuda.Event(enable_timing=timed) for _ in range(n)]
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_comp = [torch.cuda.Event() for _ in range(n)]
+        ev_down = [torch.cuda.Event() for _ in range(n)]
 
-    for _ in range(warmup):
-        flush.zero_()
-        one()
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        def upload(j):  # on the upload stream, into set j % 2
+            with torch.cuda.stream(up):
+                up.wait_event(ev_start[j - 1 if j > 0 else 0])  # inside the step whose compute hides it
+                if j >= 2:
+                    up.wait_event(ev_comp[j - 2])  # the set's previous reader (step j-2) has finished
+                for k in ("q", "k", "v", "do"):
+                    sets[j % 2]["in"][k].copy_(hin[k], non_blocking=True)
+                ev_in[j].record(up)
+
+        def download(j, after):  # on the download stream, after step j's compute and step `after`'s start
+            with torch.cuda.stream(down):
+                down.wait_event(ev_start[after])
+                down.wait_event(ev_comp[j])
+                for k in ("o", "dq", "dk", "dv"):
+                    hout[k].copy_(sets[j % 2][k], non_blocking=True)
+                ev_down[j].record(down)
+
+        up.wait_stream(s)
+        down.wait_stream(s)
+        for i in range(n):
+            B = sets[i % 2]
+            flush.zero_()
+            ev_start[i].record(s)
+            if i == 0:
+                upload(0)
+            if i >= 1:
+                download(i - 1, i)
+            if i + 1 < n:
+                upload(i + 1)
+            s.wait_event(ev_in[i])
+            if i >= 2:
+                s.wait_event(ev_down[i - 2])  # step i-2's results, in this set, have reached the host
+            x = B["in"]
+            sb.sagebwd_fwd(p, x["q"], x["k"], x["v"], B["o"], B["lse"], step.saved, step.ws0, s)
+            sb.sagebwd_bwd(p, x["q"], x["k"], x["v"], B["o"], x["do"], B["lse"], step.saved, B["dq"], B["dk"], B["dv"],
+                           step.ws1, s)
+            ev_comp[i].record(s)
+            if i == n - 1:
+                download(i, i)
+                s.wait_event(ev_down[i])
+            ev_end[i].record(s)
+        torch.cuda.synchronize()
+        return [ev_start[i].elapsed_time(ev_end[i]) for i in range(n)] if timed else []
+
+    run(warmup, False)
     dist_barrier()
     torch.cuda.synchronize()
-    for i in range(steps):
-        flush.zero_()
-        ev[i][0].record(s)
-        one()
-        ev[i][1].record(s)
-    torch.cuda.synchronize()
+    ms = run(steps, True)
     dist_barrier()
-    ms = [e[0].elapsed_time(e[1]) for e in ev]
     h2d = sum(v.numel() * v.element_size() for v in hin.values())
     d2h = sum(v.numel() * v.element_size() for v in hout.values())
     return ms, h2d, d2h
@@ -547,7 +577,9 @@ def main():
                            "vs_bf16_dense_burst": round(value / world / peaks["bf16_burst"], 4)},
         "e2e": None if e2e_ms is None else {
             "value": round(world * ops / (e2e * 1e-3) / 1e12, 3), "unit": "TOPS", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4),
+            "copies": "double-buffered on two copy streams: step i+1's inputs up and step i-1's results down while "
+                      "step i computes; each step timed from the end of its L2 flush"},
         "balance_qk": bool(args.balance_qk), "qk_subexp": bool(args.qk_subexp), "ds_subexp": bool(args.ds_subexp),
         "gpu_launches": step.launches() * args.steps,
         "clocks": clocks,
