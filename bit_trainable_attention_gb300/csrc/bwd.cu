@@ -50,9 +50,11 @@
 namespace sagebwd {
 namespace {
 
-constexpr int kBThreads = 640;
-constexpr uint32_t kBRegsLaunch = 96;
 constexpr int kDSubMax = 8;  // largest dS sub-scale exponent
+
+// d = 64 layout: softmax warpgroups and the register split (softmax, accumulator, control)
+constexpr int kSwg64 = 4;
+constexpr uint32_t kRegS64 = 64, kRegA64 = 104, kRegC64 = 40;
 
 template <int D>
 struct BwdCfg {
@@ -63,8 +65,16 @@ struct BwdCfg {
   // registers per thread after setmaxnreg: softmax, accumulator and control warpgroups.  On
   // d = 128 the accumulators need 160 (fewer spill more and cost more than the control roles
   // gain); on d = 64 the control roles get 64, which removes their spills (bwd 5% faster).
-  static constexpr uint32_t REG_S = D == 128 ? 64 : 96, REG_A = D == 128 ? 160 : 112, REG_C = D == 128 ? 32 : 64;
-  static_assert(128 * REG_C + 256 * REG_S + 256 * REG_A <= kBThreads * kBRegsLaunch,
+  static constexpr uint32_t REG_S = D == 128 ? 64 : kRegS64, REG_A = D == 128 ? 160 : kRegA64,
+                            REG_C = D == 128 ? 32 : kRegC64;
+  // softmax warpgroups: on d = 128 two (64 query columns per thread); on d = 64, where the
+  // tensor work per tile halves but the softmax work does not, four (32 columns per thread)
+  static constexpr int SWG = D == 128 ? 2 : kSwg64;
+  static constexpr int QPT = 128 / SWG;                  // query columns per softmax thread
+  static constexpr int S_WARPS = 4 * SWG, A_WARP0 = S_WARPS, C_WARP0 = S_WARPS + 8;
+  static constexpr int THREADS = 32 * (C_WARP0 + 4);
+  static constexpr uint32_t REGS_LAUNCH = (65536 / THREADS) / 8 * 8 > 96 ? 96 : (65536 / THREADS) / 8 * 8;
+  static_assert(128 * REG_C + 128 * SWG * REG_S + 256 * REG_A <= THREADS * REGS_LAUNCH,
                 "register split exceeds the launch");
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
@@ -74,9 +84,11 @@ struct BwdCfg {
   static constexpr int OFF_DST = OFF_DOQ + NS * TILE;
   static constexpr int OFF_STG = OFF_DST + CTILE;  // own staging tile (d = 64 only)
   static constexpr int OFF_VEC = OFF_STG + (ALIAS ? 0 : 128 * D * 4);
-  // -LSE log2 e [128], -D [128], P^T scale x sdO per row [2][128], dS scale [2], |dS| maxima [8],
-  // row maxima of P exchanged between the two softmax warpgroups [128]
-  static constexpr int VEC_FLOATS = 128 + 128 + 256 + 2 + 8 + 128;
+  // -LSE log2 e [128], -D [128], P^T scale x sdO per row [2][128], dS scale [2], |dS| maxima
+  // [S_WARPS], row maxima of P exchanged between the softmax warpgroups [128] (two warpgroups) or
+  // [SWG][128] (four)
+  static constexpr int PM_FLOATS = SWG == 2 ? 128 : 128 * SWG;
+  static constexpr int VEC_FLOATS = 128 + 128 + 256 + 2 + S_WARPS + PM_FLOATS;
   static constexpr int OFF_BAR = OFF_VEC + ((VEC_FLOATS * 4 + 15) / 16) * 16;
   static constexpr int NBAR = 1 + 4 + 4 * NS + 18;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
@@ -97,7 +109,7 @@ enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty,
                bSiteTmemFreeK, bSiteStaged, bSiteStgFree, bSiteC1, bSiteC2, bSiteC3, bSiteAlign };
 
 template <int D, bool CAUSAL, bool DSX>
-__global__ void __launch_bounds__(kBThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmDOQ, const __grid_constant__ CUtensorMap tmDQ,
@@ -115,8 +127,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
   float* Dv = L2v + 128;                                      // -D_q
   float* fv_ring = Dv + 128;                                  // [2][128] sP_row * sdO per tile parity
   float* sds_ring = fv_ring + 256;                            // [2] dS scale per tile parity
-  float* am = sds_ring + 2;                                   // [8] per-warp maxima of |dS|
-  float* pm = am + 8;                                         // [128] row maxima of P (exchange)
+  float* am = sds_ring + 2;                                   // [S_WARPS] per-warp maxima of |dS|
+  float* pm = am + C::S_WARPS;                                // row maxima of P (exchange)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* bar_kv = bars;
   uint64_t* bar_q_full = bar_kv + 1;              // [2]
@@ -173,22 +185,23 @@ __global__ void __launch_bounds__(kBThreads, 1)
       mbar_init(bar_doq_empty + s, 1);
     }
     mbar_init(bar_sdp, 1);
-    mbar_init(bar_pt_ready, 256);
-    mbar_init(bar_ds_ready, 256);
+    mbar_init(bar_pt_ready, 128 * C::SWG);
+    mbar_init(bar_ds_ready, 128 * C::SWG);
     mbar_init(bar_acc_v, 1);
     mbar_init(bar_acc_q, 1);
     mbar_init(bar_acc_k, 1);
     mbar_init(bar_tmem_free_v, 256);
     mbar_init(bar_dvq_free, 256);
     mbar_init(bar_tmem_free_k, 256);
-    mbar_init(bar_c1, 256);
-    mbar_init(bar_c2, 256);
+    mbar_init(bar_c1, 128 * C::SWG);
+    mbar_init(bar_c2, 128 * C::SWG);
     mbar_init(bar_c3, 128);
     mbar_init(bar_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 17) {
+  constexpr int W_LOAD = C::C_WARP0, W_MMA = C::C_WARP0 + 1, W_RED = C::C_WARP0 + 2, W_LOAD2 = C::C_WARP0 + 3;
+  if (warp == W_MMA) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -198,9 +211,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
-  if (warp >= 16) {
-    setmaxnreg_to<C::REG_C, kBRegsLaunch>();
-    if (warp == 16 && lane == 0) {
+  if (warp >= C::C_WARP0) {
+    setmaxnreg_to<C::REG_C, C::REGS_LAUNCH>();
+    if (warp == W_LOAD && lane == 0) {
       // ---------------------------------------------------------- TMA producer: K^, V, dO
       // (the dO slot is released late on d = 128, where it holds tile it-2's dQ staging
       // half 0; Q^ and dO^ have their own producer so that they never queue behind it)
@@ -229,7 +242,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       drain(bar_kv, 0, p.timeout_ns);
       for (int s = 0; s < NS; ++s)
         if (do_iss[s]) drain(bar_do_full + s, (do_iss[s] - 1) & 1, p.timeout_ns);
-    } else if (warp == 19 && lane == 0) {
+    } else if (warp == W_LOAD2 && lane == 0) {
       // ---------------------------------------------------------- TMA producer: Q^, dO^
       int q_iss[2] = {0, 0}, doq_iss[NS];
       for (int s = 0; s < NS; ++s) doq_iss[s] = 0;
@@ -251,7 +264,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         if (q_iss[s]) drain(bar_q_full + s, (q_iss[s] - 1) & 1, p.timeout_ns);
       for (int s = 0; s < NS; ++s)
         if (doq_iss[s]) drain(bar_doq_full + s, (doq_iss[s] - 1) & 1, p.timeout_ns);
-    } else if (warp == 17 && lane == 0) {
+    } else if (warp == W_MMA && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       const uint32_t idKM = idesc_bf16_f32(128, D, false, true);     // dK (SS), dV (TS): B MN-major
@@ -335,7 +348,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       // Every MMA issued above must complete before TMEM is released.
       umma_commit(bar_final);
       drain(bar_final, 0, p.timeout_ns);
-    } else if (warp == 18 && lane == 0) {
+    } else if (warp == W_RED && lane == 0) {
       // ---------------------------------------------------------- dQ reducer
       // Half h of the FP32 dQ tile (columns [h d/2, (h+1) d/2)) is staged by accumulator
       // warpgroup h.  Half 1 goes first: on d = 128 it occupies the dS code tile that the
@@ -358,12 +371,13 @@ __global__ void __launch_bounds__(kBThreads, 1)
       }
       bulk_wait_group0();
     }
-  } else if (warp < 8) {
-    setmaxnreg_to<C::REG_S, kBRegsLaunch>();
+  } else if (warp < C::S_WARPS) {
+    setmaxnreg_to<C::REG_S, C::REGS_LAUNCH>();
     // ------------------------------------------------------------ softmax warpgroups
-    const int ws = warp >> 2;          // query half [64 ws, 64 ws + 64)
+    constexpr int QPT = C::QPT;        // query columns per thread
+    const int ws = warp >> 2;          // query slice [QPT ws, QPT ws + QPT)
     const int r = tid & 127;           // key row == TMEM lane
-    const int qc0 = 64 * ws;           // first query column of this thread
+    const int qc0 = QPT * ws;          // first query column of this thread
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + C::C_S + qc0, dp_addr = tmem + lane_base + C::C_DP + qc0;
     const uint32_t pc_addr = tmem + lane_base + C::C_PC + qc0 / 2;
@@ -387,7 +401,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     for (int it = 0; it < T; ++it) {
       const int ib = tile_ib(it);
       // the vectors of the previous tile were last read before its c2
-      (ws == 0 ? L2v : Dv)[r] = pf_vec;
+      if (ws < 2) (ws == 0 ? L2v : Dv)[r] = pf_vec;
       const float sQt = pf_sq, sdOt = pf_sdo;
       if (it + 1 < T) {
         pf_vec = tile_vec(it + 1);
@@ -412,11 +426,11 @@ __global__ void __launch_bounds__(kBThreads, 1)
         tmem_ld8(s_addr, sv[0]);
         tmem_ld8(dp_addr, dpv[0]);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < QPT / 8; ++c) {
           const int cur = c & 1;
           tmem_ld_wait_regs(sv[cur]);
           tmem_ld_wait_regs(dpv[cur]);
-          if (c + 1 < 8) {
+          if (c + 1 < QPT / 8) {
             tmem_ld8(s_addr + (c + 1) * 8, sv[cur ^ 1]);
             tmem_ld8(dp_addr + (c + 1) * 8, dpv[cur ^ 1]);
           }
@@ -462,20 +476,31 @@ __global__ void __launch_bounds__(kBThreads, 1)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (lane == 0) am[warp] = amax;
-      if (ws == 0) pm[r] = pmax;
+      if (C::SWG == 2) {
+        if (ws == 0) pm[r] = pmax;
+      } else {
+        pm[ws * 128 + r] = pmax;
+      }
       mbar_arrive(bar_c2);
       if (!waitw(wc, bar_c2, it & 1, bSiteC2)) break;
-      if (ws == 1) {
-        pmax = fmaxf(pmax, pm[r]);
-        pm[r] = pmax;
-        mbar_arrive(bar_c3);
+      if (C::SWG == 2) {
+        if (ws == 1) {
+          pmax = fmaxf(pmax, pm[r]);
+          pm[r] = pmax;
+          mbar_arrive(bar_c3);
+        } else {
+          if (!waitw(wc, bar_c3, it & 1, bSiteC3)) break;
+          pmax = pm[r];
+        }
       } else {
-        if (!waitw(wc, bar_c3, it & 1, bSiteC3)) break;
+        // every slice reads all partial maxima (the next tile writes them only after its c1)
         pmax = pm[r];
+#pragma unroll
+        for (int q = 1; q < C::SWG; ++q) pmax = fmaxf(pmax, pm[q * 128 + r]);
       }
       float a = am[0];
 #pragma unroll
-      for (int q = 1; q < 8; ++q) a = fmaxf(a, am[q]);
+      for (int q = 1; q < C::S_WARPS; ++q) a = fmaxf(a, am[q]);
       const bool p_live = pmax >= kMinGroupMax, d_live = a >= kMinGroupMax;
       // hardware reciprocal (<= 2 ulp) rather than IEEE division: these scales only
       // decide codes of this tile and dequantize it; a code at a rounding tie may differ
@@ -511,7 +536,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       {
         const float2 invP2 = make_float2(invP, invP);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
+        for (int c0 = 0; c0 < QPT; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(s_addr + c0, v);
           tmem_ld_wait();
@@ -538,7 +563,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         break;
       {
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
+        for (int c0 = 0; c0 < QPT; c0 += 32) {
           const float2 invA2 = make_float2(invA, invA);
           const float mg = c0 == 0 ? magic_lo : magic_hi;
           const float2 magic2 = make_float2(mg, mg), neg_magic2 = make_float2(-mg, -mg);
@@ -563,10 +588,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
       mbar_arrive(bar_ds_ready);
     }
   } else {
-    setmaxnreg_to<C::REG_A, kBRegsLaunch>();
+    setmaxnreg_to<C::REG_A, C::REGS_LAUNCH>();
     // ------------------------------------------------------------ accumulator warpgroups
     constexpr int DH = D / 2;           // output columns per thread
-    const int wa = (warp - 8) >> 2;     // accumulator warpgroup 0 / 1
+    const int wa = (warp - C::A_WARP0) >> 2;  // accumulator warpgroup 0 / 1
     const int r = tid & 127;            // key row == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int kglob = k0 + r;
@@ -662,7 +687,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 17) {
+  if (warp == W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -676,7 +701,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = p.nb * p.B * p.Hkv * (p.G / p.HS);
-  kern<<<grid, kBThreads, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, p);
+  kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, p);
   return cudaGetLastError();
 }
 
