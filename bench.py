@@ -43,8 +43,8 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # the one-pass ncu capture summarised in profiles/bwd_kernel_qwen15b_ncu.md.  The
 # figure belongs to the kernel sources it was taken from: once any of them changes
 # the line reports null until the capture is repeated.
-BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1330226176 + 518849024,
-               "sources_sha256": "219354adc431c23d1d24dc51081aa6058d161807bd5eb9fc1b3071e338d315d9"}
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1329297920 + 517759232,
+               "sources_sha256": "ce6943b6a094c67b6d4aee510874549baf33669377590a8d92a73b6510cee0ba"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
