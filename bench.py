@@ -472,6 +472,22 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(vals, dist, device):
+    """Each value's maximum over the ranks (the slowest replica sets the step time); identity
+    without a process group."""
+    if dist is None:
+        return list(vals)
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_tops(ops_per_replica: float, ms_max: float, world: int) -> float:
+    """Whole-job throughput: every replica processes its own copy of the workload (weak scaling),
+    so the job does world * ops in the slowest replica's time."""
+    return world * ops_per_replica / (ms_max * 1e-3) / 1e12
+
+
 def describe(w: W.Workload) -> str:
     return (f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.N} d={w.d} {'causal' if w.causal else 'non-causal'}")
 
@@ -545,12 +561,9 @@ def main():
 
     ms = sum(total) / len(total)
     e2e = sum(e2e_ms) / len(e2e_ms) if e2e_ms else 0.0
-    if dist is not None:
-        t = torch.tensor([ms, e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e = float(t[0]), float(t[1])
+    ms, e2e = max_over_ranks([ms, e2e], dist, dev)
     ops = w.flops_fwd() + w.flops_bwd()
-    value = world * ops / (ms * 1e-3) / 1e12
+    value = whole_job_tops(ops, ms, world)
     stage_ms = [sum(s) / len(s) for s in stage]
     peaks = load_peaks()
     bwd_ms = stage_ms[3]
