@@ -451,7 +451,10 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    n = pick_sample_tokens(w, args.reference_step_s)
+    # each step a bounded sample: at most reference_step_s seconds, and the whole warm-up +
+    # timed run within reference_total_s
+    step_s = min(args.reference_step_s, args.reference_total_s / max(1, args.steps + args.warmup))
+    n = pick_sample_tokens(w, step_s)
     for _ in range(args.warmup):
         oracle_sample_run(w, n)
     times, ops, cores = [], 0.0, 1
@@ -502,6 +505,8 @@ def main():
     ap.add_argument("--impl", default="library", choices=["library", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="oracle CPU-baseline sample size (seconds)")
     ap.add_argument("--reference-step-s", type=float, default=8.0, help="oracle seconds per reference-arm step")
+    ap.add_argument("--reference-total-s", type=float, default=150.0,
+                    help="oracle seconds for the whole reference-arm run (warm-up + timed steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end pass (profiling runs)")
     ap.add_argument("--no-cossim", action="store_true", help="skip the cosine-similarity reference (profiling runs)")
