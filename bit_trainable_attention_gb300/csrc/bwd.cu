@@ -12,21 +12,24 @@
 // most query blocks), and HS is chosen on the host so that this list balances
 // over the SMs.
 //
-// Warp roles (640 threads; the work of one tile flows S -> A while the tensor
-// core already computes the next tile's S^T and dP^T):
-//   warps 0-7   softmax warpgroups S (two): thread (s, r) owns key row r (TMEM
-//               lane r) and queries [64s, 64s+64) of the tile: P, dS, the codes
-//               of P^T (row scale: the two halves of a row exchange their maxima
-//               through shared memory) written to TMEM as the A operand of dV,
-//               and the codes of dS (tile scale) written to shared memory
-//   warps 8-15  accumulator warpgroups A (two): thread (a, r) owns output
+// Warp roles (the work of one tile flows S -> A while the tensor core already
+// computes the next tile's S^T and dP^T); SWG softmax warpgroups, SWG = 2 on
+// d = 128 (640 threads) and 4 on d = 64 (896 threads):
+//   warps [0, 4 SWG)          softmax warpgroups S: thread (s, r) owns key row r
+//               (TMEM lane r) and queries [QPT s, QPT s + QPT) of the tile, QPT =
+//               128 / SWG: P, dS, the codes of P^T (row scale: the slices of a row
+//               exchange their maxima through shared memory) written to TMEM as the
+//               A operand of dV, and the codes of dS (tile scale) written to shared
+//               memory
+//   next 8 warps  accumulator warpgroups A (two): thread (a, r) owns output
 //               columns [a d/2, (a+1) d/2) of row r of dV and dK (FP32 sums in
 //               registers) and of the dQ tile it scales into the staging tile
-//   warp 16     TMA producer of K^, V, dO; warp 19 TMA producer of Q^, dO^;
-//   warp 17     TMEM allocation and the MMA-issuing thread;
-//   warp 18     dQ reducer (bulk reduce-add of each staged half)
-// Registers: 640 threads launch with 96 each; the last warpgroup drops to 32 and
-// the others rise (d = 128: S 64, A 160; 128 * 32 + 256 * 64 + 256 * 160 = 640 * 96).
+//   last 4 warps  TMA producer of K^, V, dO; TMEM allocation and the MMA-issuing
+//               thread; dQ reducer (bulk reduce-add of each staged half); TMA
+//               producer of Q^, dO^
+// Registers (setmaxnreg from the launch count): d = 128 launch 96, S 64, A 160,
+// control 32 (128 * 32 + 256 * 64 + 256 * 160 = 640 * 96); d = 64 launch 72,
+// S 64, A 104, control 40.
 // TMEM columns: S^T / P [0,128), dP^T / dS [128,256), dV [256,256+d), dK
 // [256+d,256+2d).  d = 128: dQ reuses the dV columns once they are read and the
 // P^T codes sit in the first 64 dK columns until dV has read them; d = 64: dQ

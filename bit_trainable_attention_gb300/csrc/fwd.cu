@@ -11,7 +11,7 @@
 //   warp 9           TMEM allocation and the single MMA-issuing thread
 //   warps 10-11      idle (complete the third warpgroup, which gives its
 //                    registers to the softmax warpgroups: 384 threads launch with
-//                    168 registers each; 128 * kRegsLow + 256 * kRegsHigh <= 384 * 168)
+//                    168 registers each; 128 * LOW + 256 * HIGH <= 384 * 168)
 // TMEM: tile t owns S_t [256t, 256t+128) and O_t [256t+128, 256t+128+d).  The
 // quantized P~ codes are written over S_t (packed BF16, columns [256t, 256t+64))
 // and feed O_t = P^_t V^_j as the A operand straight from TMEM.
