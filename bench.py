@@ -44,7 +44,7 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # figure belongs to the kernel sources it was taken from: once any of them changes
 # the line reports null until the capture is repeated.
 BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1329297920 + 517759232,
-               "sources_sha256": "ce6943b6a094c67b6d4aee510874549baf33669377590a8d92a73b6510cee0ba"}
+               "sources_sha256": "2ff53da927d7e0a434d2d4391dcefa8406b75d21723b9028ff1cc58b3ce6d3a2"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
