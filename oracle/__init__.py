@@ -32,7 +32,7 @@ class OracleProblem(ctypes.Structure):
         ("N", ctypes.c_int32), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
         ("smooth_k", ctypes.c_int32), ("balance_qk", ctypes.c_int32), ("exact_codes", ctypes.c_int32),
         ("threads", ctypes.c_int32), ("exact_mask", ctypes.c_uint32), ("int8_dp", ctypes.c_int32),
-        ("ds_subexp", ctypes.c_int32), ("qk_subexp", ctypes.c_int32),
+        ("ds_subexp", ctypes.c_int32), ("qk_subexp", ctypes.c_int32), ("fp8", ctypes.c_int32),
         ("softmax_scale", ctypes.c_double),
     ]
 
@@ -66,8 +66,17 @@ def _load():
         lib.oracle_fwd_tile.argtypes = [P, vp, vp] + [ctypes.c_int] * 4 + [vp, vp]
         lib.oracle_bwd_tile.argtypes = [P, vp, vp, vp, vp, vp, vp] + [ctypes.c_int] * 4 + [vp, vp, vp, vp]
         lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_round_e4m3.argtypes = [vp, vp, ctypes.c_int64]
         _lib = lib
     return _lib
+
+
+def round_e4m3(x) -> np.ndarray:
+    """FP8 E4M3 rounding (nearest, ties to even, saturating at 448) of FP64 values."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    assert _load().oracle_round_e4m3(_ptr(x), _ptr(y), x.size) == 0
+    return y
 
 
 def max_threads() -> int:
@@ -89,9 +98,9 @@ def _bf16_bits(x) -> np.ndarray:
 
 
 def problem(B, Hq, Hkv, N, d, causal, smooth_k=True, exact_codes=False, softmax_scale=0.0, threads=0, exact_mask=0,
-            balance_qk=False, int8_dp=False, ds_subexp=False, qk_subexp=False):
+            balance_qk=False, int8_dp=False, ds_subexp=False, qk_subexp=False, fp8=False):
     return OracleProblem(B, Hq, Hkv, N, d, int(causal), int(smooth_k), int(balance_qk), int(exact_codes),
-                         int(threads), int(exact_mask), int(int8_dp), int(ds_subexp), int(qk_subexp),
+                         int(threads), int(exact_mask), int(int8_dp), int(ds_subexp), int(qk_subexp), int(fp8),
                          float(softmax_scale))
 
 

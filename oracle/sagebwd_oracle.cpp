@@ -36,6 +36,9 @@
 //    sums to zero, so the mean's gradient vanishes);
 //  * ablation int8_dp (off by default): dP = dO V^T from the INT8 codes of dO
 //    and V, the variant the pages' ablation rejects;
+//  * ablation fp8 (off by default): every quantizer produces FP8 E4M3 values
+//    with scale max/448 instead of INT8 codes (the pages compare INT8 with FP8
+//    SageBwd, "SageAttention3 ..." summary, Measured effects);
 //  * optional Q/K sub-scales (qk_subexp, off by default; the library's own
 //    finer Q/K granularity): a power-of-two refinement per 8-channel group of
 //    each 128-token block (see quant_block);
@@ -79,6 +82,7 @@ typedef struct {
   int32_t int8_dp;      // ablation: dP = dO V^T from the INT8 codes of dO and V instead of BF16 operands
   int32_t ds_subexp;    // 1: dS codes carry a power-of-two sub-scale per (key, 32-query group) of a tile
   int32_t qk_subexp;    // 1: Q and K codes carry a power-of-two sub-scale per (block, 8-channel group)
+  int32_t fp8;          // ablation: every quantizer produces FP8 E4M3 values (scale max/448) instead of INT8
   double softmax_scale;  // <= 0: 1/sqrt(d)
 } oracle_problem;
 }
@@ -108,18 +112,40 @@ enum Quantizer { QZ_Q = 0, QZ_K = 1, QZ_V = 2, QZ_DO = 3, QZ_PF = 4, QZ_PB = 5, 
 // code: round to nearest, ties to even (C nearbyint in the default mode), then
 // clamp to [-127, 127].  Codes are stored as doubles: every integer product
 // sum here stays far below 2^53, so it is exact.
+// FP8 E4M3 (4 exponent bits, bias 7, 3 mantissa bits, no infinities, largest
+// finite 448): round to nearest, ties to even, saturating at 448.  Normal
+// numbers of binary exponent E (>= -6) have spacing 2^(E-3); below 2^-6 the
+// subnormal spacing is 2^-9.
+double round_e4m3(double v) {
+  const double a = std::fabs(v);
+  if (a == 0.0) return 0.0;
+  int e = 0;
+  std::frexp(a, &e);  // a = f 2^e, f in [0.5, 1): binary exponent e - 1
+  const double q = std::ldexp(1.0, std::max(e - 1, -6) - 3);
+  const double r = std::min(448.0, std::nearbyint(a / q) * q);
+  return std::copysign(r, v);
+}
+
 struct Mode {
   bool fp32;       // false only in the exact_codes pin mode
   uint32_t exact;  // bit set: that quantizer does not round
+  bool fp8 = false;       // the FP8 ablation: E4M3 values instead of INT8 codes
+  double qmax = 127.0;    // largest code: 127 (INT8) or 448 (E4M3)
   double F(double x) const { return fp32 ? (double)(float)x : x; }
   double Q(int which, double x) const {
     if (exact & (1u << which)) return x;
+    if (fp8) return round_e4m3(x);
     const double r = std::nearbyint(x);
     return std::min(127.0, std::max(-127.0, r));
   }
 };
 inline Mode mode_of(const oracle_problem* p) {
-  return p->exact_codes ? Mode{false, 0x7Fu} : Mode{true, p->exact_mask};
+  Mode m = p->exact_codes ? Mode{false, 0x7Fu} : Mode{true, p->exact_mask};
+  if (p->fp8) {
+    m.fp8 = true;
+    m.qmax = 448.0;
+  }
+  return m;
 }
 
 inline int nblocks(int N) { return (N + BLK - 1) / BLK; }
@@ -173,8 +199,8 @@ void quant_block(const Mode& M, int which, const double* x, int count, double* c
     *scale = 0;
     return;
   }
-  const double inv = M.F(127.0 / a);
-  *scale = M.F(a / 127.0);
+  const double inv = M.F(M.qmax / a);
+  *scale = M.F(a / M.qmax);
   if (!subexp) {
     for (int e = 0; e < count; ++e) codes[e] = M.Q(which, M.F(x[e] * inv));
     return;
@@ -337,7 +363,7 @@ double fwd_tile_logits(const Mode& M, const oracle_problem* p, const QTensor& qq
 
 // Code of P~ for one key: rint(127 * 2^(t - tmax)), tmax the row maximum of its tile.
 inline double fwd_p_code(const Mode& M, double t, double tmax) {
-  return M.Q(QZ_PF, M.F(127.0 * M.F(std::exp2(M.F(t - tmax)))));
+  return M.Q(QZ_PF, M.F(M.qmax * M.F(std::exp2(M.F(t - tmax)))));
 }
 
 // Forward of the quantized algorithm for query row i of head h, written as the
@@ -362,7 +388,7 @@ void fwd_row(const Mode& M, const oracle_problem* p, const QTensor& qq, const QT
   std::fill(acc.begin(), acc.end(), 0.0);
   for (int jb = 0; jb <= jb_end; ++jb) {
     if (tmax[jb] == -kInf) continue;
-    const double w = std::exp2(tmax[jb] - m) / 127.0 * vq.s(bhk, jb);
+    const double w = std::exp2(tmax[jb] - m) / M.qmax * vq.s(bhk, jb);
     for (int ch = 0; ch < d; ++ch) {
       double s = 0;
       for (int k = jb * BLK; k < std::min(N, (jb + 1) * BLK); ++k) {
@@ -469,8 +495,8 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
     double cmax = 0;
     for (int a = 0; a < T.ni; ++a) cmax = std::max(cmax, P[(size_t)a * BLK + c]);
     if (cmax < kMinGroupMax) continue;
-    const double inv = M.F(127.0 / cmax);
-    T.spc[c] = M.F(cmax / 127.0);
+    const double inv = M.F(M.qmax / cmax);
+    T.spc[c] = M.F(cmax / M.qmax);
     for (int a = 0; a < T.ni; ++a) T.pt[(size_t)c * BLK + a] = M.Q(QZ_PB, M.F(P[(size_t)a * BLK + c] * inv));
   }
   // dS quantized with one scale for the whole tile (and, with ds_subexp, a
@@ -481,8 +507,8 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
     for (int c = 0; c < T.nk; ++c) amax = std::max(amax, std::fabs(dS[(size_t)a * BLK + c]));
   T.sds = 0;
   if (amax >= kMinGroupMax) {
-    const double inv = M.F(127.0 / amax);
-    T.sds = M.F(amax / 127.0);
+    const double inv = M.F(M.qmax / amax);
+    T.sds = M.F(amax / M.qmax);
     for (int a = 0; a < T.ni; ++a)
       for (int c = 0; c < T.nk; ++c) {
         const double x = M.F(dS[(size_t)a * BLK + c] * inv);
@@ -583,6 +609,7 @@ extern "C" {
 int oracle_check_problem(const oracle_problem* p) {
   if (!p || p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->N < 1 || p->d < 1) return 1;
   if (p->Hq % p->Hkv != 0) return 1;
+  if (p->fp8 && (p->ds_subexp || p->qk_subexp)) return 1;  // sub-scales are defined for INT8 codes
   return 0;
 }
 
@@ -828,6 +855,12 @@ int oracle_bwd_tile(const oracle_problem* p, const uint16_t* q, const uint16_t* 
   std::copy(T.spc.begin(), T.spc.end(), spc);
   std::copy(T.ds.begin(), T.ds.end(), ds);  // integer codes; with ds_subexp code * 2^-k
   *sds = T.sds;
+  return 0;
+}
+
+// FP8 E4M3 rounding of n values (the fp8 ablation's element rounding), for pins.
+int oracle_round_e4m3(const double* x, double* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = round_e4m3(x[i]);
   return 0;
 }
 
