@@ -43,6 +43,7 @@ class Workload:
     k_offset_sd: float = 0.0
     outlier_frac: float = 0.0
     seed: int = SEED_BASE
+    q_offset_sd: float = 0.0  # per (query head, channel) offset of Q (none in the named workloads)
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -99,6 +100,8 @@ def make_inputs(w: Workload, seed: int | None = None) -> dict:
     if w.outlier_frac > 0:
         q = _outliers(q, w.outlier_frac, g)
         k = _outliers(k, w.outlier_frac, g)
+    if w.q_offset_sd > 0:  # drawn last, so the other draws do not depend on it
+        q = q + torch.randn(1, w.Hq, 1, w.d, generator=g) * w.q_offset_sd
     bf = torch.bfloat16
     return {"q": q.to(bf).contiguous(), "k": k.to(bf).contiguous(), "v": v.to(bf).contiguous(),
             "do": do.to(bf).contiguous()}

@@ -36,6 +36,11 @@
 //    sums to zero, so the mean's gradient vanishes);
 //  * ablation int8_dp (off by default): dP = dO V^T from the INT8 codes of dO
 //    and V, the variant the pages' ablation rejects;
+//  * optional Q-smoothing (smooth_q, off by default; the pages call it optional
+//    with limited benefit in pre-training, SageBwd Abstract, finding (iv)): each
+//    128-token block of Q subtracts its channel means before quantizing, and
+//    S gains mean_Q . K'^T in FP32; dK gains (sum over the block's queries of
+//    dS) times mean_Q (see qsmooth_bias);
 //  * ablation fp8 (off by default): every quantizer produces FP8 E4M3 values
 //    with scale max/448 instead of INT8 codes (the pages compare INT8 with FP8
 //    SageBwd, "SageAttention3 ..." summary, Measured effects);
@@ -83,6 +88,7 @@ typedef struct {
   int32_t ds_subexp;    // 1: dS codes carry a power-of-two sub-scale per (key, 32-query group) of a tile
   int32_t qk_subexp;    // 1: Q and K codes carry a power-of-two sub-scale per (block, 8-channel group)
   int32_t fp8;          // ablation: every quantizer produces FP8 E4M3 values (scale max/448) instead of INT8
+  int32_t smooth_q;     // 1: Q-smoothing (block mean of Q subtracted before quantizing, mean . K' added to S)
   double softmax_scale;  // <= 0: 1/sqrt(d)
 } oracle_problem;
 }
@@ -166,8 +172,12 @@ struct QTensor {
   std::vector<double> codes;
   std::vector<double> scale;  // [BH][nblocks]
   std::vector<double> mean;   // [BH][d] (K only)
+  std::vector<double> bmean;  // [BH][nblocks][d] block means (Q-smoothing only)
+  std::vector<double> val;    // [BH][N][d] the values the quantizer saw (K under Q-smoothing only)
   double c(int bh, int n, int ch) const { return codes[((size_t)bh * N + n) * d + ch]; }
   double s(int bh, int blk) const { return scale[(size_t)bh * nblocks(N) + blk]; }
+  double bm(int bh, int blk, int ch) const { return bmean[((size_t)bh * nblocks(N) + blk) * d + ch]; }
+  double v(int bh, int n, int ch) const { return val[((size_t)bh * N + n) * d + ch]; }
 };
 
 // Power-of-two sub-scale exponent of a group inside a quantization group
@@ -235,8 +245,12 @@ void channel_mean(const Mode& M, const uint16_t* xb, int N, int d, double* mu) {
 // smoothing) is then multiplied by its channel's factor
 // (*fac)[(bh / fac_group) * d + ch], rounded to FP32, before the block
 // quantizer sees it (channel balancing).
+// block_smooth (Q-smoothing): each block first subtracts its own channel means
+// (FP64 sum over the block's valid tokens, divided in FP64, rounded to FP32),
+// kept in out.bmean.  keep_vals keeps the values the quantizer saw in out.val.
 void quantize_tensor(const Mode& M, int which, const uint16_t* x, int BH, int N, int d, bool smooth, QTensor& out,
-                     const std::vector<double>* fac = nullptr, int fac_group = 1, bool subexp = false) {
+                     const std::vector<double>* fac = nullptr, int fac_group = 1, bool subexp = false,
+                     bool block_smooth = false, bool keep_vals = false) {
   out.BH = BH;
   out.N = N;
   out.d = d;
@@ -244,6 +258,8 @@ void quantize_tensor(const Mode& M, int which, const uint16_t* x, int BH, int N,
   out.codes.assign((size_t)BH * N * d, 0);
   out.scale.assign((size_t)BH * nb, 0.0);
   out.mean.assign(smooth ? (size_t)BH * d : 0, 0.0);
+  out.bmean.assign(block_smooth ? (size_t)BH * nb * d : 0, 0.0);
+  out.val.assign(keep_vals ? (size_t)BH * N * d : 0, 0.0);
 #pragma omp parallel for schedule(dynamic)
   for (int bh = 0; bh < BH; ++bh) {
     const uint16_t* xb = x + (size_t)bh * N * d;
@@ -262,7 +278,18 @@ void quantize_tensor(const Mode& M, int which, const uint16_t* x, int BH, int N,
           double val = smooth ? M.F(v - mu[ch]) : v;
           if (f) val = M.F(val * f[ch]);
           vals[(size_t)r * d + ch] = val;
+          if (keep_vals) out.val[((size_t)bh * N + n0 + r) * d + ch] = val;
         }
+      if (block_smooth) {
+        double* bm = &out.bmean[((size_t)bh * nb + blk) * d];
+        for (int ch = 0; ch < d; ++ch) {
+          double sum = 0;
+          for (int r = 0; r < rows; ++r) sum += vals[(size_t)r * d + ch];
+          bm[ch] = M.F(sum / (double)rows);
+        }
+        for (int r = 0; r < rows; ++r)
+          for (int ch = 0; ch < d; ++ch) vals[(size_t)r * d + ch] = M.F(vals[(size_t)r * d + ch] - bm[ch]);
+      }
       quant_block(M, which, vals.data(), rows * d, &out.codes[((size_t)bh * N + n0) * d], &out.scale[(size_t)bh * nb + blk],
                   d, subexp);
     }
@@ -328,15 +355,26 @@ void quantize_qk(const Mode& M, const oracle_problem* p, const uint16_t* q, cons
   }
   const int G = p->Hq / p->Hkv;
   quantize_tensor(M, QZ_Q, q, p->B * p->Hq, p->N, p->d, false, qq, p->balance_qk ? &f_q : nullptr, G,
-                  p->qk_subexp != 0);
+                  p->qk_subexp != 0, p->smooth_q != 0);
   quantize_tensor(M, QZ_K, k, p->B * p->Hkv, p->N, p->d, p->smooth_k != 0, kq, p->balance_qk ? &f_k : nullptr, 1,
-                  p->qk_subexp != 0);
+                  p->qk_subexp != 0, false, p->smooth_q != 0);
   if (exps) *exps = std::move(e);
   if (fq) *fq = std::move(f_q);
   if (fk) *fk = std::move(f_k);
 }
 
 inline bool visible(const oracle_problem* p, int i, int k) { return k < p->N && (!p->causal || k <= i); }
+
+// Q-smoothing's correction of S for query block ib and key k, in base 2:
+// c0 * (mean_Q(ib) . K'_k), the dot product in FP64 rounded to FP32 (K' the
+// unquantized K the quantizer saw); 0 without Q-smoothing.
+inline double qsmooth_bias(const Mode& M, const oracle_problem* p, const QTensor& qq, const QTensor& kq, int bhq,
+                           int ib, int bhk, int k, double c0) {
+  if (!p->smooth_q) return 0.0;
+  double b = 0;
+  for (int ch = 0; ch < p->d; ++ch) b += qq.bm(bhq, ib, ch) * kq.v(bhk, k, ch);
+  return M.F(M.F(b) * c0);
+}
 
 // Base-2 logits of one query row against one 128-key tile:
 // t_k = S_int * (sQ sK) * (scale log2 e) with S_int = Q^_i . K^_k, the row's
@@ -355,7 +393,7 @@ double fwd_tile_logits(const Mode& M, const oracle_problem* p, const QTensor& qq
     }
     double s = 0;
     for (int ch = 0; ch < d; ++ch) s += qq.c(bhq, i, ch) * kq.c(bhk, k, ch);
-    t[k] = M.F(s * qks);
+    t[k] = M.F(M.F(s * qks) + qsmooth_bias(M, p, qq, kq, bhq, ib, bhk, k, c0));
     tmax = std::max(tmax, t[k]);
   }
   return tmax;
@@ -471,7 +509,7 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
       if (!visible(p, i, kk)) continue;
       double s = 0;
       for (int ch = 0; ch < d; ++ch) s += qq.c(bhq, i, ch) * kq.c(bhk, kk, ch);
-      const double tt = M.F(s * qks);
+      const double tt = M.F(M.F(s * qks) + qsmooth_bias(M, p, qq, kq, bhq, ib, bhk, kk, c0));
       const double pp = M.F(std::exp2(M.F(tt - L)));  // normalized probability
       // dP = dO V^T: the product kept in high precision (BF16 inputs, FP64 sum here);
       // the int8_dp ablation takes it from the dO and V codes instead (the pages' ablation
@@ -564,6 +602,12 @@ void bwd_impl(const oracle_problem* p, const uint16_t* q, const uint16_t* k, con
               accv[(size_t)c * d + ch] += T.spc[c] * dq8.s(bhq, ib) * sv;
               acck[(size_t)c * d + ch] += sc * T.sds * qq.s(bhq, ib) * sk;
             }
+          if (p->smooth_q)  // dK = dS^T (Q_s + mean_Q): the block mean's share, from the same dS values
+            for (int c = 0; c < T.nk; ++c) {
+              double colsum = 0;
+              for (int a = 0; a < T.ni; ++a) colsum += T.ds[(size_t)a * BLK + c];
+              for (int ch = 0; ch < d; ++ch) acck[(size_t)c * d + ch] += sc * T.sds * colsum * qq.bm(bhq, ib, ch);
+            }
         }
       }
       for (int c = 0; c < std::min(BLK, N - jb * BLK); ++c)
@@ -610,6 +654,7 @@ int oracle_check_problem(const oracle_problem* p) {
   if (!p || p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->N < 1 || p->d < 1) return 1;
   if (p->Hq % p->Hkv != 0) return 1;
   if (p->fp8 && (p->ds_subexp || p->qk_subexp)) return 1;  // sub-scales are defined for INT8 codes
+  if (p->smooth_q && p->balance_qk) return 1;               // not defined together
   return 0;
 }
 

@@ -231,3 +231,43 @@ def test_int8_against_fp8_ablation(oracle_mod):
     for k in ("dq", "dk"):
         assert abs(l1(int8, k) - l1(fp8, k)) < 0.2 * l1(fp8, k), k
         assert l1(sub, k) < 0.6 * l1(fp8, k), k
+
+
+@pytest.mark.parametrize("smooth_k", [True, False])
+@pytest.mark.parametrize("w", [W.small("qoff_causal", 1, 4, 2, 300, 64, True, 71, qk_norm=True, k_offset_sd=2.0,
+                                       q_offset_sd=2.0),
+                               W.small("qoff_nc_ragged", 2, 2, 1, 200, 32, False, 73, k_offset_sd=3.0,
+                                       q_offset_sd=3.0)], ids=lambda w: w.name)
+def test_unrounded_pipeline_with_q_smoothing_is_exact_attention(oracle_mod, w, smooth_k):
+    """Q-smoothing (the pages' optional companion of K-smoothing): with every quantizer unrounded,
+    subtracting each block's Q mean, adding mean_Q . K'^T to S and (sum of dS) * mean_Q to dK is
+    exact attention -- this pins the correction terms."""
+    x = W.make_inputs(w)
+    pe = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_k=smooth_k, exact_codes=True, smooth_q=True)
+    r = oracle_mod.pipeline(pe, x["q"], x["k"], x["v"], x["do"])
+    ref = oracle_mod.pipeline(pe, x["q"], x["k"], x["v"], x["do"], exact=True)
+    for key in ("o", "dq", "dk", "dv"):
+        np.testing.assert_allclose(r[key], ref[key], rtol=0, atol=1e-10 * np.abs(ref[key]).max(), err_msg=key)
+
+
+def test_q_smoothing_helps_only_with_q_offsets(oracle_mod):
+    """"SageBwd: A Trainable Low-bit Attention" (Abstract, finding (iv)): Q-smoothing gives limited
+    benefit in pre-training, while the SageAttention3 page's ablation shows it helping where Q has
+    offsets.  With per-channel Q offsets every output moves closer to exact attention; on the
+    QK-normed recipe without Q offsets the change is within 5 % of the error."""
+    def errs(w, smooth_q):
+        x = W.make_inputs(w)
+        p0 = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal)
+        ex = oracle_mod.pipeline(p0, x["q"], x["k"], x["v"], x["do"], exact=True)
+        p = oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_q=smooth_q)
+        r = oracle_mod.pipeline(p, x["q"], x["k"], x["v"], x["do"])
+        return {k: 1 - cos(r[k], ex[k]) for k in ("o", "dq", "dk", "dv")}
+    w = W.small("qoff_nc", 1, 2, 2, 300, 128, False, 72, k_offset_sd=3.0, q_offset_sd=3.0)
+    e0, e1 = errs(w, False), errs(w, True)
+    for k in e0:
+        assert e1[k] < e0[k], (k, e0, e1)
+    assert e1["o"] < 0.5 * e0["o"] and e1["dk"] < 0.5 * e0["dk"], (e0, e1)
+    w = W.WORKLOADS["llama1b"].with_(Hq=8, Hkv=2, N=384)
+    e0, e1 = errs(w, False), errs(w, True)
+    for k in e0:
+        assert abs(e1[k] - e0[k]) < 0.05 * e0[k], (k, e0, e1)
