@@ -29,6 +29,8 @@ SMALL = [
     W.small("n129_d128_noncausal", 1, 2, 2, 129, 128, False, 205, qk_norm=True),
     W.small("n127_d64_causal_b2", 2, 2, 2, 127, 64, True, 206),
     W.small("gqa6_causal_520_d128", 1, 6, 1, 520, 128, True, 207, outlier_frac=0.01),
+    W.small("gqa8_causal_260_d64", 1, 8, 1, 260, 64, True, 208, qk_norm=True, k_offset_sd=2.0),
+    W.small("gqa12_noncausal_384_d64_b2", 2, 12, 1, 384, 64, False, 209, k_offset_sd=3.0),
 ]
 
 
