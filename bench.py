@@ -148,7 +148,7 @@ class Step:
         rec(2)
         sb.sagebwd_bwd_prepare(p, self.o, x["do"], self.ws1, s)
         rec(3)
-        sb.sagebwd_bwd_attention(p, x["v"], x["do"], self.lse, self.saved, self.ws1, s)
+        sb.sagebwd_bwd_attention(p, x["v"], x["do"], self.lse, self.saved, self.dk, self.dv, self.ws1, s)
         rec(4)
         sb.sagebwd_bwd_finish(p, self.saved, self.dq, self.dk, self.dv, self.ws1, s)
         rec(5)

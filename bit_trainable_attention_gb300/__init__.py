@@ -91,7 +91,7 @@ def load_library():
             lib.sagebwd_fwd_quantize.argtypes = [P, vp, vp, vp, vp, vp, vp]
             lib.sagebwd_fwd_attention.argtypes = [P, vp, vp, vp, vp, vp]
             lib.sagebwd_bwd_prepare.argtypes = [P, vp, vp, vp, vp]
-            lib.sagebwd_bwd_attention.argtypes = [P, vp, vp, vp, vp, vp, vp]
+            lib.sagebwd_bwd_attention.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.sagebwd_bwd_finish.argtypes = [P, vp, vp, vp, vp, vp, vp]
             lib.sagebwd_check_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
             lib.sagebwd_quantize_k_noalloc.argtypes = [P, vp, vp, vp, vp, vp]
@@ -173,9 +173,9 @@ def sagebwd_bwd_prepare(prob, o, dO, ws, stream=None):
            "sagebwd_bwd_prepare")
 
 
-def sagebwd_bwd_attention(prob, v, dO, lse, saved, ws, stream=None):
+def sagebwd_bwd_attention(prob, v, dO, lse, saved, dk, dv, ws, stream=None):
     _check(load_library().sagebwd_bwd_attention(ctypes.byref(prob), _ptr(v), _ptr(dO), _ptr(lse), _ptr(saved),
-                                                _ptr(ws), _stream(stream)),
+                                                _ptr(dk), _ptr(dv), _ptr(ws), _stream(stream)),
            "sagebwd_bwd_attention")
 
 

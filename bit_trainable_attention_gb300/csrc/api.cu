@@ -241,26 +241,6 @@ sagebwd_status fwd_attention_impl(const sagebwd_problem* p, const void* saved, v
   return cuda_status(launch_fwd(tq, tk, tv, fp, p->d, p->causal, st));
 }
 
-sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const void* dO, void* ws, cudaStream_t st) {
-  const WsLayout W = ws_layout(p, 1);
-  PrepParams pp{};
-  pp.o = static_cast<const __nv_bfloat16*>(o);
-  pp.dO = static_cast<const __nv_bfloat16*>(dO);
-  pp.D = at<float>(ws, W.D);
-  pp.dOq = at<__nv_bfloat16>(ws, W.dOq);
-  pp.sdo = at<float>(ws, W.sdo);
-  pp.dq_acc = at<float>(ws, W.dqacc);
-  pp.dk_acc = at<float>(ws, W.dkacc);
-  pp.dv_acc = at<float>(ws, W.dvacc);
-  pp.BH = p->B * p->Hq;
-  pp.BHk = p->B * p->Hkv;
-  pp.N = p->N;
-  pp.d = p->d;
-  pp.nb = nblocks(p->N);
-  pp.status = at<int>(ws, W.status);
-  return cuda_status(launch_bwd_prep(pp, st));
-}
-
 // Query heads per backward CTA for this shape on the current device, memoised
 // (the list schedule behind it costs more host time than a launch).
 int heads_per_cta(const sagebwd_problem* p) {
@@ -289,8 +269,34 @@ int heads_per_cta(const sagebwd_problem* p) {
   return hs;
 }
 
+// dK, dV go straight to their BF16 outputs when each key block has a single CTA
+// (all G query heads of a kv head in one CTA) and no factor follows (channel
+// balancing multiplies dK at the conversion): no FP32 accumulators to zero,
+// reduce or convert.
+bool direct_dkdv(const sagebwd_problem* p) { return !p->balance_qk && heads_per_cta(p) == p->Hq / p->Hkv; }
+
+sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const void* dO, void* ws, cudaStream_t st) {
+  const WsLayout W = ws_layout(p, 1);
+  PrepParams pp{};
+  pp.o = static_cast<const __nv_bfloat16*>(o);
+  pp.dO = static_cast<const __nv_bfloat16*>(dO);
+  pp.D = at<float>(ws, W.D);
+  pp.dOq = at<__nv_bfloat16>(ws, W.dOq);
+  pp.sdo = at<float>(ws, W.sdo);
+  pp.dq_acc = at<float>(ws, W.dqacc);
+  pp.dk_acc = at<float>(ws, W.dkacc);
+  pp.dv_acc = at<float>(ws, W.dvacc);
+  pp.BH = p->B * p->Hq;
+  pp.BHk = direct_dkdv(p) ? 0 : p->B * p->Hkv;  // the dK / dV accumulators to zero
+  pp.N = p->N;
+  pp.d = p->d;
+  pp.nb = nblocks(p->N);
+  pp.status = at<int>(ws, W.status);
+  return cuda_status(launch_bwd_prep(pp, st));
+}
+
 sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const void* dO, const float* lse,
-                                  const void* saved, void* ws, cudaStream_t st) {
+                                  const void* saved, void* dk, void* dv, void* ws, cudaStream_t st) {
   const SavedLayout S = saved_layout(p);
   const WsLayout W = ws_layout(p, 1);
   CUtensorMap tq, tk, tv, tdo, tdoq, tdq;
@@ -318,6 +324,9 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
   bp.dq_acc = at<float>(ws, W.dqacc);
   bp.dk_acc = at<float>(ws, W.dkacc);
   bp.dv_acc = at<float>(ws, W.dvacc);
+  const bool direct = direct_dkdv(p);
+  bp.dk_out = direct ? static_cast<__nv_bfloat16*>(dk) : nullptr;
+  bp.dv_out = direct ? static_cast<__nv_bfloat16*>(dv) : nullptr;
   bp.status = at<int>(ws, W.status);
   bp.timeout_ns = timeout_of(p);
   bp.flags = p->flags;
@@ -334,7 +343,7 @@ sagebwd_status bwd_finish_impl(const sagebwd_problem* p, const void* saved, void
       {at<float>(ws, W.dqacc), static_cast<__nv_bfloat16*>(dq), nq, bexp, -1, p->Hq / p->Hkv, p->N, p->d},
       {at<float>(ws, W.dkacc), static_cast<__nv_bfloat16*>(dk), nk, bexp, 1, 1, p->N, p->d},
       {at<float>(ws, W.dvacc), static_cast<__nv_bfloat16*>(dv), nk, nullptr, 1, 1, p->N, p->d}};
-  return cuda_status(launch_grad_convert(jobs, 3, st));
+  return cuda_status(launch_grad_convert(jobs, direct_dkdv(p) ? 1 : 3, st));  // dK, dV written directly
 }
 
 }  // namespace
@@ -414,10 +423,10 @@ sagebwd_status sagebwd_bwd_prepare(const sagebwd_problem* prob, const void* o, c
 }
 
 sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v, const void* dO, const float* lse,
-                                     const void* saved, void* ws, void* stream) {
+                                     const void* saved, void* dk, void* dv, void* ws, void* stream) {
   SB_CHECK(check_problem(prob));
-  SB_CHECK(check_ptrs({v, dO, lse, saved, ws}));
-  return bwd_attention_impl(prob, v, dO, lse, saved, ws, static_cast<cudaStream_t>(stream));
+  SB_CHECK(check_ptrs({v, dO, lse, saved, dk, dv, ws}));
+  return bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, static_cast<cudaStream_t>(stream));
 }
 
 sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, const void* saved, void* dq, void* dk, void* dv,
@@ -434,7 +443,7 @@ sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const voi
   SB_CHECK(check_ptrs({q, k, v, o, dO, lse, saved, dq, dk, dv, ws}));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   SB_CHECK(bwd_prepare_impl(prob, o, dO, ws, st));
-  SB_CHECK(bwd_attention_impl(prob, v, dO, lse, saved, ws, st));
+  SB_CHECK(bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, st));
   return bwd_finish_impl(prob, saved, dq, dk, dv, ws, st);
 }
 

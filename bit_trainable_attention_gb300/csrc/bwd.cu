@@ -677,14 +677,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_arrive(bar_dvq_free);
     }
     if (!*abort_flag && kglob < p.N) {
-      // this CTA's share of dK_j, dV_j (row kglob, columns [wa d/2, (wa+1) d/2)) into the FP32 sums
-      float* dka = p.dk_acc + ((size_t)bhk * p.N + kglob) * D + wa * DH;
-      float* dva = p.dv_acc + ((size_t)bhk * p.N + kglob) * D + wa * DH;
+      const size_t row = ((size_t)bhk * p.N + kglob) * D + wa * DH;
+      if (p.dk_out != nullptr) {
+        // the only CTA of this key block: dK_j, dV_j (row kglob, columns [wa d/2, (wa+1) d/2))
+        // rounded to BF16 as the conversion kernel would round the FP32 sums
+        uint4* dko = reinterpret_cast<uint4*>(p.dk_out + row);
+        uint4* dvo = reinterpret_cast<uint4*>(p.dv_out + row);
 #pragma unroll
-      for (int c = 0; c < DH; c += 4) {
-        const int h = c >> 1;
-        red_add_v4_f32(dka + c, lo_f32(dk_run[h]), hi_f32(dk_run[h]), lo_f32(dk_run[h + 1]), hi_f32(dk_run[h + 1]));
-        red_add_v4_f32(dva + c, lo_f32(dv_run[h]), hi_f32(dv_run[h]), lo_f32(dv_run[h + 1]), hi_f32(dv_run[h + 1]));
+        for (int c = 0; c < DH; c += 8) {
+          const int h = c >> 1;
+          dko[c / 8] = make_uint4(pack_bf16x2(lo_f32(dk_run[h]), hi_f32(dk_run[h])),
+                                  pack_bf16x2(lo_f32(dk_run[h + 1]), hi_f32(dk_run[h + 1])),
+                                  pack_bf16x2(lo_f32(dk_run[h + 2]), hi_f32(dk_run[h + 2])),
+                                  pack_bf16x2(lo_f32(dk_run[h + 3]), hi_f32(dk_run[h + 3])));
+          dvo[c / 8] = make_uint4(pack_bf16x2(lo_f32(dv_run[h]), hi_f32(dv_run[h])),
+                                  pack_bf16x2(lo_f32(dv_run[h + 1]), hi_f32(dv_run[h + 1])),
+                                  pack_bf16x2(lo_f32(dv_run[h + 2]), hi_f32(dv_run[h + 2])),
+                                  pack_bf16x2(lo_f32(dv_run[h + 3]), hi_f32(dv_run[h + 3])));
+        }
+      } else {
+        // this CTA's share of dK_j, dV_j into the FP32 sums
+        float* dka = p.dk_acc + row;
+        float* dva = p.dv_acc + row;
+#pragma unroll
+        for (int c = 0; c < DH; c += 4) {
+          const int h = c >> 1;
+          red_add_v4_f32(dka + c, lo_f32(dk_run[h]), hi_f32(dk_run[h]), lo_f32(dk_run[h + 1]),
+                         hi_f32(dk_run[h + 1]));
+          red_add_v4_f32(dva + c, lo_f32(dv_run[h]), hi_f32(dv_run[h]), lo_f32(dv_run[h + 1]),
+                         hi_f32(dv_run[h + 1]));
+        }
       }
     }
   }

@@ -119,6 +119,10 @@ struct BwdParams {
   float* dq_acc;    // [BHq][N][d]
   float* dk_acc;    // [BHk][N][d]
   float* dv_acc;    // [BHk][N][d]
+  // non-null when one CTA covers all G query heads of its key block (HS == G) and no factor
+  // has to be applied afterwards: dK, dV are then written as BF16 here, not accumulated
+  __nv_bfloat16* dk_out;  // [BHk][N][d]
+  __nv_bfloat16* dv_out;  // [BHk][N][d]
   int* status;
   uint64_t timeout_ns;
   uint32_t flags;

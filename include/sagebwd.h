@@ -158,12 +158,20 @@ sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const voi
  *   sagebwd_fwd_quantize  : K mean (and the balancing exponents) and the
  *                           Q, K, V quantization into `saved`.
  *   sagebwd_fwd_attention : the fused forward kernel on `saved` -> o, lse.
- *   sagebwd_bwd_prepare   : D = rowsum(dO * O), quantized dO, zeroed dQ, dK
- *                           and dV accumulators (all in the backward workspace).
+ *   sagebwd_bwd_prepare   : D = rowsum(dO * O), quantized dO, zeroed dQ
+ *                           accumulator and, when they are used, dK and dV
+ *                           accumulators (all in the backward workspace).
  *   sagebwd_bwd_attention : the fused backward kernel -> the FP32 dQ, dK, dV
- *                           accumulators in the workspace.
- *   sagebwd_bwd_finish    : the accumulators -> BF16 dq, dk, dv (times 2^-e
- *                           and 2^e with balance_qk; `saved` holds e).     */
+ *                           accumulators in the workspace; when one CTA covers
+ *                           all query heads of a kv head (the library's choice
+ *                           of query heads per CTA, e.g. always with Hq == Hkv)
+ *                           and balance_qk is 0, it writes BF16 dk, dv itself
+ *                           and the dK / dV accumulators are not used.
+ *   sagebwd_bwd_finish    : the accumulators -> BF16 dq and, unless the
+ *                           attention stage wrote them, dk, dv (times 2^-e
+ *                           and 2^e with balance_qk; `saved` holds e).
+ * The three backward stages must see the same problem (they take the same
+ * decision on dk, dv).                                                      */
 sagebwd_status sagebwd_fwd_quantize(const sagebwd_problem* prob, const void* q, const void* k, const void* v,
                                     void* saved, void* ws, void* stream);
 sagebwd_status sagebwd_fwd_attention(const sagebwd_problem* prob, const void* saved, void* o, float* lse, void* ws,
@@ -171,7 +179,7 @@ sagebwd_status sagebwd_fwd_attention(const sagebwd_problem* prob, const void* sa
 sagebwd_status sagebwd_bwd_prepare(const sagebwd_problem* prob, const void* o, const void* dO, void* ws,
                                    void* stream);
 sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v, const void* dO, const float* lse,
-                                     const void* saved, void* ws, void* stream);
+                                     const void* saved, void* dk, void* dv, void* ws, void* stream);
 sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, const void* saved, void* dq, void* dk, void* dv,
                                   void* ws, void* stream);
 

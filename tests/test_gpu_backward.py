@@ -86,7 +86,7 @@ def test_backward_stages_equal_single_call(oracle_mod):
     ws = sb.empty_bytes(sb.sagebwd_workspace_bytes(prob, 1), "cuda")
     dq, dk, dv = torch.empty_like(xd["q"]), torch.empty_like(xd["k"]), torch.empty_like(xd["v"])
     sb.sagebwd_bwd_prepare(prob, fwd["o"], xd["do"], ws)
-    sb.sagebwd_bwd_attention(prob, xd["v"], xd["do"], fwd["lse"], fwd["saved"], ws)
+    sb.sagebwd_bwd_attention(prob, xd["v"], xd["do"], fwd["lse"], fwd["saved"], dk, dv, ws)
     sb.sagebwd_bwd_finish(prob, fwd["saved"], dq, dk, dv, ws)
     torch.cuda.synchronize()
     assert torch.equal(dk, a["dk"]) and torch.equal(dv, a["dv"])
