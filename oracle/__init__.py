@@ -68,6 +68,7 @@ def _load():
         lib.oracle_bwd_tile.argtypes = [P, vp, vp, vp, vp, vp, vp] + [ctypes.c_int] * 4 + [vp, vp, vp, vp]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_round_e4m3.argtypes = [vp, vp, ctypes.c_int64]
+        lib.oracle_qsmooth_terms.argtypes = [P, vp, vp, vp, vp]
         _lib = lib
     return _lib
 
@@ -148,6 +149,17 @@ def quantize_qk(p: OracleProblem, q, k):
                                     _ptr(out["k"]), _ptr(out["sk"]), _ptr(out["mu"]), _ptr(out["e"]))
     assert rc == 0
     return out
+
+
+def qsmooth_terms(p: OracleProblem, q, k):
+    """Q-smoothing's FP32 block means of Q [B*Hq, nb, d] and base-2 logit terms
+    c0 * (mean_Q(block) . K'_key) [B*Hq, nb, N] (p.smooth_q must be set)."""
+    q, k = _bf16_bits(q), _bf16_bits(k)
+    BHq, nb = p.B * p.Hq, nblocks(p.N)
+    qm = np.zeros((BHq, nb, p.d), np.float32)
+    bias = np.zeros((BHq, nb, p.N), np.float32)
+    assert _load().oracle_qsmooth_terms(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(qm), _ptr(bias)) == 0
+    return {"qm": qm, "bias": bias}
 
 
 def _sel(sel, n):

@@ -709,6 +709,27 @@ int oracle_quantize_qk(const oracle_problem* p, const uint16_t* q, const uint16_
   return 0;
 }
 
+// Q-smoothing's quantities as the forward uses them (smooth_q problems): the FP32 block
+// means of Q [B*Hq][nb][d] and the base-2 logit terms [B*Hq][nb][N] of qsmooth_bias.
+int oracle_qsmooth_terms(const oracle_problem* p, const uint16_t* q, const uint16_t* k, float* qmean, float* bias) {
+  if (oracle_check_problem(p) || !p->smooth_q) return 1;
+  set_threads(p);
+  const Mode M = mode_of(p);
+  QTensor qq, kq;
+  quantize_qk(M, p, q, k, qq, kq);
+  const double c0 = M.F(scale_of(p) * kLog2e);
+  const int N = p->N, nb = nblocks(N), G = p->Hq / p->Hkv;
+  for (size_t i = 0; i < qq.bmean.size(); ++i) qmean[i] = (float)qq.bmean[i];
+#pragma omp parallel for schedule(dynamic)
+  for (int bhq = 0; bhq < p->B * p->Hq; ++bhq) {
+    const int bhk = (bhq / p->Hq) * p->Hkv + (bhq % p->Hq) / G;
+    for (int ib = 0; ib < nb; ++ib)
+      for (int key = 0; key < N; ++key)
+        bias[((size_t)bhq * nb + ib) * N + key] = (float)qsmooth_bias(M, p, qq, kq, bhq, ib, bhk, key, c0);
+  }
+  return 0;
+}
+
 // Quantized forward.  o: FP64 [B][Hq][N][d]; lse: FP64 [B][Hq][N] (natural log).
 // qsel (optional): [B*Hq][ceil(N/128)] flags; unselected query blocks are not written.
 int oracle_fwd(const oracle_problem* p, const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o,
