@@ -119,13 +119,14 @@ class ClockSampler:
 class Step:
     """Buffers and the stage-by-stage calls of one forward + backward step."""
 
-    def __init__(self, w: W.Workload, dev, balance_qk=False, ds_subexp=False, qk_subexp=False, inputs=None):
+    def __init__(self, w: W.Workload, dev, balance_qk=False, ds_subexp=False, qk_subexp=False, inputs=None,
+                 smooth_q=False):
         self.w = w
         x = W.make_inputs(w) if inputs is None else inputs
         self.host = x
         self.x = {k: v.to(dev) for k, v in x.items()}
         self.prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, balance_qk=balance_qk,
-                                    ds_subexp=ds_subexp, qk_subexp=qk_subexp)
+                                    ds_subexp=ds_subexp, qk_subexp=qk_subexp, smooth_q=smooth_q)
         p = self.prob
         self.o = torch.empty_like(self.x["q"])
         self.lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
@@ -156,7 +157,7 @@ class Step:
     # kernels of ours per step: [K mean or Q/K statistics: partial + final] + quantize + fwd + prep + bwd
     # + gradient convert
     def launches(self):
-        return (2 if (self.prob.smooth_k or self.prob.balance_qk) else 0) + 5
+        return (2 if (self.prob.smooth_k or self.prob.balance_qk) else 0) + 5 + (1 if self.prob.smooth_q else 0)
 
 
 def time_torch_sdpa(step: Step, steps: int, warmup: int, flush: torch.Tensor):
@@ -239,7 +240,7 @@ def other_settings(step: Step, args, dev, flush):
     combos = [(False,) * 3] + [tuple(i == j for j in range(3)) for i in range(3)] + [(True,) * 3]
     out = []
     for combo in combos:
-        if combo == mine:
+        if combo == mine and not step.prob.smooth_q:
             continue
         kw = dict(zip(OPTIONS, combo))
         other = Step(step.w, dev, inputs=step.host, **kw)
@@ -518,6 +519,8 @@ def main():
                     help="time the library's optional dS sub-scales (the other settings are reported beside)")
     ap.add_argument("--qk-subexp", action="store_true",
                     help="time the library's optional Q/K sub-scales (the other settings are reported beside)")
+    ap.add_argument("--smooth-q", action="store_true",
+                    help="time the library's optional Q-smoothing (block means of Q subtracted, logit term added)")
     ap.add_argument("--layer-step", type=int, default=0, metavar="TOKENS",
                     help="also time a Llama-1B-shaped 16-layer stack forward + backward at TOKENS tokens with this "
                          "library's attention and with torch SDPA (context; not the headline)")
@@ -552,7 +555,8 @@ def main():
         cpu = cpu_baseline(w, args.cpu_budget_s)
 
     sb.load_library()
-    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp, qk_subexp=args.qk_subexp)
+    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp, qk_subexp=args.qk_subexp,
+                smooth_q=args.smooth_q)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(local)
     total, stage = time_device(step, args.steps, args.warmup, flush, barrier)
@@ -599,6 +603,7 @@ def main():
             "copies": "double-buffered on two copy streams: step i+1's inputs up and step i-1's results down while "
                       "step i computes; each step timed from the end of its L2 flush"},
         "balance_qk": bool(args.balance_qk), "qk_subexp": bool(args.qk_subexp), "ds_subexp": bool(args.ds_subexp),
+        "smooth_q": bool(args.smooth_q),
         "gpu_launches": step.launches() * args.steps,
         "clocks": clocks,
         "status": [code0, code1],

@@ -51,14 +51,16 @@ class Problem(ctypes.Structure):
         ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("N", ctypes.c_int32),
         ("d", ctypes.c_int32), ("causal", ctypes.c_int32), ("smooth_k", ctypes.c_int32),
         ("balance_qk", ctypes.c_int32), ("ds_subexp", ctypes.c_int32),
-        ("qk_subexp", ctypes.c_int32), ("flags", ctypes.c_uint32), ("softmax_scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_uint32),
+        ("qk_subexp", ctypes.c_int32), ("smooth_q", ctypes.c_int32), ("flags", ctypes.c_uint32),
+        ("softmax_scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_uint32),
     ]
 
     @classmethod
     def make(cls, B, Hq, Hkv, N, d, causal, smooth_k=True, flags=0, softmax_scale=0.0, wait_timeout_ms=0,
-             balance_qk=False, ds_subexp=False, qk_subexp=False):
+             balance_qk=False, ds_subexp=False, qk_subexp=False, smooth_q=False):
         return cls(B, Hq, Hkv, N, d, int(bool(causal)), int(bool(smooth_k)), int(bool(balance_qk)),
-                   int(bool(ds_subexp)), int(bool(qk_subexp)), flags, softmax_scale, wait_timeout_ms)
+                   int(bool(ds_subexp)), int(bool(qk_subexp)), int(bool(smooth_q)), flags, softmax_scale,
+                   wait_timeout_ms)
 
     @classmethod
     def from_tensors(cls, q, k, causal, **kw):
@@ -227,6 +229,8 @@ def quantized_views(prob: Problem, saved: torch.Tensor) -> dict:
     sizes = [("q", B * Hq * N * d * 2), ("k", B * Hkv * N * d * 2), ("v", B * Hkv * N * d * 2),
              ("sq", B * Hq * nb * 4), ("sk", B * Hkv * nb * 4), ("sv", B * Hkv * nb * 4), ("mu", B * Hkv * d * 4),
              ("e", B * Hkv * d * 4)]
+    if prob.smooth_q:
+        sizes += [("qm", B * Hq * nb * d * 4), ("qb", B * Hq * nb * nb * 128 * 4)]
     out, off = {}, 0
     for name, n in sizes:
         out[name] = saved[off:off + n]
@@ -239,6 +243,9 @@ def quantized_views(prob: Problem, saved: torch.Tensor) -> dict:
     out["sv"] = out["sv"].view(torch.float32).view(B * Hkv, nb)
     out["mu"] = out["mu"].view(torch.float32).view(B * Hkv, d)
     out["e"] = out["e"].view(torch.int32).view(B * Hkv, d)
+    if prob.smooth_q:
+        out["qm"] = out["qm"].view(torch.float32).view(B * Hq, nb, d)
+        out["qb"] = out["qb"].view(torch.float32).view(B * Hq, nb, nb * 128)
     return out
 
 
@@ -253,10 +260,11 @@ class SageBwdAttention(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False,
-                qk_subexp=False):
+                qk_subexp=False, smooth_q=False):
         _check_inputs(q, k, v)
         prob = Problem.from_tensors(q, k, causal, smooth_k=smooth_k, softmax_scale=softmax_scale,
-                                    balance_qk=balance_qk, ds_subexp=ds_subexp, qk_subexp=qk_subexp)
+                                    balance_qk=balance_qk, ds_subexp=ds_subexp, qk_subexp=qk_subexp,
+                                    smooth_q=smooth_q)
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
         saved = empty_bytes(sagebwd_saved_bytes(prob), q.device)
@@ -276,15 +284,18 @@ class SageBwdAttention(torch.autograd.Function):
         dv = torch.empty_like(v)
         ws = empty_bytes(sagebwd_workspace_bytes(prob, 1), q.device)
         sagebwd_bwd(prob, q, k, v, o, do, lse, saved, dq, dk, dv, ws)
-        return dq, dk, dv, None, None, None, None, None, None
+        return dq, dk, dv, None, None, None, None, None, None, None
 
 
 def attention(q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False,
-              qk_subexp=False):
+              qk_subexp=False, smooth_q=False):
     """SageBwd attention on BF16 [B, H, N, d] CUDA tensors (GQA when k/v have fewer heads).
 
     balance_qk turns on the library's power-of-two Q/K channel balancing before quantization
     (for inputs with channel outliers; Q K^T is unchanged exactly); ds_subexp refines the dS codes
     with power-of-two sub-scales per key and 32-query group (dQ, dK several times closer to exact);
-    qk_subexp refines Q and K with power-of-two sub-scales per 8-channel group of each block."""
-    return SageBwdAttention.apply(q, k, v, causal, softmax_scale, smooth_k, balance_qk, ds_subexp, qk_subexp)
+    qk_subexp refines Q and K with power-of-two sub-scales per 8-channel group of each block;
+    smooth_q subtracts each 128-token block's channel means from Q before quantizing and adds their
+    logit term back in FP32 (for queries with a large common offset; not with balance_qk)."""
+    return SageBwdAttention.apply(q, k, v, causal, softmax_scale, smooth_k, balance_qk, ds_subexp, qk_subexp,
+                                  smooth_q)

@@ -27,13 +27,14 @@ sagebwd_status check_problem(const sagebwd_problem* p) {
   const double elems = (double)p->B * p->Hq * p->N * p->d;
   if (elems >= 2147483648.0) return SAGEBWD_ERR_UNSUPPORTED;
   if ((double)nblocks(p->N) * p->B * p->Hq >= 2147483647.0) return SAGEBWD_ERR_UNSUPPORTED;
+  if (p->smooth_q && p->balance_qk) return SAGEBWD_ERR_UNSUPPORTED;  // not defined together
   return SAGEBWD_OK;
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 struct SavedLayout {
-  size_t q, k, v, sq, sk, sv, mu, be, total;
+  size_t q, k, v, sq, sk, sv, mu, be, qm, qb, total;
 };
 SavedLayout saved_layout(const sagebwd_problem* p) {
   const size_t nb = (size_t)nblocks(p->N);
@@ -48,13 +49,18 @@ SavedLayout saved_layout(const sagebwd_problem* p) {
   L.sv = off; off += align_up((size_t)p->B * p->Hkv * nb * 4);
   L.mu = off; off += align_up((size_t)p->B * p->Hkv * p->d * 4);
   L.be = off; off += align_up((size_t)p->B * p->Hkv * p->d * 4);
+  L.qm = L.qb = 0;
+  if (p->smooth_q) {  // block means of Q, and the logit terms mean_Q . K' per (query head, query block, key)
+    L.qm = off; off += align_up((size_t)p->B * p->Hq * nb * p->d * 4);
+    L.qb = off; off += align_up((size_t)p->B * p->Hq * nb * nb * kBlk * 4);
+  }
   L.total = off;
   return L;
 }
 
 // Workspace: [status word | pass scratch].
 struct WsLayout {
-  size_t status, kpart, kmax, kmin, qmax, D, dOq, sdo, dqacc, dkacc, dvacc, total;
+  size_t status, kpart, kmax, kmin, qmax, D, dOq, sdo, dqacc, dkacc, dvacc, cs, total;
 };
 WsLayout ws_layout(const sagebwd_problem* p, int pass) {
   const size_t nb = (size_t)nblocks(p->N);
@@ -77,6 +83,11 @@ WsLayout ws_layout(const sagebwd_problem* p, int pass) {
     const size_t ke = (size_t)p->B * p->Hkv * p->N * p->d;
     L.dkacc = off; off += align_up(ke * 4);
     L.dvacc = off; off += align_up(ke * 4);
+    // Q-smoothing: per backward CTA (at most one per query head and key block) a ring of
+    // two tile parities x four softmax slices x 128 keys of dS column sums
+    if (p->smooth_q) {
+      L.cs = off; off += align_up((size_t)p->B * p->Hq * nb * 2 * 4 * 128 * 4);
+    }
   }
   L.total = off;
   return L;
@@ -197,7 +208,7 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
   const int G = p->Hq / p->Hkv;
   QuantParams qp{};
   qp.job[0] = {static_cast<const __nv_bfloat16*>(q), at<__nv_bfloat16>(saved, S.q), at<float>(saved, S.sq), nullptr,
-               p->B * p->Hq, bexp, G, -1, p->qk_subexp ? 1 : 0};
+               p->B * p->Hq, bexp, G, -1, p->qk_subexp ? 1 : 0, p->smooth_q ? at<float>(saved, S.qm) : nullptr};
   qp.job[1] = {static_cast<const __nv_bfloat16*>(k), at<__nv_bfloat16>(saved, S.k), at<float>(saved, S.sk), mean,
                p->B * p->Hkv, bexp, 1, 1, p->qk_subexp ? 1 : 0};
   qp.job[2] = {static_cast<const __nv_bfloat16*>(v), at<__nv_bfloat16>(saved, S.v), at<float>(saved, S.sv), nullptr,
@@ -210,7 +221,23 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
   qp.nb = nb;
   qp.status = status;
   qp.clear_status = (p->smooth_k || p->balance_qk) ? 0 : 1;
-  return cuda_status(launch_quantize(qp, st));
+  SB_CHECK(cuda_status(launch_quantize(qp, st)));
+  if (p->smooth_q) {
+    QBiasParams bp{};
+    bp.k = static_cast<const __nv_bfloat16*>(k);
+    bp.kmean = mean;
+    bp.qmean = at<float>(saved, S.qm);
+    bp.bias = at<float>(saved, S.qb);
+    bp.BHq = p->B * p->Hq;
+    bp.G = G;
+    bp.N = p->N;
+    bp.d = p->d;
+    bp.nb = nb;
+    bp.causal = p->causal ? 1 : 0;
+    bp.c0 = c0_of(p);
+    SB_CHECK(cuda_status(launch_qsmooth_bias(bp, st)));
+  }
+  return SAGEBWD_OK;
 }
 
 sagebwd_status fwd_attention_impl(const sagebwd_problem* p, const void* saved, void* o, float* lse, void* ws,
@@ -235,6 +262,7 @@ sagebwd_status fwd_attention_impl(const sagebwd_problem* p, const void* saved, v
   fp.sv = at<float>(saved, S.sv);
   fp.o = static_cast<__nv_bfloat16*>(o);
   fp.lse = lse;
+  fp.qbias = p->smooth_q ? at<float>(saved, S.qb) : nullptr;
   fp.status = at<int>(ws, W.status);
   fp.timeout_ns = timeout_of(p);
   fp.flags = p->flags;
@@ -327,6 +355,11 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
   const bool direct = direct_dkdv(p);
   bp.dk_out = direct ? static_cast<__nv_bfloat16*>(dk) : nullptr;
   bp.dv_out = direct ? static_cast<__nv_bfloat16*>(dv) : nullptr;
+  if (p->smooth_q) {
+    bp.qbias = at<float>(saved, S.qb);
+    bp.qmean = at<float>(saved, S.qm);
+    bp.cs_part = at<float>(ws, W.cs);
+  }
   bp.status = at<int>(ws, W.status);
   bp.timeout_ns = timeout_of(p);
   bp.flags = p->flags;
@@ -366,6 +399,8 @@ sagebwd_status sagebwd_quantize(const sagebwd_problem* prob, int which, const vo
   SB_CHECK(need(which >= SAGEBWD_Q && which <= SAGEBWD_DO, SAGEBWD_ERR_INVALID_ARG));
   // balanced Q and K codes depend on both tensors: only sagebwd_fwd_quantize makes them
   SB_CHECK(need(!(prob->balance_qk && (which == SAGEBWD_Q || which == SAGEBWD_K)), SAGEBWD_ERR_UNSUPPORTED));
+  // Q-smoothing's block means have no output here: only sagebwd_fwd_quantize makes those Q codes
+  SB_CHECK(need(!(prob->smooth_q && which == SAGEBWD_Q), SAGEBWD_ERR_UNSUPPORTED));
   const bool smooth = which == SAGEBWD_K && prob->smooth_k;
   SB_CHECK(check_ptrs({x, x_q, scales, ws}));
   if (smooth) SB_CHECK(check_ptrs({k_mean}));

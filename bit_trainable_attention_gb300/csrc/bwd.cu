@@ -40,6 +40,12 @@
 //   dP^T(i+1) = V_j dO_i+1^T (BF16)          once the dS of tile i has been coded
 //   dK(i) = dS^T Q^_i, dQ(i) = dS K^_j       from the shared dS code tile
 // so the softmax warpgroups wait for the next tile only while dP^T(i+1) runs.
+// With Q-smoothing (QSM) the recomputed logits gain the precomputed term mean_Q(block i) . K'_r
+// of the thread's key (one scalar per thread and tile, folded into -LSE), each softmax thread
+// sums its dS operand values over its queries, and the accumulator warpgroups add the block
+// mean's share of dK = dS^T (Q - mean_Q + mean_Q): scale s_dS (column sum) mean_Q(block i).
+// The per-slice column sums go through a small global scratch ring (two tile parities); there
+// is no shared memory left for them on d = 128.
 // Shared memory at d = 128 has room for one dO, dO^ stage and two Q^ stages, so
 // the FP32 dQ staging tile of tile i borrows the dO tile (dO_i+1 has been read by
 // dP^T(i+1) by then) and the dS code tile (after dK(i), dQ(i)); d = 64
@@ -111,7 +117,7 @@ enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty,
                bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAccV, bSiteAccQ, bSiteAccK, bSiteTmemFreeV, bSiteDVQFree,
                bSiteTmemFreeK, bSiteStaged, bSiteStgFree, bSiteC1, bSiteC2, bSiteC3, bSiteAlign };
 
-template <int D, bool CAUSAL, bool DSX>
+template <int D, bool CAUSAL, bool DSX, bool QSM>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -398,18 +404,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     };
     auto tile_sq = [&](int t) { return p.sq[(size_t)tile_bhq(t) * p.nb + tile_ib(t)]; };
     auto tile_sdo = [&](int t) { return p.sdo[(size_t)tile_bhq(t) * p.nb + tile_ib(t)]; };
-    float pf_vec = tile_vec(0), pf_sq = tile_sq(0), pf_sdo = tile_sdo(0);
+    // Q-smoothing: the logit term mean_Q(tile's query block) . K'_r of this thread's key
+    auto tile_bias = [&](int t) -> float {
+      return QSM ? p.qbias[((size_t)tile_bhq(t) * p.nb + tile_ib(t)) * ((size_t)p.nb * kBlk) + k0 + r] : 0.f;
+    };
+    float pf_vec = tile_vec(0), pf_sq = tile_sq(0), pf_sdo = tile_sdo(0), pf_bias = tile_bias(0);
     const float2 kMagic2 = make_float2(12582912.0f, 12582912.0f), kNegMagic2 = make_float2(-12582912.0f, -12582912.0f);
 
     for (int it = 0; it < T; ++it) {
       const int ib = tile_ib(it);
       // the vectors of the previous tile were last read before its c2
       if (ws < 2) (ws == 0 ? L2v : Dv)[r] = pf_vec;
-      const float sQt = pf_sq, sdOt = pf_sdo;
+      const float sQt = pf_sq, sdOt = pf_sdo, bk = pf_bias;
       if (it + 1 < T) {
         pf_vec = tile_vec(it + 1);
         pf_sq = tile_sq(it + 1);
         pf_sdo = tile_sdo(it + 1);
+        if (QSM) pf_bias = tile_bias(it + 1);
       }
       mbar_arrive(bar_c1);
       if (!waitw(wc, bar_c1, it & 1, bSiteC1)) break;
@@ -445,7 +456,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
             for (int e2 = 0; e2 < 4; e2 += 2) {
               const int e = e4 + e2;
-              const float2 nl = e2 == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+              float2 nl = e2 == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+              if (QSM) nl = fadd2(nl, make_float2(bk, bk));
               const float2 nd = e2 == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
               const float2 x =
                   ffma2(make_float2(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])), qks2, nl);
@@ -564,6 +576,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (it >= 1 && !(C::ALIAS ? waitw(wc, bar_stg_free + 1, (it - 1) & 1, bSiteStgFree)
                                 : waitw(wc, bar_acc_q, (it - 1) & 1, bSiteAccQ)))
         break;
+      // Q-smoothing on d = 64: the accumulator warpgroups have finished tile i-1 (so they read the
+      // column sums of tile i-2 from this parity's slot, and waited for tile i-1's dS release
+      // before this tile's can complete); on d = 128 the staging wait above implies both
+      if (QSM && !C::ALIAS && it >= 1 && !waitw(wc, bar_dvq_free, (it - 1) & 1, bSiteDVQFree)) break;
+      float2 csum = make_float2(0.f, 0.f);  // this thread's sum of its dS operand values (exact in FP32)
       {
 #pragma unroll
         for (int c0 = 0; c0 < QPT; c0 += 32) {
@@ -578,6 +595,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             const float2 cd = fadd2(
                 fadd2(fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invA2), magic2),
                 neg_magic2);
+            if (QSM) csum = fadd2(csum, cd);
             v[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
           }
 #pragma unroll
@@ -586,6 +604,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                          v[4 * h + 3]);
         }
       }
+      if (QSM) p.cs_part[(((size_t)blockIdx.x * 2 + (it & 1)) * C::SWG + ws) * 128 + r] = csum.x + csum.y;
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar_ds_ready);
@@ -607,6 +626,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     for (int it = 0; it < T; ++it) {
       const float sQt = sq_next;
       if (it + 1 < T) sq_next = p.sq[(size_t)tile_bhq(it + 1) * p.nb + tile_ib(it + 1)];
+      // Q-smoothing: this warpgroup's half of mean_Q(tile's query block) into L1 now, read at
+      // the end of the tile (a quarter of a line per lane group: lanes 0..DH/32-1 of each warp)
+      if (QSM && lane < DH / 32)
+        prefetch_l1(p.qmean + ((size_t)tile_bhq(it) * p.nb + tile_ib(it)) * D + wa * DH + lane * 32);
       if (!waitw(wc, bar_acc_v, it & 1, bSiteAccV)) break;
       // the tile's scales were stored before the P^T codes were released
       if (!waitw(wc, bar_pt_ready, it & 1, bSitePTReady)) break;
@@ -645,6 +668,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(bar_tmem_free_k);
+      if (QSM) {
+        // Q-smoothing, while dQ(i) runs: dK_r += scale s_dS (sum over the tile's queries of the dS
+        // operand values) mean_Q(block i); the slices' column sums were stored before dS was
+        // released
+        if (!waitw(wc, bar_ds_ready, it & 1, bSiteDSReady)) break;
+        const float* cs = p.cs_part + ((size_t)blockIdx.x * 2 + (it & 1)) * C::SWG * 128 + r;
+        float colsum = cs[0];
+#pragma unroll
+        for (int q = 1; q < C::SWG; ++q) colsum += cs[q * 128];
+        const float wcs = __fmul_rn(__fmul_rn(p.sc, sDS), colsum);
+        const uint64_t w2 = pack_f32x2(wcs, wcs);
+        const float4* mq =
+            reinterpret_cast<const float4*>(p.qmean + ((size_t)tile_bhq(it) * p.nb + tile_ib(it)) * D + wa * DH);
+#pragma unroll
+        for (int c = 0; c < DH; c += 4) {
+          const float4 m = __ldg(mq + c / 4);
+          ffma2_acc(dk_run[c >> 1], w2, __float_as_uint(m.x), __float_as_uint(m.y));
+          ffma2_acc(dk_run[(c >> 1) + 1], w2, __float_as_uint(m.z), __float_as_uint(m.w));
+        }
+      }
       // dQ tile (lane r = query row i0 + r) -> scaled FP32 staging half wa: boxes of
       // [128 rows][32 floats] with the 128-byte swizzle, reduced into global by the reducer
       // (on d = 128 half 0 overwrites dO_i+1, which dP^T(i+1) has read, and half 1 the dS
@@ -722,7 +765,7 @@ template <int D, bool CAUSAL, bool DSX>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                          const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s) {
   using C = BwdCfg<D>;
-  auto kern = bwd_kernel<D, CAUSAL, DSX>;
+  auto kern = p.qbias != nullptr ? bwd_kernel<D, CAUSAL, DSX, true> : bwd_kernel<D, CAUSAL, DSX, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = p.nb * p.B * p.Hkv * (p.G / p.HS);

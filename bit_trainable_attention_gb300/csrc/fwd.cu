@@ -27,6 +27,9 @@
 //   l     = l a + (r/127) sum_k 2^(t - tmax + log2 127)   (unquantized P~)
 //   O    <- O a + (r/127) sV_j [P^ V^]_j   (dequantization per tile, applied one
 //           tile late, once the P V product has landed)
+// With Q-smoothing the logits gain a term per key of the tile, mean_Q(query block) . K'_k
+// (base 2, precomputed), copied next to V_j and added with the same FMA: t = S_int sQ sK c0 + b_k;
+// pass 1 writes t back over S_int, and pass 2 then adds log2 127 - tmax.
 // Epilogue: O / l as BF16, LSE = (m_ref + log2 l) ln 2.  The quotient does not depend
 // on the reference, so this is the online softmax of the definition.
 #include "kernel_common.cuh"
@@ -53,7 +56,8 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;           // two Q^ tiles
   static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  static constexpr int OFF_BIAS = OFF_V + NS * TILE;  // Q-smoothing logit terms [NS][2 tiles][128]
+  static constexpr int OFF_BAR = OFF_BIAS + NS * 2 * 512;
   static constexpr int NBAR = 1 + 4 * NS + 2 * 4 + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
@@ -64,7 +68,7 @@ struct FwdCfg {
 enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteSFull, kSitePFull, kSitePVDone,
                kSiteOEmpty };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool QSM>
 __global__ void __launch_bounds__(kFThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -152,9 +156,19 @@ __global__ void __launch_bounds__(kFThreads, 1)
           k_issued[s] = n + 1;
         }
         if (j >= NS && !wait1(wc, bar_v_empty + s, (n - 1) & 1, kSiteVEmpty)) break;
-        mbar_arrive_expect_tx(bar_v_full + s, C::TILE);
+        // Q-smoothing: the logit terms of tile j for each query tile that reads it ride on the
+        // V stage, which is released only after both tiles' codes of key tile j are written
+        const int nbias = QSM ? (j < nkb[0]) + (j < nkb[1]) : 0;
+        mbar_arrive_expect_tx(bar_v_full + s, C::TILE + nbias * 512);
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + C::OFF_V + s * C::TILE + c * 16384, &tmV, bar_v_full + s, c * 64, j * kBlk, bhk);
+        if (QSM) {
+          for (int t = 0; t < 2; ++t)
+            if (j < nkb[t])
+              bulk_load_1d(smem + C::OFF_BIAS + (s * 2 + t) * 512,
+                           p.qbias + ((size_t)bhq * p.nb + 2 * pr + t) * ((size_t)p.nb * kBlk) + (size_t)j * kBlk, 512,
+                           bar_v_full + s);
+        }
         v_issued[s] = n + 1;
       }
       // Copies still in flight must land before the CTA's shared memory is released.
@@ -294,30 +308,73 @@ __global__ void __launch_bounds__(kFThreads, 1)
       const int k0 = j * kBlk;
       const bool need_mask = (CAUSAL && j == qb) || (k0 + kBlk > p.N);
       const int kvis = need_mask ? (min(p.N, CAUSAL ? i + 1 : p.N) - k0) : kBlk;  // visible keys of this row
-      // pass 1: row maximum of S_int over the visible keys
-      float smax = -INFINITY;
-      if (need_mask) {
+      const float2 qks2 = make_float2(qks, qks);
+      // Q-smoothing: this tile's logit terms mean_Q . K'_k (base 2), one per key, in shared memory
+      const float* bsm = reinterpret_cast<const float*>(smem + C::OFF_BIAS + ((j % NS) * 2 + t) * 512);
+      float tmax;
+      if constexpr (QSM) {
+        // pass 1: row maximum of t = S_int sQ sK c0 + bias over the visible keys
+        if (!waitw(wc, bar_v_full + (j % NS), (j / NS) & 1, kSiteVFull)) {
+          ok = false;
+          break;
+        }
+        float xmax = -INFINITY;
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(s_addr + c0, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            smax = fmax3(smax, c0 + e < kvis ? __uint_as_float(v[e]) : -INFINITY,
-                         c0 + e + 1 < kvis ? __uint_as_float(v[e + 1]) : -INFINITY);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 b4 = *reinterpret_cast<const float4*>(bsm + c0 + e);
+            const float2 x01 = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), qks2,
+                                     make_float2(b4.x, b4.y));
+            const float2 x23 = ffma2(make_float2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), qks2,
+                                     make_float2(b4.z, b4.w));
+            if (need_mask) {
+              xmax = fmax3(xmax, c0 + e < kvis ? x01.x : -INFINITY, c0 + e + 1 < kvis ? x01.y : -INFINITY);
+              xmax = fmax3(xmax, c0 + e + 2 < kvis ? x23.x : -INFINITY, c0 + e + 3 < kvis ? x23.y : -INFINITY);
+            } else {
+              xmax = fmax3(xmax, x01.x, x01.y);
+              xmax = fmax3(xmax, x23.x, x23.y);
+            }
+            v[e] = __float_as_uint(x01.x);
+            v[e + 1] = __float_as_uint(x01.y);
+            v[e + 2] = __float_as_uint(x23.x);
+            v[e + 3] = __float_as_uint(x23.y);
+          }
+          // the logits replace S_int in TMEM, so that pass 2 only adds the row's offset
+          tmem_st16(s_addr + c0, *reinterpret_cast<const uint32_t(*)[16]>(v));
+          tmem_st16(s_addr + c0 + 16, *reinterpret_cast<const uint32_t(*)[16]>(v + 16));
         }
+        tmem_st_wait();
+        tmax = xmax;
       } else {
+        // pass 1: row maximum of S_int over the visible keys
+        float smax = -INFINITY;
+        if (need_mask) {
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(s_addr + c0, v);
-          tmem_ld_wait();
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(s_addr + c0, v);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) smax = fmax3(smax, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            for (int e = 0; e < 32; e += 2)
+              smax = fmax3(smax, c0 + e < kvis ? __uint_as_float(v[e]) : -INFINITY,
+                           c0 + e + 1 < kvis ? __uint_as_float(v[e + 1]) : -INFINITY);
+          }
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(s_addr + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) smax = fmax3(smax, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+          }
         }
+        tmax = __fmul_rn(smax, qks);
       }
-      const float tmax = __fmul_rn(smax, qks);
       float a = 1.f;
       if (tmax > m_ref + 8.f) {
         a = ex2_approx(m_ref - tmax);
@@ -327,7 +384,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       const float bias = kLog2_127 - tmax;
       // pass 2: codes of P~ written over the S columns already read (chunk c of 32 keys
       // -> 16 packed columns starting at 16c), and the unquantized row sum
-      const float2 qks2 = make_float2(qks, qks), bias2 = make_float2(bias, bias);
+      const float2 bias2 = make_float2(bias, bias);
       const float2 mg = make_float2(12582912.0f, 12582912.0f), nmg = make_float2(-12582912.0f, -12582912.0f);
       float2 usum = make_float2(0.f, 0.f);
 #pragma unroll
@@ -338,7 +395,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), qks2, bias2);
+          const float2 x = QSM ? fadd2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), bias2)
+                               : ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), qks2, bias2);
           float2 u = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (need_mask) {
             if (c0 + e >= kvis) u.x = 0.f;
@@ -387,7 +445,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                          cudaStream_t s) {
   using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL>;
+  auto kern = p.qbias != nullptr ? fwd_kernel<D, CAUSAL, true> : fwd_kernel<D, CAUSAL, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = (p.nb + 1) / 2 * p.B * p.Hq;

@@ -71,6 +71,47 @@ __device__ __forceinline__ int binary_exponent(float a) {
   return biased ? biased - 127 : (31 - __clz((int)u)) - 149;
 }
 
+// Exact channel sums of one thread's rows (u: RPL 16-byte vectors of 8 BF16
+// channels; rows past N were loaded as zeros).  FP32 additions are checked
+// with Knuth's error-free TwoSum (s = a + b, err = (a - (s - (s - a))) +
+// (b - (s - a))); when none of them rounded, the FP32 sums are exact and only
+// they are widened to FP64 -- FP64 is slow on this GPU.  A thread whose values
+// span too wide a range for that re-sums its rows in FP64.  The result is the
+// exact sum either way (for BF16 inputs of ordinary range, where the FP64
+// additions that follow are exact too).
+template <int RPL>
+__device__ __forceinline__ void exact_row_sums(const uint4 (&u)[RPL], double (&acc)[8]) {
+  float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  bool exact = true;
+#pragma unroll
+  for (int i = 0; i < RPL; ++i) {
+    float f[8];
+    unpack8(u[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float t = __fadd_rn(sum[e], f[e]);
+      const float bv = __fsub_rn(t, sum[e]);
+      const float err = __fadd_rn(__fsub_rn(sum[e], __fsub_rn(t, bv)), __fsub_rn(f[e], bv));
+      exact = exact && (err == 0.f);
+      sum[e] = t;
+    }
+  }
+  if (exact) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = (double)sum[e];
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0;
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+      float f[8];
+      unpack8(u[i], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += (double)f[e];
+    }
+  }
+}
+
 // Quantize the 128 x D block (bh, blk) of one tensor.  V8 = D / 8 16-byte vectors per row;
 // a thread keeps one 8-channel group (kThreads is a multiple of V8) over PER rows, holds
 // the raw vectors in registers and unpacks them twice (absmax pass, code pass), which keeps
@@ -78,10 +119,14 @@ __device__ __forceinline__ int binary_exponent(float a) {
 // fac (optional): the channel balancing factors of this head's channels, in shared memory.
 // gred (non-null: Q/K sub-scales): shared scratch [kThreads / 32][D / 8] for the maxima of the
 // 8-channel groups; each group's codes are then refined by 2^k (see below).
-template <int D>
+// BM (Q-smoothing): the block's own channel means are subtracted instead of a head-wide mean
+// and written to bmean[bh][blk][D]; mred / smean are shared scratch [kThreads / 32][D] / [D]
+// for them.
+template <int D, bool BM = false>
 __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xq,
                                float* __restrict__ scale, const float* __restrict__ mean, int bh, int blk, int N,
-                               int nb, float* red, const float* fac = nullptr, float* gred = nullptr) {
+                               int nb, float* red, const float* fac = nullptr, float* gred = nullptr,
+                               float* __restrict__ bmean = nullptr, double* mred = nullptr, float* smean = nullptr) {
   constexpr int V8 = D / 8, RL = kThreads / V8;
   constexpr int PER = kBlk / RL;  // rows (16-byte vectors) per thread
   static_assert(kThreads % V8 == 0 && kBlk % RL == 0, "thread layout");
@@ -94,10 +139,11 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
     mu[k] = mean != nullptr ? mean[(size_t)bh * D + c8 * 8 + k] : 0.f;
     fc[k] = fac != nullptr ? fac[c8 * 8 + k] : 1.f;
   }
-  // K - mean, then times the balancing factor (each an FP32 rounding), as configured
+  const bool sub = BM || mean != nullptr;
+  // x - mean, then times the balancing factor (each an FP32 rounding), as configured
   auto load = [&](const uint4& u, float (&v)[8]) {
     unpack8(u, v);
-    if (mean != nullptr) {
+    if (sub) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) v[k] = __fsub_rn(v[k], mu[k]);
     }
@@ -112,6 +158,35 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
     const int r = rl + e * RL;
     raw[e] = row0 + r < N ? *reinterpret_cast<const uint4*>(x + base + (size_t)r * D + c8 * 8)
                           : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if constexpr (BM) {
+    // Q-smoothing: the channel sums of the block's valid rows (rows past N were loaded as
+    // zeros), exact (FP32 checked by TwoSum, else FP64; the FP64 combination across row lanes
+    // and warps is exact for BF16 inputs of ordinary range), divided in FP64 and rounded to FP32
+    double acc[8];
+    exact_row_sums<PER>(raw, acc);
+#pragma unroll
+    for (int o = V8; o < 32; o <<= 1) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane < V8) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mred[warp * D + lane * 8 + k] = acc[k];
+    }
+    __syncthreads();
+    if (threadIdx.x < D) {
+      double sum = 0.0;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) sum += mred[w * D + threadIdx.x];
+      const float m = __double2float_rn(sum / (double)min(kBlk, N - row0));
+      smean[threadIdx.x] = m;
+      bmean[((size_t)bh * nb + blk) * D + threadIdx.x] = m;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mu[k] = smean[c8 * 8 + k];
   }
   float amax = 0.f;
 #pragma unroll
@@ -177,8 +252,8 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
   if (threadIdx.x == 0) scale[(size_t)bh * nb + blk] = live ? __fdiv_rn(a, 127.f) : 0.f;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 4) quantize_kernel(const QuantParams p) {
+template <int D, bool BM>
+__global__ void __launch_bounds__(kThreads, BM ? 2 : 4) quantize_kernel(const QuantParams p) {
   __shared__ float red[kThreads / 32];
   __shared__ float fac[D];
   __shared__ float gred[kThreads / 32 * (D / 8)];
@@ -192,49 +267,18 @@ __global__ void __launch_bounds__(kThreads, 4) quantize_kernel(const QuantParams
     if (threadIdx.x < D) fac[threadIdx.x] = exp2_int(job.bexp_sign * job.bexp[(bh / job.bexp_group) * D + threadIdx.x]);
     __syncthreads();  // quantize_block reads fac only after this
   }
+  if constexpr (BM) {
+    __shared__ double mred[kThreads / 32 * D];
+    __shared__ float smean[D];
+    if (job.bmean != nullptr) {
+      quantize_block<D, true>(job.x, job.xq, job.scale, job.mean, bh, local % p.nb, p.N, p.nb, red,
+                              job.bexp != nullptr ? fac : nullptr, job.subexp ? gred : nullptr, job.bmean, mred,
+                              smean);
+      return;
+    }
+  }
   quantize_block<D>(job.x, job.xq, job.scale, job.mean, bh, local % p.nb, p.N, p.nb, red,
                     job.bexp != nullptr ? fac : nullptr, job.subexp ? gred : nullptr);
-}
-
-// Exact channel sums of one thread's rows (u: RPL 16-byte vectors of 8 BF16
-// channels; rows past N were loaded as zeros).  FP32 additions are checked
-// with Knuth's error-free TwoSum (s = a + b, err = (a - (s - (s - a))) +
-// (b - (s - a))); when none of them rounded, the FP32 sums are exact and only
-// they are widened to FP64 -- FP64 is slow on this GPU.  A thread whose values
-// span too wide a range for that re-sums its rows in FP64.  The result is the
-// exact sum either way (for BF16 inputs of ordinary range, where the FP64
-// additions that follow are exact too).
-template <int RPL>
-__device__ __forceinline__ void exact_row_sums(const uint4 (&u)[RPL], double (&acc)[8]) {
-  float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  bool exact = true;
-#pragma unroll
-  for (int i = 0; i < RPL; ++i) {
-    float f[8];
-    unpack8(u[i], f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float t = __fadd_rn(sum[e], f[e]);
-      const float bv = __fsub_rn(t, sum[e]);
-      const float err = __fadd_rn(__fsub_rn(sum[e], __fsub_rn(t, bv)), __fsub_rn(f[e], bv));
-      exact = exact && (err == 0.f);
-      sum[e] = t;
-    }
-  }
-  if (exact) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = (double)sum[e];
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.0;
-#pragma unroll
-    for (int i = 0; i < RPL; ++i) {
-      float f[8];
-      unpack8(u[i], f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += (double)f[e];
-    }
-  }
 }
 
 // Channel statistics of one 128-token block of one head.  Blocks with
@@ -447,6 +491,65 @@ __global__ void __launch_bounds__(kFinalSlices * 32) kmean_final_kernel(const do
 // Backward preprocess for one 128-query block: D_i = sum_c dO[i,c] O[i,c]
 // (FP32), the dO block quantization, and zeroing the block's rows of the FP32
 // dQ accumulator.
+// Q-smoothing's logit terms ("SageBwd: A Trainable Low-bit Attention", Abstract, finding
+// (iv); the library's reading of the optional Q-smoothing): with Q = (Q - mean_Q) + mean_Q per
+// 128-token block, S = Q K'^T gains mean_Q(block of i) . K'_k, which depends on the query only
+// through its block.  Thread k of CTA (key block jb, query head bhq) holds K'_k = K_k - mean_K
+// (one FP32 rounding each; K itself without smoothing) in registers and writes, for every
+// query block ib that sees key block jb, c0 * (mean_Q(bhq, ib) . K'_k): FP32 products summed in
+// four interleaved partial sums, times c0 (the logits' base-2 units).  Keys past N get 0.  The
+// means of kQB query blocks at a time are staged in shared memory (broadcast reads) and their
+// kQB dot products run as independent chains.
+constexpr int kQB = 8;
+template <int D>
+__global__ void __launch_bounds__(kBlk) qsmooth_bias_kernel(const QBiasParams p) {
+  __shared__ float4 msm[kQB * D / 4];
+  const int jb = blockIdx.x, bhq = blockIdx.y;
+  const int key = jb * kBlk + threadIdx.x;
+  const int bhk = bhq / p.G;  // b Hq + h -> b Hkv + h / G
+  const size_t np = (size_t)p.nb * kBlk;
+  const bool live = key < p.N;
+  float kr[D];
+#pragma unroll
+  for (int v = 0; v < D / 8; ++v) {
+    float f[8];
+    if (live) {
+      unpack8(*reinterpret_cast<const uint4*>(p.k + ((size_t)bhk * p.N + key) * D + v * 8), f);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) kr[v * 8 + e] = p.kmean != nullptr ? __fsub_rn(f[e], p.kmean[(size_t)bhk * D + v * 8 + e]) : f[e];
+  }
+  const float4* mg = reinterpret_cast<const float4*>(p.qmean + (size_t)bhq * p.nb * D);
+  for (int ib0 = p.causal ? jb : 0; ib0 < p.nb; ib0 += kQB) {
+    const int nq = min(kQB, p.nb - ib0);
+    __syncthreads();  // the previous chunk's means have been read
+    for (int e = threadIdx.x; e < nq * D / 4; e += kBlk) msm[e] = mg[(size_t)ib0 * D / 4 + e];
+    __syncthreads();
+    float acc[kQB][4];
+#pragma unroll
+    for (int q = 0; q < kQB; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+#pragma unroll
+    for (int c4 = 0; c4 < D / 4; ++c4) {
+#pragma unroll
+      for (int q = 0; q < kQB; ++q) {
+        const float4 m = msm[q * D / 4 + c4];  // rows past nq hold stale values; not stored
+        acc[q][0] = fmaf(m.x, kr[4 * c4], acc[q][0]);
+        acc[q][1] = fmaf(m.y, kr[4 * c4 + 1], acc[q][1]);
+        acc[q][2] = fmaf(m.z, kr[4 * c4 + 2], acc[q][2]);
+        acc[q][3] = fmaf(m.w, kr[4 * c4 + 3], acc[q][3]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kQB; ++q)
+      if (q < nq)
+        p.bias[((size_t)bhq * p.nb + ib0 + q) * np + key] =
+            live ? __fmul_rn((acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]), p.c0) : 0.f;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const PrepParams p) {
   __shared__ float red[kThreads / 32];
@@ -528,10 +631,13 @@ __global__ void grad_convert_kernel(const ConvertJobs J) {
 cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s) {
   const int blocks = p.block_start[p.njobs];
   if (blocks == 0) return cudaSuccess;
+  bool bm = false;  // Q-smoothing's block means: a separate instantiation
+  for (int j = 0; j < p.njobs; ++j) bm = bm || p.job[j].bmean != nullptr;
   if (p.d == 64)
-    quantize_kernel<64><<<blocks, kThreads, 0, s>>>(p);
+    bm ? quantize_kernel<64, true><<<blocks, kThreads, 0, s>>>(p) : quantize_kernel<64, false><<<blocks, kThreads, 0, s>>>(p);
   else
-    quantize_kernel<128><<<blocks, kThreads, 0, s>>>(p);
+    bm ? quantize_kernel<128, true><<<blocks, kThreads, 0, s>>>(p)
+       : quantize_kernel<128, false><<<blocks, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -585,6 +691,15 @@ cudaError_t launch_grad_convert(const ConvertJob* jobs, int njobs, cudaStream_t 
   const size_t want = (n4 + 255) / 256;
   const int blocks = (int)(want < (size_t)sms * 8 ? want : (size_t)sms * 8);
   grad_convert_kernel<<<blocks, 256, 0, s>>>(J);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qsmooth_bias(const QBiasParams& p, cudaStream_t s) {
+  const dim3 grid(p.nb, p.BHq);
+  if (p.d == 64)
+    qsmooth_bias_kernel<64><<<grid, kBlk, 0, s>>>(p);
+  else
+    qsmooth_bias_kernel<128><<<grid, kBlk, 0, s>>>(p);
   return cudaGetLastError();
 }
 

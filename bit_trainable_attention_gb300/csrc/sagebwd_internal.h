@@ -36,6 +36,8 @@ struct QuantJob {
   int bexp_group;          // heads per exponent row: Hq/Hkv for Q, 1 for K
   int bexp_sign;           // -1: x times 2^-e (Q); +1: x times 2^e (K)
   int subexp;              // 1: power-of-two sub-scales per 8-channel group of each block (Q/K option)
+  float* bmean;            // [BH][nb][d] or nullptr: Q-smoothing, each block's channel means subtracted
+                           // first (and written here)
 };
 struct QuantParams {
   QuantJob job[3];
@@ -63,6 +65,17 @@ struct StatsParams {
   int* status;             // cleared by the first block
 };
 cudaError_t launch_qk_stats(const StatsParams& p, cudaStream_t s);
+// Q-smoothing's logit terms bias[bhq][ib][k] = c0 * (mean_Q(bhq, ib) . K'_k), K' = K - mean_K
+// (kmean non-null) or K, for every key k < 128 * nb (0 past N); causal: only ib >= k / 128.
+struct QBiasParams {
+  const __nv_bfloat16* k;  // [B*Hkv][N][d]
+  const float* kmean;      // [B*Hkv][d] or nullptr
+  const float* qmean;      // [B*Hq][nb][d]
+  float* bias;             // [B*Hq][nb][128 nb]
+  int BHq, G, N, d, nb, causal;
+  float c0;
+};
+cudaError_t launch_qsmooth_bias(const QBiasParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ backward helpers
 struct PrepParams {
@@ -99,6 +112,7 @@ struct FwdParams {
   const float* sv;
   __nv_bfloat16* o;
   float* lse;
+  const float* qbias;  // Q-smoothing logit terms [BHq][nb][128 nb] (base 2), or nullptr
   int* status;
   uint64_t timeout_ns;
   uint32_t flags;
@@ -123,6 +137,12 @@ struct BwdParams {
   // has to be applied afterwards: dK, dV are then written as BF16 here, not accumulated
   __nv_bfloat16* dk_out;  // [BHk][N][d]
   __nv_bfloat16* dv_out;  // [BHk][N][d]
+  // Q-smoothing (all three non-null, or all null): the logit terms [BHq][nb][128 nb], the block
+  // means of Q [BHq][nb][d], and scratch for the per-slice column sums of the dS codes
+  // [grid][2][4][128]
+  const float* qbias;
+  const float* qmean;
+  float* cs_part;
   int* status;
   uint64_t timeout_ns;
   uint32_t flags;

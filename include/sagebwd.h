@@ -42,6 +42,18 @@
  * below 2^-100): code = rint(dS * 127/max * 2^k), operand value code * 2^-k,
  * exact in BF16, read as is by dK = dS^T Q and dQ = dS K (their FP32 sums are
  * then no longer exact integers, but rounding there is at the 2^-24 level).
+ * Optional Q-smoothing (smooth_q = 1; off by default; the SageBwd page calls
+ * it optional with limited benefit, Abstract, finding (iv)): each 128-token
+ * block of each query head subtracts its FP32 channel means mean_Q (exact sum
+ * over the block's tokens, divided, rounded to FP32) before quantizing, and
+ * the logits gain the FP32 term mean_Q(block of i) . K'_k (K' the K that the
+ * quantizer sees: K - mean_K with smooth_k), so S = Q K'^T is unchanged up to
+ * quantization.  The backward adds the same term to the recomputed S and, for
+ * dK = dS^T (Q - mean_Q + mean_Q), the block mean's share: per tile
+ * scale * s_dS * (sum over the tile's queries of the dS codes) * mean_Q.  dQ
+ * needs no correction.  Not combined with balance_qk (SAGEBWD_ERR_UNSUPPORTED);
+ * sagebwd_quantize returns SAGEBWD_ERR_UNSUPPORTED for Q under it (its codes
+ * come with block means, which only sagebwd_fwd_quantize stores).
  * The INT8 codes are held as integer-valued BF16 and multiplied on the
  * tensor cores with FP32 accumulation, which is exact for these tiles
  * (|sum| <= 128 * 127^2 < 2^24).
@@ -95,6 +107,7 @@ typedef struct {
   int32_t balance_qk;   /* 1: power-of-two Q/K channel balancing before quantizing (see above); 0 in the method */
   int32_t ds_subexp;    /* 1: dS sub-scales per key and 32-query group (see above); 0: one dS scale per tile */
   int32_t qk_subexp;    /* 1: Q/K sub-scales per 8-channel group of each block (see above); 0: block scale only */
+  int32_t smooth_q;     /* 1: Q-smoothing, block means of Q subtracted (see above); 0: plain Q (the default) */
   uint32_t flags;       /* SAGEBWD_FLAG_* (0 in normal use) */
   float softmax_scale;  /* <= 0 selects 1/sqrt(d) */
   uint32_t wait_timeout_ms; /* bound of every in-kernel wait; 0 selects 2000 ms */
@@ -102,16 +115,20 @@ typedef struct {
 
 /* Bytes of the `saved` buffer that sagebwd_fwd fills and sagebwd_bwd reads:
  * the quantized Q, K, V (integer-valued BF16, same shapes as the inputs),
- * their FP32 block scales, the FP32 mean of K [B*Hkv][d] and the int32
- * balancing exponents [B*Hkv][d] (written only with balance_qk), each section
- * starting on a 256-byte boundary.  Returns 0 for an invalid problem. */
+ * their FP32 block scales, the FP32 mean of K [B*Hkv][d], the int32
+ * balancing exponents [B*Hkv][d] (written only with balance_qk) and, with
+ * smooth_q, the FP32 block means of Q [B*Hq][ceil(N/128)][d] and the FP32
+ * logit terms mean_Q . K' [B*Hq][ceil(N/128)][128 * ceil(N/128)] (in base-2
+ * units, times scale * log2 e), each section starting on a 256-byte
+ * boundary.  Returns 0 for an invalid problem. */
 size_t sagebwd_saved_bytes(const sagebwd_problem* prob);
 
 /* Bytes of workspace for pass 0 (forward, sagebwd_fwd / sagebwd_quantize) or
  * pass 1 (backward, sagebwd_bwd).  The workspace holds the status word first,
  * then scratch (K-mean partial sums, and with balance_qk the per-block channel
  * maxima of Q and K; D = rowsum(dO*O), the quantized dO and its scales, the
- * FP32 dQ, dK and dV accumulators).  Contents need no initialisation and are
+ * FP32 dQ, dK and dV accumulators, and with smooth_q a small ring of dS column
+ * sums per backward CTA).  Contents need no initialisation and are
  * not meaningful between calls, except the status word. */
 size_t sagebwd_workspace_bytes(const sagebwd_problem* prob, int pass);
 

@@ -81,10 +81,11 @@ def device_inputs(w, dev="cuda"):
     return x, {k: v.to(dev) for k, v in x.items()}
 
 
-def gpu_forward(w, xd, smooth_k=True, flags=0, timeout_ms=0, balance_qk=False, ds_subexp=False, qk_subexp=False):
+def gpu_forward(w, xd, smooth_k=True, flags=0, timeout_ms=0, balance_qk=False, ds_subexp=False, qk_subexp=False,
+                smooth_q=False):
     prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_k=smooth_k, flags=flags,
                            wait_timeout_ms=timeout_ms, balance_qk=balance_qk, ds_subexp=ds_subexp,
-                           qk_subexp=qk_subexp)
+                           qk_subexp=qk_subexp, smooth_q=smooth_q)
     dev = xd["q"].device
     o = torch.empty_like(xd["q"])
     lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
@@ -107,9 +108,9 @@ def gpu_backward(w, xd, fwd):
     return {"dq": dq, "dk": dk, "dv": dv, "ws": ws, "status": code, "word": word}
 
 
-def oracle_problem(oracle_mod, w, smooth_k=True, balance_qk=False, ds_subexp=False, qk_subexp=False):
+def oracle_problem(oracle_mod, w, smooth_k=True, balance_qk=False, ds_subexp=False, qk_subexp=False, smooth_q=False):
     return oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_k=smooth_k, balance_qk=balance_qk,
-                              ds_subexp=ds_subexp, qk_subexp=qk_subexp)
+                              ds_subexp=ds_subexp, qk_subexp=qk_subexp, smooth_q=smooth_q)
 
 
 def block_selection(w, heads, blocks, kv=False):

@@ -101,3 +101,22 @@ def test_balancing_sizes_and_rejections(lib):
     odd = ctypes.c_void_p((1 << 20) + 4)
     assert lib.sagebwd_bwd_finish(ctypes.byref(p1), odd, fake, fake, fake, fake, None) == 3
     assert lib.sagebwd_bwd_finish(ctypes.byref(p1), None, fake, fake, fake, fake, None) == 1
+
+
+def test_q_smoothing_sizes_and_rejections(lib):
+    """With smooth_q the saved buffer adds the block means of Q and the logit terms, the backward
+    workspace a ring of dS column sums per CTA; balancing together with it, and the single-operand
+    quantizer for Q under it, are refused before any launch."""
+    p0 = sb.Problem.make(2, 4, 2, 300, 64, True)
+    p1 = sb.Problem.make(2, 4, 2, 300, 64, True, smooth_q=True)
+    nb = 3
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert sb.sagebwd_saved_bytes(p1) == sb.sagebwd_saved_bytes(p0) + al(2 * 4 * nb * 64 * 4) + al(
+        2 * 4 * nb * nb * 128 * 4)
+    assert sb.sagebwd_workspace_bytes(p1, 0) == sb.sagebwd_workspace_bytes(p0, 0)
+    assert sb.sagebwd_workspace_bytes(p1, 1) == sb.sagebwd_workspace_bytes(p0, 1) + al(2 * 4 * nb * 2 * 4 * 128 * 4)
+    both = sb.Problem.make(2, 4, 2, 300, 64, True, smooth_q=True, balance_qk=True)
+    assert sb.sagebwd_saved_bytes(both) == 0 and sb.sagebwd_workspace_bytes(both, 1) == 0
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the calls return before any launch
+    assert lib.sagebwd_quantize(ctypes.byref(p1), sb.SAGEBWD_Q, fake, fake, fake, fake, fake, None) == 2
+    assert lib.sagebwd_fwd(ctypes.byref(both), fake, fake, fake, fake, fake, fake, fake, None) == 2
