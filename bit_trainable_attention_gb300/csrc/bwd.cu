@@ -628,7 +628,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (it + 1 < T) sq_next = p.sq[(size_t)tile_bhq(it + 1) * p.nb + tile_ib(it + 1)];
       // Q-smoothing: this warpgroup's half of mean_Q(tile's query block) into L1 now, read at
       // the end of the tile (a quarter of a line per lane group: lanes 0..DH/32-1 of each warp)
-      if (QSM && lane < DH / 32)
+      if (QSM && C::ALIAS && lane < DH / 32)  // (on d = 64 the prefetch measured slower)
         prefetch_l1(p.qmean + ((size_t)tile_bhq(it) * p.nb + tile_ib(it)) * D + wa * DH + lane * 32);
       if (!waitw(wc, bar_acc_v, it & 1, bSiteAccV)) break;
       // the tile's scales were stored before the P^T codes were released
