@@ -43,8 +43,8 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # the one-pass ncu capture summarised in profiles/bwd_kernel_qwen15b_ncu.md.  The
 # figure belongs to the kernel sources it was taken from: once any of them changes
 # the line reports null until the capture is repeated.
-BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1329297920 + 517759232,
-               "sources_sha256": "2ff53da927d7e0a434d2d4391dcefa8406b75d21723b9028ff1cc58b3ce6d3a2"}
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1329221632 + 516835584,
+               "sources_sha256": "32628836b291ee4fd85b1ac81b9fcc1f63dc55f91dc1057e50be90b8e2caa546"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
