@@ -4,6 +4,7 @@
 // sagebwd_check_status).
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -282,9 +283,15 @@ int heads_per_cta(const sagebwd_problem* p) {
   static Key keys[16];
   static int vals[16];
   static int used = 0, next = 0;
+  static std::atomic<int> sm_count[64];  // per device, queried once (zero until then)
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64 && sm_count[dev].load(std::memory_order_relaxed) > 0) {
+    sms = sm_count[dev].load(std::memory_order_relaxed);
+  } else {
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && dev < 64) sm_count[dev].store(sms, std::memory_order_relaxed);
+  }
   const Key k{p->B, p->Hkv, p->Hq / p->Hkv, nblocks(p->N), p->causal ? 1 : 0, sms};
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < used; ++i)
@@ -301,9 +308,10 @@ int heads_per_cta(const sagebwd_problem* p) {
 // (all G query heads of a kv head in one CTA) and no factor follows (channel
 // balancing multiplies dK at the conversion): no FP32 accumulators to zero,
 // reduce or convert.
-bool direct_dkdv(const sagebwd_problem* p) { return !p->balance_qk && heads_per_cta(p) == p->Hq / p->Hkv; }
+bool direct_dkdv(const sagebwd_problem* p, int hs) { return !p->balance_qk && hs == p->Hq / p->Hkv; }
 
-sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const void* dO, void* ws, cudaStream_t st) {
+sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const void* dO, void* ws, cudaStream_t st,
+                                int hs) {
   const WsLayout W = ws_layout(p, 1);
   PrepParams pp{};
   pp.o = static_cast<const __nv_bfloat16*>(o);
@@ -315,7 +323,7 @@ sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const v
   pp.dk_acc = at<float>(ws, W.dkacc);
   pp.dv_acc = at<float>(ws, W.dvacc);
   pp.BH = p->B * p->Hq;
-  pp.BHk = direct_dkdv(p) ? 0 : p->B * p->Hkv;  // the dK / dV accumulators to zero
+  pp.BHk = direct_dkdv(p, hs) ? 0 : p->B * p->Hkv;  // the dK / dV accumulators to zero
   pp.N = p->N;
   pp.d = p->d;
   pp.nb = nblocks(p->N);
@@ -324,7 +332,7 @@ sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const v
 }
 
 sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const void* dO, const float* lse,
-                                  const void* saved, void* dk, void* dv, void* ws, cudaStream_t st) {
+                                  const void* saved, void* dk, void* dv, void* ws, cudaStream_t st, int hs) {
   const SavedLayout S = saved_layout(p);
   const WsLayout W = ws_layout(p, 1);
   CUtensorMap tq, tk, tv, tdo, tdoq, tdq;
@@ -334,7 +342,7 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
       !make_map(&tdoq, at<uint8_t>(ws, W.dOq), p->B * p->Hq, p->N, p->d) ||
       !make_map_f32(&tdq, at<uint8_t>(ws, W.dqacc), p->B * p->Hq, p->N, p->d))
     return SAGEBWD_ERR_CUDA;
-  BwdParams bp{};
+  BwdQsmParams bp{};
   bp.B = p->B;
   bp.Hq = p->Hq;
   bp.Hkv = p->Hkv;
@@ -348,13 +356,11 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
   bp.sdo = at<float>(ws, W.sdo);
   bp.lse = lse;
   bp.D = at<float>(ws, W.D);
-  bp.HS = heads_per_cta(p);
+  bp.HS = hs;
   bp.dq_acc = at<float>(ws, W.dqacc);
-  bp.dk_acc = at<float>(ws, W.dkacc);
-  bp.dv_acc = at<float>(ws, W.dvacc);
-  const bool direct = direct_dkdv(p);
-  bp.dk_out = direct ? static_cast<__nv_bfloat16*>(dk) : nullptr;
-  bp.dv_out = direct ? static_cast<__nv_bfloat16*>(dv) : nullptr;
+  const bool direct = direct_dkdv(p, hs);
+  bp.dk_dst = direct ? dk : static_cast<void*>(at<float>(ws, W.dkacc));
+  bp.dv_dst = direct ? dv : static_cast<void*>(at<float>(ws, W.dvacc));
   if (p->smooth_q) {
     bp.qbias = at<float>(saved, S.qb);
     bp.qmean = at<float>(saved, S.qm);
@@ -362,12 +368,12 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
   }
   bp.status = at<int>(ws, W.status);
   bp.timeout_ns = timeout_of(p);
-  bp.flags = p->flags;
+  bp.flags = (p->flags & ~kBwdDirectDKDV) | (direct ? kBwdDirectDKDV : 0u);
   return cuda_status(launch_bwd(tq, tk, tv, tdo, tdoq, tdq, bp, p->d, p->causal, p->ds_subexp ? 1 : 0, st));
 }
 
 sagebwd_status bwd_finish_impl(const sagebwd_problem* p, const void* saved, void* dq, void* dk, void* dv, void* ws,
-                               cudaStream_t st) {
+                               cudaStream_t st, int hs) {
   const WsLayout W = ws_layout(p, 1);
   const size_t nq = (size_t)p->B * p->Hq * p->N * p->d, nk = (size_t)p->B * p->Hkv * p->N * p->d;
   // with channel balancing: dQ = dS (K 2^e) 2^-e and dK = dS^T (Q 2^-e) 2^e
@@ -376,7 +382,7 @@ sagebwd_status bwd_finish_impl(const sagebwd_problem* p, const void* saved, void
       {at<float>(ws, W.dqacc), static_cast<__nv_bfloat16*>(dq), nq, bexp, -1, p->Hq / p->Hkv, p->N, p->d},
       {at<float>(ws, W.dkacc), static_cast<__nv_bfloat16*>(dk), nk, bexp, 1, 1, p->N, p->d},
       {at<float>(ws, W.dvacc), static_cast<__nv_bfloat16*>(dv), nk, nullptr, 1, 1, p->N, p->d}};
-  return cuda_status(launch_grad_convert(jobs, direct_dkdv(p) ? 1 : 3, st));  // dK, dV written directly
+  return cuda_status(launch_grad_convert(jobs, direct_dkdv(p, hs) ? 1 : 3, st));  // dK, dV written directly
 }
 
 }  // namespace
@@ -454,21 +460,22 @@ sagebwd_status sagebwd_bwd_prepare(const sagebwd_problem* prob, const void* o, c
                                    void* stream) {
   SB_CHECK(check_problem(prob));
   SB_CHECK(check_ptrs({o, dO, ws}));
-  return bwd_prepare_impl(prob, o, dO, ws, static_cast<cudaStream_t>(stream));
+  return bwd_prepare_impl(prob, o, dO, ws, static_cast<cudaStream_t>(stream), heads_per_cta(prob));
 }
 
 sagebwd_status sagebwd_bwd_attention(const sagebwd_problem* prob, const void* v, const void* dO, const float* lse,
                                      const void* saved, void* dk, void* dv, void* ws, void* stream) {
   SB_CHECK(check_problem(prob));
   SB_CHECK(check_ptrs({v, dO, lse, saved, dk, dv, ws}));
-  return bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, static_cast<cudaStream_t>(stream));
+  return bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, static_cast<cudaStream_t>(stream),
+                            heads_per_cta(prob));
 }
 
 sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, const void* saved, void* dq, void* dk, void* dv,
                                   void* ws, void* stream) {
   SB_CHECK(check_problem(prob));
   SB_CHECK(check_ptrs({saved, dq, dk, dv, ws}));
-  return bwd_finish_impl(prob, saved, dq, dk, dv, ws, static_cast<cudaStream_t>(stream));
+  return bwd_finish_impl(prob, saved, dq, dk, dv, ws, static_cast<cudaStream_t>(stream), heads_per_cta(prob));
 }
 
 sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const void* k, const void* v, const void* o,
@@ -477,9 +484,10 @@ sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const voi
   SB_CHECK(check_problem(prob));
   SB_CHECK(check_ptrs({q, k, v, o, dO, lse, saved, dq, dk, dv, ws}));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  SB_CHECK(bwd_prepare_impl(prob, o, dO, ws, st));
-  SB_CHECK(bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, st));
-  return bwd_finish_impl(prob, saved, dq, dk, dv, ws, st);
+  const int hs = heads_per_cta(prob);
+  SB_CHECK(bwd_prepare_impl(prob, o, dO, ws, st, hs));
+  SB_CHECK(bwd_attention_impl(prob, v, dO, lse, saved, dk, dv, ws, st, hs));
+  return bwd_finish_impl(prob, saved, dq, dk, dv, ws, st, hs);
 }
 
 sagebwd_status sagebwd_check_status(const void* ws, void* stream, int32_t* detail) {

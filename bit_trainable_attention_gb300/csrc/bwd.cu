@@ -117,12 +117,22 @@ enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty,
                bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAccV, bSiteAccQ, bSiteAccK, bSiteTmemFreeV, bSiteDVQFree,
                bSiteTmemFreeK, bSiteStaged, bSiteStgFree, bSiteC1, bSiteC2, bSiteC3, bSiteAlign };
 
+// The plain instantiations take BwdParams (128 bytes), the Q-smoothing ones BwdQsmParams.
+template <bool QSM>
+struct BwdParamsOf {
+  using type = BwdParams;
+};
+template <>
+struct BwdParamsOf<true> {
+  using type = BwdQsmParams;
+};
+
 template <int D, bool CAUSAL, bool DSX, bool QSM>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmDOQ, const __grid_constant__ CUtensorMap tmDQ,
-               const BwdParams p) {
+               const typename BwdParamsOf<QSM>::type p) {
   using C = BwdCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -406,7 +416,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     auto tile_sdo = [&](int t) { return p.sdo[(size_t)tile_bhq(t) * p.nb + tile_ib(t)]; };
     // Q-smoothing: the logit term mean_Q(tile's query block) . K'_r of this thread's key
     auto tile_bias = [&](int t) -> float {
-      return QSM ? p.qbias[((size_t)tile_bhq(t) * p.nb + tile_ib(t)) * ((size_t)p.nb * kBlk) + k0 + r] : 0.f;
+      if constexpr (QSM)
+        return p.qbias[((size_t)tile_bhq(t) * p.nb + tile_ib(t)) * ((size_t)p.nb * kBlk) + k0 + r];
+      else
+        return 0.f;
     };
     float pf_vec = tile_vec(0), pf_sq = tile_sq(0), pf_sdo = tile_sdo(0), pf_bias = tile_bias(0);
     const float2 kMagic2 = make_float2(12582912.0f, 12582912.0f), kNegMagic2 = make_float2(-12582912.0f, -12582912.0f);
@@ -604,7 +617,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                          v[4 * h + 3]);
         }
       }
-      if (QSM) p.cs_part[(((size_t)blockIdx.x * 2 + (it & 1)) * C::SWG + ws) * 128 + r] = csum.x + csum.y;
+      if constexpr (QSM) p.cs_part[(((size_t)blockIdx.x * 2 + (it & 1)) * C::SWG + ws) * 128 + r] = csum.x + csum.y;
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar_ds_ready);
@@ -628,8 +641,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (it + 1 < T) sq_next = p.sq[(size_t)tile_bhq(it + 1) * p.nb + tile_ib(it + 1)];
       // Q-smoothing: this warpgroup's half of mean_Q(tile's query block) into L1 now, read at
       // the end of the tile (a quarter of a line per lane group: lanes 0..DH/32-1 of each warp)
-      if (QSM && C::ALIAS && lane < DH / 32)  // (on d = 64 the prefetch measured slower)
-        prefetch_l1(p.qmean + ((size_t)tile_bhq(it) * p.nb + tile_ib(it)) * D + wa * DH + lane * 32);
+      if constexpr (QSM && C::ALIAS) {  // (on d = 64 the prefetch measured slower)
+        if (lane < DH / 32)
+          prefetch_l1(p.qmean + ((size_t)tile_bhq(it) * p.nb + tile_ib(it)) * D + wa * DH + lane * 32);
+      }
       if (!waitw(wc, bar_acc_v, it & 1, bSiteAccV)) break;
       // the tile's scales were stored before the P^T codes were released
       if (!waitw(wc, bar_pt_ready, it & 1, bSitePTReady)) break;
@@ -668,7 +683,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(bar_tmem_free_k);
-      if (QSM) {
+      if constexpr (QSM) {
         // Q-smoothing, while dQ(i) runs: dK_r += scale s_dS (sum over the tile's queries of the dS
         // operand values) mean_Q(block i); the slices' column sums were stored before dS was
         // released
@@ -721,11 +736,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     if (!*abort_flag && kglob < p.N) {
       const size_t row = ((size_t)bhk * p.N + kglob) * D + wa * DH;
-      if (p.dk_out != nullptr) {
+      if (p.flags & kBwdDirectDKDV) {
         // the only CTA of this key block: dK_j, dV_j (row kglob, columns [wa d/2, (wa+1) d/2))
         // rounded to BF16 as the conversion kernel would round the FP32 sums
-        uint4* dko = reinterpret_cast<uint4*>(p.dk_out + row);
-        uint4* dvo = reinterpret_cast<uint4*>(p.dv_out + row);
+        uint4* dko = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk_dst) + row);
+        uint4* dvo = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv_dst) + row);
 #pragma unroll
         for (int c = 0; c < DH; c += 8) {
           const int h = c >> 1;
@@ -740,8 +755,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
       } else {
         // this CTA's share of dK_j, dV_j into the FP32 sums
-        float* dka = p.dk_acc + row;
-        float* dva = p.dv_acc + row;
+        float* dka = static_cast<float*>(p.dk_dst) + row;
+        float* dva = static_cast<float*>(p.dv_dst) + row;
 #pragma unroll
         for (int c = 0; c < DH; c += 4) {
           const int h = c >> 1;
@@ -763,20 +778,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
 template <int D, bool CAUSAL, bool DSX>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                         const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s) {
+                         const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdQsmParams& p, cudaStream_t s) {
   using C = BwdCfg<D>;
-  auto kern = p.qbias != nullptr ? bwd_kernel<D, CAUSAL, DSX, true> : bwd_kernel<D, CAUSAL, DSX, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
   const int grid = p.nb * p.B * p.Hkv * (p.G / p.HS);
-  kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, p);
+  if (p.qbias != nullptr) {
+    auto kern = bwd_kernel<D, CAUSAL, DSX, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, p);
+  } else {
+    auto kern = bwd_kernel<D, CAUSAL, DSX, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, static_cast<const BwdParams&>(p));
+  }
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, int d, int causal,
+                       const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdQsmParams& p, int d, int causal,
                        int ds_subexp, cudaStream_t s) {
 #define SAGEBWD_BWD_CASE(D_, C_)                                                                  \
   if (d == D_ && (causal != 0) == C_)                                                             \

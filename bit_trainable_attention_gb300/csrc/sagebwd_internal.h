@@ -120,6 +120,7 @@ struct FwdParams {
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                        int d, int causal, cudaStream_t s);
 
+// Kept at 128 bytes: a larger parameter block made ptxas spill in the d = 64 kernels.
 struct BwdParams {
   int B, Hq, Hkv, N, nb, G;
   float c0;        // softmax_scale * log2(e)
@@ -130,27 +131,29 @@ struct BwdParams {
   const float* lse; // [BHq][N]
   const float* D;   // [BHq][N]
   int HS;           // query heads per CTA (a divisor of G)
+  uint32_t flags;   // SAGEBWD_FLAG_* | kBwdDirectDKDV
   float* dq_acc;    // [BHq][N][d]
-  float* dk_acc;    // [BHk][N][d]
-  float* dv_acc;    // [BHk][N][d]
-  // non-null when one CTA covers all G query heads of its key block (HS == G) and no factor
-  // has to be applied afterwards: dK, dV are then written as BF16 here, not accumulated
-  __nv_bfloat16* dk_out;  // [BHk][N][d]
-  __nv_bfloat16* dv_out;  // [BHk][N][d]
-  // Q-smoothing (all three non-null, or all null): the logit terms [BHq][nb][128 nb], the block
-  // means of Q [BHq][nb][d], and scratch for the per-slice column sums of the dS codes
-  // [grid][2][4][128]
+  // dK, dV destinations [BHk][N][d]: FP32 accumulators (added into), or, with kBwdDirectDKDV
+  // (one CTA covers all G query heads of its key block and no factor follows), the BF16 outputs
+  void* dk_dst;
+  void* dv_dst;
+  int* status;
+  uint64_t timeout_ns;
+};
+constexpr uint32_t kBwdDirectDKDV = 1u << 31;
+static_assert(sizeof(BwdParams) <= 128, "backward parameter block above 128 bytes");
+// The Q-smoothing instantiations take these extra tables: the logit terms [BHq][nb][128 nb], the
+// block means of Q [BHq][nb][d], and scratch for the per-slice column sums of the dS codes
+// [grid][2][4][128].
+struct BwdQsmParams : BwdParams {
   const float* qbias;
   const float* qmean;
   float* cs_part;
-  int* status;
-  uint64_t timeout_ns;
-  uint32_t flags;
 };
+// p.qbias == nullptr selects the plain instantiations (which take only the BwdParams part).
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdParams& p, int d, int causal,
-                       int ds_subexp,
-                       cudaStream_t s);
+                       const CUtensorMap& tdoq, const CUtensorMap& tdq, const BwdQsmParams& p, int d, int causal,
+                       int ds_subexp, cudaStream_t s);
 // Query heads per backward CTA: the divisor of G whose CTAs, dispatched longest
 // first onto `sms` multiprocessors, finish soonest (ties: more heads per CTA).
 int bwd_heads_per_cta(int B, int Hkv, int G, int nb, int causal, int sms);
