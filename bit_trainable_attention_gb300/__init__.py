@@ -23,11 +23,13 @@ __all__ = [
     "sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd", "sagebwd_fwd_quantize", "sagebwd_fwd_attention",
     "sagebwd_bwd_prepare", "sagebwd_bwd_attention", "sagebwd_bwd_finish", "sagebwd_check_status",
     "sagebwd_status_string", "sagebwd_version", "sagebwd_quantize_k_noalloc", "attention", "SageBwdAttention",
-    "SAGEBWD_Q", "SAGEBWD_K", "SAGEBWD_V", "SAGEBWD_DO", "FLAG_DROP_ONE_LOAD",
+    "SAGEBWD_Q", "SAGEBWD_K", "SAGEBWD_V", "SAGEBWD_DO", "FLAG_DROP_ONE_LOAD", "FLAG_DEBUG_DUMP",
+    "sagebwd_debug_dump_offset", "debug_dump_views",
 ]
 
 SAGEBWD_Q, SAGEBWD_K, SAGEBWD_V, SAGEBWD_DO = 0, 1, 2, 3
 FLAG_DROP_ONE_LOAD = 0x1
+FLAG_DEBUG_DUMP = 0x2
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA", 5: "TIMEOUT",
                 6: "SCRATCH_LIMIT"}
 
@@ -35,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "sagebwd_saved_bytes", "sagebwd_workspace_bytes", "sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd",
     "sagebwd_fwd_quantize", "sagebwd_fwd_attention", "sagebwd_bwd_prepare", "sagebwd_bwd_attention",
     "sagebwd_bwd_finish", "sagebwd_check_status", "sagebwd_status_string", "sagebwd_version",
-    "sagebwd_quantize_k_noalloc",
+    "sagebwd_quantize_k_noalloc", "sagebwd_debug_dump_offset",
 )
 
 
@@ -100,6 +102,8 @@ def load_library():
             lib.sagebwd_status_string.argtypes = [ctypes.c_int]
             lib.sagebwd_status_string.restype = ctypes.c_char_p
             lib.sagebwd_version.restype = ctypes.c_int32
+            lib.sagebwd_debug_dump_offset.argtypes = [P, ctypes.c_int]
+            lib.sagebwd_debug_dump_offset.restype = ctypes.c_size_t
             for name in ("sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd", "sagebwd_fwd_quantize",
                          "sagebwd_fwd_attention", "sagebwd_bwd_prepare", "sagebwd_bwd_attention",
                          "sagebwd_bwd_finish", "sagebwd_check_status", "sagebwd_quantize_k_noalloc"):
@@ -209,6 +213,37 @@ def sagebwd_status_string(code: int) -> str:
 
 def sagebwd_version() -> int:
     return int(load_library().sagebwd_version())
+
+
+def sagebwd_debug_dump_offset(prob, pass_: int) -> int:
+    return int(load_library().sagebwd_debug_dump_offset(ctypes.byref(prob), pass_))
+
+
+def debug_dump_views(prob: Problem, ws: torch.Tensor, pass_: int) -> dict:
+    """Views of the debug dump (SAGEBWD_FLAG_DEBUG_DUMP) inside a workspace, one record per
+    tile [B*Hq, nb (query block), nb (key block)].  Forward (pass 0): s [.., 128 q, 128 k] FP32,
+    p [.., 128 q, 128 k] BF16 codes, pv [.., 128 q, d] FP32.  Backward (pass 1): pt and ds
+    [.., 128 keys, 128 queries] BF16 codes, dv and dk [.., 128 keys, d], dq [.., 128 queries, d] FP32."""
+    off = sagebwd_debug_dump_offset(prob, pass_)
+    if off == 0:
+        raise ValueError("the problem has no debug dump (SAGEBWD_FLAG_DEBUG_DUMP not set)")
+    nb = (prob.N + 127) // 128
+    d = prob.d
+    n = prob.B * prob.Hq * nb * nb
+    if pass_ == 0:
+        parts = [("s", 128 * 128 * 4, torch.float32, (128, 128)), ("p", 128 * 128 * 2, torch.bfloat16, (128, 128)),
+                 ("pv", 128 * d * 4, torch.float32, (128, d))]
+    else:
+        parts = [("pt", 128 * 128 * 2, torch.bfloat16, (128, 128)), ("ds", 128 * 128 * 2, torch.bfloat16, (128, 128)),
+                 ("dv", 128 * d * 4, torch.float32, (128, d)), ("dk", 128 * d * 4, torch.float32, (128, d)),
+                 ("dq", 128 * d * 4, torch.float32, (128, d))]
+    rec = sum(nbytes for _, nbytes, _, _ in parts)
+    raw = ws[off:off + n * rec].view(n, rec)
+    out, o = {}, 0
+    for name, nbytes, dt, shape in parts:
+        out[name] = raw[:, o:o + nbytes].contiguous().view(dt).view(prob.B * prob.Hq, nb, nb, *shape)
+        o += nbytes
+    return out
 
 
 # ---------------------------------------------------------------------------- buffers and autograd

@@ -29,6 +29,12 @@ sagebwd_status check_problem(const sagebwd_problem* p) {
   if (elems >= 2147483648.0) return SAGEBWD_ERR_UNSUPPORTED;
   if ((double)nblocks(p->N) * p->B * p->Hq >= 2147483647.0) return SAGEBWD_ERR_UNSUPPORTED;
   if (p->smooth_q && p->balance_qk) return SAGEBWD_ERR_UNSUPPORTED;  // not defined together
+  if (p->flags & SAGEBWD_FLAG_DEBUG_DUMP) {
+    // the dump covers the plain kernels (integer-valued operands), at most 2^31 bytes
+    if (p->ds_subexp || p->qk_subexp || p->smooth_q) return SAGEBWD_ERR_UNSUPPORTED;
+    const double nb = nblocks(p->N);
+    if ((double)p->B * p->Hq * nb * nb * (98304.0 + 1536.0 * p->d) >= 2147483648.0) return SAGEBWD_ERR_UNSUPPORTED;
+  }
   return SAGEBWD_OK;
 }
 
@@ -61,7 +67,7 @@ SavedLayout saved_layout(const sagebwd_problem* p) {
 
 // Workspace: [status word | pass scratch].
 struct WsLayout {
-  size_t status, kpart, kmax, kmin, qmax, D, dOq, sdo, dqacc, dkacc, dvacc, cs, total;
+  size_t status, kpart, kmax, kmin, qmax, D, dOq, sdo, dqacc, dkacc, dvacc, cs, dump, total;
 };
 WsLayout ws_layout(const sagebwd_problem* p, int pass) {
   const size_t nb = (size_t)nblocks(p->N);
@@ -89,6 +95,12 @@ WsLayout ws_layout(const sagebwd_problem* p, int pass) {
     if (p->smooth_q) {
       L.cs = off; off += align_up((size_t)p->B * p->Hq * nb * 2 * 4 * 128 * 4);
     }
+  }
+  if (p->flags & SAGEBWD_FLAG_DEBUG_DUMP) {
+    // one record per (b, query head, query block, key block): forward 128*128*(4 + 2) + 128*d*4
+    // bytes, backward 2*128*128*2 + 3*128*d*4 bytes
+    const size_t rec = pass == 0 ? 98304 + (size_t)512 * p->d : 65536 + (size_t)1536 * p->d;
+    L.dump = off; off += align_up((size_t)p->B * p->Hq * nb * nb * rec);
   }
   L.total = off;
   return L;
@@ -250,7 +262,7 @@ sagebwd_status fwd_attention_impl(const sagebwd_problem* p, const void* saved, v
       !make_map(&tk, at<uint8_t>(saved, S.k), p->B * p->Hkv, p->N, p->d) ||
       !make_map(&tv, at<uint8_t>(saved, S.v), p->B * p->Hkv, p->N, p->d))
     return SAGEBWD_ERR_CUDA;
-  FwdParams fp{};
+  FwdDumpParams fp{};
   fp.B = p->B;
   fp.Hq = p->Hq;
   fp.Hkv = p->Hkv;
@@ -264,6 +276,7 @@ sagebwd_status fwd_attention_impl(const sagebwd_problem* p, const void* saved, v
   fp.o = static_cast<__nv_bfloat16*>(o);
   fp.lse = lse;
   fp.qbias = p->smooth_q ? at<float>(saved, S.qb) : nullptr;
+  fp.dump = (p->flags & SAGEBWD_FLAG_DEBUG_DUMP) ? at<uint8_t>(ws, W.dump) : nullptr;
   fp.status = at<int>(ws, W.status);
   fp.timeout_ns = timeout_of(p);
   fp.flags = p->flags;
@@ -366,6 +379,7 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
     bp.qmean = at<float>(saved, S.qm);
     bp.cs_part = at<float>(ws, W.cs);
   }
+  bp.dump = (p->flags & SAGEBWD_FLAG_DEBUG_DUMP) ? at<uint8_t>(ws, W.dump) : nullptr;
   bp.status = at<int>(ws, W.status);
   bp.timeout_ns = timeout_of(p);
   bp.flags = (p->flags & ~kBwdDirectDKDV) | (direct ? kBwdDirectDKDV : 0u);
@@ -512,6 +526,12 @@ const char* sagebwd_status_string(sagebwd_status s) {
     case SAGEBWD_ERR_SCRATCH_LIMIT: return "problem too large for the fixed scratch of sagebwd_quantize_k_noalloc";
   }
   return "unknown status";
+}
+
+size_t sagebwd_debug_dump_offset(const sagebwd_problem* prob, int pass) {
+  if (check_problem(prob) != SAGEBWD_OK || (pass != 0 && pass != 1) || !(prob->flags & SAGEBWD_FLAG_DEBUG_DUMP))
+    return 0;
+  return ws_layout(prob, pass).dump;
 }
 
 int32_t sagebwd_version(void) { return 100; }

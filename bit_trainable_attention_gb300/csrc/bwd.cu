@@ -117,22 +117,41 @@ enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty,
                bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAccV, bSiteAccQ, bSiteAccK, bSiteTmemFreeV, bSiteDVQFree,
                bSiteTmemFreeK, bSiteStaged, bSiteStgFree, bSiteC1, bSiteC2, bSiteC3, bSiteAlign };
 
-// The plain instantiations take BwdParams (128 bytes), the Q-smoothing ones BwdQsmParams.
-template <bool QSM>
+// The plain instantiations take BwdParams (128 bytes), the Q-smoothing ones BwdQsmParams, the
+// debug-dump one (DBG) BwdDumpParams.
+template <bool QSM, bool DBG>
 struct BwdParamsOf {
   using type = BwdParams;
 };
 template <>
-struct BwdParamsOf<true> {
+struct BwdParamsOf<true, false> {
   using type = BwdQsmParams;
 };
+template <>
+struct BwdParamsOf<false, true> {
+  using type = BwdDumpParams;
+};
 
-template <int D, bool CAUSAL, bool DSX, bool QSM>
+// Debug dump record of one tile: P^T codes and dS codes (BF16 [128 keys][128 queries]), then the
+// raw FP32 tile products [P^T dO^], [dS^T Q^] ([128 keys][D]) and [dS K^] ([128 queries][D]).
+template <int D>
+struct BwdDump {
+  static constexpr size_t PT = 0, DS = 128 * 128 * 2, DV = 2 * 128 * 128 * 2, DK = DV + 128 * D * 4,
+                          DQ = DK + 128 * D * 4, BYTES = DQ + 128 * D * 4;
+};
+// Write 16 consecutive 32-bit words (64 bytes, 16-byte aligned) to global memory.
+__device__ __forceinline__ void dump16(uint8_t* dst, const uint32_t* w) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
+template <int D, bool CAUSAL, bool DSX, bool QSM, bool DBG>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmDOQ, const __grid_constant__ CUtensorMap tmDQ,
-               const typename BwdParamsOf<QSM>::type p) {
+               const typename BwdParamsOf<QSM, DBG>::type p) {
   using C = BwdCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -188,6 +207,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const int T = p.HS * nq;
   auto tile_bhq = [&](int t) { return b * p.Hq + hq0 + t / nq; };
   auto tile_ib = [&](int t) { return ib0 + t % nq; };
+  // debug dump record of tile t (DBG instantiation only)
+  auto dump_rec = [&](int t) -> uint8_t* {
+    if constexpr (DBG)
+      return p.dump + (((size_t)tile_bhq(t) * p.nb + tile_ib(t)) * p.nb + j) * BwdDump<D>::BYTES;
+    else
+      return nullptr;
+  };
 
   if (tid == 0) {
     mbar_init(bar_kv, 1);
@@ -576,6 +602,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 kNegMagic2);
             pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
           }
+          if constexpr (DBG) dump16(dump_rec(it) + BwdDump<D>::PT + ((size_t)r * 128 + qc0 + c0) * 2, pk);
           tmem_st16(pc_addr + (c0 >> 1), pk);
         }
       }
@@ -611,6 +638,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             if (QSM) csum = fadd2(csum, cd);
             v[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
           }
+          if constexpr (DBG) dump16(dump_rec(it) + BwdDump<D>::DS + ((size_t)r * 128 + qc0 + c0) * 2, v);
 #pragma unroll
           for (int h = 0; h < 4; ++h)
             st_shared_v4(ds_base + sw128_offset(r, ((qc0 + c0) >> 3) + h), v[4 * h], v[4 * h + 1], v[4 * h + 2],
@@ -660,6 +688,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           uint32_t v[16];
           tmem_ld16(tmem + lane_base + C::C_DV + wa * DH + c0, v);
           tmem_ld_wait_regs(v);
+          if constexpr (DBG) dump16(dump_rec(it) + BwdDump<D>::DV + ((size_t)r * D + wa * DH + c0) * 4, v);
 #pragma unroll
           for (int e = 0; e < 16; e += 2) ffma2_acc(dv_run[(c0 + e) >> 1], fv2, v[e], v[e + 1]);
         }
@@ -677,6 +706,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           uint32_t v[16];
           tmem_ld16(tmem + lane_base + C::C_DK + wa * DH + c0, v);
           tmem_ld_wait_regs(v);
+          if constexpr (DBG) dump16(dump_rec(it) + BwdDump<D>::DK + ((size_t)r * D + wa * DH + c0) * 4, v);
 #pragma unroll
           for (int e = 0; e < 16; e += 2) ffma2_acc(dk_run[(c0 + e) >> 1], fk2, v[e], v[e + 1]);
         }
@@ -717,6 +747,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           uint32_t v[16];
           tmem_ld16(tmem + lane_base + C::C_DQ + wa * DH + c0, v);
           tmem_ld_wait_regs(v);
+          if constexpr (DBG) dump16(dump_rec(it) + BwdDump<D>::DQ + ((size_t)r * D + wa * DH + c0) * 4, v);
 #pragma unroll
           for (int c4 = 0; c4 < 16; c4 += 4) {
             const int col = wa * DH + c0 + c4;
@@ -782,12 +813,21 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   using C = BwdCfg<D>;
   const int grid = p.nb * p.B * p.Hkv * (p.G / p.HS);
   if (p.qbias != nullptr) {
-    auto kern = bwd_kernel<D, CAUSAL, DSX, true>;
+    auto kern = bwd_kernel<D, CAUSAL, DSX, true, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, p);
+  } else if (p.dump != nullptr) {
+    if (DSX) return cudaErrorInvalidValue;  // the dump covers the plain instantiation only
+    auto kern = bwd_kernel<D, CAUSAL, false, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    BwdDumpParams dp;
+    static_cast<BwdParams&>(dp) = static_cast<const BwdParams&>(p);
+    dp.dump = p.dump;
+    kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, dp);
   } else {
-    auto kern = bwd_kernel<D, CAUSAL, DSX, false>;
+    auto kern = bwd_kernel<D, CAUSAL, DSX, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, static_cast<const BwdParams&>(p));

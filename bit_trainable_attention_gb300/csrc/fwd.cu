@@ -68,10 +68,32 @@ struct FwdCfg {
 enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteSFull, kSitePFull, kSitePVDone,
                kSiteOEmpty };
 
-template <int D, bool CAUSAL, bool QSM>
+// The debug-dump instantiation (DBG) takes FwdDumpParams; one record per tile: the raw FP32
+// S_int [128 queries][128 keys], the P~ codes (BF16 [128 queries][128 keys]) and the raw FP32
+// [P^ V^] [128 queries][D].
+template <bool DBG>
+struct FwdParamsOf {
+  using type = FwdParams;
+};
+template <>
+struct FwdParamsOf<true> {
+  using type = FwdDumpParams;
+};
+template <int D>
+struct FwdDump {
+  static constexpr size_t S = 0, PC = 128 * 128 * 4, PV = PC + 128 * 128 * 2, BYTES = PV + 128 * D * 4;
+};
+// Write 16 consecutive 32-bit words (64 bytes, 16-byte aligned) to global memory.
+__device__ __forceinline__ void fdump16(uint8_t* dst, const uint32_t* w) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
+template <int D, bool CAUSAL, bool QSM, bool DBG>
 __global__ void __launch_bounds__(kFThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tmV, const typename FwdParamsOf<DBG>::type p) {
   using C = FwdCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -268,6 +290,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
     bool ok = true;
 
     // Fold tile jj's P V product into the running output: o = o * a + w * [P^ V^]_jj.
+    // debug dump record of key tile jj of this warpgroup's query tile (DBG instantiation only)
+    auto dump_rec = [&](int jj) -> uint8_t* {
+      if constexpr (DBG)
+        return p.dump + (((size_t)bhq * p.nb + qb) * p.nb + jj) * FwdDump<D>::BYTES;
+      else
+        return nullptr;
+    };
     auto fold = [&](int jj, float a, float w) -> bool {
       if (!waitw(wc, bar_pv_done + t, jj & 1, kSitePVDone)) return false;
       tc_fence_after();
@@ -282,6 +311,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
         uint32_t v[32];
         tmem_ld32(o_addr + c0, v);
         tmem_ld_wait();
+        if constexpr (DBG) {
+          fdump16(dump_rec(jj) + FwdDump<D>::PV + ((size_t)r * D + c0) * 4, v);
+          fdump16(dump_rec(jj) + FwdDump<D>::PV + ((size_t)r * D + c0 + 16) * 4, v + 16);
+        }
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
           ffma2_acc(o_acc[(c0 + e) >> 1], w2, v[e], v[e + 1]);
@@ -362,6 +395,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
             for (int e = 0; e < 32; e += 2)
               smax = fmax3(smax, c0 + e < kvis ? __uint_as_float(v[e]) : -INFINITY,
                            c0 + e + 1 < kvis ? __uint_as_float(v[e + 1]) : -INFINITY);
+            if constexpr (DBG) {
+              fdump16(dump_rec(j) + FwdDump<D>::S + ((size_t)r * 128 + c0) * 4, v);
+              fdump16(dump_rec(j) + FwdDump<D>::S + ((size_t)r * 128 + c0 + 16) * 4, v + 16);
+            }
           }
         } else {
 #pragma unroll
@@ -371,6 +408,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; e += 2) smax = fmax3(smax, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            if constexpr (DBG) {
+              fdump16(dump_rec(j) + FwdDump<D>::S + ((size_t)r * 128 + c0) * 4, v);
+              fdump16(dump_rec(j) + FwdDump<D>::S + ((size_t)r * 128 + c0 + 16) * 4, v + 16);
+            }
           }
         }
         tmax = __fmul_rn(smax, qks);
@@ -407,6 +448,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
           const float2 cd = fadd2(fadd2(u, mg), nmg);
           pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
         }
+        if constexpr (DBG) fdump16(dump_rec(j) + FwdDump<D>::PC + ((size_t)r * 128 + c0) * 2, pk);
         tmem_st16(s_addr + (c0 >> 1), pk);
       }
       tmem_st_wait();
@@ -442,21 +484,29 @@ __global__ void __launch_bounds__(kFThreads, 1)
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdDumpParams& p,
                          cudaStream_t s) {
   using C = FwdCfg<D>;
-  auto kern = p.qbias != nullptr ? fwd_kernel<D, CAUSAL, true> : fwd_kernel<D, CAUSAL, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
   const int grid = (p.nb + 1) / 2 * p.B * p.Hq;
-  kern<<<grid, kFThreads, C::SMEM, s>>>(tq, tk, tv, p);
+  if (p.dump != nullptr) {
+    if (p.qbias != nullptr) return cudaErrorInvalidValue;  // the dump covers the plain instantiation only
+    auto kern = fwd_kernel<D, CAUSAL, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kFThreads, C::SMEM, s>>>(tq, tk, tv, p);
+  } else {
+    auto kern = p.qbias != nullptr ? fwd_kernel<D, CAUSAL, true, false> : fwd_kernel<D, CAUSAL, false, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kFThreads, C::SMEM, s>>>(tq, tk, tv, static_cast<const FwdParams&>(p));
+  }
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p, int d,
-                       int causal, cudaStream_t s) {
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdDumpParams& p,
+                       int d, int causal, cudaStream_t s) {
   if (d == 64) return causal ? launch_fwd_t<64, true>(tq, tk, tv, p, s) : launch_fwd_t<64, false>(tq, tk, tv, p, s);
   return causal ? launch_fwd_t<128, true>(tq, tk, tv, p, s) : launch_fwd_t<128, false>(tq, tk, tv, p, s);
 }

@@ -117,7 +117,13 @@ struct FwdParams {
   uint64_t timeout_ns;
   uint32_t flags;
 };
-cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+// The debug-dump instantiation (SAGEBWD_FLAG_DEBUG_DUMP) takes this extension: one record per
+// tile, layout as documented at sagebwd_debug_dump_offset.
+struct FwdDumpParams : FwdParams {
+  uint8_t* dump;
+};
+// dump == nullptr selects the plain (or Q-smoothing) instantiations.
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdDumpParams& p,
                        int d, int causal, cudaStream_t s);
 
 // Kept at 128 bytes: a larger parameter block made ptxas spill in the d = 64 kernels.
@@ -149,6 +155,10 @@ struct BwdQsmParams : BwdParams {
   const float* qbias;
   const float* qmean;
   float* cs_part;
+  uint8_t* dump;  // debug dump (plain instantiation only), or nullptr
+};
+struct BwdDumpParams : BwdParams {
+  uint8_t* dump;
 };
 // p.qbias == nullptr selects the plain instantiations (which take only the BwdParams part).
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,

@@ -99,6 +99,10 @@ enum { SAGEBWD_Q = 0, SAGEBWD_K = 1, SAGEBWD_V = 2, SAGEBWD_DO = 3 };
 /* sagebwd_problem.flags */
 #define SAGEBWD_FLAG_DROP_ONE_LOAD 0x1u /* fault injection: the forward kernel skips one K-tile load, so its
                                            bounded wait runs out and the call reports SAGEBWD_ERR_TIMEOUT */
+#define SAGEBWD_FLAG_DEBUG_DUMP 0x2u    /* parity checking: the attention kernels also write every tile's
+                                           INT8-semantics operands and raw tensor-core products into the
+                                           workspace (layout at sagebwd_debug_dump_offset; small problems
+                                           only; not with ds_subexp, qk_subexp or smooth_q) */
 
 typedef struct {
   int32_t B, Hq, Hkv, N, d;
@@ -233,6 +237,21 @@ sagebwd_status sagebwd_check_status(const void* ws, void* stream, int32_t* detai
 const char* sagebwd_status_string(sagebwd_status s);
 
 /* Library version, as major*10000 + minor*100 + patch. */
+/* Byte offset inside the pass-0 (forward) or pass-1 (backward) workspace of the
+ * debug dump written under SAGEBWD_FLAG_DEBUG_DUMP; 0 when the flag is not set
+ * or the problem is invalid.  One record per 128 x 128 tile (b, query head h,
+ * query block i, key block j), at index ((b*Hq + h)*nb + i)*nb + j, nb =
+ * ceil(N/128); records of tiles a causal problem skips are not written.
+ * Forward record (T_f = 128*128*4 + 128*128*2 + 128*d*4 bytes):
+ *   FP32 S_int [128 queries][128 keys] = Q^ K^T of the codes, as accumulated;
+ *   BF16 P~ codes [128 queries][128 keys];  FP32 [P^ V^] [128 queries][d].
+ * Backward record (T_b = 2*128*128*2 + 3*128*d*4 bytes):
+ *   BF16 P^T codes [128 keys][128 queries];  BF16 dS codes [128 keys][128 queries];
+ *   FP32 [P^T dO^] [128 keys][d];  FP32 [dS^T Q^] [128 keys][d];  FP32 [dS K^] [128 queries][d].
+ * The workspace of a flagged problem is that much larger; a problem whose dump
+ * would exceed 2^31 bytes is refused (SAGEBWD_ERR_UNSUPPORTED). */
+size_t sagebwd_debug_dump_offset(const sagebwd_problem* prob, int pass);
+
 int32_t sagebwd_version(void);
 
 #ifdef __cplusplus
