@@ -7,7 +7,8 @@
  * recompute, dV = P^T dO, dQ = dS K and dK = dS^T Q -- and keep only
  * dP = dO V^T in 16-bit floating point ("SageAttention3: Microscaling FP4
  * Attention for Inference and An Exploration of 8-Bit Training", summary
- * page, Approach, and the "Measured effects" row "Keep dO V^T in FP16").
+ * page, Approach, and the "Measured effects" row on leaving dO V^T
+ * unquantized).
  * K is smoothed by subtracting its per-channel mean over tokens (SageBwd
  * Abstract, finding (iv)); QK-norm, where used, is applied by the caller.
  *

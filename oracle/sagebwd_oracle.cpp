@@ -9,7 +9,7 @@
 //    the score gradient dS is the main error source.
 //  * "SageAttention3: Microscaling FP4 Attention for Inference and An
 //    Exploration of 8-Bit Training" (summary page), Approach and the
-//    "Measured effects" row "Keep dO V^T in FP16": the product dO.V^T is the
+//    "Measured effects" row on leaving dO.V^T unquantized: the product is the
 //    one matmul left in 16/64-bit floating point.
 //  * FlashAttention / FlashAttention-2 (listed under "Builds on" of the SageBwd
 //    page): the forward keeps the log-sum-exp of each query row, and the
@@ -512,8 +512,8 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
       const double tt = M.F(M.F(s * qks) + qsmooth_bias(M, p, qq, kq, bhq, ib, bhk, kk, c0));
       const double pp = M.F(std::exp2(M.F(tt - L)));  // normalized probability
       // dP = dO V^T: the product kept in high precision (BF16 inputs, FP64 sum here);
-      // the int8_dp ablation takes it from the dO and V codes instead (the pages' ablation
-      // "Keep dO V^T in FP16 instead of quantizing it to INT8", run the other way round).
+      // the int8_dp ablation takes it from the dO and V codes instead (the pages' ablation of
+      // leaving this product unquantized, run the other way round).
       double dp = 0;
       if (doq && vq) {
         for (int ch = 0; ch < d; ++ch) dp += doq->c(bhq, i, ch) * vq->c(bhk, kk, ch);
