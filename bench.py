@@ -43,8 +43,8 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # the one-pass ncu capture summarised in profiles/bwd_kernel_qwen15b_ncu.md.  The
 # figure belongs to the kernel sources it was taken from: once any of them changes
 # the line reports null until the capture is repeated.
-BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1326663168 + 516049408,
-               "sources_sha256": "68110d713904367f783853b5753eaee6bc4bbe56f35f7f39d5c8c459cbdf9474"}
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1329497600 + 517275904,
+               "sources_sha256": "0847bac826e4c639e5249ec969dd627e09ad6f56afd263bb3f145d2a2cb8163d"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
