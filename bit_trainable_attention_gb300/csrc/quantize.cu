@@ -494,59 +494,76 @@ __global__ void __launch_bounds__(kFinalSlices * 32) kmean_final_kernel(const do
 // Q-smoothing's logit terms ("SageBwd: A Trainable Low-bit Attention", Abstract, finding
 // (iv); the library's reading of the optional Q-smoothing): with Q = (Q - mean_Q) + mean_Q per
 // 128-token block, S = Q K'^T gains mean_Q(block of i) . K'_k, which depends on the query only
-// through its block.  Thread k of CTA (key block jb, query head bhq) holds K'_k = K_k - mean_K
-// (one FP32 rounding each; K itself without smoothing) in registers and writes, for every
-// query block ib that sees key block jb, c0 * (mean_Q(bhq, ib) . K'_k): FP32 products summed in
-// four interleaved partial sums, times c0 (the logits' base-2 units).  Keys past N get 0.  The
-// means of kQB query blocks at a time are staged in shared memory (broadcast reads) and their
-// kQB dot products run as independent chains.
+// through its block.  CTA (key block jb, query head bhq) writes, for every query block ib that
+// sees key block jb, c0 * (mean_Q(bhq, ib) . K'_k) for its 128 keys, K' = K - mean_K (one FP32
+// rounding each; K itself without smoothing), 0 past N.  Thread t holds keys 2 (t/2) and
+// 2 (t/2) + 1 over channel half t % 2 in registers; the means of kQB query blocks at a time are
+// staged in shared memory (broadcast reads, 8 FMAs per 16-byte load), each (key, block) sums its
+// half in one FP32 chain, and the two halves are added with a lane shuffle.
 constexpr int kQB = 8;
 template <int D>
 __global__ void __launch_bounds__(kBlk) qsmooth_bias_kernel(const QBiasParams p) {
+  constexpr int DH = D / 2;
   __shared__ float4 msm[kQB * D / 4];
-  const int jb = blockIdx.x, bhq = blockIdx.y;
-  const int key = jb * kBlk + threadIdx.x;
+  // causal: key block jb sees nb - jb query blocks; blocks are dispatched in launch order with
+  // blockIdx.x fastest, so the longest (small jb) go first
+  const int jb = blockIdx.y, bhq = blockIdx.x;
+  const int pair = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int key0 = jb * kBlk + 2 * pair;
   const int bhk = bhq / p.G;  // b Hq + h -> b Hkv + h / G
   const size_t np = (size_t)p.nb * kBlk;
-  const bool live = key < p.N;
-  float kr[D];
+  float kr[2][DH];
 #pragma unroll
-  for (int v = 0; v < D / 8; ++v) {
-    float f[8];
-    if (live) {
-      unpack8(*reinterpret_cast<const uint4*>(p.k + ((size_t)bhk * p.N + key) * D + v * 8), f);
-    } else {
+  for (int u = 0; u < 2; ++u) {
+    const bool live = key0 + u < p.N;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = 0.f;
+    for (int v = 0; v < DH / 8; ++v) {
+      float f[8];
+      if (live) {
+        unpack8(*reinterpret_cast<const uint4*>(p.k + ((size_t)bhk * p.N + key0 + u) * D + half * DH + v * 8), f);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int ch = half * DH + v * 8 + e;
+        kr[u][v * 8 + e] = p.kmean != nullptr ? __fsub_rn(f[e], p.kmean[(size_t)bhk * D + ch]) : f[e];
+      }
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) kr[v * 8 + e] = p.kmean != nullptr ? __fsub_rn(f[e], p.kmean[(size_t)bhk * D + v * 8 + e]) : f[e];
   }
   const float4* mg = reinterpret_cast<const float4*>(p.qmean + (size_t)bhq * p.nb * D);
+  const int mykey = key0 + half;  // the key this thread writes
   for (int ib0 = p.causal ? jb : 0; ib0 < p.nb; ib0 += kQB) {
     const int nq = min(kQB, p.nb - ib0);
     __syncthreads();  // the previous chunk's means have been read
     for (int e = threadIdx.x; e < nq * D / 4; e += kBlk) msm[e] = mg[(size_t)ib0 * D / 4 + e];
     __syncthreads();
-    float acc[kQB][4];
+    float acc[kQB][2];
 #pragma unroll
-    for (int q = 0; q < kQB; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+    for (int q = 0; q < kQB; ++q) acc[q][0] = acc[q][1] = 0.f;
 #pragma unroll
-    for (int c4 = 0; c4 < D / 4; ++c4) {
+    for (int c4 = 0; c4 < DH / 4; ++c4) {
 #pragma unroll
       for (int q = 0; q < kQB; ++q) {
-        const float4 m = msm[q * D / 4 + c4];  // rows past nq hold stale values; not stored
-        acc[q][0] = fmaf(m.x, kr[4 * c4], acc[q][0]);
-        acc[q][1] = fmaf(m.y, kr[4 * c4 + 1], acc[q][1]);
-        acc[q][2] = fmaf(m.z, kr[4 * c4 + 2], acc[q][2]);
-        acc[q][3] = fmaf(m.w, kr[4 * c4 + 3], acc[q][3]);
+        const float4 m = msm[q * D / 4 + half * DH / 4 + c4];  // rows past nq hold stale values; not stored
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          acc[q][u] = fmaf(m.x, kr[u][4 * c4], acc[q][u]);
+          acc[q][u] = fmaf(m.y, kr[u][4 * c4 + 1], acc[q][u]);
+          acc[q][u] = fmaf(m.z, kr[u][4 * c4 + 2], acc[q][u]);
+          acc[q][u] = fmaf(m.w, kr[u][4 * c4 + 3], acc[q][u]);
+        }
       }
     }
 #pragma unroll
-    for (int q = 0; q < kQB; ++q)
-      if (q < nq)
-        p.bias[((size_t)bhq * p.nb + ib0 + q) * np + key] =
-            live ? __fmul_rn((acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]), p.c0) : 0.f;
+    for (int q = 0; q < kQB; ++q) {
+      // channel half 0 + half 1 of key 2 pair + half (the partner holds the other half)
+      const float mine = half ? acc[q][1] : acc[q][0];
+      const float other = __shfl_xor_sync(0xffffffffu, half ? acc[q][0] : acc[q][1], 1);
+      const float dot = half == 0 ? mine + other : other + mine;
+      if (q < nq) p.bias[((size_t)bhq * p.nb + ib0 + q) * np + mykey] = mykey < p.N ? __fmul_rn(dot, p.c0) : 0.f;
+    }
   }
 }
 
@@ -695,7 +712,7 @@ cudaError_t launch_grad_convert(const ConvertJob* jobs, int njobs, cudaStream_t 
 }
 
 cudaError_t launch_qsmooth_bias(const QBiasParams& p, cudaStream_t s) {
-  const dim3 grid(p.nb, p.BHq);
+  const dim3 grid(p.BHq, p.nb);
   if (p.d == 64)
     qsmooth_bias_kernel<64><<<grid, kBlk, 0, s>>>(p);
   else
