@@ -73,31 +73,51 @@ def load_peaks():
 
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 25 ms, read by a background thread; wait()
+    returns once the first sample has arrived, so the timed region that follows is covered."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
-        self.proc = None
+        import threading
+        self.proc, self.lines, self.first = None, [], threading.Event()
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "25",
                  "-i", str(device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
 
-    def stop(self):
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
+            self.first.set()
+
+    def wait(self, timeout: float = 10.0):
+        if self.proc is not None:
+            self.first.wait(timeout)
+
+    def mark(self):
+        """Index of the next sample: samples before it are not part of the timed region."""
+        return len(self.lines)
+
+    def stop(self, start: int = 0, end: int = None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        self.reader.join(timeout=5)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        lines = self.lines[start:end] or self.lines[-1:]  # a very short region: the sample that follows it
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -211,7 +231,7 @@ def cossim_vs_torch(step: Step):
     return out
 
 
-def time_device(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_barrier):
+def time_device(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_barrier, on_timed=None):
     for _ in range(warmup):
         flush.zero_()
         step.run()
@@ -219,6 +239,8 @@ def time_device(step: Step, steps: int, warmup: int, flush: torch.Tensor, dist_b
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
     dist_barrier()
     torch.cuda.synchronize()
+    if on_timed is not None:
+        on_timed()  # the timed region starts here
     for i in range(steps):
         flush.zero_()  # L2 flush between timed steps, outside the events
         step.run(evs[i])
@@ -559,8 +581,12 @@ def main():
                 smooth_q=args.smooth_q)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(local)
-    total, stage = time_device(step, args.steps, args.warmup, flush, barrier)
-    clocks = sampler.stop()
+    sampler.wait()
+    mark = [0]
+    total, stage = time_device(step, args.steps, args.warmup, flush, barrier,
+                               on_timed=lambda: mark.__setitem__(0, sampler.mark()))
+    end = sampler.mark()
+    clocks = sampler.stop(mark[0], end + 1)  # and the sample in flight when the region ended
     if args.no_e2e:
         e2e_ms, h2d, d2h = None, 0, 0
     else:
