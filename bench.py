@@ -44,7 +44,7 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # figure belongs to the kernel sources it was taken from: once any of them changes
 # the line reports null until the capture is repeated.
 BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1329497600 + 517275904,
-               "sources_sha256": "0847bac826e4c639e5249ec969dd627e09ad6f56afd263bb3f145d2a2cb8163d"}
+               "sources_sha256": "86077e0c6a080ec1e8b4d1dc79b42dca87b7bbea75c933ad2e02e4c84596e244"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]

@@ -133,7 +133,8 @@ size_t sagebwd_saved_bytes(const sagebwd_problem* prob);
  * then scratch (K-mean partial sums, and with balance_qk the per-block channel
  * maxima of Q and K; D = rowsum(dO*O), the quantized dO and its scales, the
  * FP32 dQ, dK and dV accumulators, and with smooth_q a small ring of dS column
- * sums per backward CTA).  Contents need no initialisation and are
+ * sums per backward CTA; with SAGEBWD_FLAG_DEBUG_DUMP the dump follows).
+ * Contents need no initialisation and are
  * not meaningful between calls, except the status word. */
 size_t sagebwd_workspace_bytes(const sagebwd_problem* prob, int pass);
 
@@ -237,7 +238,6 @@ sagebwd_status sagebwd_check_status(const void* ws, void* stream, int32_t* detai
 
 const char* sagebwd_status_string(sagebwd_status s);
 
-/* Library version, as major*10000 + minor*100 + patch. */
 /* Byte offset inside the pass-0 (forward) or pass-1 (backward) workspace of the
  * debug dump written under SAGEBWD_FLAG_DEBUG_DUMP; 0 when the flag is not set
  * or the problem is invalid.  One record per 128 x 128 tile (b, query head h,
@@ -253,6 +253,7 @@ const char* sagebwd_status_string(sagebwd_status s);
  * would exceed 2^31 bytes is refused (SAGEBWD_ERR_UNSUPPORTED). */
 size_t sagebwd_debug_dump_offset(const sagebwd_problem* prob, int pass);
 
+/* Library version, as major*10000 + minor*100 + patch. */
 int32_t sagebwd_version(void);
 
 #ifdef __cplusplus
