@@ -43,8 +43,8 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # the one-pass ncu capture summarised in profiles/bwd_kernel_qwen15b_ncu.md.  The
 # figure belongs to the kernel sources it was taken from: once any of them changes
 # the line reports null until the capture is repeated.
-BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 1329497600 + 517275904,
-               "sources_sha256": "86077e0c6a080ec1e8b4d1dc79b42dca87b7bbea75c933ad2e02e4c84596e244"}
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 777630464 + 285536000,
+               "sources_sha256": "fec5f7a1719768235bf01f0e4553c74737ce782fc1533fd00ec2b940f25784e9"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
