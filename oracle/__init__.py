@@ -33,7 +33,7 @@ class OracleProblem(ctypes.Structure):
         ("smooth_k", ctypes.c_int32), ("balance_qk", ctypes.c_int32), ("exact_codes", ctypes.c_int32),
         ("threads", ctypes.c_int32), ("exact_mask", ctypes.c_uint32), ("int8_dp", ctypes.c_int32),
         ("ds_subexp", ctypes.c_int32), ("qk_subexp", ctypes.c_int32), ("fp8", ctypes.c_int32),
-        ("smooth_q", ctypes.c_int32),
+        ("smooth_q", ctypes.c_int32), ("l_from_codes", ctypes.c_int32),
         ("softmax_scale", ctypes.c_double),
     ]
 
@@ -100,10 +100,13 @@ def _bf16_bits(x) -> np.ndarray:
 
 
 def problem(B, Hq, Hkv, N, d, causal, smooth_k=True, exact_codes=False, softmax_scale=0.0, threads=0, exact_mask=0,
-            balance_qk=False, int8_dp=False, ds_subexp=False, qk_subexp=False, fp8=False, smooth_q=False):
+            balance_qk=False, int8_dp=False, ds_subexp=False, qk_subexp=False, fp8=False, smooth_q=False,
+            l_from_codes=False):
+    """l_from_codes plants a misreading (softmax denominator from the dequantized P~ codes); only the
+    tests that show a pin catches it set it."""
     return OracleProblem(B, Hq, Hkv, N, d, int(causal), int(smooth_k), int(balance_qk), int(exact_codes),
                          int(threads), int(exact_mask), int(int8_dp), int(ds_subexp), int(qk_subexp), int(fp8),
-                         int(smooth_q), float(softmax_scale))
+                         int(smooth_q), int(l_from_codes), float(softmax_scale))
 
 
 def nblocks(N: int) -> int:

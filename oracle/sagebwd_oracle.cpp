@@ -89,6 +89,8 @@ typedef struct {
   int32_t qk_subexp;    // 1: Q and K codes carry a power-of-two sub-scale per (block, 8-channel group)
   int32_t fp8;          // ablation: every quantizer produces FP8 E4M3 values (scale max/448) instead of INT8
   int32_t smooth_q;     // 1: Q-smoothing (block mean of Q subtracted before quantizing, mean . K' added to S)
+  int32_t l_from_codes; // planted misreading, for the tests only: the softmax denominator summed from the
+                        // dequantized P~ codes instead of the unquantized P~ (the reading kept here, r8)
   double softmax_scale;  // <= 0: 1/sqrt(d)
 } oracle_problem;
 }
@@ -421,8 +423,19 @@ void fwd_row(const Mode& M, const oracle_problem* p, const QTensor& qq, const QT
   double m = -kInf;
   for (int jb = 0; jb <= jb_end; ++jb) m = std::max(m, tmax[jb]);
   double l = 0;
-  for (int k = 0; k < std::min(N, (jb_end + 1) * BLK); ++k)
-    if (t[k] != -kInf) l += std::exp2(t[k] - m);
+  if (p->l_from_codes) {
+    // the misreading the tests plant: l from the codes, sum_j 2^(tmax_j - m)/127 * sum_k code_k
+    for (int jb = 0; jb <= jb_end; ++jb) {
+      if (tmax[jb] == -kInf) continue;
+      double cs = 0;
+      for (int k = jb * BLK; k < std::min(N, (jb + 1) * BLK); ++k)
+        if (t[k] != -kInf) cs += fwd_p_code(M, t[k], tmax[jb]);
+      l += std::exp2(tmax[jb] - m) / M.qmax * cs;
+    }
+  } else {
+    for (int k = 0; k < std::min(N, (jb_end + 1) * BLK); ++k)
+      if (t[k] != -kInf) l += std::exp2(t[k] - m);
+  }
   std::fill(acc.begin(), acc.end(), 0.0);
   for (int jb = 0; jb <= jb_end; ++jb) {
     if (tmax[jb] == -kInf) continue;
