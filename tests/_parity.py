@@ -43,8 +43,22 @@ def bf16_round(x):
     return r.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+# Every assert_parity call records (test, tensor, relative L2, max element error / max|ref|) here;
+# tests/conftest.py prints the table at the end of the run, so the distance of each config from
+# the 2e-3 target is visible in the log.
+REPORT = []
+
+
+def _current_test():
+    import os
+    return os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+
+
 def assert_parity(gpu, ref, name, rel_l2_tol=REL_L2_TOL, elem_tol=ELEM_TOL):
-    """gpu: the library's BF16 output; ref: the oracle's FP64 result (NaN = not computed)."""
+    """gpu: the library's BF16 output; ref: the oracle's FP64 result (NaN = not computed).
+
+    Returns {"rel_l2": ||gpu - ref|| / ||ref||, "max_elem": max|gpu - ref| / max|ref|} (ref rounded
+    to BF16), after checking both bounds."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     m = np.isfinite(ref)
@@ -55,15 +69,19 @@ def assert_parity(gpu, ref, name, rel_l2_tol=REL_L2_TOL, elem_tol=ELEM_TOL):
         # e.g. one token: P = 1 and dS = dP - D = 0 exactly, so dQ = dK = 0; the
         # library's FP32 dP - D leaves at most rounding-level residue
         assert np.abs(g).max() <= 1e-4, f"{name}: reference is zero, GPU max {np.abs(g).max():.3e}"
-        return 0.0
+        out = {"rel_l2": 0.0, "max_elem": 0.0}
+        REPORT.append((_current_test(), name, out["rel_l2"], out["max_elem"]))
+        return out
     rel_l2 = float(np.linalg.norm(g - r) / np.linalg.norm(r))
-    assert rel_l2 <= rel_l2_tol, f"{name}: relative L2 error {rel_l2:.3e} > {rel_l2_tol}"
     scale = np.max(np.abs(r))
     err = np.abs(g - r)
+    out = {"rel_l2": rel_l2, "max_elem": float(err.max() / scale)}
+    REPORT.append((_current_test(), name, out["rel_l2"], out["max_elem"]))
+    assert rel_l2 <= rel_l2_tol, f"{name}: relative L2 error {rel_l2:.3e} > {rel_l2_tol}"
     bad = err > elem_tol * scale + bf16_ulp(r)
     assert not bad.any(), (f"{name}: {int(bad.sum())} of {bad.size} elements beyond {elem_tol} of the max; "
                            f"worst at ref={r[bad][0]:.6g} gpu={g[bad][0]:.6g}")
-    return rel_l2
+    return out
 
 
 def cos(a, b):
@@ -81,7 +99,7 @@ def device_inputs(w, dev="cuda"):
     return x, {k: v.to(dev) for k, v in x.items()}
 
 
-def gpu_forward(w, xd, smooth_k=True, flags=0, timeout_ms=0, balance_qk=False, ds_subexp=False, qk_subexp=False,
+def gpu_forward(w, xd, smooth_k=True, flags=0, timeout_ms=0, balance_qk=False, ds_subexp=False, qk_subexp=True,
                 smooth_q=False):
     prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_k=smooth_k, flags=flags,
                            wait_timeout_ms=timeout_ms, balance_qk=balance_qk, ds_subexp=ds_subexp,
@@ -108,7 +126,9 @@ def gpu_backward(w, xd, fwd):
     return {"dq": dq, "dk": dk, "dv": dv, "ws": ws, "status": code, "word": word}
 
 
-def oracle_problem(oracle_mod, w, smooth_k=True, balance_qk=False, ds_subexp=False, qk_subexp=False, smooth_q=False):
+def oracle_problem(oracle_mod, w, smooth_k=True, balance_qk=False, ds_subexp=False, qk_subexp=True, smooth_q=False):
+    """The oracle problem matching gpu_forward's defaults (the library's: K-smoothing and the Q/K
+    sub-scales on)."""
     return oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_k=smooth_k, balance_qk=balance_qk,
                               ds_subexp=ds_subexp, qk_subexp=qk_subexp, smooth_q=smooth_q)
 

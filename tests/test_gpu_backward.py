@@ -15,7 +15,7 @@ import torch
 
 import bit_trainable_attention_gb300 as sb
 from bit_trainable_attention_gb300 import workloads as W
-from _parity import (assert_parity, block_selection, cos, device_inputs, gpu_backward, gpu_forward, oracle_problem,
+from _parity import (assert_parity, cos, device_inputs, gpu_backward, gpu_forward, oracle_problem,
                      to_np)
 
 pytestmark = pytest.mark.gpu
@@ -116,13 +116,16 @@ def test_backward_full_size_sampled(oracle_mod, name):
     bwd = gpu_backward(w, xd, fwd)
     assert fwd["status"] == 0 and bwd["status"] == 0
     nb = (w.N + 127) // 128
-    qsel = block_selection(w, [w.Hq - 1], [-1, nb // 2])
-    ksel = block_selection(w, [0], [0, -1], kv=True)
-    if w.B > 1:  # keep the oracle's work bounded: batch 0 only
-        qsel = qsel.reshape(w.B, -1).copy()
-        qsel[1:] = 0
-        ksel = ksel.reshape(w.B, -1).copy()
-        ksel[1:] = 0
+    # bounded oracle work: in batch 0, two query blocks of the last query head and two key blocks of
+    # kv head 0; in the last batch, one query block of the last query head and one key block of the
+    # last kv head (a batch- or head-stride error shows there)
+    qsel = np.zeros((w.B, w.Hq, nb), np.uint8)
+    ksel = np.zeros((w.B, w.Hkv, nb), np.uint8)
+    qsel[0, w.Hq - 1, [nb - 1, nb // 2]] = 1
+    ksel[0, 0, [0, nb - 1]] = 1
+    qsel[w.B - 1, w.Hq - 1, nb // 3] = 1
+    ksel[w.B - 1, w.Hkv - 1, (2 * nb) // 3] = 1
+    qsel, ksel = qsel.reshape(-1), ksel.reshape(-1)
     op = oracle_problem(oracle_mod, w)
     ref = oracle_mod.pipeline(op, x["q"], x["k"], x["v"], x["do"], qsel=qsel, ksel=ksel)
     for key in ("dq", "dk", "dv"):
