@@ -24,7 +24,7 @@ __all__ = [
     "sagebwd_bwd_prepare", "sagebwd_bwd_attention", "sagebwd_bwd_finish", "sagebwd_check_status",
     "sagebwd_status_string", "sagebwd_version", "sagebwd_quantize_k_noalloc", "attention", "SageBwdAttention",
     "SAGEBWD_Q", "SAGEBWD_K", "SAGEBWD_V", "SAGEBWD_DO", "FLAG_DROP_ONE_LOAD", "FLAG_DEBUG_DUMP",
-    "sagebwd_debug_dump_offset", "debug_dump_views",
+    "sagebwd_debug_dump_offset", "debug_dump_views", "check_errors",
 ]
 
 SAGEBWD_Q, SAGEBWD_K, SAGEBWD_V, SAGEBWD_DO = 0, 1, 2, 3
@@ -59,7 +59,9 @@ class Problem(ctypes.Structure):
 
     @classmethod
     def make(cls, B, Hq, Hkv, N, d, causal, smooth_k=True, flags=0, softmax_scale=0.0, wait_timeout_ms=0,
-             balance_qk=False, ds_subexp=False, qk_subexp=False, smooth_q=False):
+             balance_qk=False, ds_subexp=False, qk_subexp=True, smooth_q=False):
+        """The library's defaults: K-smoothing on and the Q/K 8-channel sub-scales on (qk_subexp=False
+        selects the plain one-scale-per-block mode for Q and K)."""
         return cls(B, Hq, Hkv, N, d, int(bool(causal)), int(bool(smooth_k)), int(bool(balance_qk)),
                    int(bool(ds_subexp)), int(bool(qk_subexp)), int(bool(smooth_q)), flags, softmax_scale,
                    wait_timeout_ms)
@@ -290,27 +292,77 @@ def _check_inputs(q, k, v):
             raise ValueError("q, k, v must be contiguous 4-D bfloat16 CUDA tensors [B, H, N, d]")
 
 
+# ---------------------------------------------------------------------------- device status of autograd calls
+# Every kernel bounds its waits; a wait that runs out writes SAGEBWD_ERR_TIMEOUT into the status word
+# of the call's workspace and the call's outputs are then incomplete.  The autograd path does not
+# synchronize after each call: it copies the status word to pinned host memory behind the call's
+# kernels and records an event; the word is read once the event has completed -- at the start of
+# any later forward or backward call, or by check_errors(), which waits -- and a non-OK word raises
+# SageBwdError there, naming the call it came from.
+_status_lock = threading.Lock()
+_status_pending = []  # (event, pinned int32 host tensor, call name)
+
+
+def _queue_status(ws: torch.Tensor, where: str):
+    host = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    host.copy_(ws[:4].view(torch.int32), non_blocking=True)
+    ev = torch.cuda.Event()
+    ev.record()
+    with _status_lock:
+        _status_pending.append((ev, host, where))
+
+
+def _poll_status(block: bool = False):
+    with _status_lock:
+        pending = list(_status_pending)
+        _status_pending.clear()
+    keep, err = [], None
+    for ev, host, where in pending:
+        if block:
+            ev.synchronize()
+        if err is None and (block or ev.query()):
+            code = int(host.item()) & 0xFF
+            if code != 0:
+                err = SageBwdError(code, f"{where} (device status)")
+        elif err is None:
+            keep.append((ev, host, where))
+    with _status_lock:
+        _status_pending[:0] = keep
+    if err is not None:
+        raise err
+
+
+def check_errors():
+    """Wait for every attention() call issued so far and raise SageBwdError if any of them reported a
+    device-side error (a bounded wait that ran out).  Later calls also raise the errors of earlier
+    calls whose kernels have finished by then."""
+    _poll_status(block=True)
+
+
 class SageBwdAttention(torch.autograd.Function):
     """softmax(scale Q K^T) V with SageBwd's INT8 forward and backward."""
 
     @staticmethod
     def forward(ctx, q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False,
-                qk_subexp=False, smooth_q=False):
+                qk_subexp=True, smooth_q=False, flags=0, wait_timeout_ms=0):
+        _poll_status()
         _check_inputs(q, k, v)
         prob = Problem.from_tensors(q, k, causal, smooth_k=smooth_k, softmax_scale=softmax_scale,
                                     balance_qk=balance_qk, ds_subexp=ds_subexp, qk_subexp=qk_subexp,
-                                    smooth_q=smooth_q)
+                                    smooth_q=smooth_q, flags=flags, wait_timeout_ms=wait_timeout_ms)
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
         saved = empty_bytes(sagebwd_saved_bytes(prob), q.device)
         ws = empty_bytes(sagebwd_workspace_bytes(prob, 0), q.device)
         sagebwd_fwd(prob, q, k, v, o, lse, saved, ws)
+        _queue_status(ws, "sagebwd_fwd")
         ctx.prob = prob
         ctx.save_for_backward(q, k, v, o, lse, saved)
         return o
 
     @staticmethod
     def backward(ctx, do):
+        _poll_status()
         q, k, v, o, lse, saved = ctx.saved_tensors
         prob = ctx.prob
         do = do.contiguous()
@@ -319,18 +371,24 @@ class SageBwdAttention(torch.autograd.Function):
         dv = torch.empty_like(v)
         ws = empty_bytes(sagebwd_workspace_bytes(prob, 1), q.device)
         sagebwd_bwd(prob, q, k, v, o, do, lse, saved, dq, dk, dv, ws)
-        return dq, dk, dv, None, None, None, None, None, None, None
+        _queue_status(ws, "sagebwd_bwd")
+        return dq, dk, dv, None, None, None, None, None, None, None, None, None
 
 
 def attention(q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False,
-              qk_subexp=False, smooth_q=False):
+              qk_subexp=True, smooth_q=False, flags=0, wait_timeout_ms=0):
     """SageBwd attention on BF16 [B, H, N, d] CUDA tensors (GQA when k/v have fewer heads).
 
     balance_qk turns on the library's power-of-two Q/K channel balancing before quantization
     (for inputs with channel outliers; Q K^T is unchanged exactly); ds_subexp refines the dS codes
     with power-of-two sub-scales per key and 32-query group (dQ, dK several times closer to exact);
-    qk_subexp refines Q and K with power-of-two sub-scales per 8-channel group of each block;
+    qk_subexp (on by default, the library's Q/K granularity) refines Q and K with power-of-two
+    sub-scales per 8-channel group of each block; qk_subexp=False keeps one scale per block;
     smooth_q subtracts each 128-token block's channel means from Q before quantizing and adds their
-    logit term back in FP32 (for queries with a large common offset; not with balance_qk)."""
+    logit term back in FP32 (for queries with a large common offset; not with balance_qk).
+    flags (SAGEBWD_FLAG_*) and wait_timeout_ms pass through to the library (0: defaults).
+
+    Device-side errors of a call (a bounded wait that ran out) raise SageBwdError at the next
+    forward or backward call once the failing kernels have finished, or at check_errors()."""
     return SageBwdAttention.apply(q, k, v, causal, softmax_scale, smooth_k, balance_qk, ds_subexp, qk_subexp,
-                                  smooth_q)
+                                  smooth_q, flags, wait_timeout_ms)

@@ -31,8 +31,8 @@ sagebwd_status check_problem(const sagebwd_problem* p) {
   if (p->smooth_q && p->balance_qk) return SAGEBWD_ERR_UNSUPPORTED;  // not defined together
   if (p->smooth_q && nblocks(p->N) > 65535) return SAGEBWD_ERR_UNSUPPORTED;  // logit-term grid limit
   if (p->flags & SAGEBWD_FLAG_DEBUG_DUMP) {
-    // the dump covers the plain kernels (integer-valued operands), at most 2^31 bytes
-    if (p->ds_subexp || p->qk_subexp || p->smooth_q) return SAGEBWD_ERR_UNSUPPORTED;
+    // the dump covers the kernels without dS sub-scales and Q-smoothing, at most 2^31 bytes
+    if (p->ds_subexp || p->smooth_q) return SAGEBWD_ERR_UNSUPPORTED;
     const double nb = nblocks(p->N);
     if ((double)p->B * p->Hq * nb * nb * (98304.0 + 1536.0 * p->d) >= 2147483648.0) return SAGEBWD_ERR_UNSUPPORTED;
   }

@@ -29,13 +29,20 @@
  * the block quantizers, which leaves Q K^T unchanged exactly and evens out
  * channel outliers between the two operands; dQ is multiplied by 2^-e and
  * dK by 2^e when they are converted to BF16.
- * Optional Q/K sub-scales (qk_subexp = 1; off by default, this library's finer
- * Q/K granularity): each 8-channel group of a 128-token block of Q and of K
- * keeps the block scale and is refined by 2^k, k = clamp(floor(log2(block max
- * / group max)), 0, 8) (0 if the group max is below 2^-100): stored value
- * rint(x * 127/max * 2^k) * 2^-k, exact in BF16 (x_q of sagebwd_quantize then
- * holds such values for Q and K).  Channel outliers then cost precision only
- * in their own group.
+ * Q/K sub-scales (qk_subexp = 1: this library's default Q/K granularity, which
+ * the Python binding and the benchmark select unless told otherwise; 0 keeps
+ * one scale per block, the plainest reading): each 8-channel group of a
+ * 128-token block of Q and of K keeps the block scale and is refined by 2^k,
+ * k = clamp(floor(log2(block max / group max)), 0, 8) (0 if the group max is
+ * below 2^-100): stored value rint(x * 127/max * 2^k) * 2^-k, exact in BF16
+ * (x_q of sagebwd_quantize then holds such values for Q and K).  Channel
+ * outliers then cost precision only in their own group: on inputs with 1% of
+ * the channels scaled x20 the plain mode misses cosine similarity 0.995 (O) /
+ * 0.99 (dQ, dK) against exact attention and this mode meets it; on inputs
+ * without channel outliers (QK-normed, or roughly Gaussian per channel) every
+ * k is 0 and both modes give the same codes.  (The
+ * SageBwd pages fix INT8 per-block quantization of Q and K, Abstract, but no
+ * block shape; the sub-scales are a power-of-two refinement inside the block.)
  * Optional dS sub-scales (ds_subexp = 1; off by default, this library's finer
  * dS granularity): the tile keeps its scale max|dS| / 127, and each key's codes
  * within a group of 32 queries of the tile are refined by 2^k,
@@ -103,7 +110,7 @@ enum { SAGEBWD_Q = 0, SAGEBWD_K = 1, SAGEBWD_V = 2, SAGEBWD_DO = 3 };
 #define SAGEBWD_FLAG_DEBUG_DUMP 0x2u    /* parity checking: the attention kernels also write every tile's
                                            INT8-semantics operands and raw tensor-core products into the
                                            workspace (layout at sagebwd_debug_dump_offset; small problems
-                                           only; not with ds_subexp, qk_subexp or smooth_q) */
+                                           only; not with ds_subexp or smooth_q) */
 
 typedef struct {
   int32_t B, Hq, Hkv, N, d;
@@ -111,7 +118,8 @@ typedef struct {
   int32_t smooth_k;     /* 1: subtract the per-channel mean of K over tokens before quantizing (the method) */
   int32_t balance_qk;   /* 1: power-of-two Q/K channel balancing before quantizing (see above); 0 in the method */
   int32_t ds_subexp;    /* 1: dS sub-scales per key and 32-query group (see above); 0: one dS scale per tile */
-  int32_t qk_subexp;    /* 1: Q/K sub-scales per 8-channel group of each block (see above); 0: block scale only */
+  int32_t qk_subexp;    /* 1 (recommended default): Q/K sub-scales per 8-channel group of each block (see
+                           above); 0: one scale per block */
   int32_t smooth_q;     /* 1: Q-smoothing, block means of Q subtracted (see above); 0: plain Q (the default) */
   uint32_t flags;       /* SAGEBWD_FLAG_* (0 in normal use) */
   float softmax_scale;  /* <= 0 selects 1/sqrt(d) */
@@ -163,9 +171,13 @@ sagebwd_status sagebwd_quantize(const sagebwd_problem* prob, int which, const vo
 sagebwd_status sagebwd_fwd(const sagebwd_problem* prob, const void* q, const void* k, const void* v, void* o,
                            float* lse, void* saved, void* ws, void* stream);
 
-/* Backward: D = rowsum(dO * O) and the quantized dO, then the fused backward
- * (S recompute, dV = P^T dO, dP = dO V^T in BF16, dS = P (dP - D),
- * dK = dS^T Q, dQ = dS K) and the FP32 -> BF16 conversion of dQ.
+/* Backward ("SageBwd: A Trainable Low-bit Attention", Abstract: the INT8 S
+ * recompute and the INT8 products dV = P^T dO, dQ = dS K, dK = dS^T Q; the
+ * "SageAttention3 ... 8-Bit Training" summary page, Approach: dP = dO V^T kept
+ * in 16-bit floating point; D = rowsum(dO * O) and dS = P (dP - D) from the
+ * FlashAttention-2 backward listed under "Builds on"): D and the quantized dO,
+ * then the fused backward (S recompute, dV = P^T dO, dP = dO V^T in BF16,
+ * dS = P (dP - D), dK = dS^T Q, dQ = dS K) and the FP32 -> BF16 conversion of dQ.
  *   q, k, v, o, dO : the forward's inputs and output and the gradient of o.
  *   lse, saved     : exactly as produced by sagebwd_fwd for these inputs.
  *   dq : BF16 [B][Hq][N][d]; dk, dv : BF16 [B][Hkv][N][d] (summed over the
@@ -222,7 +234,9 @@ sagebwd_status sagebwd_bwd_finish(const sagebwd_problem* prob, const void* saved
  *     before any launch.  With smooth_k == 0 no scratch is used.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.  It allocates nothing at any time.
+ *     before any stream capture.  The address is kept per device and context:
+ *     after cudaDeviceReset the next call looks it up again (and that call,
+ *     too, should come before any capture).  It allocates nothing at any time.
  *   - All calls share the one array: calls that can overlap on the GPU (other
  *     streams, other host threads) race and must be serialized by the caller.
  *     Every partial sum is written before it is read, so the array needs no
@@ -244,7 +258,9 @@ const char* sagebwd_status_string(sagebwd_status s);
  * query block i, key block j), at index ((b*Hq + h)*nb + i)*nb + j, nb =
  * ceil(N/128); records of tiles a causal problem skips are not written.
  * Forward record (T_f = 128*128*4 + 128*128*2 + 128*d*4 bytes):
- *   FP32 S_int [128 queries][128 keys] = Q^ K^T of the codes, as accumulated;
+ *   FP32 S_int [128 queries][128 keys] = Q^ K^T of the stored values, as accumulated (integers
+ *   without Q/K sub-scales; with them sums of (code 2^-k)(code 2^-k') products, which FP32 need
+ *   not hold exactly);
  *   BF16 P~ codes [128 queries][128 keys];  FP32 [P^ V^] [128 queries][d].
  * Backward record (T_b = 2*128*128*2 + 3*128*d*4 bytes):
  *   BF16 P^T codes [128 keys][128 queries];  BF16 dS codes [128 keys][128 queries];

@@ -17,6 +17,7 @@ static sagebwd_problem make(int B, int Hq, int Hkv, int N, int d, int causal) {
   p.d = d;
   p.causal = causal;
   p.smooth_k = 1;
+  p.qk_subexp = 1; /* the library's default Q/K granularity */
   return p;
 }
 

@@ -124,8 +124,8 @@ def test_q_smoothing_sizes_and_rejections(lib):
 
 def test_debug_dump_sizes_and_rejections(lib):
     """SAGEBWD_FLAG_DEBUG_DUMP adds one record per tile to each workspace (forward 128*128*6 + 512 d
-    bytes, backward 65536 + 1536 d bytes) and is refused with the options whose operands are not
-    integer-valued (dS or Q/K sub-scales, Q-smoothing)."""
+    bytes, backward 65536 + 1536 d bytes), with the Q/K sub-scales (the default) or without, and is
+    refused with the dS sub-scales and Q-smoothing (other kernel instantiations)."""
     p0 = sb.Problem.make(1, 2, 1, 300, 64, True)
     p1 = sb.Problem.make(1, 2, 1, 300, 64, True, flags=sb.FLAG_DEBUG_DUMP)
     nb = 3
@@ -134,7 +134,9 @@ def test_debug_dump_sizes_and_rejections(lib):
     assert sb.sagebwd_workspace_bytes(p1, 1) == sb.sagebwd_workspace_bytes(p0, 1) + al(2 * nb * nb * (65536 + 1536 * 64))
     assert sb.sagebwd_debug_dump_offset(p0, 0) == 0 and sb.sagebwd_debug_dump_offset(p1, 1) > 0
     assert sb.sagebwd_debug_dump_offset(p1, 0) + al(2 * nb * nb * (98304 + 512 * 64)) == sb.sagebwd_workspace_bytes(p1, 0)
-    for opt in ("ds_subexp", "qk_subexp", "smooth_q"):
+    plain = sb.Problem.make(1, 2, 1, 300, 64, True, flags=sb.FLAG_DEBUG_DUMP, qk_subexp=False)
+    assert sb.sagebwd_workspace_bytes(plain, 1) == sb.sagebwd_workspace_bytes(p1, 1)
+    for opt in ("ds_subexp", "smooth_q"):
         bad = sb.Problem.make(1, 2, 1, 300, 64, True, flags=sb.FLAG_DEBUG_DUMP, **{opt: True})
         assert sb.sagebwd_workspace_bytes(bad, 1) == 0, opt
     huge = sb.Problem.make(1, 32, 8, 65536, 128, False, flags=sb.FLAG_DEBUG_DUMP)

@@ -29,18 +29,25 @@ SMALL = [
 
 
 def check_quantized(oracle_mod, w, x, fwd, smooth_k=True):
-    op = oracle_problem(oracle_mod, w, smooth_k)
+    """Q^, K^ (with the default Q/K sub-scales: codes times 2^-k), V^, the block scales and the K mean
+    bit for bit against the oracle's quantizers."""
+    qk_subexp = bool(fwd["prob"].qk_subexp)
+    op = oracle_problem(oracle_mod, w, smooth_k, qk_subexp=qk_subexp)
     views = sb.quantized_views(fwd["prob"], fwd["saved"])
-    for name, key, BH, smooth in (("q", "q", w.B * w.Hq, False), ("k", "k", w.B * w.Hkv, smooth_k),
-                                  ("v", "v", w.B * w.Hkv, False)):
-        codes, scales, mean = oracle_mod.quantize(op, x[key], BH, smooth)
-        gcodes = views[name].float().cpu().numpy().reshape(codes.shape)
-        np.testing.assert_array_equal(gcodes, codes.astype(np.float32), err_msg=f"{name} codes")
-        gs = views["s" + name].cpu().numpy()
-        np.testing.assert_array_equal(gs.view(np.uint32), scales.view(np.uint32), err_msg=f"{name} scales")
-        if smooth:
-            gm = views["mu"].cpu().numpy()
-            np.testing.assert_array_equal(gm.view(np.uint32), mean.view(np.uint32), err_msg="k mean")
+    ref = oracle_mod.quantize_qk(op, x["q"], x["k"])
+    for name in ("q", "k"):
+        g = views[name].float().cpu().numpy().reshape(ref[name].shape)
+        np.testing.assert_array_equal(g, ref[name], err_msg=f"{name} values")
+        np.testing.assert_array_equal(views["s" + name].cpu().numpy().view(np.uint32),
+                                      ref["s" + name].view(np.uint32), err_msg=f"{name} scales")
+    if smooth_k:
+        np.testing.assert_array_equal(views["mu"].cpu().numpy().view(np.uint32), ref["mu"].view(np.uint32),
+                                      err_msg="k mean")
+    codes, scales, _ = oracle_mod.quantize(op, x["v"], w.B * w.Hkv, False)
+    gcodes = views["v"].float().cpu().numpy().reshape(codes.shape)
+    np.testing.assert_array_equal(gcodes, codes.astype(np.float32), err_msg="v codes")
+    np.testing.assert_array_equal(views["sv"].cpu().numpy().view(np.uint32), scales.view(np.uint32),
+                                  err_msg="v scales")
 
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)

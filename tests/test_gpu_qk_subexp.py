@@ -1,5 +1,7 @@
-"""GPU parity of the optional Q/K sub-scales (qk_subexp), alone and with the other
-refinements (channel balancing, dS sub-scales), against the oracle.
+"""GPU parity of the Q/K granularity against the oracle: the library's default Q/K
+sub-scales (qk_subexp), alone and with the other refinements (channel balancing,
+dS sub-scales), and the plain one-scale-per-block mode (qk_subexp=False, the
+pages' plainest reading), which every other GPU test leaves aside.
 
 The stored Q^ and K^ values (codes times 2^-k per 8-channel group of a block),
 the block scales and the K means must equal the oracle's bit for bit; O, LSE,
@@ -117,3 +119,30 @@ def test_all_refinements_full_size_long_context(oracle_mod):
     rows = np.isfinite(ex["o"]) & mq
     assert cos(o[rows], ex["o"][rows]) >= 0.995
     assert cos(to_np(bwd["dq"])[mq], ex["dq"][mq]) >= 0.99
+
+
+PLAIN = [
+    W.small("plain_gqa_causal_300_d64", 1, 4, 2, 300, 64, True, 621, qk_norm=True, k_offset_sd=2.0),
+    W.small("plain_outlier_gqa_nc_257_d128", 2, 3, 1, 257, 128, False, 622, outlier_frac=0.02),
+    W.small("plain_outlier_causal_384_d128", 1, 6, 1, 384, 128, True, 623, outlier_frac=0.01),
+    W.small("plain_n1_d64", 1, 2, 1, 1, 64, True, 624),
+]
+
+
+@pytest.mark.parametrize("w", PLAIN, ids=lambda w: w.name)
+def test_plain_block_scales_forward_backward(oracle_mod, w):
+    """qk_subexp=False: one FP32 scale per 128-token block of Q and K, all the way through."""
+    x, xd = device_inputs(w)
+    fwd = gpu_forward(w, xd, qk_subexp=False)
+    bwd = gpu_backward(w, xd, fwd)
+    assert fwd["status"] == 0 and bwd["status"] == 0
+    check_values(oracle_mod, w, x, fwd, dict(qk_subexp=False))
+    views = sb.quantized_views(fwd["prob"], fwd["saved"])
+    for name in ("q", "k"):  # integer codes: no sub-scale anywhere
+        a = views[name].float().cpu().numpy()
+        assert np.all(a == np.round(a)), name
+    ref = oracle_mod.pipeline(oracle_problem(oracle_mod, w, qk_subexp=False), x["q"], x["k"], x["v"], x["do"])
+    assert_parity(to_np(fwd["o"]), ref["o"], "O")
+    np.testing.assert_allclose(to_np(fwd["lse"]), ref["lse"], rtol=0, atol=LSE_TOL)
+    for key in ("dq", "dk", "dv"):
+        assert_parity(to_np(bwd[key]), ref[key], key)
