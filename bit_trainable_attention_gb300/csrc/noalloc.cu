@@ -9,6 +9,8 @@
 // entry point serves them with a fixed scratch array compiled into the
 // library: every GPU that loads the library reserves it (8 MiB) until the
 // process exits.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "sagebwd_internal.h"
@@ -22,18 +24,48 @@ static __device__ __align__(256) double g_kmean_scratch[kScratchDoubles];
 constexpr int kMaxDevices = 64;
 std::mutex g_lock;
 double* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // id of the context the address belongs to
 
-// Device address of the scratch array on the current device, looked up once per
-// device (the host-side symbol is only a stand-in and must not reach a kernel).
+// Unique id of the calling thread's current CUDA context (the driver never reuses one within a
+// process), or 0 when it cannot be read.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context, looked up once per device and
+// context (the host-side symbol is only a stand-in and must not reach a kernel).  A context that was
+// destroyed (cudaDeviceReset) and created again has a new id, so the address is looked up again; when
+// the id cannot be read the address is looked up on every call.
 double* scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> guard(g_lock);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_kmean_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = static_cast<double*>(ptr);
-  }
+  const unsigned long long ctx = current_context_id();
+  if (g_scratch_ptr[dev] != nullptr && ctx != 0 && ctx == g_scratch_ctx[dev]) return g_scratch_ptr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_kmean_scratch) != cudaSuccess) return nullptr;
+  g_scratch_ptr[dev] = static_cast<double*>(ptr);
+  g_scratch_ctx[dev] = current_context_id();  // the lookup made the runtime's context current
   return g_scratch_ptr[dev];
 }
 

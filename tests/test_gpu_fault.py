@@ -49,3 +49,26 @@ def test_dropped_load_times_out_and_the_context_survives(oracle_mod, causal):
     np.testing.assert_allclose(to_np(good["lse"]), lse_ref, rtol=0, atol=LSE_TOL)
     bwd = gpu_backward(w, xd, good)
     assert bwd["status"] == 0
+
+
+def test_autograd_path_reports_a_device_timeout():
+    """The autograd path does not synchronize after each call; the status word of every call is read
+    back behind its kernels and a non-OK word raises at the next call (here the backward of the same
+    forward) or at check_errors()."""
+    w = W.small("fault_autograd", 1, 2, 2, 512, 64, False, 302)
+    _, xd = device_inputs(w)
+    q, k, v = (xd[n].clone().requires_grad_(True) for n in ("q", "k", "v"))
+    o = sb.attention(q, k, v, flags=SAGEBWD_FLAG_DROP_ONE_LOAD, wait_timeout_ms=100)
+    torch.cuda.synchronize()
+    with pytest.raises(RuntimeError, match="TIMEOUT"):
+        o.backward(xd["do"])
+    sb.check_errors()  # reported once
+    o = sb.attention(q, k, v, flags=SAGEBWD_FLAG_DROP_ONE_LOAD, wait_timeout_ms=100)
+    with pytest.raises(sb.SageBwdError) as err:
+        sb.check_errors()
+    assert err.value.code == SAGEBWD_ERR_TIMEOUT
+    # ordinary calls afterwards raise nothing
+    q.grad = k.grad = v.grad = None
+    sb.attention(q, k, v).backward(xd["do"])
+    sb.check_errors()
+    assert q.grad is not None and torch.isfinite(q.grad.float()).all()
