@@ -39,10 +39,10 @@ INT8_MMA_SYNC_TOPS = 150.5
 INT8_TORCH_INT_MM_TOPS = 78.3
 
 
-# DRAM bytes (read + write) of one bwd_kernel launch on the qwen15b workload, from
-# the one-pass ncu capture summarised in profiles/bwd_kernel_qwen15b_ncu.md.  The
-# figure belongs to the kernel sources it was taken from: once any of them changes
-# the line reports null until the capture is repeated.
+# DRAM bytes (read + write) of one bwd_kernel launch on the qwen15b workload, from a
+# one-pass ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of the timed step's
+# launch).  The figure belongs to the kernel sources it was taken from: once any of them
+# changes the line reports null until the capture is repeated.
 BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 777630464 + 285536000,
                "sources_sha256": "fec5f7a1719768235bf01f0e4553c74737ce782fc1533fd00ec2b940f25784e9"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
@@ -139,7 +139,7 @@ class ClockSampler:
 class Step:
     """Buffers and the stage-by-stage calls of one forward + backward step."""
 
-    def __init__(self, w: W.Workload, dev, balance_qk=False, ds_subexp=False, qk_subexp=False, inputs=None,
+    def __init__(self, w: W.Workload, dev, balance_qk=False, ds_subexp=False, qk_subexp=True, inputs=None,
                  smooth_q=False):
         self.w = w
         x = W.make_inputs(w) if inputs is None else inputs
@@ -518,6 +518,108 @@ def describe(w: W.Workload) -> str:
     return (f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.N} d={w.d} {'causal' if w.causal else 'non-causal'}")
 
 
+# ---------------------------------------------------------------------------- per-kernel times
+KERNELS = ("kmean_partial_kernel", "kmean_final_kernel", "qk_stats_partial_kernel", "qk_stats_final_kernel",
+           "quantize_kernel", "qsmooth_bias_kernel", "fwd_kernel", "bwd_prep_kernel", "bwd_kernel",
+           "grad_convert_kernel")
+
+
+def _kernel_of(name: str):
+    for k in KERNELS:
+        if k + "<" in name or k + "(" in name or name.endswith(k):
+            return k
+    return None
+
+
+def kernel_times(step: "Step", flush: torch.Tensor, steps: int = 3):
+    """Device time of each of the library's kernels per step (CUPTI activity records through
+    torch.profiler, outside the timed region): {kernel: (launches per step, mean us per launch)}."""
+    from torch.profiler import ProfilerActivity, profile
+    for _ in range(2):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        for _ in range(steps):
+            flush.zero_()
+            step.run()
+        torch.cuda.synchronize()
+    agg = {}
+    for e in prof.key_averages():
+        k = _kernel_of(e.key)
+        if k is None:
+            continue
+        t = getattr(e, "device_time_total", None)
+        if t is None:
+            t = getattr(e, "cuda_time_total", 0.0)
+        n, tot = agg.get(k, (0, 0.0))
+        agg[k] = (n + e.count, tot + float(t))
+    return {k: (n / steps, tot / n) for k, (n, tot) in agg.items() if n > 0}
+
+
+def quantize_bandwidth(w: W.Workload, prob, times: dict, hbm_gbs: float):
+    """HBM GB/s of each kernel of the quantize stage: algorithmic bytes per launch (each input
+    element read once per pass that must read it, each output written once) / device time.
+    The quantized values are stored as 2-byte integer-valued BF16 (the tensor cores' operand form)."""
+    nb = (w.N + 127) // 128
+    qe, ke = w.B * w.Hq * w.N * w.d, w.B * w.Hkv * w.N * w.d
+    scales = 4 * nb * (w.B * w.Hq + 2 * w.B * w.Hkv)
+    part = 8 * w.B * w.Hkv * nb * w.d  # FP64 partial channel sums of K
+    mean = 4 * w.B * w.Hkv * w.d
+    alg = {
+        "kmean_partial_kernel": 2 * ke + part,
+        "kmean_final_kernel": part + mean,
+        # reads Q, K, V (and the K mean), writes the three code tensors and their block scales
+        "quantize_kernel": 2 * (qe + 2 * ke) + mean + 2 * (qe + 2 * ke) + scales,
+    }
+    out = {}
+    for k, b in alg.items():
+        if k in times:
+            launches, us = times[k]
+            gbs = b / (us * 1e-6) / 1e9
+            out[k] = {"bytes_per_launch": int(b), "us_per_launch": round(us, 2), "gb_per_s": round(gbs, 1),
+                      "frac_of_hbm": round(gbs / hbm_gbs, 3)}
+    stage_b = sum(alg[k] for k in alg if k in times)
+    stage_us = sum(times[k][1] * times[k][0] for k in alg if k in times)
+    if stage_us > 0:
+        out["stage"] = {"bytes": int(stage_b), "us": round(stage_us, 2),
+                        "gb_per_s": round(stage_b / (stage_us * 1e-6) / 1e9, 1),
+                        "frac_of_hbm": round(stage_b / (stage_us * 1e-6) / 1e9 / hbm_gbs, 3)}
+    return out
+
+
+def roofline_peak(peaks: dict, clocks: dict):
+    """The BF16 dense denominator for the backward kernel: the burst figure, unless the clock record
+    of the timed region shows the power cap (then the seconds-long sustained figure)."""
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    return (peaks["bf16_sustained"], "sustained") if capped else (peaks["bf16_burst"], "burst")
+
+
+def config_summary(w: W.Workload, dev, args, flush, peaks):
+    """A second configuration of the metric (the 8K-token GQA layer), timed like the headline:
+    ms and TOPS of the step, the backward kernel's fraction of the BF16 peaks, CosSim vs FP32."""
+    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp, qk_subexp=not args.qk_plain,
+                smooth_q=args.smooth_q)
+    total, stage = time_device(step, max(10, args.steps // 2), max(3, args.warmup), flush, lambda: None)
+    ms = sum(total) / len(total)
+    st = [sum(x) / len(x) for x in stage]
+    bwd_tf = w.flops_bwd() / (st[3] * 1e-3) / 1e12
+    fwd_tf = w.flops_fwd() / (st[1] * 1e-3) / 1e12
+    out = {"workload": describe(w), "ms_per_step": round(ms, 4),
+           "tops": round((w.flops_fwd() + w.flops_bwd()) / (ms * 1e-3) / 1e12, 2),
+           "breakdown_ms": {"quantize": round(st[0], 4), "fwd": round(st[1], 4), "bwd_prepare": round(st[2], 4),
+                            "bwd": round(st[3], 4), "grad_convert": round(st[4], 4)},
+           "bwd_kernel_tflops": round(bwd_tf, 1), "bwd_frac_bf16_burst": round(bwd_tf / peaks["bf16_burst"], 4),
+           "fwd_kernel_tflops": round(fwd_tf, 1), "fwd_frac_bf16_burst": round(fwd_tf / peaks["bf16_burst"], 4),
+           "cossim_vs_torch_fp32": None if args.no_cossim else cossim_vs_torch(step)}
+    code0, _ = sb.sagebwd_check_status(step.ws0)
+    code1, _ = sb.sagebwd_check_status(step.ws1)
+    out["status"] = [code0, code1]
+    del step
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -533,19 +635,24 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end pass (profiling runs)")
     ap.add_argument("--no-cossim", action="store_true", help="skip the cosine-similarity reference (profiling runs)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="profiling runs: skip the second configuration, the layer stack, the per-kernel times "
+                         "and the other option settings")
     ap.add_argument("--compare-sdpa", action="store_true",
                     help="also time PyTorch's BF16 SDPA forward + backward on the same inputs (context)")
     ap.add_argument("--balance-qk", action="store_true",
                     help="time the library's optional Q/K channel balancing (the other settings are reported beside)")
     ap.add_argument("--ds-subexp", action="store_true",
                     help="time the library's optional dS sub-scales (the other settings are reported beside)")
-    ap.add_argument("--qk-subexp", action="store_true",
-                    help="time the library's optional Q/K sub-scales (the other settings are reported beside)")
+    ap.add_argument("--qk-plain", action="store_true",
+                    help="time the plain one-scale-per-block Q/K mode instead of the default Q/K sub-scales")
     ap.add_argument("--smooth-q", action="store_true",
                     help="time the library's optional Q-smoothing (block means of Q subtracted, logit term added)")
-    ap.add_argument("--layer-step", type=int, default=0, metavar="TOKENS",
+    ap.add_argument("--layer-step", type=int, default=8192, metavar="TOKENS",
                     help="also time a Llama-1B-shaped 16-layer stack forward + backward at TOKENS tokens with this "
-                         "library's attention and with torch SDPA (context; not the headline)")
+                         "library's attention and with torch SDPA (context; 0 skips it)")
+    ap.add_argument("--second-config", default="llama1b", choices=sorted(W.WORKLOADS) + ["none"],
+                    help="the metric's other sequence length, reported as per_config (not the headline)")
     ap.add_argument("--seq", type=int, default=0,
                     help="profiling only: override the workload's sequence length (the line then names it)")
     args = ap.parse_args()
@@ -577,7 +684,7 @@ def main():
         cpu = cpu_baseline(w, args.cpu_budget_s)
 
     sb.load_library()
-    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp, qk_subexp=args.qk_subexp,
+    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp, qk_subexp=not args.qk_plain,
                 smooth_q=args.smooth_q)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(local)
@@ -601,14 +708,18 @@ def main():
     value = whole_job_tops(ops, ms, world)
     stage_ms = [sum(s) / len(s) for s in stage]
     peaks = load_peaks()
+    peak, peak_kind = roofline_peak(peaks, clocks)
     bwd_ms = stage_ms[3]
     achieved = w.flops_bwd() / (bwd_ms * 1e-3) / 1e12
+    fwd_achieved = w.flops_fwd() / (stage_ms[1] * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 (integer-valued bf16 on tcgen05, fp32 accumulate) + bf16 dP",
         "data": "synthetic",
         "config": {"workload": describe(w), "l2": "flushed between timed steps (256 MB write)",
+                   "qk_granularity": "per-block scale + 8-channel power-of-two sub-scales (library default)"
+                   if not args.qk_plain else "one scale per 128-token block",
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
         "breakdown_ms": {"quantize": round(stage_ms[0], 4), "fwd": round(stage_ms[1], 4),
                          "bwd_prepare": round(stage_ms[2], 4), "bwd": round(stage_ms[3], 4),
@@ -616,19 +727,26 @@ def main():
         "tops": {"fwd_incl_quantize": round(w.flops_fwd() / ((stage_ms[0] + stage_ms[1]) * 1e-3) / 1e12, 2),
                  "bwd_incl_prepare": round(w.flops_bwd() / (sum(stage_ms[2:]) * 1e-3) / 1e12, 2)},
         "roofline": {"kernel": "sagebwd bwd_kernel", "bound": "tensor", "achieved": round(achieved, 2),
-                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": round(achieved / peaks["bf16_sustained"], 4), "traffic": bwd_traffic(w),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": bwd_traffic(w),
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-                     "peak_kind": f"bf16 dense, sustained ({peaks['source']})"},
-        "int8_peak_frac": {"vs_mma_sync_s8": round(value / world / INT8_MMA_SYNC_TOPS, 3),
-                           "vs_torch_int_mm": round(value / world / INT8_TORCH_INT_MM_TOPS, 3),
-                           "vs_bf16_dense_burst": round(value / world / peaks["bf16_burst"], 4)},
+                     "peak_kind": f"bf16 dense, {peak_kind} ({peaks['source']}): burst unless the timed "
+                                  "region's clock record shows sw_power_cap",
+                     "frac_of_burst": round(achieved / peaks["bf16_burst"], 4),
+                     "frac_of_sustained": round(achieved / peaks["bf16_sustained"], 4),
+                     "fwd_kernel": {"achieved": round(fwd_achieved, 2),
+                                    "frac_of_burst": round(fwd_achieved / peaks["bf16_burst"], 4)}},
+        "int8_peak_frac": {"vs_mma_sync_s8_ratio": round(value / world / INT8_MMA_SYNC_TOPS, 3),
+                           "vs_torch_int_mm_ratio": round(value / world / INT8_TORCH_INT_MM_TOPS, 3),
+                           "vs_bf16_dense_burst": round(value / world / peaks["bf16_burst"], 4),
+                           "note": "ratios to the legacy INT8 paths measured on this GPU (mma.sync s8, "
+                                   "torch._int_mm), not peak fractions: tcgen05 kind::i8 does not exist on "
+                                   "sm_103a; the BF16 fraction is the peak of the instructions used"},
         "e2e": None if e2e_ms is None else {
             "value": round(world * ops / (e2e * 1e-3) / 1e12, 3), "unit": "TOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4),
             "copies": "double-buffered on two copy streams: step i+1's inputs up and step i-1's results down while "
                       "step i computes; each step timed from the end of its L2 flush"},
-        "balance_qk": bool(args.balance_qk), "qk_subexp": bool(args.qk_subexp), "ds_subexp": bool(args.ds_subexp),
+        "balance_qk": bool(args.balance_qk), "qk_subexp": not args.qk_plain, "ds_subexp": bool(args.ds_subexp),
         "smooth_q": bool(args.smooth_q),
         "gpu_launches": step.launches() * args.steps,
         "clocks": clocks,
@@ -636,11 +754,24 @@ def main():
     }
     if rank == 0:
         line["cossim_vs_torch_fp32"] = None if args.no_cossim else cossim_vs_torch(step)
-        if not args.no_cossim:
-            line["other_settings"] = other_settings(step, args, dev, flush)
+        if not args.no_extras:
+            try:
+                times = kernel_times(step, flush)
+                line["kernel_us"] = {k: {"launches_per_step": n, "us_per_launch": round(us, 2)}
+                                     for k, (n, us) in sorted(times.items())}
+                line["quantize_hbm"] = quantize_bandwidth(w, step.prob, times, peaks["hbm_gbs"])
+            except Exception as exc:  # noqa: BLE001 - the profiler is context, not the measurement
+                line["kernel_us"] = {"unavailable": f"{type(exc).__name__}: {exc}"}
+            if not args.no_cossim:
+                line["other_settings"] = other_settings(step, args, dev, flush)
         if args.compare_sdpa:
             line["torch_sdpa_bf16"] = time_torch_sdpa(step, max(5, args.steps // 2), args.warmup, flush)
-        if args.layer_step > 0:
+        if not args.no_extras and args.second_config != "none" and args.second_config != w.name:
+            del step
+            torch.cuda.empty_cache()
+            line["per_config"] = {args.second_config: config_summary(W.WORKLOADS[args.second_config], dev, args,
+                                                                     flush, peaks)}
+        if not args.no_extras and args.layer_step > 0:
             line["layer_step"] = time_layer_stack(args.layer_step, max(3, args.steps // 5), 2, dev)
         line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
