@@ -140,13 +140,13 @@ class Step:
     """Buffers and the stage-by-stage calls of one forward + backward step."""
 
     def __init__(self, w: W.Workload, dev, balance_qk=False, ds_subexp=False, qk_subexp=True, inputs=None,
-                 smooth_q=False):
+                 smooth_q=False, flags=0):
         self.w = w
         x = W.make_inputs(w) if inputs is None else inputs
         self.host = x
         self.x = {k: v.to(dev) for k, v in x.items()}
         self.prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, balance_qk=balance_qk,
-                                    ds_subexp=ds_subexp, qk_subexp=qk_subexp, smooth_q=smooth_q)
+                                    ds_subexp=ds_subexp, qk_subexp=qk_subexp, smooth_q=smooth_q, flags=flags)
         p = self.prob
         self.o = torch.empty_like(self.x["q"])
         self.lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
@@ -212,22 +212,51 @@ def time_torch_sdpa(step: Step, steps: int, warmup: int, flush: torch.Tensor):
             "dtype": "bf16", "note": "torch.nn.functional.scaled_dot_product_attention fwd+bwd, same shapes"}
 
 
+_REF_CACHE = {}
+
+
+def torch_reference(step: Step):
+    """O, dQ, dK, dV of PyTorch FP32 attention on the step's inputs (computed once per input set)."""
+    key = (step.w, id(step.host))
+    if key not in _REF_CACHE:
+        _REF_CACHE.clear()
+        w, x = step.w, step.x
+        q = x["q"].float().requires_grad_(True)
+        k = x["k"].float().requires_grad_(True)
+        v = x["v"].float().requires_grad_(True)
+        kk = k.repeat_interleave(w.G, dim=1)
+        vv = v.repeat_interleave(w.G, dim=1)
+        o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=w.causal)
+        o.backward(x["do"].float())
+        _REF_CACHE[key] = {"o": o.detach(), "dq": q.grad, "dk": k.grad, "dv": v.grad}
+    return _REF_CACHE[key]
+
+
 def cossim_vs_torch(step: Step):
     """Cosine similarity of O, dQ, dK, dV against PyTorch FP32 attention (not timed)."""
-    w, x = step.w, step.x
-    q = x["q"].float().requires_grad_(True)
-    k = x["k"].float().requires_grad_(True)
-    v = x["v"].float().requires_grad_(True)
-    kk = k.repeat_interleave(w.G, dim=1)
-    vv = v.repeat_interleave(w.G, dim=1)
-    o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=w.causal)
-    o.backward(x["do"].float())
-    ref = {"o": o.detach(), "dq": q.grad, "dk": k.grad, "dv": v.grad}
+    ref = torch_reference(step)
     got = {"o": step.o, "dq": step.dq, "dk": step.dk, "dv": step.dv}
     out = {}
     for name in ("o", "dq", "dk", "dv"):
         a, b = got[name].float().reshape(-1), ref[name].reshape(-1)
         out[name] = round(float(torch.nn.functional.cosine_similarity(a, b, dim=0)), 6)
+    return out
+
+
+def error_attribution(step: Step, dev):
+    """CosSim against FP32 attention with one quantizer at a time storing BF16 of its scaled values
+    instead of INT8 codes (SAGEBWD_FLAG_BF16_*): which quantizer carries the error, on this workload
+    at full size (untimed)."""
+    out = {"none": cossim_vs_torch(step)}
+    for name, flag in sb.FLAG_BF16.items():
+        other = Step(step.w, dev, inputs=step.host, flags=flag, balance_qk=bool(step.prob.balance_qk),
+                     qk_subexp=bool(step.prob.qk_subexp))
+        other.run()
+        torch.cuda.synchronize()
+        code0, _ = sb.sagebwd_check_status(other.ws0)
+        code1, _ = sb.sagebwd_check_status(other.ws1)
+        out[name] = {**cossim_vs_torch(other), "status": [code0, code1]}
+        del other
     return out
 
 
@@ -525,35 +554,48 @@ KERNELS = ("kmean_partial_kernel", "kmean_final_kernel", "qk_stats_partial_kerne
 
 
 def _kernel_of(name: str):
+    """The library kernel a profiler event name belongs to (demangled "...::bwd_kernel<...>(...)" or
+    mangled "...10bwd_kernelI..."), else None."""
+    import re
     for k in KERNELS:
-        if k + "<" in name or k + "(" in name or name.endswith(k):
+        if re.search(r"(?:^|[^A-Za-z_])" + k + r"(?:$|[<(I])", name):
             return k
     return None
 
 
 def kernel_times(step: "Step", flush: torch.Tensor, steps: int = 3):
-    """Device time of each of the library's kernels per step (CUPTI activity records through
-    torch.profiler, outside the timed region): {kernel: (launches per step, mean us per launch)}."""
+    """Device time of each of the library's kernels per step (CUPTI kernel activity records through
+    torch.profiler, read from its exported trace; outside the timed region):
+    {kernel: (launches per step, mean us per launch)}."""
+    import tempfile
     from torch.profiler import ProfilerActivity, profile
     for _ in range(2):
         flush.zero_()
         step.run()
     torch.cuda.synchronize()
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+    with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
         for _ in range(steps):
             flush.zero_()
             step.run()
         torch.cuda.synchronize()
-    agg = {}
-    for e in prof.key_averages():
-        k = _kernel_of(e.key)
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "trace.json")
+        prof.export_chrome_trace(path)
+        with open(path) as f:
+            trace = json.load(f)
+    events = trace["traceEvents"] if isinstance(trace, dict) else trace
+    agg, seen = {}, set()
+    for e in events:
+        if e.get("ph") != "X" or str(e.get("cat", "")).lower() != "kernel":
+            continue
+        seen.add(str(e.get("name", ""))[:80])
+        k = _kernel_of(str(e.get("name", "")))
         if k is None:
             continue
-        t = getattr(e, "device_time_total", None)
-        if t is None:
-            t = getattr(e, "cuda_time_total", 0.0)
         n, tot = agg.get(k, (0, 0.0))
-        agg[k] = (n + e.count, tot + float(t))
+        agg[k] = (n + 1, tot + float(e.get("dur", 0.0)))
+    if not agg:
+        raise RuntimeError(f"no library kernel among the profiled device events: {sorted(seen)[:8]}")
     return {k: (n / steps, tot / n) for k, (n, tot) in agg.items() if n > 0}
 
 
@@ -764,6 +806,8 @@ def main():
                 line["kernel_us"] = {"unavailable": f"{type(exc).__name__}: {exc}"}
             if not args.no_cossim:
                 line["other_settings"] = other_settings(step, args, dev, flush)
+                if not (args.ds_subexp or args.smooth_q):
+                    line["error_attribution"] = error_attribution(step, dev)
         if args.compare_sdpa:
             line["torch_sdpa_bf16"] = time_torch_sdpa(step, max(5, args.steps // 2), args.warmup, flush)
         if not args.no_extras and args.second_config != "none" and args.second_config != w.name:

@@ -23,13 +23,15 @@ __all__ = [
     "sagebwd_quantize", "sagebwd_fwd", "sagebwd_bwd", "sagebwd_fwd_quantize", "sagebwd_fwd_attention",
     "sagebwd_bwd_prepare", "sagebwd_bwd_attention", "sagebwd_bwd_finish", "sagebwd_check_status",
     "sagebwd_status_string", "sagebwd_version", "sagebwd_quantize_k_noalloc", "attention", "SageBwdAttention",
-    "SAGEBWD_Q", "SAGEBWD_K", "SAGEBWD_V", "SAGEBWD_DO", "FLAG_DROP_ONE_LOAD", "FLAG_DEBUG_DUMP",
+    "SAGEBWD_Q", "SAGEBWD_K", "SAGEBWD_V", "SAGEBWD_DO", "FLAG_DROP_ONE_LOAD", "FLAG_DEBUG_DUMP", "FLAG_BF16",
     "sagebwd_debug_dump_offset", "debug_dump_views", "check_errors",
 ]
 
 SAGEBWD_Q, SAGEBWD_K, SAGEBWD_V, SAGEBWD_DO = 0, 1, 2, 3
 FLAG_DROP_ONE_LOAD = 0x1
 FLAG_DEBUG_DUMP = 0x2
+# error attribution: one quantizer stores BF16 of its scaled values instead of INT8 codes
+FLAG_BF16 = {"q": 0x10, "k": 0x20, "v": 0x40, "do": 0x80, "p_fwd": 0x100, "p_bwd": 0x200, "ds": 0x400}
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "MISALIGNED", 4: "CUDA", 5: "TIMEOUT",
                 6: "SCRATCH_LIMIT"}
 

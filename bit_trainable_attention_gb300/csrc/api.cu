@@ -30,6 +30,9 @@ sagebwd_status check_problem(const sagebwd_problem* p) {
   if ((double)nblocks(p->N) * p->B * p->Hq >= 2147483647.0) return SAGEBWD_ERR_UNSUPPORTED;
   if (p->smooth_q && p->balance_qk) return SAGEBWD_ERR_UNSUPPORTED;  // not defined together
   if (p->smooth_q && nblocks(p->N) > 65535) return SAGEBWD_ERR_UNSUPPORTED;  // logit-term grid limit
+  // the attribution instantiations cover the kernels without dS sub-scales, Q-smoothing and the dump
+  if ((p->flags & SAGEBWD_FLAGS_BF16) && (p->ds_subexp || p->smooth_q || (p->flags & SAGEBWD_FLAG_DEBUG_DUMP)))
+    return SAGEBWD_ERR_UNSUPPORTED;
   if (p->flags & SAGEBWD_FLAG_DEBUG_DUMP) {
     // the dump covers the kernels without dS sub-scales and Q-smoothing, at most 2^31 bytes
     if (p->ds_subexp || p->smooth_q) return SAGEBWD_ERR_UNSUPPORTED;
@@ -227,6 +230,9 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
                p->B * p->Hkv, bexp, 1, 1, p->qk_subexp ? 1 : 0};
   qp.job[2] = {static_cast<const __nv_bfloat16*>(v), at<__nv_bfloat16>(saved, S.v), at<float>(saved, S.sv), nullptr,
                p->B * p->Hkv, nullptr, 1, 1};
+  qp.job[0].bf16 = (p->flags & SAGEBWD_FLAG_BF16_Q) ? 1 : 0;
+  qp.job[1].bf16 = (p->flags & SAGEBWD_FLAG_BF16_K) ? 1 : 0;
+  qp.job[2].bf16 = (p->flags & SAGEBWD_FLAG_BF16_V) ? 1 : 0;
   qp.njobs = 3;
   qp.block_start[0] = 0;
   for (int j = 0; j < 3; ++j) qp.block_start[j + 1] = qp.block_start[j] + qp.job[j].BH * nb;
@@ -342,6 +348,7 @@ sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const v
   pp.d = p->d;
   pp.nb = nblocks(p->N);
   pp.status = at<int>(ws, W.status);
+  pp.bf16 = (p->flags & SAGEBWD_FLAG_BF16_DO) ? 1 : 0;
   return cuda_status(launch_bwd_prep(pp, st));
 }
 
@@ -437,6 +444,7 @@ sagebwd_status sagebwd_quantize(const sagebwd_problem* prob, int which, const vo
   qp.job[0] = {static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(x_q), scales,
                smooth ? k_mean : nullptr, BH, nullptr, 1, 1,
                (prob->qk_subexp && (which == SAGEBWD_Q || which == SAGEBWD_K)) ? 1 : 0};
+  qp.job[0].bf16 = (prob->flags & (SAGEBWD_FLAG_BF16_Q << which)) ? 1 : 0;
   qp.njobs = 1;
   qp.block_start[0] = 0;
   qp.block_start[1] = BH * nb;

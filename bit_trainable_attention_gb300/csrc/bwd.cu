@@ -146,7 +146,9 @@ __device__ __forceinline__ void dump16(uint8_t* dst, const uint32_t* w) {
   for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
-template <int D, bool CAUSAL, bool DSX, bool QSM, bool DBG>
+// ATTR (error attribution, SAGEBWD_FLAG_BF16_PB / _DS in p.flags): the P^T and / or dS operands are
+// the BF16 rounding of the scaled values instead of their integer codes (plain instantiation otherwise).
+template <int D, bool CAUSAL, bool DSX, bool QSM, bool DBG, bool ATTR = false>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -589,6 +591,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_after();
       {
         const float2 invP2 = make_float2(invP, invP);
+        const bool pt_bf16 = ATTR && (p.flags & SAGEBWD_FLAG_BF16_PB);
 #pragma unroll
         for (int c0 = 0; c0 < QPT; c0 += 32) {
           uint32_t v[32];
@@ -597,10 +600,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float2 cd = fadd2(
-                fadd2(fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invP2), kMagic2),
-                kNegMagic2);
-            pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+            const float2 sc2 = fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invP2);
+            if (pt_bf16) {
+              pk[e >> 1] = pack_bf16x2(sc2.x, sc2.y);
+            } else {
+              const float2 cd = fadd2(fadd2(sc2, kMagic2), kNegMagic2);
+              pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+            }
           }
           if constexpr (DBG) dump16(dump_rec(it) + BwdDump<D>::PT + ((size_t)r * 128 + qc0 + c0) * 2, pk);
           tmem_st16(pc_addr + (c0 >> 1), pk);
@@ -622,6 +628,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (QSM && !C::ALIAS && it >= 1 && !waitw(wc, bar_dvq_free, (it - 1) & 1, bSiteDVQFree)) break;
       float2 csum = make_float2(0.f, 0.f);  // this thread's sum of its dS operand values (exact in FP32)
       {
+        const bool ds_bf16 = ATTR && (p.flags & SAGEBWD_FLAG_BF16_DS);
 #pragma unroll
         for (int c0 = 0; c0 < QPT; c0 += 32) {
           const float2 invA2 = make_float2(invA, invA);
@@ -632,9 +639,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float2 cd = fadd2(
-                fadd2(fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invA2), magic2),
-                neg_magic2);
+            const float2 sc2 = fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invA2);
+            if (ds_bf16) {
+              v[e >> 1] = pack_bf16x2(sc2.x, sc2.y);
+              continue;
+            }
+            const float2 cd = fadd2(fadd2(sc2, magic2), neg_magic2);
             if (QSM) csum = fadd2(csum, cd);
             v[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
           }
@@ -826,6 +836,12 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     static_cast<BwdParams&>(dp) = static_cast<const BwdParams&>(p);
     dp.dump = p.dump;
     kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, dp);
+  } else if (p.flags & (SAGEBWD_FLAG_BF16_PB | SAGEBWD_FLAG_BF16_DS)) {
+    if (DSX) return cudaErrorInvalidValue;  // attribution covers the plain instantiation only
+    auto kern = bwd_kernel<D, CAUSAL, false, false, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, static_cast<const BwdParams&>(p));
   } else {
     auto kern = bwd_kernel<D, CAUSAL, DSX, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

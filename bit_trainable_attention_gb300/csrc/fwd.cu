@@ -90,7 +90,9 @@ __device__ __forceinline__ void fdump16(uint8_t* dst, const uint32_t* w) {
   for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
-template <int D, bool CAUSAL, bool QSM, bool DBG>
+// ATTR (error attribution, SAGEBWD_FLAG_BF16_PF): the P~ operand is the BF16 rounding of
+// 127 * 2^(t - tmax) instead of its integer code; everything else as the plain instantiation.
+template <int D, bool CAUSAL, bool QSM, bool DBG, bool ATTR = false>
 __global__ void __launch_bounds__(kFThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const typename FwdParamsOf<DBG>::type p) {
@@ -444,9 +446,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
             if (c0 + e + 1 >= kvis) u.y = 0.f;
           }
           usum = fadd2(usum, u);
-          // round to the nearest integer (ties to even) with the 1.5 * 2^23 constant
-          const float2 cd = fadd2(fadd2(u, mg), nmg);
-          pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+          if constexpr (ATTR) {
+            pk[e >> 1] = pack_bf16x2(u.x, u.y);
+          } else {
+            // round to the nearest integer (ties to even) with the 1.5 * 2^23 constant
+            const float2 cd = fadd2(fadd2(u, mg), nmg);
+            pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+          }
         }
         if constexpr (DBG) fdump16(dump_rec(j) + FwdDump<D>::PC + ((size_t)r * 128 + c0) * 2, pk);
         tmem_st16(s_addr + (c0 >> 1), pk);
@@ -494,6 +500,12 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kFThreads, C::SMEM, s>>>(tq, tk, tv, p);
+  } else if (p.flags & SAGEBWD_FLAG_BF16_PF) {
+    if (p.qbias != nullptr) return cudaErrorInvalidValue;  // attribution covers the plain instantiation only
+    auto kern = fwd_kernel<D, CAUSAL, false, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kFThreads, C::SMEM, s>>>(tq, tk, tv, static_cast<const FwdParams&>(p));
   } else {
     auto kern = p.qbias != nullptr ? fwd_kernel<D, CAUSAL, true, false> : fwd_kernel<D, CAUSAL, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

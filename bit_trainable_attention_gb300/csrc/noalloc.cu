@@ -102,6 +102,7 @@ extern "C" sagebwd_status sagebwd_quantize_k_noalloc(const sagebwd_problem* prob
   QuantParams qp{};
   qp.job[0] = {static_cast<const __nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(k_q), scales,
                smooth ? k_mean : nullptr, BH, nullptr, 1, 1, prob->qk_subexp ? 1 : 0};
+  qp.job[0].bf16 = (prob->flags & SAGEBWD_FLAG_BF16_K) ? 1 : 0;
   qp.njobs = 1;
   qp.block_start[0] = 0;
   qp.block_start[1] = BH * nb;

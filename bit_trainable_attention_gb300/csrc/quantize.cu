@@ -122,11 +122,14 @@ __device__ __forceinline__ void exact_row_sums(const uint4 (&u)[RPL], double (&a
 // BM (Q-smoothing): the block's own channel means are subtracted instead of a head-wide mean
 // and written to bmean[bh][blk][D]; mred / smean are shared scratch [kThreads / 32][D] / [D]
 // for them.
+// bf16 (error attribution, uniform over the CTA): the block keeps its scale but stores the BF16
+// rounding (to nearest even) of x * inv instead of the code (no sub-scales).
 template <int D, bool BM = false>
 __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xq,
                                float* __restrict__ scale, const float* __restrict__ mean, int bh, int blk, int N,
                                int nb, float* red, const float* fac = nullptr, float* gred = nullptr,
-                               float* __restrict__ bmean = nullptr, double* mred = nullptr, float* smean = nullptr) {
+                               float* __restrict__ bmean = nullptr, double* mred = nullptr, float* smean = nullptr,
+                               bool bf16 = false) {
   constexpr int V8 = D / 8, RL = kThreads / V8;
   constexpr int PER = kBlk / RL;  // rows (16-byte vectors) per thread
   static_assert(kThreads % V8 == 0 && kBlk % RL == 0, "thread layout");
@@ -202,7 +205,20 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
   const float a = block_max(amax, red);
   const bool live = a >= kMinGroupMax;
   const float inv = live ? __fdiv_rn(127.f, a) : 0.f;
-  if (gred != nullptr) {
+  if (bf16) {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int r = rl + e * RL;
+      if (row0 + r < N) {
+        float v[8];
+        load(raw[e], v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = __fmul_rn(v[q], inv);
+        const uint4 out = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+        *reinterpret_cast<uint4*>(xq + base + (size_t)r * D + c8 * 8) = out;
+      }
+    }
+  } else if (gred != nullptr) {
     // Q/K sub-scales: the group's maximum over the block's rows (the lanes that share c8,
     // then the warps), k = floor(log2(a / group max)) in [0, 8] (0 below 2^-100); the
     // codes are rint(x * inv * 2^k) and the stored values code * 2^-k, rounded onto that
@@ -273,12 +289,13 @@ __global__ void __launch_bounds__(kThreads, BM ? 2 : 4) quantize_kernel(const Qu
     if (job.bmean != nullptr) {
       quantize_block<D, true>(job.x, job.xq, job.scale, job.mean, bh, local % p.nb, p.N, p.nb, red,
                               job.bexp != nullptr ? fac : nullptr, job.subexp ? gred : nullptr, job.bmean, mred,
-                              smean);
+                              smean, job.bf16 != 0);
       return;
     }
   }
   quantize_block<D>(job.x, job.xq, job.scale, job.mean, bh, local % p.nb, p.N, p.nb, red,
-                    job.bexp != nullptr ? fac : nullptr, job.subexp ? gred : nullptr);
+                    job.bexp != nullptr ? fac : nullptr, job.subexp ? gred : nullptr, nullptr, nullptr, nullptr,
+                    job.bf16 != 0);
 }
 
 // Channel statistics of one 128-token block of one head.  Blocks with
@@ -601,7 +618,8 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const PrepParams p) 
     for (int o = V8 / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (c8 == 0 && row0 + r < p.N) p.D[(size_t)bh * p.N + row0 + r] = s;
   }
-  quantize_block<D>(p.dO, p.dOq, p.sdo, nullptr, bh, blk, p.N, p.nb, red);
+  quantize_block<D>(p.dO, p.dOq, p.sdo, nullptr, bh, blk, p.N, p.nb, red, nullptr, nullptr, nullptr, nullptr,
+                    nullptr, p.bf16 != 0);
 }
 
 struct ConvertJobs {

@@ -38,6 +38,7 @@ struct QuantJob {
   int subexp;              // 1: power-of-two sub-scales per 8-channel group of each block (Q/K option)
   float* bmean;            // [BH][nb][d] or nullptr: Q-smoothing, each block's channel means subtracted
                            // first (and written here)
+  int bf16;                // error attribution: store the BF16 rounding of x * 127/max instead of the code
 };
 struct QuantParams {
   QuantJob job[3];
@@ -89,6 +90,7 @@ struct PrepParams {
   float* dv_acc;            // [BHk][N][d], zeroed
   int BH, BHk, N, d, nb;
   int* status;
+  int bf16;                 // error attribution: dO stored as the BF16 rounding of dO * 127/max
 };
 cudaError_t launch_bwd_prep(const PrepParams& p, cudaStream_t s);
 // FP32 gradient accumulators -> BF16 outputs, up to three arrays in one launch.

@@ -111,6 +111,20 @@ enum { SAGEBWD_Q = 0, SAGEBWD_K = 1, SAGEBWD_V = 2, SAGEBWD_DO = 3 };
                                            INT8-semantics operands and raw tensor-core products into the
                                            workspace (layout at sagebwd_debug_dump_offset; small problems
                                            only; not with ds_subexp or smooth_q) */
+/* Error attribution ("SageBwd: A Trainable Low-bit Attention", Abstract, finding (ii): the backward's
+ * error comes mainly from dS; "SageAttention3 ... 8-Bit Training" summary, Measured effects: the dO V^T
+ * row): each flag makes one quantizer keep its scale but store the BF16 rounding (to nearest even) of
+ * the scaled value, x * 127/max, instead of its INT8 code, so that comparing runs with one flag set
+ * shows how much of the error that quantizer carries.  Q^ and K^ then carry no sub-scales.  Not with
+ * ds_subexp, smooth_q or SAGEBWD_FLAG_DEBUG_DUMP (SAGEBWD_ERR_UNSUPPORTED). */
+#define SAGEBWD_FLAG_BF16_Q 0x10u   /* Q^ */
+#define SAGEBWD_FLAG_BF16_K 0x20u   /* K^ */
+#define SAGEBWD_FLAG_BF16_V 0x40u   /* V^ */
+#define SAGEBWD_FLAG_BF16_DO 0x80u  /* dO^ */
+#define SAGEBWD_FLAG_BF16_PF 0x100u /* forward P~ (per row and key tile) */
+#define SAGEBWD_FLAG_BF16_PB 0x200u /* backward P^T (per key and query tile) */
+#define SAGEBWD_FLAG_BF16_DS 0x400u /* backward dS (per tile) */
+#define SAGEBWD_FLAGS_BF16 0x7F0u
 
 typedef struct {
   int32_t B, Hq, Hkv, N, d;

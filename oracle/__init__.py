@@ -33,7 +33,7 @@ class OracleProblem(ctypes.Structure):
         ("smooth_k", ctypes.c_int32), ("balance_qk", ctypes.c_int32), ("exact_codes", ctypes.c_int32),
         ("threads", ctypes.c_int32), ("exact_mask", ctypes.c_uint32), ("int8_dp", ctypes.c_int32),
         ("ds_subexp", ctypes.c_int32), ("qk_subexp", ctypes.c_int32), ("fp8", ctypes.c_int32),
-        ("smooth_q", ctypes.c_int32), ("l_from_codes", ctypes.c_int32),
+        ("smooth_q", ctypes.c_int32), ("l_from_codes", ctypes.c_int32), ("bf16_mask", ctypes.c_uint32),
         ("softmax_scale", ctypes.c_double),
     ]
 
@@ -99,14 +99,19 @@ def _bf16_bits(x) -> np.ndarray:
     return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
 
 
+# Quantizer bits of exact_mask and bf16_mask.
+QZ_Q, QZ_K, QZ_V, QZ_DO, QZ_PF, QZ_PB, QZ_DS = range(7)
+
+
 def problem(B, Hq, Hkv, N, d, causal, smooth_k=True, exact_codes=False, softmax_scale=0.0, threads=0, exact_mask=0,
             balance_qk=False, int8_dp=False, ds_subexp=False, qk_subexp=False, fp8=False, smooth_q=False,
-            l_from_codes=False):
+            l_from_codes=False, bf16_mask=0):
     """l_from_codes plants a misreading (softmax denominator from the dequantized P~ codes); only the
-    tests that show a pin catches it set it."""
+    tests that show a pin catches it set it.  exact_mask / bf16_mask (bits QZ_*): those quantizers keep
+    their scales but skip the rounding (FP64) / round to BF16 instead of to an INT8 code."""
     return OracleProblem(B, Hq, Hkv, N, d, int(causal), int(smooth_k), int(balance_qk), int(exact_codes),
                          int(threads), int(exact_mask), int(int8_dp), int(ds_subexp), int(qk_subexp), int(fp8),
-                         int(smooth_q), int(l_from_codes), float(softmax_scale))
+                         int(smooth_q), int(l_from_codes), int(bf16_mask), float(softmax_scale))
 
 
 def nblocks(N: int) -> int:

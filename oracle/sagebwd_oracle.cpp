@@ -91,6 +91,8 @@ typedef struct {
   int32_t smooth_q;     // 1: Q-smoothing (block mean of Q subtracted before quantizing, mean . K' added to S)
   int32_t l_from_codes; // planted misreading, for the tests only: the softmax denominator summed from the
                         // dequantized P~ codes instead of the unquantized P~ (the reading kept here, r8)
+  uint32_t bf16_mask;   // error attribution (same bit order as exact_mask): that quantizer keeps its scale
+                        // but stores the BF16 rounding of the scaled value instead of its INT8 code
   double softmax_scale;  // <= 0: 1/sqrt(d)
 } oracle_problem;
 }
@@ -134,14 +136,28 @@ double round_e4m3(double v) {
   return std::copysign(r, v);
 }
 
+// Round to BF16 (8 significant bits), to nearest with ties to even, from the FP32 value of v.
+double round_bf16(double v) {
+  const float f = (float)v;
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u) return v;  // inf / nan unchanged
+  u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+  float r;
+  std::memcpy(&r, &u, 4);
+  return (double)r;
+}
+
 struct Mode {
   bool fp32;       // false only in the exact_codes pin mode
   uint32_t exact;  // bit set: that quantizer does not round
+  uint32_t bf16 = 0;      // bit set: that quantizer rounds to BF16 instead of to an INT8 code
   bool fp8 = false;       // the FP8 ablation: E4M3 values instead of INT8 codes
   double qmax = 127.0;    // largest code: 127 (INT8) or 448 (E4M3)
   double F(double x) const { return fp32 ? (double)(float)x : x; }
   double Q(int which, double x) const {
     if (exact & (1u << which)) return x;
+    if (bf16 & (1u << which)) return round_bf16(x);
     if (fp8) return round_e4m3(x);
     const double r = std::nearbyint(x);
     return std::min(127.0, std::max(-127.0, r));
@@ -149,6 +165,7 @@ struct Mode {
 };
 inline Mode mode_of(const oracle_problem* p) {
   Mode m = p->exact_codes ? Mode{false, 0x7Fu} : Mode{true, p->exact_mask};
+  m.bf16 = p->exact_codes ? 0u : p->bf16_mask;
   if (p->fp8) {
     m.fp8 = true;
     m.qmax = 448.0;
@@ -710,7 +727,9 @@ int oracle_quantize_qk(const oracle_problem* p, const uint16_t* q, const uint16_
   set_threads(p);
   QTensor qq, kq;
   std::vector<int> e;
-  quantize_qk(Mode{true, 0}, p, q, k, qq, kq, &e);
+  Mode M{true, 0};
+  M.bf16 = p->bf16_mask & ((1u << QZ_Q) | (1u << QZ_K));  // the attribution mode, where it applies to Q and K
+  quantize_qk(M, p, q, k, qq, kq, &e);
   for (size_t i = 0; i < qq.codes.size(); ++i) qc[i] = (float)qq.codes[i];
   for (size_t i = 0; i < qq.scale.size(); ++i) qs[i] = (float)qq.scale[i];
   for (size_t i = 0; i < kq.codes.size(); ++i) kc[i] = (float)kq.codes[i];

@@ -141,3 +141,12 @@ def test_debug_dump_sizes_and_rejections(lib):
         assert sb.sagebwd_workspace_bytes(bad, 1) == 0, opt
     huge = sb.Problem.make(1, 32, 8, 65536, 128, False, flags=sb.FLAG_DEBUG_DUMP)
     assert sb.sagebwd_saved_bytes(huge) == 0
+
+
+def test_attribution_flags_refused_with_unsupported_options(lib):
+    """The BF16 attribution flags cover the kernels without dS sub-scales, Q-smoothing and the dump."""
+    ok = sb.Problem.make(1, 2, 1, 300, 64, True, flags=sb.FLAG_BF16["ds"] | sb.FLAG_BF16["q"])
+    assert sb.sagebwd_workspace_bytes(ok, 1) > 0
+    for opts, flags in (({"ds_subexp": True}, 0), ({"smooth_q": True}, 0), ({}, sb.FLAG_DEBUG_DUMP)):
+        p = sb.Problem.make(1, 2, 1, 300, 64, True, flags=sb.FLAG_BF16["ds"] | flags, **opts)
+        assert sb.sagebwd_workspace_bytes(p, 1) == 0, opts
