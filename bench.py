@@ -547,86 +547,53 @@ def describe(w: W.Workload) -> str:
     return (f"{w.name}: B={w.B} Hq={w.Hq} Hkv={w.Hkv} N={w.N} d={w.d} {'causal' if w.causal else 'non-causal'}")
 
 
-# ---------------------------------------------------------------------------- per-kernel times
-KERNELS = ("kmean_partial_kernel", "kmean_final_kernel", "qk_stats_partial_kernel", "qk_stats_final_kernel",
-           "quantize_kernel", "qsmooth_bias_kernel", "fwd_kernel", "bwd_prep_kernel", "bwd_kernel",
-           "grad_convert_kernel")
-
-
-def _kernel_of(name: str):
-    """The library kernel a profiler event name belongs to (demangled "...::bwd_kernel<...>(...)" or
-    mangled "...10bwd_kernelI..."), else None."""
-    import re
-    for k in KERNELS:
-        if re.search(r"(?:^|[^A-Za-z_])" + k + r"(?:$|[<(I])", name):
-            return k
-    return None
-
-
-def kernel_times(step: "Step", flush: torch.Tensor, steps: int = 3):
-    """Device time of each of the library's kernels per step (CUPTI kernel activity records through
-    torch.profiler, read from its exported trace; outside the timed region):
-    {kernel: (launches per step, mean us per launch)}."""
-    import tempfile
-    from torch.profiler import ProfilerActivity, profile
-    for _ in range(2):
-        flush.zero_()
-        step.run()
-    torch.cuda.synchronize()
-    with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
-        for _ in range(steps):
-            flush.zero_()
-            step.run()
-        torch.cuda.synchronize()
-    with tempfile.TemporaryDirectory() as tmp:
-        path = os.path.join(tmp, "trace.json")
-        prof.export_chrome_trace(path)
-        with open(path) as f:
-            trace = json.load(f)
-    events = trace["traceEvents"] if isinstance(trace, dict) else trace
-    agg, seen = {}, set()
-    for e in events:
-        if e.get("ph") != "X" or str(e.get("cat", "")).lower() != "kernel":
-            continue
-        seen.add(str(e.get("name", ""))[:80])
-        k = _kernel_of(str(e.get("name", "")))
-        if k is None:
-            continue
-        n, tot = agg.get(k, (0, 0.0))
-        agg[k] = (n + 1, tot + float(e.get("dur", 0.0)))
-    if not agg:
-        raise RuntimeError(f"no library kernel among the profiled device events: {sorted(seen)[:8]}")
-    return {k: (n / steps, tot / n) for k, (n, tot) in agg.items() if n > 0}
-
-
-def quantize_bandwidth(w: W.Workload, prob, times: dict, hbm_gbs: float):
-    """HBM GB/s of each kernel of the quantize stage: algorithmic bytes per launch (each input
-    element read once per pass that must read it, each output written once) / device time.
-    The quantized values are stored as 2-byte integer-valued BF16 (the tensor cores' operand form)."""
+# ---------------------------------------------------------------------------- quantize stage bandwidth
+def quantize_bandwidth(step: "Step", flush: torch.Tensor, hbm_gbs: float, reps: int = 10):
+    """HBM GB/s of the quantize stage and of its kernels, each timed with CUDA events on the launching
+    stream (L2 flushed before every call, outside the events): algorithmic bytes per call / time.
+    Algorithmic bytes: every input element read once per pass that must read it (K twice with
+    K-smoothing: its channel sums, then its codes), every output written once; the quantized values
+    are 2-byte integer-valued BF16 (the tensor cores' operand form).
+      stage      sagebwd_fwd_quantize (K chunk sums beside Q's codes, then K's and V's codes)
+      quantize_q sagebwd_quantize(Q): one quantize_kernel launch on Q alone
+      quantize_v sagebwd_quantize(V): one quantize_kernel launch on V alone
+      k_path     sagebwd_quantize(K): the single-operand K path (K mean pair, then K's codes)"""
+    w, p, x = step.w, step.prob, step.x
     nb = (w.N + 127) // 128
     qe, ke = w.B * w.Hq * w.N * w.d, w.B * w.Hkv * w.N * w.d
-    scales = 4 * nb * (w.B * w.Hq + 2 * w.B * w.Hkv)
-    part = 8 * w.B * w.Hkv * nb * w.d  # FP64 partial channel sums of K
-    mean = 4 * w.B * w.Hkv * w.d
-    alg = {
-        "kmean_partial_kernel": 2 * ke + part,
-        "kmean_final_kernel": part + mean,
-        # reads Q, K, V (and the K mean), writes the three code tensors and their block scales
-        "quantize_kernel": 2 * (qe + 2 * ke) + mean + 2 * (qe + 2 * ke) + scales,
+    s = torch.cuda.current_stream()
+    dev = x["q"].device
+    xq = torch.empty_like(x["q"])
+    sq = torch.empty(w.B * w.Hq * nb, dtype=torch.float32, device=dev)
+    mu = torch.empty(w.B * w.Hkv * w.d, dtype=torch.float32, device=dev)
+    calls = {
+        "stage": (lambda: sb.sagebwd_fwd_quantize(p, x["q"], x["k"], x["v"], step.saved, step.ws0, s),
+                  4 * qe + (6 if p.smooth_k else 4) * ke + 4 * ke + 4 * nb * (w.B * w.Hq + 2 * w.B * w.Hkv)),
+        "quantize_q": (lambda: sb.sagebwd_quantize(p, sb.SAGEBWD_Q, x["q"], xq, sq, None, step.ws0, s),
+                       4 * qe + 4 * nb * w.B * w.Hq),
+        "quantize_v": (lambda: sb.sagebwd_quantize(p, sb.SAGEBWD_V, x["v"], xq, sq, None, step.ws0, s),
+                       4 * ke + 4 * nb * w.B * w.Hkv),
+        "k_path": (lambda: sb.sagebwd_quantize(p, sb.SAGEBWD_K, x["k"], xq, sq, mu, step.ws0, s),
+                   (6 if p.smooth_k else 4) * ke + 4 * nb * w.B * w.Hkv),
     }
     out = {}
-    for k, b in alg.items():
-        if k in times:
-            launches, us = times[k]
-            gbs = b / (us * 1e-6) / 1e9
-            out[k] = {"bytes_per_launch": int(b), "us_per_launch": round(us, 2), "gb_per_s": round(gbs, 1),
-                      "frac_of_hbm": round(gbs / hbm_gbs, 3)}
-    stage_b = sum(alg[k] for k in alg if k in times)
-    stage_us = sum(times[k][1] * times[k][0] for k in alg if k in times)
-    if stage_us > 0:
-        out["stage"] = {"bytes": int(stage_b), "us": round(stage_us, 2),
-                        "gb_per_s": round(stage_b / (stage_us * 1e-6) / 1e9, 1),
-                        "frac_of_hbm": round(stage_b / (stage_us * 1e-6) / 1e9 / hbm_gbs, 3)}
+    for name, (fn, nbytes) in calls.items():
+        if p.smooth_q and name in ("stage", "quantize_q"):
+            continue  # Q-smoothing's stage adds the logit terms; its Q path is the fused one only
+        ts = []
+        for r in range(reps + 2):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            if r >= 2:
+                ts.append(e0.elapsed_time(e1))
+        us = statistics.median(ts) * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"bytes": int(nbytes), "us": round(us, 2), "gb_per_s": round(gbs, 1),
+                     "frac_of_hbm": round(gbs / hbm_gbs, 3)}
     return out
 
 
@@ -797,13 +764,7 @@ def main():
     if rank == 0:
         line["cossim_vs_torch_fp32"] = None if args.no_cossim else cossim_vs_torch(step)
         if not args.no_extras:
-            try:
-                times = kernel_times(step, flush)
-                line["kernel_us"] = {k: {"launches_per_step": n, "us_per_launch": round(us, 2)}
-                                     for k, (n, us) in sorted(times.items())}
-                line["quantize_hbm"] = quantize_bandwidth(w, step.prob, times, peaks["hbm_gbs"])
-            except Exception as exc:  # noqa: BLE001 - the profiler is context, not the measurement
-                line["kernel_us"] = {"unavailable": f"{type(exc).__name__}: {exc}"}
+            line["quantize_hbm"] = quantize_bandwidth(step, flush, peaks["hbm_gbs"])
             if not args.no_cossim:
                 line["other_settings"] = other_settings(step, args, dev, flush)
                 if not (args.ds_subexp or args.smooth_q):

@@ -56,17 +56,20 @@ class Problem(ctypes.Structure):
         ("d", ctypes.c_int32), ("causal", ctypes.c_int32), ("smooth_k", ctypes.c_int32),
         ("balance_qk", ctypes.c_int32), ("ds_subexp", ctypes.c_int32),
         ("qk_subexp", ctypes.c_int32), ("smooth_q", ctypes.c_int32), ("flags", ctypes.c_uint32),
-        ("softmax_scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_uint32),
+        ("softmax_scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_uint32), ("fp8", ctypes.c_int32),
     ]
 
     @classmethod
     def make(cls, B, Hq, Hkv, N, d, causal, smooth_k=True, flags=0, softmax_scale=0.0, wait_timeout_ms=0,
-             balance_qk=False, ds_subexp=False, qk_subexp=True, smooth_q=False):
-        """The library's defaults: K-smoothing on and the Q/K 8-channel sub-scales on (qk_subexp=False
-        selects the plain one-scale-per-block mode for Q and K)."""
+             balance_qk=False, ds_subexp=False, qk_subexp=None, smooth_q=False, fp8=False):
+        """The library's defaults: K-smoothing on and, for INT8, the Q/K 8-channel sub-scales on
+        (qk_subexp=False selects the plain one-scale-per-block mode for Q and K).  fp8=True selects
+        the FP8 E4M3 variant, which has no sub-scales."""
+        if qk_subexp is None:
+            qk_subexp = not fp8
         return cls(B, Hq, Hkv, N, d, int(bool(causal)), int(bool(smooth_k)), int(bool(balance_qk)),
                    int(bool(ds_subexp)), int(bool(qk_subexp)), int(bool(smooth_q)), flags, softmax_scale,
-                   wait_timeout_ms)
+                   wait_timeout_ms, int(bool(fp8)))
 
     @classmethod
     def from_tensors(cls, q, k, causal, **kw):
@@ -346,12 +349,12 @@ class SageBwdAttention(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False,
-                qk_subexp=True, smooth_q=False, flags=0, wait_timeout_ms=0):
+                qk_subexp=None, smooth_q=False, flags=0, wait_timeout_ms=0, fp8=False):
         _poll_status()
         _check_inputs(q, k, v)
         prob = Problem.from_tensors(q, k, causal, smooth_k=smooth_k, softmax_scale=softmax_scale,
                                     balance_qk=balance_qk, ds_subexp=ds_subexp, qk_subexp=qk_subexp,
-                                    smooth_q=smooth_q, flags=flags, wait_timeout_ms=wait_timeout_ms)
+                                    smooth_q=smooth_q, flags=flags, wait_timeout_ms=wait_timeout_ms, fp8=fp8)
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
         saved = empty_bytes(sagebwd_saved_bytes(prob), q.device)
@@ -374,11 +377,11 @@ class SageBwdAttention(torch.autograd.Function):
         ws = empty_bytes(sagebwd_workspace_bytes(prob, 1), q.device)
         sagebwd_bwd(prob, q, k, v, o, do, lse, saved, dq, dk, dv, ws)
         _queue_status(ws, "sagebwd_bwd")
-        return dq, dk, dv, None, None, None, None, None, None, None, None, None
+        return dq, dk, dv, None, None, None, None, None, None, None, None, None, None
 
 
 def attention(q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_qk=False, ds_subexp=False,
-              qk_subexp=True, smooth_q=False, flags=0, wait_timeout_ms=0):
+              qk_subexp=None, smooth_q=False, flags=0, wait_timeout_ms=0, fp8=False):
     """SageBwd attention on BF16 [B, H, N, d] CUDA tensors (GQA when k/v have fewer heads).
 
     balance_qk turns on the library's power-of-two Q/K channel balancing before quantization
@@ -389,8 +392,10 @@ def attention(q, k, v, causal=False, softmax_scale=0.0, smooth_k=True, balance_q
     smooth_q subtracts each 128-token block's channel means from Q before quantizing and adds their
     logit term back in FP32 (for queries with a large common offset; not with balance_qk).
     flags (SAGEBWD_FLAG_*) and wait_timeout_ms pass through to the library (0: defaults).
+    fp8=True runs the FP8 E4M3 variant of the method (every quantizer stores E4M3 values scaled to
+    448 instead of INT8 codes; not with the optional refinements).
 
     Device-side errors of a call (a bounded wait that ran out) raise SageBwdError at the next
     forward or backward call once the failing kernels have finished, or at check_errors()."""
     return SageBwdAttention.apply(q, k, v, causal, softmax_scale, smooth_k, balance_qk, ds_subexp, qk_subexp,
-                                  smooth_q, flags, wait_timeout_ms)
+                                  smooth_q, flags, wait_timeout_ms, fp8)

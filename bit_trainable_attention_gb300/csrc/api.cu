@@ -30,6 +30,11 @@ sagebwd_status check_problem(const sagebwd_problem* p) {
   if ((double)nblocks(p->N) * p->B * p->Hq >= 2147483647.0) return SAGEBWD_ERR_UNSUPPORTED;
   if (p->smooth_q && p->balance_qk) return SAGEBWD_ERR_UNSUPPORTED;  // not defined together
   if (p->smooth_q && nblocks(p->N) > 65535) return SAGEBWD_ERR_UNSUPPORTED;  // logit-term grid limit
+  // the FP8 variant: block scales without sub-scales, no balancing, Q-smoothing, attribution or dump
+  if (p->fp8 && (p->qk_subexp || p->ds_subexp || p->balance_qk || p->smooth_q ||
+                 (p->flags & (SAGEBWD_FLAGS_BF16 | SAGEBWD_FLAG_DEBUG_DUMP))))
+    return SAGEBWD_ERR_UNSUPPORTED;
+  if (p->fp8 != 0 && p->fp8 != 1) return SAGEBWD_ERR_INVALID_ARG;
   // the attribution instantiations cover the kernels without dS sub-scales, Q-smoothing and the dump
   if ((p->flags & SAGEBWD_FLAGS_BF16) && (p->ds_subexp || p->smooth_q || (p->flags & SAGEBWD_FLAG_DEBUG_DUMP)))
     return SAGEBWD_ERR_UNSUPPORTED;
@@ -174,6 +179,13 @@ uint64_t timeout_of(const sagebwd_problem* p) {
 
 sagebwd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SAGEBWD_OK : SAGEBWD_ERR_CUDA; }
 
+// What the quantizer selected by its attribution flag stores (ValueMode).
+int vmode_of(const sagebwd_problem* p, uint32_t bf16_flag) {
+  return p->fp8 ? kValFp8 : ((p->flags & bf16_flag) ? kValBf16 : kValInt8);
+}
+// Flags the attention kernels get: the caller's, plus the FP8 variant's code rounding.
+uint32_t kernel_flags(const sagebwd_problem* p) { return p->flags | (p->fp8 ? kFlagFp8Codes : 0u); }
+
 #define SB_CHECK(expr)                          \
   do {                                          \
     const sagebwd_status st_ = (expr);          \
@@ -225,14 +237,12 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
   const int G = p->Hq / p->Hkv;
   QuantParams qp{};
   qp.job[0] = {static_cast<const __nv_bfloat16*>(q), at<__nv_bfloat16>(saved, S.q), at<float>(saved, S.sq), nullptr,
-               p->B * p->Hq, bexp, G, -1, p->qk_subexp ? 1 : 0, p->smooth_q ? at<float>(saved, S.qm) : nullptr};
+               p->B * p->Hq, bexp, G, -1, p->qk_subexp ? 1 : 0, p->smooth_q ? at<float>(saved, S.qm) : nullptr,
+               vmode_of(p, SAGEBWD_FLAG_BF16_Q)};
   qp.job[1] = {static_cast<const __nv_bfloat16*>(k), at<__nv_bfloat16>(saved, S.k), at<float>(saved, S.sk), mean,
-               p->B * p->Hkv, bexp, 1, 1, p->qk_subexp ? 1 : 0};
+               p->B * p->Hkv, bexp, 1, 1, p->qk_subexp ? 1 : 0, nullptr, vmode_of(p, SAGEBWD_FLAG_BF16_K)};
   qp.job[2] = {static_cast<const __nv_bfloat16*>(v), at<__nv_bfloat16>(saved, S.v), at<float>(saved, S.sv), nullptr,
-               p->B * p->Hkv, nullptr, 1, 1};
-  qp.job[0].bf16 = (p->flags & SAGEBWD_FLAG_BF16_Q) ? 1 : 0;
-  qp.job[1].bf16 = (p->flags & SAGEBWD_FLAG_BF16_K) ? 1 : 0;
-  qp.job[2].bf16 = (p->flags & SAGEBWD_FLAG_BF16_V) ? 1 : 0;
+               p->B * p->Hkv, nullptr, 1, 1, 0, nullptr, vmode_of(p, SAGEBWD_FLAG_BF16_V)};
   qp.njobs = 3;
   qp.block_start[0] = 0;
   for (int j = 0; j < 3; ++j) qp.block_start[j + 1] = qp.block_start[j] + qp.job[j].BH * nb;
@@ -286,7 +296,7 @@ sagebwd_status fwd_attention_impl(const sagebwd_problem* p, const void* saved, v
   fp.dump = (p->flags & SAGEBWD_FLAG_DEBUG_DUMP) ? at<uint8_t>(ws, W.dump) : nullptr;
   fp.status = at<int>(ws, W.status);
   fp.timeout_ns = timeout_of(p);
-  fp.flags = p->flags;
+  fp.flags = kernel_flags(p);
   return cuda_status(launch_fwd(tq, tk, tv, fp, p->d, p->causal, st));
 }
 
@@ -348,7 +358,7 @@ sagebwd_status bwd_prepare_impl(const sagebwd_problem* p, const void* o, const v
   pp.d = p->d;
   pp.nb = nblocks(p->N);
   pp.status = at<int>(ws, W.status);
-  pp.bf16 = (p->flags & SAGEBWD_FLAG_BF16_DO) ? 1 : 0;
+  pp.vmode = vmode_of(p, SAGEBWD_FLAG_BF16_DO);
   return cuda_status(launch_bwd_prep(pp, st));
 }
 
@@ -390,7 +400,7 @@ sagebwd_status bwd_attention_impl(const sagebwd_problem* p, const void* v, const
   bp.dump = (p->flags & SAGEBWD_FLAG_DEBUG_DUMP) ? at<uint8_t>(ws, W.dump) : nullptr;
   bp.status = at<int>(ws, W.status);
   bp.timeout_ns = timeout_of(p);
-  bp.flags = (p->flags & ~kBwdDirectDKDV) | (direct ? kBwdDirectDKDV : 0u);
+  bp.flags = (kernel_flags(p) & ~kBwdDirectDKDV) | (direct ? kBwdDirectDKDV : 0u);
   return cuda_status(launch_bwd(tq, tk, tv, tdo, tdoq, tdq, bp, p->d, p->causal, p->ds_subexp ? 1 : 0, st));
 }
 
@@ -444,7 +454,7 @@ sagebwd_status sagebwd_quantize(const sagebwd_problem* prob, int which, const vo
   qp.job[0] = {static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(x_q), scales,
                smooth ? k_mean : nullptr, BH, nullptr, 1, 1,
                (prob->qk_subexp && (which == SAGEBWD_Q || which == SAGEBWD_K)) ? 1 : 0};
-  qp.job[0].bf16 = (prob->flags & (SAGEBWD_FLAG_BF16_Q << which)) ? 1 : 0;
+  qp.job[0].vmode = vmode_of(prob, SAGEBWD_FLAG_BF16_Q << which);
   qp.njobs = 1;
   qp.block_start[0] = 0;
   qp.block_start[1] = BH * nb;

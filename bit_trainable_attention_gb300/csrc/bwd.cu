@@ -146,9 +146,10 @@ __device__ __forceinline__ void dump16(uint8_t* dst, const uint32_t* w) {
   for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
-// ATTR (error attribution, SAGEBWD_FLAG_BF16_PB / _DS in p.flags): the P^T and / or dS operands are
-// the BF16 rounding of the scaled values instead of their integer codes (plain instantiation otherwise).
-template <int D, bool CAUSAL, bool DSX, bool QSM, bool DBG, bool ATTR = false>
+// VAR: kValBf16 (error attribution, SAGEBWD_FLAG_BF16_PB / _DS in p.flags) the P^T and / or dS
+// operands are the BF16 rounding of the scaled values instead of their integer codes; kValFp8 (the
+// FP8 variant) both are the E4M3 rounding of the values scaled to 448 (scales max / 448).
+template <int D, bool CAUSAL, bool DSX, bool QSM, bool DBG, int VAR = kValInt8>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -560,10 +561,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const bool p_live = pmax >= kMinGroupMax, d_live = a >= kMinGroupMax;
       // hardware reciprocal (<= 2 ulp) rather than IEEE division: these scales only
       // decide codes of this tile and dequantize it; a code at a rounding tie may differ
-      const float invP = p_live ? __fdividef(127.f, pmax) : 0.f;
-      const float sPc = p_live ? pmax * (1.f / 127.f) : 0.f;
-      const float invA = d_live ? __fdividef(127.f, a) : 0.f;
-      const float sDS = d_live ? a * (1.f / 127.f) : 0.f;
+      constexpr float kQMax = VAR == kValFp8 ? kFp8Max : 127.f;
+      const float invP = p_live ? __fdividef(kQMax, pmax) : 0.f;
+      const float sPc = p_live ? pmax * (1.f / kQMax) : 0.f;
+      const float invA = d_live ? __fdividef(kQMax, a) : 0.f;
+      const float sDS = d_live ? a * (1.f / kQMax) : 0.f;
       // dS sub-scales: group g of this thread's key gets k = floor(log2(a / max_g)) in
       // [0, 8] (0 below 2^-100), from the binary exponents and fractions; its operand values
       // are rint(dS * invA * 2^k) * 2^-k (a code times 2^-k, exact in BF16).  Adding and
@@ -591,7 +593,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_after();
       {
         const float2 invP2 = make_float2(invP, invP);
-        const bool pt_bf16 = ATTR && (p.flags & SAGEBWD_FLAG_BF16_PB);
+        const bool pt_bf16 = VAR == kValBf16 && (p.flags & SAGEBWD_FLAG_BF16_PB);
 #pragma unroll
         for (int c0 = 0; c0 < QPT; c0 += 32) {
           uint32_t v[32];
@@ -601,7 +603,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float2 sc2 = fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invP2);
-            if (pt_bf16) {
+            if (VAR == kValFp8) {
+              pk[e >> 1] = e4m3x2_bf16x2(sc2.x, sc2.y);
+            } else if (pt_bf16) {
               pk[e >> 1] = pack_bf16x2(sc2.x, sc2.y);
             } else {
               const float2 cd = fadd2(fadd2(sc2, kMagic2), kNegMagic2);
@@ -628,7 +632,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (QSM && !C::ALIAS && it >= 1 && !waitw(wc, bar_dvq_free, (it - 1) & 1, bSiteDVQFree)) break;
       float2 csum = make_float2(0.f, 0.f);  // this thread's sum of its dS operand values (exact in FP32)
       {
-        const bool ds_bf16 = ATTR && (p.flags & SAGEBWD_FLAG_BF16_DS);
+        const bool ds_bf16 = VAR == kValBf16 && (p.flags & SAGEBWD_FLAG_BF16_DS);
 #pragma unroll
         for (int c0 = 0; c0 < QPT; c0 += 32) {
           const float2 invA2 = make_float2(invA, invA);
@@ -640,6 +644,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float2 sc2 = fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invA2);
+            if (VAR == kValFp8) {
+              v[e >> 1] = e4m3x2_bf16x2(sc2.x, sc2.y);
+              continue;
+            }
             if (ds_bf16) {
               v[e >> 1] = pack_bf16x2(sc2.x, sc2.y);
               continue;
@@ -836,9 +844,10 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     static_cast<BwdParams&>(dp) = static_cast<const BwdParams&>(p);
     dp.dump = p.dump;
     kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, dp);
-  } else if (p.flags & (SAGEBWD_FLAG_BF16_PB | SAGEBWD_FLAG_BF16_DS)) {
-    if (DSX) return cudaErrorInvalidValue;  // attribution covers the plain instantiation only
-    auto kern = bwd_kernel<D, CAUSAL, false, false, false, true>;
+  } else if (p.flags & (SAGEBWD_FLAG_BF16_PB | SAGEBWD_FLAG_BF16_DS | kFlagFp8Codes)) {
+    if (DSX) return cudaErrorInvalidValue;  // these cover the plain instantiation only
+    auto kern = (p.flags & kFlagFp8Codes) ? bwd_kernel<D, CAUSAL, false, false, false, kValFp8>
+                                          : bwd_kernel<D, CAUSAL, false, false, false, kValBf16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::THREADS, C::SMEM, s>>>(tq, tk, tv, tdo, tdoq, tdq, static_cast<const BwdParams&>(p));

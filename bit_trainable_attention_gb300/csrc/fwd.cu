@@ -90,9 +90,10 @@ __device__ __forceinline__ void fdump16(uint8_t* dst, const uint32_t* w) {
   for (int k = 0; k < 4; ++k) d4[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
-// ATTR (error attribution, SAGEBWD_FLAG_BF16_PF): the P~ operand is the BF16 rounding of
-// 127 * 2^(t - tmax) instead of its integer code; everything else as the plain instantiation.
-template <int D, bool CAUSAL, bool QSM, bool DBG, bool ATTR = false>
+// VAR (ValueMode of the P~ operand): kValInt8 its integer code rint(127 * 2^(t - tmax)); kValBf16
+// (error attribution, SAGEBWD_FLAG_BF16_PF) the BF16 rounding of 127 * 2^(t - tmax); kValFp8 (the
+// FP8 variant) the E4M3 rounding of 448 * 2^(t - tmax), dequantized by 2^(tmax - m) / 448.
+template <int D, bool CAUSAL, bool QSM, bool DBG, int VAR = kValInt8>
 __global__ void __launch_bounds__(kFThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const typename FwdParamsOf<DBG>::type p) {
@@ -424,7 +425,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         m_ref = tmax;
       }
       const float rj = ex2_approx(tmax - m_ref);
-      const float bias = kLog2_127 - tmax;
+      constexpr float kQLog2 = VAR == kValFp8 ? kLog2_448 : kLog2_127, kQInv = VAR == kValFp8 ? 1.f / kFp8Max : 1.f / 127.f;
+      const float bias = kQLog2 - tmax;
       // pass 2: codes of P~ written over the S columns already read (chunk c of 32 keys
       // -> 16 packed columns starting at 16c), and the unquantized row sum
       const float2 bias2 = make_float2(bias, bias);
@@ -446,8 +448,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
             if (c0 + e + 1 >= kvis) u.y = 0.f;
           }
           usum = fadd2(usum, u);
-          if constexpr (ATTR) {
+          if constexpr (VAR == kValBf16) {
             pk[e >> 1] = pack_bf16x2(u.x, u.y);
+          } else if constexpr (VAR == kValFp8) {
+            pk[e >> 1] = e4m3x2_bf16x2(u.x, u.y);
           } else {
             // round to the nearest integer (ties to even) with the 1.5 * 2^23 constant
             const float2 cd = fadd2(fadd2(u, mg), nmg);
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p_full + t);
-      const float w_l = rj * (1.f / 127.f);
+      const float w_l = rj * kQInv;
       l = fmaf(w_l, usum.x + usum.y, l * a);
       pend_a = a;
       pend_w = w_l * sVv;
@@ -500,9 +504,10 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kFThreads, C::SMEM, s>>>(tq, tk, tv, p);
-  } else if (p.flags & SAGEBWD_FLAG_BF16_PF) {
-    if (p.qbias != nullptr) return cudaErrorInvalidValue;  // attribution covers the plain instantiation only
-    auto kern = fwd_kernel<D, CAUSAL, false, false, true>;
+  } else if (p.flags & (SAGEBWD_FLAG_BF16_PF | kFlagFp8Codes)) {
+    if (p.qbias != nullptr) return cudaErrorInvalidValue;  // these cover the plain instantiation only
+    auto kern = (p.flags & kFlagFp8Codes) ? fwd_kernel<D, CAUSAL, false, false, kValFp8>
+                                          : fwd_kernel<D, CAUSAL, false, false, kValBf16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kFThreads, C::SMEM, s>>>(tq, tk, tv, static_cast<const FwdParams&>(p));

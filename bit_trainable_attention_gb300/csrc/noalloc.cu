@@ -78,6 +78,7 @@ extern "C" sagebwd_status sagebwd_quantize_k_noalloc(const sagebwd_problem* prob
     return SAGEBWD_ERR_INVALID_ARG;
   if (prob->d != 64 && prob->d != 128) return SAGEBWD_ERR_UNSUPPORTED;
   if (prob->balance_qk) return SAGEBWD_ERR_UNSUPPORTED;  // balanced K codes depend on Q
+  if (prob->fp8 && prob->qk_subexp) return SAGEBWD_ERR_UNSUPPORTED;  // E4M3 values carry no sub-scales
   if ((double)prob->B * prob->Hkv * prob->N * prob->d >= 2147483648.0) return SAGEBWD_ERR_UNSUPPORTED;
   const bool smooth = prob->smooth_k != 0;
   for (const void* ptr : {k, (const void*)k_q, (const void*)scales}) {
@@ -102,7 +103,7 @@ extern "C" sagebwd_status sagebwd_quantize_k_noalloc(const sagebwd_problem* prob
   QuantParams qp{};
   qp.job[0] = {static_cast<const __nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(k_q), scales,
                smooth ? k_mean : nullptr, BH, nullptr, 1, 1, prob->qk_subexp ? 1 : 0};
-  qp.job[0].bf16 = (prob->flags & SAGEBWD_FLAG_BF16_K) ? 1 : 0;
+  qp.job[0].vmode = prob->fp8 ? kValFp8 : ((prob->flags & SAGEBWD_FLAG_BF16_K) ? kValBf16 : kValInt8);
   qp.njobs = 1;
   qp.block_start[0] = 0;
   qp.block_start[1] = BH * nb;

@@ -427,6 +427,21 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// Two floats rounded to FP8 E4M3 (to nearest even, saturating at +-448) and returned as bf16x2
+// (lo = a, hi = b): E4M3 values convert exactly to FP16, FP32 and BF16.
+__device__ __forceinline__ uint32_t e4m3x2_bf16x2(float a, float b) {
+  uint16_t e;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(e) : "f"(a), "f"(b));
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(e));
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
 // Pack two floats into bf16x2 (lo = a, hi = b), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   uint32_t r;

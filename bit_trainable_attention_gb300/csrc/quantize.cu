@@ -19,6 +19,7 @@
 // the channel's max |Q| over the kv head's query heads and of its max
 // |K - mean|; Q's channel is multiplied by 2^-e and K's by 2^e (one exact FP32
 // multiply, after the smoothing) before the block quantizer.
+#include "ptx.cuh"
 #include "sagebwd_internal.h"
 
 namespace sagebwd {
@@ -122,14 +123,16 @@ __device__ __forceinline__ void exact_row_sums(const uint4 (&u)[RPL], double (&a
 // BM (Q-smoothing): the block's own channel means are subtracted instead of a head-wide mean
 // and written to bmean[bh][blk][D]; mred / smean are shared scratch [kThreads / 32][D] / [D]
 // for them.
-// bf16 (error attribution, uniform over the CTA): the block keeps its scale but stores the BF16
-// rounding (to nearest even) of x * inv instead of the code (no sub-scales).
+// vmode (uniform over the CTA): kValInt8 the codes as above; kValBf16 (error attribution) the block
+// keeps its scale but stores the BF16 rounding (to nearest even) of x * inv instead of the code (no
+// sub-scales); kValFp8 (the FP8 variant) scale = a/448, inv = 448/a and the stored value is the
+// E4M3 rounding (to nearest even, saturating) of x * inv, held exactly in BF16.
 template <int D, bool BM = false>
 __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xq,
                                float* __restrict__ scale, const float* __restrict__ mean, int bh, int blk, int N,
                                int nb, float* red, const float* fac = nullptr, float* gred = nullptr,
                                float* __restrict__ bmean = nullptr, double* mred = nullptr, float* smean = nullptr,
-                               bool bf16 = false) {
+                               int vmode = kValInt8) {
   constexpr int V8 = D / 8, RL = kThreads / V8;
   constexpr int PER = kBlk / RL;  // rows (16-byte vectors) per thread
   static_assert(kThreads % V8 == 0 && kBlk % RL == 0, "thread layout");
@@ -139,7 +142,7 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
   float mu[8], fc[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    mu[k] = mean != nullptr ? mean[(size_t)bh * D + c8 * 8 + k] : 0.f;
+    mu[k] = mean != nullptr ? mean[c8 * 8 + k] : 0.f;
     fc[k] = fac != nullptr ? fac[c8 * 8 + k] : 1.f;
   }
   const bool sub = BM || mean != nullptr;
@@ -204,8 +207,9 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
   float gmax = amax;  // this thread's part of its 8-channel group's maximum
   const float a = block_max(amax, red);
   const bool live = a >= kMinGroupMax;
-  const float inv = live ? __fdiv_rn(127.f, a) : 0.f;
-  if (bf16) {
+  const float qmax = vmode == kValFp8 ? kFp8Max : 127.f;
+  const float inv = live ? __fdiv_rn(qmax, a) : 0.f;
+  if (vmode != kValInt8) {
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
       const int r = rl + e * RL;
@@ -214,7 +218,11 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
         load(raw[e], v);
 #pragma unroll
         for (int q = 0; q < 8; ++q) v[q] = __fmul_rn(v[q], inv);
-        const uint4 out = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+        const uint4 out =
+            vmode == kValBf16
+                ? make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]))
+                : make_uint4(e4m3x2_bf16x2(v[0], v[1]), e4m3x2_bf16x2(v[2], v[3]), e4m3x2_bf16x2(v[4], v[5]),
+                             e4m3x2_bf16x2(v[6], v[7]));
         *reinterpret_cast<uint4*>(xq + base + (size_t)r * D + c8 * 8) = out;
       }
     }
@@ -265,7 +273,7 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
       }
     }
   }
-  if (threadIdx.x == 0) scale[(size_t)bh * nb + blk] = live ? __fdiv_rn(a, 127.f) : 0.f;
+  if (threadIdx.x == 0) scale[(size_t)bh * nb + blk] = live ? __fdiv_rn(a, qmax) : 0.f;
 }
 
 template <int D, bool BM>
@@ -279,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, BM ? 2 : 4) quantize_kernel(const Qu
   const int local = blockIdx.x - p.block_start[j];
   const QuantJob& job = p.job[j];
   const int bh = local / p.nb;
+  const float* mean = job.mean != nullptr ? job.mean + (size_t)bh * D : nullptr;  // this head's channel means
   if (job.bexp != nullptr) {
     if (threadIdx.x < D) fac[threadIdx.x] = exp2_int(job.bexp_sign * job.bexp[(bh / job.bexp_group) * D + threadIdx.x]);
     __syncthreads();  // quantize_block reads fac only after this
@@ -287,15 +296,15 @@ __global__ void __launch_bounds__(kThreads, BM ? 2 : 4) quantize_kernel(const Qu
     __shared__ double mred[kThreads / 32 * D];
     __shared__ float smean[D];
     if (job.bmean != nullptr) {
-      quantize_block<D, true>(job.x, job.xq, job.scale, job.mean, bh, local % p.nb, p.N, p.nb, red,
+      quantize_block<D, true>(job.x, job.xq, job.scale, mean, bh, local % p.nb, p.N, p.nb, red,
                               job.bexp != nullptr ? fac : nullptr, job.subexp ? gred : nullptr, job.bmean, mred,
-                              smean, job.bf16 != 0);
+                              smean, job.vmode);
       return;
     }
   }
-  quantize_block<D>(job.x, job.xq, job.scale, job.mean, bh, local % p.nb, p.N, p.nb, red,
+  quantize_block<D>(job.x, job.xq, job.scale, mean, bh, local % p.nb, p.N, p.nb, red,
                     job.bexp != nullptr ? fac : nullptr, job.subexp ? gred : nullptr, nullptr, nullptr, nullptr,
-                    job.bf16 != 0);
+                    job.vmode);
 }
 
 // Channel statistics of one 128-token block of one head.  Blocks with
@@ -619,7 +628,7 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const PrepParams p) 
     if (c8 == 0 && row0 + r < p.N) p.D[(size_t)bh * p.N + row0 + r] = s;
   }
   quantize_block<D>(p.dO, p.dOq, p.sdo, nullptr, bh, blk, p.N, p.nb, red, nullptr, nullptr, nullptr, nullptr,
-                    nullptr, p.bf16 != 0);
+                    nullptr, p.vmode);
 }
 
 struct ConvertJobs {

@@ -11,6 +11,12 @@
 namespace sagebwd {
 
 constexpr int kBlk = 128;                            // tokens per quantization block and per tile
+// What a quantizer stores: the INT8 code (the method), the BF16 rounding of the scaled value (error
+// attribution), or the FP8 E4M3 rounding of the value scaled to 448 (the FP8 variant); the last two
+// are exact in the BF16 operand carrier.
+enum ValueMode { kValInt8 = 0, kValBf16 = 1, kValFp8 = 2 };
+constexpr float kFp8Max = 448.f;                     // largest finite E4M3 value
+constexpr float kLog2_448 = 8.8073549220576041f;     // log2(448)
 constexpr float kLog2e = 1.4426950408889634f;        // log2(e)
 constexpr float kLn2 = 0.69314718055994531f;         // ln(2)
 constexpr float kLog2_127 = 6.9886846867721655f;     // log2(127)
@@ -38,7 +44,7 @@ struct QuantJob {
   int subexp;              // 1: power-of-two sub-scales per 8-channel group of each block (Q/K option)
   float* bmean;            // [BH][nb][d] or nullptr: Q-smoothing, each block's channel means subtracted
                            // first (and written here)
-  int bf16;                // error attribution: store the BF16 rounding of x * 127/max instead of the code
+  int vmode;               // ValueMode: INT8 code (0), BF16 of x * 127/max (1), E4M3 of x * 448/max (2)
 };
 struct QuantParams {
   QuantJob job[3];
@@ -90,7 +96,7 @@ struct PrepParams {
   float* dv_acc;            // [BHk][N][d], zeroed
   int BH, BHk, N, d, nb;
   int* status;
-  int bf16;                 // error attribution: dO stored as the BF16 rounding of dO * 127/max
+  int vmode;                // ValueMode of the dO quantizer
 };
 cudaError_t launch_bwd_prep(const PrepParams& p, cudaStream_t s);
 // FP32 gradient accumulators -> BF16 outputs, up to three arrays in one launch.
@@ -149,6 +155,8 @@ struct BwdParams {
   uint64_t timeout_ns;
 };
 constexpr uint32_t kBwdDirectDKDV = 1u << 31;
+// FwdParams.flags / BwdParams.flags: the FP8 variant's codes (set by the library, not by callers)
+constexpr uint32_t kFlagFp8Codes = 1u << 30;
 static_assert(sizeof(BwdParams) <= 128, "backward parameter block above 128 bytes");
 // The Q-smoothing instantiations take these extra tables: the logit terms [BHq][nb][128 nb], the
 // block means of Q [BHq][nb][d], and scratch for the per-slice column sums of the dS codes

@@ -65,6 +65,13 @@
  * The INT8 codes are held as integer-valued BF16 and multiplied on the
  * tensor cores with FP32 accumulation, which is exact for these tiles
  * (|sum| <= 128 * 127^2 < 2^24).
+ * FP8 variant (fp8 = 1; the pages compare INT8 with FP8 SageBwd, "SageAttention3 ... 8-Bit
+ * Training" summary page, Measured effects): every quantizer of the method stores the FP8 E4M3
+ * rounding (to nearest even, saturating at 448) of its value scaled to 448 instead of an INT8 code,
+ * with the same granularity (Q, K, V, dO per 128-token block, scale max/448; forward P~ per row and
+ * key tile, E4M3 of 448 * 2^(t - tmax); backward P per key and query tile, scale max/448; dS per
+ * tile, scale max/448); dP = dO V^T stays BF16.  Not with qk_subexp, ds_subexp, balance_qk,
+ * smooth_q, the BF16 attribution flags or SAGEBWD_FLAG_DEBUG_DUMP (SAGEBWD_ERR_UNSUPPORTED).
  *
  * Conventions for every entry point:
  *   - Tensors are row-major contiguous. Q, dO, O, dQ: BF16 [B][Hq][N][d];
@@ -138,6 +145,7 @@ typedef struct {
   uint32_t flags;       /* SAGEBWD_FLAG_* (0 in normal use) */
   float softmax_scale;  /* <= 0 selects 1/sqrt(d) */
   uint32_t wait_timeout_ms; /* bound of every in-kernel wait; 0 selects 2000 ms */
+  int32_t fp8;          /* 1: the FP8 variant (see above); 0: INT8, the method */
 } sagebwd_problem;
 
 /* Bytes of the `saved` buffer that sagebwd_fwd fills and sagebwd_bwd reads:

@@ -729,6 +729,10 @@ int oracle_quantize_qk(const oracle_problem* p, const uint16_t* q, const uint16_
   std::vector<int> e;
   Mode M{true, 0};
   M.bf16 = p->bf16_mask & ((1u << QZ_Q) | (1u << QZ_K));  // the attribution mode, where it applies to Q and K
+  if (p->fp8) {  // the FP8 variant's E4M3 values
+    M.fp8 = true;
+    M.qmax = 448.0;
+  }
   quantize_qk(M, p, q, k, qq, kq, &e);
   for (size_t i = 0; i < qq.codes.size(); ++i) qc[i] = (float)qq.codes[i];
   for (size_t i = 0; i < qq.scale.size(); ++i) qs[i] = (float)qq.scale[i];

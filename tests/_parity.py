@@ -99,11 +99,11 @@ def device_inputs(w, dev="cuda"):
     return x, {k: v.to(dev) for k, v in x.items()}
 
 
-def gpu_forward(w, xd, smooth_k=True, flags=0, timeout_ms=0, balance_qk=False, ds_subexp=False, qk_subexp=True,
-                smooth_q=False):
+def gpu_forward(w, xd, smooth_k=True, flags=0, timeout_ms=0, balance_qk=False, ds_subexp=False, qk_subexp=None,
+                smooth_q=False, fp8=False):
     prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_k=smooth_k, flags=flags,
                            wait_timeout_ms=timeout_ms, balance_qk=balance_qk, ds_subexp=ds_subexp,
-                           qk_subexp=qk_subexp, smooth_q=smooth_q)
+                           qk_subexp=qk_subexp, smooth_q=smooth_q, fp8=fp8)
     dev = xd["q"].device
     o = torch.empty_like(xd["q"])
     lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
@@ -126,11 +126,14 @@ def gpu_backward(w, xd, fwd):
     return {"dq": dq, "dk": dk, "dv": dv, "ws": ws, "status": code, "word": word}
 
 
-def oracle_problem(oracle_mod, w, smooth_k=True, balance_qk=False, ds_subexp=False, qk_subexp=True, smooth_q=False):
-    """The oracle problem matching gpu_forward's defaults (the library's: K-smoothing and the Q/K
-    sub-scales on)."""
+def oracle_problem(oracle_mod, w, smooth_k=True, balance_qk=False, ds_subexp=False, qk_subexp=None, smooth_q=False,
+                   fp8=False):
+    """The oracle problem matching gpu_forward's defaults (the library's: K-smoothing and, for INT8,
+    the Q/K sub-scales on)."""
+    if qk_subexp is None:
+        qk_subexp = not fp8
     return oracle_mod.problem(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, smooth_k=smooth_k, balance_qk=balance_qk,
-                              ds_subexp=ds_subexp, qk_subexp=qk_subexp, smooth_q=smooth_q)
+                              ds_subexp=ds_subexp, qk_subexp=qk_subexp, smooth_q=smooth_q, fp8=fp8)
 
 
 def block_selection(w, heads, blocks, kv=False):

@@ -150,3 +150,16 @@ def test_attribution_flags_refused_with_unsupported_options(lib):
     for opts, flags in (({"ds_subexp": True}, 0), ({"smooth_q": True}, 0), ({}, sb.FLAG_DEBUG_DUMP)):
         p = sb.Problem.make(1, 2, 1, 300, 64, True, flags=sb.FLAG_BF16["ds"] | flags, **opts)
         assert sb.sagebwd_workspace_bytes(p, 1) == 0, opts
+
+
+def test_fp8_variant_sizes_and_refusals(lib):
+    """The FP8 variant has the INT8 layouts (E4M3 values held in the same BF16 buffers) and refuses the
+    INT8-only refinements."""
+    p8 = sb.Problem.make(1, 4, 2, 300, 64, True, fp8=True)
+    assert p8.qk_subexp == 0  # no sub-scales for E4M3 values
+    p0 = sb.Problem.make(1, 4, 2, 300, 64, True, qk_subexp=False)
+    assert sb.sagebwd_saved_bytes(p8) == sb.sagebwd_saved_bytes(p0) > 0
+    assert sb.sagebwd_workspace_bytes(p8, 1) == sb.sagebwd_workspace_bytes(p0, 1)
+    for opts in ({"qk_subexp": True}, {"ds_subexp": True}, {"balance_qk": True}, {"smooth_q": True},
+                 {"flags": sb.FLAG_BF16["ds"]}, {"flags": sb.FLAG_DEBUG_DUMP}):
+        assert sb.sagebwd_saved_bytes(sb.Problem.make(1, 4, 2, 300, 64, True, fp8=True, **opts)) == 0, opts

@@ -73,27 +73,3 @@ def test_roofline_peak_follows_the_power_cap(bench_mod):
     peaks = {"bf16_burst": 1926.9, "bf16_sustained": 1715.2}
     assert bench_mod.roofline_peak(peaks, {"reasons": []}) == (1926.9, "burst")
     assert bench_mod.roofline_peak(peaks, {"reasons": ["sw_power_cap"]}) == (1715.2, "sustained")
-
-
-def test_kernel_names_are_matched_exactly(bench_mod):
-    k = bench_mod._kernel_of
-    assert k("void sagebwd::(anonymous namespace)::bwd_kernel<128, true, false, false, false>(CUtensorMap_st)") \
-        == "bwd_kernel"
-    assert k("void sagebwd::(anonymous namespace)::bwd_prep_kernel<64>(sagebwd::PrepParams)") == "bwd_prep_kernel"
-    assert k("void sagebwd::(anonymous namespace)::quantize_kernel<128, false>(sagebwd::QuantParams)") \
-        == "quantize_kernel"
-    assert k("void at::native::vectorized_elementwise_kernel<4, at::native::FillFunctor<unsigned char>>") is None
-
-
-def test_quantize_bandwidth_arithmetic(bench_mod):
-    from bit_trainable_attention_gb300 import workloads as W
-    w = W.small("bw", 1, 4, 2, 256, 64, True, 1)
-    # 1 us per launch: bytes per launch / 1e-6 s
-    times = {"kmean_partial_kernel": (1, 1.0), "kmean_final_kernel": (1, 1.0), "quantize_kernel": (1, 1.0)}
-    out = bench_mod.quantize_bandwidth(w, None, times, 6800.0)
-    qe, ke, nb = 4 * 256 * 64, 2 * 256 * 64, 2
-    assert out["kmean_partial_kernel"]["bytes_per_launch"] == 2 * ke + 8 * 2 * nb * 64
-    assert out["quantize_kernel"]["bytes_per_launch"] == 4 * (qe + 2 * ke) + 4 * 2 * 64 + 4 * nb * (4 + 4)
-    assert out["quantize_kernel"]["gb_per_s"] == pytest.approx(out["quantize_kernel"]["bytes_per_launch"] / 1e3,
-                                                               rel=1e-3)
-    assert out["stage"]["us"] == 3.0
