@@ -139,14 +139,15 @@ class ClockSampler:
 class Step:
     """Buffers and the stage-by-stage calls of one forward + backward step."""
 
-    def __init__(self, w: W.Workload, dev, balance_qk=False, ds_subexp=False, qk_subexp=True, inputs=None,
-                 smooth_q=False, flags=0):
+    def __init__(self, w: W.Workload, dev, balance_qk=False, ds_subexp=False, qk_subexp=None, inputs=None,
+                 smooth_q=False, flags=0, fp8=False):
         self.w = w
         x = W.make_inputs(w) if inputs is None else inputs
         self.host = x
         self.x = {k: v.to(dev) for k, v in x.items()}
         self.prob = sb.Problem.make(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, balance_qk=balance_qk,
-                                    ds_subexp=ds_subexp, qk_subexp=qk_subexp, smooth_q=smooth_q, flags=flags)
+                                    ds_subexp=ds_subexp, qk_subexp=qk_subexp, smooth_q=smooth_q, flags=flags,
+                                    fp8=fp8)
         p = self.prob
         self.o = torch.empty_like(self.x["q"])
         self.lse = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
@@ -240,6 +241,27 @@ def cossim_vs_torch(step: Step):
     for name in ("o", "dq", "dk", "dv"):
         a, b = got[name].float().reshape(-1), ref[name].reshape(-1)
         out[name] = round(float(torch.nn.functional.cosine_similarity(a, b, dim=0)), 6)
+    return out
+
+
+def fp8_variant(step: Step, args, dev, flush):
+    """The FP8 E4M3 variant of the method on the same inputs (forward on the FP8 tensor cores):
+    step time and its stages (timed like the headline, shorter) and CosSim against FP32 attention."""
+    other = Step(step.w, dev, inputs=step.host, fp8=True)
+    total, stage = time_device(other, max(10, args.steps // 5), 3, flush, lambda: None)
+    ms = sum(total) / len(total)
+    st = [sum(x) / len(x) for x in stage]
+    w = step.w
+    out = {"ms_per_step": round(ms, 4), "tops": round((w.flops_fwd() + w.flops_bwd()) / (ms * 1e-3) / 1e12, 2),
+           "breakdown_ms": {"quantize": round(st[0], 4), "fwd": round(st[1], 4), "bwd": round(st[3], 4)},
+           "fwd_kernel_tflops": round(w.flops_fwd() / (st[1] * 1e-3) / 1e12, 1),
+           "cossim_vs_torch_fp32": cossim_vs_torch(other),
+           "note": "E4M3 values scaled to 448 at the INT8 granularity; forward S and PV on tcgen05 kind::f8f6f4, "
+                   "backward on the same values in BF16 operands"}
+    code0, _ = sb.sagebwd_check_status(other.ws0)
+    code1, _ = sb.sagebwd_check_status(other.ws1)
+    out["status"] = [code0, code1]
+    del other
     return out
 
 
@@ -607,8 +629,8 @@ def roofline_peak(peaks: dict, clocks: dict):
 def config_summary(w: W.Workload, dev, args, flush, peaks):
     """A second configuration of the metric (the 8K-token GQA layer), timed like the headline:
     ms and TOPS of the step, the backward kernel's fraction of the BF16 peaks, CosSim vs FP32."""
-    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp, qk_subexp=not args.qk_plain,
-                smooth_q=args.smooth_q)
+    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp,
+                qk_subexp=not (args.qk_plain or args.fp8), smooth_q=args.smooth_q, fp8=args.fp8)
     total, stage = time_device(step, max(10, args.steps // 2), max(3, args.warmup), flush, lambda: None)
     ms = sum(total) / len(total)
     st = [sum(x) / len(x) for x in stage]
@@ -655,6 +677,8 @@ def main():
                     help="time the library's optional dS sub-scales (the other settings are reported beside)")
     ap.add_argument("--qk-plain", action="store_true",
                     help="time the plain one-scale-per-block Q/K mode instead of the default Q/K sub-scales")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the FP8 E4M3 variant instead of INT8 (forward on the FP8 tensor cores; no sub-scales)")
     ap.add_argument("--smooth-q", action="store_true",
                     help="time the library's optional Q-smoothing (block means of Q subtracted, logit term added)")
     ap.add_argument("--layer-step", type=int, default=8192, metavar="TOKENS",
@@ -693,8 +717,8 @@ def main():
         cpu = cpu_baseline(w, args.cpu_budget_s)
 
     sb.load_library()
-    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp, qk_subexp=not args.qk_plain,
-                smooth_q=args.smooth_q)
+    step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp,
+                qk_subexp=not (args.qk_plain or args.fp8), smooth_q=args.smooth_q, fp8=args.fp8)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sampler = ClockSampler(local)
     sampler.wait()
@@ -724,11 +748,13 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8 (integer-valued bf16 on tcgen05, fp32 accumulate) + bf16 dP",
+        "vs_baseline": None,
+        "dtype": ("fp8 e4m3 (forward on tcgen05 kind::f8f6f4; backward e4m3 values in bf16 operands) + bf16 dP"
+                  if args.fp8 else "int8 (integer-valued bf16 on tcgen05, fp32 accumulate) + bf16 dP"),
         "data": "synthetic",
         "config": {"workload": describe(w), "l2": "flushed between timed steps (256 MB write)",
                    "qk_granularity": "per-block scale + 8-channel power-of-two sub-scales (library default)"
-                   if not args.qk_plain else "one scale per 128-token block",
+                   if not (args.qk_plain or args.fp8) else "one scale per 128-token block",
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
         "breakdown_ms": {"quantize": round(stage_ms[0], 4), "fwd": round(stage_ms[1], 4),
                          "bwd_prepare": round(stage_ms[2], 4), "bwd": round(stage_ms[3], 4),
@@ -755,8 +781,8 @@ def main():
             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4),
             "copies": "double-buffered on two copy streams: step i+1's inputs up and step i-1's results down while "
                       "step i computes; each step timed from the end of its L2 flush"},
-        "balance_qk": bool(args.balance_qk), "qk_subexp": not args.qk_plain, "ds_subexp": bool(args.ds_subexp),
-        "smooth_q": bool(args.smooth_q),
+        "balance_qk": bool(args.balance_qk), "qk_subexp": bool(step.prob.qk_subexp),
+        "ds_subexp": bool(args.ds_subexp), "smooth_q": bool(args.smooth_q), "fp8": bool(args.fp8),
         "gpu_launches": step.launches() * args.steps,
         "clocks": clocks,
         "status": [code0, code1],
@@ -765,8 +791,9 @@ def main():
         line["cossim_vs_torch_fp32"] = None if args.no_cossim else cossim_vs_torch(step)
         if not args.no_extras:
             line["quantize_hbm"] = quantize_bandwidth(step, flush, peaks["hbm_gbs"])
-            if not args.no_cossim:
+            if not args.no_cossim and not args.fp8:
                 line["other_settings"] = other_settings(step, args, dev, flush)
+                line["fp8_variant"] = fp8_variant(step, args, dev, flush)
                 if not (args.ds_subexp or args.smooth_q):
                     line["error_attribution"] = error_attribution(step, dev)
         if args.compare_sdpa:

@@ -273,6 +273,8 @@ def quantized_views(prob: Problem, saved: torch.Tensor) -> dict:
              ("e", B * Hkv * d * 4)]
     if prob.smooth_q:
         sizes += [("qm", B * Hq * nb * d * 4), ("qb", B * Hq * nb * nb * 128 * 4)]
+    if prob.fp8:
+        sizes += [("q8", B * Hq * N * d), ("k8", B * Hkv * N * d), ("v8t", B * Hkv * d * nb * 128)]
     out, off = {}, 0
     for name, n in sizes:
         out[name] = saved[off:off + n]
@@ -288,6 +290,10 @@ def quantized_views(prob: Problem, saved: torch.Tensor) -> dict:
     if prob.smooth_q:
         out["qm"] = out["qm"].view(torch.float32).view(B * Hq, nb, d)
         out["qb"] = out["qb"].view(torch.float32).view(B * Hq, nb, nb * 128)
+    if prob.fp8:  # E4M3 bytes
+        out["q8"] = out["q8"].view(B * Hq, N, d)
+        out["k8"] = out["k8"].view(B * Hkv, N, d)
+        out["v8t"] = out["v8t"].view(B * Hkv, d, nb * 128)
     return out
 
 

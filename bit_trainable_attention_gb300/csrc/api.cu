@@ -50,7 +50,7 @@ sagebwd_status check_problem(const sagebwd_problem* p) {
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 struct SavedLayout {
-  size_t q, k, v, sq, sk, sv, mu, be, qm, qb, total;
+  size_t q, k, v, sq, sk, sv, mu, be, qm, qb, q8, k8, v8t, total;
 };
 SavedLayout saved_layout(const sagebwd_problem* p) {
   const size_t nb = (size_t)nblocks(p->N);
@@ -65,10 +65,15 @@ SavedLayout saved_layout(const sagebwd_problem* p) {
   L.sv = off; off += align_up((size_t)p->B * p->Hkv * nb * 4);
   L.mu = off; off += align_up((size_t)p->B * p->Hkv * p->d * 4);
   L.be = off; off += align_up((size_t)p->B * p->Hkv * p->d * 4);
-  L.qm = L.qb = 0;
+  L.qm = L.qb = L.q8 = L.k8 = L.v8t = 0;
   if (p->smooth_q) {  // block means of Q, and the logit terms mean_Q . K' per (query head, query block, key)
     L.qm = off; off += align_up((size_t)p->B * p->Hq * nb * p->d * 4);
     L.qb = off; off += align_up((size_t)p->B * p->Hq * nb * nb * kBlk * 4);
+  }
+  if (p->fp8) {  // the E4M3 values as bytes for the FP8 forward: Q, K row-major, V transposed per head
+    L.q8 = off; off += align_up(qe);
+    L.k8 = off; off += align_up(ke);
+    L.v8t = off; off += align_up((size_t)p->B * p->Hkv * p->d * nb * kBlk);
   }
   L.total = off;
   return L;
@@ -166,6 +171,21 @@ bool make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over a byte tensor [outer][mid][inner] (E4M3 values): box = box_inner bytes x box_mid x 1,
+// swizzle of box_inner bytes (128 or 64); rows past mid read as zero.
+bool make_map_u8(CUtensorMap* m, const void* base, int outer, int mid, int inner, int box_inner, int box_mid) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)inner, (cuuint64_t)inner * mid};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_mid, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz = box_inner == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 float softmax_scale_of(const sagebwd_problem* p) {
   return p->softmax_scale > 0.f ? p->softmax_scale : (float)(1.0 / std::sqrt((double)p->d));
 }
@@ -230,9 +250,6 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
     sp.status = status;
     SB_CHECK(cuda_status(launch_qk_stats(sp, st)));
     bexp = at<int>(saved, S.be);
-  } else if (p->smooth_k) {
-    SB_CHECK(cuda_status(launch_kmean(static_cast<const __nv_bfloat16*>(k), at<double>(ws, W.kpart),
-                                      at<float>(saved, S.mu), p->B * p->Hkv, p->N, p->d, status, 1, st)));
   }
   const int G = p->Hq / p->Hkv;
   QuantParams qp{};
@@ -243,15 +260,41 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
                p->B * p->Hkv, bexp, 1, 1, p->qk_subexp ? 1 : 0, nullptr, vmode_of(p, SAGEBWD_FLAG_BF16_K)};
   qp.job[2] = {static_cast<const __nv_bfloat16*>(v), at<__nv_bfloat16>(saved, S.v), at<float>(saved, S.sv), nullptr,
                p->B * p->Hkv, nullptr, 1, 1, 0, nullptr, vmode_of(p, SAGEBWD_FLAG_BF16_V)};
-  qp.njobs = 3;
-  qp.block_start[0] = 0;
-  for (int j = 0; j < 3; ++j) qp.block_start[j + 1] = qp.block_start[j] + qp.job[j].BH * nb;
+  if (p->fp8) {  // the bytes the FP8 forward reads
+    qp.job[0].x8 = at<uint8_t>(saved, S.q8);
+    qp.job[1].x8 = at<uint8_t>(saved, S.k8);
+    qp.job[2].x8t = at<uint8_t>(saved, S.v8t);
+  }
   qp.N = p->N;
   qp.d = p->d;
   qp.nb = nb;
   qp.status = status;
-  qp.clear_status = (p->smooth_k || p->balance_qk) ? 0 : 1;
-  SB_CHECK(cuda_status(launch_quantize(qp, st)));
+  auto launch_jobs = [&](std::initializer_list<QuantJob> jobs, int clear) -> sagebwd_status {
+    QuantParams lp = qp;
+    lp.njobs = 0;
+    lp.block_start[0] = 0;
+    for (const QuantJob& j : jobs) {
+      lp.job[lp.njobs] = j;
+      lp.block_start[lp.njobs + 1] = lp.block_start[lp.njobs] + j.BH * nb;
+      ++lp.njobs;
+    }
+    lp.clear_status = clear;
+    return cuda_status(launch_quantize(lp, st));
+  };
+  if (p->smooth_k && !p->balance_qk) {
+    // K-smoothing: K's block sums ride in the launch that quantizes Q and V, the channel means follow
+    // (a small kernel), then K's codes
+    QuantJob jsum{};
+    jsum.x = static_cast<const __nv_bfloat16*>(k);
+    jsum.BH = p->B * p->Hkv;
+    jsum.part = at<double>(ws, W.kpart);
+    SB_CHECK(launch_jobs({jsum, qp.job[0], qp.job[2]}, 1));
+    SB_CHECK(cuda_status(launch_kmean_final(at<double>(ws, W.kpart), at<float>(saved, S.mu), p->B * p->Hkv, p->N,
+                                            p->d, st)));
+    SB_CHECK(launch_jobs({qp.job[1]}, 0));
+  } else {
+    SB_CHECK(launch_jobs({qp.job[0], qp.job[1], qp.job[2]}, p->balance_qk ? 0 : 1));
+  }
   if (p->smooth_q) {
     QBiasParams bp{};
     bp.k = static_cast<const __nv_bfloat16*>(k);
@@ -275,10 +318,17 @@ sagebwd_status fwd_attention_impl(const sagebwd_problem* p, const void* saved, v
   const SavedLayout S = saved_layout(p);
   const WsLayout W = ws_layout(p, 0);
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, at<uint8_t>(saved, S.q), p->B * p->Hq, p->N, p->d) ||
-      !make_map(&tk, at<uint8_t>(saved, S.k), p->B * p->Hkv, p->N, p->d) ||
-      !make_map(&tv, at<uint8_t>(saved, S.v), p->B * p->Hkv, p->N, p->d))
+  if (p->fp8) {  // the FP8 tensor cores read the E4M3 bytes (V transposed per head)
+    const int nb = nblocks(p->N);
+    if (!make_map_u8(&tq, at<uint8_t>(saved, S.q8), p->B * p->Hq, p->N, p->d, p->d, 128) ||
+        !make_map_u8(&tk, at<uint8_t>(saved, S.k8), p->B * p->Hkv, p->N, p->d, p->d, 128) ||
+        !make_map_u8(&tv, at<uint8_t>(saved, S.v8t), p->B * p->Hkv, p->d, nb * kBlk, 128, p->d))
+      return SAGEBWD_ERR_CUDA;
+  } else if (!make_map(&tq, at<uint8_t>(saved, S.q), p->B * p->Hq, p->N, p->d) ||
+             !make_map(&tk, at<uint8_t>(saved, S.k), p->B * p->Hkv, p->N, p->d) ||
+             !make_map(&tv, at<uint8_t>(saved, S.v), p->B * p->Hkv, p->N, p->d)) {
     return SAGEBWD_ERR_CUDA;
+  }
   FwdDumpParams fp{};
   fp.B = p->B;
   fp.Hq = p->Hq;
@@ -297,7 +347,7 @@ sagebwd_status fwd_attention_impl(const sagebwd_problem* p, const void* saved, v
   fp.status = at<int>(ws, W.status);
   fp.timeout_ns = timeout_of(p);
   fp.flags = kernel_flags(p);
-  return cuda_status(launch_fwd(tq, tk, tv, fp, p->d, p->causal, st));
+  return cuda_status(launch_fwd(tq, tk, tv, fp, p->d, p->causal, p->fp8, st));
 }
 
 // Query heads per backward CTA for this shape on the current device, memoised

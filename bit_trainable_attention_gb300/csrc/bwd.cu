@@ -558,7 +558,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       float a = am[0];
 #pragma unroll
       for (int q = 1; q < C::S_WARPS; ++q) a = fmaxf(a, am[q]);
-      const bool p_live = pmax >= kMinGroupMax, d_live = a >= kMinGroupMax;
+      constexpr float kMinMax = VAR == kValFp8 ? kMinGroupMaxFp8 : kMinGroupMax;
+      const bool p_live = pmax >= kMinMax, d_live = a >= kMinMax;
       // hardware reciprocal (<= 2 ulp) rather than IEEE division: these scales only
       // decide codes of this tile and dequantize it; a code at a rounding tie may differ
       constexpr float kQMax = VAR == kValFp8 ? kFp8Max : 127.f;

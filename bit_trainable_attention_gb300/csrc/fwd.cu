@@ -49,10 +49,12 @@ struct FwdRegs {
   static_assert(128 * LOW + 256 * HIGH <= kFThreads * kFRegsLaunch, "register split exceeds the launch");
 };
 
-template <int D>
+// F8: the FP8 variant on the FP8 tensor cores (1-byte E4M3 tiles: Q^, K^ [128 tokens][D], V^
+// transposed [D][128 keys]; three K / V stages).
+template <int D, bool F8 = false>
 struct FwdCfg {
-  static constexpr int NS = 2;             // K / V stages
-  static constexpr int TILE = 128 * D * 2;  // one Q^ / K^ / V^ tile (bytes)
+  static constexpr int NS = F8 ? 3 : 2;                 // K / V stages
+  static constexpr int TILE = 128 * D * (F8 ? 1 : 2);  // one Q^ / K^ / V^ tile (bytes)
   static constexpr int OFF_Q = 0;           // two Q^ tiles
   static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
@@ -93,11 +95,15 @@ __device__ __forceinline__ void fdump16(uint8_t* dst, const uint32_t* w) {
 // VAR (ValueMode of the P~ operand): kValInt8 its integer code rint(127 * 2^(t - tmax)); kValBf16
 // (error attribution, SAGEBWD_FLAG_BF16_PF) the BF16 rounding of 127 * 2^(t - tmax); kValFp8 (the
 // FP8 variant) the E4M3 rounding of 448 * 2^(t - tmax), dequantized by 2^(tmax - m) / 448.
-template <int D, bool CAUSAL, bool QSM, bool DBG, int VAR = kValInt8>
+// F8 (with VAR == kValFp8): the same values as E4M3 bytes on the FP8 tensor cores (tcgen05.mma
+// kind::f8f6f4, K = 32 per instruction): S from the byte tiles of Q^ and K^, O = P^ V^ with the P~
+// bytes packed four per TMEM column and V^ read from its transposed tile (all operands K-major).
+template <int D, bool CAUSAL, bool QSM, bool DBG, int VAR = kValInt8, bool F8 = false>
 __global__ void __launch_bounds__(kFThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const typename FwdParamsOf<DBG>::type p) {
-  using C = FwdCfg<D>;
+  static_assert(!F8 || (VAR == kValFp8 && !QSM && !DBG), "the FP8 tensor-core path is the FP8 variant only");
+  using C = FwdCfg<D, F8>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -168,16 +174,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
       const int nq = (nkb[0] > 0) + (nkb[1] > 0);
       mbar_arrive_expect_tx(bar_q, nq * C::TILE);
       for (int t = 0; t < 2; ++t)
-        if (nkb[t] > 0)
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + C::OFF_Q + t * C::TILE + c * 16384, &tmQ, bar_q, c * 64, (2 * pr + t) * kBlk, bhq);
+        if (nkb[t] > 0) {
+          if constexpr (F8)
+            tma_load_3d(smem + C::OFF_Q + t * C::TILE, &tmQ, bar_q, 0, (2 * pr + t) * kBlk, bhq);
+          else
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(smem + C::OFF_Q + t * C::TILE + c * 16384, &tmQ, bar_q, c * 64, (2 * pr + t) * kBlk, bhq);
+        }
       for (int j = 0; j < nkb_max; ++j) {
         const int s = j % NS, n = j / NS;
         if (j >= NS && !wait1(wc, bar_k_empty + s, (n - 1) & 1, kSiteKEmpty)) break;
         if (!((p.flags & SAGEBWD_FLAG_DROP_ONE_LOAD) && j == 1)) {  // fault injection skips one load
           mbar_arrive_expect_tx(bar_k_full + s, C::TILE);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + C::OFF_K + s * C::TILE + c * 16384, &tmK, bar_k_full + s, c * 64, j * kBlk, bhk);
+          if constexpr (F8)
+            tma_load_3d(smem + C::OFF_K + s * C::TILE, &tmK, bar_k_full + s, 0, j * kBlk, bhk);
+          else
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(smem + C::OFF_K + s * C::TILE + c * 16384, &tmK, bar_k_full + s, c * 64, j * kBlk, bhk);
           k_issued[s] = n + 1;
         }
         if (j >= NS && !wait1(wc, bar_v_empty + s, (n - 1) & 1, kSiteVEmpty)) break;
@@ -185,8 +198,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
         // V stage, which is released only after both tiles' codes of key tile j are written
         const int nbias = QSM ? (j < nkb[0]) + (j < nkb[1]) : 0;
         mbar_arrive_expect_tx(bar_v_full + s, C::TILE + nbias * 512);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * 16384, &tmV, bar_v_full + s, c * 64, j * kBlk, bhk);
+        if constexpr (F8)  // the transposed V^ tile [D][128 keys]
+          tma_load_3d(smem + C::OFF_V + s * C::TILE, &tmV, bar_v_full + s, j * kBlk, 0, bhk);
+        else
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::OFF_V + s * C::TILE + c * 16384, &tmV, bar_v_full + s, c * 64, j * kBlk, bhk);
         if (QSM) {
           for (int t = 0; t < 2; ++t)
             if (j < nkb[t])
@@ -204,21 +220,37 @@ __global__ void __launch_bounds__(kFThreads, 1)
       }
     } else if (warp == 9 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      const uint32_t idO = idesc_bf16_f32(128, D, false, true);
+      const uint32_t idS = F8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
+      const uint32_t idO = F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, false, true);
+      // FP8 tiles: rows of D bytes (128-byte swizzle for D = 128, 64-byte for D = 64; 8-row stride
+      // 8 D bytes); the transposed V^ tile has 128-byte rows
+      constexpr uint32_t kF8Swz = D == 128 ? kSwizzle128B : kSwizzle64B;
       // S_t = Q^_t K^_j^T into TMEM columns [col_s(t), col_s(t) + 128)
       auto issue_s = [&](int t, uint32_t kdesc) {
-        const uint32_t qdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_Q + t * C::TILE), 16);
-        if constexpr (D == 128)
-          umma_chain8_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
-        else
-          umma_chain4_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
+        const uint32_t qaddr = smem_u32(smem + C::OFF_Q + t * C::TILE);
+        if constexpr (F8) {
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk)  // 32 bytes of the K dimension per MMA
+            umma_f8_ss(tmem + C::col_s(t), sdesc_kmajor(qaddr + kk * 32, 8 * D, kF8Swz),
+                       sdesc_kmajor(kdesc + kk * 32, 8 * D, kF8Swz), idS, kk > 0);
+        } else {
+          const uint32_t qdesc = sdesc_sw128_lo(qaddr, 16);
+          if constexpr (D == 128)
+            umma_chain8_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
+          else
+            umma_chain4_kk(tmem + C::col_s(t), sdesc_from_lo(qdesc), sdesc_from_lo(kdesc), idS);
+        }
         umma_commit(bar_s_full + t);
+      };
+      // FP8: issue_s takes the K^ tile's shared address, the BF16 path its descriptor low word
+      auto k_arg = [&](int st) -> uint32_t {
+        const uint32_t a = smem_u32(smem + C::OFF_K + st * C::TILE);
+        return F8 ? a : sdesc_sw128_lo(a, 16);
       };
       bool ok = wait1(wc, bar_q, 0, kSiteQ) && wait1(wc, bar_k_full, 0, kSiteKFull);
       if (ok) {
         tc_fence_after();
-        const uint32_t kdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_K), 16);
+        const uint32_t kdesc = k_arg(0);
         for (int t = 0; t < 2; ++t)
           if (nkb[t] > 0) issue_s(t, kdesc);
         umma_commit(bar_k_empty);
@@ -228,8 +260,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
       for (int j = 0; ok && j < nkb_max; ++j) {
         const int s = j % NS, s1 = (j + 1) % NS;
         if (!wait1(wc, bar_v_full + s, (j / NS) & 1, kSiteVFull)) break;
-        const uint32_t vdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_V + s * C::TILE), 16384);
-        const uint32_t kdesc = sdesc_sw128_lo(smem_u32(smem + C::OFF_K + s1 * C::TILE), 16);
+        const uint32_t vaddr = smem_u32(smem + C::OFF_V + s * C::TILE);
+        const uint32_t vdesc = sdesc_sw128_lo(vaddr, 16384);
+        const uint32_t kdesc = k_arg(s1);
         bool k_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -240,11 +273,21 @@ __global__ void __launch_bounds__(kFThreads, 1)
               break;
             }
             tc_fence_after();
-            // O_t = P^_t V^_j: A = the codes in TMEM (128 keys = 64 packed columns, 8 per
-            // K step), B = V^_j [key][d] read MN-major
+            if constexpr (F8) {
+              // O_t = P^_t V^_j: A = the E4M3 bytes in TMEM (128 keys = 32 columns, 8 per K step of
+              // 32), B = the transposed V^_j [d][key], K-major (32 bytes per K step)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_from_lo(vdesc + kk * 128), idO, kk > 0);
+              for (int kk = 0; kk < 4; ++kk)
+                umma_f8_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+                           sdesc_kmajor(vaddr + kk * 32, 1024, kSwizzle128B), idO, kk > 0);
+            } else {
+              // O_t = P^_t V^_j: A = the codes in TMEM (128 keys = 64 packed columns, 8 per
+              // K step), B = V^_j [key][d] read MN-major
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_from_lo(vdesc + kk * 128), idO,
+                        kk > 0);
+            }
             umma_commit(bar_pv_done + t);
           }
           if (j + 1 < nkb[t]) {
@@ -438,6 +481,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         tmem_ld32(s_addr + c0, v);
         tmem_ld_wait();
         uint32_t pk[16];
+        uint32_t pb[8];  // F8: the chunk's 32 E4M3 bytes, four per word
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float2 x = QSM ? fadd2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), bias2)
@@ -448,7 +492,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
             if (c0 + e + 1 >= kvis) u.y = 0.f;
           }
           usum = fadd2(usum, u);
-          if constexpr (VAR == kValBf16) {
+          if constexpr (F8) {
+            const uint32_t b2 = e4m3x2_bytes(u.x, u.y);
+            if (e & 2)
+              pb[e >> 2] |= b2 << 16;
+            else
+              pb[e >> 2] = b2;
+          } else if constexpr (VAR == kValBf16) {
             pk[e >> 1] = pack_bf16x2(u.x, u.y);
           } else if constexpr (VAR == kValFp8) {
             pk[e >> 1] = e4m3x2_bf16x2(u.x, u.y);
@@ -459,7 +509,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
           }
         }
         if constexpr (DBG) fdump16(dump_rec(j) + FwdDump<D>::PC + ((size_t)r * 128 + c0) * 2, pk);
-        tmem_st16(s_addr + (c0 >> 1), pk);
+        if constexpr (F8)
+          tmem_st8(s_addr + (c0 >> 2), pb);
+        else
+          tmem_st16(s_addr + (c0 >> 1), pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -495,10 +548,17 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdDumpParams& p,
-                         cudaStream_t s) {
+                         int f8, cudaStream_t s) {
   using C = FwdCfg<D>;
   const int grid = (p.nb + 1) / 2 * p.B * p.Hq;
-  if (p.dump != nullptr) {
+  if (f8) {
+    if (p.qbias != nullptr || p.dump != nullptr || !(p.flags & kFlagFp8Codes)) return cudaErrorInvalidValue;
+    auto kern = fwd_kernel<D, CAUSAL, false, false, kValFp8, true>;
+    constexpr int smem = FwdCfg<D, true>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kFThreads, smem, s>>>(tq, tk, tv, static_cast<const FwdParams&>(p));
+  } else if (p.dump != nullptr) {
     if (p.qbias != nullptr) return cudaErrorInvalidValue;  // the dump covers the plain instantiation only
     auto kern = fwd_kernel<D, CAUSAL, false, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -523,9 +583,10 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdDumpParams& p,
-                       int d, int causal, cudaStream_t s) {
-  if (d == 64) return causal ? launch_fwd_t<64, true>(tq, tk, tv, p, s) : launch_fwd_t<64, false>(tq, tk, tv, p, s);
-  return causal ? launch_fwd_t<128, true>(tq, tk, tv, p, s) : launch_fwd_t<128, false>(tq, tk, tv, p, s);
+                       int d, int causal, int f8, cudaStream_t s) {
+  if (d == 64)
+    return causal ? launch_fwd_t<64, true>(tq, tk, tv, p, f8, s) : launch_fwd_t<64, false>(tq, tk, tv, p, f8, s);
+  return causal ? launch_fwd_t<128, true>(tq, tk, tv, p, f8, s) : launch_fwd_t<128, false>(tq, tk, tv, p, f8, s);
 }
 
 }  // namespace sagebwd

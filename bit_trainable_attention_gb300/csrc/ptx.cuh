@@ -173,6 +173,24 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D(tmem) (+)= A(smem) * B(smem), FP8 E4M3 operands (kind::f8f6f4, K = 32 per instruction).
+__device__ __forceinline__ void umma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem), FP8 E4M3 operands; A packs four values per 32-bit column.
+__device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // ---------------------------------------------------------------- chained MMAs
 // One K loop of tcgen05.mma kind::f16 in a single asm block (the first MMA
 // overwrites D, the rest accumulate), so the issuing thread spends about three
@@ -281,6 +299,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with E4M3 A/B (format 0) and FP32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Swizzle modes of the tcgen05 shared-memory descriptor (bits [61,64)).
+constexpr uint32_t kSwizzle128B = 2, kSwizzle64B = 4;
+// K-major descriptor with a given 8-row stride and swizzle mode (leading byte offset unused: 16).
+__device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr, uint32_t sbo_bytes, uint32_t swizzle) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)swizzle << 61;
+  return d;
+}
 // Shared-memory matrix descriptor (tcgen05 layout): [0,14) start>>4,
 // [16,30) leading byte offset>>4, [32,46) stride byte offset>>4,
 // [46,48) version = 1, [61,64) swizzle mode (2 = 128-byte swizzle).
@@ -441,6 +475,12 @@ __device__ __forceinline__ uint32_t e4m3x2_bf16x2(float a, float b) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
   return r;
+}
+// Two floats rounded to FP8 E4M3 (to nearest even, saturating) as two bytes (lo = a, hi = b).
+__device__ __forceinline__ uint32_t e4m3x2_bytes(float a, float b) {
+  uint16_t e;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(e) : "f"(a), "f"(b));
+  return (uint32_t)e;
 }
 // Pack two floats into bf16x2 (lo = a, hi = b), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

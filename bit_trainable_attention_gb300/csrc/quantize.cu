@@ -127,12 +127,15 @@ __device__ __forceinline__ void exact_row_sums(const uint4 (&u)[RPL], double (&a
 // keeps its scale but stores the BF16 rounding (to nearest even) of x * inv instead of the code (no
 // sub-scales); kValFp8 (the FP8 variant) scale = a/448, inv = 448/a and the stored value is the
 // E4M3 rounding (to nearest even, saturating) of x * inv, held exactly in BF16.
+// x8 / x8t (kValFp8 only, optional): the E4M3 values also as bytes, [BH][N][D] and transposed
+// [BH][D][128 nb] (through the shared tile t8 [D][128]; zero past N).
 template <int D, bool BM = false>
 __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ xq,
                                float* __restrict__ scale, const float* __restrict__ mean, int bh, int blk, int N,
                                int nb, float* red, const float* fac = nullptr, float* gred = nullptr,
                                float* __restrict__ bmean = nullptr, double* mred = nullptr, float* smean = nullptr,
-                               int vmode = kValInt8) {
+                               int vmode = kValInt8, uint8_t* __restrict__ x8 = nullptr,
+                               uint8_t* __restrict__ x8t = nullptr, uint8_t* t8 = nullptr) {
   constexpr int V8 = D / 8, RL = kThreads / V8;
   constexpr int PER = kBlk / RL;  // rows (16-byte vectors) per thread
   static_assert(kThreads % V8 == 0 && kBlk % RL == 0, "thread layout");
@@ -206,24 +209,51 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
   }
   float gmax = amax;  // this thread's part of its 8-channel group's maximum
   const float a = block_max(amax, red);
-  const bool live = a >= kMinGroupMax;
+  const bool live = a >= (vmode == kValFp8 ? kMinGroupMaxFp8 : kMinGroupMax);
   const float qmax = vmode == kValFp8 ? kFp8Max : 127.f;
   const float inv = live ? __fdiv_rn(qmax, a) : 0.f;
   if (vmode != kValInt8) {
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
       const int r = rl + e * RL;
-      if (row0 + r < N) {
-        float v[8];
+      const bool valid = row0 + r < N;
+      float v[8];
+      if (valid) {
         load(raw[e], v);
 #pragma unroll
         for (int q = 0; q < 8; ++q) v[q] = __fmul_rn(v[q], inv);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.f;
+      }
+      if (valid) {
         const uint4 out =
             vmode == kValBf16
                 ? make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]))
                 : make_uint4(e4m3x2_bf16x2(v[0], v[1]), e4m3x2_bf16x2(v[2], v[3]), e4m3x2_bf16x2(v[4], v[5]),
                              e4m3x2_bf16x2(v[6], v[7]));
         *reinterpret_cast<uint4*>(xq + base + (size_t)r * D + c8 * 8) = out;
+      }
+      if (vmode == kValFp8 && (x8 != nullptr || x8t != nullptr)) {
+        const uint32_t b01 = e4m3x2_bytes(v[0], v[1]), b23 = e4m3x2_bytes(v[2], v[3]);
+        const uint32_t b45 = e4m3x2_bytes(v[4], v[5]), b67 = e4m3x2_bytes(v[6], v[7]);
+        if (x8 != nullptr && valid)
+          *reinterpret_cast<uint2*>(x8 + base + (size_t)r * D + c8 * 8) =
+              make_uint2(b01 | (b23 << 16), b45 | (b67 << 16));
+        if (x8t != nullptr) {
+          const uint32_t b[4] = {b01, b23, b45, b67};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) t8[(c8 * 8 + q) * kBlk + r] = (uint8_t)(b[q >> 1] >> (8 * (q & 1)));
+        }
+      }
+    }
+    if (vmode == kValFp8 && x8t != nullptr) {
+      // the transposed tile [D][128 tokens] as 16-byte rows pieces (rows past N were written as zero)
+      __syncthreads();
+      for (int i = threadIdx.x; i < D * (kBlk / 16); i += kThreads) {
+        const int c = i / (kBlk / 16), v16 = i % (kBlk / 16);
+        *reinterpret_cast<uint4*>(x8t + ((size_t)bh * D + c) * ((size_t)nb * kBlk) + row0 + v16 * 16) =
+            *reinterpret_cast<const uint4*>(t8 + c * kBlk + v16 * 16);
       }
     }
   } else if (gred != nullptr) {
@@ -276,8 +306,41 @@ __device__ void quantize_block(const __nv_bfloat16* __restrict__ x, __nv_bfloat1
   if (threadIdx.x == 0) scale[(size_t)bh * nb + blk] = live ? __fdiv_rn(a, qmax) : 0.f;
 }
 
+// The exact FP64 channel sums of one 128-token block of one head (rows past N add nothing):
+// part[bh][blk][D], four rows per lane at a time (exact_row_sums), then across the row lanes.
+template <int D>
+__device__ void block_channel_sums(const __nv_bfloat16* __restrict__ k, double* __restrict__ part, int bh, int blk,
+                                   int N, int nb, double* red) {
+  constexpr int V8 = D / 8, RL = kThreads / V8, RPL = kBlk / RL, G = 4;
+  const int c8 = threadIdx.x % V8, rl = threadIdx.x / V8;
+  double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int g = 0; g < RPL; g += G) {
+    uint4 u[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const int r = blk * kBlk + rl + (g + i) * RL;
+      u[i] = r < N ? *reinterpret_cast<const uint4*>(k + ((size_t)bh * N + r) * D + c8 * 8)
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+    double s[8];
+    exact_row_sums<G>(u, s);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += s[e];
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[rl * D + c8 * 8 + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    double t = 0;
+#pragma unroll
+    for (int q = 0; q < RL; ++q) t += red[q * D + threadIdx.x];
+    part[((size_t)bh * nb + blk) * D + threadIdx.x] = t;
+  }
+}
+
 template <int D, bool BM>
-__global__ void __launch_bounds__(kThreads, BM ? 2 : 4) quantize_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kThreads, BM ? 2 : 3) quantize_kernel(const QuantParams p) {
   __shared__ float red[kThreads / 32];
   __shared__ float fac[D];
   __shared__ float gred[kThreads / 32 * (D / 8)];
@@ -287,6 +350,11 @@ __global__ void __launch_bounds__(kThreads, BM ? 2 : 4) quantize_kernel(const Qu
   const int local = blockIdx.x - p.block_start[j];
   const QuantJob& job = p.job[j];
   const int bh = local / p.nb;
+  if (job.part != nullptr) {  // the K-mean pass's block sums, beside the other operands' codes
+    __shared__ double sred[(kThreads / (D / 8)) * D];
+    block_channel_sums<D>(job.x, job.part, bh, local % p.nb, p.N, p.nb, sred);
+    return;
+  }
   const float* mean = job.mean != nullptr ? job.mean + (size_t)bh * D : nullptr;  // this head's channel means
   if (job.bexp != nullptr) {
     if (threadIdx.x < D) fac[threadIdx.x] = exp2_int(job.bexp_sign * job.bexp[(bh / job.bexp_group) * D + threadIdx.x]);
@@ -301,6 +369,12 @@ __global__ void __launch_bounds__(kThreads, BM ? 2 : 4) quantize_kernel(const Qu
                               smean, job.vmode);
       return;
     }
+  }
+  if (job.vmode == kValFp8) {
+    __shared__ __align__(16) uint8_t t8[D * kBlk];  // transposed E4M3 tile
+    quantize_block<D>(job.x, job.xq, job.scale, mean, bh, local % p.nb, p.N, p.nb, red, nullptr, nullptr, nullptr,
+                      nullptr, nullptr, kValFp8, job.x8, job.x8t, t8);
+    return;
   }
   quantize_block<D>(job.x, job.xq, job.scale, mean, bh, local % p.nb, p.N, p.nb, red,
                     job.bexp != nullptr ? fac : nullptr, job.subexp ? gred : nullptr, nullptr, nullptr, nullptr,
@@ -682,6 +756,11 @@ cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s) {
   else
     bm ? quantize_kernel<128, true><<<blocks, kThreads, 0, s>>>(p)
        : quantize_kernel<128, false><<<blocks, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kmean_final(const double* part, float* mean, int BH, int N, int d, cudaStream_t s) {
+  kmean_final_kernel<<<dim3(BH, d / 32), kFinalSlices * 32, 0, s>>>(part, mean, N, nblocks(N), d);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,8 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 // below 2^-120 quantizes to zero codes with scale 0, so that 127/max never
 // overflows FP32.
 constexpr float kMinGroupMax = 7.52316384526264e-37f;  // 2^-120
+// The same rule for the FP8 variant, whose 448/max overflows FP32 already below ~2^-119.2.
+constexpr float kMinGroupMaxFp8 = 3.00926553810506e-36f;  // 2^-118
 
 // Status word codes written by kernels (low byte = sagebwd_status, bits 8..15 = wait site).
 __host__ __device__ constexpr int status_timeout(int site) { return (int)SAGEBWD_ERR_TIMEOUT | (site << 8); }
@@ -45,6 +47,11 @@ struct QuantJob {
   float* bmean;            // [BH][nb][d] or nullptr: Q-smoothing, each block's channel means subtracted
                            // first (and written here)
   int vmode;               // ValueMode: INT8 code (0), BF16 of x * 127/max (1), E4M3 of x * 448/max (2)
+  // FP8 variant only (else nullptr): the same E4M3 values as bytes, for the FP8 tensor cores
+  uint8_t* x8;             // [BH][N][d]
+  uint8_t* x8t;            // [BH][d][128 nb]: each head's values transposed (tokens contiguous), zero past N
+  double* part;            // non-null: this job only writes the FP64 channel sums of each block [BH][nb][d]
+                           // (the K-mean pass), no codes
 };
 struct QuantParams {
   QuantJob job[3];
@@ -57,6 +64,8 @@ struct QuantParams {
 cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s);
 cudaError_t launch_kmean(const __nv_bfloat16* k, double* part, float* mean, int BH, int N, int d, int* status,
                          int clear_status, cudaStream_t s);
+// The second half of the K-mean pass alone: mean[bh][c] = (sum of the block sums) / N.
+cudaError_t launch_kmean_final(const double* part, float* mean, int BH, int N, int d, cudaStream_t s);
 // Channel statistics of Q and K for the channel balancing: per (b, kv head,
 // channel) the K mean (smooth) and the balancing exponent.
 struct StatsParams {
@@ -130,9 +139,11 @@ struct FwdParams {
 struct FwdDumpParams : FwdParams {
   uint8_t* dump;
 };
-// dump == nullptr selects the plain (or Q-smoothing) instantiations.
+// dump == nullptr selects the plain (or Q-smoothing) instantiations.  f8: the FP8 variant on the
+// FP8 tensor cores (tq, tk over the E4M3 bytes of Q^, K^ [BH][N][d], tv over V^ transposed
+// [BHk][d][128 nb]; p.flags must carry kFlagFp8Codes).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdDumpParams& p,
-                       int d, int causal, cudaStream_t s);
+                       int d, int causal, int f8, cudaStream_t s);
 
 // Kept at 128 bytes: a larger parameter block made ptxas spill in the d = 64 kernels.
 struct BwdParams {

@@ -155,7 +155,9 @@ typedef struct {
  * smooth_q, the FP32 block means of Q [B*Hq][ceil(N/128)][d] and the FP32
  * logit terms mean_Q . K' [B*Hq][ceil(N/128)][128 * ceil(N/128)] (in base-2
  * units, times scale * log2 e), each section starting on a 256-byte
- * boundary.  Returns 0 for an invalid problem. */
+ * boundary, and with fp8 the same E4M3 values as bytes for the FP8 tensor cores: Q [B*Hq][N][d],
+ * K [B*Hkv][N][d] and V transposed per head [B*Hkv][d][128 * ceil(N/128)] (zero past N).  Returns 0
+ * for an invalid problem. */
 size_t sagebwd_saved_bytes(const sagebwd_problem* prob);
 
 /* Bytes of workspace for pass 0 (forward, sagebwd_fwd / sagebwd_quantize) or

@@ -100,9 +100,6 @@ typedef struct {
 namespace {
 
 constexpr int BLK = 128;  // tokens per quantization block and per tile
-// A quantization group (block, P^T row, dS tile) whose largest magnitude is
-// below this quantizes to all-zero codes with scale 0: 127/a stays finite in FP32.
-const double kMinGroupMax = std::ldexp(1.0, -120);
 constexpr double kLog2e = 1.4426950408889634073599246810019;
 constexpr double kLn2 = 0.69314718055994530941723212145818;
 const double kInf = std::numeric_limits<double>::infinity();
@@ -154,6 +151,10 @@ struct Mode {
   uint32_t bf16 = 0;      // bit set: that quantizer rounds to BF16 instead of to an INT8 code
   bool fp8 = false;       // the FP8 ablation: E4M3 values instead of INT8 codes
   double qmax = 127.0;    // largest code: 127 (INT8) or 448 (E4M3)
+  // A quantization group (block, P^T row, dS tile) whose largest magnitude is below this gets
+  // all-zero codes and scale 0, so that qmax/max stays finite in FP32: 2^-120 for INT8 codes,
+  // 2^-118 for E4M3 values (448/max overflows below ~2^-119.2)
+  double min_group() const { return fp8 ? std::ldexp(1.0, -118) : std::ldexp(1.0, -120); }
   double F(double x) const { return fp32 ? (double)(float)x : x; }
   double Q(int which, double x) const {
     if (exact & (1u << which)) return x;
@@ -223,7 +224,7 @@ void quant_block(const Mode& M, int which, const double* x, int count, double* c
                  bool subexp = false) {
   double a = 0;
   for (int e = 0; e < count; ++e) a = std::max(a, std::fabs(x[e]));
-  if (a < kMinGroupMax) {
+  if (a < M.min_group()) {
     for (int e = 0; e < count; ++e) codes[e] = 0;
     *scale = 0;
     return;
@@ -562,7 +563,7 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
   for (int c = 0; c < T.nk; ++c) {
     double cmax = 0;
     for (int a = 0; a < T.ni; ++a) cmax = std::max(cmax, P[(size_t)a * BLK + c]);
-    if (cmax < kMinGroupMax) continue;
+    if (cmax < M.min_group()) continue;
     const double inv = M.F(M.qmax / cmax);
     T.spc[c] = M.F(cmax / M.qmax);
     for (int a = 0; a < T.ni; ++a) T.pt[(size_t)c * BLK + a] = M.Q(QZ_PB, M.F(P[(size_t)a * BLK + c] * inv));
@@ -574,7 +575,7 @@ void bwd_tile(const Mode& M, const oracle_problem* p, const QTensor& qq, const Q
   for (int a = 0; a < T.ni; ++a)
     for (int c = 0; c < T.nk; ++c) amax = std::max(amax, std::fabs(dS[(size_t)a * BLK + c]));
   T.sds = 0;
-  if (amax >= kMinGroupMax) {
+  if (amax >= M.min_group()) {
     const double inv = M.F(M.qmax / amax);
     T.sds = M.F(amax / M.qmax);
     for (int a = 0; a < T.ni; ++a)

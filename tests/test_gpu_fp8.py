@@ -44,6 +44,17 @@ def check_values(oracle_mod, w, x, fwd):
         m, _ = np.frexp(a)  # E4M3 values (normal or subnormal) have at most 4 significant bits
         assert np.all((m * 16) == np.round(m * 16)), name
     np.testing.assert_array_equal(views["mu"].cpu().numpy().view(np.uint32), ref["mu"].view(np.uint32))
+    # the E4M3 bytes the FP8 tensor cores read: the same values (Q, K row-major, V transposed per head,
+    # zero past N)
+    e4m3 = torch.float8_e4m3fn
+    for name in ("q", "k"):
+        b = views[name + "8"].cpu().view(e4m3).float().numpy()
+        np.testing.assert_array_equal(b.reshape(-1), views[name].float().cpu().numpy().reshape(-1), err_msg=name)
+    nb = (w.N + 127) // 128
+    vt = views["v8t"].cpu().view(e4m3).float().numpy()  # [BHk][d][128 nb]
+    v = views["v"].float().cpu().numpy().reshape(w.B * w.Hkv, w.N, w.d)
+    np.testing.assert_array_equal(vt[:, :, :w.N], v.transpose(0, 2, 1))
+    assert not vt[:, :, w.N:].any()
 
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
@@ -67,6 +78,8 @@ def test_fp8_full_size_sampled(oracle_mod, name):
     fwd = gpu_forward(w, xd, fp8=True)
     bwd = gpu_backward(w, xd, fwd)
     assert fwd["status"] == 0 and bwd["status"] == 0
+    for key, t in (("o", fwd["o"]), ("lse", fwd["lse"]), ("dq", bwd["dq"]), ("dk", bwd["dk"]), ("dv", bwd["dv"])):
+        assert bool(torch.isfinite(t).all()), key  # every element, not only the sampled blocks
     check_values(oracle_mod, w, x, fwd)
     nb = (w.N + 127) // 128
     op = oracle_problem(oracle_mod, w, fp8=True)
