@@ -491,31 +491,39 @@ def time_layer_stack(n_tokens: int, steps: int, warmup: int, dev):
 
 
 # ---------------------------------------------------------------------------- the oracle (CPU) arm
-def oracle_sample_run(w: W.Workload, n_tokens: int):
+def oracle_sample_run(w: W.Workload, n_tokens: int, opts: dict):
     """Time the oracle on the first n_tokens tokens of the workload's own inputs (all heads, full
-    forward + backward of that prefix).  Returns (seconds, algorithmic ops of the sample)."""
+    forward + backward of that prefix), with the library arm's quantizer settings (opts).
+    Returns (seconds, algorithmic ops of the sample, threads)."""
     import oracle  # the CPU baseline leg is the one place bench.py runs the oracle
     x = W.make_inputs(w)
     sub = {k: v[:, :, :n_tokens].contiguous() for k, v in x.items()}
     ws = w.with_(N=n_tokens)
-    op = oracle.problem(ws.B, ws.Hq, ws.Hkv, ws.N, ws.d, ws.causal)
+    op = oracle.problem(ws.B, ws.Hq, ws.Hkv, ws.N, ws.d, ws.causal, **opts)
     t0 = time.perf_counter()
     oracle.pipeline(op, sub["q"], sub["k"], sub["v"], sub["do"])
     dt = time.perf_counter() - t0
     return dt, ws.flops_fwd() + ws.flops_bwd(), oracle.max_threads()
 
 
-def pick_sample_tokens(w: W.Workload, budget_s: float):
+def oracle_opts(args) -> dict:
+    """The oracle's settings for the quantizer configuration the library arm times."""
+    fp8 = bool(getattr(args, "fp8", False))
+    return {"qk_subexp": not (args.qk_plain or fp8), "ds_subexp": bool(args.ds_subexp),
+            "balance_qk": bool(args.balance_qk), "smooth_q": bool(args.smooth_q), "fp8": fp8}
+
+
+def pick_sample_tokens(w: W.Workload, budget_s: float, opts: dict):
     """Largest multiple of 128 tokens whose oracle run should take about budget_s seconds (quadratic cost)."""
     n = min(256, w.N)
-    dt, _, _ = oracle_sample_run(w, n)
+    dt, _, _ = oracle_sample_run(w, n, opts)
     target = int(n * (budget_s / max(dt, 1e-3)) ** 0.5)
     return max(128, min(w.N, target // 128 * 128))
 
 
-def cpu_baseline(w: W.Workload, budget_s: float):
-    n = pick_sample_tokens(w, budget_s)
-    dt, ops, cores = oracle_sample_run(w, n)
+def cpu_baseline(w: W.Workload, budget_s: float, opts: dict):
+    n = pick_sample_tokens(w, budget_s, opts)
+    dt, ops, cores = oracle_sample_run(w, n, opts)
     return {"value": round(ops / dt / 1e12, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
             "sample": f"first {n} of {w.N} tokens of the same inputs, all {w.B}x{w.Hq} heads, full forward + "
                       f"backward of that prefix ({ops:.3e} ops in {dt:.2f} s)"}
@@ -528,12 +536,13 @@ def run_reference(args, w):
     # each step a bounded sample: at most reference_step_s seconds, and the whole warm-up +
     # timed run within reference_total_s
     step_s = min(args.reference_step_s, args.reference_total_s / max(1, args.steps + args.warmup))
-    n = pick_sample_tokens(w, step_s)
+    opts = oracle_opts(args)
+    n = pick_sample_tokens(w, step_s, opts)
     for _ in range(args.warmup):
-        oracle_sample_run(w, n)
+        oracle_sample_run(w, n, opts)
     times, ops, cores = [], 0.0, 1
     for _ in range(args.steps):
-        dt, ops, cores = oracle_sample_run(w, n)
+        dt, ops, cores = oracle_sample_run(w, n, opts)
         times.append(dt)
     mean = sum(times) / len(times)
     value = ops / mean / 1e12
@@ -714,7 +723,7 @@ def main():
     # the CPU baseline first (before any GPU work), rank 0 at N = 1 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_budget_s)
+        cpu = cpu_baseline(w, args.cpu_budget_s, oracle_opts(args))
 
     sb.load_library()
     step = Step(w, dev, balance_qk=args.balance_qk, ds_subexp=args.ds_subexp,

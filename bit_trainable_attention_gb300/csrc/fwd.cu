@@ -13,11 +13,14 @@
 //                    registers to the softmax warpgroups: 384 threads launch with
 //                    168 registers each; 128 * LOW + 256 * HIGH <= 384 * 168)
 // TMEM: tile t owns S_t [256t, 256t+128) and O_t [256t+128, 256t+128+d).  The
-// quantized P~ codes are written over S_t (packed BF16, columns [256t, 256t+64))
-// and feed O_t = P^_t V^_j as the A operand straight from TMEM.
-// MMA order: S_0(0), S_1(0), then per key tile j: P^_0 V^_j, S_0(j+1), P^_1 V^_j,
-// S_1(j+1).  S_t(j+1) waits until P^_t V^_j has consumed the codes that share its
-// columns; the softmax of one tile runs while the tensor core serves the other.
+// quantized P~ codes (packed BF16, 64 columns) feed O_t = P^_t V^_j as the A operand
+// straight from TMEM.  d = 128: they are written over S_t (columns [256t, 256t+64)),
+// and the MMA order is S_0(0), S_1(0), then per key tile j: P^_0 V^_j, S_0(j+1),
+// P^_1 V^_j, S_1(j+1), S_t(j+1) waiting until P^_t V^_j has consumed the codes that
+// share its columns.  d = 64: they have their own columns [256t+192, 256t+256), so
+// S_t(j+1) is issued as soon as the softmax has read S_t(j), before P^_t V^_j, and the
+// softmax folds P^_t V^_j in after its first pass over S_t(j+1).  Either way the
+// softmax of one tile runs while the tensor core serves the other.
 //
 // Softmax of tile j for one row (FP32, base-2 logits t = S_int * sQ sK scale log2e):
 //   tmax  = max_k t_k over the visible keys of the row in the tile
@@ -65,6 +68,10 @@ struct FwdCfg {
   static_assert(SMEM <= 232448, "shared memory beyond the per-CTA limit");
   __host__ __device__ static constexpr int col_s(int t) { return 256 * t; }
   __host__ __device__ static constexpr int col_o(int t) { return 256 * t + 128; }
+  // D = 64 leaves 64 columns per tile free after S_t and O_t: the codes of P~ get their own
+  // columns there, so S_t(j+1) need not wait for P^_t V^_j (SEPC); D = 128 writes them over S_t.
+  static constexpr bool SEPC = D == 64;
+  __host__ __device__ static constexpr int col_c(int t) { return SEPC ? 256 * t + 192 : 256 * t; }
 };
 
 enum FwdSite { kSiteQ = 1, kSiteKFull, kSiteKEmpty, kSiteVFull, kSiteVEmpty, kSiteSFull, kSitePFull, kSitePVDone,
@@ -256,7 +263,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         umma_commit(bar_k_empty);
       }
       // Per key tile j: P^_0 V^_j, S_0(j+1), P^_1 V^_j, S_1(j+1), so that the tensor
-      // core works on one tile while the softmax warpgroup of the other runs.
+      // core works on one tile while the softmax warpgroup of the other runs.  With separate
+      // code columns (D = 64) S_t(j+1) goes first, as soon as the softmax has read S_t(j).
       for (int j = 0; ok && j < nkb_max; ++j) {
         const int s = j % NS, s1 = (j + 1) % NS;
         if (!wait1(wc, bar_v_full + s, (j / NS) & 1, kSiteVFull)) break;
@@ -267,8 +275,20 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (j < nkb[t]) {
-            if (!wait1(wc, bar_p_full + t, j & 1, kSitePFull) ||
-                (j >= 1 && !wait1(wc, bar_o_empty + t, (j - 1) & 1, kSiteOEmpty))) {
+            if (!wait1(wc, bar_p_full + t, j & 1, kSitePFull)) {
+              ok = false;
+              break;
+            }
+            if (C::SEPC && j + 1 < nkb[t]) {
+              if (!k_ready && !wait1(wc, bar_k_full + s1, ((j + 1) / NS) & 1, kSiteKFull)) {
+                ok = false;
+                break;
+              }
+              k_ready = true;
+              tc_fence_after();
+              issue_s(t, kdesc);  // S_t(j) has been read: its columns are free
+            }
+            if (j >= 1 && !wait1(wc, bar_o_empty + t, (j - 1) & 1, kSiteOEmpty)) {
               ok = false;
               break;
             }
@@ -278,19 +298,19 @@ __global__ void __launch_bounds__(kFThreads, 1)
               // 32), B = the transposed V^_j [d][key], K-major (32 bytes per K step)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_f8_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+                umma_f8_ts(tmem + C::col_o(t), tmem + C::col_c(t) + kk * 8,
                            sdesc_kmajor(vaddr + kk * 32, 1024, kSwizzle128B), idO, kk > 0);
             } else {
               // O_t = P^_t V^_j: A = the codes in TMEM (128 keys = 64 packed columns, 8 per
               // K step), B = V^_j [key][d] read MN-major
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_from_lo(vdesc + kk * 128), idO,
+                umma_ts(tmem + C::col_o(t), tmem + C::col_c(t) + kk * 8, sdesc_from_lo(vdesc + kk * 128), idO,
                         kk > 0);
             }
             umma_commit(bar_pv_done + t);
           }
-          if (j + 1 < nkb[t]) {
+          if (!C::SEPC && j + 1 < nkb[t]) {
             if (!k_ready && !wait1(wc, bar_k_full + s1, ((j + 1) / NS) & 1, kSiteKFull)) {
               ok = false;
               break;
@@ -324,6 +344,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + C::col_s(t);
     const uint32_t o_addr = tmem + lane_base + C::col_o(t);
+    const uint32_t c_addr = tmem + lane_base + C::col_c(t);  // the codes of P~
     const float sQv = nk > 0 ? p.sq[(size_t)bhq * p.nb + qb] : 0.f;
     // The running output and sum are kept relative to a reference maximum m_ref that
     // only moves when a tile's maximum exceeds it by more than 2^8; the result is the
@@ -371,8 +392,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     };
 
     for (int j = 0; j < nk; ++j) {
-      // the previous tile's product lands while S_t(j) is computed
-      if (j >= 1 && !fold(j - 1, pend_a, pend_w)) {
+      // the previous tile's product lands while S_t(j) is computed (with separate code columns it
+      // is folded after pass 1, since S_t(j) was issued before P^_t V^_(j-1))
+      if (!C::SEPC && j >= 1 && !fold(j - 1, pend_a, pend_w)) {
         ok = false;
         break;
       }
@@ -468,6 +490,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
         m_ref = tmax;
       }
       const float rj = ex2_approx(tmax - m_ref);
+      // separate code columns: fold tile j-1's product now (it ran behind S_t(j)), before pass 2
+      // writes this tile's codes over the columns it read
+      if (C::SEPC && j >= 1 && !fold(j - 1, pend_a, pend_w)) {
+        ok = false;
+        break;
+      }
       constexpr float kQLog2 = VAR == kValFp8 ? kLog2_448 : kLog2_127, kQInv = VAR == kValFp8 ? 1.f / kFp8Max : 1.f / 127.f;
       const float bias = kQLog2 - tmax;
       // pass 2: codes of P~ written over the S columns already read (chunk c of 32 keys
@@ -510,9 +538,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
         if constexpr (DBG) fdump16(dump_rec(j) + FwdDump<D>::PC + ((size_t)r * 128 + c0) * 2, pk);
         if constexpr (F8)
-          tmem_st8(s_addr + (c0 >> 2), pb);
+          tmem_st8(c_addr + (c0 >> 2), pb);
         else
-          tmem_st16(s_addr + (c0 >> 1), pk);
+          tmem_st16(c_addr + (c0 >> 1), pk);
       }
       tmem_st_wait();
       tc_fence_before();
