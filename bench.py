@@ -585,9 +585,11 @@ def quantize_bandwidth(step: "Step", flush: torch.Tensor, hbm_gbs: float, reps: 
     Algorithmic bytes: every input element read once per pass that must read it (K twice with
     K-smoothing: its channel sums, then its codes), every output written once; the quantized values
     are 2-byte integer-valued BF16 (the tensor cores' operand form).
-      stage      sagebwd_fwd_quantize (K chunk sums beside Q's codes, then K's and V's codes)
-      quantize_q sagebwd_quantize(Q): one quantize_kernel launch on Q alone
-      quantize_v sagebwd_quantize(V): one quantize_kernel launch on V alone
+      stage      sagebwd_fwd_quantize: K's block sums, their channel means, then one persistent launch
+                 of Q's, V's and K's codes (the last two launched as programmatic dependents: the Q
+                 and V blocks run beside the K-mean pass, the K blocks wait for the means)
+      quantize_q sagebwd_quantize(Q): one persistent quantizer launch on Q alone
+      quantize_v sagebwd_quantize(V): one persistent quantizer launch on V alone
       k_path     sagebwd_quantize(K): the single-operand K path (K mean pair, then K's codes)"""
     w, p, x = step.w, step.prob, step.x
     nb = (w.N + 127) // 128

@@ -269,7 +269,7 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
   qp.d = p->d;
   qp.nb = nb;
   qp.status = status;
-  auto launch_jobs = [&](std::initializer_list<QuantJob> jobs, int clear) -> sagebwd_status {
+  auto launch_jobs = [&](std::initializer_list<QuantJob> jobs, int clear, bool pdl = false) -> sagebwd_status {
     QuantParams lp = qp;
     lp.njobs = 0;
     lp.block_start[0] = 0;
@@ -279,19 +279,21 @@ sagebwd_status fwd_quantize_impl(const sagebwd_problem* p, const void* q, const 
       ++lp.njobs;
     }
     lp.clear_status = clear;
-    return cuda_status(launch_quantize(lp, st));
+    return cuda_status(launch_quantize(lp, st, pdl));
   };
   if (p->smooth_k && !p->balance_qk) {
-    // K-smoothing: K's block sums ride in the launch that quantizes Q and V, the channel means follow
-    // (a small kernel), then K's codes
+    // K-smoothing: K's block sums, then the channel means (a small kernel), then one launch of the
+    // Q, V and K codes.  The last two are programmatic dependents of the launch before them: the Q
+    // and V blocks run while the sums and means are computed, and only the K blocks (last in the
+    // grid) wait for the means.
     QuantJob jsum{};
     jsum.x = static_cast<const __nv_bfloat16*>(k);
     jsum.BH = p->B * p->Hkv;
     jsum.part = at<double>(ws, W.kpart);
-    SB_CHECK(launch_jobs({jsum, qp.job[0], qp.job[2]}, 1));
+    SB_CHECK(launch_jobs({jsum}, 1));
     SB_CHECK(cuda_status(launch_kmean_final(at<double>(ws, W.kpart), at<float>(saved, S.mu), p->B * p->Hkv, p->N,
-                                            p->d, st)));
-    SB_CHECK(launch_jobs({qp.job[1]}, 0));
+                                            p->d, st, true)));
+    SB_CHECK(launch_jobs({qp.job[0], qp.job[2], qp.job[1]}, 0, true));
   } else {
     SB_CHECK(launch_jobs({qp.job[0], qp.job[1], qp.job[2]}, p->balance_qk ? 0 : 1));
   }

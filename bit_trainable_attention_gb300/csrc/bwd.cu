@@ -93,13 +93,18 @@ struct BwdCfg {
   static constexpr int OFF_DST = OFF_DOQ + NS * TILE;
   static constexpr int OFF_STG = OFF_DST + CTILE;  // own staging tile (d = 64 only)
   static constexpr int OFF_VEC = OFF_STG + (ALIAS ? 0 : 128 * D * 4);
+  // Softmax passes per tile.  SPLIT (d = 128): P from S^T alone, then dS once dP^T is there (its
+  // MMA runs behind the first pass); the row maxima of P are combined by an atomic maximum on the bit
+  // patterns (P >= 0 orders like its unsigned bits) in one slot per row.  Otherwise (d = 64) P and dS
+  // in one pass after both products, each slice's row maxima in a slot of its own.
+  static constexpr bool SPLIT = D == 128;
+  static_assert(SPLIT || SWG > 2, "the fused pass exchanges the row maxima of P among more than two slices");
+  static constexpr int PM_FLOATS = SPLIT ? 128 : 128 * SWG;
   // -LSE log2 e [128], -D [128], P^T scale x sdO per row [2][128], dS scale [2], |dS| maxima
-  // [S_WARPS], row maxima of P exchanged between the softmax warpgroups [128] (two warpgroups) or
-  // [SWG][128] (four)
-  static constexpr int PM_FLOATS = SWG == 2 ? 128 : 128 * SWG;
+  // [S_WARPS], row maxima of P [PM_FLOATS]
   static constexpr int VEC_FLOATS = 128 + 128 + 256 + 2 + S_WARPS + PM_FLOATS;
   static constexpr int OFF_BAR = OFF_VEC + ((VEC_FLOATS * 4 + 15) / 16) * 16;
-  static constexpr int NBAR = 1 + 4 + 4 * NS + 18;
+  static constexpr int NBAR = 1 + 4 + 4 * NS + 19;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
   // The tiles need a 1024-byte aligned base; the d = 128 layout leaves no room for padding.
   static constexpr int SMEM = BYTES + 1024 <= 232448 ? BYTES + 1024 : BYTES;
@@ -114,8 +119,8 @@ struct BwdCfg {
 };
 
 enum BwdSite { bSiteKV = 16, bSiteQFull, bSiteQEmpty, bSiteDOFull, bSiteDOEmpty, bSiteDOQFull, bSiteDOQEmpty,
-               bSiteSDP, bSitePTReady, bSiteDSReady, bSiteAccV, bSiteAccQ, bSiteAccK, bSiteTmemFreeV, bSiteDVQFree,
-               bSiteTmemFreeK, bSiteStaged, bSiteStgFree, bSiteC1, bSiteC2, bSiteC3, bSiteAlign };
+               bSiteS, bSitePTReady, bSiteDSReady, bSiteAccV, bSiteAccQ, bSiteAccK, bSiteTmemFreeV, bSiteDVQFree,
+               bSiteTmemFreeK, bSiteStaged, bSiteStgFree, bSiteC1, bSiteC2, bSiteC3, bSiteAlign, bSiteDP };
 
 // The plain instantiations take BwdParams (128 bytes), the Q-smoothing ones BwdQsmParams, the
 // debug-dump one (DBG) BwdDumpParams.
@@ -139,6 +144,10 @@ struct BwdDump {
   static constexpr size_t PT = 0, DS = 128 * 128 * 2, DV = 2 * 128 * 128 * 2, DK = DV + 128 * D * 4,
                           DQ = DK + 128 * D * 4, BYTES = DQ + 128 * D * 4;
 };
+// Write 4 consecutive 32-bit words (16 bytes, 16-byte aligned) to global memory.
+__device__ __forceinline__ void dump4(uint8_t* dst, const uint32_t* w) {
+  *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
 // Write 16 consecutive 32-bit words (64 bytes, 16-byte aligned) to global memory.
 __device__ __forceinline__ void dump16(uint8_t* dst, const uint32_t* w) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -167,9 +176,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   float* L2v = reinterpret_cast<float*>(smem + C::OFF_VEC);  // -LSE_q log2 e of the tile's queries
   float* Dv = L2v + 128;                                      // -D_q
   float* fv_ring = Dv + 128;                                  // [2][128] sP_row * sdO per tile parity
-  float* sds_ring = fv_ring + 256;                            // [2] dS scale per tile parity
-  float* am = sds_ring + 2;                                   // [S_WARPS] per-warp maxima of |dS|
-  float* pm = am + C::S_WARPS;                                // row maxima of P (exchange)
+  float* sds_ring = fv_ring + 256;                              // [2] dS scale per tile parity
+  float* am = sds_ring + 2;                                     // [S_WARPS] per-warp maxima of |dS|
+  uint32_t* pm = reinterpret_cast<uint32_t*>(am + C::S_WARPS);  // row maxima of P (bits; PM_FLOATS)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* bar_kv = bars;
   uint64_t* bar_q_full = bar_kv + 1;              // [2]
@@ -178,10 +187,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar_do_empty = bar_do_full + NS;      // [NS]
   uint64_t* bar_doq_full = bar_do_empty + NS;     // [NS]
   uint64_t* bar_doq_empty = bar_doq_full + NS;    // [NS] (own staging only)
-  uint64_t* bar_sdp = bar_doq_empty + NS;         // S^T and dP^T of the tile in TMEM
-  uint64_t* bar_pt_ready = bar_sdp + 1;           // P^T codes in TMEM, tile scales stored (S)
-  uint64_t* bar_ds_ready = bar_pt_ready + 1;      // dS codes in shared memory, dS read (S)
-  uint64_t* bar_acc_v = bar_ds_ready + 1;         // dV tile in TMEM
+  uint64_t* bar_s = bar_doq_empty + NS;           // S^T of the tile in TMEM
+  uint64_t* bar_dp = bar_s + 1;                   // dP^T of the tile in TMEM
+  uint64_t* bar_pt_ready = bar_dp + 1;            // P^T codes in TMEM, P read, row scales stored (S)
+  // [2] by tile parity (phase = tile / 2): dS codes in shared memory, dS read, dS scale stored
+  // (S).  Two, so that no waiter can miss a phase: the one after next needs every role's work
+  // on the tile after this one.
+  uint64_t* bar_ds_ready = bar_pt_ready + 1;
+  uint64_t* bar_acc_v = bar_ds_ready + 2;         // dV tile in TMEM
   uint64_t* bar_acc_q = bar_acc_v + 1;            // dQ tile in TMEM
   uint64_t* bar_acc_k = bar_acc_q + 1;            // dK tile in TMEM (dS codes no longer read)
   uint64_t* bar_tmem_free_v = bar_acc_k + 1;      // dV tile read (A; gates the aliased dQ)
@@ -190,8 +203,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar_staged = bar_tmem_free_k + 1;     // [2] staging half h written (A warpgroup h)
   uint64_t* bar_stg_free = bar_staged + 2;        // [2] staging half h read by the reduce (reducer)
   uint64_t* bar_c1 = bar_stg_free + 2;            // S: the tile's -LSE / -D vectors stored
-  uint64_t* bar_c2 = bar_c1 + 1;                  // S: |dS| maxima and half-row maxima of P stored
-  uint64_t* bar_c3 = bar_c2 + 1;                  // S: row maxima of P combined
+  uint64_t* bar_c2 = bar_c1 + 1;                  // S: row maxima of P combined
+  uint64_t* bar_c3 = bar_c2 + 1;                  // S: |dS| maxima stored
   uint64_t* bar_final = bar_c3 + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_final + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -232,9 +245,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_init(bar_doq_full + s, 1);
       mbar_init(bar_doq_empty + s, 1);
     }
-    mbar_init(bar_sdp, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
     mbar_init(bar_pt_ready, 128 * C::SWG);
     mbar_init(bar_ds_ready, 128 * C::SWG);
+    mbar_init(bar_ds_ready + 1, 128 * C::SWG);
     mbar_init(bar_acc_v, 1);
     mbar_init(bar_acc_q, 1);
     mbar_init(bar_acc_k, 1);
@@ -243,11 +258,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar_tmem_free_k, 256);
     mbar_init(bar_c1, 128 * C::SWG);
     mbar_init(bar_c2, 128 * C::SWG);
-    mbar_init(bar_c3, 128);
+    mbar_init(bar_c3, 128 * C::SWG);
     mbar_init(bar_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (tid < 128) pm[tid] = 0u;
   constexpr int W_LOAD = C::C_WARP0, W_MMA = C::C_WARP0 + 1, W_RED = C::C_WARP0 + 2, W_LOAD2 = C::C_WARP0 + 3;
   if (warp == W_MMA) {
     tmem_alloc(tmem_slot, 512);
@@ -339,8 +355,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (ok) {
         tc_fence_after();
         chain_kk(C::C_S, dK_k, dQ_k(0), idSS);
+        if (C::SPLIT) umma_commit(bar_s);  // (d = 64 waits for S^T and dP^T together: bar_dp)
         chain_kk(C::C_DP, dV_k, dDO_k(0), idSS);
-        umma_commit(bar_sdp);
+        umma_commit(bar_dp);
         umma_commit(bar_do_empty);
       }
       for (int it = 0; ok && it < T; ++it) {
@@ -369,14 +386,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         umma_commit(bar_acc_v);
         umma_commit(bar_doq_empty + s);
+        if (C::SPLIT && next) umma_commit(bar_s);  // S^T(i+1), issued before dV(i)
         // dP^T of the next tile once dS is coded (its columns are free)
-        if (!wait1(wc, bar_ds_ready, it & 1, bSiteDSReady)) break;
+        if (!wait1(wc, bar_ds_ready + (it & 1), (it >> 1) & 1, bSiteDSReady)) break;
         if (next) {
           const int s2 = (it + 1) % NS;
           if (!wait1(wc, bar_do_full + s2, ((it + 1) / NS) & 1, bSiteDOFull)) break;
           tc_fence_after();
           chain_kk(C::C_DP, dV_k, dDO_k(s2), idSS);
-          umma_commit(bar_sdp);  // covers S^T(i+1) issued above
+          umma_commit(bar_dp);
           if (!C::ALIAS) umma_commit(bar_do_empty + s2);
         }
         // dK = dS^T Q^  (A: dS^T codes [key][query], K-major; B: Q^ [query][d], MN-major);
@@ -455,7 +473,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
     for (int it = 0; it < T; ++it) {
       const int ib = tile_ib(it);
-      // the vectors of the previous tile were last read before its c2
+      // the vectors of the previous tile were last read before its c2 (d = 64) or c3 (d = 128)
       if (ws < 2) (ws == 0 ? L2v : Dv)[r] = pf_vec;
       const float sQt = pf_sq, sdOt = pf_sdo, bk = pf_bias;
       if (it + 1 < T) {
@@ -470,157 +488,297 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const float2 qks2 = make_float2(qks, qks);
       const bool diag = CAUSAL && ib == j;
       const bool masked = diag || (k0 + kBlk > p.N);
-      if (!waitw(wc, bar_sdp, it & 1, bSiteSDP)) break;
-      tc_fence_after();
-      // pass 1: P = 2^(S sQ sK scale log2e - LSE log2e), dS = P (dP - D), written back in
-      // place; the next chunk's TMEM loads are in flight while a chunk is computed
-      // amax: |dS| maximum of this thread's first 32 queries, amax_hi: of its last 32 (the
-      // two sub-scale groups; without sub-scales one maximum covers all 64)
-      float pmax = 0.f, amax = 0.f, amax_hi = 0.f;
-      {
-        uint32_t sv[2][8], dpv[2][8];
-        tmem_ld8(s_addr, sv[0]);
-        tmem_ld8(dp_addr, dpv[0]);
+      float invA = 0.f, magic_lo = 12582912.0f, magic_hi = 12582912.0f;  // the dS code parameters
+      if constexpr (C::SPLIT) {
+        // d = 128: P first (S^T only), dP^T waited for only then
+        if (!waitw(wc, bar_s, it & 1, bSiteS)) break;
+        tc_fence_after();
+        // pass 1: P = 2^(S sQ sK scale log2e - LSE log2e), written over S^T in place, and this
+        // thread's share of its row maximum; the next chunk's TMEM load is in flight while a chunk
+        // is computed.  dP^T is not read yet: its MMA runs behind this pass.
+        float pmax = 0.f;
+        {
+          uint32_t sv[2][8];
+          tmem_ld8(s_addr, sv[0]);
 #pragma unroll
-        for (int c = 0; c < QPT / 8; ++c) {
-          const int cur = c & 1;
-          tmem_ld_wait_regs(sv[cur]);
-          tmem_ld_wait_regs(dpv[cur]);
-          if (c + 1 < QPT / 8) {
-            tmem_ld8(s_addr + (c + 1) * 8, sv[cur ^ 1]);
-            tmem_ld8(dp_addr + (c + 1) * 8, dpv[cur ^ 1]);
-          }
+          for (int c = 0; c < QPT / 8; ++c) {
+            const int cur = c & 1;
+            tmem_ld_wait_regs(sv[cur]);
+            if (c + 1 < QPT / 8) tmem_ld8(s_addr + (c + 1) * 8, sv[cur ^ 1]);
 #pragma unroll
-          for (int e4 = 0; e4 < 8; e4 += 4) {
-            const int q = qc0 + c * 8 + e4;  // query column within the tile
-            const float4 l4 = ld_shared_v4_f32(l2v_s + q * 4);
-            const float4 d4 = ld_shared_v4_f32(dv_s + q * 4);
+            for (int e4 = 0; e4 < 8; e4 += 4) {
+              const int q = qc0 + c * 8 + e4;  // query column within the tile
+              const float4 l4 = ld_shared_v4_f32(l2v_s + q * 4);
 #pragma unroll
-            for (int e2 = 0; e2 < 4; e2 += 2) {
-              const int e = e4 + e2;
-              float2 nl = e2 == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
-              if (QSM) nl = fadd2(nl, make_float2(bk, bk));
-              const float2 nd = e2 == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
-              const float2 x =
-                  ffma2(make_float2(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])), qks2, nl);
-              float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              if (masked) {
-                if (!key_ok || (diag && q + e2 < r)) pr.x = 0.f;
-                if (!key_ok || (diag && q + e2 + 1 < r)) pr.y = 0.f;
+              for (int e2 = 0; e2 < 4; e2 += 2) {
+                const int e = e4 + e2;
+                float2 nl = e2 == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+                if (QSM) nl = fadd2(nl, make_float2(bk, bk));
+                const float2 x =
+                    ffma2(make_float2(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])), qks2, nl);
+                float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                if (masked) {
+                  if (!key_ok || (diag && q + e2 < r)) pr.x = 0.f;
+                  if (!key_ok || (diag && q + e2 + 1 < r)) pr.y = 0.f;
+                }
+                pmax = fmax3(pmax, pr.x, pr.y);
+                sv[cur][e] = __float_as_uint(pr.x);
+                sv[cur][e + 1] = __float_as_uint(pr.y);
               }
-              const float2 ds = fmul2(
-                  pr, fadd2(make_float2(__uint_as_float(dpv[cur][e]), __uint_as_float(dpv[cur][e + 1])), nd));
-              pmax = fmax3(pmax, pr.x, pr.y);
-              if (DSX && c >= 4)
-                amax_hi = fmax3(amax_hi, fabsf(ds.x), fabsf(ds.y));
-              else
-                amax = fmax3(amax, fabsf(ds.x), fabsf(ds.y));
-              sv[cur][e] = __float_as_uint(pr.x);
-              sv[cur][e + 1] = __float_as_uint(pr.y);
-              dpv[cur][e] = __float_as_uint(ds.x);
-              dpv[cur][e + 1] = __float_as_uint(ds.y);
             }
+            tmem_st8(s_addr + c * 8, sv[cur]);
           }
-          tmem_st8(s_addr + c * 8, sv[cur]);
-          tmem_st8(dp_addr + c * 8, dpv[cur]);
         }
-      }
-      tmem_st_wait();
-      // tile maximum of |dS| over the 8 softmax warps; row maximum of P over the two halves:
-      // half 0 publishes its maximum, half 1 combines and publishes the row's
-      const float amax_lo = amax;
-      if (DSX) amax = fmaxf(amax, amax_hi);
+        // row maximum of P over the slices: the maximum of the bit patterns (P >= 0 orders like
+        // its unsigned bits) in a slot that was cleared after every slice had read the previous
+        // tile's value (and before this tile's c1)
+        atomicMax(pm + r, __float_as_uint(pmax));
+        tmem_st_wait();
+        mbar_arrive(bar_c2);
+        if (!waitw(wc, bar_c2, it & 1, bSiteC2)) break;
+        pmax = __uint_as_float(pm[r]);
+        constexpr float kMinMax = VAR == kValFp8 ? kMinGroupMaxFp8 : kMinGroupMax;
+        constexpr float kQMax = VAR == kValFp8 ? kFp8Max : 127.f;
+        // hardware reciprocal (<= 2 ulp) rather than IEEE division: these scales only
+        // decide codes of this tile and dequantize it; a code at a rounding tie may differ
+        const bool p_live = pmax >= kMinMax;
+        const float invP = p_live ? __fdividef(kQMax, pmax) : 0.f;
+        const float sPc = p_live ? pmax * (1.f / kQMax) : 0.f;
+        if (ws == 0) fv_ring[(it & 1) * 128 + r] = __fmul_rn(sPc, sdOt);
+        // pass 2: dS = P (dP - D), written over dP^T in place, with this thread's maxima of |dS|,
+        // and the codes of P^T (row scale; 8 queries -> 4 packed columns) over the previous tile's
+        // codes: dV(i-1) must have read them (d = 64), and on d = 128, where they share the dK
+        // columns, dK(i-1) must have been read too (which implies the former)
+        if (it >= 1 && !(C::ALIAS ? waitw(wc, bar_tmem_free_k, (it - 1) & 1, bSiteTmemFreeK)
+                                  : waitw(wc, bar_acc_v, (it - 1) & 1, bSiteAccV)))
+          break;
+        if (!waitw(wc, bar_dp, it & 1, bSiteDP)) break;
+        tc_fence_after();
+        // amax: |dS| maximum of this thread's first 32 queries, amax_hi: of its last 32 (the
+        // two sub-scale groups; without sub-scales one maximum covers all 64)
+        float amax = 0.f, amax_hi = 0.f;
+        {
+          const float2 invP2 = make_float2(invP, invP);
+          const bool pt_bf16 = VAR == kValBf16 && (p.flags & SAGEBWD_FLAG_BF16_PB);
+          uint32_t pv[2][8], dpv[2][8];
+          tmem_ld8(s_addr, pv[0]);
+          tmem_ld8(dp_addr, dpv[0]);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      if (lane == 0) am[warp] = amax;
-      if (C::SWG == 2) {
-        if (ws == 0) pm[r] = pmax;
-      } else {
-        pm[ws * 128 + r] = pmax;
-      }
-      mbar_arrive(bar_c2);
-      if (!waitw(wc, bar_c2, it & 1, bSiteC2)) break;
-      if (C::SWG == 2) {
-        if (ws == 1) {
-          pmax = fmaxf(pmax, pm[r]);
-          pm[r] = pmax;
-          mbar_arrive(bar_c3);
-        } else {
-          if (!waitw(wc, bar_c3, it & 1, bSiteC3)) break;
-          pmax = pm[r];
+          for (int c = 0; c < QPT / 8; ++c) {
+            const int cur = c & 1;
+            tmem_ld_wait_regs(pv[cur]);
+            tmem_ld_wait_regs(dpv[cur]);
+            if (c + 1 < QPT / 8) {
+              tmem_ld8(s_addr + (c + 1) * 8, pv[cur ^ 1]);
+              tmem_ld8(dp_addr + (c + 1) * 8, dpv[cur ^ 1]);
+            }
+            uint32_t pk[4];
+#pragma unroll
+            for (int e4 = 0; e4 < 8; e4 += 4) {
+              const float4 d4 = ld_shared_v4_f32(dv_s + (qc0 + c * 8 + e4) * 4);
+#pragma unroll
+              for (int e2 = 0; e2 < 4; e2 += 2) {
+                const int e = e4 + e2;
+                const float2 nd = e2 == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+                const float2 pr = make_float2(__uint_as_float(pv[cur][e]), __uint_as_float(pv[cur][e + 1]));
+                const float2 ds = fmul2(
+                    pr, fadd2(make_float2(__uint_as_float(dpv[cur][e]), __uint_as_float(dpv[cur][e + 1])), nd));
+                if (DSX && c >= 4)
+                  amax_hi = fmax3(amax_hi, fabsf(ds.x), fabsf(ds.y));
+                else
+                  amax = fmax3(amax, fabsf(ds.x), fabsf(ds.y));
+                dpv[cur][e] = __float_as_uint(ds.x);
+                dpv[cur][e + 1] = __float_as_uint(ds.y);
+                const float2 sc2 = fmul2(pr, invP2);
+                if (VAR == kValFp8) {
+                  pk[e >> 1] = e4m3x2_bf16x2(sc2.x, sc2.y);
+                } else if (pt_bf16) {
+                  pk[e >> 1] = pack_bf16x2(sc2.x, sc2.y);
+                } else {
+                  const float2 cd = fadd2(fadd2(sc2, kMagic2), kNegMagic2);
+                  pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+                }
+              }
+            }
+            tmem_st8(dp_addr + c * 8, dpv[cur]);
+            tmem_st4(pc_addr + c * 4, pk);
+            if constexpr (DBG) dump4(dump_rec(it) + BwdDump<D>::PT + ((size_t)r * 128 + qc0 + c * 8) * 2, pk);
+          }
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_pt_ready);
+        // tile maximum of |dS| over the softmax warps
+        const float amax_lo = amax;
+        if (DSX) amax = fmaxf(amax, amax_hi);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) am[warp] = amax;
+        mbar_arrive(bar_c3);
+        if (!waitw(wc, bar_c3, it & 1, bSiteC3)) break;
+        // every slice has read the row maximum of P: clear it for the next tile
+        if (ws == 0) pm[r] = 0u;
+        float a = am[0];
+#pragma unroll
+        for (int q = 1; q < C::S_WARPS; ++q) a = fmaxf(a, am[q]);
+        const bool d_live = a >= kMinMax;
+        invA = d_live ? __fdividef(kQMax, a) : 0.f;
+        const float sDS = d_live ? a * (1.f / kQMax) : 0.f;
+        // dS sub-scales: group g of this thread's key gets k = floor(log2(a / max_g)) in
+        // [0, 8] (0 below 2^-100), from the binary exponents and fractions; its operand values
+        // are rint(dS * invA * 2^k) * 2^-k (a code times 2^-k, exact in BF16).  Adding and
+        // subtracting 1.5 * 2^(23-k), whose unit in the last place is 2^-k, rounds to that
+        // grid directly (ties to even), so the sub-scale costs no instruction per element.
+        if (DSX) {
+          auto subexp = [&](float g) -> int {
+            if (!(g >= 0x1p-100f)) return 0;
+            const uint32_t ua = __float_as_uint(a), ug = __float_as_uint(g);
+            const int k = (int)(ua >> 23) - (int)(ug >> 23) - ((ua & 0x7FFFFFu) < (ug & 0x7FFFFFu) ? 1 : 0);
+            return min(k, kDSubMax);
+          };
+          magic_lo = __int_as_float(((127 + 23 - subexp(amax_lo)) << 23) | 0x400000);
+          magic_hi = __int_as_float(((127 + 23 - subexp(amax_hi)) << 23) | 0x400000);
+        }
+        if (tid == 0) sds_ring[it & 1] = sDS;
       } else {
+        // d = 64: S^T and dP^T together (its dP^T product is short and done by the time S^T is)
+        float* pmf = reinterpret_cast<float*>(pm);  // [SWG][128] row maxima of P per slice
+        if (!waitw(wc, bar_dp, it & 1, bSiteDP)) break;  // (its commit follows S^T's MMAs too)
+        tc_fence_after();
+        // pass 1: P = 2^(S sQ sK scale log2e - LSE log2e), dS = P (dP - D), written back in
+        // place; the next chunk's TMEM loads are in flight while a chunk is computed
+        // amax: |dS| maximum of this thread's first 32 queries, amax_hi: of its last 32 (the
+        // two sub-scale groups; without sub-scales one maximum covers all 64)
+        float pmax = 0.f, amax = 0.f, amax_hi = 0.f;
+        {
+          uint32_t sv[2][8], dpv[2][8];
+          tmem_ld8(s_addr, sv[0]);
+          tmem_ld8(dp_addr, dpv[0]);
+#pragma unroll
+          for (int c = 0; c < QPT / 8; ++c) {
+            const int cur = c & 1;
+            tmem_ld_wait_regs(sv[cur]);
+            tmem_ld_wait_regs(dpv[cur]);
+            if (c + 1 < QPT / 8) {
+              tmem_ld8(s_addr + (c + 1) * 8, sv[cur ^ 1]);
+              tmem_ld8(dp_addr + (c + 1) * 8, dpv[cur ^ 1]);
+            }
+#pragma unroll
+            for (int e4 = 0; e4 < 8; e4 += 4) {
+              const int q = qc0 + c * 8 + e4;  // query column within the tile
+              const float4 l4 = ld_shared_v4_f32(l2v_s + q * 4);
+              const float4 d4 = ld_shared_v4_f32(dv_s + q * 4);
+#pragma unroll
+              for (int e2 = 0; e2 < 4; e2 += 2) {
+                const int e = e4 + e2;
+                float2 nl = e2 == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+                if (QSM) nl = fadd2(nl, make_float2(bk, bk));
+                const float2 nd = e2 == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+                const float2 x =
+                    ffma2(make_float2(__uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1])), qks2, nl);
+                float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                if (masked) {
+                  if (!key_ok || (diag && q + e2 < r)) pr.x = 0.f;
+                  if (!key_ok || (diag && q + e2 + 1 < r)) pr.y = 0.f;
+                }
+                const float2 ds = fmul2(
+                    pr, fadd2(make_float2(__uint_as_float(dpv[cur][e]), __uint_as_float(dpv[cur][e + 1])), nd));
+                pmax = fmax3(pmax, pr.x, pr.y);
+                if (DSX && c >= 4)
+                  amax_hi = fmax3(amax_hi, fabsf(ds.x), fabsf(ds.y));
+                else
+                  amax = fmax3(amax, fabsf(ds.x), fabsf(ds.y));
+                sv[cur][e] = __float_as_uint(pr.x);
+                sv[cur][e + 1] = __float_as_uint(pr.y);
+                dpv[cur][e] = __float_as_uint(ds.x);
+                dpv[cur][e + 1] = __float_as_uint(ds.y);
+              }
+            }
+            tmem_st8(s_addr + c * 8, sv[cur]);
+            tmem_st8(dp_addr + c * 8, dpv[cur]);
+          }
+        }
+        tmem_st_wait();
+        // tile maximum of |dS| over the 8 softmax warps; row maximum of P over the two halves:
+        // half 0 publishes its maximum, half 1 combines and publishes the row's
+        const float amax_lo = amax;
+        if (DSX) amax = fmaxf(amax, amax_hi);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) am[warp] = amax;
+        pmf[ws * 128 + r] = pmax;
+        mbar_arrive(bar_c2);
+        if (!waitw(wc, bar_c2, it & 1, bSiteC2)) break;
         // every slice reads all partial maxima (the next tile writes them only after its c1)
-        pmax = pm[r];
+        pmax = pmf[r];
 #pragma unroll
-        for (int q = 1; q < C::SWG; ++q) pmax = fmaxf(pmax, pm[q * 128 + r]);
-      }
-      float a = am[0];
+        for (int q = 1; q < C::SWG; ++q) pmax = fmaxf(pmax, pmf[q * 128 + r]);
+        float a = am[0];
 #pragma unroll
-      for (int q = 1; q < C::S_WARPS; ++q) a = fmaxf(a, am[q]);
-      constexpr float kMinMax = VAR == kValFp8 ? kMinGroupMaxFp8 : kMinGroupMax;
-      const bool p_live = pmax >= kMinMax, d_live = a >= kMinMax;
-      // hardware reciprocal (<= 2 ulp) rather than IEEE division: these scales only
-      // decide codes of this tile and dequantize it; a code at a rounding tie may differ
-      constexpr float kQMax = VAR == kValFp8 ? kFp8Max : 127.f;
-      const float invP = p_live ? __fdividef(kQMax, pmax) : 0.f;
-      const float sPc = p_live ? pmax * (1.f / kQMax) : 0.f;
-      const float invA = d_live ? __fdividef(kQMax, a) : 0.f;
-      const float sDS = d_live ? a * (1.f / kQMax) : 0.f;
-      // dS sub-scales: group g of this thread's key gets k = floor(log2(a / max_g)) in
-      // [0, 8] (0 below 2^-100), from the binary exponents and fractions; its operand values
-      // are rint(dS * invA * 2^k) * 2^-k (a code times 2^-k, exact in BF16).  Adding and
-      // subtracting 1.5 * 2^(23-k), whose unit in the last place is 2^-k, rounds to that
-      // grid directly (ties to even), so the sub-scale costs no instruction per element.
-      float magic_lo = 12582912.0f, magic_hi = 12582912.0f;
-      if (DSX) {
-        auto subexp = [&](float g) -> int {
-          if (!(g >= 0x1p-100f)) return 0;
-          const uint32_t ua = __float_as_uint(a), ug = __float_as_uint(g);
-          const int k = (int)(ua >> 23) - (int)(ug >> 23) - ((ua & 0x7FFFFFu) < (ug & 0x7FFFFFu) ? 1 : 0);
-          return min(k, kDSubMax);
-        };
-        magic_lo = __int_as_float(((127 + 23 - subexp(amax_lo)) << 23) | 0x400000);
-        magic_hi = __int_as_float(((127 + 23 - subexp(amax_hi)) << 23) | 0x400000);
-      }
-      if (ws == 0) fv_ring[(it & 1) * 128 + r] = __fmul_rn(sPc, sdOt);
-      if (tid == 0) sds_ring[it & 1] = sDS;
-      // pass 2a: codes of P^T (row scale), 32 queries -> 16 packed columns, over the previous
-      // tile's codes: dV(i-1) must have read them (d = 64), and on d = 128, where they share
-      // the dK columns, dK(i-1) must have been read too (which implies the former)
-      if (it >= 1 && !(C::ALIAS ? waitw(wc, bar_tmem_free_k, (it - 1) & 1, bSiteTmemFreeK)
-                                : waitw(wc, bar_acc_v, (it - 1) & 1, bSiteAccV)))
-        break;
-      tc_fence_after();
-      {
-        const float2 invP2 = make_float2(invP, invP);
-        const bool pt_bf16 = VAR == kValBf16 && (p.flags & SAGEBWD_FLAG_BF16_PB);
-#pragma unroll
-        for (int c0 = 0; c0 < QPT; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(s_addr + c0, v);
-          tmem_ld_wait();
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 sc2 = fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invP2);
-            if (VAR == kValFp8) {
-              pk[e >> 1] = e4m3x2_bf16x2(sc2.x, sc2.y);
-            } else if (pt_bf16) {
-              pk[e >> 1] = pack_bf16x2(sc2.x, sc2.y);
-            } else {
-              const float2 cd = fadd2(fadd2(sc2, kMagic2), kNegMagic2);
-              pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
-            }
-          }
-          if constexpr (DBG) dump16(dump_rec(it) + BwdDump<D>::PT + ((size_t)r * 128 + qc0 + c0) * 2, pk);
-          tmem_st16(pc_addr + (c0 >> 1), pk);
+        for (int q = 1; q < C::S_WARPS; ++q) a = fmaxf(a, am[q]);
+        constexpr float kMinMax = VAR == kValFp8 ? kMinGroupMaxFp8 : kMinGroupMax;
+        const bool p_live = pmax >= kMinMax, d_live = a >= kMinMax;
+        // hardware reciprocal (<= 2 ulp) rather than IEEE division: these scales only
+        // decide codes of this tile and dequantize it; a code at a rounding tie may differ
+        constexpr float kQMax = VAR == kValFp8 ? kFp8Max : 127.f;
+        const float invP = p_live ? __fdividef(kQMax, pmax) : 0.f;
+        const float sPc = p_live ? pmax * (1.f / kQMax) : 0.f;
+        invA = d_live ? __fdividef(kQMax, a) : 0.f;
+        const float sDS = d_live ? a * (1.f / kQMax) : 0.f;
+        // dS sub-scales: group g of this thread's key gets k = floor(log2(a / max_g)) in
+        // [0, 8] (0 below 2^-100), from the binary exponents and fractions; its operand values
+        // are rint(dS * invA * 2^k) * 2^-k (a code times 2^-k, exact in BF16).  Adding and
+        // subtracting 1.5 * 2^(23-k), whose unit in the last place is 2^-k, rounds to that
+        // grid directly (ties to even), so the sub-scale costs no instruction per element.
+        if (DSX) {
+          auto subexp = [&](float g) -> int {
+            if (!(g >= 0x1p-100f)) return 0;
+            const uint32_t ua = __float_as_uint(a), ug = __float_as_uint(g);
+            const int k = (int)(ua >> 23) - (int)(ug >> 23) - ((ua & 0x7FFFFFu) < (ug & 0x7FFFFFu) ? 1 : 0);
+            return min(k, kDSubMax);
+          };
+          magic_lo = __int_as_float(((127 + 23 - subexp(amax_lo)) << 23) | 0x400000);
+          magic_hi = __int_as_float(((127 + 23 - subexp(amax_hi)) << 23) | 0x400000);
         }
+        if (ws == 0) fv_ring[(it & 1) * 128 + r] = __fmul_rn(sPc, sdOt);
+        if (tid == 0) sds_ring[it & 1] = sDS;
+        // pass 2a: codes of P^T (row scale), 32 queries -> 16 packed columns, over the previous
+        // tile's codes: dV(i-1) must have read them (d = 64), and on d = 128, where they share
+        // the dK columns, dK(i-1) must have been read too (which implies the former)
+        if (it >= 1 && !(C::ALIAS ? waitw(wc, bar_tmem_free_k, (it - 1) & 1, bSiteTmemFreeK)
+                                  : waitw(wc, bar_acc_v, (it - 1) & 1, bSiteAccV)))
+          break;
+        tc_fence_after();
+        {
+          const float2 invP2 = make_float2(invP, invP);
+          const bool pt_bf16 = VAR == kValBf16 && (p.flags & SAGEBWD_FLAG_BF16_PB);
+#pragma unroll
+          for (int c0 = 0; c0 < QPT; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(s_addr + c0, v);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 sc2 = fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), invP2);
+              if (VAR == kValFp8) {
+                pk[e >> 1] = e4m3x2_bf16x2(sc2.x, sc2.y);
+              } else if (pt_bf16) {
+                pk[e >> 1] = pack_bf16x2(sc2.x, sc2.y);
+              } else {
+                const float2 cd = fadd2(fadd2(sc2, kMagic2), kNegMagic2);
+                pk[e >> 1] = pack_int_bf16x2(cd.x, cd.y);
+              }
+            }
+            if constexpr (DBG) dump16(dump_rec(it) + BwdDump<D>::PT + ((size_t)r * 128 + qc0 + c0) * 2, pk);
+            tmem_st16(pc_addr + (c0 >> 1), pk);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_pt_ready);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar_pt_ready);
-      // pass 2b: codes of dS (tile scale) into the shared A tile [key r][query], 16-byte
+      // pass 3: codes of dS (tile scale) into the shared A tile [key r][query], 16-byte
       // chunk = 8 queries, 128-byte swizzle, over the previous tile's codes: dK(i-1) and
       // dQ(i-1) must have read them (d = 64), and on d = 128 the tile is then the previous
       // tile's dQ staging half 1 until the reducer has read it (which implies the former)
@@ -667,7 +825,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if constexpr (QSM) p.cs_part[(((size_t)blockIdx.x * 2 + (it & 1)) * C::SWG + ws) * 128 + r] = csum.x + csum.y;
       tc_fence_before();
       fence_proxy_async_smem();
-      mbar_arrive(bar_ds_ready);
+      mbar_arrive(bar_ds_ready + (it & 1));
     }
   } else {
     setmaxnreg_to<C::REG_A, C::REGS_LAUNCH>();
@@ -693,13 +851,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           prefetch_l1(p.qmean + ((size_t)tile_bhq(it) * p.nb + tile_ib(it)) * D + wa * DH + lane * 32);
       }
       if (!waitw(wc, bar_acc_v, it & 1, bSiteAccV)) break;
-      // the tile's scales were stored before the P^T codes were released
+      // the row scales of P were stored before the P^T codes were released
       if (!waitw(wc, bar_pt_ready, it & 1, bSitePTReady)) break;
       tc_fence_after();
       const float fv = fv_ring[(it & 1) * 128 + r];
-      const float sDS = sds_ring[it & 1];
-      const float fk = __fmul_rn(__fmul_rn(p.sc, sDS), sQt);
-      const float fq = __fmul_rn(__fmul_rn(p.sc, sDS), sKv);
+      // the dS scale and the factors of the dK and dQ tiles: on d = 64 stored with the row scales
+      // of P, on d = 128 only before the dS codes are released (read after dK(i) below)
+      float sDS = 0.f, fk = 0.f, fq = 0.f;
+      if constexpr (!C::SPLIT) {
+        sDS = sds_ring[it & 1];
+        fk = __fmul_rn(__fmul_rn(p.sc, sDS), sQt);
+        fq = __fmul_rn(__fmul_rn(p.sc, sDS), sKv);
+      }
       {
         const uint64_t fv2 = pack_f32x2(fv, fv);
 #pragma unroll
@@ -717,6 +880,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         mbar_arrive(bar_tmem_free_v);
       }
       if (!waitw(wc, bar_acc_k, it & 1, bSiteAccK)) break;
+      if constexpr (C::SPLIT) {
+        if (!waitw(wc, bar_ds_ready + (it & 1), (it >> 1) & 1, bSiteDSReady)) break;
+        sDS = sds_ring[it & 1];
+        fk = __fmul_rn(__fmul_rn(p.sc, sDS), sQt);
+        fq = __fmul_rn(__fmul_rn(p.sc, sDS), sKv);
+      }
       tc_fence_after();
       {
         const uint64_t fk2 = pack_f32x2(fk, fk);
@@ -735,8 +904,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if constexpr (QSM) {
         // Q-smoothing, while dQ(i) runs: dK_r += scale s_dS (sum over the tile's queries of the dS
         // operand values) mean_Q(block i); the slices' column sums were stored before dS was
-        // released
-        if (!waitw(wc, bar_ds_ready, it & 1, bSiteDSReady)) break;
+        // released (on d = 128 waited for above)
+        if (!C::SPLIT && !waitw(wc, bar_ds_ready + (it & 1), (it >> 1) & 1, bSiteDSReady)) break;
         const float* cs = p.cs_part + ((size_t)blockIdx.x * 2 + (it & 1)) * C::SWG * 128 + r;
         float colsum = cs[0];
 #pragma unroll

@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, BM ? 2 : 3) quantize_kernel(const Qu
   __shared__ float fac[D];
   __shared__ float gred[kThreads / 32 * (D / 8)];
   if (p.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = 0;
+  pdl_trigger();
   int j = 0;
   while (j + 1 < p.njobs && (int)blockIdx.x >= p.block_start[j + 1]) ++j;
   const int local = blockIdx.x - p.block_start[j];
@@ -356,6 +357,9 @@ __global__ void __launch_bounds__(kThreads, BM ? 2 : 3) quantize_kernel(const Qu
     return;
   }
   const float* mean = job.mean != nullptr ? job.mean + (size_t)bh * D : nullptr;  // this head's channel means
+  // launched as a dependent of the kernel that computes the means: only the blocks that subtract
+  // them wait for it
+  if (mean != nullptr) pdl_wait();
   if (job.bexp != nullptr) {
     if (threadIdx.x < D) fac[threadIdx.x] = exp2_int(job.bexp_sign * job.bexp[(bh / job.bexp_group) * D + threadIdx.x]);
     __syncthreads();  // quantize_block reads fac only after this
@@ -576,6 +580,8 @@ __global__ void __launch_bounds__(kFinalSlices * 32) kmean_final_kernel(const do
                                                                         float* __restrict__ mean, int N, int nb,
                                                                         int d) {
   __shared__ double ssum[kFinalSlices][32];
+  pdl_trigger();
+  pdl_wait();  // the block sums, when launched as a dependent of their kernel
   const int bh = blockIdx.x, lane = threadIdx.x & 31, sl = threadIdx.x >> 5;
   const int c = blockIdx.y * 32 + lane;
   double s = 0;
@@ -746,22 +752,36 @@ __global__ void grad_convert_kernel(const ConvertJobs J) {
 
 }  // namespace
 
-cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s) {
+// Launch with the programmatic-serialization attribute when pdl is set (the kernel may start
+// while the previous grid in the stream runs; it waits for it where it reads its results).
+template <typename... Args>
+cudaError_t launch_ex(void (*kernel)(Args...), dim3 grid, dim3 block, bool pdl, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s, bool pdl) {
   const int blocks = p.block_start[p.njobs];
   if (blocks == 0) return cudaSuccess;
   bool bm = false;  // Q-smoothing's block means: a separate instantiation
   for (int j = 0; j < p.njobs; ++j) bm = bm || p.job[j].bmean != nullptr;
-  if (p.d == 64)
-    bm ? quantize_kernel<64, true><<<blocks, kThreads, 0, s>>>(p) : quantize_kernel<64, false><<<blocks, kThreads, 0, s>>>(p);
-  else
-    bm ? quantize_kernel<128, true><<<blocks, kThreads, 0, s>>>(p)
-       : quantize_kernel<128, false><<<blocks, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  auto kernel = p.d == 64 ? (bm ? quantize_kernel<64, true> : quantize_kernel<64, false>)
+                          : (bm ? quantize_kernel<128, true> : quantize_kernel<128, false>);
+  return launch_ex(kernel, dim3(blocks), dim3(kThreads), pdl, s, p);
 }
 
-cudaError_t launch_kmean_final(const double* part, float* mean, int BH, int N, int d, cudaStream_t s) {
-  kmean_final_kernel<<<dim3(BH, d / 32), kFinalSlices * 32, 0, s>>>(part, mean, N, nblocks(N), d);
-  return cudaGetLastError();
+cudaError_t launch_kmean_final(const double* part, float* mean, int BH, int N, int d, cudaStream_t s, bool pdl) {
+  return launch_ex(kmean_final_kernel, dim3(BH, d / 32), dim3(kFinalSlices * 32), pdl, s, part, mean, N, nblocks(N),
+                   d);
 }
 
 cudaError_t launch_kmean(const __nv_bfloat16* k, double* part, float* mean, int BH, int N, int d, int* status,

@@ -61,11 +61,14 @@ struct QuantParams {
   int* status;         // cleared by block 0 when clear_status
   int clear_status;
 };
-cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s);
+// pdl: launched as a programmatic dependent of the previous grid in the stream (the blocks of a
+// job with a mean wait for that grid; the others may run beside it).
+cudaError_t launch_quantize(const QuantParams& p, cudaStream_t s, bool pdl = false);
 cudaError_t launch_kmean(const __nv_bfloat16* k, double* part, float* mean, int BH, int N, int d, int* status,
                          int clear_status, cudaStream_t s);
 // The second half of the K-mean pass alone: mean[bh][c] = (sum of the block sums) / N.
-cudaError_t launch_kmean_final(const double* part, float* mean, int BH, int N, int d, cudaStream_t s);
+cudaError_t launch_kmean_final(const double* part, float* mean, int BH, int N, int d, cudaStream_t s,
+                               bool pdl = false);
 // Channel statistics of Q and K for the channel balancing: per (b, kv head,
 // channel) the K mean (smooth) and the balancing exponent.
 struct StatsParams {
