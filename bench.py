@@ -581,7 +581,9 @@ def describe(w: W.Workload) -> str:
 # ---------------------------------------------------------------------------- quantize stage bandwidth
 def quantize_bandwidth(step: "Step", flush: torch.Tensor, hbm_gbs: float, reps: int = 10):
     """HBM GB/s of the quantize stage and of its kernels, each timed with CUDA events on the launching
-    stream (L2 flushed before every call, outside the events): algorithmic bytes per call / time.
+    stream: algorithmic bytes per call / time.  Before every call, outside the events, L2 is flushed
+    (a buffer larger than L2 written) and then a second buffer larger than L2 is read, so that the
+    flush's dirty lines are written back before the call starts and the call's own traffic is timed.
     Algorithmic bytes: every input element read once per pass that must read it (K twice with
     K-smoothing: its channel sums, then its codes), every output written once; the quantized values
     are 2-byte integer-valued BF16 (the tensor cores' operand form).
@@ -610,12 +612,15 @@ def quantize_bandwidth(step: "Step", flush: torch.Tensor, hbm_gbs: float, reps: 
                    (6 if p.smooth_k else 4) * ke + 4 * nb * w.B * w.Hkv),
     }
     out = {}
+    evict = torch.empty(flush.numel() // 4, dtype=torch.float32, device=dev)
+    evict.zero_()
     for name, (fn, nbytes) in calls.items():
         if p.smooth_q and name in ("stage", "quantize_q"):
             continue  # Q-smoothing's stage adds the logit terms; its Q path is the fused one only
         ts = []
         for r in range(reps + 2):
             flush.zero_()
+            evict.sum()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(s)
             fn()

@@ -387,29 +387,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         umma_commit(bar_acc_v);
         umma_commit(bar_doq_empty + s);
         if (C::SPLIT && next) umma_commit(bar_s);  // S^T(i+1), issued before dV(i)
-        // dP^T of the next tile once dS is coded (its columns are free)
+        // Once dS is coded: dP^T of the next tile (its columns are free), dK(i) and dQ(i).  On d = 128
+        // dK(i) goes first: the next tile's second pass needs both dP^T(i+1) and dK(i) read (the
+        // P^T codes share the dK columns), and dK(i) waits behind nothing; on d = 64 the next tile
+        // starts with dP^T(i+1).
         if (!wait1(wc, bar_ds_ready + (it & 1), (it >> 1) & 1, bSiteDSReady)) break;
-        if (next) {
+        auto issue_dp = [&]() -> bool {
+          if (!next) return true;
           const int s2 = (it + 1) % NS;
-          if (!wait1(wc, bar_do_full + s2, ((it + 1) / NS) & 1, bSiteDOFull)) break;
+          if (!wait1(wc, bar_do_full + s2, ((it + 1) / NS) & 1, bSiteDOFull)) return false;
           tc_fence_after();
           chain_kk(C::C_DP, dV_k, dDO_k(s2), idSS);
           umma_commit(bar_dp);
           if (!C::ALIAS) umma_commit(bar_do_empty + s2);
-        }
+          return true;
+        };
         // dK = dS^T Q^  (A: dS^T codes [key][query], K-major; B: Q^ [query][d], MN-major);
         // on d = 128 it overwrites the P^T codes, so dV must have read them
-        if (C::ALIAS && !wait1(wc, bar_acc_v, it & 1, bSiteAccV)) break;
-        if (it >= 1 && !wait1(wc, bar_tmem_free_k, (it - 1) & 1, bSiteTmemFreeK)) break;
-        tc_fence_after();
-        umma_chain8_km(tmem + C::C_DK, sdesc_from_lo(dDS_k), sdesc_from_lo(dQ_mn(it & 1)), idKM);
-        umma_commit(bar_acc_k);
-        umma_commit(bar_q_empty + (it & 1));
+        auto issue_dk = [&]() -> bool {
+          if (C::ALIAS && !wait1(wc, bar_acc_v, it & 1, bSiteAccV)) return false;
+          if (it >= 1 && !wait1(wc, bar_tmem_free_k, (it - 1) & 1, bSiteTmemFreeK)) return false;
+          tc_fence_after();
+          umma_chain8_km(tmem + C::C_DK, sdesc_from_lo(dDS_k), sdesc_from_lo(dQ_mn(it & 1)), idKM);
+          umma_commit(bar_acc_k);
+          umma_commit(bar_q_empty + (it & 1));
+          return true;
+        };
         // dQ = dS K^  (A: the dS^T code tile read MN-major as [query][key]; B: K^ [key][d], MN-major)
-        if (C::ALIAS && !wait1(wc, bar_tmem_free_v, it & 1, bSiteTmemFreeV)) break;
-        tc_fence_after();
-        umma_chain8_mm(tmem + C::C_DQ, sdesc_from_lo(dDS_mn), sdesc_from_lo(dK_mn), idQM);
-        umma_commit(bar_acc_q);
+        auto issue_dq = [&]() -> bool {
+          if (C::ALIAS && !wait1(wc, bar_tmem_free_v, it & 1, bSiteTmemFreeV)) return false;
+          tc_fence_after();
+          umma_chain8_mm(tmem + C::C_DQ, sdesc_from_lo(dDS_mn), sdesc_from_lo(dK_mn), idQM);
+          umma_commit(bar_acc_q);
+          return true;
+        };
+        if (!(C::SPLIT ? issue_dk() && issue_dp() && issue_dq() : issue_dp() && issue_dk() && issue_dq())) break;
       }
       // Every MMA issued above must complete before TMEM is released.
       umma_commit(bar_final);

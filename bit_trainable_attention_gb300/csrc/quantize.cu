@@ -340,7 +340,7 @@ __device__ void block_channel_sums(const __nv_bfloat16* __restrict__ k, double* 
 }
 
 template <int D, bool BM>
-__global__ void __launch_bounds__(kThreads, BM ? 2 : 3) quantize_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kThreads, BM ? 2 : 4) quantize_kernel(const QuantParams p) {
   __shared__ float red[kThreads / 32];
   __shared__ float fac[D];
   __shared__ float gred[kThreads / 32 * (D / 8)];
