@@ -43,8 +43,8 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # one-pass ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of the timed step's
 # launch).  The figure belongs to the kernel sources it was taken from: once any of them
 # changes the line reports null until the capture is repeated.
-BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 775950592 + 284439296,
-               "sources_sha256": "bbf84d9322ff952799b90f3be3598559bbccd68c1244ea9adc0f4a15077472dc"}
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 767834368 + 278770176,
+               "sources_sha256": "99909819f68cbdd9f7533c50ce3a4c87c0eda6b530384a0c876fcd7b8e50097e"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
