@@ -391,7 +391,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
       return true;
     };
 
+    // the K and V block scales, loaded one key tile ahead (their latency hides behind a tile)
+    float pf_sk = nk > 0 ? p.sk[(size_t)bhk * p.nb] : 0.f, pf_sv = nk > 0 ? p.sv[(size_t)bhk * p.nb] : 0.f;
     for (int j = 0; j < nk; ++j) {
+      const float sKv = pf_sk, sVv = pf_sv;
+      if (j + 1 < nk) {
+        pf_sk = p.sk[(size_t)bhk * p.nb + j + 1];
+        pf_sv = p.sv[(size_t)bhk * p.nb + j + 1];
+      }
       // the previous tile's product lands while S_t(j) is computed (with separate code columns it
       // is folded after pass 1, since S_t(j) was issued before P^_t V^_(j-1))
       if (!C::SEPC && j >= 1 && !fold(j - 1, pend_a, pend_w)) {
@@ -403,8 +410,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
         break;
       }
       tc_fence_after();
-      const float sKv = p.sk[(size_t)bhk * p.nb + j];
-      const float sVv = p.sv[(size_t)bhk * p.nb + j];
       const float qks = __fmul_rn(__fmul_rn(sQv, sKv), p.c0);
       const int k0 = j * kBlk;
       const bool need_mask = (CAUSAL && j == qb) || (k0 + kBlk > p.N);
