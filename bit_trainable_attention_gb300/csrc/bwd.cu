@@ -502,7 +502,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const bool masked = diag || (k0 + kBlk > p.N);
       float invA = 0.f, magic_lo = 12582912.0f, magic_hi = 12582912.0f;  // the dS code parameters
       if constexpr (C::SPLIT) {
-        // d = 128: P first (S^T only), dP^T waited for only then
+        // d = 128: P first from S^T alone (its barrier is committed with dV(i-1)'s), dP^T waited
+        // for only then
         if (!waitw(wc, bar_s, it & 1, bSiteS)) break;
         tc_fence_after();
         // pass 1: P = 2^(S sQ sK scale log2e - LSE log2e), written over S^T in place, and this
