@@ -20,7 +20,9 @@
 //               128 / SWG: P, dS, the codes of P^T (row scale: the slices of a row
 //               exchange their maxima through shared memory) written to TMEM as the
 //               A operand of dV, and the codes of dS (tile scale) written to shared
-//               memory
+//               memory.  d = 128 in three passes: P from S^T (before dP^T is waited
+//               for); dS with the P^T codes; the dS codes.  d = 64 in the order P and
+//               dS; the P^T codes; the dS codes.
 //   next 8 warps  accumulator warpgroups A (two): thread (a, r) owns output
 //               columns [a d/2, (a+1) d/2) of row r of dV and dK (FP32 sums in
 //               registers) and of the dQ tile it scales into the staging tile
@@ -39,7 +41,9 @@
 //   dV(i) = P^T codes (TMEM) x dO^_i         while the dS of tile i is coded
 //   dP^T(i+1) = V_j dO_i+1^T (BF16)          once the dS of tile i has been coded
 //   dK(i) = dS^T Q^_i, dQ(i) = dS K^_j       from the shared dS code tile
-// so the softmax warpgroups wait for the next tile only while dP^T(i+1) runs.
+// (d = 128 issues dK(i) before dP^T(i+1): the next tile's second pass needs both), so
+// the softmax warpgroups of d = 128 start the next tile as soon as S^T(i+1) (committed
+// with dV(i)) is there, and those of d = 64 once dP^T(i+1) is.
 // With Q-smoothing (QSM) the recomputed logits gain the precomputed term mean_Q(block i) . K'_r
 // of the thread's key (one scalar per thread and tile, folded into -LSE), each softmax thread
 // sums its dS operand values over its queries, and the accumulator warpgroups add the block
