@@ -44,7 +44,7 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # launch).  The figure belongs to the kernel sources it was taken from: once any of them
 # changes the line reports null until the capture is repeated.
 BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 767834368 + 278770176,
-               "sources_sha256": "f61dc3e0cde0997d4b6726cbdcc21c3291c0e19f46ea7b17fa7a8c3a047ae507"}
+               "sources_sha256": "c6bc2050e8bd6bc55c34399462eee835f0c153fdc9cd9f161fae9c8b6ba79a67"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]

@@ -215,7 +215,13 @@ sagebwd_status sagebwd_bwd(const sagebwd_problem* prob, const void* q, const voi
  * that schedule or time them separately.  Calling the stages in this order,
  * on one stream, is exactly sagebwd_fwd / sagebwd_bwd.
  *   sagebwd_fwd_quantize  : K mean (and the balancing exponents) and the
- *                           Q, K, V quantization into `saved`.
+ *                           Q, K, V quantization into `saved`.  With
+ *                           K-smoothing (and no balancing) its later launches
+ *                           are programmatic dependents of the earlier ones
+ *                           (CUDA's programmatic stream serialization): Q and V
+ *                           are quantized while K's mean is computed.  The
+ *                           stage's first launch, and every launch after the
+ *                           stage, are ordinary stream-ordered launches.
  *   sagebwd_fwd_attention : the fused forward kernel on `saved` -> o, lse.
  *   sagebwd_bwd_prepare   : D = rowsum(dO * O), quantized dO, zeroed dQ
  *                           accumulator and, when they are used, dK and dV
