@@ -413,8 +413,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           if (it >= 1 && !wait1(wc, bar_tmem_free_k, (it - 1) & 1, bSiteTmemFreeK)) return false;
           tc_fence_after();
           umma_chain8_km(tmem + C::C_DK, sdesc_from_lo(dDS_k), sdesc_from_lo(dQ_mn(it & 1)), idKM);
-          umma_commit(bar_acc_k);
-          umma_commit(bar_q_empty + (it & 1));
+          if (C::SPLIT) {
+            umma_commit(bar_acc_k);
+            umma_commit(bar_q_empty + (it & 1));
+          }
           return true;
         };
         // dQ = dS K^  (A: the dS^T code tile read MN-major as [query][key]; B: K^ [key][d], MN-major)
@@ -422,6 +424,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           if (C::ALIAS && !wait1(wc, bar_tmem_free_v, it & 1, bSiteTmemFreeV)) return false;
           tc_fence_after();
           umma_chain8_mm(tmem + C::C_DQ, sdesc_from_lo(dDS_mn), sdesc_from_lo(dK_mn), idQM);
+          if (!C::SPLIT) {  // d = 64: dK(i)'s barriers too (one commit point fewer per tile)
+            umma_commit(bar_acc_k);
+            umma_commit(bar_q_empty + (it & 1));
+          }
           umma_commit(bar_acc_q);
           return true;
         };
