@@ -43,8 +43,8 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # one-pass ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of the timed step's
 # launch).  The figure belongs to the kernel sources it was taken from: once any of them
 # changes the line reports null until the capture is repeated.
-BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 767834368 + 278770176,
-               "sources_sha256": "c6bc2050e8bd6bc55c34399462eee835f0c153fdc9cd9f161fae9c8b6ba79a67"}
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 769017600 + 279151616,
+               "sources_sha256": "10078f7bc9b922a37dd540dd35c300c7217b3774bfdb83a5b0c0ce8f64c8da56"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
