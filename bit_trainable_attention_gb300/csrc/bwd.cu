@@ -323,10 +323,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tma_load_3d(smem + C::OFF_Q + sq * C::TILE + c * 16384, &tmQ, bar_q_full + sq, c * 64, i0, bhq);
         q_iss[sq] = nq2 + 1;
         if (it >= NS && !wait1(wc, bar_doq_empty + s, (n - 1) & 1, bSiteDOQEmpty)) break;
-        mbar_arrive_expect_tx(bar_doq_full + s, C::TILE);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::OFF_DOQ + s * C::TILE + c * 16384, &tmDOQ, bar_doq_full + s, c * 64, i0, bhq);
-        doq_iss[s] = n + 1;
+        if (!((p.flags & SAGEBWD_FLAG_DROP_ONE_LOAD) && it == 1)) {  // fault injection skips one load
+          mbar_arrive_expect_tx(bar_doq_full + s, C::TILE);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::OFF_DOQ + s * C::TILE + c * 16384, &tmDOQ, bar_doq_full + s, c * 64, i0, bhq);
+          doq_iss[s] = n + 1;
+        }
       }
       for (int s = 0; s < 2; ++s)
         if (q_iss[s]) drain(bar_q_full + s, (q_iss[s] - 1) & 1, p.timeout_ns);

@@ -112,8 +112,10 @@ typedef enum {
 enum { SAGEBWD_Q = 0, SAGEBWD_K = 1, SAGEBWD_V = 2, SAGEBWD_DO = 3 };
 
 /* sagebwd_problem.flags */
-#define SAGEBWD_FLAG_DROP_ONE_LOAD 0x1u /* fault injection: the forward kernel skips one K-tile load, so its
-                                           bounded wait runs out and the call reports SAGEBWD_ERR_TIMEOUT */
+#define SAGEBWD_FLAG_DROP_ONE_LOAD 0x1u /* fault injection: the forward kernel skips one K-tile load and the
+                                           backward kernel the dO^ load of each CTA's second tile, so
+                                           their bounded waits run out and the call reports
+                                           SAGEBWD_ERR_TIMEOUT */
 #define SAGEBWD_FLAG_DEBUG_DUMP 0x2u    /* parity checking: the attention kernels also write every tile's
                                            INT8-semantics operands and raw tensor-core products into the
                                            workspace (layout at sagebwd_debug_dump_offset; small problems

@@ -1,7 +1,7 @@
 """Failure detection on the GPU without a GPU fault.
 
 The problem flag SAGEBWD_FLAG_DROP_ONE_LOAD makes the forward kernel's producer
-skip the TMA load of one K tile.  Nothing then completes that tile's mbarrier:
+skip the TMA load of one K tile (and the backward kernel's that of one dO^ tile).  Nothing then completes that tile's mbarrier:
 the waits behind it run out after the problem's short wait_timeout_ms, record
 SAGEBWD_ERR_TIMEOUT with the site of the first wait that gave up, raise the
 CTA's abort flag so every other role leaves its loop, drain the copies and MMAs
@@ -49,6 +49,41 @@ def test_dropped_load_times_out_and_the_context_survives(oracle_mod, causal):
     np.testing.assert_allclose(to_np(good["lse"]), lse_ref, rtol=0, atol=LSE_TOL)
     bwd = gpu_backward(w, xd, good)
     assert bwd["status"] == 0
+
+
+BWD_SITES = range(16, 39)  # the backward kernel's wait sites (K/V .. dP^T)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_dropped_load_times_out_and_the_context_survives(oracle_mod, d):
+    """The same flag makes the backward kernel skip the dO^ load of each CTA's second tile: the MMA
+    issuer's wait for it runs out, every other role leaves on the abort flag, the copies and MMAs in
+    flight are drained and TMEM is freed.  The call reports a backward wait site, and an ordinary
+    backward afterwards is correct."""
+    # 384 tokens, two query heads per kv head: every CTA has at least two tiles
+    w = W.small(f"fault_bwd_{d}", 1, 4, 2, 384, d, False, 303)
+    x, xd = device_inputs(w)
+    fwd = gpu_forward(w, xd)
+    assert fwd["status"] == 0
+    prob = fwd["prob"]
+    prob.flags = SAGEBWD_FLAG_DROP_ONE_LOAD
+    prob.wait_timeout_ms = 100
+    t0 = time.time()
+    bad = gpu_backward(w, xd, fwd)
+    elapsed = time.time() - t0
+    assert bad["status"] == SAGEBWD_ERR_TIMEOUT, sb.sagebwd_status_string(bad["status"])
+    assert (bad["word"] >> 8) in BWD_SITES, hex(bad["word"])
+    assert elapsed < 30.0
+    # the context is still usable: the ordinary backward of the same forward matches the oracle
+    torch.cuda.synchronize()
+    prob.flags = 0
+    prob.wait_timeout_ms = 0
+    good = gpu_backward(w, xd, fwd)
+    assert good["status"] == 0
+    op = oracle_problem(oracle_mod, w)
+    ref = oracle_mod.pipeline(op, x["q"], x["k"], x["v"], x["do"])
+    for key in ("dq", "dk", "dv"):
+        assert_parity(to_np(good[key]), ref[key], key)
 
 
 def test_autograd_path_reports_a_device_timeout():
