@@ -43,12 +43,13 @@ namespace {
 constexpr int kFThreads = 384;
 constexpr uint32_t kFRegsLaunch = 168;
 // registers per thread after setmaxnreg: control warps (producer, MMA) and softmax
-// warpgroups.  Measured: 40 / 232 made the control warps spill (forward 0.846 ms on the
-// long-context workload), 56 / 224 does not (0.825 ms); on d = 64, 88 / 208 (0.478 ms
-// against 0.496 ms at 40 / 232 on the 8K-token GQA workload).
+// warpgroups.  Measured on d = 128 (long-context workload): 40 / 232 0.846 ms, 56 / 224
+// 0.825 ms (before the scale prefetch; 0.820 ms after it), 64 / 216 0.815 ms (ptxas: 128 B of
+// spill stores per thread against 240 B at 56 / 224), 96 / 200 0.820 ms; on d = 64, 88 / 208
+// (0.478 ms against 0.496 ms at 40 / 232 on the 8K-token GQA workload).
 template <int D>
 struct FwdRegs {
-  static constexpr uint32_t LOW = D == 128 ? 56 : 88, HIGH = D == 128 ? 224 : 208;
+  static constexpr uint32_t LOW = D == 128 ? 64 : 88, HIGH = D == 128 ? 216 : 208;
   static_assert(128 * LOW + 256 * HIGH <= kFThreads * kFRegsLaunch, "register split exceeds the launch");
 };
 
