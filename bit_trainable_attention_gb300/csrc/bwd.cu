@@ -227,6 +227,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const int T = p.HS * nq;
   auto tile_bhq = [&](int t) { return b * p.Hq + hq0 + t / nq; };
   auto tile_ib = [&](int t) { return ib0 + t % nq; };
+  // The same walk without a division per tile: (query head within the CTA's heads, query block)
+  // of tile t + 1 from that of tile t, for the roles that need them every tile.
+  struct TilePos {
+    int h, ib;
+  };
+  auto next_pos = [&](TilePos t) {
+    if (++t.ib == ib0 + nq) {
+      t.ib = ib0;
+      ++t.h;
+    }
+    return t;
+  };
+  auto pos_bhq = [&](TilePos t) { return b * p.Hq + hq0 + t.h; };
   // debug dump record of tile t (DBG instantiation only)
   auto dump_rec = [&](int t) -> uint8_t* {
     if constexpr (DBG)
@@ -292,7 +305,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tma_load_3d(smem + C::OFF_K + c * 16384, &tmK, bar_kv, c * 64, k0, bhk);
         tma_load_3d(smem + C::OFF_V + c * 16384, &tmV, bar_kv, c * 64, k0, bhk);
       }
-      for (int it = 0; it < T; ++it) {
+      TilePos pos{0, ib0};
+      for (int it = 0; it < T; ++it, pos = next_pos(pos)) {
         const int s = it % NS, n = it / NS;
         if (C::ALIAS) {
           if (it == 1 && !wait1(wc, bar_do_empty, 0, bSiteDOEmpty)) break;
@@ -303,7 +317,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(bar_do_full + s, C::TILE);
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + C::OFF_DO + s * C::TILE + c * 16384, &tmDO, bar_do_full + s, c * 64,
-                      tile_ib(it) * kBlk, tile_bhq(it));
+                      pos.ib * kBlk, pos_bhq(pos));
         do_iss[s] = n + 1;
       }
       // Copies still in flight must land before the CTA's shared memory is released.
@@ -314,9 +328,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // ---------------------------------------------------------- TMA producer: Q^, dO^
       int q_iss[2] = {0, 0}, doq_iss[NS];
       for (int s = 0; s < NS; ++s) doq_iss[s] = 0;
-      for (int it = 0; it < T; ++it) {
+      TilePos pos{0, ib0};
+      for (int it = 0; it < T; ++it, pos = next_pos(pos)) {
         const int s = it % NS, n = it / NS, sq = it & 1, nq2 = it >> 1;
-        const int bhq = tile_bhq(it), i0 = tile_ib(it) * kBlk;
+        const int bhq = pos_bhq(pos), i0 = pos.ib * kBlk;
         if (it >= 2 && !wait1(wc, bar_q_empty + sq, (nq2 - 1) & 1, bSiteQEmpty)) break;
         mbar_arrive_expect_tx(bar_q_full + sq, C::TILE);
         for (int c = 0; c < D / 64; ++c)
@@ -444,8 +459,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // warpgroup h.  Half 1 goes first: on d = 128 it occupies the dS code tile that the
       // softmax warpgroups need next; both reduces run at once and each half is released
       // as soon as its own read has finished.
-      for (int it = 0; it < T; ++it) {
-        const int bhq = tile_bhq(it), i0 = tile_ib(it) * kBlk;
+      TilePos pos{0, ib0};
+      for (int it = 0; it < T; ++it, pos = next_pos(pos)) {
+        const int bhq = pos_bhq(pos), i0 = pos.ib * kBlk;
         if (!wait1(wc, bar_staged + 1, it & 1, bSiteStaged)) break;
 #pragma unroll
         for (int bx = D / 64; bx < D / 32; ++bx) tma_reduce_add_3d(&tmDQ, smem + C::stg_box(bx), bx * 32, i0, bhq);
@@ -477,34 +493,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t l2v_s = smem_u32(L2v), dv_s = smem_u32(Dv);
     // Per tile: half 0 stores -LSE (base 2) of query r, half 1 stores -D (-inf / 0
     // past N); loaded one tile ahead so that their latency hides behind the current tile.
-    auto tile_vec = [&](int t) -> float {
-      const int row = tile_ib(t) * kBlk + r;
+    auto tile_vec = [&](TilePos t) -> float {
+      const int row = t.ib * kBlk + r;
       if (row >= p.N) return ws == 0 ? -INFINITY : 0.f;
-      const size_t idx = (size_t)tile_bhq(t) * p.N + row;
+      const size_t idx = (size_t)pos_bhq(t) * p.N + row;
       return ws == 0 ? -__fmul_rn(p.lse[idx], kLog2e) : -p.D[idx];
     };
-    auto tile_sq = [&](int t) { return p.sq[(size_t)tile_bhq(t) * p.nb + tile_ib(t)]; };
-    auto tile_sdo = [&](int t) { return p.sdo[(size_t)tile_bhq(t) * p.nb + tile_ib(t)]; };
+    auto tile_sq = [&](TilePos t) { return p.sq[(size_t)pos_bhq(t) * p.nb + t.ib]; };
+    auto tile_sdo = [&](TilePos t) { return p.sdo[(size_t)pos_bhq(t) * p.nb + t.ib]; };
     // Q-smoothing: the logit term mean_Q(tile's query block) . K'_r of this thread's key
-    auto tile_bias = [&](int t) -> float {
+    auto tile_bias = [&](TilePos t) -> float {
       if constexpr (QSM)
-        return p.qbias[((size_t)tile_bhq(t) * p.nb + tile_ib(t)) * ((size_t)p.nb * kBlk) + k0 + r];
+        return p.qbias[((size_t)pos_bhq(t) * p.nb + t.ib) * ((size_t)p.nb * kBlk) + k0 + r];
       else
         return 0.f;
     };
-    float pf_vec = tile_vec(0), pf_sq = tile_sq(0), pf_sdo = tile_sdo(0), pf_bias = tile_bias(0);
+    TilePos pos{0, ib0};  // tile it (tile it + 1 once the prefetch below has advanced it)
+    float pf_vec = tile_vec(pos), pf_sq = tile_sq(pos), pf_sdo = tile_sdo(pos), pf_bias = tile_bias(pos);
     const float2 kMagic2 = make_float2(12582912.0f, 12582912.0f), kNegMagic2 = make_float2(-12582912.0f, -12582912.0f);
 
     for (int it = 0; it < T; ++it) {
-      const int ib = tile_ib(it);
+      const int ib = pos.ib;
       // the vectors of the previous tile were last read before its c2 (d = 64) or c3 (d = 128)
       if (ws < 2) (ws == 0 ? L2v : Dv)[r] = pf_vec;
       const float sQt = pf_sq, sdOt = pf_sdo, bk = pf_bias;
+      pos = next_pos(pos);
       if (it + 1 < T) {
-        pf_vec = tile_vec(it + 1);
-        pf_sq = tile_sq(it + 1);
-        pf_sdo = tile_sdo(it + 1);
-        if (QSM) pf_bias = tile_bias(it + 1);
+        pf_vec = tile_vec(pos);
+        pf_sq = tile_sq(pos);
+        pf_sdo = tile_sdo(pos);
+        if (QSM) pf_bias = tile_bias(pos);
       }
       mbar_arrive(bar_c1);
       if (!waitw(wc, bar_c1, it & 1, bSiteC1)) break;
@@ -864,16 +882,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     uint64_t dv_run[DH / 2], dk_run[DH / 2];  // packed FP32 pairs (columns c, c + 1)
 #pragma unroll
     for (int c = 0; c < DH / 2; ++c) dv_run[c] = dk_run[c] = 0ull;
-    float sq_next = p.sq[(size_t)tile_bhq(0) * p.nb + tile_ib(0)];
+    TilePos apos{0, ib0};
+    float sq_next = p.sq[(size_t)pos_bhq(apos) * p.nb + apos.ib];
 
     for (int it = 0; it < T; ++it) {
       const float sQt = sq_next;
-      if (it + 1 < T) sq_next = p.sq[(size_t)tile_bhq(it + 1) * p.nb + tile_ib(it + 1)];
+      const TilePos cur = apos;  // this tile
+      apos = next_pos(apos);
+      if (it + 1 < T) sq_next = p.sq[(size_t)pos_bhq(apos) * p.nb + apos.ib];
       // Q-smoothing: this warpgroup's half of mean_Q(tile's query block) into L1 now, read at
       // the end of the tile (a quarter of a line per lane group: lanes 0..DH/32-1 of each warp)
       if constexpr (QSM && C::ALIAS) {  // (on d = 64 the prefetch measured slower)
         if (lane < DH / 32)
-          prefetch_l1(p.qmean + ((size_t)tile_bhq(it) * p.nb + tile_ib(it)) * D + wa * DH + lane * 32);
+          prefetch_l1(p.qmean + ((size_t)pos_bhq(cur) * p.nb + cur.ib) * D + wa * DH + lane * 32);
       }
       if (!waitw(wc, bar_acc_v, it & 1, bSiteAccV)) break;
       // the row scales of P were stored before the P^T codes were released
@@ -938,7 +959,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const float wcs = __fmul_rn(__fmul_rn(p.sc, sDS), colsum);
         const uint64_t w2 = pack_f32x2(wcs, wcs);
         const float4* mq =
-            reinterpret_cast<const float4*>(p.qmean + ((size_t)tile_bhq(it) * p.nb + tile_ib(it)) * D + wa * DH);
+            reinterpret_cast<const float4*>(p.qmean + ((size_t)pos_bhq(cur) * p.nb + cur.ib) * D + wa * DH);
 #pragma unroll
         for (int c = 0; c < DH; c += 4) {
           const float4 m = __ldg(mq + c / 4);
