@@ -509,7 +509,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         return 0.f;
     };
     TilePos pos{0, ib0};  // tile it (tile it + 1 once the prefetch below has advanced it)
-    float pf_vec = tile_vec(pos), pf_sq = tile_sq(pos), pf_sdo = tile_sdo(pos), pf_bias = tile_bias(pos);
+    // (only slices 0 and 1 store the vectors, only slice 0 the row factor that needs sdO)
+    float pf_vec = ws < 2 ? tile_vec(pos) : 0.f, pf_sq = tile_sq(pos), pf_sdo = ws == 0 ? tile_sdo(pos) : 0.f,
+          pf_bias = tile_bias(pos);
     const float2 kMagic2 = make_float2(12582912.0f, 12582912.0f), kNegMagic2 = make_float2(-12582912.0f, -12582912.0f);
 
     for (int it = 0; it < T; ++it) {
@@ -519,9 +521,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const float sQt = pf_sq, sdOt = pf_sdo, bk = pf_bias;
       pos = next_pos(pos);
       if (it + 1 < T) {
-        pf_vec = tile_vec(pos);
+        if (ws < 2) pf_vec = tile_vec(pos);
         pf_sq = tile_sq(pos);
-        pf_sdo = tile_sdo(pos);
+        if (ws == 0) pf_sdo = tile_sdo(pos);
         if (QSM) pf_bias = tile_bias(pos);
       }
       mbar_arrive(bar_c1);
