@@ -104,8 +104,8 @@ struct BwdCfg {
   static constexpr bool SPLIT = D == 128;
   static_assert(SPLIT || SWG > 2, "the fused pass exchanges the row maxima of P among more than two slices");
   static constexpr int PM_FLOATS = SPLIT ? 128 : 128 * SWG;
-  // -LSE log2 e [128], -D [128], P^T scale x sdO per row [2][128], dS scale [2], |dS| maxima
-  // [S_WARPS], row maxima of P [PM_FLOATS]
+  // -LSE log2 e [128], -D [128], P^T scale x sdO per row [2][128], |dS| maxima [S_WARPS] (read
+  // as 16-byte vectors), dS scale [2], row maxima of P [PM_FLOATS]
   static constexpr int VEC_FLOATS = 128 + 128 + 256 + 2 + S_WARPS + PM_FLOATS;
   static constexpr int OFF_BAR = OFF_VEC + ((VEC_FLOATS * 4 + 15) / 16) * 16;
   static constexpr int NBAR = 1 + 4 + 4 * NS + 19;
@@ -148,6 +148,18 @@ struct BwdDump {
   static constexpr size_t PT = 0, DS = 128 * 128 * 2, DV = 2 * 128 * 128 * 2, DK = DV + 128 * D * 4,
                           DQ = DK + 128 * D * 4, BYTES = DQ + 128 * D * 4;
 };
+// Maximum of the per-warp maxima am[0, NW) (16-byte aligned shared memory, NW a multiple of 4).
+template <int NW>
+__device__ __forceinline__ float max_of_warps(const float* am) {
+  static_assert(NW % 4 == 0, "whole vectors");
+  float a = 0.f;  // the maxima are of absolute values
+#pragma unroll
+  for (int q = 0; q < NW; q += 4) {
+    const float4 v = ld_shared_v4_f32(smem_u32(am + q));
+    a = fmax3(a, fmax3(v.x, v.y, v.z), v.w);
+  }
+  return a;
+}
 // Write 4 consecutive 32-bit words (16 bytes, 16-byte aligned) to global memory.
 __device__ __forceinline__ void dump4(uint8_t* dst, const uint32_t* w) {
   *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -180,9 +192,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   float* L2v = reinterpret_cast<float*>(smem + C::OFF_VEC);  // -LSE_q log2 e of the tile's queries
   float* Dv = L2v + 128;                                      // -D_q
   float* fv_ring = Dv + 128;                                  // [2][128] sP_row * sdO per tile parity
-  float* sds_ring = fv_ring + 256;                              // [2] dS scale per tile parity
-  float* am = sds_ring + 2;                                     // [S_WARPS] per-warp maxima of |dS|
-  uint32_t* pm = reinterpret_cast<uint32_t*>(am + C::S_WARPS);  // row maxima of P (bits; PM_FLOATS)
+  float* am = fv_ring + 256;                                    // [S_WARPS] per-warp maxima of |dS| (16-B aligned)
+  float* sds_ring = am + C::S_WARPS;                            // [2] dS scale per tile parity
+  uint32_t* pm = reinterpret_cast<uint32_t*>(sds_ring + 2);     // row maxima of P (bits; PM_FLOATS)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* bar_kv = bars;
   uint64_t* bar_q_full = bar_kv + 1;              // [2]
@@ -663,9 +675,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!waitw(wc, bar_c3, it & 1, bSiteC3)) break;
         // every slice has read the row maximum of P: clear it for the next tile
         if (ws == 0) pm[r] = 0u;
-        float a = am[0];
-#pragma unroll
-        for (int q = 1; q < C::S_WARPS; ++q) a = fmaxf(a, am[q]);
+        const float a = max_of_warps<C::S_WARPS>(am);
         const bool d_live = a >= kMinMax;
         invA = d_live ? __fdividef(kQMax, a) : 0.f;
         const float sDS = d_live ? a * (1.f / kQMax) : 0.f;
@@ -758,9 +768,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         pmax = pmf[r];
 #pragma unroll
         for (int q = 1; q < C::SWG; ++q) pmax = fmaxf(pmax, pmf[q * 128 + r]);
-        float a = am[0];
-#pragma unroll
-        for (int q = 1; q < C::S_WARPS; ++q) a = fmaxf(a, am[q]);
+        const float a = max_of_warps<C::S_WARPS>(am);
         constexpr float kMinMax = VAR == kValFp8 ? kMinGroupMaxFp8 : kMinGroupMax;
         const bool p_live = pmax >= kMinMax, d_live = a >= kMinMax;
         // hardware reciprocal (<= 2 ulp) rather than IEEE division: these scales only
