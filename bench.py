@@ -43,8 +43,8 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # one-pass ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of the timed step's
 # launch).  The figure belongs to the kernel sources it was taken from: once any of them
 # changes the line reports null until the capture is repeated.
-BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 772499456 + 281160704,
-               "sources_sha256": "ef23986f45d7df81920d4488c30e0bef7842c9f4e2c748148bfd41eb7733cf99"}
+BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 771040512 + 281135360,
+               "sources_sha256": "9d445b5c764bf050d15683f9ba59246d88612ceea6d18e3bea1e0b82fe5074e0"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]
