@@ -44,7 +44,7 @@ INT8_TORCH_INT_MM_TOPS = 78.3
 # launch).  The figure belongs to the kernel sources it was taken from: once any of them
 # changes the line reports null until the capture is repeated.
 BWD_TRAFFIC = {"workload": "qwen15b", "bytes": 771040512 + 281135360,
-               "sources_sha256": "9d445b5c764bf050d15683f9ba59246d88612ceea6d18e3bea1e0b82fe5074e0"}
+               "sources_sha256": "31e4ead463e229feda528d0fbcabbb57133c3fc75b1c80dcefae01fa31ccb2a8"}
 BWD_SOURCES = ["bit_trainable_attention_gb300/csrc/bwd.cu", "bit_trainable_attention_gb300/csrc/kernel_common.cuh",
                "bit_trainable_attention_gb300/csrc/ptx.cuh", "bit_trainable_attention_gb300/csrc/sagebwd_internal.h",
                "include/sagebwd.h"]

@@ -80,7 +80,10 @@
  *   - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned.
  *     The library allocates, frees and synchronizes nothing (except
  *     sagebwd_check_status, which synchronizes the given stream), keeps no
- *     global state, and launches only on the given stream.
+ *     state between calls beyond read-only caches (driver entry points, SM
+ *     counts, the query heads per backward CTA chosen for a shape) and the
+ *     static scratch array of sagebwd_quantize_k_noalloc, and launches only
+ *     on the given stream.
  *   - Supported: d in {64, 128}; Hq % Hkv == 0; N >= 1; B, Hq, Hkv >= 1.
  *   - Errors are returned before any launch for bad arguments; a launch
  *     failure returns SAGEBWD_ERR_CUDA.  Kernels bound every wait; a wait
