@@ -31,6 +31,21 @@ def test_header_declares_the_entry_points():
     assert set(names) == set(sb.EXPORTED_SYMBOLS)
 
 
+def test_binding_constants_match_the_header():
+    """The binding's copies of the header's flag and operand constants (the problem struct carries
+    them as plain integers, so a mismatch would silently select another option)."""
+    text = open(os.path.join(ROOT, "include", "sagebwd.h")).read()
+    flags = {m[0]: int(m[1], 16) for m in re.findall(r"#define (SAGEBWD_FLAG_[A-Z0-9_]+) (0x[0-9a-fA-F]+)u", text)}
+    assert flags["SAGEBWD_FLAG_DROP_ONE_LOAD"] == sb.FLAG_DROP_ONE_LOAD
+    assert flags["SAGEBWD_FLAG_DEBUG_DUMP"] == sb.FLAG_DEBUG_DUMP
+    for name, value in sb.FLAG_BF16.items():
+        assert flags["SAGEBWD_FLAG_BF16_" + name.upper().replace("P_FWD", "PF").replace("P_BWD", "PB")] == value, name
+    assert len({v for k, v in flags.items()}) == len(flags)  # no two flags share a bit pattern
+    ops = dict(re.findall(r"(SAGEBWD_(?:Q|K|V|DO)) = (\d+)", text))
+    assert {k: int(v) for k, v in ops.items()} == {"SAGEBWD_Q": sb.SAGEBWD_Q, "SAGEBWD_K": sb.SAGEBWD_K,
+                                                   "SAGEBWD_V": sb.SAGEBWD_V, "SAGEBWD_DO": sb.SAGEBWD_DO}
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
